@@ -1,0 +1,52 @@
+"""The pins must catch plausible slips: each test here compiles a copy of the
+oracle with one deliberate mistake (on the CPU, in a temporary directory) and
+checks that at least one pin in test_oracle_pins fails against it."""
+import os
+import subprocess
+
+import pytest
+
+import oracle
+from tests import test_oracle_pins as pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "gdn_oracle.cpp")
+
+FWD_PINS = [pins.test_hand_worked_cases, pins.test_gqa_head_map_contiguous_groups,
+            pins.test_beta_zero_is_pure_decay, pins.test_orthonormal_keys_store_values_exactly,
+            pins.test_reset_at_boundaries_equals_separate_runs, pins.test_empty_documents_pass_the_state_through,
+            lambda: pins.test_brute_force_quadratic_form(17, 8, 5)]
+BWD_PINS = [pins.test_backward_matches_finite_differences]
+
+# (name, original text, mutated text, which pins)
+MUTANTS = [
+    ("decay dropped", "for (int c = 0; c < w; ++c) S[r * w + c] *= a;", "for (int c = 0; c < w; ++c) S[r * w + c] *= 1.0;", FWD_PINS),
+    ("correction sign", "d[c] = b * (vt[c] - p[c]);", "d[c] = b * (vt[c] + p[c]);", FWD_PINS),
+    ("beta dropped", "d[c] = b * (vt[c] - p[c]);", "d[c] = (vt[c] - p[c]);", FWD_PINS),
+    ("output reads k", "double qr = qt[r];", "double qr = kt[r];", FWD_PINS),
+    ("interleaved head map", "const int hk = h / G;\n    std::vector<std::vector<double>> fin(N);",
+     "const int hk = h % Hk;\n    std::vector<std::vector<double>> fin(N);", FWD_PINS),
+    ("no reset", "std::fill(S, S + (size_t)s.Dk * w, 0.0);", "(void)S;", FWD_PINS),
+    ("dg sign", "dgt += dS[e] * Sp[e];", "dgt -= dS[e] * Sp[e];", BWD_PINS),
+    ("dk drops prediction term", "acc += Sp[(size_t)r * w + c] * dp[c];", "acc += 0.0;", BWD_PINS),
+    ("dbeta uses v", "dbt += ddel[c] * vp[c];", "dbt += ddel[c] * vt[c];", BWD_PINS),
+    ("decay not carried into dS", "for (size_t e = 0; e < SZ; ++e) dS[e] *= a;", "(void)a;", BWD_PINS),
+]
+
+
+@pytest.mark.parametrize("name,orig,mut,which", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_pins_catch_mutant(name, orig, mut, which, tmp_path, monkeypatch):
+    src = open(SRC).read()
+    assert src.count(orig) >= 1, f"mutation site for '{name}' not found"
+    bad = src.replace(orig, mut, 1)
+    cpp = tmp_path / "mut.cpp"
+    cpp.write_text(bad)
+    so = tmp_path / "libmut.so"
+    subprocess.check_call(["g++", "-O1", "-std=c++17", "-shared", "-fPIC", "-pthread", str(cpp), "-o", str(so)])
+    monkeypatch.setattr(oracle, "_lib", oracle.load_library(str(so)))
+    failed = []
+    for pin in which:
+        try:
+            pin()
+        except AssertionError:
+            failed.append(getattr(pin, "__name__", "pin"))
+    assert failed, f"no pin caught the '{name}' mutant"
