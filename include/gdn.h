@@ -1,0 +1,140 @@
+/*
+ * gdn.h — C ABI of the GB300 (sm_103a) chunked Gated DeltaNet library.
+ *
+ * The library computes the gated delta rule over a packed batch of documents,
+ * forward and backward. For document i = tokens [cu_seqlens[i], cu_seqlens[i+1])
+ * and value head h (key head hk = h / (H_v / H_k)), the per-head state
+ * S in R^{d_k x d_v} (d_k = d_v = 128) evolves as
+ *     S_t = exp(g_t) (I - beta_t k_t k_t^T) S_{t-1} + beta_t k_t v_t^T,   o_t = S_t^T q_t
+ * ("How to Speed Up GDN Kernels for Qwen Models", section "What GDN actually
+ * computes": S in R^{d_k x d_v}, alpha_t = e^{g_t}, the erase-then-write factor;
+ * "Musings on long-context fine-tuning", section "Isolating the recurrent
+ * layers": decay first, then correct the decayed memory's prediction; the query
+ * reads the updated matrix). The state restarts at every document boundary and
+ * may instead start from a pool entry or from another document's final state
+ * (same page: a continuation receives the shared prefix's final state through
+ * initial_state, with boundaries given by cu_seqlens). Work is done in chunks
+ * of 64 tokens (the chunked formulation of the first page, same section).
+ *
+ * Conventions for every entry point below:
+ *  - All tensor pointers are DEVICE pointers, token-major and contiguous:
+ *      q, k      : bf16 [T, H_k, 128]
+ *      v, out    : bf16 [T, H_v, 128]
+ *      g, beta   : fp32 [T, H_v]        (g = log-decay, expected <= 0; beta in [0, 1])
+ *      cu_seqlens: int32 [N + 1]        (0 = cu[0] <= cu[1] <= ... <= cu[N] = T)
+ *      init_idx  : int32 [N] or NULL    (NULL = every document starts from zero)
+ *                  -1           : zero state
+ *                  0..n_init-1  : initial_state[init_idx[i]]
+ *                  n_init + j   : the final state of document j < i of this same call
+ *      initial_state : fp32 [n_init, H_v, 128, 128] or NULL when n_init == 0
+ *      final_state   : fp32 [N, H_v, 128, 128]  (layout [d_k][d_v] per head)
+ *    q, k, v, out and every gradient of them must be 16-byte aligned.
+ *  - Ownership: the caller owns all memory, including the workspace. The library
+ *    never allocates, frees or synchronises; every kernel is enqueued on `stream`.
+ *    Inputs are read-only; outputs are overwritten in full.
+ *  - Errors: an int status is returned and nothing is thrown across the ABI.
+ *    Argument errors the host can see are reported before any launch. Errors that
+ *    need the device data (bad cu_seqlens / init_idx, an expired bounded wait) are
+ *    written to a status word in the workspace; read it with gdn_workspace_status().
+ *    After a device-side error the outputs are unspecified.
+ *  - GPUs: built for sm_103a (GB300) only; any other GPU returns
+ *    GDN_ERR_UNSUPPORTED ("Using it, and the fine print": the kernels refuse
+ *    hardware they were not built for). The device is the one that holds the
+ *    workspace.
+ */
+#ifndef GDN_H_
+#define GDN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* gdn_stream_t; /* a cudaStream_t; NULL = legacy default stream */
+
+enum gdn_status_code {
+  GDN_OK = 0,
+  GDN_ERR_INVALID_ARG = -1, /* bad shapes, pointers, alignment, cu_seqlens or init_idx */
+  GDN_ERR_UNSUPPORTED = -2, /* head_dim != 128, or the GPU is not sm_103 */
+  GDN_ERR_CUDA = -3,        /* a CUDA launch or runtime call failed */
+  GDN_ERR_TIMEOUT = -4,     /* a bounded device-side wait ran out */
+  GDN_ERR_WORKSPACE = -5    /* the workspace is smaller than the size query returned */
+};
+
+enum gdn_mode {
+  GDN_MODE_EXACT = 0,   /* default: long documents split into segments, exact cross-segment fix-up */
+  GDN_MODE_TRUNCATE = 1 /* opt-in: segment carries rebuilt from a warmup window ("Lever 1") */
+};
+
+typedef struct gdn_options {
+  int32_t mode;              /* gdn_mode */
+  float trunc_log_threshold; /* truncation mode: warmup window ends once the summed log-decay < this (-10) */
+  int32_t segment_chunks;    /* segment length in 64-token chunks; 0 = automatic, < 0 = never split */
+  float scale;               /* multiplies q (1.0: inputs already scaled) */
+  int32_t reserved;          /* must be 0 */
+} gdn_options;
+
+/* Fill `opt` with the defaults: exact mode, threshold -10, automatic segments, scale 1. */
+void gdn_default_options(gdn_options* opt);
+
+/* Workspace bytes gdn_chunk_fwd needs for these sizes (opt may be NULL for defaults).
+ * Returns 0 for invalid sizes. The value depends on the current device's SM count. */
+size_t gdn_fwd_workspace_size(int N, int T, int H_k, int H_v, const gdn_options* opt);
+
+/* Workspace bytes gdn_chunk_bwd needs. */
+size_t gdn_bwd_workspace_size(int N, int T, int H_k, int H_v, const gdn_options* opt);
+
+/*
+ * Forward: out[t, h, :] = o_t for every token and value head; final_state[i, h] = state
+ * after the last token of document i (its start state if the document is empty).
+ * n_init: number of pool entries in initial_state (0 allowed).
+ * head_dim must be 128. workspace: device memory of at least gdn_fwd_workspace_size() bytes,
+ * 256-byte aligned; its contents need no initialisation.
+ */
+int gdn_chunk_fwd(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                  const int32_t* cu_seqlens, int N, int T, int H_k, int H_v, int head_dim,
+                  const int32_t* init_idx, const float* initial_state, int n_init, void* out,
+                  float* final_state, void* workspace, size_t ws_bytes, const gdn_options* opt,
+                  gdn_stream_t stream);
+
+/*
+ * Backward of gdn_chunk_fwd for the loss sum(dout * out) + sum(dfinal_state * final_state).
+ * dout: bf16 [T, H_v, 128]; dfinal_state: fp32 [N, H_v, 128, 128] or NULL (zero).
+ * Outputs: dq, dk bf16 [T, H_k, 128] (summed over the value heads of each key head);
+ * dv bf16 [T, H_v, 128]; dg, dbeta fp32 [T, H_v]; dinitial_state fp32 [n_init, H_v, 128, 128]
+ * (summed over every document that starts from the same pool entry; NULL allowed when n_init == 0).
+ * A document forked from document j of the same call sends its gradient back into j
+ * ("Musings on long-context fine-tuning", section "Backward through P").
+ */
+int gdn_chunk_bwd(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                  const int32_t* cu_seqlens, int N, int T, int H_k, int H_v, int head_dim,
+                  const int32_t* init_idx, const float* initial_state, int n_init, const void* dout,
+                  const float* dfinal_state, void* dq, void* dk, void* dv, float* dg, float* dbeta,
+                  float* dinitial_state, void* workspace, size_t ws_bytes, const gdn_options* opt,
+                  gdn_stream_t stream);
+
+/* Copy the workspace's device status word to the host (synchronises `stream`) and return it:
+ * GDN_OK or the first device-side error of the last call that used this workspace. */
+int gdn_workspace_status(const void* workspace, gdn_stream_t stream);
+
+/* Human-readable name of a status code (static string). */
+const char* gdn_status_string(int status);
+
+/* Host-side planner, exported for inspection and tests: given HOST copies of cu_seqlens
+ * (int32[N+1]) and init_idx (int32[N] or NULL), fill the chunk and segment maps exactly as the
+ * device planner does. Arrays (host memory, caller-owned):
+ *   chunk_seq, chunk_tok0, chunk_len : int32[max_chunks]   (max_chunks >= T/64 + N)
+ *   seg_info : int32[max_segs * 4]  (per segment: sequence, first chunk, chunk count, dependency)
+ * num_sms: SM count to plan for. Returns the number of chunks in out_counts[0], segments in
+ * out_counts[1], chosen segment length (chunks) in out_counts[2]; status as the return value. */
+int gdn_plan_host(const int32_t* cu_seqlens, int N, int T, int H_v, const int32_t* init_idx, int n_init,
+                  const gdn_options* opt, int num_sms, int32_t* chunk_seq, int32_t* chunk_tok0,
+                  int32_t* chunk_len, int max_chunks, int32_t* seg_info, int max_segs, int32_t* out_counts);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H_ */

@@ -1,0 +1,244 @@
+"""Chunked Gated DeltaNet over packed varlen batches on GB300 (sm_103a).
+
+A thin binding over the C ABI declared in include/gdn.h: argument marshalling
+only. Every step of the computation runs in the CUDA library
+`_build/libgdn_gb300.so`; if that library is missing, every call raises.
+PyTorch is used for device memory and streams.
+
+    import linear_attention_varlen_gb300 as gdn
+    out, final_state = gdn.chunk_fwd(q, k, v, g, beta, cu_seqlens)
+    grads = gdn.chunk_bwd(q, k, v, g, beta, cu_seqlens, dout)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from dataclasses import dataclass
+from typing import Optional
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "_build", "libgdn_gb300.so")
+
+GDN_OK, GDN_ERR_INVALID_ARG, GDN_ERR_UNSUPPORTED, GDN_ERR_CUDA, GDN_ERR_TIMEOUT, GDN_ERR_WORKSPACE = 0, -1, -2, -3, -4, -5
+MODE_EXACT, MODE_TRUNCATE = 0, 1
+HEAD_DIM = 128
+CHUNK = 64
+
+# Every symbol include/gdn.h declares.
+EXPORTS = ("gdn_default_options", "gdn_fwd_workspace_size", "gdn_bwd_workspace_size", "gdn_chunk_fwd",
+           "gdn_chunk_bwd", "gdn_workspace_status", "gdn_status_string", "gdn_plan_host")
+
+
+class GdnError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} ({status})")
+
+
+class COptions(ctypes.Structure):
+    _fields_ = [("mode", ctypes.c_int32), ("trunc_log_threshold", ctypes.c_float),
+                ("segment_chunks", ctypes.c_int32), ("scale", ctypes.c_float), ("reserved", ctypes.c_int32)]
+
+
+@dataclass
+class Options:
+    """Mirror of gdn_options. mode: "exact" (default) or "truncate"."""
+    mode: str = "exact"
+    trunc_log_threshold: float = -10.0
+    segment_chunks: int = 0
+    scale: float = 1.0
+
+    def c(self) -> COptions:
+        m = {"exact": MODE_EXACT, "truncate": MODE_TRUNCATE}[self.mode]
+        return COptions(m, float(self.trunc_log_threshold), int(self.segment_chunks), float(self.scale), 0)
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    return LIB_PATH
+
+
+def load(path: Optional[str] = None):
+    """Open the compiled library (no fallback: raises if it is missing) and declare signatures."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise RuntimeError(f"GDN CUDA library not built: {p} is missing (run linear_attention_varlen_gb300.build)")
+        lib = ctypes.CDLL(p)
+        P, I, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+        OP = ctypes.POINTER(COptions)
+        lib.gdn_default_options.argtypes = [OP]
+        lib.gdn_default_options.restype = None
+        lib.gdn_fwd_workspace_size.argtypes = [I, I, I, I, OP]
+        lib.gdn_fwd_workspace_size.restype = Z
+        lib.gdn_bwd_workspace_size.argtypes = [I, I, I, I, OP]
+        lib.gdn_bwd_workspace_size.restype = Z
+        lib.gdn_chunk_fwd.argtypes = [P, P, P, P, P, P, I, I, I, I, I, P, P, I, P, P, P, Z, OP, P]
+        lib.gdn_chunk_fwd.restype = I
+        lib.gdn_chunk_bwd.argtypes = [P, P, P, P, P, P, I, I, I, I, I, P, P, I, P, P, P, P, P, P, P, P, P, Z, OP, P]
+        lib.gdn_chunk_bwd.restype = I
+        lib.gdn_workspace_status.argtypes = [P, P]
+        lib.gdn_workspace_status.restype = I
+        lib.gdn_status_string.argtypes = [I]
+        lib.gdn_status_string.restype = ctypes.c_char_p
+        lib.gdn_plan_host.argtypes = [P, I, I, I, P, I, OP, I, P, P, P, I, P, I, P]
+        lib.gdn_plan_host.restype = I
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def status_string(status: int) -> str:
+    try:
+        return load().gdn_status_string(int(status)).decode()
+    except RuntimeError:
+        return {0: "GDN_OK", -1: "GDN_ERR_INVALID_ARG", -2: "GDN_ERR_UNSUPPORTED", -3: "GDN_ERR_CUDA",
+                -4: "GDN_ERR_TIMEOUT", -5: "GDN_ERR_WORKSPACE"}.get(int(status), "GDN_ERR_UNKNOWN")
+
+
+def _opts(options: Optional[Options]) -> COptions:
+    return (options or Options()).c()
+
+
+def fwd_workspace_size(N: int, T: int, H_k: int, H_v: int, options: Optional[Options] = None) -> int:
+    o = _opts(options)
+    return int(load().gdn_fwd_workspace_size(N, T, H_k, H_v, ctypes.byref(o)))
+
+
+def bwd_workspace_size(N: int, T: int, H_k: int, H_v: int, options: Optional[Options] = None) -> int:
+    o = _opts(options)
+    return int(load().gdn_bwd_workspace_size(N, T, H_k, H_v, ctypes.byref(o)))
+
+
+def plan_host(cu_seqlens, H_v: int, init_idx=None, n_init: int = 0, options: Optional[Options] = None,
+              num_sms: int = 152):
+    """Run the exported host planner on host arrays; returns (chunks [n,3], segments [s,4], seg_len)."""
+    import numpy as np
+    cu = np.ascontiguousarray(cu_seqlens, dtype=np.int32)
+    N = cu.shape[0] - 1
+    T = int(cu[-1])
+    ii = None if init_idx is None else np.ascontiguousarray(init_idx, dtype=np.int32)
+    mc = T // CHUNK + N + 1
+    ms = mc + N + 1
+    cs, ct, cl = (np.zeros(mc, np.int32) for _ in range(3))
+    si = np.zeros(4 * ms, np.int32)
+    cnt = np.zeros(3, np.int32)
+    o = _opts(options)
+    ptr = lambda a: None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+    rc = load().gdn_plan_host(ptr(cu), N, T, H_v, ptr(ii), n_init, ctypes.byref(o), num_sms, ptr(cs), ptr(ct),
+                              ptr(cl), mc, ptr(si), ms, ptr(cnt))
+    if rc != GDN_OK:
+        raise GdnError(rc, "gdn_plan_host")
+    nc, ns, L = int(cnt[0]), int(cnt[1]), int(cnt[2])
+    chunks = np.stack([cs[:nc], ct[:nc], cl[:nc]], axis=1)
+    return chunks, si[:4 * ns].reshape(ns, 4), L
+
+
+# ----------------------------------------------------------------------------- torch-facing calls
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(stream):
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(t, name, dtype, shape=None):
+    torch = _torch()
+    if t is None:
+        raise ValueError(f"{name} is required")
+    if not t.is_cuda or t.dtype != dtype or not t.is_contiguous():
+        raise ValueError(f"{name}: expected a contiguous CUDA {dtype} tensor")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: expected shape {tuple(shape)}, got {tuple(t.shape)}")
+    return t
+
+
+def chunk_fwd(q, k, v, g, beta, cu_seqlens, init_idx=None, initial_state=None, options: Optional[Options] = None,
+              out=None, final_state=None, workspace=None, stream=None):
+    """Forward over a packed batch. Shapes: q, k [T, Hk, 128] bf16; v [T, Hv, 128] bf16;
+    g, beta [T, Hv] fp32; cu_seqlens [N+1] int32 (device); init_idx [N] int32 or None;
+    initial_state [n_init, Hv, 128, 128] fp32 or None. Returns (out, final_state)."""
+    torch = _torch()
+    T, Hk, D = q.shape
+    Hv = v.shape[1]
+    N = cu_seqlens.shape[0] - 1
+    _check(q, "q", torch.bfloat16, (T, Hk, D))
+    _check(k, "k", torch.bfloat16, (T, Hk, D))
+    _check(v, "v", torch.bfloat16, (T, Hv, D))
+    _check(g, "g", torch.float32, (T, Hv))
+    _check(beta, "beta", torch.float32, (T, Hv))
+    _check(cu_seqlens, "cu_seqlens", torch.int32, (N + 1,))
+    n_init = 0
+    if initial_state is not None:
+        _check(initial_state, "initial_state", torch.float32)
+        n_init = initial_state.shape[0]
+    if init_idx is not None:
+        _check(init_idx, "init_idx", torch.int32, (N,))
+    dev = q.device
+    if out is None:
+        out = torch.empty((T, Hv, D), dtype=torch.bfloat16, device=dev)
+    if final_state is None:
+        final_state = torch.empty((N, Hv, D, D), dtype=torch.float32, device=dev)
+    o = _opts(options)
+    need = int(load().gdn_fwd_workspace_size(N, T, Hk, Hv, ctypes.byref(o)))
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    rc = load().gdn_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(cu_seqlens), N, T, Hk, Hv, D,
+                              _ptr(init_idx), _ptr(initial_state), n_init, _ptr(out), _ptr(final_state),
+                              _ptr(workspace), workspace.numel(), ctypes.byref(o), _stream_handle(stream))
+    if rc != GDN_OK:
+        raise GdnError(rc, "gdn_chunk_fwd")
+    return out, final_state
+
+
+def chunk_bwd(q, k, v, g, beta, cu_seqlens, dout, dfinal_state=None, init_idx=None, initial_state=None,
+              options: Optional[Options] = None, workspace=None, stream=None):
+    """Backward. Returns dict dq, dk, dv (bf16), dg, dbeta (fp32), dinit (fp32 or None)."""
+    torch = _torch()
+    T, Hk, D = q.shape
+    Hv = v.shape[1]
+    N = cu_seqlens.shape[0] - 1
+    _check(dout, "dout", torch.bfloat16, (T, Hv, D))
+    if dfinal_state is not None:
+        _check(dfinal_state, "dfinal_state", torch.float32, (N, Hv, D, D))
+    n_init = 0 if initial_state is None else initial_state.shape[0]
+    dev = q.device
+    dq = torch.empty_like(q)
+    dk = torch.empty_like(k)
+    dv = torch.empty_like(v)
+    dg = torch.empty((T, Hv), dtype=torch.float32, device=dev)
+    db = torch.empty((T, Hv), dtype=torch.float32, device=dev)
+    dinit = torch.empty_like(initial_state) if n_init > 0 else None
+    o = _opts(options)
+    need = int(load().gdn_bwd_workspace_size(N, T, Hk, Hv, ctypes.byref(o)))
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    rc = load().gdn_chunk_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(cu_seqlens), N, T, Hk, Hv, D,
+                              _ptr(init_idx), _ptr(initial_state), n_init, _ptr(dout), _ptr(dfinal_state),
+                              _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dg), _ptr(db), _ptr(dinit), _ptr(workspace),
+                              workspace.numel(), ctypes.byref(o), _stream_handle(stream))
+    if rc != GDN_OK:
+        raise GdnError(rc, "gdn_chunk_bwd")
+    return dict(dq=dq, dk=dk, dv=dv, dg=dg, dbeta=db, dinit=dinit)
+
+
+def workspace_status(workspace, stream=None) -> int:
+    """Device status word of the last call that used `workspace` (synchronises the stream)."""
+    return int(load().gdn_workspace_status(_ptr(workspace), _stream_handle(stream)))

@@ -1,0 +1,261 @@
+// C ABI of the GDN library (declared in include/gdn.h): argument checks, workspace sizing,
+// tensor-map creation and kernel launches. No allocation, no synchronisation.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+#include <vector>
+
+#include "../../include/gdn.h"
+#include "gdn_bwd.h"
+#include "gdn_common.cuh"
+#include "gdn_fwd.h"
+#include "tmap.h"
+
+using namespace gdn;
+
+namespace {
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Make the device that owns `ptr` current (the caller's tensors decide the GPU).
+int select_device_of(const void* ptr) {
+  cudaPointerAttributes attr;
+  if (cudaPointerGetAttributes(&attr, ptr) != cudaSuccess) {
+    cudaGetLastError();
+    return kErrInvalid;
+  }
+  if (attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged) return kErrInvalid;
+  return cudaSetDevice(attr.device) == cudaSuccess ? kOk : kErrCuda;
+}
+
+int current_sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+// The kernels use tcgen05 and are compiled for sm_103a (GB300, compute capability 10.3) only.
+int check_arch() {
+  int dev = 0, major = 0, minor = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return kErrCuda;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess) return kErrCuda;
+  if (cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) return kErrCuda;
+  return (major == 10 && minor == 3) ? kOk : kErrUnsupported;
+}
+
+gdn_options resolve(const gdn_options* opt) {
+  gdn_options o;
+  gdn_default_options(&o);
+  if (opt) o = *opt;
+  return o;
+}
+
+bool valid_options(const gdn_options& o) {
+  return (o.mode == GDN_MODE_EXACT || o.mode == GDN_MODE_TRUNCATE) && o.reserved == 0 && o.scale == o.scale;
+}
+
+PlanDims make_dims(int N, int T, int H_k, int H_v, int n_init, const gdn_options& o, int sms) {
+  PlanDims d;
+  d.N = N;
+  d.T = T;
+  d.Hk = H_k;
+  d.Hv = H_v;
+  d.n_init = n_init;
+  d.num_sms = sms > 0 ? sms : 1;
+  d.seg_override = o.segment_chunks;
+  d.mode = o.mode;
+  return d;
+}
+
+bool sizes_ok(int N, int T, int H_k, int H_v) {
+  if (N < 1 || T < 0 || H_k < 1 || H_v < 1 || H_v % H_k != 0) return false;
+  if ((int64_t)T * H_v * kDim > ((int64_t)1 << 40)) return false;
+  return true;
+}
+
+}  // namespace
+
+extern "C" {
+
+void gdn_default_options(gdn_options* opt) {
+  if (!opt) return;
+  opt->mode = GDN_MODE_EXACT;
+  opt->trunc_log_threshold = -10.0f;
+  opt->segment_chunks = 0;
+  opt->scale = 1.0f;
+  opt->reserved = 0;
+}
+
+const char* gdn_status_string(int status) {
+  switch (status) {
+    case GDN_OK:
+      return "GDN_OK";
+    case GDN_ERR_INVALID_ARG:
+      return "GDN_ERR_INVALID_ARG";
+    case GDN_ERR_UNSUPPORTED:
+      return "GDN_ERR_UNSUPPORTED";
+    case GDN_ERR_CUDA:
+      return "GDN_ERR_CUDA";
+    case GDN_ERR_TIMEOUT:
+      return "GDN_ERR_TIMEOUT";
+    case GDN_ERR_WORKSPACE:
+      return "GDN_ERR_WORKSPACE";
+    default:
+      return "GDN_ERR_UNKNOWN";
+  }
+}
+
+size_t gdn_fwd_workspace_size(int N, int T, int H_k, int H_v, const gdn_options* opt) {
+  if (!sizes_ok(N, T, H_k, H_v)) return 0;
+  const gdn_options o = resolve(opt);
+  if (!valid_options(o)) return 0;
+  return fwd_layout(make_dims(N, T, H_k, H_v, 0, o, current_sm_count())).total;
+}
+
+size_t gdn_bwd_workspace_size(int N, int T, int H_k, int H_v, const gdn_options* opt) {
+  if (!sizes_ok(N, T, H_k, H_v)) return 0;
+  const gdn_options o = resolve(opt);
+  if (!valid_options(o)) return 0;
+  return bwd_layout(make_dims(N, T, H_k, H_v, 0, o, current_sm_count())).total;
+}
+
+int gdn_workspace_status(const void* workspace, gdn_stream_t stream) {
+  if (!workspace) return GDN_ERR_INVALID_ARG;
+  int32_t st = 0;
+  if (cudaMemcpyAsync(&st, workspace, sizeof(st), cudaMemcpyDeviceToHost, (cudaStream_t)stream) != cudaSuccess)
+    return GDN_ERR_CUDA;
+  if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return GDN_ERR_CUDA;
+  return st;
+}
+
+int gdn_chunk_fwd(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                  const int32_t* cu_seqlens, int N, int T, int H_k, int H_v, int head_dim,
+                  const int32_t* init_idx, const float* initial_state, int n_init, void* out, float* final_state,
+                  void* workspace, size_t ws_bytes, const gdn_options* opt, gdn_stream_t stream) {
+  if (head_dim != kDim) return GDN_ERR_UNSUPPORTED;
+  if (!sizes_ok(N, T, H_k, H_v) || n_init < 0) return GDN_ERR_INVALID_ARG;
+  const gdn_options o = resolve(opt);
+  if (!valid_options(o)) return GDN_ERR_INVALID_ARG;
+  if (!cu_seqlens || !final_state || !workspace) return GDN_ERR_INVALID_ARG;
+  if (T > 0 && (!q || !k || !v || !g || !beta || !out)) return GDN_ERR_INVALID_ARG;
+  if (n_init > 0 && !initial_state) return GDN_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) || !aligned(final_state, 16) ||
+      !aligned(initial_state, 16) || !aligned(workspace, 256))
+    return GDN_ERR_INVALID_ARG;
+  const int dev = select_device_of(workspace);
+  if (dev != kOk) return dev;
+  const int arch = check_arch();
+  if (arch != kOk) return arch;
+  const int sms = current_sm_count();
+  FwdParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.d = make_dims(N, T, H_k, H_v, n_init, o, sms);
+  p.L = fwd_layout(p.d);
+  if (ws_bytes < p.L.total) return GDN_ERR_WORKSPACE;
+  if (T > 0) {
+    const uint64_t row_k = (uint64_t)H_k * kDim * 2, row_v = (uint64_t)H_v * kDim * 2;
+    if (!make_tmap_bf16_3d(&p.tm_q, q, kDim, H_k, T, kDim * 2, row_k, 64, 1, 64) ||
+        !make_tmap_bf16_3d(&p.tm_k, k, kDim, H_k, T, kDim * 2, row_k, 64, 1, 64) ||
+        !make_tmap_bf16_3d(&p.tm_v, v, kDim, H_v, T, kDim * 2, row_v, 64, 1, 64))
+      return GDN_ERR_CUDA;
+  }
+  p.g = g;
+  p.beta = beta;
+  p.cu = cu_seqlens;
+  p.init_idx = init_idx;
+  p.initial_state = initial_state;
+  p.out = reinterpret_cast<__nv_bfloat16*>(out);
+  p.final_state = final_state;
+  p.ws = reinterpret_cast<uint8_t*>(workspace);
+  p.trunc_thr = o.trunc_log_threshold;
+  p.scale = o.scale;
+  return launch_fwd(p, (cudaStream_t)stream);
+}
+
+int gdn_chunk_bwd(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                  const int32_t* cu_seqlens, int N, int T, int H_k, int H_v, int head_dim,
+                  const int32_t* init_idx, const float* initial_state, int n_init, const void* dout,
+                  const float* dfinal_state, void* dq, void* dk, void* dv, float* dg, float* dbeta,
+                  float* dinitial_state, void* workspace, size_t ws_bytes, const gdn_options* opt,
+                  gdn_stream_t stream) {
+  if (head_dim != kDim) return GDN_ERR_UNSUPPORTED;
+  if (!sizes_ok(N, T, H_k, H_v) || n_init < 0) return GDN_ERR_INVALID_ARG;
+  const gdn_options o = resolve(opt);
+  if (!valid_options(o)) return GDN_ERR_INVALID_ARG;
+  if (!cu_seqlens || !workspace) return GDN_ERR_INVALID_ARG;
+  if (T > 0 && (!q || !k || !v || !g || !beta || !dout || !dq || !dk || !dv || !dg || !dbeta))
+    return GDN_ERR_INVALID_ARG;
+  if (n_init > 0 && (!initial_state || !dinitial_state)) return GDN_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(dout, 16) || !aligned(dq, 16) ||
+      !aligned(dk, 16) || !aligned(dv, 16) || !aligned(initial_state, 16) || !aligned(dfinal_state, 16) ||
+      !aligned(dinitial_state, 16) || !aligned(workspace, 256))
+    return GDN_ERR_INVALID_ARG;
+  const int dev = select_device_of(workspace);
+  if (dev != kOk) return dev;
+  const int arch = check_arch();
+  if (arch != kOk) return arch;
+  BwdArgs a;
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.g = g;
+  a.beta = beta;
+  a.cu = cu_seqlens;
+  a.init_idx = init_idx;
+  a.initial_state = initial_state;
+  a.dout = dout;
+  a.dfinal = dfinal_state;
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.dg = dg;
+  a.dbeta = dbeta;
+  a.dinit = dinitial_state;
+  a.ws = workspace;
+  a.ws_bytes = ws_bytes;
+  a.d = make_dims(N, T, H_k, H_v, n_init, o, current_sm_count());
+  a.trunc_thr = o.trunc_log_threshold;
+  a.scale = o.scale;
+  return launch_bwd(a, (cudaStream_t)stream);
+}
+
+int gdn_plan_host(const int32_t* cu, int N, int T, int H_v, const int32_t* init_idx, int n_init,
+                  const gdn_options* opt, int num_sms, int32_t* chunk_seq, int32_t* chunk_tok0, int32_t* chunk_len,
+                  int max_chunks_arg, int32_t* seg_info, int max_segs_arg, int32_t* out_counts) {
+  if (!cu || N < 1 || T < 0 || H_v < 1 || n_init < 0 || !out_counts) return GDN_ERR_INVALID_ARG;
+  const gdn_options o = resolve(opt);
+  if (!valid_options(o)) return GDN_ERR_INVALID_ARG;
+  if (cu[0] != 0 || cu[N] != T) return GDN_ERR_INVALID_ARG;
+  for (int i = 0; i < N; ++i)
+    if (plan_check_doc(i, cu, init_idx, n_init) != kOk) return GDN_ERR_INVALID_ARG;
+  PlanDims d = make_dims(N, T, 1, H_v, n_init, o, num_sms);
+  std::vector<int32_t> seq_chunk0(N + 1), seq_seg0(N + 1);
+  int total = 0, longest = 0;
+  for (int i = 0; i < N; ++i) {
+    seq_chunk0[i] = total;
+    const int c = doc_chunks(i, cu);
+    total += c;
+    if (c > longest) longest = c;
+  }
+  seq_chunk0[N] = total;
+  const int L = plan_seg_len(d, total, longest);
+  int segs = 0;
+  for (int i = 0; i < N; ++i) {
+    seq_seg0[i] = segs;
+    segs += doc_segs(doc_chunks(i, cu), L);
+  }
+  seq_seg0[N] = segs;
+  out_counts[0] = total;
+  out_counts[1] = segs;
+  out_counts[2] = L;
+  if (total > max_chunks_arg || segs > max_segs_arg) return GDN_ERR_WORKSPACE;
+  for (int c = 0; c < total; ++c) plan_chunk(c, seq_chunk0.data(), N, cu, chunk_seq + c, chunk_tok0 + c, chunk_len + c);
+  for (int s = 0; s < segs; ++s)
+    plan_segment(s, seq_seg0.data(), seq_chunk0.data(), N, cu, L, init_idx, n_init, seg_info + 4 * s);
+  return GDN_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,919 @@
+// Forward kernels of the chunked Gated DeltaNet over packed varlen batches (sm_103a).
+//
+//   plan_kernel       chunk map, segment map, dependencies, queue and flag reset (device planner)
+//   kkt_solve_kernel  per (chunk, key head): K K^T on tcgen05, then per value head of the group the
+//                     chunk-local cumulative gate gamma, A = diag(beta) (e^{gamma_i-gamma_j} o K K^T)
+//                     (strictly lower), T = (I + A)^{-1} by blocked forward substitution, and
+//                     T diag(beta e^gamma), T diag(beta) in bf16 ("How to Speed Up GDN Kernels for Qwen
+//                     Models", sections "What GDN actually computes" (kkt_solve, one 64x64 system per
+//                     chunk per head) and "Lever 2" (gate cumsum once per chunk, triangular inverse
+//                     solved once and reused by the output path and the state update)).
+//   chain_kernel<OUT> persistent over (segment, value head) items in dependency order: the state S
+//                     (fp32, 128x128) lives in registers across 8 warps; per chunk, tcgen05 MMAs compute
+//                     W = T_w K, P = Q K^T, then [Q~; -W] S + [0; U] (U = T_u V preloaded into the same
+//                     accumulator), V' = U - W S, S += K^T diag(e^{gamma_C - gamma}) V', O = Q~ S + P V'.
+//   chain_kernel<P1>  pass 1 of the exact segment split: per segment, the end state from zero (B) and
+//                     the segment transition (M, started from I) -- or, for a first segment with a known
+//                     start, its end state directly -- so that segment end states can be published as
+//                     soon as the start state is known ("Lever 1": a sequence is split into segments
+//                     that run in parallel; here the carry is exact instead of truncated).
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "bw_prims.cuh"
+#include "gdn_common.cuh"
+#include "gdn_fwd.h"
+
+namespace gdn {
+using namespace bw;
+
+constexpr long long kWaitBudget = 4000000000LL;  // clock cycles (about two seconds)
+
+__device__ __forceinline__ int ld_acquire(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release(int* p, int v) {
+  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ void set_status(Header* hd, int code) { atomicCAS(&hd->status, 0, code); }
+__device__ __forceinline__ int get_status(const Header* hd) {
+  return *reinterpret_cast<const volatile int*>(&hd->status);
+}
+
+// Bounded wait on a publication flag; false on timeout (status set) or on an earlier error.
+__device__ bool wait_flag(const int* flag, Header* hd) {
+  const long long t0 = clock64();
+  while (ld_acquire(flag) == 0) {
+    if (get_status(hd) != 0) return false;
+    if (clock64() - t0 > kWaitBudget) {
+      set_status(hd, kErrTimeout);
+      return false;
+    }
+    __nanosleep(128);
+  }
+  return true;
+}
+
+// All threads of the CTA wait on `bar`; the outcome is made uniform with a vote so that no
+// thread leaves while others still expect a barrier. On failure each thread waits once more
+// (bounded) so that copies or MMAs still in flight can land before the caller gives up.
+__device__ __forceinline__ bool wait_all(uint64_t* bar, uint32_t parity) {
+  const bool ok = bw::mbar_wait(bar, parity, kWaitBudget);
+  if (__syncthreads_or(!ok)) {
+    bw::mbar_wait(bar, parity, kWaitBudget);
+    return false;
+  }
+  return true;
+}
+
+template <class T>
+__device__ __forceinline__ T* ws_ptr(const FwdParams& p, size_t off) {
+  return reinterpret_cast<T*>(p.ws + off);
+}
+
+// ============================================================================================ plan
+
+__global__ void __launch_bounds__(1024) plan_kernel(const __grid_constant__ FwdParams p) {
+  Header* hd = ws_ptr<Header>(p, p.L.header);
+  int32_t* seq_chunk0 = ws_ptr<int32_t>(p, p.L.seq_chunk0);
+  int32_t* seq_seg0 = ws_ptr<int32_t>(p, p.L.seq_seg0);
+  const int N = p.d.N;
+  const int tid = threadIdx.x, nt = blockDim.x;
+  __shared__ int s_bad, s_L, s_longest;
+  __shared__ int s_carry[2];
+  __shared__ int s_scan[1024];
+  if (tid == 0) {
+    s_bad = 0;
+    s_longest = 0;
+  }
+  __syncthreads();
+  // validation
+  if (tid == 0 && (p.cu[0] != 0 || p.cu[N] != p.d.T)) s_bad = 1;
+  for (int i = tid; i < N; i += nt)
+    if (plan_check_doc(i, p.cu, p.init_idx, p.d.n_init) != kOk) s_bad = 1;
+  __syncthreads();
+  if (s_bad) {
+    if (tid == 0) {
+      hd->status = kErrInvalid;
+      hd->n_chunks = 0;
+      hd->n_segs = 0;
+      hd->n_p1 = 0;
+      hd->q_p1 = 0;
+      hd->q_chain = 0;
+    }
+    return;
+  }
+  // exclusive scan of chunk counts -> seq_chunk0 (tiles of nt documents)
+  if (tid == 0) s_carry[0] = 0;
+  __syncthreads();
+  for (int base = 0; base < N; base += nt) {
+    const int i = base + tid;
+    const int c = (i < N) ? doc_chunks(i, p.cu) : 0;
+    if (i < N) atomicMax(&s_longest, c);
+    s_scan[tid] = c;
+    __syncthreads();
+    for (int off = 1; off < nt; off <<= 1) {
+      const int v = (tid >= off) ? s_scan[tid - off] : 0;
+      __syncthreads();
+      s_scan[tid] += v;
+      __syncthreads();
+    }
+    if (i < N) seq_chunk0[i] = s_carry[0] + s_scan[tid] - c;
+    __syncthreads();
+    if (tid == nt - 1) s_carry[0] += s_scan[tid];
+    __syncthreads();
+  }
+  const int total_chunks = s_carry[0];
+  if (tid == 0) {
+    seq_chunk0[N] = total_chunks;
+    s_L = plan_seg_len(p.d, total_chunks, s_longest);
+  }
+  __syncthreads();
+  const int L = s_L;
+  // exclusive scan of segment counts -> seq_seg0
+  if (tid == 0) s_carry[1] = 0;
+  __syncthreads();
+  for (int base = 0; base < N; base += nt) {
+    const int i = base + tid;
+    const int c = (i < N) ? doc_segs(doc_chunks(i, p.cu), L) : 0;
+    s_scan[tid] = c;
+    __syncthreads();
+    for (int off = 1; off < nt; off <<= 1) {
+      const int v = (tid >= off) ? s_scan[tid - off] : 0;
+      __syncthreads();
+      s_scan[tid] += v;
+      __syncthreads();
+    }
+    if (i < N) seq_seg0[i] = s_carry[1] + s_scan[tid] - c;
+    __syncthreads();
+    if (tid == nt - 1) s_carry[1] += s_scan[tid];
+    __syncthreads();
+  }
+  const int total_segs = s_carry[1];
+  if (tid == 0) seq_seg0[N] = total_segs;
+  __syncthreads();
+  // chunk and segment tables
+  int32_t* cs = ws_ptr<int32_t>(p, p.L.chunk_seq);
+  int32_t* ct = ws_ptr<int32_t>(p, p.L.chunk_tok0);
+  int32_t* cl = ws_ptr<int32_t>(p, p.L.chunk_len);
+  for (int c = tid; c < total_chunks; c += nt) plan_chunk(c, seq_chunk0, N, p.cu, cs + c, ct + c, cl + c);
+  int32_t* si = ws_ptr<int32_t>(p, p.L.seg_info);
+  for (int s = tid; s < total_segs; s += nt)
+    plan_segment(s, seq_seg0, seq_chunk0, N, p.cu, L, p.init_idx, p.d.n_init, si + 4 * s);
+  // flags
+  int32_t* fs = ws_ptr<int32_t>(p, p.L.flags_seg);
+  int32_t* ff = ws_ptr<int32_t>(p, p.L.flags_fin);
+  for (int e = tid; e < total_segs * p.d.Hv; e += nt) fs[e] = 0;
+  for (int e = tid; e < N * p.d.Hv; e += nt) ff[e] = 0;
+  __syncthreads();
+  // slots and pass-1 units (serial: only split segments get them)
+  if (tid == 0) {
+    int32_t* slot = ws_ptr<int32_t>(p, p.L.seg_slot);
+    int32_t* p1 = ws_ptr<int32_t>(p, p.L.p1_list);
+    int ns = 0, nu = 0, out_of_slots = 0;
+    for (int s = 0; s < total_segs; ++s) {
+      const int i = si[4 * s];
+      const bool last = (s + 1 == seq_seg0[i + 1]);
+      const bool split = (seq_seg0[i + 1] - seq_seg0[i]) > 1;
+      slot[s] = -1;
+      if (split && !last && p.d.mode == 0) {
+        if (ns >= p.L.slots) {
+          out_of_slots = 1;
+          break;
+        }
+        slot[s] = ns++;
+        if (si[4 * s + 3] == -1) {
+          p1[2 * nu] = s;
+          p1[2 * nu + 1] = 2;  // end state from the known start, published directly
+          ++nu;
+        } else {
+          p1[2 * nu] = s;
+          p1[2 * nu + 1] = 0;  // transition M
+          ++nu;
+          p1[2 * nu] = s;
+          p1[2 * nu + 1] = 1;  // end state from zero B
+          ++nu;
+        }
+      }
+    }
+    hd->status = out_of_slots ? kErrWorkspace : 0;
+    hd->n_chunks = out_of_slots ? 0 : total_chunks;
+    hd->n_segs = out_of_slots ? 0 : total_segs;
+    hd->seg_chunks = L;
+    hd->n_p1 = out_of_slots ? 0 : nu;
+    hd->q_p1 = 0;
+    hd->q_chain = 0;
+  }
+}
+
+// ======================================================================================= kkt_solve
+
+// Shared memory of kkt_solve (after 1024-byte alignment).
+struct KktSmem {
+  uint8_t k_tile[2][8192];  // K rows of the chunk, two 64-wide dk blocks, SW128
+  float kk[64][65];
+  float a[64][65];
+  float t[64][65];
+  float y[3][16][16];
+  float gam[64];
+  float beta[64];
+};
+
+__global__ void __launch_bounds__(128) kkt_solve_kernel(const __grid_constant__ FwdParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  KktSmem& sm = *reinterpret_cast<KktSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ uint64_t bar_ld, bar_mma;
+  __shared__ uint32_t tmem_holder;
+  Header* hd = ws_ptr<Header>(p, p.L.header);
+  const int chunk = blockIdx.x, hk = blockIdx.y;
+  if (chunk >= hd->n_chunks || get_status(hd) != 0) return;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tok0 = ws_ptr<int32_t>(p, p.L.chunk_tok0)[chunk];
+  const int n = ws_ptr<int32_t>(p, p.L.chunk_len)[chunk];
+  const int Hv = p.d.Hv, G = p.d.Hv / p.d.Hk;
+
+  if (tid == 0) {
+    mbar_init(&bar_ld, 1);
+    mbar_init(&bar_mma, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) tmem_alloc(&tmem_holder, 64);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_holder;
+  bool ok = true;
+  if (tid == 0) {
+    mbar_arrive_expect_tx(&bar_ld, 16384);
+    tma_load_3d(sm.k_tile[0], &p.tm_k, 0, hk, tok0, &bar_ld);
+    tma_load_3d(sm.k_tile[1], &p.tm_k, 64, hk, tok0, &bar_ld);
+    ok = mbar_wait(&bar_ld, 0, kWaitBudget);
+    if (!ok) mbar_wait(&bar_ld, 0, kWaitBudget);  // let a late copy land before the CTA can exit
+    if (ok) {
+      tc_fence_after();
+      const uint32_t kt = smem_u32(sm.k_tile[0]);
+      for (int ks = 0; ks < 8; ++ks)
+        umma_bf16(tmem, kmajor_desc(kt, 8192, ks), kmajor_desc(kt, 8192, ks), idesc_bf16(64, 64, 0, 0), ks > 0);
+      umma_commit(&bar_mma);
+    }
+  }
+  // zero T (upper blocks stay zero)
+  for (int e = tid; e < 64 * 65; e += 128) (&sm.t[0][0])[e] = 0.f;
+  __shared__ int s_ld_ok;
+  if (tid == 0) s_ld_ok = ok ? 1 : 0;
+  __syncthreads();
+  bool ok_mma = false;
+  if (s_ld_ok) ok_mma = wait_all(&bar_mma, 0);
+  tc_fence_after();
+  if (!ok_mma) {
+    if (tid == 0) set_status(hd, kErrTimeout);
+  } else {
+    // K K^T readback (M = 64: row 16q + l sits in lane 32q + l, l < 16)
+    const int q4 = warp & 3;
+    for (int c = 0; c < 64; c += 16) {
+      float v[16];
+      tmem_ld16(tmem + ((uint32_t)(32 * q4) << 16) + c, v);
+      tmem_ld_wait();
+      if (lane < 16)
+        for (int i = 0; i < 16; ++i) sm.kk[16 * q4 + lane][c + i] = v[i];
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, 64);
+  if (!ok_mma) return;
+
+  float* gam_ws = ws_ptr<float>(p, p.L.gam);
+  uint8_t* tw_ws = ws_ptr<uint8_t>(p, p.L.tw);
+  uint8_t* tu_ws = ws_ptr<uint8_t>(p, p.L.tu);
+  for (int hh = 0; hh < G; ++hh) {
+    const int h = hk * G + hh;
+    // chunk-local cumulative gate (inclusive scan over 64 tokens in two warps)
+    if (tid < 64) {
+      const float gi = (tid < n) ? p.g[(size_t)(tok0 + tid) * Hv + h] : 0.f;
+      const float bi = (tid < n) ? p.beta[(size_t)(tok0 + tid) * Hv + h] : 0.f;
+      float s = gi;
+      for (int off = 1; off < 32; off <<= 1) {
+        const float o = __shfl_up_sync(0xffffffffu, s, off);
+        if (lane >= off) s += o;
+      }
+      sm.gam[tid] = s;
+      sm.beta[tid] = bi;
+    }
+    __syncthreads();
+    if (tid >= 32 && tid < 64) sm.gam[tid] += sm.gam[31];
+    __syncthreads();
+    if (tid < 64) gam_ws[((size_t)chunk * Hv + h) * 64 + tid] = sm.gam[tid];
+    // A (strictly lower)
+    for (int e = tid; e < 64 * 64; e += 128) {
+      const int i = e >> 6, j = e & 63;
+      sm.a[i][j] = (j < i) ? sm.beta[i] * __expf(sm.gam[i] - sm.gam[j]) * sm.kk[i][j] : 0.f;
+    }
+    __syncthreads();
+    // (I + A)^{-1}: diagonal 16x16 blocks by forward substitution, one warp per block
+    if (lane < 16) {
+      const int b = warp, c = lane;
+      float x[16];
+#pragma unroll
+      for (int r = 0; r < 16; ++r) {
+        float s = (r == c) ? 1.f : 0.f;
+#pragma unroll
+        for (int m = 0; m < r; ++m) s -= sm.a[16 * b + r][16 * b + m] * x[m];
+        x[r] = s;
+      }
+#pragma unroll
+      for (int r = 0; r < 16; ++r) sm.t[16 * b + r][16 * b + c] = x[r];
+    }
+    __syncthreads();
+    // off-diagonal blocks by block distance: T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj
+    for (int dd = 1; dd < 4; ++dd) {
+      const int nb = 4 - dd;
+      for (int e = tid; e < nb * 256; e += 128) {
+        const int bi = e >> 8, r = (e >> 4) & 15, cc = e & 15;
+        const int i = dd + bi, j = i - dd;
+        float s = 0.f;
+        for (int kb = j; kb < i; ++kb)
+#pragma unroll
+          for (int m = 0; m < 16; ++m) s += sm.a[16 * i + r][16 * kb + m] * sm.t[16 * kb + m][16 * j + cc];
+        sm.y[bi][r][cc] = s;
+      }
+      __syncthreads();
+      for (int e = tid; e < nb * 256; e += 128) {
+        const int bi = e >> 8, r = (e >> 4) & 15, cc = e & 15;
+        const int i = dd + bi, j = i - dd;
+        float s = 0.f;
+#pragma unroll
+        for (int m = 0; m < 16; ++m) s += sm.t[16 * i + r][16 * i + m] * sm.y[bi][m][cc];
+        sm.t[16 * i + r][16 * j + cc] = -s;
+      }
+      __syncthreads();
+    }
+    // T diag(beta e^gamma) and T diag(beta), bf16, stored as the SW128 K-major smem image
+    uint8_t* dw = tw_ws + ((size_t)chunk * Hv + h) * 8192;
+    uint8_t* du = tu_ws + ((size_t)chunk * Hv + h) * 8192;
+    for (int e = tid; e < 2 * 64 * 8; e += 128) {
+      const int mat = e >> 9, r = (e >> 3) & 63, cj = e & 7;
+      uint32_t w[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int j0 = cj * 8 + 2 * u;
+        float s0 = sm.beta[j0], s1 = sm.beta[j0 + 1];
+        if (mat == 0) {
+          s0 *= __expf(sm.gam[j0]);
+          s1 *= __expf(sm.gam[j0 + 1]);
+        }
+        w[u] = pack_bf16x2(sm.t[r][j0] * s0, sm.t[r][j0 + 1] * s1);
+      }
+      uint8_t* dst = (mat == 0 ? dw : du) + r * 128 + ((cj ^ (r & 7)) << 4);
+      *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    __syncthreads();
+  }
+}
+
+// =========================================================================================== chain
+
+enum ChainMode { kModeOut = 0, kModeP1 = 1 };
+
+// Shared memory of the chain kernel (after 1024-byte alignment). Every operand block is a
+// 128B-swizzled image (rows of 64 bf16); see bw_prims.cuh for the descriptor conventions.
+struct ChainSmem {
+  uint8_t q[2][8192];     // Q rows t, dk blocks                      (A, K-major: P = Q K^T)
+  uint8_t k[2][8192];     // K rows t, dk blocks                      (B K-major / B MN-major / A MN-major)
+  uint8_t v[2][8192];     // V rows t, dv blocks                      (B, MN-major: U)
+  uint8_t p[8192];        // P = (Q K^T) o E, rows t                  ([P; 0] A operand)
+  uint8_t z[8192];        // zeros                                    ([0; T_u] A operand)
+  uint8_t tu[8192];       // T diag(beta)
+  uint8_t tw[8192];       // T diag(beta e^gamma)                     (A, M=64: W = T_w K)
+  uint8_t qw[2][16384];   // dk block b: rows 0-63 Q~ = diag(e^gamma) Q, rows 64-127 -W   (A, M=128)
+  uint8_t vo[2][8192];    // V' rows t, dv blocks                     (B, MN-major: P V')
+  uint8_t vs[2][8192];    // diag(e^{gamma_C - gamma}) V'             (B, MN-major: K^T V's)
+  uint8_t s[2][16384];    // S in bf16: rows dk, dv blocks            (B, MN-major: [Q~; -W] S)
+  float gam[64];
+};
+constexpr size_t kChainSmemBytes = sizeof(ChainSmem) + 1024;
+
+// TMEM columns.
+constexpr uint32_t kTmD1 = 0;    // [Q~ S + P V' ; U - W S]   (M = 128, 128 cols)
+constexpr uint32_t kTmD2 = 128;  // K^T V's                   (M = 128, 128 cols)
+constexpr uint32_t kTmW = 256;   // W                         (M = 64, 128 cols)
+constexpr uint32_t kTmG = 384;   // Q K^T                     (M = 64, 64 cols)
+
+struct ChainCtx {
+  ChainSmem* sm;
+  uint64_t* bar_ld;
+  uint64_t* bar_mma;
+  uint32_t tmem;
+  uint32_t ph_ld, ph_mma;
+  int tid, warp, lane, q4, half;
+};
+
+// Write this thread's 64 state values (row dk = 32*q4 + lane, columns 64*half ..) as bf16 into sm.s.
+__device__ __forceinline__ void store_state_bf16(ChainCtx& cx, const float* S) {
+  const int r = 32 * cx.q4 + cx.lane;
+  uint8_t* blk = cx.sm->s[cx.half];
+#pragma unroll
+  for (int cj = 0; cj < 8; ++cj) {
+    uint4 w = make_uint4(pack_bf16x2(S[8 * cj + 0], S[8 * cj + 1]), pack_bf16x2(S[8 * cj + 2], S[8 * cj + 3]),
+                         pack_bf16x2(S[8 * cj + 4], S[8 * cj + 5]), pack_bf16x2(S[8 * cj + 6], S[8 * cj + 7]));
+    *reinterpret_cast<uint4*>(blk + r * 128 + ((cj ^ (r & 7)) << 4)) = w;
+  }
+}
+
+__device__ __forceinline__ void sync_generic_to_async() {
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+}
+
+// One chunk of the chain. S: this thread's 64 fp32 state values (updated in place).
+// Returns false if a bounded wait ran out (status already set).
+template <bool kOut, bool kWithU>
+__device__ bool chain_chunk(const FwdParams& p, ChainCtx& cx, float* S, int gc, int h, int hk, int tok0, int n) {
+  ChainSmem& sm = *cx.sm;
+  const int Hv = p.d.Hv;
+  if (cx.tid == 0) {
+    uint32_t bytes = 2 * 8192 /*K*/ + 8192 /*Tw*/ + 256;
+    if (kOut) bytes += 2 * 8192;
+    if (kWithU) bytes += 2 * 8192 + 8192;
+    mbar_arrive_expect_tx(cx.bar_ld, bytes);
+    tma_load_3d(sm.k[0], &p.tm_k, 0, hk, tok0, cx.bar_ld);
+    tma_load_3d(sm.k[1], &p.tm_k, 64, hk, tok0, cx.bar_ld);
+    if (kOut) {
+      tma_load_3d(sm.q[0], &p.tm_q, 0, hk, tok0, cx.bar_ld);
+      tma_load_3d(sm.q[1], &p.tm_q, 64, hk, tok0, cx.bar_ld);
+    }
+    if (kWithU) {
+      tma_load_3d(sm.v[0], &p.tm_v, 0, h, tok0, cx.bar_ld);
+      tma_load_3d(sm.v[1], &p.tm_v, 64, h, tok0, cx.bar_ld);
+      bulk_load(sm.tu, p.ws + p.L.tu + ((size_t)gc * Hv + h) * 8192, 8192, cx.bar_ld);
+    }
+    bulk_load(sm.tw, p.ws + p.L.tw + ((size_t)gc * Hv + h) * 8192, 8192, cx.bar_ld);
+    bulk_load(sm.gam, p.ws + p.L.gam + ((size_t)gc * Hv + h) * 256, 256, cx.bar_ld);
+  }
+  if (!wait_all(cx.bar_ld, cx.ph_ld)) return false;
+  cx.ph_ld ^= 1;
+  tc_fence_after();
+
+  // -- MMA group 1: W = T_w K (M=64), P-raw = Q K^T (M=64)
+  if (cx.tid == 0) {
+    const uint32_t k0 = smem_u32(sm.k[0]);
+    for (int ks = 0; ks < 4; ++ks)
+      umma_bf16(cx.tmem + kTmW, kmajor_desc(smem_u32(sm.tw), 8192, ks), mnmajor_desc(k0, 8192, ks),
+                idesc_bf16(64, 128, 0, 1), ks > 0);
+    if (kOut)
+      for (int ks = 0; ks < 8; ++ks)
+        umma_bf16(cx.tmem + kTmG, kmajor_desc(smem_u32(sm.q[0]), 8192, ks), kmajor_desc(k0, 8192, ks),
+                  idesc_bf16(64, 64, 0, 0), ks > 0);
+    umma_commit(cx.bar_mma);
+  }
+  const float gC = sm.gam[63];
+  if (kOut) {
+    // Q~ = diag(e^gamma) Q into rows 0-63 of sm.qw
+    for (int e = cx.tid; e < 2 * 64 * 8; e += 256) {
+      const int b = e >> 9, r = (e >> 3) & 63, cj = e & 7;
+      const uint32_t off = r * 128 + ((cj ^ (r & 7)) << 4);
+      uint4 raw = *reinterpret_cast<const uint4*>(sm.q[b] + off);
+      const float sc = __expf(sm.gam[r]) * p.scale;
+      __nv_bfloat162* x = reinterpret_cast<__nv_bfloat162*>(&raw);
+      uint32_t w[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        float2 f = __bfloat1622float2(x[u]);
+        w[u] = pack_bf16x2(f.x * sc, f.y * sc);
+      }
+      *reinterpret_cast<uint4*>(sm.qw[b] + off) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  }
+  if (!wait_all(cx.bar_mma, cx.ph_mma)) return false;
+  cx.ph_mma ^= 1;
+  tc_fence_after();
+  {
+    const uint32_t lane_base = (uint32_t)(32 * cx.q4) << 16;
+    const int i = 16 * cx.q4 + cx.lane;  // row for lanes < 16 (M = 64 layout)
+    // -W into rows 64-127 of sm.qw (dk block = half)
+    for (int cc = 0; cc < 64; cc += 16) {
+      float v[16];
+      tmem_ld16(cx.tmem + kTmW + lane_base + 64 * cx.half + cc, v);
+      tmem_ld_wait();
+      if (cx.lane < 16) {
+        const int r = 64 + i;
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int cj = (cc >> 3) + u;
+          uint4 w = make_uint4(pack_bf16x2(-v[8 * u + 0], -v[8 * u + 1]), pack_bf16x2(-v[8 * u + 2], -v[8 * u + 3]),
+                               pack_bf16x2(-v[8 * u + 4], -v[8 * u + 5]), pack_bf16x2(-v[8 * u + 6], -v[8 * u + 7]));
+          *reinterpret_cast<uint4*>(sm.qw[cx.half] + r * 128 + ((cj ^ (r & 7)) << 4)) = w;
+        }
+      }
+    }
+    if (kOut) {
+      // P = (Q K^T) o E, masked causal and to the chunk's valid tokens (32 columns per half)
+      for (int cc = 0; cc < 32; cc += 16) {
+        float v[16];
+        tmem_ld16(cx.tmem + kTmG + lane_base + 32 * cx.half + cc, v);
+        tmem_ld_wait();
+        if (cx.lane < 16) {
+          const float gi = sm.gam[i];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            float pv[8];
+#pragma unroll
+            for (int x = 0; x < 8; ++x) {
+              const int j = 32 * cx.half + cc + 8 * u + x;
+              pv[x] = (j <= i && i < n) ? __expf(gi - sm.gam[j]) * p.scale * v[8 * u + x] : 0.f;
+            }
+            const int cj = ((32 * cx.half + cc) >> 3) + u;
+            uint4 w = make_uint4(pack_bf16x2(pv[0], pv[1]), pack_bf16x2(pv[2], pv[3]), pack_bf16x2(pv[4], pv[5]),
+                                 pack_bf16x2(pv[6], pv[7]));
+            *reinterpret_cast<uint4*>(sm.p + i * 128 + ((cj ^ (i & 7)) << 4)) = w;
+          }
+        }
+      }
+    }
+  }
+  sync_generic_to_async();
+
+  // -- MMA group 2: D1 = [0; T_u] V + [Q~; -W] S
+  if (cx.tid == 0) {
+    if (kWithU)
+      for (int ks = 0; ks < 4; ++ks)
+        umma_bf16(cx.tmem + kTmD1, kmajor_desc(smem_u32(sm.z), 16384, ks), mnmajor_desc(smem_u32(sm.v[0]), 8192, ks),
+                  idesc_bf16(128, 128, 0, 1), ks > 0);
+    for (int ks = 0; ks < 8; ++ks)
+      umma_bf16(cx.tmem + kTmD1, kmajor_desc(smem_u32(sm.qw[0]), 16384, ks),
+                mnmajor_desc(smem_u32(sm.s[0]), 16384, ks), idesc_bf16(128, 128, 0, 1), (kWithU || ks > 0) ? 1 : 0);
+    umma_commit(cx.bar_mma);
+  }
+  if (!wait_all(cx.bar_mma, cx.ph_mma)) return false;
+  cx.ph_mma ^= 1;
+  tc_fence_after();
+  // V' = rows 64-127 of D1 (lanes 64-127: quarters 2 and 3)
+  if (cx.q4 >= 2) {
+    const int t = 32 * (cx.q4 - 2) + cx.lane;
+    const float sc = __expf(gC - sm.gam[t]);
+    const uint32_t lane_base = (uint32_t)(32 * cx.q4) << 16;
+    for (int cc = 0; cc < 64; cc += 16) {
+      float v[16];
+      tmem_ld16(cx.tmem + kTmD1 + lane_base + 64 * cx.half + cc, v);
+      tmem_ld_wait();
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int cj = (cc >> 3) + u;
+        const uint32_t off = t * 128 + ((cj ^ (t & 7)) << 4);
+        const float* x = v + 8 * u;
+        *reinterpret_cast<uint4*>(sm.vo[cx.half] + off) =
+            make_uint4(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]), pack_bf16x2(x[4], x[5]), pack_bf16x2(x[6], x[7]));
+        *reinterpret_cast<uint4*>(sm.vs[cx.half] + off) =
+            make_uint4(pack_bf16x2(x[0] * sc, x[1] * sc), pack_bf16x2(x[2] * sc, x[3] * sc),
+                       pack_bf16x2(x[4] * sc, x[5] * sc), pack_bf16x2(x[6] * sc, x[7] * sc));
+      }
+    }
+  }
+  sync_generic_to_async();
+
+  // -- MMA group 3: D2 = K^T V's ; D1 += [P; 0] V'
+  if (cx.tid == 0) {
+    for (int ks = 0; ks < 4; ++ks)
+      umma_bf16(cx.tmem + kTmD2, mnmajor_desc(smem_u32(sm.k[0]), 8192, ks), mnmajor_desc(smem_u32(sm.vs[0]), 8192, ks),
+                idesc_bf16(128, 128, 1, 1), ks > 0);
+    if (kOut)
+      for (int ks = 0; ks < 4; ++ks)
+        umma_bf16(cx.tmem + kTmD1, kmajor_desc(smem_u32(sm.p), 16384, ks), mnmajor_desc(smem_u32(sm.vo[0]), 8192, ks),
+                  idesc_bf16(128, 128, 0, 1), 1);
+    umma_commit(cx.bar_mma);
+  }
+  if (!wait_all(cx.bar_mma, cx.ph_mma)) return false;
+  cx.ph_mma ^= 1;
+  tc_fence_after();
+  {
+    const uint32_t lane_base = (uint32_t)(32 * cx.q4) << 16;
+    const float GC = __expf(gC);
+    for (int cc = 0; cc < 64; cc += 16) {
+      float v[16];
+      tmem_ld16(cx.tmem + kTmD2 + lane_base + 64 * cx.half + cc, v);
+      tmem_ld_wait();
+#pragma unroll
+      for (int x = 0; x < 16; ++x) S[cc + x] = GC * S[cc + x] + v[x];
+    }
+    store_state_bf16(cx, S);
+    if (kOut && cx.q4 < 2) {
+      const int t = 32 * cx.q4 + cx.lane;
+      __nv_bfloat16* orow = p.out + ((size_t)(tok0 + t) * Hv + h) * kDim + 64 * cx.half;
+      for (int cc = 0; cc < 64; cc += 16) {
+        float v[16];
+        tmem_ld16(cx.tmem + kTmD1 + lane_base + 64 * cx.half + cc, v);
+        tmem_ld_wait();
+        if (t < n) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + cc);
+          dst[0] = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
+                              pack_bf16x2(v[6], v[7]));
+          dst[1] = make_uint4(pack_bf16x2(v[8], v[9]), pack_bf16x2(v[10], v[11]), pack_bf16x2(v[12], v[13]),
+                              pack_bf16x2(v[14], v[15]));
+        }
+      }
+    }
+  }
+  sync_generic_to_async();
+  return true;
+}
+
+// Load a 128x128 fp32 state (row-major [dk][dv]) into this thread's registers.
+__device__ __forceinline__ void load_state(const ChainCtx& cx, const float* src, float* S, bool cg) {
+  const float* row = src + (size_t)(32 * cx.q4 + cx.lane) * kDim + 64 * cx.half;
+  for (int c = 0; c < 64; c += 4) {
+    float4 f = cg ? __ldcg(reinterpret_cast<const float4*>(row + c)) : *reinterpret_cast<const float4*>(row + c);
+    S[c] = f.x;
+    S[c + 1] = f.y;
+    S[c + 2] = f.z;
+    S[c + 3] = f.w;
+  }
+}
+__device__ __forceinline__ void save_state(const ChainCtx& cx, float* dst, const float* S) {
+  float* row = dst + (size_t)(32 * cx.q4 + cx.lane) * kDim + 64 * cx.half;
+  for (int c = 0; c < 64; c += 4) *reinterpret_cast<float4*>(row + c) = make_float4(S[c], S[c + 1], S[c + 2], S[c + 3]);
+}
+
+// S_end = M S_start + B through one UMMA (M staged as bf16 in sm.qw, S_start in sm.s).
+__device__ bool affine_apply(const FwdParams& p, ChainCtx& cx, const float* Mm, const float* Bm, float* out) {
+  ChainSmem& sm = *cx.sm;
+  {
+    const int r = cx.tid >> 1, c0 = (cx.tid & 1) * 64;
+    const float* row = Mm + (size_t)r * kDim + c0;
+    uint8_t* blk = sm.qw[c0 >> 6];
+    for (int cj = 0; cj < 8; ++cj) {
+      float4 a = __ldcg(reinterpret_cast<const float4*>(row + 8 * cj));
+      float4 b = __ldcg(reinterpret_cast<const float4*>(row + 8 * cj + 4));
+      *reinterpret_cast<uint4*>(blk + r * 128 + ((cj ^ (r & 7)) << 4)) =
+          make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w), pack_bf16x2(b.x, b.y), pack_bf16x2(b.z, b.w));
+    }
+  }
+  sync_generic_to_async();
+  if (cx.tid == 0) {
+    for (int ks = 0; ks < 8; ++ks)
+      umma_bf16(cx.tmem + kTmD2, kmajor_desc(smem_u32(sm.qw[0]), 16384, ks), mnmajor_desc(smem_u32(sm.s[0]), 16384, ks),
+                idesc_bf16(128, 128, 0, 1), ks > 0);
+    umma_commit(cx.bar_mma);
+  }
+  if (!wait_all(cx.bar_mma, cx.ph_mma)) return false;
+  cx.ph_mma ^= 1;
+  tc_fence_after();
+  const uint32_t lane_base = (uint32_t)(32 * cx.q4) << 16;
+  const int r = 32 * cx.q4 + cx.lane;
+  for (int cc = 0; cc < 64; cc += 16) {
+    float v[16];
+    tmem_ld16(cx.tmem + kTmD2 + lane_base + 64 * cx.half + cc, v);
+    tmem_ld_wait();
+    const float* brow = Bm + (size_t)r * kDim + 64 * cx.half + cc;
+    float* orow = out + (size_t)r * kDim + 64 * cx.half + cc;
+    for (int x = 0; x < 16; x += 4) {
+      float4 b = __ldcg(reinterpret_cast<const float4*>(brow + x));
+      *reinterpret_cast<float4*>(orow + x) = make_float4(v[x] + b.x, v[x + 1] + b.y, v[x + 2] + b.z, v[x + 3] + b.w);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  return true;
+}
+
+__device__ __forceinline__ void publish(int* flag) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    st_release(flag, 1);
+  }
+}
+
+template <int kMode>
+__global__ void __launch_bounds__(256, 1) chain_kernel(const __grid_constant__ FwdParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  ChainSmem* smp = reinterpret_cast<ChainSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ uint64_t bar_ld, bar_mma;
+  __shared__ uint32_t tmem_holder;
+  __shared__ int s_item, s_ok;
+  Header* hd = ws_ptr<Header>(p, p.L.header);
+  ChainCtx cx;
+  cx.sm = smp;
+  cx.bar_ld = &bar_ld;
+  cx.bar_mma = &bar_mma;
+  cx.tid = threadIdx.x;
+  cx.warp = cx.tid >> 5;
+  cx.lane = cx.tid & 31;
+  cx.q4 = cx.warp & 3;
+  cx.half = cx.warp >> 2;
+  cx.ph_ld = 0;
+  cx.ph_mma = 0;
+  const int Hv = p.d.Hv, G = p.d.Hv / p.d.Hk;
+  const int n_items = (kMode == kModeOut ? hd->n_segs : hd->n_p1) * Hv;
+  if (blockIdx.x >= n_items || get_status(hd) != 0) return;
+
+  if (cx.tid == 0) {
+    mbar_init(&bar_ld, 1);
+    mbar_init(&bar_mma, 1);
+    fence_mbar_init();
+  }
+  // zero blocks: sm.z always; sm.qw rows 0-63 stay zero in pass 1 (no Q~)
+  for (int e = cx.tid; e < 8192 / 16; e += 256) reinterpret_cast<uint4*>(smp->z)[e] = make_uint4(0, 0, 0, 0);
+  if (kMode == kModeP1)
+    for (int e = cx.tid; e < 2 * 16384 / 16; e += 256) reinterpret_cast<uint4*>(smp->qw)[e] = make_uint4(0, 0, 0, 0);
+  if (cx.warp == 0) tmem_alloc(&tmem_holder, 512);
+  sync_generic_to_async();
+  cx.tmem = tmem_holder;
+
+  const int32_t* si = ws_ptr<int32_t>(p, p.L.seg_info);
+  const int32_t* slot = ws_ptr<int32_t>(p, p.L.seg_slot);
+  const int32_t* seq_seg0 = ws_ptr<int32_t>(p, p.L.seq_seg0);
+  const int32_t* ctok = ws_ptr<int32_t>(p, p.L.chunk_tok0);
+  const int32_t* clen = ws_ptr<int32_t>(p, p.L.chunk_len);
+  int* flags_seg = ws_ptr<int>(p, p.L.flags_seg);
+  int* flags_fin = ws_ptr<int>(p, p.L.flags_fin);
+  const size_t st_elems = (size_t)kDim * kDim;
+  float S[64];
+
+  for (;;) {
+    if (cx.tid == 0) {
+      const int it = (int)atomicAdd(kMode == kModeOut ? &hd->q_chain : &hd->q_p1, 1u);
+      s_item = (get_status(hd) != 0) ? n_items : it;
+    }
+    __syncthreads();
+    const int item = s_item;
+    if (item >= n_items) break;
+    const int h = item % Hv, hk = h / G;
+    bool ok = true;
+    if (kMode == kModeP1) {
+      const int32_t* p1 = ws_ptr<int32_t>(p, p.L.p1_list);
+      const int unit = item / Hv;
+      const int s = p1[2 * unit], part = p1[2 * unit + 1];
+      const int seq = si[4 * s], c0 = si[4 * s + 1], nch = si[4 * s + 2];
+      const int sl = slot[s];
+      // start: identity (part 0), zero (part 1) or the known start state (part 2)
+      if (part == 0) {
+        const int r = 32 * cx.q4 + cx.lane;
+        for (int c = 0; c < 64; ++c) S[c] = (r == 64 * cx.half + c) ? 1.f : 0.f;
+      } else if (part == 1) {
+        for (int c = 0; c < 64; ++c) S[c] = 0.f;
+      } else {
+        const int x = p.init_idx ? p.init_idx[seq] : -1;
+        if (x >= 0 && x < p.d.n_init)
+          load_state(cx, p.initial_state + ((size_t)x * Hv + h) * st_elems, S, false);
+        else
+          for (int c = 0; c < 64; ++c) S[c] = 0.f;
+      }
+      store_state_bf16(cx, S);
+      sync_generic_to_async();
+      for (int c = 0; c < nch && ok; ++c) {
+        const int gc = c0 + c;
+        if (part == 0)
+          ok = chain_chunk<false, false>(p, cx, S, gc, h, hk, ctok[gc], clen[gc]);
+        else
+          ok = chain_chunk<false, true>(p, cx, S, gc, h, hk, ctok[gc], clen[gc]);
+      }
+      if (!ok) break;
+      float* dst = (part == 0) ? ws_ptr<float>(p, p.L.mmat) : (part == 1) ? ws_ptr<float>(p, p.L.bmat)
+                                                                          : ws_ptr<float>(p, p.L.pub);
+      save_state(cx, dst + ((size_t)sl * Hv + h) * st_elems, S);
+      if (part == 2) publish(&flags_seg[s * Hv + h]);
+      __syncthreads();
+      continue;
+    }
+
+    // ---------------------------------------------------------------- output pass
+    const int s = item / Hv;
+    const int seq = si[4 * s], c0 = si[4 * s + 1], nch = si[4 * s + 2], dep = si[4 * s + 3];
+    const bool last = (s + 1 == seq_seg0[seq + 1]);
+    int first_chunk = c0;  // truncation mode may start earlier (warmup)
+    bool have_start = true;
+    if (dep == -1) {
+      const int x = p.init_idx ? p.init_idx[seq] : -1;
+      if (x >= 0 && x < p.d.n_init)
+        load_state(cx, p.initial_state + ((size_t)x * Hv + h) * st_elems, S, false);
+      else
+        for (int c = 0; c < 64; ++c) S[c] = 0.f;
+    } else if (dep <= -2) {
+      const int j = dep_fork_seq(dep);
+      if (cx.tid == 0) {
+        s_ok = wait_flag(&flags_fin[j * Hv + h], hd) ? 1 : 0;
+        __threadfence();
+      }
+      __syncthreads();
+      have_start = s_ok != 0;
+      if (have_start) load_state(cx, p.final_state + ((size_t)j * Hv + h) * st_elems, S, true);
+    } else if (p.d.mode == 0) {
+      if (cx.tid == 0) {
+        s_ok = wait_flag(&flags_seg[dep * Hv + h], hd) ? 1 : 0;
+        __threadfence();
+      }
+      __syncthreads();
+      have_start = s_ok != 0;
+      if (have_start) load_state(cx, ws_ptr<float>(p, p.L.pub) + ((size_t)slot[dep] * Hv + h) * st_elems, S, true);
+    } else {
+      // truncation: fewest preceding whole chunks of this document whose summed log-decay is
+      // below the threshold; from zero, or from the document's start state if the window reaches it
+      const float* gam = ws_ptr<float>(p, p.L.gam);
+      const int doc_c0 = ws_ptr<int32_t>(p, p.L.seq_chunk0)[seq];
+      int w = c0;
+      float acc = 0.f;
+      while (w > doc_c0 && acc >= p.trunc_thr) {
+        --w;
+        acc += gam[((size_t)w * Hv + h) * 64 + 63];
+      }
+      first_chunk = w;
+      for (int c = 0; c < 64; ++c) S[c] = 0.f;
+      if (w == doc_c0 && acc >= p.trunc_thr) {
+        const int s0 = seq_seg0[seq];
+        const int d0 = si[4 * s0 + 3];
+        if (d0 == -1) {
+          const int x = p.init_idx ? p.init_idx[seq] : -1;
+          if (x >= 0 && x < p.d.n_init) load_state(cx, p.initial_state + ((size_t)x * Hv + h) * st_elems, S, false);
+        } else {
+          const int j = dep_fork_seq(d0);
+          if (cx.tid == 0) {
+            s_ok = wait_flag(&flags_fin[j * Hv + h], hd) ? 1 : 0;
+            __threadfence();
+          }
+          __syncthreads();
+          have_start = s_ok != 0;
+          if (have_start) load_state(cx, p.final_state + ((size_t)j * Hv + h) * st_elems, S, true);
+        }
+      }
+    }
+    if (!have_start) break;
+    store_state_bf16(cx, S);
+    sync_generic_to_async();
+    // early publication of this segment's end state (exact split)
+    if (p.d.mode == 0 && slot[s] >= 0 && dep != -1) {
+      const size_t off = ((size_t)slot[s] * Hv + h) * st_elems;
+      if (!affine_apply(p, cx, ws_ptr<float>(p, p.L.mmat) + off, ws_ptr<float>(p, p.L.bmat) + off,
+                        ws_ptr<float>(p, p.L.pub) + off)) {
+        set_status(hd, kErrTimeout);
+        break;
+      }
+      publish(&flags_seg[s * Hv + h]);
+    }
+    for (int gc = first_chunk; gc < c0 && ok; ++gc) ok = chain_chunk<false, true>(p, cx, S, gc, h, hk, ctok[gc], clen[gc]);
+    for (int c = 0; c < nch && ok; ++c) {
+      const int gc = c0 + c;
+      ok = chain_chunk<true, true>(p, cx, S, gc, h, hk, ctok[gc], clen[gc]);
+    }
+    if (!ok) {
+      set_status(hd, kErrTimeout);
+      break;
+    }
+    if (last) {
+      save_state(cx, p.final_state + ((size_t)seq * Hv + h) * st_elems, S);
+      publish(&flags_fin[seq * Hv + h]);
+    }
+    __syncthreads();
+  }
+  // drain: make sure no MMA is in flight before releasing tensor memory
+  if (cx.tid == 0) {
+    umma_commit(&bar_mma);
+    mbar_wait(&bar_mma, cx.ph_mma, kWaitBudget);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (cx.warp == 0) tmem_dealloc(cx.tmem, 512);
+}
+
+// ========================================================================================= launch
+
+int launch_fwd(const FwdParams& p, cudaStream_t stream) {
+  static bool attr_done = false;
+  if (!attr_done) {
+    if (cudaFuncSetAttribute(kkt_solve_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)(sizeof(KktSmem) + 1024)) != cudaSuccess)
+      return kErrCuda;
+    if (cudaFuncSetAttribute(chain_kernel<kModeOut>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kChainSmemBytes) != cudaSuccess)
+      return kErrCuda;
+    if (cudaFuncSetAttribute(chain_kernel<kModeP1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kChainSmemBytes) != cudaSuccess)
+      return kErrCuda;
+    attr_done = true;
+  }
+  plan_kernel<<<1, 1024, 0, stream>>>(p);
+  if (p.d.T > 0) {
+    dim3 grid((unsigned)p.L.cmax, (unsigned)p.d.Hk);
+    kkt_solve_kernel<<<grid, 128, sizeof(KktSmem) + 1024, stream>>>(p);
+  }
+  const int64_t items_cap = (int64_t)p.d.num_sms;
+  if (p.d.mode == 0 && p.L.slots > 0 && p.d.T > 0) {
+    const int64_t units = (2 * p.L.slots + 1) * p.d.Hv;
+    const int grid = (int)(units < items_cap ? units : items_cap);
+    chain_kernel<kModeP1><<<grid, 256, kChainSmemBytes, stream>>>(p);
+  }
+  {
+    const int64_t items = p.L.smax * p.d.Hv;
+    const int grid = (int)(items < items_cap ? items : items_cap);
+    chain_kernel<kModeOut><<<grid, 256, kChainSmemBytes, stream>>>(p);
+  }
+  return cudaGetLastError() == cudaSuccess ? kOk : kErrCuda;
+}
+
+}  // namespace gdn

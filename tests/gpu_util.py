@@ -1,0 +1,79 @@
+"""Helpers for the GPU parity tests: move a synth.Problem to the device, run the
+library through its C ABI binding, and compare against the fp64 oracle with the
+stated tolerances (relative L2 <= 1e-2 and max-abs <= 2e-2 per output tensor)."""
+from __future__ import annotations
+
+import numpy as np
+
+import synth
+
+REL_L2 = 1e-2
+MAX_ABS = 2e-2
+
+
+def to_device(p: synth.Problem, device="cuda"):
+    import torch
+    bf = lambda a: torch.from_numpy(np.ascontiguousarray(a)).view(torch.bfloat16).to(device)
+    f32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(device)
+    d = dict(q=bf(p.q), k=bf(p.k), v=bf(p.v), g=f32(p.g), beta=f32(p.beta),
+             cu_seqlens=torch.from_numpy(p.cu_seqlens.astype(np.int32)).to(device))
+    d["init_idx"] = None if p.init_idx is None else torch.from_numpy(p.init_idx.astype(np.int32)).to(device)
+    d["initial_state"] = None if p.initial_state is None else f32(p.initial_state)
+    if p.dout is not None:
+        d["dout"] = bf(p.dout)
+    if p.dfinal is not None:
+        d["dfinal_state"] = f32(p.dfinal)
+    return d
+
+
+def bf16_to_f64(t):
+    import torch
+    return t.detach().to(torch.float32).cpu().numpy().astype(np.float64)
+
+
+def run_fwd(p: synth.Problem, options=None):
+    import linear_attention_varlen_gb300 as gdn
+    import torch
+    d = to_device(p)
+    ws = torch.empty(gdn.fwd_workspace_size(p.N, p.T, p.Hk, p.Hv, options), dtype=torch.uint8, device="cuda")
+    out, fin = gdn.chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"], d["init_idx"],
+                             d["initial_state"], options=options, workspace=ws)
+    st = gdn.workspace_status(ws)
+    assert st == 0, f"device status {gdn.status_string(st)}"
+    return bf16_to_f64(out), fin.double().cpu().numpy()
+
+
+def errors(got, ref):
+    diff = got - ref
+    n = np.linalg.norm(ref)
+    rel = np.linalg.norm(diff) / n if n > 0 else np.linalg.norm(diff)
+    return float(rel), float(np.abs(diff).max()) if diff.size else 0.0
+
+
+def assert_close(name, got, ref, rel_l2=REL_L2, max_abs=MAX_ABS):
+    assert got.shape == ref.shape, f"{name}: shape {got.shape} vs {ref.shape}"
+    assert np.all(np.isfinite(got)), f"{name}: non-finite values"
+    rel, mx = errors(got, ref)
+    assert rel <= rel_l2 and mx <= max_abs, f"{name}: rel-L2 {rel:.3e} (<= {rel_l2}), max-abs {mx:.3e} (<= {max_abs})"
+    return rel, mx
+
+
+def head_slice(p: synth.Problem, heads):
+    """The sub-problem of the given value heads (all in one GQA group) with its key head.
+    Value heads are independent given their key head, so the oracle can check a sample
+    of heads of a full-size workload one head at a time."""
+    G = p.Hv // p.Hk
+    hk = heads[0] // G
+    assert all(h // G == hk for h in heads)
+    q = synth.Problem(name=p.name + f"_h{heads}", q=p.q[:, hk:hk + 1], k=p.k[:, hk:hk + 1],
+                      v=p.v[:, heads], g=p.g[:, heads], beta=p.beta[:, heads], cu_seqlens=p.cu_seqlens,
+                      Hk=1, Hv=len(heads), Dk=p.Dk, Dv=p.Dv, init_idx=p.init_idx,
+                      initial_state=None if p.initial_state is None else p.initial_state[:, heads])
+    q.q = np.ascontiguousarray(q.q)
+    q.k = np.ascontiguousarray(q.k)
+    q.v = np.ascontiguousarray(q.v)
+    q.g = np.ascontiguousarray(q.g)
+    q.beta = np.ascontiguousarray(q.beta)
+    if q.initial_state is not None:
+        q.initial_state = np.ascontiguousarray(q.initial_state)
+    return q

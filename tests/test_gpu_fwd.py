@@ -1,0 +1,255 @@
+"""Forward parity on the GPU: the CUDA library (through its C ABI) against the fp64
+oracle on the same seeded inputs. Tolerances: relative L2 <= 1e-2 and max-abs <=
+2e-2 on out and final_state. Integer maps are checked bit-exact against the host
+planner."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from tests import chunked_ref as cr
+from tests.gpu_util import assert_close, errors, head_slice, run_fwd, to_device
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+import linear_attention_varlen_gb300 as gdn  # noqa: E402
+
+
+def check_problem(p, options=None, heads_note=""):
+    out, fin = run_fwd(p, options)
+    ro, rf = oracle.fwd_problem(p)
+    r1 = assert_close(f"{p.name} out{heads_note}", out, ro)
+    r2 = assert_close(f"{p.name} final_state{heads_note}", fin, rf)
+    return r1, r2
+
+
+# ----------------------------------------------------------------------------- small shapes, ragged tails
+
+
+@pytest.mark.parametrize("T", [1, 2, 63, 64, 65, 127, 130, 700])
+@pytest.mark.parametrize("Hk,Hv", [(1, 1), (2, 8), (1, 4)])
+def test_single_document_shapes(T, Hk, Hv):
+    p = synth.make_problem(f"one_T{T}", 11 + T, [T], Hk, Hv)
+    check_problem(p)
+
+
+def test_workload_single_T512_full():
+    check_problem(synth.workload_single())
+
+
+def test_packed_with_tiny_and_empty_documents():
+    lens = [1, 0, 64, 5, 129, 0, 63, 300, 2, 640]
+    p = synth.make_problem("ragged", 77, lens, 2, 4)
+    check_problem(p)
+
+
+def test_packed_lognormal_small():
+    p = synth.workload_packed(total=4096, n_docs=12, Hk=2, Hv=8)
+    check_problem(p)
+
+
+def test_pool_initial_states_and_forks():
+    lens = [70, 0, 130, 64, 9, 200]
+    init = [1, 0, 3, 0, 5, -1]  # n_init = 2: x >= 2 means fork from document x - 2
+    p = synth.make_problem("forks", 91, lens, 2, 4, init_idx=init, n_init=2)
+    check_problem(p)
+
+
+def test_chained_forks():
+    lens = [300, 128, 65, 40]
+    init = [-1, 0, 1, 2]
+    p = synth.make_problem("chain", 92, lens, 1, 2, init_idx=init)
+    check_problem(p)
+
+
+# ----------------------------------------------------------------------------- exact segment split
+
+
+@pytest.mark.parametrize("seg", [1, 2, 3, 5])
+@pytest.mark.parametrize("g_mean", [2.0, 6.0])
+def test_exact_split_forced_segments(seg, g_mean):
+    """Slow decay (g_mean = 6, about -0.0025 per token) makes the carried state matter."""
+    p = synth.make_problem(f"split_s{seg}_g{g_mean}", 120 + seg, [64 * 23 + 17], 2, 4, g_mean=g_mean)
+    check_problem(p, gdn.Options(segment_chunks=seg))
+
+
+def test_exact_split_with_initial_state_and_fork():
+    lens = [64 * 9 + 3, 64 * 7, 100]
+    p = synth.make_problem("split_fork", 131, lens, 1, 2, init_idx=[0, 1, 1], n_init=1, g_mean=5.0)
+    check_problem(p, gdn.Options(segment_chunks=2))
+
+
+def test_split_matches_unsplit_closely():
+    p = synth.make_problem("split_vs_unsplit", 140, [64 * 40], 2, 8, g_mean=5.0)
+    a_out, a_fin = run_fwd(p, gdn.Options(segment_chunks=-1))
+    b_out, b_fin = run_fwd(p, gdn.Options(segment_chunks=4))
+    assert errors(b_out, a_out)[0] < 5e-3
+    assert errors(b_fin, a_fin)[0] < 5e-3
+
+
+# ----------------------------------------------------------------------------- truncation mode
+
+
+def test_truncation_mode_against_chunked_truncation():
+    """Truncation mode matches the fp64 chunked truncation algebra (same windows), and its
+    distance from the exact result stays within the e^-10 bound plus bf16 rounding."""
+    L = 64 * 24
+    p = synth.make_problem("trunc", 150, [L], 1, 1, g_mean=3.0)
+    opts = gdn.Options(mode="truncate", segment_chunks=4)
+    out, fin = run_fwd(p, opts)
+    f = p.as_f64()
+    ot, st, nw = cr.doc_fwd_truncated(f["q"][:, 0], f["k"][:, 0], f["v"][:, 0], f["g"][:, 0], f["beta"][:, 0],
+                                      np.zeros((128, 128)), seg_chunks=4)
+    assert max(nw) >= 2
+    assert_close("trunc out", out[:, 0], ot)
+    assert_close("trunc final", fin[0, 0], st)
+    ro, rf = oracle.fwd_problem(p)
+    assert_close("trunc vs exact out", out, ro)
+
+
+def test_truncation_mode_long_workload_error_report(record_property):
+    p = synth.workload_long(T=8192)
+    ro, rf = oracle.fwd_problem(p)
+    out_e, fin_e = run_fwd(p)
+    out_t, fin_t = run_fwd(p, gdn.Options(mode="truncate"))
+    e_exact = errors(out_e, ro)
+    e_trunc = errors(out_t, ro)
+    record_property("exact_rel_l2", e_exact[0])
+    record_property("trunc_rel_l2", e_trunc[0])
+    assert_close("long exact", out_e, ro)
+    assert_close("long trunc", out_t, ro)
+    assert_close("long trunc final", fin_t, rf)
+
+
+# ----------------------------------------------------------------------------- packing properties
+
+
+def test_contamination_probe():
+    """Changing document A must not change document B's outputs (block-diagonal)."""
+    p = synth.make_problem("probe", 160, [300, 200], 2, 4)
+    a, _ = run_fwd(p)
+    p.v[:300] = synth.to_bf16_bits(-synth.bf16_bits_to_f32(p.v[:300]) * 3)
+    p.k[:300] = p.k[::-1][-300:]
+    b, _ = run_fwd(p)
+    np.testing.assert_array_equal(a[300:], b[300:])
+    assert np.abs(a[:300] - b[:300]).max() > 1e-3
+
+
+def test_packed_equals_separate_calls():
+    p = synth.make_problem("sep", 161, [130, 77, 256], 2, 4)
+    out, fin = run_fwd(p)
+    cu = p.cu_seqlens
+    for i in range(p.N):
+        sl = slice(cu[i], cu[i + 1])
+        q = synth.Problem(name="part", q=p.q[sl].copy(), k=p.k[sl].copy(), v=p.v[sl].copy(), g=p.g[sl].copy(),
+                          beta=p.beta[sl].copy(), cu_seqlens=np.array([0, cu[i + 1] - cu[i]], np.int32),
+                          Hk=p.Hk, Hv=p.Hv, Dk=128, Dv=128)
+        o1, f1 = run_fwd(q)
+        np.testing.assert_array_equal(out[sl], o1)
+        np.testing.assert_array_equal(fin[i], f1[0])
+
+
+def test_deterministic_across_runs():
+    p = synth.workload_long(T=4096)
+    a = run_fwd(p)
+    b = run_fwd(p)
+    np.testing.assert_array_equal(a[0], b[0])
+    np.testing.assert_array_equal(a[1], b[1])
+
+
+def test_device_maps_match_host_planner():
+    p = synth.make_problem("maps", 170, [1, 0, 64, 65, 700, 3000], 2, 8, init_idx=[-1, 0, -1, 2, 3, -1])
+    d = to_device(p)
+    opts = gdn.Options(segment_chunks=4)
+    ws = torch.zeros(gdn.fwd_workspace_size(p.N, p.T, p.Hk, p.Hv, opts), dtype=torch.uint8, device="cuda")
+    gdn.chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"], d["init_idx"], None, options=opts,
+                  workspace=ws)
+    assert gdn.workspace_status(ws) == 0
+    nsm = torch.cuda.get_device_properties(0).multi_processor_count
+    chunks, segs, L = gdn.plan_host(p.cu_seqlens, p.Hv, p.init_idx, 0, opts, num_sms=nsm)
+    hdr = ws[:256].view(torch.int32).cpu().numpy()
+    assert hdr[1] == len(chunks) and hdr[2] == len(segs) and hdr[3] == L
+    # offsets of the chunk and segment tables follow the documented layout: read via the
+    # same order the library allocates (header, seq_chunk0, seq_seg0, chunk tables, seg_info)
+    N = p.N
+    cmax = p.T // 64 + N + 1
+    off = lambda x: (x + 255) // 256 * 256
+    o = 256
+    o += off(4 * (N + 1))
+    o += off(4 * (N + 1))
+    w32 = ws.view(torch.int32)
+    cs = w32[o // 4:o // 4 + len(chunks)].cpu().numpy()
+    o += off(4 * cmax)
+    ct = w32[o // 4:o // 4 + len(chunks)].cpu().numpy()
+    o += off(4 * cmax)
+    cl = w32[o // 4:o // 4 + len(chunks)].cpu().numpy()
+    o += off(4 * cmax)
+    si = w32[o // 4:o // 4 + 4 * len(segs)].cpu().numpy().reshape(-1, 4)
+    np.testing.assert_array_equal(np.stack([cs, ct, cl], 1), chunks)
+    np.testing.assert_array_equal(si, segs)
+
+
+def test_invalid_cu_seqlens_reported_on_device():
+    p = synth.make_problem("bad", 180, [64, 64], 1, 1)
+    d = to_device(p)
+    d["cu_seqlens"] = torch.tensor([0, 100, 64 + 64], dtype=torch.int32, device="cuda")
+    d["cu_seqlens"][1] = 130  # > cu[2]
+    ws = torch.empty(gdn.fwd_workspace_size(p.N, p.T, p.Hk, p.Hv), dtype=torch.uint8, device="cuda")
+    gdn.chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"], None, None, workspace=ws)
+    assert gdn.workspace_status(ws) == gdn.GDN_ERR_INVALID_ARG
+
+
+# ----------------------------------------------------------------------------- full-size workloads
+
+
+def test_workload_packed_full():
+    check_problem(synth.workload_packed())
+
+
+def test_workload_long_full_exact():
+    check_problem(synth.workload_long())
+
+
+def test_workload_long_full_truncate():
+    check_problem(synth.workload_long(), gdn.Options(mode="truncate"))
+
+
+def test_workload_fork_full_sampled_heads():
+    """Full-size shared-prefix workload (64 value heads): all heads run on the GPU; the oracle
+    checks a sample of heads (heads are independent given their key head)."""
+    p = synth.workload_fork()
+    out, fin = run_fwd(p)
+    for heads in ([0], [37], [63]):
+        sub = head_slice(p, heads)
+        ro, rf = oracle.fwd_problem(sub)
+        assert_close(f"fork out heads {heads}", out[:, heads], ro)
+        assert_close(f"fork final heads {heads}", fin[:, heads], rf)
+
+
+def test_workload_fork_equals_prefix_then_branches():
+    """In-call fork == two calls (prefix, then branches starting from its final state)."""
+    p = synth.workload_fork(prefix=1024, n_branch=4, lo=256, hi=512, Hk=2, Hv=8)
+    out, fin = run_fwd(p)
+    cu = p.cu_seqlens
+    pre = slice(0, cu[1])
+    p0 = synth.Problem(name="pre", q=p.q[pre].copy(), k=p.k[pre].copy(), v=p.v[pre].copy(), g=p.g[pre].copy(),
+                       beta=p.beta[pre].copy(), cu_seqlens=np.array([0, cu[1]], np.int32), Hk=p.Hk, Hv=p.Hv,
+                       Dk=128, Dv=128)
+    o0, f0 = run_fwd(p0)
+    rest = slice(cu[1], cu[-1])
+    p1 = synth.Problem(name="br", q=p.q[rest].copy(), k=p.k[rest].copy(), v=p.v[rest].copy(), g=p.g[rest].copy(),
+                       beta=p.beta[rest].copy(), cu_seqlens=(cu[1:] - cu[1]).astype(np.int32), Hk=p.Hk, Hv=p.Hv,
+                       Dk=128, Dv=128, init_idx=np.zeros(p.N - 1, np.int32),
+                       initial_state=f0.astype(np.float32))
+    o1, f1 = run_fwd(p1)
+    np.testing.assert_array_equal(out[pre], o0)
+    np.testing.assert_allclose(out[rest], o1, atol=1e-6)
+    np.testing.assert_allclose(fin[1:], f1, atol=1e-6)
+
+
+def test_workload_train_forward_full():
+    check_problem(synth.workload_train())
