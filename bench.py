@@ -1,0 +1,379 @@
+"""Benchmark of the chunked Gated DeltaNet on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--mode exact|truncate]
+
+Workload: one 32768-token sequence, 8 value heads over 2 key heads, head dimension
+128, chunk 64 (the 32K prefill at a TP8-style per-GPU shape of "How to Speed Up GDN
+Kernels for Qwen Models", sections "The real enemy: an idle GPU" and "What it adds
+up to"); seeded synthetic inputs (synth.workload_long). A step is one pass of the
+library's forward (and backward, when the library provides it) over that batch.
+
+Prints ONE JSON line (rank 0). `value` is Mtokens/s over all ranks; `roofline`
+describes the dominant kernel (achieved algorithmic bytes / its CUDA-event time);
+`cpu_baseline` is the fp64 oracle timed on this host's cores; `e2e` is the same
+metric through the public API with host buffers and host<->device copies inside
+the timed region. N > 1 runs independent replicas (one per GPU, no collective on
+the data path) launched by torchrun.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "GDN fwd/bwd Mtokens/s at 32K x 8 heads; % of binding bf16-TC/HBM roofline"
+UNIT = "Mtokens/s"
+# Context only (another machine): FlashQLA forward, 32K prefill at TP8 on H200, 0.31 ms.
+PAGE_FWD_MTOK_S = 32768 / 0.31e-3 / 1e6
+# Algorithmic counts per token at H_v = 8, H_k = 2, d = 128 (inputs read once, outputs written once;
+# FLOPs of the chunked method with K K^T / Q K^T shared across a key-head group).
+D = 128
+
+
+def algorithmic_fwd(T, Hk, Hv, N):
+    bytes_ = T * (2 * Hk * D * 2 + Hv * D * 2 + 2 * Hv * 4 + Hv * D * 2) + N * Hv * D * D * 4
+    flops = T * (Hk * 4 * 64 * D + Hv * (6 * 64 * D + 6 * D * D))
+    return bytes_, flops
+
+
+def algorithmic_bwd(T, Hk, Hv, N):
+    # read q, k, v, g, beta, dO; write dq, dk, dv, dg, dbeta
+    bytes_ = T * (2 * Hk * D * 2 + Hv * D * 2 + 2 * Hv * 4 + Hv * D * 2 + 2 * Hk * D * 2 + Hv * D * 2 + 2 * Hv * 4)
+    flops = T * (Hk * 4 * 64 * D + Hv * (16 * D * D + 26 * 64 * D))
+    return bytes_, flops
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            pk = json.load(f)
+        return dict(hbm=float(pk["hbm_gbs"]), tc=float(pk["bf16_tflops"]), tc_sus=float(pk.get(
+            "bf16_tflops_sustained", pk["bf16_tflops"])), src="measured")
+    return dict(hbm=6800.0, tc=1900.0, tc_sus=1700.0, src="fallback")
+
+
+# ----------------------------------------------------------------------------- clocks
+
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "50"], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, ValueError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[4:8]):
+                if val.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return None
+        sm.sort()
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": max(mx), "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- reference arm (fp64 oracle)
+
+
+def run_reference(args, rank):
+    if rank != 0:
+        return None
+    import numpy as np
+
+    import oracle
+    import synth
+    oracle.build()
+    T_sample = 2048
+    p = synth.workload_long(T=T_sample)
+    f = p.as_f64()
+    cores = oracle.hw_threads()
+    for _ in range(args.warmup):
+        oracle.fwd(f["q"], f["k"], f["v"], f["g"], f["beta"], p.cu_seqlens, threads=cores)
+    ts = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.fwd(f["q"], f["k"], f["v"], f["g"], f["beta"], p.cu_seqlens, threads=cores)
+        ts.append(time.perf_counter() - t0)
+    sec = float(np.mean(ts))
+    value = T_sample / sec / 1e6
+    sample = f"first {T_sample} tokens of the 32768-token, 8-head workload per step (fp64 oracle forward)"
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "GDN fwd, single sequence, H_v=8, H_k=2, d=128 (oracle on host cores)",
+                   "T": T_sample, "H_v": 8, "H_k": 2},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def cpu_baseline():
+    """The fp64 oracle on the full workload, repeated until about 10 s of CPU work."""
+    import oracle
+    import synth
+    oracle.build()
+    p = synth.workload_long()
+    f = p.as_f64()
+    cores = oracle.hw_threads()
+    total, runs = 0.0, 0
+    while runs < 1 or (total < 10.0 and runs < 4):
+        t0 = time.perf_counter()
+        oracle.fwd(f["q"], f["k"], f["v"], f["g"], f["beta"], p.cu_seqlens, threads=cores)
+        total += time.perf_counter() - t0
+        runs += 1
+    return {"value": p.T * runs / total / 1e6, "unit": UNIT, "cores": cores,
+            "kind": "oracle", "sample": f"full 32768-token x 8-head forward, {runs} run(s), {total:.1f} s"}
+
+
+# ----------------------------------------------------------------------------- our arm
+
+
+def traffic_record(kernel_src):
+    """DRAM bytes per launch of the dominant kernel from a committed ncu summary, if it was
+    taken on the current source of that kernel (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    try:
+        rec = json.load(open(path))
+        sha = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()
+        if rec.get("source_sha256") == sha:
+            return rec
+    except (OSError, ValueError):
+        pass
+    return None
+
+
+def run_ours(args, rank, world, local_rank):
+    import numpy as np
+    import torch
+
+    import linear_attention_varlen_gb300 as gdn
+    import synth
+    from linear_attention_varlen_gb300 import build as gdn_build
+    from tests.gpu_util import to_device
+
+    gdn_build.build()
+    gdn.load()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    p = synth.workload_long()
+    d = to_device(p, dev)
+    T, Hk, Hv, N = p.T, p.Hk, p.Hv, p.N
+    stream = torch.cuda.current_stream()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * gdn.NUM_STAGES)]
+    for e in ev:
+        e.record(stream)
+    opts = gdn.Options(mode=args.mode)
+    opts_ev = gdn.Options(mode=args.mode, stage_events=ev)
+    ws = torch.empty(max(gdn.fwd_workspace_size(N, T, Hk, Hv, opts), gdn.bwd_workspace_size(N, T, Hk, Hv, opts)),
+                     dtype=torch.uint8, device=dev)
+    out = torch.empty((T, Hv, D), dtype=torch.bfloat16, device=dev)
+    fin = torch.empty((N, Hv, D, D), dtype=torch.float32, device=dev)
+    dout = torch.randn((T, Hv, D), device=dev).to(torch.bfloat16)
+
+    def fwd(o):
+        gdn.chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"], None, None, options=o, out=out,
+                      final_state=fin, workspace=ws)
+
+    has_bwd = True
+    try:
+        gdn.chunk_bwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"], dout, options=opts, workspace=ws)
+    except gdn.GdnError as e:
+        if e.status != gdn.GDN_ERR_UNSUPPORTED:
+            raise
+        has_bwd = False
+
+    def step(o):
+        fwd(o)
+        if has_bwd:
+            gdn.chunk_bwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"], dout, options=o, workspace=ws)
+
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)  # > 129 MB L2
+    for _ in range(args.warmup):
+        step(opts)
+    torch.cuda.synchronize()
+    st = gdn.workspace_status(ws)
+    if st != gdn.GDN_OK:
+        raise RuntimeError(f"device status after warm-up: {gdn.status_string(st)}")
+    n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
+    split_launched = args.mode == "exact" and N * Hv < 2 * n_sm  # pass 1 of the exact split runs
+
+    clocks = ClockSampler(local_rank) if rank == 0 else None
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    if clocks:
+        clocks.start()
+        time.sleep(0.3)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    stops = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    stage_ms = np.zeros((args.steps, gdn.NUM_STAGES))
+    for i in range(args.steps):
+        flush.zero_()
+        starts[i].record(stream)
+        step(opts_ev)
+        stops[i].record(stream)
+        stops[i].synchronize()
+        for s in range(gdn.NUM_STAGES):
+            stage_ms[i, s] = ev[2 * s].elapsed_time(ev[2 * s + 1])
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop() if clocks else None
+    step_ms = np.array([a.elapsed_time(b) for a, b in zip(starts, stops)])
+    ms = float(step_ms.mean())
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    value = T * world / (ms * 1e-3) / 1e6
+
+    # e2e: the same step through the public API from pinned host buffers, copies inside
+    host = {k: v.detach().cpu().pin_memory() for k, v in d.items() if v is not None}
+    out_h = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    fin_h = torch.empty(fin.shape, dtype=fin.dtype, pin_memory=True)
+    dev_in = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = out.numel() * out.element_size() + fin.numel() * fin.element_size()
+    e2e_steps = max(3, min(args.steps, 50))
+    torch.cuda.synchronize()
+    ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ea.record(stream)
+    for _ in range(e2e_steps):
+        for k2, v2 in host.items():
+            dev_in[k2].copy_(v2, non_blocking=True)
+        gdn.chunk_fwd(dev_in["q"], dev_in["k"], dev_in["v"], dev_in["g"], dev_in["beta"], dev_in["cu_seqlens"], None,
+                      None, options=opts, out=out, final_state=fin, workspace=ws)
+        out_h.copy_(out, non_blocking=True)
+        fin_h.copy_(fin, non_blocking=True)
+    eb.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = ea.elapsed_time(eb) / e2e_steps
+    e2e_value = T * world / (e2e_ms * 1e-3) / 1e6
+
+    if rank != 0:
+        return None
+    peaks = load_peaks()
+    names = {gdn.STAGE_PLAN: "plan_kernel", gdn.STAGE_KKT_SOLVE: "kkt_solve_kernel",
+             gdn.STAGE_SPLIT: "chain_kernel<pass1>", gdn.STAGE_CHAIN: "chain_kernel<out>"}
+    avg = stage_ms.mean(axis=0)
+    dom = int(np.argmax(avg[:4]))
+    fb, ff = algorithmic_fwd(T, Hk, Hv, N)
+    # The chain kernel reads q, k, v and writes o and the final state: the forward's algorithmic bytes.
+    hbm_t = fb / (peaks["hbm"] * 1e9)
+    tc_t = ff / (peaks["tc_sus"] * 1e12)
+    bound = "hbm" if hbm_t >= tc_t else "tensor"
+    kern_s = avg[dom] * 1e-3
+    if bound == "hbm":
+        achieved, peak, unit_r = fb / kern_s / 1e9, peaks["hbm"], "GB/s"
+    else:
+        achieved, peak, unit_r = ff / kern_s / 1e12, peaks["tc_sus"], "TFLOP/s"
+    tr = traffic_record(os.path.join(ROOT, "linear_attention_varlen_gb300", "csrc", "gdn_fwd.cu"))
+    launches_per_step = 3 + (1 if split_launched else 0)
+    fwd_ms = float(avg[:4].sum())
+    res = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": value / PAGE_FWD_MTOK_S if not has_bwd else None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "GDN " + ("fwd+bwd" if has_bwd else "fwd") + ", one 32768-token sequence, H_v=8, "
+                   "H_k=2, d_k=d_v=128, chunk 64, " + args.mode + " mode", "T": T, "H_v": Hv, "H_k": Hk,
+                   "mode": args.mode, "pass": "fwd+bwd" if has_bwd else "fwd",
+                   "l2": "flushed between timed steps (512 MiB write outside the timed events)"},
+        "roofline": {"bound": bound, "kernel": names[dom], "achieved": achieved, "peak": peak, "unit": unit_r,
+                     "frac": achieved / peak, "traffic": (tr["bytes_per_launch"] if tr else None),
+                     "peak_source": peaks["src"] + (" hbm_gbs" if bound == "hbm" else " bf16_tflops_sustained"),
+                     "algorithmic_bytes": fb, "algorithmic_flops": ff},
+        "step_roofline": {"bound": bound, "frac": (max(hbm_t, tc_t) / (fwd_ms * 1e-3)),
+                          "note": "forward algorithmic time at measured peaks / whole forward time"},
+        "stages_ms": {names[s]: float(avg[s]) for s in range(4)},
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
+        "gpu_launches": int(launches_per_step * args.steps),
+        "clocks": clk,
+    }
+    if not has_bwd:
+        res["vs_baseline_note"] = "value / FlashQLA forward on H200 (0.31 ms for 32K at TP8), context only"
+    if world == 1 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline()
+    return res
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--mode", choices=["exact", "truncate"], default="exact")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        res = run_reference(args, rank)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+        return
+    if world > 1:
+        import torch
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl")
+    res = run_ours(args, rank, world, local_rank)
+    if res is not None:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

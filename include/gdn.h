@@ -74,9 +74,21 @@ typedef struct gdn_options {
   int32_t segment_chunks;    /* segment length in 64-token chunks; 0 = automatic, < 0 = never split */
   float scale;               /* multiplies q (1.0: inputs already scaled) */
   int32_t reserved;          /* must be 0 */
+  void* stage_events;        /* optional profiling hook: NULL, or a cudaEvent_t[2 * GDN_NUM_STAGES] array;
+                                events 2s and 2s+1 are recorded on `stream` right before and right after
+                                stage s (both at the same point when the stage has nothing to launch) */
 } gdn_options;
 
-/* Fill `opt` with the defaults: exact mode, threshold -10, automatic segments, scale 1. */
+/* Stages of one forward call, in launch order (indices into gdn_options.stage_events). */
+enum gdn_fwd_stage {
+  GDN_STAGE_PLAN = 0,      /* chunk / segment maps */
+  GDN_STAGE_KKT_SOLVE = 1, /* intra-chunk K K^T, triangular solve, WY factors */
+  GDN_STAGE_SPLIT = 2,     /* exact split, pass 1: segment transitions and local end states */
+  GDN_STAGE_CHAIN = 3,     /* state chain fused with the output */
+  GDN_NUM_STAGES = 8       /* room for the backward stages */
+};
+
+/* Fill `opt` with the defaults: exact mode, threshold -10, automatic segments, scale 1, no events. */
 void gdn_default_options(gdn_options* opt);
 
 /* Workspace bytes gdn_chunk_fwd needs for these sizes (opt may be NULL for defaults).

@@ -38,7 +38,12 @@ class GdnError(RuntimeError):
 
 class COptions(ctypes.Structure):
     _fields_ = [("mode", ctypes.c_int32), ("trunc_log_threshold", ctypes.c_float),
-                ("segment_chunks", ctypes.c_int32), ("scale", ctypes.c_float), ("reserved", ctypes.c_int32)]
+                ("segment_chunks", ctypes.c_int32), ("scale", ctypes.c_float), ("reserved", ctypes.c_int32),
+                ("stage_events", ctypes.c_void_p)]
+
+
+NUM_STAGES = 8
+STAGE_PLAN, STAGE_KKT_SOLVE, STAGE_SPLIT, STAGE_CHAIN = 0, 1, 2, 3
 
 
 @dataclass
@@ -48,10 +53,18 @@ class Options:
     trunc_log_threshold: float = -10.0
     segment_chunks: int = 0
     scale: float = 1.0
+    stage_events: Optional[object] = None  # optional list of 2 * NUM_STAGES timing torch.cuda.Event
 
     def c(self) -> COptions:
         m = {"exact": MODE_EXACT, "truncate": MODE_TRUNCATE}[self.mode]
-        return COptions(m, float(self.trunc_log_threshold), int(self.segment_chunks), float(self.scale), 0)
+        ev = None
+        if self.stage_events is not None:
+            handles = [int(e.cuda_event) for e in self.stage_events]
+            if len(handles) != 2 * NUM_STAGES or not all(handles):
+                raise ValueError("stage_events: 2 * NUM_STAGES recorded timing events are required")
+            self._ev_array = (ctypes.c_void_p * len(handles))(*handles)
+            ev = ctypes.cast(self._ev_array, ctypes.c_void_p)
+        return COptions(m, float(self.trunc_log_threshold), int(self.segment_chunks), float(self.scale), 0, ev)
 
 
 _lock = threading.Lock()

@@ -87,6 +87,7 @@ void gdn_default_options(gdn_options* opt) {
   opt->segment_chunks = 0;
   opt->scale = 1.0f;
   opt->reserved = 0;
+  opt->stage_events = nullptr;
 }
 
 const char* gdn_status_string(int status) {
@@ -172,7 +173,7 @@ int gdn_chunk_fwd(const void* q, const void* k, const void* v, const float* g, c
   p.ws = reinterpret_cast<uint8_t*>(workspace);
   p.trunc_thr = o.trunc_log_threshold;
   p.scale = o.scale;
-  return launch_fwd(p, (cudaStream_t)stream);
+  return launch_fwd(p, (cudaStream_t)stream, reinterpret_cast<cudaEvent_t*>(o.stage_events));
 }
 
 int gdn_chunk_bwd(const void* q, const void* k, const void* v, const float* g, const float* beta,
@@ -219,7 +220,7 @@ int gdn_chunk_bwd(const void* q, const void* k, const void* v, const float* g, c
   a.d = make_dims(N, T, H_k, H_v, n_init, o, current_sm_count());
   a.trunc_thr = o.trunc_log_threshold;
   a.scale = o.scale;
-  return launch_bwd(a, (cudaStream_t)stream);
+  return launch_bwd(a, (cudaStream_t)stream, reinterpret_cast<cudaEvent_t*>(o.stage_events));
 }
 
 int gdn_plan_host(const int32_t* cu, int N, int T, int H_v, const int32_t* init_idx, int n_init,

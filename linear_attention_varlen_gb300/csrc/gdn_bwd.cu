@@ -3,9 +3,10 @@
 
 namespace gdn {
 
-int launch_bwd(const BwdArgs& a, cudaStream_t stream) {
+int launch_bwd(const BwdArgs& a, cudaStream_t stream, cudaEvent_t* events) {
   (void)a;
   (void)stream;
+  (void)events;
   return kErrUnsupported;
 }
 

@@ -31,6 +31,6 @@ inline BwdLayout bwd_layout(const PlanDims& d) {
   return L;
 }
 
-int launch_bwd(const BwdArgs& a, cudaStream_t stream);
+int launch_bwd(const BwdArgs& a, cudaStream_t stream, cudaEvent_t* events);
 
 }  // namespace gdn

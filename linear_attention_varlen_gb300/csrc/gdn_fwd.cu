@@ -883,7 +883,7 @@ __global__ void __launch_bounds__(256, 1) chain_kernel(const __grid_constant__ F
 
 // ========================================================================================= launch
 
-int launch_fwd(const FwdParams& p, cudaStream_t stream) {
+int launch_fwd(const FwdParams& p, cudaStream_t stream, cudaEvent_t* ev) {
   static bool attr_done = false;
   if (!attr_done) {
     if (cudaFuncSetAttribute(kkt_solve_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -897,22 +897,33 @@ int launch_fwd(const FwdParams& p, cudaStream_t stream) {
       return kErrCuda;
     attr_done = true;
   }
+  auto mark = [&](int i) {
+    if (ev) cudaEventRecord(ev[i], stream);
+  };
+  mark(0);
   plan_kernel<<<1, 1024, 0, stream>>>(p);
+  mark(1);
+  mark(2);
   if (p.d.T > 0) {
     dim3 grid((unsigned)p.L.cmax, (unsigned)p.d.Hk);
     kkt_solve_kernel<<<grid, 128, sizeof(KktSmem) + 1024, stream>>>(p);
   }
+  mark(3);
   const int64_t items_cap = (int64_t)p.d.num_sms;
+  mark(4);
   if (p.d.mode == 0 && p.L.slots > 0 && p.d.T > 0) {
     const int64_t units = (2 * p.L.slots + 1) * p.d.Hv;
     const int grid = (int)(units < items_cap ? units : items_cap);
     chain_kernel<kModeP1><<<grid, 256, kChainSmemBytes, stream>>>(p);
   }
+  mark(5);
+  mark(6);
   {
     const int64_t items = p.L.smax * p.d.Hv;
     const int grid = (int)(items < items_cap ? items : items_cap);
     chain_kernel<kModeOut><<<grid, 256, kChainSmemBytes, stream>>>(p);
   }
+  mark(7);
   return cudaGetLastError() == cudaSuccess ? kOk : kErrCuda;
 }
 

@@ -26,6 +26,7 @@ struct FwdParams {
   float scale;
 };
 
-int launch_fwd(const FwdParams& p, cudaStream_t stream);
+// events: NULL or cudaEvent_t[2 * 8], recorded around each stage (see gdn_fwd_stage).
+int launch_fwd(const FwdParams& p, cudaStream_t stream, cudaEvent_t* events);
 
 }  // namespace gdn

@@ -45,6 +45,7 @@ def test_default_options(lib):
     o = gdn.COptions()
     lib.gdn_default_options(ctypes.byref(o))
     assert (o.mode, o.trunc_log_threshold, o.segment_chunks, o.scale, o.reserved) == (0, -10.0, 0, 1.0, 0)
+    assert o.stage_events is None
 
 
 def test_workspace_size_queries(lib):
@@ -60,7 +61,7 @@ def _fwd_raw(lib, **kw):
     args = dict(q=1 << 20, k=1 << 20, v=1 << 20, g=1 << 20, beta=1 << 20, cu=1 << 20, N=1, T=64, Hk=1, Hv=1, D=128,
                 init=None, h0=None, n_init=0, out=1 << 20, fin=1 << 20, ws=1 << 20, ws_bytes=1 << 30)
     args.update(kw)
-    o = gdn.COptions(0, -10.0, 0, 1.0, 0)
+    o = gdn.COptions(0, -10.0, 0, 1.0, 0, None)
     P = ctypes.c_void_p
     return lib.gdn_chunk_fwd(P(args["q"]), P(args["k"]), P(args["v"]), P(args["g"]), P(args["beta"]), P(args["cu"]),
                              args["N"], args["T"], args["Hk"], args["Hv"], args["D"], P(args["init"]), P(args["h0"]),
