@@ -28,7 +28,9 @@
  *                  n_init + j   : the final state of document j < i of this same call
  *      initial_state : fp32 [n_init, H_v, 128, 128] or NULL when n_init == 0
  *      final_state   : fp32 [N, H_v, 128, 128]  (layout [d_k][d_v] per head)
- *    q, k, v, out and every gradient of them must be 16-byte aligned.
+ *    q, k, v, out and every gradient of them must be 16-byte aligned. Gradients are fp32:
+ *    dq reaches magnitudes where one bf16 rounding step exceeds the accuracy the library
+ *    keeps for it, so the caller decides when to round.
  *  - Ownership: the caller owns all memory, including the workspace. The library
  *    never allocates, frees or synchronises; every kernel is enqueued on `stream`.
  *    Inputs are read-only; outputs are overwritten in full.
@@ -79,13 +81,17 @@ typedef struct gdn_options {
                                 stage s (both at the same point when the stage has nothing to launch) */
 } gdn_options;
 
-/* Stages of one forward call, in launch order (indices into gdn_options.stage_events). */
+/* Stages of a call, in launch order (indices into gdn_options.stage_events). A backward call
+ * runs stages 0-3 (the forward recompute) and then 4-6. */
 enum gdn_fwd_stage {
   GDN_STAGE_PLAN = 0,      /* chunk / segment maps */
   GDN_STAGE_KKT_SOLVE = 1, /* intra-chunk K K^T, triangular solve, WY factors */
   GDN_STAGE_SPLIT = 2,     /* exact split, pass 1: segment transitions and local end states */
-  GDN_STAGE_CHAIN = 3,     /* state chain fused with the output */
-  GDN_NUM_STAGES = 8       /* room for the backward stages */
+  GDN_STAGE_CHAIN = 3,     /* state chain fused with the output (records states in the backward) */
+  GDN_STAGE_REV_CHAIN = 4, /* backward: reverse state-gradient chain */
+  GDN_STAGE_GRADS = 5,     /* backward: per-chunk dq, dk, dv, dg, dbeta */
+  GDN_STAGE_DINIT = 6,     /* backward: d(initial_state) sums over documents sharing a pool entry */
+  GDN_NUM_STAGES = 8
 };
 
 /* Fill `opt` with the defaults: exact mode, threshold -10, automatic segments, scale 1, no events. */
@@ -114,8 +120,8 @@ int gdn_chunk_fwd(const void* q, const void* k, const void* v, const float* g, c
 /*
  * Backward of gdn_chunk_fwd for the loss sum(dout * out) + sum(dfinal_state * final_state).
  * dout: bf16 [T, H_v, 128]; dfinal_state: fp32 [N, H_v, 128, 128] or NULL (zero).
- * Outputs: dq, dk bf16 [T, H_k, 128] (summed over the value heads of each key head);
- * dv bf16 [T, H_v, 128]; dg, dbeta fp32 [T, H_v]; dinitial_state fp32 [n_init, H_v, 128, 128]
+ * Outputs, all fp32: dq, dk [T, H_k, 128] (summed over the value heads of each key head);
+ * dv [T, H_v, 128]; dg, dbeta [T, H_v]; dinitial_state [n_init, H_v, 128, 128]
  * (summed over every document that starts from the same pool entry; NULL allowed when n_init == 0).
  * A document forked from document j of the same call sends its gradient back into j
  * ("Musings on long-context fine-tuning", section "Backward through P").
@@ -123,7 +129,7 @@ int gdn_chunk_fwd(const void* q, const void* k, const void* v, const float* g, c
 int gdn_chunk_bwd(const void* q, const void* k, const void* v, const float* g, const float* beta,
                   const int32_t* cu_seqlens, int N, int T, int H_k, int H_v, int head_dim,
                   const int32_t* init_idx, const float* initial_state, int n_init, const void* dout,
-                  const float* dfinal_state, void* dq, void* dk, void* dv, float* dg, float* dbeta,
+                  const float* dfinal_state, float* dq, float* dk, float* dv, float* dg, float* dbeta,
                   float* dinitial_state, void* workspace, size_t ws_bytes, const gdn_options* opt,
                   gdn_stream_t stream);
 

@@ -43,7 +43,7 @@ class COptions(ctypes.Structure):
 
 
 NUM_STAGES = 8
-STAGE_PLAN, STAGE_KKT_SOLVE, STAGE_SPLIT, STAGE_CHAIN = 0, 1, 2, 3
+STAGE_PLAN, STAGE_KKT_SOLVE, STAGE_SPLIT, STAGE_CHAIN, STAGE_REV_CHAIN, STAGE_GRADS, STAGE_DINIT = range(7)
 
 
 @dataclass
@@ -223,7 +223,7 @@ def chunk_fwd(q, k, v, g, beta, cu_seqlens, init_idx=None, initial_state=None, o
 
 def chunk_bwd(q, k, v, g, beta, cu_seqlens, dout, dfinal_state=None, init_idx=None, initial_state=None,
               options: Optional[Options] = None, workspace=None, stream=None):
-    """Backward. Returns dict dq, dk, dv (bf16), dg, dbeta (fp32), dinit (fp32 or None)."""
+    """Backward. Returns dict of fp32 gradients dq, dk, dv, dg, dbeta and dinit (None without a pool)."""
     torch = _torch()
     T, Hk, D = q.shape
     Hv = v.shape[1]
@@ -233,9 +233,9 @@ def chunk_bwd(q, k, v, g, beta, cu_seqlens, dout, dfinal_state=None, init_idx=No
         _check(dfinal_state, "dfinal_state", torch.float32, (N, Hv, D, D))
     n_init = 0 if initial_state is None else initial_state.shape[0]
     dev = q.device
-    dq = torch.empty_like(q)
-    dk = torch.empty_like(k)
-    dv = torch.empty_like(v)
+    dq = torch.empty(q.shape, dtype=torch.float32, device=dev)
+    dk = torch.empty(k.shape, dtype=torch.float32, device=dev)
+    dv = torch.empty(v.shape, dtype=torch.float32, device=dev)
     dg = torch.empty((T, Hv), dtype=torch.float32, device=dev)
     db = torch.empty((T, Hv), dtype=torch.float32, device=dev)
     dinit = torch.empty_like(initial_state) if n_init > 0 else None

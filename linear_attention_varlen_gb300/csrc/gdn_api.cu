@@ -179,7 +179,7 @@ int gdn_chunk_fwd(const void* q, const void* k, const void* v, const float* g, c
 int gdn_chunk_bwd(const void* q, const void* k, const void* v, const float* g, const float* beta,
                   const int32_t* cu_seqlens, int N, int T, int H_k, int H_v, int head_dim,
                   const int32_t* init_idx, const float* initial_state, int n_init, const void* dout,
-                  const float* dfinal_state, void* dq, void* dk, void* dv, float* dg, float* dbeta,
+                  const float* dfinal_state, float* dq, float* dk, float* dv, float* dg, float* dbeta,
                   float* dinitial_state, void* workspace, size_t ws_bytes, const gdn_options* opt,
                   gdn_stream_t stream) {
   if (head_dim != kDim) return GDN_ERR_UNSUPPORTED;

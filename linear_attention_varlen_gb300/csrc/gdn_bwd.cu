@@ -1,13 +1,1048 @@
-// Backward kernels of the chunked Gated DeltaNet.
+// Backward of the chunked Gated DeltaNet (sm_103a).
+//
+// The backward recomputes the forward chunk states instead of keeping them from the forward
+// call ("How to Speed Up GDN Kernels for Qwen Models", section "Lever 2": the backward pass
+// recomputes hidden states in one dedicated pass), then runs the state-gradient chain in
+// reverse and the per-chunk gradients in parallel:
+//
+//   1. forward recompute (plan, kkt_solve, chain in record mode): for every chunk c and value
+//      head, S_c (state at the chunk start, bf16), V'_c = U - W S_c (bf16) and T_c (fp32).
+//   2. rev_chain_kernel, per (document, value head), chunks in reverse:
+//        dV' = K~ dS_{c+1} + P^T dO,    dS_c = e^{gamma_C} dS_{c+1} + Q~^T dO - W^T dV'
+//      (K~ = diag(e^{gamma_C - gamma}) K, Q~ = diag(e^{gamma}) Q, P = (Q K^T) o E); records
+//      dS_{c+1} and dV' per chunk, and dL/dS at the document start. A document whose final
+//      state was forked first collects the d(initial state) of every document that started from
+//      it ("Musings on long-context fine-tuning", section "Backward through P": the gradients of
+//      the branches add up at the shared state).
+//   3. grad_kernel, per (chunk, key head), looping over the value heads of the group: dk
+//      (summed over the group in tensor memory), dv, dbeta and dg from S_c, dS_{c+1}, V', dV'
+//      and T, through the reverse mode of the chunk algebra (T = (I + A)^{-1}, W = T diag(beta
+//      e^gamma) K, U = T diag(beta) V, O = Q~ S + P V', S_{c+1} = e^{gamma_C} S + K~^T V').
+//      dq_kernel computes dq the same way with compensated bf16 operands (see there).
+//   4. dinit_reduce_kernel: d(initial_state) of each pool entry = the sum, in document order,
+//      over the documents that start from it.
+//
+// Precision: the recompute keeps T diag(beta e^gamma), T diag(beta) and diag(e^{gamma_C-gamma}) V'
+// as compensated bf16 pairs (x = hi + lo, two MMAs), so that the recorded states and V' carry
+// fp32-level accuracy into the gradients; all gradients are written in fp32.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstring>
+
+#include "bw_prims.cuh"
 #include "gdn_bwd.h"
+#include "gdn_common.cuh"
+#include "gdn_dev.cuh"
+#include "gdn_fwd.h"
+#include "tmap.h"
 
 namespace gdn {
+using namespace bw;
 
-int launch_bwd(const BwdArgs& a, cudaStream_t stream, cudaEvent_t* events) {
-  (void)a;
-  (void)stream;
-  (void)events;
-  return kErrUnsupported;
+struct BwdParams {
+  CUtensorMap tm_q, tm_k, tm_v, tm_do;
+  const float* g;
+  const float* beta;
+  const int32_t* cu;
+  const int32_t* init_idx;
+  const float* dfinal;
+  float* dq;
+  float* dk;
+  float* dv;
+  float* dg;
+  float* dbeta;
+  float* dinit;
+  uint8_t* ws;
+  PlanDims d;
+  BwdLayout L;
+  float scale;
+};
+
+__device__ __forceinline__ uint4 pack8(const float* x) {
+  return make_uint4(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]), pack_bf16x2(x[4], x[5]),
+                    pack_bf16x2(x[6], x[7]));
+}
+__device__ __forceinline__ float bf16_at(const uint8_t* blk, int row, int col) {
+  return __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(blk + sw128_off(row, col)));
+}
+// Scale row r of a [64 x 64] bf16 SW128 block (8 KB) in place; 256 threads, one 16-byte piece each pass.
+__device__ __forceinline__ void scale_rows(uint8_t* blk, const float* rs, int tid) {
+  for (int o = tid * 16; o < 8192; o += 256 * 16) {
+    const float sc = rs[o >> 7];
+    uint4 raw = *reinterpret_cast<uint4*>(blk + o);
+    __nv_bfloat162* x = reinterpret_cast<__nv_bfloat162*>(&raw);
+    uint32_t w[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      float2 f = __bfloat1622float2(x[u]);
+      w[u] = pack_bf16x2(f.x * sc, f.y * sc);
+    }
+    *reinterpret_cast<uint4*>(blk + o) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+struct Ctx {
+  uint64_t* bar_ld;
+  uint64_t* bar_mma;
+  uint32_t tmem, ph_ld, ph_mma;
+  int tid, warp, lane, q4, half;
+  __device__ bool wait_ld() {
+    if (!wait_all(bar_ld, ph_ld)) return false;
+    ph_ld ^= 1;
+    tc_fence_after();
+    return true;
+  }
+  __device__ bool commit_wait() {
+    if (tid == 0) umma_commit(bar_mma);
+    if (!wait_all(bar_mma, ph_mma)) return false;
+    ph_mma ^= 1;
+    tc_fence_after();
+    return true;
+  }
+  __device__ uint32_t lane_base() const { return (uint32_t)(32 * q4) << 16; }
+};
+
+__device__ __forceinline__ void ctx_init(Ctx& c, uint64_t* bl, uint64_t* bm) {
+  c.bar_ld = bl;
+  c.bar_mma = bm;
+  c.tid = threadIdx.x;
+  c.warp = c.tid >> 5;
+  c.lane = c.tid & 31;
+  c.q4 = c.warp & 3;
+  c.half = c.warp >> 2;
+  c.ph_ld = 0;
+  c.ph_mma = 0;
+}
+
+// ===================================================================================== reverse chain
+
+struct RevSmem {
+  uint8_t q[2][8192];     // Q tile (A K-major: Q K^T)
+  uint8_t k[2][8192];     // K tile (B K-major: Q K^T; B MN-major: T_w K)
+  uint8_t qt[2][8192];    // Q~ = scale diag(e^gamma) Q, rows >= n zero (A MN-major: Q~^T dO)
+  uint8_t kt[2][8192];    // K~ = diag(e^{gamma_C - gamma}) K            (A K-major: K~ dS)
+  uint8_t wn[2][8192];    // -W rows t                                    (A MN-major: -W^T dV')
+  uint8_t p[8192];        // P = scale (Q K^T) o E                        (A MN-major: P^T dO)
+  uint8_t tw[8192];       // T diag(beta e^gamma)                         (A K-major: W = T_w K)
+  uint8_t dout[2][8192];  // dO rows t, dv blocks                         (B MN-major)
+  uint8_t dvp[2][8192];   // dV' rows t, dv blocks                        (B MN-major)
+  uint8_t ds[2][16384];   // dS bf16 rows dk, dv blocks                   (B MN-major)
+  float gam[64];
+};
+constexpr size_t kRevSmemBytes = sizeof(RevSmem) + 1024;
+constexpr uint32_t kRtW = 0, kRtG = 128, kRtA = 256, kRtC = 384;
+
+__device__ __forceinline__ void rev_store_ds(const Ctx& cx, RevSmem& sm, const float* dS) {
+  const int r = 32 * cx.q4 + cx.lane;
+  uint8_t* blk = sm.ds[cx.half];
+#pragma unroll
+  for (int cj = 0; cj < 8; ++cj) *reinterpret_cast<uint4*>(blk + r * 128 + ((cj ^ (r & 7)) << 4)) = pack8(dS + 8 * cj);
+}
+
+__device__ bool rev_chunk(const BwdParams& p, Ctx& cx, RevSmem& sm, float* dS, int gc, int h, int hk, int tok0,
+                          int n) {
+  const int Hv = p.d.Hv;
+  // record dL/dS at this chunk's end
+  copy_smem_to_global(p.ws + p.L.ds_img + ((size_t)gc * Hv + h) * 32768, sm.ds[0], 32768, cx.tid);
+  if (cx.tid == 0) {
+    mbar_arrive_expect_tx(cx.bar_ld, 6 * 8192 + 8192 + 256);
+    tma_load_3d(sm.k[0], &p.tm_k, 0, hk, tok0, cx.bar_ld);
+    tma_load_3d(sm.k[1], &p.tm_k, 64, hk, tok0, cx.bar_ld);
+    tma_load_3d(sm.q[0], &p.tm_q, 0, hk, tok0, cx.bar_ld);
+    tma_load_3d(sm.q[1], &p.tm_q, 64, hk, tok0, cx.bar_ld);
+    tma_load_3d(sm.dout[0], &p.tm_do, 0, h, tok0, cx.bar_ld);
+    tma_load_3d(sm.dout[1], &p.tm_do, 64, h, tok0, cx.bar_ld);
+    bulk_load(sm.tw, p.ws + p.L.f.tw + ((size_t)gc * Hv + h) * 8192, 8192, cx.bar_ld);
+    bulk_load(sm.gam, p.ws + p.L.f.gam + ((size_t)gc * Hv + h) * 256, 256, cx.bar_ld);
+  }
+  if (!cx.wait_ld()) return false;
+  if (cx.tid == 0) {
+    for (int ks = 0; ks < 4; ++ks)
+      umma_bf16(cx.tmem + kRtW, kmajor_desc(smem_u32(sm.tw), 8192, ks), mnmajor_desc(smem_u32(sm.k[0]), 8192, ks),
+                idesc_bf16(64, 128, 0, 1), ks > 0);
+    for (int ks = 0; ks < 8; ++ks)
+      umma_bf16(cx.tmem + kRtG, kmajor_desc(smem_u32(sm.q[0]), 8192, ks), kmajor_desc(smem_u32(sm.k[0]), 8192, ks),
+                idesc_bf16(64, 64, 0, 0), ks > 0);
+  }
+  const float gC = sm.gam[63];
+  // Q~ and K~ (rows >= n of Q~ are zeroed: they belong to the next document)
+  for (int e = cx.tid; e < 2 * 2 * 64 * 8; e += 256) {
+    const int which = e >> 10, b = (e >> 9) & 1, r = (e >> 3) & 63, cj = e & 7;
+    const uint32_t off = r * 128 + ((cj ^ (r & 7)) << 4);
+    const float sc = which == 0 ? ((r < n) ? __expf(sm.gam[r]) * p.scale : 0.f) : __expf(gC - sm.gam[r]);
+    uint4 raw = *reinterpret_cast<const uint4*>((which == 0 ? sm.q[b] : sm.k[b]) + off);
+    __nv_bfloat162* x = reinterpret_cast<__nv_bfloat162*>(&raw);
+    uint32_t w[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      float2 f = __bfloat1622float2(x[u]);
+      w[u] = pack_bf16x2(f.x * sc, f.y * sc);
+    }
+    *reinterpret_cast<uint4*>((which == 0 ? sm.qt[b] : sm.kt[b]) + off) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+  if (!cx.commit_wait()) return false;
+  {
+    const int i = 16 * cx.q4 + cx.lane;
+    for (int cc = 0; cc < 64; cc += 16) {
+      float v[16];
+      tmem_ld16(cx.tmem + kRtW + cx.lane_base() + 64 * cx.half + cc, v);
+      tmem_ld_wait();
+      if (cx.lane < 16) {
+        for (int x = 0; x < 16; ++x) v[x] = -v[x];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int cj = (cc >> 3) + u;
+          *reinterpret_cast<uint4*>(sm.wn[cx.half] + i * 128 + ((cj ^ (i & 7)) << 4)) = pack8(v + 8 * u);
+        }
+      }
+    }
+    for (int cc = 0; cc < 32; cc += 16) {
+      float v[16];
+      tmem_ld16(cx.tmem + kRtG + cx.lane_base() + 32 * cx.half + cc, v);
+      tmem_ld_wait();
+      if (cx.lane < 16) {
+        const float gi = sm.gam[i];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          float pv[8];
+          for (int x = 0; x < 8; ++x) {
+            const int j = 32 * cx.half + cc + 8 * u + x;
+            pv[x] = (j <= i && i < n) ? __expf(gi - sm.gam[j]) * p.scale * v[8 * u + x] : 0.f;
+          }
+          const int cj = ((32 * cx.half + cc) >> 3) + u;
+          *reinterpret_cast<uint4*>(sm.p + i * 128 + ((cj ^ (i & 7)) << 4)) = pack8(pv);
+        }
+      }
+    }
+  }
+  sync_generic_to_async();
+  // dV' = K~ dS + P^T dO
+  if (cx.tid == 0) {
+    for (int ks = 0; ks < 8; ++ks)
+      umma_bf16(cx.tmem + kRtA, kmajor_desc(smem_u32(sm.kt[0]), 8192, ks), mnmajor_desc(smem_u32(sm.ds[0]), 16384, ks),
+                idesc_bf16(64, 128, 0, 1), ks > 0);
+    for (int ks = 0; ks < 4; ++ks)
+      umma_bf16(cx.tmem + kRtA, mnmajor_desc(smem_u32(sm.p), 8192, ks), mnmajor_desc(smem_u32(sm.dout[0]), 8192, ks),
+                idesc_bf16(64, 128, 1, 1), 1);
+  }
+  if (!cx.commit_wait()) return false;
+  {
+    const int t = 16 * cx.q4 + cx.lane;
+    for (int cc = 0; cc < 64; cc += 16) {
+      float v[16];
+      tmem_ld16(cx.tmem + kRtA + cx.lane_base() + 64 * cx.half + cc, v);
+      tmem_ld_wait();
+      if (cx.lane < 16) {
+        if (t >= n)
+          for (int x = 0; x < 16; ++x) v[x] = 0.f;
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int cj = (cc >> 3) + u;
+          *reinterpret_cast<uint4*>(sm.dvp[cx.half] + t * 128 + ((cj ^ (t & 7)) << 4)) = pack8(v + 8 * u);
+        }
+      }
+    }
+  }
+  sync_generic_to_async();
+  copy_smem_to_global(p.ws + p.L.dvp_img + ((size_t)gc * Hv + h) * 16384, sm.dvp[0], 16384, cx.tid);
+  // dS_c = e^{gamma_C} dS + Q~^T dO - W^T dV'
+  if (cx.tid == 0) {
+    for (int ks = 0; ks < 4; ++ks)
+      umma_bf16(cx.tmem + kRtC, mnmajor_desc(smem_u32(sm.qt[0]), 8192, ks), mnmajor_desc(smem_u32(sm.dout[0]), 8192, ks),
+                idesc_bf16(128, 128, 1, 1), ks > 0);
+    for (int ks = 0; ks < 4; ++ks)
+      umma_bf16(cx.tmem + kRtC, mnmajor_desc(smem_u32(sm.wn[0]), 8192, ks), mnmajor_desc(smem_u32(sm.dvp[0]), 8192, ks),
+                idesc_bf16(128, 128, 1, 1), 1);
+  }
+  if (!cx.commit_wait()) return false;
+  {
+    const float GC = __expf(gC);
+    for (int cc = 0; cc < 64; cc += 16) {
+      float v[16];
+      tmem_ld16(cx.tmem + kRtC + cx.lane_base() + 64 * cx.half + cc, v);
+      tmem_ld_wait();
+      for (int x = 0; x < 16; ++x) dS[cc + x] = GC * dS[cc + x] + v[x];
+    }
+    rev_store_ds(cx, sm, dS);
+  }
+  sync_generic_to_async();
+  return true;
+}
+
+__global__ void __launch_bounds__(256, 1) rev_chain_kernel(const __grid_constant__ BwdParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  RevSmem& sm = *reinterpret_cast<RevSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ uint64_t bar_ld, bar_mma;
+  __shared__ uint32_t tmem_holder;
+  __shared__ int s_item, s_ok;
+  Header* hd = reinterpret_cast<Header*>(p.ws + p.L.f.header);
+  Header* h2 = reinterpret_cast<Header*>(p.ws + p.L.hdr2);
+  const int N = p.d.N, Hv = p.d.Hv, G = p.d.Hv / p.d.Hk;
+  const int n_items = N * Hv;
+  if (blockIdx.x >= n_items || get_status(hd) != 0) return;
+  Ctx cx;
+  ctx_init(cx, &bar_ld, &bar_mma);
+  if (cx.tid == 0) {
+    mbar_init(&bar_ld, 1);
+    mbar_init(&bar_mma, 1);
+    fence_mbar_init();
+  }
+  if (cx.warp == 0) tmem_alloc(&tmem_holder, 512);
+  sync_generic_to_async();
+  cx.tmem = tmem_holder;
+  const int32_t* seq_chunk0 = reinterpret_cast<const int32_t*>(p.ws + p.L.f.seq_chunk0);
+  const int32_t* ctok = reinterpret_cast<const int32_t*>(p.ws + p.L.f.chunk_tok0);
+  const int32_t* clen = reinterpret_cast<const int32_t*>(p.ws + p.L.f.chunk_len);
+  float* ds0 = reinterpret_cast<float*>(p.ws + p.L.ds0);
+  int* flags = reinterpret_cast<int*>(p.ws + p.L.flags_ds0);
+  const size_t st = (size_t)kDim * kDim;
+  float dS[64];
+  for (;;) {
+    if (cx.tid == 0) {
+      const int it = (int)atomicAdd(&h2->q_chain, 1u);
+      s_item = (get_status(hd) != 0) ? n_items : it;
+    }
+    __syncthreads();
+    const int item = s_item;
+    if (item >= n_items) break;
+    const int seq = N - 1 - item / Hv, h = item % Hv, hk = h / G;
+    const int r = 32 * cx.q4 + cx.lane;
+    if (p.dfinal) {
+      const float* src = p.dfinal + ((size_t)seq * Hv + h) * st + (size_t)r * kDim + 64 * cx.half;
+      for (int c = 0; c < 64; ++c) dS[c] = src[c];
+    } else {
+      for (int c = 0; c < 64; ++c) dS[c] = 0.f;
+    }
+    // documents that started from this one's final state send their gradient back (in order)
+    bool ok = true;
+    if (p.init_idx) {
+      for (int x = seq + 1; x < N && ok; ++x) {
+        if (p.init_idx[x] != p.d.n_init + seq) continue;
+        if (cx.tid == 0) {
+          s_ok = wait_flag(&flags[x * Hv + h], hd) ? 1 : 0;
+          __threadfence();
+        }
+        __syncthreads();
+        ok = s_ok != 0;
+        if (ok) {
+          const float* src = ds0 + ((size_t)x * Hv + h) * st + (size_t)r * kDim + 64 * cx.half;
+          for (int c = 0; c < 64; c += 4) {
+            const float4 f = __ldcg(reinterpret_cast<const float4*>(src + c));
+            dS[c] += f.x;
+            dS[c + 1] += f.y;
+            dS[c + 2] += f.z;
+            dS[c + 3] += f.w;
+          }
+        }
+        __syncthreads();
+      }
+    }
+    if (!ok) break;
+    rev_store_ds(cx, sm, dS);
+    sync_generic_to_async();
+    const int c0 = seq_chunk0[seq], c1 = seq_chunk0[seq + 1];
+    for (int gc = c1 - 1; gc >= c0 && ok; --gc) ok = rev_chunk(p, cx, sm, dS, gc, h, hk, ctok[gc], clen[gc]);
+    if (!ok) {
+      set_status(hd, kErrTimeout);
+      break;
+    }
+    float* dst = ds0 + ((size_t)seq * Hv + h) * st + (size_t)r * kDim + 64 * cx.half;
+    for (int c = 0; c < 64; c += 4) *reinterpret_cast<float4*>(dst + c) = make_float4(dS[c], dS[c + 1], dS[c + 2], dS[c + 3]);
+    __syncthreads();
+    if (cx.tid == 0) {
+      __threadfence();
+      st_release(&flags[seq * Hv + h], 1);
+    }
+    __syncthreads();
+  }
+  if (cx.tid == 0) {
+    umma_commit(&bar_mma);
+    mbar_wait(&bar_mma, cx.ph_mma, kWaitBudget);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (cx.warp == 0) tmem_dealloc(cx.tmem, 512);
+}
+
+// ===================================================================================== gradients
+
+struct GradSmem {
+  uint8_t q[2][8192];
+  uint8_t k[2][8192];
+  float kkf[64][64];       // K K^T
+  float qkf[64][64];       // scale Q K^T
+  uint8_t bS[2][16384];    // S_c image       | phase 2: T fp32 [0, 16K), T bf16 [16K, 24K)
+  uint8_t bdS[2][16384];   // dS_{c+1} image  | phase 2: T_w [0, 8K), T_u [8K, 16K), dT [16K, 24K), R [24K, 32K)
+  uint8_t bVp[2][8192];    // V' -> V'_s      | fp32 64x64 scratch (vy products, then dA)
+  uint8_t bdVp[2][8192];   // dV'             | fp32 64x64 scratch (kx products)
+  uint8_t bdO[2][8192];    // dO              | phase 2: V
+  uint8_t bW[2][8192];     // fp32 scratch (dEg) | dW rows t
+  uint8_t bP[8192];        // scale dQK, then dKK + dKK^T
+  float gam[64], beta[64], Gm[64];
+  float part[8][64];
+  float vy[64], kx[64], rA[64], cA[64], db3[64];
+  float red[256];
+};
+constexpr size_t kGradSmemBytes = sizeof(GradSmem) + 1024;
+constexpr uint32_t kGtK = 128, kGt1 = 256, kGt2 = 384;
+
+__global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ BwdParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  GradSmem& sm = *reinterpret_cast<GradSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ uint64_t bar_ld, bar_mma;
+  __shared__ uint32_t tmem_holder;
+  Header* hd = reinterpret_cast<Header*>(p.ws + p.L.f.header);
+  const int chunk = blockIdx.x, hk = blockIdx.y;
+  if (chunk >= hd->n_chunks || get_status(hd) != 0) return;
+  const int Hv = p.d.Hv, Hk = p.d.Hk, G = Hv / Hk;
+  const int tok0 = reinterpret_cast<const int32_t*>(p.ws + p.L.f.chunk_tok0)[chunk];
+  const int n = reinterpret_cast<const int32_t*>(p.ws + p.L.f.chunk_len)[chunk];
+  Ctx cx;
+  ctx_init(cx, &bar_ld, &bar_mma);
+  const int tid = cx.tid;
+  if (tid == 0) {
+    mbar_init(&bar_ld, 1);
+    mbar_init(&bar_mma, 1);
+    fence_mbar_init();
+  }
+  if (cx.warp == 0) tmem_alloc(&tmem_holder, 512);
+  sync_generic_to_async();
+  cx.tmem = tmem_holder;
+  const uint32_t tm = cx.tmem;
+  bool ok = true;
+  const int i_row = 16 * cx.q4 + cx.lane;  // row held by this thread in M = 64 accumulators (lane < 16)
+  const bool has_row = cx.lane < 16;
+
+  // ---- per key head: Q, K, K K^T, Q K^T
+  if (tid == 0) {
+    mbar_arrive_expect_tx(&bar_ld, 4 * 8192);
+    tma_load_3d(sm.q[0], &p.tm_q, 0, hk, tok0, &bar_ld);
+    tma_load_3d(sm.q[1], &p.tm_q, 64, hk, tok0, &bar_ld);
+    tma_load_3d(sm.k[0], &p.tm_k, 0, hk, tok0, &bar_ld);
+    tma_load_3d(sm.k[1], &p.tm_k, 64, hk, tok0, &bar_ld);
+  }
+  ok = cx.wait_ld();
+  if (ok) {
+    if (tid == 0) {
+      for (int ks = 0; ks < 8; ++ks) {
+        umma_bf16(tm + kGt1, kmajor_desc(smem_u32(sm.k[0]), 8192, ks), kmajor_desc(smem_u32(sm.k[0]), 8192, ks),
+                  idesc_bf16(64, 64, 0, 0), ks > 0);
+        umma_bf16(tm + kGt1 + 64, kmajor_desc(smem_u32(sm.q[0]), 8192, ks), kmajor_desc(smem_u32(sm.k[0]), 8192, ks),
+                  idesc_bf16(64, 64, 0, 0), ks > 0);
+      }
+    }
+    ok = cx.commit_wait();
+  }
+  if (ok) {
+    for (int cc = 0; cc < 32; cc += 16) {
+      float a[16], b[16];
+      tmem_ld16(tm + kGt1 + cx.lane_base() + 32 * cx.half + cc, a);
+      tmem_ld16(tm + kGt1 + 64 + cx.lane_base() + 32 * cx.half + cc, b);
+      tmem_ld_wait();
+      if (has_row)
+        for (int x = 0; x < 16; ++x) {
+          sm.kkf[i_row][32 * cx.half + cc + x] = a[x];
+          sm.qkf[i_row][32 * cx.half + cc + x] = b[x] * p.scale;
+        }
+    }
+  }
+  __syncthreads();
+
+  bool first_k = true;
+  for (int hh = 0; hh < G && ok; ++hh) {
+    const int h = hk * G + hh;
+    const size_t rec = (size_t)chunk * Hv + h;
+    // ---------------- phase 1 loads
+    if (tid == 0) {
+      mbar_arrive_expect_tx(&bar_ld, 32768 * 2 + 16384 * 2 + 2 * 8192 + 256);
+      bulk_load(sm.bS[0], p.ws + p.L.st_img + rec * 32768, 32768, &bar_ld);
+      bulk_load(sm.bdS[0], p.ws + p.L.ds_img + rec * 32768, 32768, &bar_ld);
+      bulk_load(sm.bVp[0], p.ws + p.L.vp_img + rec * 16384, 16384, &bar_ld);
+      bulk_load(sm.bdVp[0], p.ws + p.L.dvp_img + rec * 16384, 16384, &bar_ld);
+      tma_load_3d(sm.bdO[0], &p.tm_do, 0, h, tok0, &bar_ld);
+      tma_load_3d(sm.bdO[1], &p.tm_do, 64, h, tok0, &bar_ld);
+      bulk_load(sm.gam, p.ws + p.L.f.gam + rec * 256, 256, &bar_ld);
+    }
+    if (tid < 64) sm.beta[tid] = (tid < n) ? p.beta[(size_t)(tok0 + tid) * Hv + h] : 0.f;
+    if (!(ok = cx.wait_ld())) break;
+    if (tid < 64) sm.Gm[tid] = __expf(sm.gam[tid]);
+    __syncthreads();
+    const float gC = sm.gam[63], GC = __expf(gC);
+    float* dEg = reinterpret_cast<float*>(sm.bW[0]);
+    // ---------------- (a) dP = dO V'^T ; K dS
+    if (tid == 0) {
+      for (int ks = 0; ks < 8; ++ks)
+        umma_bf16(tm + kGt1, kmajor_desc(smem_u32(sm.bdO[0]), 8192, ks), kmajor_desc(smem_u32(sm.bVp[0]), 8192, ks),
+                  idesc_bf16(64, 64, 0, 0), ks > 0);
+      for (int ks = 0; ks < 8; ++ks)
+        umma_bf16(tm + kGt2, kmajor_desc(smem_u32(sm.k[0]), 8192, ks), mnmajor_desc(smem_u32(sm.bdS[0]), 16384, ks),
+                  idesc_bf16(64, 128, 0, 1), ks > 0);
+    }
+    if (!(ok = cx.commit_wait())) break;
+    {
+      float rs = 0.f;
+      for (int cc = 0; cc < 32; cc += 16) {
+        float v[16];
+        tmem_ld16(tm + kGt1 + cx.lane_base() + 32 * cx.half + cc, v);
+        tmem_ld_wait();
+        if (has_row) {
+          const int i = i_row;
+          float dq8[16];
+          for (int x = 0; x < 16; ++x) {
+            const int j = 32 * cx.half + cc + x;
+            const float e = (j <= i && i < n) ? __expf(sm.gam[i] - sm.gam[j]) : 0.f;
+            const float dqk = v[x] * e;
+            dq8[x] = dqk * p.scale;
+            const float eg = dqk * sm.qkf[i][j];
+            dEg[i * 64 + j] = eg;
+            rs += eg;
+          }
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int cj = ((32 * cx.half + cc) >> 3) + u;
+            *reinterpret_cast<uint4*>(sm.bP + i * 128 + ((cj ^ (i & 7)) << 4)) = pack8(dq8 + 8 * u);
+          }
+        }
+      }
+      if (has_row) sm.part[0 + cx.half][i_row] = rs;
+      float kt = 0.f;
+      for (int cc = 0; cc < 64; cc += 16) {
+        float v[16];
+        tmem_ld16(tm + kGt2 + cx.lane_base() + 64 * cx.half + cc, v);
+        tmem_ld_wait();
+        if (has_row)
+          for (int x = 0; x < 16; ++x) kt += bf16_at(sm.bVp[cx.half], i_row, cc + x) * v[x];
+      }
+      if (has_row) sm.part[2 + cx.half][i_row] = kt;
+    }
+    __syncthreads();
+    if (tid < 64) {
+      float s = 0.f;
+      for (int i = 0; i < 64; ++i) s += dEg[i * 64 + tid];
+      sm.part[4][tid] = s;
+    }
+    __syncthreads();
+    // ---------------- (b) Q S ; dV' S^T (-> dW) ; <dS, S>
+    if (tid == 0) {
+      for (int ks = 0; ks < 8; ++ks)
+        umma_bf16(tm + kGt1, kmajor_desc(smem_u32(sm.q[0]), 8192, ks), mnmajor_desc(smem_u32(sm.bS[0]), 16384, ks),
+                  idesc_bf16(64, 128, 0, 1), ks > 0);
+      for (int ks = 0; ks < 8; ++ks)
+        umma_bf16(tm + kGt2, kmajor_desc(smem_u32(sm.bdVp[0]), 8192, ks), kmajor_desc(smem_u32(sm.bS[0]), 16384, ks),
+                  idesc_bf16(64, 128, 0, 0), ks > 0);
+    }
+    {
+      // Frobenius product of the two state images (same layout, so element-by-element)
+      float fr = 0.f;
+      for (int o = tid * 16; o < 32768; o += 256 * 16) {
+        uint4 a = *reinterpret_cast<const uint4*>(sm.bS[0] + o);
+        uint4 b = *reinterpret_cast<const uint4*>(sm.bdS[0] + o);
+        const __nv_bfloat162* xa = reinterpret_cast<const __nv_bfloat162*>(&a);
+        const __nv_bfloat162* xb = reinterpret_cast<const __nv_bfloat162*>(&b);
+        for (int u = 0; u < 4; ++u) {
+          float2 fa = __bfloat1622float2(xa[u]), fb = __bfloat1622float2(xb[u]);
+          fr += fa.x * fb.x + fa.y * fb.y;
+        }
+      }
+      sm.red[tid] = fr;
+    }
+    if (!(ok = cx.commit_wait())) break;
+    {
+      float qs = 0.f;
+      for (int cc = 0; cc < 64; cc += 16) {
+        float v[16], w[16];
+        tmem_ld16(tm + kGt1 + cx.lane_base() + 64 * cx.half + cc, v);
+        tmem_ld16(tm + kGt2 + cx.lane_base() + 64 * cx.half + cc, w);
+        tmem_ld_wait();
+        if (has_row) {
+          for (int x = 0; x < 16; ++x) qs += bf16_at(sm.bdO[cx.half], i_row, cc + x) * v[x];
+          for (int x = 0; x < 16; ++x) w[x] = -w[x];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int cj = (cc >> 3) + u;
+            *reinterpret_cast<uint4*>(sm.bW[cx.half] + i_row * 128 + ((cj ^ (i_row & 7)) << 4)) = pack8(w + 8 * u);
+          }
+        }
+      }
+      if (has_row) sm.part[5 + cx.half][i_row] = qs * sm.Gm[i_row] * p.scale;
+    }
+    // ---------------- (c) V'_s = diag(e^{gamma_C - gamma}) V' ; dk accumulation (dq has its own kernel)
+    if (tid < 64) sm.cA[tid] = __expf(gC - sm.gam[tid]);
+    __syncthreads();
+    scale_rows(sm.bVp[0], sm.cA, tid);
+    scale_rows(sm.bVp[1], sm.cA, tid);
+    sync_generic_to_async();
+    if (tid == 0) {
+      for (int ks = 0; ks < 8; ++ks)
+        umma_bf16(tm + kGtK, kmajor_desc(smem_u32(sm.bVp[0]), 8192, ks), kmajor_desc(smem_u32(sm.bdS[0]), 16384, ks),
+                  idesc_bf16(64, 128, 0, 0), (!first_k || ks > 0) ? 1 : 0);
+      for (int ks = 0; ks < 4; ++ks)
+        umma_bf16(tm + kGtK, mnmajor_desc(smem_u32(sm.bP), 8192, ks), mnmajor_desc(smem_u32(sm.q[0]), 8192, ks),
+                  idesc_bf16(64, 128, 1, 1), 1);
+    }
+    first_k = false;
+    float fro = 0.f;
+    if (tid == 0)
+      for (int x = 0; x < 256; ++x) fro += sm.red[x];
+    if (!(ok = cx.commit_wait())) break;
+    // ---------------- phase 2 loads: V, T, T_w, T_u
+    if (tid == 0) {
+      mbar_arrive_expect_tx(&bar_ld, 2 * 8192 + 16384 + 2 * 8192);
+      tma_load_3d(sm.bdO[0], &p.tm_v, 0, h, tok0, &bar_ld);
+      tma_load_3d(sm.bdO[1], &p.tm_v, 64, h, tok0, &bar_ld);
+      bulk_load(sm.bS[0], p.ws + p.L.t_f32 + rec * 16384, 16384, &bar_ld);
+      bulk_load(sm.bdS[0], p.ws + p.L.f.tw + rec * 8192, 8192, &bar_ld);
+      bulk_load(sm.bdS[0] + 8192, p.ws + p.L.f.tu + rec * 8192, 8192, &bar_ld);
+    }
+    if (!(ok = cx.wait_ld())) break;
+    const float* Tf = reinterpret_cast<const float*>(sm.bS[0]);
+    uint8_t* Tb = sm.bS[1];                 // T bf16 image (bytes [16K, 24K) of bS)
+    uint8_t* Tw = sm.bdS[0];
+    uint8_t* Tu = sm.bdS[0] + 8192;
+    uint8_t* dTt = sm.bdS[1];
+    uint8_t* Rt = sm.bdS[1] + 8192;
+    for (int e = tid; e < 64 * 8; e += 256) {
+      const int r = e >> 3, cj = e & 7;
+      float x[8];
+      for (int u = 0; u < 8; ++u) x[u] = Tf[r * 64 + cj * 8 + u];
+      *reinterpret_cast<uint4*>(Tb + r * 128 + ((cj ^ (r & 7)) << 4)) = pack8(x);
+    }
+    sync_generic_to_async();
+    // ---------------- (d) dv = T_u^T dV' ; D1 = dV' V^T ; D2 = dW K^T ; dk += T_w^T dW
+    if (tid == 0) {
+      for (int ks = 0; ks < 4; ++ks)
+        umma_bf16(tm + kGt1, mnmajor_desc(smem_u32(Tu), 8192, ks), mnmajor_desc(smem_u32(sm.bdVp[0]), 8192, ks),
+                  idesc_bf16(64, 128, 1, 1), ks > 0);
+      for (int ks = 0; ks < 8; ++ks)
+        umma_bf16(tm + kGt2, kmajor_desc(smem_u32(sm.bdVp[0]), 8192, ks), kmajor_desc(smem_u32(sm.bdO[0]), 8192, ks),
+                  idesc_bf16(64, 64, 0, 0), ks > 0);
+      for (int ks = 0; ks < 8; ++ks)
+        umma_bf16(tm + kGt2 + 64, kmajor_desc(smem_u32(sm.bW[0]), 8192, ks), kmajor_desc(smem_u32(sm.k[0]), 8192, ks),
+                  idesc_bf16(64, 64, 0, 0), ks > 0);
+      for (int ks = 0; ks < 4; ++ks)
+        umma_bf16(tm + kGtK, mnmajor_desc(smem_u32(Tw), 8192, ks), mnmajor_desc(smem_u32(sm.bW[0]), 8192, ks),
+                  idesc_bf16(64, 128, 1, 1), 1);
+    }
+    if (!(ok = cx.commit_wait())) break;
+    float* vyM = reinterpret_cast<float*>(sm.bVp[0]);
+    float* kxM = reinterpret_cast<float*>(sm.bdVp[0]);
+    {
+      float* dvrow = p.dv + ((size_t)(tok0 + i_row) * Hv + h) * kDim + 64 * cx.half;
+      for (int cc = 0; cc < 64; cc += 16) {
+        float v[16];
+        tmem_ld16(tm + kGt1 + cx.lane_base() + 64 * cx.half + cc, v);
+        tmem_ld_wait();
+        if (has_row && i_row < n)
+          for (int x = 0; x < 16; x += 4)
+            *reinterpret_cast<float4*>(dvrow + cc + x) = make_float4(v[x], v[x + 1], v[x + 2], v[x + 3]);
+      }
+      for (int cc = 0; cc < 32; cc += 16) {
+        float d1[16], d2[16];
+        tmem_ld16(tm + kGt2 + cx.lane_base() + 32 * cx.half + cc, d1);
+        tmem_ld16(tm + kGt2 + 64 + cx.lane_base() + 32 * cx.half + cc, d2);
+        tmem_ld_wait();
+        if (has_row) {
+          const int i = i_row;
+          float dt[16];
+          for (int x = 0; x < 16; ++x) {
+            const int j = 32 * cx.half + cc + x;
+            dt[x] = d1[x] * sm.beta[j] + d2[x] * sm.beta[j] * sm.Gm[j];
+            vyM[i * 64 + j] = Tf[i * 64 + j] * d1[x];
+            kxM[i * 64 + j] = Tf[i * 64 + j] * d2[x];
+          }
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int cj = ((32 * cx.half + cc) >> 3) + u;
+            *reinterpret_cast<uint4*>(dTt + i * 128 + ((cj ^ (i & 7)) << 4)) = pack8(dt + 8 * u);
+          }
+        }
+      }
+    }
+    sync_generic_to_async();
+    if (tid < 64) {
+      float a = 0.f, b = 0.f;
+      for (int i = 0; i < 64; ++i) {
+        a += vyM[i * 64 + tid];
+        b += kxM[i * 64 + tid];
+      }
+      sm.vy[tid] = a;
+      sm.kx[tid] = b;
+    }
+    // ---------------- (e) R = dT T^T
+    if (tid == 0)
+      for (int ks = 0; ks < 4; ++ks)
+        umma_bf16(tm + kGt1, kmajor_desc(smem_u32(dTt), 8192, ks), kmajor_desc(smem_u32(Tb), 8192, ks),
+                  idesc_bf16(64, 64, 0, 0), ks > 0);
+    if (!(ok = cx.commit_wait())) break;
+    for (int cc = 0; cc < 32; cc += 16) {
+      float v[16];
+      tmem_ld16(tm + kGt1 + cx.lane_base() + 32 * cx.half + cc, v);
+      tmem_ld_wait();
+      if (has_row) {
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int cj = ((32 * cx.half + cc) >> 3) + u;
+          *reinterpret_cast<uint4*>(Rt + i_row * 128 + ((cj ^ (i_row & 7)) << 4)) = pack8(v + 8 * u);
+        }
+      }
+    }
+    sync_generic_to_async();
+    // ---------------- (f) dA = -(T^T R), strictly lower and inside the chunk
+    if (tid == 0)
+      for (int ks = 0; ks < 4; ++ks)
+        umma_bf16(tm + kGt1, mnmajor_desc(smem_u32(Tb), 8192, ks), mnmajor_desc(smem_u32(Rt), 8192, ks),
+                  idesc_bf16(64, 64, 1, 1), ks > 0);
+    if (!(ok = cx.commit_wait())) break;
+    float* dA = vyM;  // vy column sums are done
+    for (int cc = 0; cc < 32; cc += 16) {
+      float v[16];
+      tmem_ld16(tm + kGt1 + cx.lane_base() + 32 * cx.half + cc, v);
+      tmem_ld_wait();
+      if (has_row)
+        for (int x = 0; x < 16; ++x) {
+          const int j = 32 * cx.half + cc + x;
+          dA[i_row * 64 + j] = (j < i_row && i_row < n) ? -v[x] : 0.f;
+        }
+    }
+    __syncthreads();
+    // dKK + dKK^T (dKK_ij = dA_ij beta_i E_ij), row and column sums for dbeta and dgamma
+    for (int e = tid; e < 64 * 8; e += 256) {
+      const int i = e >> 3, cj = e & 7;
+      float x[8];
+      for (int u = 0; u < 8; ++u) {
+        const int j = cj * 8 + u;
+        float s = 0.f;
+        if (j < i) s += dA[i * 64 + j] * sm.beta[i] * __expf(sm.gam[i] - sm.gam[j]);
+        if (i < j) s += dA[j * 64 + i] * sm.beta[j] * __expf(sm.gam[j] - sm.gam[i]);
+        x[u] = s;
+      }
+      *reinterpret_cast<uint4*>(sm.bP + i * 128 + ((cj ^ (i & 7)) << 4)) = pack8(x);
+    }
+    if (tid < 64) {
+      const int i = tid;
+      float b3 = 0.f, ra = 0.f;
+      for (int j = 0; j < i; ++j) {
+        const float ekk = __expf(sm.gam[i] - sm.gam[j]) * sm.kkf[i][j];
+        b3 += dA[i * 64 + j] * ekk;
+        ra += dA[i * 64 + j] * sm.beta[i] * ekk;
+      }
+      sm.db3[i] = b3;
+      sm.rA[i] = ra;
+    } else if (tid < 128) {
+      const int j = tid - 64;
+      float ca = 0.f;
+      for (int i = j + 1; i < 64; ++i) ca += dA[i * 64 + j] * sm.beta[i] * __expf(sm.gam[i] - sm.gam[j]) * sm.kkf[i][j];
+      sm.cA[j] = ca;
+    }
+    sync_generic_to_async();
+    // ---------------- (g) dk += (dKK + dKK^T) K
+    if (tid == 0)
+      for (int ks = 0; ks < 4; ++ks)
+        umma_bf16(tm + kGtK, kmajor_desc(smem_u32(sm.bP), 8192, ks), mnmajor_desc(smem_u32(sm.k[0]), 8192, ks),
+                  idesc_bf16(64, 128, 0, 1), 1);
+    if (!(ok = cx.commit_wait())) break;
+    // ---------------- (h) dgamma -> dg (reverse cumulative sum in the chunk), dbeta
+    if (tid == 0) {
+      float ktsum = 0.f;
+      for (int i = 0; i < n; ++i) ktsum += __expf(gC - sm.gam[i]) * (sm.part[2][i] + sm.part[3][i]);
+      sm.red[0] = ktsum;
+      sm.red[1] = fro;
+    }
+    __syncthreads();
+    if (tid < 64) {
+      const int i = tid;
+      float dgam = 0.f;
+      if (i < n) {
+        const float ktd = __expf(gC - sm.gam[i]) * (sm.part[2][i] + sm.part[3][i]);
+        dgam = sm.part[0][i] + sm.part[1][i] - sm.part[4][i] + sm.part[5][i] + sm.part[6][i] - ktd +
+               sm.beta[i] * sm.Gm[i] * sm.kx[i] + sm.rA[i] - sm.cA[i];
+        if (i == n - 1) dgam += GC * sm.red[1] + sm.red[0];
+      }
+      sm.part[7][i] = dgam;
+    }
+    __syncthreads();
+    if (tid < n) {
+      float s = 0.f;
+      for (int i = n - 1; i >= tid; --i) s += sm.part[7][i];
+      p.dg[(size_t)(tok0 + tid) * Hv + h] = s;
+      p.dbeta[(size_t)(tok0 + tid) * Hv + h] = sm.vy[tid] + sm.Gm[tid] * sm.kx[tid] + sm.db3[tid];
+    }
+    __syncthreads();
+  }
+  if (ok) {
+    // dk: sum over the value heads of this key head
+    const size_t row = ((size_t)(tok0 + i_row) * Hk + hk) * kDim + 64 * cx.half;
+    for (int cc = 0; cc < 64; cc += 16) {
+      float b[16];
+      tmem_ld16(tm + kGtK + cx.lane_base() + 64 * cx.half + cc, b);
+      tmem_ld_wait();
+      if (has_row && i_row < n)
+        for (int x = 0; x < 16; x += 4)
+          *reinterpret_cast<float4*>(p.dk + row + cc + x) = make_float4(b[x], b[x + 1], b[x + 2], b[x + 3]);
+    }
+  } else if (tid == 0) {
+    set_status(hd, kErrTimeout);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (cx.warp == 0) tmem_dealloc(tm, 512);
+}
+
+// ============================================================================================ dq
+//
+// dq = sum over the value heads h of the key head of
+//        scale diag(e^gamma) dO S_c^T  +  (scale (dO V'^T) o E) K
+// with S_c and V' in compensated bf16 (hi + lo, two MMAs each) so that dq, whose entries reach
+// O(10) at these shapes, keeps the accuracy of the other gradients; the per-row e^gamma scaling is
+// applied in fp32 and the sum over value heads is kept in fp32 registers.
+
+struct DqSmem {
+  uint8_t k[2][8192];    // K tile                  (B MN-major: dQK K)
+  uint8_t dout[2][8192]; // dO tile                 (A K-major)
+  uint8_t sh[2][16384];  // S_c high part           (B K-major: dO S^T)
+  uint8_t sl[2][16384];  // S_c low part
+  uint8_t vh[2][8192];   // V' high part            (B K-major: dO V'^T)
+  uint8_t vl[2][8192];   // V' low part
+  uint8_t qh[8192];      // scale dQK high part     (A K-major)
+  uint8_t ql[8192];      // scale dQK low part
+  float gam[64];
+};
+constexpr size_t kDqSmemBytes = sizeof(DqSmem) + 1024;
+constexpr uint32_t kDtP = 0, kDt1 = 128, kDt2 = 256;
+
+__global__ void __launch_bounds__(256, 1) dq_kernel(const __grid_constant__ BwdParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  DqSmem& sm = *reinterpret_cast<DqSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ uint64_t bar_ld, bar_mma;
+  __shared__ uint32_t tmem_holder;
+  Header* hd = reinterpret_cast<Header*>(p.ws + p.L.f.header);
+  const int chunk = blockIdx.x, hk = blockIdx.y;
+  if (chunk >= hd->n_chunks || get_status(hd) != 0) return;
+  const int Hv = p.d.Hv, Hk = p.d.Hk, G = Hv / Hk;
+  const int tok0 = reinterpret_cast<const int32_t*>(p.ws + p.L.f.chunk_tok0)[chunk];
+  const int n = reinterpret_cast<const int32_t*>(p.ws + p.L.f.chunk_len)[chunk];
+  Ctx cx;
+  ctx_init(cx, &bar_ld, &bar_mma);
+  const int tid = cx.tid;
+  if (tid == 0) {
+    mbar_init(&bar_ld, 1);
+    mbar_init(&bar_mma, 1);
+    fence_mbar_init();
+  }
+  if (cx.warp == 0) tmem_alloc(&tmem_holder, 512);
+  sync_generic_to_async();
+  const uint32_t tm = tmem_holder;
+  cx.tmem = tm;
+  const int i_row = 16 * cx.q4 + cx.lane;
+  const bool has_row = cx.lane < 16;
+  float dq[64];
+  for (int c = 0; c < 64; ++c) dq[c] = 0.f;
+  bool ok = true;
+  for (int hh = 0; hh < G && ok; ++hh) {
+    const int h = hk * G + hh;
+    const size_t rec = (size_t)chunk * Hv + h;
+    if (tid == 0) {
+      mbar_arrive_expect_tx(&bar_ld, (hh == 0 ? 2 * 8192 : 0) + 2 * 8192 + 2 * 32768 + 2 * 16384 + 256);
+      if (hh == 0) {
+        tma_load_3d(sm.k[0], &p.tm_k, 0, hk, tok0, &bar_ld);
+        tma_load_3d(sm.k[1], &p.tm_k, 64, hk, tok0, &bar_ld);
+      }
+      tma_load_3d(sm.dout[0], &p.tm_do, 0, h, tok0, &bar_ld);
+      tma_load_3d(sm.dout[1], &p.tm_do, 64, h, tok0, &bar_ld);
+      bulk_load(sm.sh[0], p.ws + p.L.st_img + rec * 32768, 32768, &bar_ld);
+      bulk_load(sm.sl[0], p.ws + p.L.st_lo + rec * 32768, 32768, &bar_ld);
+      bulk_load(sm.vh[0], p.ws + p.L.vp_img + rec * 16384, 16384, &bar_ld);
+      bulk_load(sm.vl[0], p.ws + p.L.vp_lo + rec * 16384, 16384, &bar_ld);
+      bulk_load(sm.gam, p.ws + p.L.f.gam + rec * 256, 256, &bar_ld);
+    }
+    if (!(ok = cx.wait_ld())) break;
+    // dP = dO V'^T (hi + lo)
+    if (tid == 0) {
+      for (int ks = 0; ks < 8; ++ks)
+        umma_bf16(tm + kDtP, kmajor_desc(smem_u32(sm.dout[0]), 8192, ks), kmajor_desc(smem_u32(sm.vh[0]), 8192, ks),
+                  idesc_bf16(64, 64, 0, 0), ks > 0);
+      for (int ks = 0; ks < 8; ++ks)
+        umma_bf16(tm + kDtP, kmajor_desc(smem_u32(sm.dout[0]), 8192, ks), kmajor_desc(smem_u32(sm.vl[0]), 8192, ks),
+                  idesc_bf16(64, 64, 0, 0), 1);
+    }
+    if (!(ok = cx.commit_wait())) break;
+    for (int cc = 0; cc < 32; cc += 16) {
+      float v[16];
+      tmem_ld16(tm + kDtP + cx.lane_base() + 32 * cx.half + cc, v);
+      tmem_ld_wait();
+      if (has_row) {
+        float hi[16], lo[16];
+        for (int x = 0; x < 16; ++x) {
+          const int j = 32 * cx.half + cc + x;
+          const float d = (j <= i_row && i_row < n) ? v[x] * __expf(sm.gam[i_row] - sm.gam[j]) * p.scale : 0.f;
+          hi[x] = __bfloat162float(__float2bfloat16_rn(d));
+          lo[x] = d - hi[x];
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int cj = ((32 * cx.half + cc) >> 3) + u;
+          const uint32_t off = i_row * 128 + ((cj ^ (i_row & 7)) << 4);
+          *reinterpret_cast<uint4*>(sm.qh + off) = pack8(hi + 8 * u);
+          *reinterpret_cast<uint4*>(sm.ql + off) = pack8(lo + 8 * u);
+        }
+      }
+    }
+    sync_generic_to_async();
+    // dO S^T (hi + lo) and dQK K (hi + lo)
+    if (tid == 0) {
+      for (int ks = 0; ks < 8; ++ks)
+        umma_bf16(tm + kDt1, kmajor_desc(smem_u32(sm.dout[0]), 8192, ks), kmajor_desc(smem_u32(sm.sh[0]), 16384, ks),
+                  idesc_bf16(64, 128, 0, 0), ks > 0);
+      for (int ks = 0; ks < 8; ++ks)
+        umma_bf16(tm + kDt1, kmajor_desc(smem_u32(sm.dout[0]), 8192, ks), kmajor_desc(smem_u32(sm.sl[0]), 16384, ks),
+                  idesc_bf16(64, 128, 0, 0), 1);
+      for (int ks = 0; ks < 4; ++ks)
+        umma_bf16(tm + kDt2, kmajor_desc(smem_u32(sm.qh), 8192, ks), mnmajor_desc(smem_u32(sm.k[0]), 8192, ks),
+                  idesc_bf16(64, 128, 0, 1), ks > 0);
+      for (int ks = 0; ks < 4; ++ks)
+        umma_bf16(tm + kDt2, kmajor_desc(smem_u32(sm.ql), 8192, ks), mnmajor_desc(smem_u32(sm.k[0]), 8192, ks),
+                  idesc_bf16(64, 128, 0, 1), 1);
+    }
+    if (!(ok = cx.commit_wait())) break;
+    {
+      const float sc = has_row ? __expf(sm.gam[i_row]) * p.scale : 0.f;
+      for (int cc = 0; cc < 64; cc += 16) {
+        float a[16], b[16];
+        tmem_ld16(tm + kDt1 + cx.lane_base() + 64 * cx.half + cc, a);
+        tmem_ld16(tm + kDt2 + cx.lane_base() + 64 * cx.half + cc, b);
+        tmem_ld_wait();
+        for (int x = 0; x < 16; ++x) dq[cc + x] += sc * a[x] + b[x];
+      }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+  }
+  if (ok) {
+    if (has_row && i_row < n) {
+      float* row = p.dq + ((size_t)(tok0 + i_row) * Hk + hk) * kDim + 64 * cx.half;
+      for (int c = 0; c < 64; c += 4) *reinterpret_cast<float4*>(row + c) = make_float4(dq[c], dq[c + 1], dq[c + 2], dq[c + 3]);
+    }
+  } else if (tid == 0) {
+    set_status(hd, kErrTimeout);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (cx.warp == 0) tmem_dealloc(tm, 512);
+}
+
+// d(initial_state)[x][h] = sum over documents i (in order) with init_idx[i] == x of dL/dS_start(i, h).
+__global__ void __launch_bounds__(256) dinit_reduce_kernel(const __grid_constant__ BwdParams p) {
+  const int x = blockIdx.x / p.d.Hv, h = blockIdx.x % p.d.Hv;
+  const float* ds0 = reinterpret_cast<const float*>(p.ws + p.L.ds0);
+  const size_t st = (size_t)kDim * kDim;
+  float* dst = p.dinit + ((size_t)x * p.d.Hv + h) * st;
+  for (int e = threadIdx.x; e < kDim * kDim; e += 256) {
+    float acc = 0.f;
+    if (p.init_idx)
+      for (int i = 0; i < p.d.N; ++i)
+        if (p.init_idx[i] == x) acc += ds0[((size_t)i * p.d.Hv + h) * st + e];
+    dst[e] = acc;
+  }
+}
+
+// ============================================================================================ launch
+
+int launch_bwd(const BwdArgs& a, cudaStream_t stream, cudaEvent_t* ev) {
+  static bool attr_done = false;
+  if (!attr_done) {
+    if (cudaFuncSetAttribute(rev_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRevSmemBytes) !=
+        cudaSuccess)
+      return kErrCuda;
+    if (cudaFuncSetAttribute(grad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGradSmemBytes) !=
+        cudaSuccess)
+      return kErrCuda;
+    if (cudaFuncSetAttribute(dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDqSmemBytes) !=
+        cudaSuccess)
+      return kErrCuda;
+    attr_done = true;
+  }
+  const PlanDims& d = a.d;
+  BwdParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.d = d;
+  p.L = bwd_layout(d);
+  if (a.ws_bytes < p.L.total) return kErrWorkspace;
+  uint8_t* ws = reinterpret_cast<uint8_t*>(a.ws);
+  // forward recompute with per-chunk records
+  FwdParams f;
+  std::memset(&f, 0, sizeof(f));
+  f.d = d;
+  f.L = p.L.f;
+  if (d.T > 0) {
+    const uint64_t row_k = (uint64_t)d.Hk * kDim * 2, row_v = (uint64_t)d.Hv * kDim * 2;
+    if (!make_tmap_bf16_3d(&f.tm_q, a.q, kDim, d.Hk, d.T, kDim * 2, row_k, 64, 1, 64) ||
+        !make_tmap_bf16_3d(&f.tm_k, a.k, kDim, d.Hk, d.T, kDim * 2, row_k, 64, 1, 64) ||
+        !make_tmap_bf16_3d(&f.tm_v, a.v, kDim, d.Hv, d.T, kDim * 2, row_v, 64, 1, 64) ||
+        !make_tmap_bf16_3d(&p.tm_do, a.dout, kDim, d.Hv, d.T, kDim * 2, row_v, 64, 1, 64))
+      return kErrCuda;
+  }
+  p.tm_q = f.tm_q;
+  p.tm_k = f.tm_k;
+  p.tm_v = f.tm_v;
+  f.g = a.g;
+  f.beta = a.beta;
+  f.cu = a.cu;
+  f.init_idx = a.init_idx;
+  f.initial_state = a.initial_state;
+  f.out = nullptr;
+  f.final_state = reinterpret_cast<float*>(ws + p.L.fin);
+  f.ws = ws;
+  f.trunc_thr = a.trunc_thr;
+  f.scale = a.scale;
+  f.st_img = ws + p.L.st_img;
+  f.vp_img = ws + p.L.vp_img;
+  f.t_f32 = reinterpret_cast<float*>(ws + p.L.t_f32);
+  f.tw_lo = ws + p.L.tw_lo;
+  f.tu_lo = ws + p.L.tu_lo;
+  f.st_lo_img = ws + p.L.st_lo;
+  f.vp_lo_img = ws + p.L.vp_lo;
+  int rc = launch_fwd(f, stream, ev);
+  if (rc != kOk) return rc;
+  p.g = a.g;
+  p.beta = a.beta;
+  p.cu = a.cu;
+  p.init_idx = a.init_idx;
+  p.dfinal = a.dfinal;
+  p.dq = reinterpret_cast<float*>(a.dq);
+  p.dk = reinterpret_cast<float*>(a.dk);
+  p.dv = reinterpret_cast<float*>(a.dv);
+  p.dg = a.dg;
+  p.dbeta = a.dbeta;
+  p.dinit = a.dinit;
+  p.ws = ws;
+  p.scale = a.scale;
+  auto mark = [&](int i) {
+    if (ev) cudaEventRecord(ev[i], stream);
+  };
+  if (cudaMemsetAsync(ws + p.L.flags_ds0, 0, (size_t)d.N * d.Hv * 4, stream) != cudaSuccess) return kErrCuda;
+  if (cudaMemsetAsync(ws + p.L.hdr2, 0, sizeof(Header), stream) != cudaSuccess) return kErrCuda;
+  mark(8);
+  {
+    const int items = d.N * d.Hv;
+    const int grid = items < d.num_sms ? items : d.num_sms;
+    rev_chain_kernel<<<grid, 256, kRevSmemBytes, stream>>>(p);
+  }
+  mark(9);
+  mark(10);
+  if (d.T > 0) {
+    grad_kernel<<<dim3((unsigned)p.L.f.cmax, (unsigned)d.Hk), 256, kGradSmemBytes, stream>>>(p);
+    dq_kernel<<<dim3((unsigned)p.L.f.cmax, (unsigned)d.Hk), 256, kDqSmemBytes, stream>>>(p);
+  }
+  mark(11);
+  mark(12);
+  if (d.n_init > 0) dinit_reduce_kernel<<<d.n_init * d.Hv, 256, 0, stream>>>(p);
+  mark(13);
+  return cudaGetLastError() == cudaSuccess ? kOk : kErrCuda;
 }
 
 }  // namespace gdn

@@ -23,56 +23,11 @@
 
 #include "bw_prims.cuh"
 #include "gdn_common.cuh"
+#include "gdn_dev.cuh"
 #include "gdn_fwd.h"
 
 namespace gdn {
 using namespace bw;
-
-constexpr long long kWaitBudget = 4000000000LL;  // clock cycles (about two seconds)
-
-__device__ __forceinline__ int ld_acquire(const int* p) {
-  int v;
-  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-__device__ __forceinline__ void st_release(int* p, int v) {
-  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-__device__ __forceinline__ void set_status(Header* hd, int code) { atomicCAS(&hd->status, 0, code); }
-__device__ __forceinline__ int get_status(const Header* hd) {
-  return *reinterpret_cast<const volatile int*>(&hd->status);
-}
-
-// Bounded wait on a publication flag; false on timeout (status set) or on an earlier error.
-__device__ bool wait_flag(const int* flag, Header* hd) {
-  const long long t0 = clock64();
-  while (ld_acquire(flag) == 0) {
-    if (get_status(hd) != 0) return false;
-    if (clock64() - t0 > kWaitBudget) {
-      set_status(hd, kErrTimeout);
-      return false;
-    }
-    __nanosleep(128);
-  }
-  return true;
-}
-
-// All threads of the CTA wait on `bar`; the outcome is made uniform with a vote so that no
-// thread leaves while others still expect a barrier. On failure each thread waits once more
-// (bounded) so that copies or MMAs still in flight can land before the caller gives up.
-__device__ __forceinline__ bool wait_all(uint64_t* bar, uint32_t parity) {
-  const bool ok = bw::mbar_wait(bar, parity, kWaitBudget);
-  if (__syncthreads_or(!ok)) {
-    bw::mbar_wait(bar, parity, kWaitBudget);
-    return false;
-  }
-  return true;
-}
-
-template <class T>
-__device__ __forceinline__ T* ws_ptr(const FwdParams& p, size_t off) {
-  return reinterpret_cast<T*>(p.ws + off);
-}
 
 // ============================================================================================ plan
 
@@ -351,12 +306,16 @@ __global__ void __launch_bounds__(128) kkt_solve_kernel(const __grid_constant__ 
       }
       __syncthreads();
     }
+    if (p.t_f32) {
+      float* tdst = p.t_f32 + ((size_t)chunk * Hv + h) * 4096;
+      for (int e = tid; e < 4096; e += 128) tdst[e] = sm.t[e >> 6][e & 63];
+    }
     // T diag(beta e^gamma) and T diag(beta), bf16, stored as the SW128 K-major smem image
     uint8_t* dw = tw_ws + ((size_t)chunk * Hv + h) * 8192;
     uint8_t* du = tu_ws + ((size_t)chunk * Hv + h) * 8192;
     for (int e = tid; e < 2 * 64 * 8; e += 128) {
       const int mat = e >> 9, r = (e >> 3) & 63, cj = e & 7;
-      uint32_t w[4];
+      uint32_t w[4], wl[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int j0 = cj * 8 + 2 * u;
@@ -365,10 +324,18 @@ __global__ void __launch_bounds__(128) kkt_solve_kernel(const __grid_constant__ 
           s0 *= __expf(sm.gam[j0]);
           s1 *= __expf(sm.gam[j0 + 1]);
         }
-        w[u] = pack_bf16x2(sm.t[r][j0] * s0, sm.t[r][j0 + 1] * s1);
+        const float x0 = sm.t[r][j0] * s0, x1 = sm.t[r][j0 + 1] * s1;
+        w[u] = pack_bf16x2(x0, x1);
+        const __nv_bfloat162 hb = *reinterpret_cast<const __nv_bfloat162*>(&w[u]);
+        const float2 hf = __bfloat1622float2(hb);
+        wl[u] = pack_bf16x2(x0 - hf.x, x1 - hf.y);
       }
       uint8_t* dst = (mat == 0 ? dw : du) + r * 128 + ((cj ^ (r & 7)) << 4);
       *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+      if (p.tw_lo) {
+        uint8_t* lo = (mat == 0 ? p.tw_lo : p.tu_lo) + ((size_t)chunk * Hv + h) * 8192 + r * 128 + ((cj ^ (r & 7)) << 4);
+        *reinterpret_cast<uint4*>(lo) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+      }
     }
     __syncthreads();
   }
@@ -392,6 +359,11 @@ struct ChainSmem {
   uint8_t vo[2][8192];    // V' rows t, dv blocks                     (B, MN-major: P V')
   uint8_t vs[2][8192];    // diag(e^{gamma_C - gamma}) V'             (B, MN-major: K^T V's)
   uint8_t s[2][16384];    // S in bf16: rows dk, dv blocks            (B, MN-major: [Q~; -W] S)
+  // record mode only (compensated bf16: x = hi + lo)
+  uint8_t z2[8192];       // zeros                                    ([0; T_u lo] A operand)
+  uint8_t tu_lo[8192];    // low part of T diag(beta)
+  uint8_t tw_lo[8192];    // low part of T diag(beta e^gamma)
+  uint8_t vs_lo[2][8192]; // low part of diag(e^{gamma_C - gamma}) V'
   float gam[64];
 };
 constexpr size_t kChainSmemBytes = sizeof(ChainSmem) + 1024;
@@ -423,16 +395,13 @@ __device__ __forceinline__ void store_state_bf16(ChainCtx& cx, const float* S) {
   }
 }
 
-__device__ __forceinline__ void sync_generic_to_async() {
-  fence_proxy_async_smem();
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-}
 
 // One chunk of the chain. S: this thread's 64 fp32 state values (updated in place).
 // Returns false if a bounded wait ran out (status already set).
-template <bool kOut, bool kWithU>
+// kOut: write O; kWithU: include the U = T diag(beta) V term (off only for the transition chain M);
+// kStore: record S, V' and their low parts for the backward; kComp: compensated bf16 operands
+// (x = hi + lo) for T diag(beta e^gamma), T diag(beta), W, S and diag(e^{gamma_C - gamma}) V'.
+template <bool kOut, bool kWithU, bool kStore = false, bool kComp = kStore>
 __device__ bool chain_chunk(const FwdParams& p, ChainCtx& cx, float* S, int gc, int h, int hk, int tok0, int n) {
   ChainSmem& sm = *cx.sm;
   const int Hv = p.d.Hv;
@@ -440,6 +409,7 @@ __device__ bool chain_chunk(const FwdParams& p, ChainCtx& cx, float* S, int gc, 
     uint32_t bytes = 2 * 8192 /*K*/ + 8192 /*Tw*/ + 256;
     if (kOut) bytes += 2 * 8192;
     if (kWithU) bytes += 2 * 8192 + 8192;
+    if (kComp) bytes += kWithU ? 2 * 8192 : 8192;
     mbar_arrive_expect_tx(cx.bar_ld, bytes);
     tma_load_3d(sm.k[0], &p.tm_k, 0, hk, tok0, cx.bar_ld);
     tma_load_3d(sm.k[1], &p.tm_k, 64, hk, tok0, cx.bar_ld);
@@ -454,10 +424,32 @@ __device__ bool chain_chunk(const FwdParams& p, ChainCtx& cx, float* S, int gc, 
     }
     bulk_load(sm.tw, p.ws + p.L.tw + ((size_t)gc * Hv + h) * 8192, 8192, cx.bar_ld);
     bulk_load(sm.gam, p.ws + p.L.gam + ((size_t)gc * Hv + h) * 256, 256, cx.bar_ld);
+    if (kComp) {
+      bulk_load(sm.tw_lo, p.tw_lo + ((size_t)gc * Hv + h) * 8192, 8192, cx.bar_ld);
+      if (kWithU) bulk_load(sm.tu_lo, p.tu_lo + ((size_t)gc * Hv + h) * 8192, 8192, cx.bar_ld);
+    }
   }
   if (!wait_all(cx.bar_ld, cx.ph_ld)) return false;
   cx.ph_ld ^= 1;
   tc_fence_after();
+  if (kStore) copy_smem_to_global(p.st_img + ((size_t)gc * Hv + h) * 32768, sm.s[0], 32768, cx.tid);
+  if (kComp) {
+    // low part S - bf16(S), same image layout as sm.s. In this mode Q and V'-out are idle when
+    // W S is formed: they hold the two dv blocks of S lo.
+    const int r = 32 * cx.q4 + cx.lane;
+    uint8_t* dst = kStore ? p.st_lo_img + ((size_t)gc * Hv + h) * 32768 + cx.half * 16384 : nullptr;
+    uint8_t* slo = cx.half == 0 ? sm.q[0] : sm.vo[0];
+#pragma unroll
+    for (int cj = 0; cj < 8; ++cj) {
+      float lo[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) lo[u] = S[8 * cj + u] - __bfloat162float(__float2bfloat16_rn(S[8 * cj + u]));
+      const uint4 w = make_uint4(pack_bf16x2(lo[0], lo[1]), pack_bf16x2(lo[2], lo[3]), pack_bf16x2(lo[4], lo[5]),
+                                 pack_bf16x2(lo[6], lo[7]));
+      if (kStore) *reinterpret_cast<uint4*>(dst + r * 128 + ((cj ^ (r & 7)) << 4)) = w;
+      *reinterpret_cast<uint4*>(slo + r * 128 + ((cj ^ (r & 7)) << 4)) = w;
+    }
+  }
 
   // -- MMA group 1: W = T_w K (M=64), P-raw = Q K^T (M=64)
   if (cx.tid == 0) {
@@ -465,6 +457,10 @@ __device__ bool chain_chunk(const FwdParams& p, ChainCtx& cx, float* S, int gc, 
     for (int ks = 0; ks < 4; ++ks)
       umma_bf16(cx.tmem + kTmW, kmajor_desc(smem_u32(sm.tw), 8192, ks), mnmajor_desc(k0, 8192, ks),
                 idesc_bf16(64, 128, 0, 1), ks > 0);
+    if (kComp)
+      for (int ks = 0; ks < 4; ++ks)
+        umma_bf16(cx.tmem + kTmW, kmajor_desc(smem_u32(sm.tw_lo), 8192, ks), mnmajor_desc(k0, 8192, ks),
+                  idesc_bf16(64, 128, 0, 1), 1);
     if (kOut)
       for (int ks = 0; ks < 8; ++ks)
         umma_bf16(cx.tmem + kTmG, kmajor_desc(smem_u32(sm.q[0]), 8192, ks), kmajor_desc(k0, 8192, ks),
@@ -508,6 +504,20 @@ __device__ bool chain_chunk(const FwdParams& p, ChainCtx& cx, float* S, int gc, 
           uint4 w = make_uint4(pack_bf16x2(-v[8 * u + 0], -v[8 * u + 1]), pack_bf16x2(-v[8 * u + 2], -v[8 * u + 3]),
                                pack_bf16x2(-v[8 * u + 4], -v[8 * u + 5]), pack_bf16x2(-v[8 * u + 6], -v[8 * u + 7]));
           *reinterpret_cast<uint4*>(sm.qw[cx.half] + r * 128 + ((cj ^ (r & 7)) << 4)) = w;
+          if (kComp) {
+            // -W lo in rows 0-63 (the Q~ rows, idle in this mode)
+            const __nv_bfloat162* hb = reinterpret_cast<const __nv_bfloat162*>(&w);
+            float lo[8];
+#pragma unroll
+            for (int x = 0; x < 4; ++x) {
+              const float2 hf = __bfloat1622float2(hb[x]);
+              lo[2 * x] = -v[8 * u + 2 * x] - hf.x;
+              lo[2 * x + 1] = -v[8 * u + 2 * x + 1] - hf.y;
+            }
+            *reinterpret_cast<uint4*>(sm.qw[cx.half] + i * 128 + ((cj ^ (i & 7)) << 4)) =
+                make_uint4(pack_bf16x2(lo[0], lo[1]), pack_bf16x2(lo[2], lo[3]), pack_bf16x2(lo[4], lo[5]),
+                           pack_bf16x2(lo[6], lo[7]));
+          }
         }
       }
     }
@@ -544,9 +554,24 @@ __device__ bool chain_chunk(const FwdParams& p, ChainCtx& cx, float* S, int gc, 
       for (int ks = 0; ks < 4; ++ks)
         umma_bf16(cx.tmem + kTmD1, kmajor_desc(smem_u32(sm.z), 16384, ks), mnmajor_desc(smem_u32(sm.v[0]), 8192, ks),
                   idesc_bf16(128, 128, 0, 1), ks > 0);
+    if (kComp && kWithU)
+      for (int ks = 0; ks < 4; ++ks)
+        umma_bf16(cx.tmem + kTmD1, kmajor_desc(smem_u32(sm.z2), 16384, ks), mnmajor_desc(smem_u32(sm.v[0]), 8192, ks),
+                  idesc_bf16(128, 128, 0, 1), 1);
     for (int ks = 0; ks < 8; ++ks)
       umma_bf16(cx.tmem + kTmD1, kmajor_desc(smem_u32(sm.qw[0]), 16384, ks),
                 mnmajor_desc(smem_u32(sm.s[0]), 16384, ks), idesc_bf16(128, 128, 0, 1), (kWithU || ks > 0) ? 1 : 0);
+    if (kComp) {
+      // compensated W S: + (-W hi) S lo + (-W lo) S hi. The second A operand starts 8 KB before
+      // sm.qw so that its rows 64-127 are the -W lo rows; its rows 0-63 feed unused accumulator rows.
+      const uint32_t slo_lbo = smem_u32(sm.vo[0]) - smem_u32(sm.q[0]);
+      for (int ks = 0; ks < 8; ++ks)
+        umma_bf16(cx.tmem + kTmD1, kmajor_desc(smem_u32(sm.qw[0]), 16384, ks),
+                  mnmajor_desc(smem_u32(sm.q[0]), slo_lbo, ks), idesc_bf16(128, 128, 0, 1), 1);
+      for (int ks = 0; ks < 8; ++ks)
+        umma_bf16(cx.tmem + kTmD1, kmajor_desc(smem_u32(sm.qw[0]) - 8192, 16384, ks),
+                  mnmajor_desc(smem_u32(sm.s[0]), 16384, ks), idesc_bf16(128, 128, 0, 1), 1);
+    }
     umma_commit(cx.bar_mma);
   }
   if (!wait_all(cx.bar_mma, cx.ph_mma)) return false;
@@ -571,16 +596,37 @@ __device__ bool chain_chunk(const FwdParams& p, ChainCtx& cx, float* S, int gc, 
         *reinterpret_cast<uint4*>(sm.vs[cx.half] + off) =
             make_uint4(pack_bf16x2(x[0] * sc, x[1] * sc), pack_bf16x2(x[2] * sc, x[3] * sc),
                        pack_bf16x2(x[4] * sc, x[5] * sc), pack_bf16x2(x[6] * sc, x[7] * sc));
+        if (kComp) {
+          float lo[8], los[8];
+#pragma unroll
+          for (int u2 = 0; u2 < 8; ++u2) {
+            const float xs = x[u2] * sc;
+            lo[u2] = x[u2] - __bfloat162float(__float2bfloat16_rn(x[u2]));
+            los[u2] = xs - __bfloat162float(__float2bfloat16_rn(xs));
+          }
+          *reinterpret_cast<uint4*>(sm.vs_lo[cx.half] + off) =
+              make_uint4(pack_bf16x2(los[0], los[1]), pack_bf16x2(los[2], los[3]), pack_bf16x2(los[4], los[5]),
+                         pack_bf16x2(los[6], los[7]));
+          if (kStore)
+            *reinterpret_cast<uint4*>(p.vp_lo_img + ((size_t)gc * Hv + h) * 16384 + cx.half * 8192 + off) =
+                make_uint4(pack_bf16x2(lo[0], lo[1]), pack_bf16x2(lo[2], lo[3]), pack_bf16x2(lo[4], lo[5]),
+                           pack_bf16x2(lo[6], lo[7]));
+        }
       }
     }
   }
   sync_generic_to_async();
+  if (kStore) copy_smem_to_global(p.vp_img + ((size_t)gc * Hv + h) * 16384, sm.vo[0], 16384, cx.tid);
 
   // -- MMA group 3: D2 = K^T V's ; D1 += [P; 0] V'
   if (cx.tid == 0) {
     for (int ks = 0; ks < 4; ++ks)
       umma_bf16(cx.tmem + kTmD2, mnmajor_desc(smem_u32(sm.k[0]), 8192, ks), mnmajor_desc(smem_u32(sm.vs[0]), 8192, ks),
                 idesc_bf16(128, 128, 1, 1), ks > 0);
+    if (kComp)
+      for (int ks = 0; ks < 4; ++ks)
+        umma_bf16(cx.tmem + kTmD2, mnmajor_desc(smem_u32(sm.k[0]), 8192, ks),
+                  mnmajor_desc(smem_u32(sm.vs_lo[0]), 8192, ks), idesc_bf16(128, 128, 1, 1), 1);
     if (kOut)
       for (int ks = 0; ks < 4; ++ks)
         umma_bf16(cx.tmem + kTmD1, kmajor_desc(smem_u32(sm.p), 16384, ks), mnmajor_desc(smem_u32(sm.vo[0]), 8192, ks),
@@ -638,25 +684,53 @@ __device__ __forceinline__ void save_state(const ChainCtx& cx, float* dst, const
   for (int c = 0; c < 64; c += 4) *reinterpret_cast<float4*>(row + c) = make_float4(S[c], S[c + 1], S[c + 2], S[c + 3]);
 }
 
-// S_end = M S_start + B through one UMMA (M staged as bf16 in sm.qw, S_start in sm.s).
-__device__ bool affine_apply(const FwdParams& p, ChainCtx& cx, const float* Mm, const float* Bm, float* out) {
+// S_end = M S_start + B on the tensor cores with compensated bf16 operands (x = hi + lo):
+// M hi S hi + M hi S lo + M lo S hi. At the start of an item every staging buffer except sm.s
+// (S_start hi) is idle: M hi goes to sm.qw, M lo to sm.q / sm.vo, S lo to sm.v / sm.vs.
+__device__ bool affine_apply(const FwdParams& p, ChainCtx& cx, const float* Mm, const float* Bm, const float* S,
+                             float* out) {
   ChainSmem& sm = *cx.sm;
   {
     const int r = cx.tid >> 1, c0 = (cx.tid & 1) * 64;
     const float* row = Mm + (size_t)r * kDim + c0;
-    uint8_t* blk = sm.qw[c0 >> 6];
+    uint8_t* bhi = sm.qw[c0 >> 6];
+    uint8_t* blo = (c0 == 0) ? sm.q[0] : sm.vo[0];
     for (int cj = 0; cj < 8; ++cj) {
-      float4 a = __ldcg(reinterpret_cast<const float4*>(row + 8 * cj));
-      float4 b = __ldcg(reinterpret_cast<const float4*>(row + 8 * cj + 4));
-      *reinterpret_cast<uint4*>(blk + r * 128 + ((cj ^ (r & 7)) << 4)) =
-          make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w), pack_bf16x2(b.x, b.y), pack_bf16x2(b.z, b.w));
+      float x[8], lo[8];
+      const float4 a = __ldcg(reinterpret_cast<const float4*>(row + 8 * cj));
+      const float4 b = __ldcg(reinterpret_cast<const float4*>(row + 8 * cj + 4));
+      x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+      for (int u = 0; u < 8; ++u) lo[u] = x[u] - __bfloat162float(__float2bfloat16_rn(x[u]));
+      const uint32_t off = r * 128 + ((cj ^ (r & 7)) << 4);
+      *reinterpret_cast<uint4*>(bhi + off) = make_uint4(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]),
+                                                        pack_bf16x2(x[4], x[5]), pack_bf16x2(x[6], x[7]));
+      *reinterpret_cast<uint4*>(blo + off) = make_uint4(pack_bf16x2(lo[0], lo[1]), pack_bf16x2(lo[2], lo[3]),
+                                                        pack_bf16x2(lo[4], lo[5]), pack_bf16x2(lo[6], lo[7]));
+    }
+    // S lo (this thread's row of S_start, 64 columns of dv block `half`)
+    const int rr = 32 * cx.q4 + cx.lane;
+    uint8_t* slo = cx.half == 0 ? sm.v[0] : sm.vs[0];
+    for (int cj = 0; cj < 8; ++cj) {
+      float lo[8];
+      for (int u = 0; u < 8; ++u) lo[u] = S[8 * cj + u] - __bfloat162float(__float2bfloat16_rn(S[8 * cj + u]));
+      *reinterpret_cast<uint4*>(slo + rr * 128 + ((cj ^ (rr & 7)) << 4)) =
+          make_uint4(pack_bf16x2(lo[0], lo[1]), pack_bf16x2(lo[2], lo[3]), pack_bf16x2(lo[4], lo[5]),
+                     pack_bf16x2(lo[6], lo[7]));
     }
   }
   sync_generic_to_async();
   if (cx.tid == 0) {
+    const uint32_t m_lo_stride = smem_u32(sm.vo[0]) - smem_u32(sm.q[0]);
+    const uint32_t s_lo_lbo = smem_u32(sm.vs[0]) - smem_u32(sm.v[0]);
     for (int ks = 0; ks < 8; ++ks)
       umma_bf16(cx.tmem + kTmD2, kmajor_desc(smem_u32(sm.qw[0]), 16384, ks), mnmajor_desc(smem_u32(sm.s[0]), 16384, ks),
                 idesc_bf16(128, 128, 0, 1), ks > 0);
+    for (int ks = 0; ks < 8; ++ks)
+      umma_bf16(cx.tmem + kTmD2, kmajor_desc(smem_u32(sm.qw[0]), 16384, ks),
+                mnmajor_desc(smem_u32(sm.v[0]), s_lo_lbo, ks), idesc_bf16(128, 128, 0, 1), 1);
+    for (int ks = 0; ks < 8; ++ks)
+      umma_bf16(cx.tmem + kTmD2, kmajor_desc(smem_u32(sm.q[0]), m_lo_stride, ks),
+                mnmajor_desc(smem_u32(sm.s[0]), 16384, ks), idesc_bf16(128, 128, 0, 1), 1);
     umma_commit(cx.bar_mma);
   }
   if (!wait_all(cx.bar_mma, cx.ph_mma)) return false;
@@ -718,7 +792,10 @@ __global__ void __launch_bounds__(256, 1) chain_kernel(const __grid_constant__ F
     fence_mbar_init();
   }
   // zero blocks: sm.z always; sm.qw rows 0-63 stay zero in pass 1 (no Q~)
-  for (int e = cx.tid; e < 8192 / 16; e += 256) reinterpret_cast<uint4*>(smp->z)[e] = make_uint4(0, 0, 0, 0);
+  for (int e = cx.tid; e < 8192 / 16; e += 256) {
+    reinterpret_cast<uint4*>(smp->z)[e] = make_uint4(0, 0, 0, 0);
+    reinterpret_cast<uint4*>(smp->z2)[e] = make_uint4(0, 0, 0, 0);
+  }
   if (kMode == kModeP1)
     for (int e = cx.tid; e < 2 * 16384 / 16; e += 256) reinterpret_cast<uint4*>(smp->qw)[e] = make_uint4(0, 0, 0, 0);
   if (cx.warp == 0) tmem_alloc(&tmem_holder, 512);
@@ -768,10 +845,13 @@ __global__ void __launch_bounds__(256, 1) chain_kernel(const __grid_constant__ F
       sync_generic_to_async();
       for (int c = 0; c < nch && ok; ++c) {
         const int gc = c0 + c;
+        const bool comp = p.st_img != nullptr;  // backward recompute: compensated arithmetic
         if (part == 0)
-          ok = chain_chunk<false, false>(p, cx, S, gc, h, hk, ctok[gc], clen[gc]);
+          ok = comp ? chain_chunk<false, false, false, true>(p, cx, S, gc, h, hk, ctok[gc], clen[gc])
+                    : chain_chunk<false, false>(p, cx, S, gc, h, hk, ctok[gc], clen[gc]);
         else
-          ok = chain_chunk<false, true>(p, cx, S, gc, h, hk, ctok[gc], clen[gc]);
+          ok = comp ? chain_chunk<false, true, false, true>(p, cx, S, gc, h, hk, ctok[gc], clen[gc])
+                    : chain_chunk<false, true>(p, cx, S, gc, h, hk, ctok[gc], clen[gc]);
       }
       if (!ok) break;
       float* dst = (part == 0) ? ws_ptr<float>(p, p.L.mmat) : (part == 1) ? ws_ptr<float>(p, p.L.bmat)
@@ -848,17 +928,22 @@ __global__ void __launch_bounds__(256, 1) chain_kernel(const __grid_constant__ F
     // early publication of this segment's end state (exact split)
     if (p.d.mode == 0 && slot[s] >= 0 && dep != -1) {
       const size_t off = ((size_t)slot[s] * Hv + h) * st_elems;
-      if (!affine_apply(p, cx, ws_ptr<float>(p, p.L.mmat) + off, ws_ptr<float>(p, p.L.bmat) + off,
+      if (!affine_apply(p, cx, ws_ptr<float>(p, p.L.mmat) + off, ws_ptr<float>(p, p.L.bmat) + off, S,
                         ws_ptr<float>(p, p.L.pub) + off)) {
         set_status(hd, kErrTimeout);
         break;
       }
       publish(&flags_seg[s * Hv + h]);
     }
-    for (int gc = first_chunk; gc < c0 && ok; ++gc) ok = chain_chunk<false, true>(p, cx, S, gc, h, hk, ctok[gc], clen[gc]);
+    for (int gc = first_chunk; gc < c0 && ok; ++gc)
+      ok = p.st_img ? chain_chunk<false, true, false, true>(p, cx, S, gc, h, hk, ctok[gc], clen[gc])
+                    : chain_chunk<false, true>(p, cx, S, gc, h, hk, ctok[gc], clen[gc]);
     for (int c = 0; c < nch && ok; ++c) {
       const int gc = c0 + c;
-      ok = chain_chunk<true, true>(p, cx, S, gc, h, hk, ctok[gc], clen[gc]);
+      if (p.st_img)
+        ok = chain_chunk<false, true, true>(p, cx, S, gc, h, hk, ctok[gc], clen[gc]);
+      else
+        ok = chain_chunk<true, true>(p, cx, S, gc, h, hk, ctok[gc], clen[gc]);
     }
     if (!ok) {
       set_status(hd, kErrTimeout);

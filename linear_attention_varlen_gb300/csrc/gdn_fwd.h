@@ -24,6 +24,17 @@ struct FwdParams {
   FwdLayout L;
   float trunc_thr;
   float scale;
+  // Backward recompute only (all NULL for a plain forward): per (chunk, value head) records
+  uint8_t* st_img;  // S at each chunk start, bf16, 128B-swizzled smem image [cmax][Hv][32 KB]
+  uint8_t* vp_img;  // V' = U - W S of each chunk, bf16 smem image [cmax][Hv][16 KB]
+  float* t_f32;     // T = (I + A)^{-1}, fp32 [cmax][Hv][64][64]
+  // Compensated bf16 (x = hi + lo, both bf16) for the backward recompute: the low parts of
+  // T diag(beta e^gamma) and T diag(beta) (written by kkt_solve, read by the chain), and of
+  // S and V' (written by the chain for the gradient kernels).
+  uint8_t* tw_lo;      // [cmax][Hv][8 KB]
+  uint8_t* tu_lo;      // [cmax][Hv][8 KB]
+  uint8_t* st_lo_img;  // [cmax][Hv][32 KB]
+  uint8_t* vp_lo_img;  // [cmax][Hv][16 KB]
 };
 
 // events: NULL or cudaEvent_t[2 * 8], recorded around each stage (see gdn_fwd_stage).

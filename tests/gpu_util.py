@@ -77,3 +77,18 @@ def head_slice(p: synth.Problem, heads):
     if q.initial_state is not None:
         q.initial_state = np.ascontiguousarray(q.initial_state)
     return q
+
+
+def run_bwd(p: synth.Problem, options=None):
+    """Backward through the library; returns fp64 numpy dq, dk, dv, dg, dbeta, dinit."""
+    import linear_attention_varlen_gb300 as gdn
+    import torch
+    d = to_device(p)
+    ws = torch.empty(gdn.bwd_workspace_size(p.N, p.T, p.Hk, p.Hv, options), dtype=torch.uint8, device="cuda")
+    gr = gdn.chunk_bwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"], d["dout"], d.get("dfinal_state"),
+                       d["init_idx"], d["initial_state"], options=options, workspace=ws)
+    st = gdn.workspace_status(ws)
+    assert st == 0, f"device status {gdn.status_string(st)}"
+    out = {k: gr[k].double().cpu().numpy() for k in ("dq", "dk", "dv", "dg", "dbeta")}
+    out["dinit"] = None if gr["dinit"] is None else gr["dinit"].double().cpu().numpy()
+    return out
