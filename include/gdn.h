@@ -133,6 +133,24 @@ int gdn_chunk_bwd(const void* q, const void* k, const void* v, const float* g, c
                   float* dinitial_state, void* workspace, size_t ws_bytes, const gdn_options* opt,
                   gdn_stream_t stream);
 
+/* Forward without a workspace argument, for callers that cannot allocate device memory (a host
+ * program with no device allocator of its own, or a plugin inside a framework whose memory pool
+ * owns all device memory). The pages have no counterpart to this entry point. It runs the same
+ * kernels as gdn_chunk_fwd with the scratch in a fixed array of gdn_noalloc_scratch_bytes() bytes
+ * (128 MiB) compiled into the library: every GPU that loads the library holds that array until the
+ * process exits, and every call shares it. Problems whose gdn_fwd_workspace_size() exceeds it return
+ * GDN_ERR_WORKSPACE. Calls that overlap on the GPU race on the array: order them on one stream.
+ * The array needs no clearing (the forward rewrites everything it reads). The first call on each
+ * device looks up the array's device address; make it before any stream capture. Device-side
+ * status: gdn_workspace_status() cannot name this array, so check results through the outputs. */
+int gdn_chunk_fwd_noalloc(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                          const int32_t* cu_seqlens, int N, int T, int H_k, int H_v, int head_dim,
+                          const int32_t* init_idx, const float* initial_state, int n_init, void* out,
+                          float* final_state, const gdn_options* opt, gdn_stream_t stream);
+
+/* Size in bytes of the array gdn_chunk_fwd_noalloc uses. */
+size_t gdn_noalloc_scratch_bytes(void);
+
 /* Copy the workspace's device status word to the host (synchronises `stream`) and return it:
  * GDN_OK or the first device-side error of the last call that used this workspace. */
 int gdn_workspace_status(const void* workspace, gdn_stream_t stream);

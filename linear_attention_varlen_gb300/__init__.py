@@ -27,7 +27,8 @@ CHUNK = 64
 
 # Every symbol include/gdn.h declares.
 EXPORTS = ("gdn_default_options", "gdn_fwd_workspace_size", "gdn_bwd_workspace_size", "gdn_chunk_fwd",
-           "gdn_chunk_bwd", "gdn_workspace_status", "gdn_status_string", "gdn_plan_host")
+           "gdn_chunk_bwd", "gdn_workspace_status", "gdn_status_string", "gdn_plan_host", "gdn_chunk_fwd_noalloc",
+           "gdn_noalloc_scratch_bytes")
 
 
 class GdnError(RuntimeError):
@@ -103,6 +104,10 @@ def load(path: Optional[str] = None):
         lib.gdn_status_string.restype = ctypes.c_char_p
         lib.gdn_plan_host.argtypes = [P, I, I, I, P, I, OP, I, P, P, P, I, P, I, P]
         lib.gdn_plan_host.restype = I
+        lib.gdn_chunk_fwd_noalloc.argtypes = [P, P, P, P, P, P, I, I, I, I, I, P, P, I, P, P, OP, P]
+        lib.gdn_chunk_fwd_noalloc.restype = I
+        lib.gdn_noalloc_scratch_bytes.argtypes = []
+        lib.gdn_noalloc_scratch_bytes.restype = Z
         if path is None:
             _lib = lib
         return lib
