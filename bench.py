@@ -207,11 +207,13 @@ def run_ours(args, rank, world, local_rank):
     d = to_device(p, dev)
     T, Hk, Hv, N = p.T, p.Hk, p.Hv, p.N
     stream = torch.cuda.current_stream()
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * gdn.NUM_STAGES)]
-    for e in ev:
+    ev_f = [torch.cuda.Event(enable_timing=True) for _ in range(2 * gdn.NUM_STAGES)]
+    ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(2 * gdn.NUM_STAGES)]
+    for e in ev_f + ev_b:
         e.record(stream)
     opts = gdn.Options(mode=args.mode)
-    opts_ev = gdn.Options(mode=args.mode, stage_events=ev)
+    opts_f = gdn.Options(mode=args.mode, stage_events=ev_f)
+    opts_b = gdn.Options(mode=args.mode, stage_events=ev_b)
     ws = torch.empty(max(gdn.fwd_workspace_size(N, T, Hk, Hv, opts), gdn.bwd_workspace_size(N, T, Hk, Hv, opts)),
                      dtype=torch.uint8, device=dev)
     out = torch.empty((T, Hv, D), dtype=torch.bfloat16, device=dev)
@@ -230,14 +232,14 @@ def run_ours(args, rank, world, local_rank):
             raise
         has_bwd = False
 
-    def step(o):
-        fwd(o)
+    def step(of, ob):
+        fwd(of)
         if has_bwd:
-            gdn.chunk_bwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"], dout, options=o, workspace=ws)
+            gdn.chunk_bwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"], dout, options=ob, workspace=ws)
 
     flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)  # > 129 MB L2
     for _ in range(args.warmup):
-        step(opts)
+        step(opts, opts)
     torch.cuda.synchronize()
     st = gdn.workspace_status(ws)
     if st != gdn.GDN_OK:
@@ -254,15 +256,18 @@ def run_ours(args, rank, world, local_rank):
         time.sleep(0.3)
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     stops = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    stage_ms = np.zeros((args.steps, gdn.NUM_STAGES))
+    stage_f = np.zeros((args.steps, gdn.NUM_STAGES))
+    stage_b = np.zeros((args.steps, gdn.NUM_STAGES))
     for i in range(args.steps):
         flush.zero_()
         starts[i].record(stream)
-        step(opts_ev)
+        step(opts_f, opts_b)
         stops[i].record(stream)
         stops[i].synchronize()
-        for s in range(gdn.NUM_STAGES):
-            stage_ms[i, s] = ev[2 * s].elapsed_time(ev[2 * s + 1])
+        for s_ in range(gdn.NUM_STAGES):
+            stage_f[i, s_] = ev_f[2 * s_].elapsed_time(ev_f[2 * s_ + 1])
+            if has_bwd and s_ <= gdn.STAGE_DINIT:
+                stage_b[i, s_] = ev_b[2 * s_].elapsed_time(ev_b[2 * s_ + 1])
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
@@ -275,13 +280,22 @@ def run_ours(args, rank, world, local_rank):
         ms = float(t.item())
     value = T * world / (ms * 1e-3) / 1e6
 
-    # e2e: the same step through the public API from pinned host buffers, copies inside
+    # e2e: the same step through the public API from pinned host buffers, copies inside the timed
+    # region: inputs (and the output gradient) host->device, outputs (and the gradients) device->host
     host = {k: v.detach().cpu().pin_memory() for k, v in d.items() if v is not None}
+    if has_bwd:
+        host["dout"] = dout.cpu().pin_memory()
     out_h = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
     fin_h = torch.empty(fin.shape, dtype=fin.dtype, pin_memory=True)
+    grad_h = {}
+    if has_bwd:
+        for k2, shape in (("dq", d["q"].shape), ("dk", d["k"].shape), ("dv", d["v"].shape), ("dg", (T, Hv)),
+                          ("dbeta", (T, Hv))):
+            grad_h[k2] = torch.empty(shape, dtype=torch.float32, pin_memory=True)
     dev_in = {k: torch.empty_like(v, device=dev) for k, v in host.items()}
     h2d = sum(v.numel() * v.element_size() for v in host.values())
-    d2h = out.numel() * out.element_size() + fin.numel() * fin.element_size()
+    d2h = (out.numel() * out.element_size() + fin.numel() * fin.element_size()
+           + sum(v.numel() * v.element_size() for v in grad_h.values()))
     e2e_steps = max(3, min(args.steps, 50))
     torch.cuda.synchronize()
     ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -293,6 +307,11 @@ def run_ours(args, rank, world, local_rank):
                       None, options=opts, out=out, final_state=fin, workspace=ws)
         out_h.copy_(out, non_blocking=True)
         fin_h.copy_(fin, non_blocking=True)
+        if has_bwd:
+            gr = gdn.chunk_bwd(dev_in["q"], dev_in["k"], dev_in["v"], dev_in["g"], dev_in["beta"],
+                               dev_in["cu_seqlens"], dev_in["dout"], options=opts, workspace=ws)
+            for k2, v2 in grad_h.items():
+                v2.copy_(gr[k2], non_blocking=True)
     eb.record(stream)
     torch.cuda.synchronize()
     e2e_ms = ea.elapsed_time(eb) / e2e_steps
@@ -303,7 +322,12 @@ def run_ours(args, rank, world, local_rank):
     peaks = load_peaks()
     names = {gdn.STAGE_PLAN: "plan_kernel", gdn.STAGE_KKT_SOLVE: "kkt_solve_kernel",
              gdn.STAGE_SPLIT: "chain_kernel<pass1>", gdn.STAGE_CHAIN: "chain_kernel<out>"}
-    avg = stage_ms.mean(axis=0)
+    bnames = {gdn.STAGE_PLAN: "plan_kernel", gdn.STAGE_KKT_SOLVE: "kkt_solve_kernel",
+              gdn.STAGE_SPLIT: "chain_kernel<pass1,record>", gdn.STAGE_CHAIN: "chain_kernel<out,record>",
+              gdn.STAGE_REV_CHAIN: "rev_chain_kernel", gdn.STAGE_GRADS: "grad_kernel+dq_kernel",
+              gdn.STAGE_DINIT: "dinit_reduce_kernel"}
+    avg = stage_f.mean(axis=0)
+    bavg = stage_b.mean(axis=0)
     dom = int(np.argmax(avg[:4]))
     fb, ff = algorithmic_fwd(T, Hk, Hv, N)
     # The chain kernel reads q, k, v and writes o and the final state: the forward's algorithmic bytes.
@@ -317,6 +341,8 @@ def run_ours(args, rank, world, local_rank):
         achieved, peak, unit_r = ff / kern_s / 1e12, peaks["tc_sus"], "TFLOP/s"
     tr = traffic_record(os.path.join(ROOT, "linear_attention_varlen_gb300", "csrc", "gdn_fwd.cu"))
     launches_per_step = 3 + (1 if split_launched else 0)
+    if has_bwd:  # recompute (same launches as the forward) + reverse chain, grad, dq kernels
+        launches_per_step += 3 + (1 if split_launched else 0) + 3
     fwd_ms = float(avg[:4].sum())
     res = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -333,7 +359,9 @@ def run_ours(args, rank, world, local_rank):
                      "algorithmic_bytes": fb, "algorithmic_flops": ff},
         "step_roofline": {"bound": bound, "frac": (max(hbm_t, tc_t) / (fwd_ms * 1e-3)),
                           "note": "forward algorithmic time at measured peaks / whole forward time"},
-        "stages_ms": {names[s]: float(avg[s]) for s in range(4)},
+        "stages_ms": {names[s_]: float(avg[s_]) for s_ in range(4)},
+        "bwd_stages_ms": ({bnames[s_]: float(bavg[s_]) for s_ in range(7)} if has_bwd else None),
+        "fwd_ms": fwd_ms, "bwd_ms": (float(bavg[:7].sum()) if has_bwd else None),
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
         "gpu_launches": int(launches_per_step * args.steps),
         "clocks": clk,

@@ -123,6 +123,8 @@ __global__ void __launch_bounds__(1024) plan_kernel(const __grid_constant__ FwdP
   int32_t* ff = ws_ptr<int32_t>(p, p.L.flags_fin);
   for (int e = tid; e < total_segs * p.d.Hv; e += nt) fs[e] = 0;
   for (int e = tid; e < N * p.d.Hv; e += nt) ff[e] = 0;
+  int32_t* mz = ws_ptr<int32_t>(p, p.L.mzero);
+  for (int e = tid; e < (int)p.L.slots * p.d.Hv; e += nt) mz[e] = 0;
   __syncthreads();
   // slots and pass-1 units (serial: only split segments get them)
   if (tid == 0) {
@@ -366,7 +368,6 @@ struct ChainSmem {
   uint8_t vs_lo[2][8192]; // low part of diag(e^{gamma_C - gamma}) V'
   float gam[64];
 };
-constexpr size_t kChainSmemBytes = sizeof(ChainSmem) + 1024;
 
 // TMEM columns.
 constexpr uint32_t kTmD1 = 0;    // [Q~ S + P V' ; U - W S]   (M = 128, 128 cols)
@@ -375,7 +376,8 @@ constexpr uint32_t kTmW = 256;   // W                         (M = 64, 128 cols)
 constexpr uint32_t kTmG = 384;   // Q K^T                     (M = 64, 64 cols)
 
 struct ChainCtx {
-  ChainSmem* sm;
+  ChainSmem* sm;   // record-mode layout
+  uint8_t* base;   // 1024-aligned dynamic shared memory (both layouts start here)
   uint64_t* bar_ld;
   uint64_t* bar_mma;
   uint32_t tmem;
@@ -384,9 +386,10 @@ struct ChainCtx {
 };
 
 // Write this thread's 64 state values (row dk = 32*q4 + lane, columns 64*half ..) as bf16 into sm.s.
-__device__ __forceinline__ void store_state_bf16(ChainCtx& cx, const float* S) {
+template <class SM>
+__device__ __forceinline__ void store_state_bf16_to(SM& sm, const ChainCtx& cx, const float* S) {
   const int r = 32 * cx.q4 + cx.lane;
-  uint8_t* blk = cx.sm->s[cx.half];
+  uint8_t* blk = sm.s[cx.half];
 #pragma unroll
   for (int cj = 0; cj < 8; ++cj) {
     uint4 w = make_uint4(pack_bf16x2(S[8 * cj + 0], S[8 * cj + 1]), pack_bf16x2(S[8 * cj + 2], S[8 * cj + 3]),
@@ -394,13 +397,8 @@ __device__ __forceinline__ void store_state_bf16(ChainCtx& cx, const float* S) {
     *reinterpret_cast<uint4*>(blk + r * 128 + ((cj ^ (r & 7)) << 4)) = w;
   }
 }
+__device__ __forceinline__ void store_state_bf16(ChainCtx& cx, const float* S) { store_state_bf16_to(*cx.sm, cx, S); }
 
-
-// One chunk of the chain. S: this thread's 64 fp32 state values (updated in place).
-// Returns false if a bounded wait ran out (status already set).
-// kOut: write O; kWithU: include the U = T diag(beta) V term (off only for the transition chain M);
-// kStore: record S, V' and their low parts for the backward; kComp: compensated bf16 operands
-// (x = hi + lo) for T diag(beta e^gamma), T diag(beta), W, S and diag(e^{gamma_C - gamma}) V'.
 template <bool kOut, bool kWithU, bool kStore = false, bool kComp = kStore>
 __device__ bool chain_chunk(const FwdParams& p, ChainCtx& cx, float* S, int gc, int h, int hk, int tok0, int n) {
   ChainSmem& sm = *cx.sm;
@@ -684,13 +682,13 @@ __device__ __forceinline__ void save_state(const ChainCtx& cx, float* dst, const
   for (int c = 0; c < 64; c += 4) *reinterpret_cast<float4*>(row + c) = make_float4(S[c], S[c + 1], S[c + 2], S[c + 3]);
 }
 
-// S_end = M S_start + B on the tensor cores with compensated bf16 operands (x = hi + lo):
+// out = M S_start + B (B may be null) on the tensor cores with compensated bf16 operands (x = hi + lo):
 // M hi S hi + M hi S lo + M lo S hi. At the start of an item every staging buffer except sm.s
 // (S_start hi) is idle: M hi goes to sm.qw, M lo to sm.q / sm.vo, S lo to sm.v / sm.vs.
-__device__ bool affine_apply(const FwdParams& p, ChainCtx& cx, const float* Mm, const float* Bm, const float* S,
-                             float* out) {
-  ChainSmem& sm = *cx.sm;
-  {
+template <class SM>
+__device__ bool affine_apply(const FwdParams& p, ChainCtx& cx, SM& sm, const float* Mm, const float* Bm,
+                             const float* S, float* out) {
+  if (cx.tid < 256) {
     const int r = cx.tid >> 1, c0 = (cx.tid & 1) * 64;
     const float* row = Mm + (size_t)r * kDim + c0;
     uint8_t* bhi = sm.qw[c0 >> 6];
@@ -708,7 +706,7 @@ __device__ bool affine_apply(const FwdParams& p, ChainCtx& cx, const float* Mm, 
                                                         pack_bf16x2(lo[4], lo[5]), pack_bf16x2(lo[6], lo[7]));
     }
     // S lo (this thread's row of S_start, 64 columns of dv block `half`)
-    const int rr = 32 * cx.q4 + cx.lane;
+    const int rr = 32 * cx.q4 + cx.lane;  // (threads below 256 only)
     uint8_t* slo = cx.half == 0 ? sm.v[0] : sm.vs[0];
     for (int cj = 0; cj < 8; ++cj) {
       float lo[8];
@@ -736,23 +734,334 @@ __device__ bool affine_apply(const FwdParams& p, ChainCtx& cx, const float* Mm, 
   if (!wait_all(cx.bar_mma, cx.ph_mma)) return false;
   cx.ph_mma ^= 1;
   tc_fence_after();
-  const uint32_t lane_base = (uint32_t)(32 * cx.q4) << 16;
-  const int r = 32 * cx.q4 + cx.lane;
-  for (int cc = 0; cc < 64; cc += 16) {
-    float v[16];
-    tmem_ld16(cx.tmem + kTmD2 + lane_base + 64 * cx.half + cc, v);
-    tmem_ld_wait();
-    const float* brow = Bm + (size_t)r * kDim + 64 * cx.half + cc;
-    float* orow = out + (size_t)r * kDim + 64 * cx.half + cc;
-    for (int x = 0; x < 16; x += 4) {
-      float4 b = __ldcg(reinterpret_cast<const float4*>(brow + x));
-      *reinterpret_cast<float4*>(orow + x) = make_float4(v[x] + b.x, v[x + 1] + b.y, v[x + 2] + b.z, v[x + 3] + b.w);
+  if (cx.tid < 256) {
+    const uint32_t lane_base = (uint32_t)(32 * cx.q4) << 16;
+    const int r = 32 * cx.q4 + cx.lane;
+    for (int cc = 0; cc < 64; cc += 16) {
+      float v[16];
+      tmem_ld16(cx.tmem + kTmD2 + lane_base + 64 * cx.half + cc, v);
+      tmem_ld_wait();
+      float* orow = out + (size_t)r * kDim + 64 * cx.half + cc;
+      for (int x = 0; x < 16; x += 4) {
+        float4 b = Bm ? __ldcg(reinterpret_cast<const float4*>(Bm + (size_t)r * kDim + 64 * cx.half + cc + x))
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
+        *reinterpret_cast<float4*>(orow + x) = make_float4(v[x] + b.x, v[x + 1] + b.y, v[x + 2] + b.z, v[x + 3] + b.w);
+      }
     }
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   return true;
+}
+
+
+// =========================================================================== warp-specialized chain
+//
+// The forward chain with three roles in one CTA of 10 warps:
+//   warp 8      TMA producer: K, V, T_u and gamma of chunk j into stage j & 1; Q and T_w (one buffer).
+//   warp 9      MMA issuer (one lane), per chunk j:
+//                 U = [*; T_u] V -> D2 rows 64-127, D1 = [Q~; -W] S, then chunk j+1's W = T_w K and
+//                 Q K^T (staged by the epilogue while chunk j runs), then D2 = K^T V'_s, D1 += [P; *] V'.
+//   warps 0-7   epilogue: V' = U - W S, staging of chunk j+1 (-W, P, Q~), S += K^T V'_s, O.
+// Hand-offs are mbarriers only: tcgen05.commit from the issuer, one elected arrival from the
+// epilogue after a named barrier, TMA transaction counts from the producer. Rows 0-63 of the U
+// product and rows 64-127 of the P product are never read, so neither operand needs zero rows.
+
+struct WsSmem {
+  uint8_t k[2][16384];   // [stage] K rows t, two dk blocks     (B K-major, B MN-major, A MN-major)
+  uint8_t v[2][16384];   // [stage] V rows t, two dv blocks     (B MN-major)
+  uint8_t q[2][8192];    // Q rows t, two dk blocks (one buffer) (A K-major)
+  uint8_t pt[4][8192];   // P stage 0, P stage 1, T_u stage 0, T_u stage 1 (contiguous)
+  uint8_t tw[8192];      // T diag(beta e^gamma) (one buffer)  (A, M = 64)
+  uint8_t qw[2][16384];  // dk block b: rows 0-63 Q~, rows 64-127 -W   (A, M = 128)
+  uint8_t vo[2][8192];   // V'                                  (B MN-major)
+  uint8_t vs[2][8192];   // diag(e^{gamma_C - gamma}) V'        (B MN-major)
+  uint8_t s[2][16384];   // S bf16 rows dk                      (B MN-major)
+  float gam[2][64];      // [stage] chunk-local cumulative gate
+};
+constexpr size_t kSmemBytes = (sizeof(WsSmem) > sizeof(ChainSmem) ? sizeof(WsSmem) : sizeof(ChainSmem)) + 1024;
+constexpr int kWsThreads = 320;
+
+struct WsBars {
+  uint64_t full[2], fullq, empty[2], emptyq, a_done, pre_done, b_done, epi1, staged, epi2;
+};
+struct WsPhase {
+  uint32_t full[2], fullq, empty[2], emptyq, a_done, pre_done, b_done, epi1, staged, epi2;
+};
+
+__device__ __forceinline__ void e_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+
+// Bounded wait that never diverges: after the first failure (recorded in *abort) every later
+// wait returns at once, so all threads keep executing the same barriers.
+__device__ __forceinline__ void role_wait(uint64_t* bar, uint32_t& ph, volatile int* abort) {
+  if (!*abort && !mbar_wait(bar, ph, kWaitBudget)) *abort = 1;
+  ph ^= 1;
+  tc_fence_after();
+}
+
+// Epilogue hand-off: make this thread's shared-memory writes visible to the async proxy and its
+// TMEM reads ordered, meet the other epilogue threads, then one thread arrives on each barrier.
+__device__ __forceinline__ void e_handoff(int tid, uint64_t* b1, uint64_t* b2 = nullptr) {
+  fence_proxy_async_smem();
+  tc_fence_before();
+  e_sync();
+  if (tid == 0) {
+    mbar_arrive(b1);
+    if (b2) mbar_arrive(b2);
+  }
+}
+
+// Run chunks [gc0, gc1) of one document for value head h from S (epilogue registers; its bf16
+// copy is already in sm.s). Chunks gc >= gc_out write O. kWithU = false runs the transition
+// chain (no U term, no output). All 320 threads call this; returns false after a failed wait.
+template <bool kWithU>
+__device__ bool run_ws(const FwdParams& p, ChainCtx& cx, WsBars& bb, WsPhase& ph, volatile int* abort, float* S,
+                       int gc0, int gc1, int gc_out, int h, int hk) {
+  WsSmem& sm = *reinterpret_cast<WsSmem*>(cx.base);
+  const int n = gc1 - gc0;
+  if (n <= 0) return true;
+  const int Hv = p.d.Hv;
+  const int32_t* ctok = ws_ptr<int32_t>(p, p.L.chunk_tok0);
+  const int32_t* clen = ws_ptr<int32_t>(p, p.L.chunk_len);
+
+  if (cx.warp == 8) {
+    // ------------------------------------------------------------------ TMA producer
+    if (cx.lane == 0) {
+      for (int j = 0; j < n; ++j) {
+        const int gc = gc0 + j, st = j & 1, tok0 = ctok[gc];
+        const bool out = gc >= gc_out;
+        if (j >= 2) role_wait(&bb.empty[st], ph.empty[st], abort);
+        if (*abort) break;
+        mbar_arrive_expect_tx(&bb.full[st], 16384 + 256 + (kWithU ? 16384 + 8192 : 0));
+        tma_load_3d(sm.k[st], &p.tm_k, 0, hk, tok0, &bb.full[st]);
+        tma_load_3d(sm.k[st] + 8192, &p.tm_k, 64, hk, tok0, &bb.full[st]);
+        if (kWithU) {
+          tma_load_3d(sm.v[st], &p.tm_v, 0, h, tok0, &bb.full[st]);
+          tma_load_3d(sm.v[st] + 8192, &p.tm_v, 64, h, tok0, &bb.full[st]);
+          bulk_load(sm.pt[2 + st], p.ws + p.L.tu + ((size_t)gc * Hv + h) * 8192, 8192, &bb.full[st]);
+        }
+        bulk_load(sm.gam[st], p.ws + p.L.gam + ((size_t)gc * Hv + h) * 256, 256, &bb.full[st]);
+        if (j >= 1) role_wait(&bb.emptyq, ph.emptyq, abort);
+        if (*abort) break;
+        mbar_arrive_expect_tx(&bb.fullq, 8192 + (out ? 16384 : 0));
+        if (out) {
+          tma_load_3d(sm.q[0], &p.tm_q, 0, hk, tok0, &bb.fullq);
+          tma_load_3d(sm.q[1], &p.tm_q, 64, hk, tok0, &bb.fullq);
+        }
+        bulk_load(sm.tw, p.ws + p.L.tw + ((size_t)gc * Hv + h) * 8192, 8192, &bb.fullq);
+      }
+      // drain: wait for the release of the last uses so that every phase is consumed
+      for (int j = (n >= 2 ? n - 2 : 0); j < n; ++j) role_wait(&bb.empty[j & 1], ph.empty[j & 1], abort);
+      role_wait(&bb.emptyq, ph.emptyq, abort);
+    }
+    return !*abort;
+  }
+  if (cx.warp == 9) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (cx.lane == 0) {
+      const uint32_t tm = cx.tmem;
+      auto prep = [&](int j) {
+        const int st = j & 1;
+        const uint32_t k0 = smem_u32(sm.k[st]);
+        for (int ks = 0; ks < 4; ++ks)
+          umma_bf16(tm + kTmW, kmajor_desc(smem_u32(sm.tw), 8192, ks), mnmajor_desc(k0, 8192, ks),
+                    idesc_bf16(64, 128, 0, 1), ks > 0);
+        if (gc0 + j >= gc_out)
+          for (int ks = 0; ks < 8; ++ks)
+            umma_bf16(tm + kTmG, kmajor_desc(smem_u32(sm.q[0]), 8192, ks), kmajor_desc(k0, 8192, ks),
+                      idesc_bf16(64, 64, 0, 0), ks > 0);
+        umma_commit(&bb.pre_done);
+        umma_commit(&bb.emptyq);
+      };
+      role_wait(&bb.full[0], ph.full[0], abort);
+      role_wait(&bb.fullq, ph.fullq, abort);
+      if (!*abort) prep(0);
+      for (int j = 0; j < n && !*abort; ++j) {
+        const int st = j & 1;
+        const bool out = gc0 + j >= gc_out;
+        role_wait(&bb.staged, ph.staged, abort);
+        role_wait(&bb.epi2, ph.epi2, abort);
+        if (*abort) break;
+        if (kWithU)
+          for (int ks = 0; ks < 4; ++ks)
+            umma_bf16(tm + kTmD2, kmajor_desc(smem_u32(sm.pt[1 + st]), 16384, ks),
+                      mnmajor_desc(smem_u32(sm.v[st]), 8192, ks), idesc_bf16(128, 128, 0, 1), ks > 0);
+        for (int ks = 0; ks < 8; ++ks)
+          umma_bf16(tm + kTmD1, kmajor_desc(smem_u32(sm.qw[0]), 16384, ks), mnmajor_desc(smem_u32(sm.s[0]), 16384, ks),
+                    idesc_bf16(128, 128, 0, 1), ks > 0);
+        umma_commit(&bb.a_done);
+        if (j + 1 < n) {
+          role_wait(&bb.full[st ^ 1], ph.full[st ^ 1], abort);
+          role_wait(&bb.fullq, ph.fullq, abort);
+          if (*abort) break;
+          prep(j + 1);
+        }
+        role_wait(&bb.epi1, ph.epi1, abort);
+        if (*abort) break;
+        for (int ks = 0; ks < 4; ++ks)
+          umma_bf16(tm + kTmD2, mnmajor_desc(smem_u32(sm.k[st]), 8192, ks), mnmajor_desc(smem_u32(sm.vs[0]), 8192, ks),
+                    idesc_bf16(128, 128, 1, 1), ks > 0);
+        if (out)
+          for (int ks = 0; ks < 4; ++ks)
+            umma_bf16(tm + kTmD1, kmajor_desc(smem_u32(sm.pt[j & 1]), 16384, ks),
+                      mnmajor_desc(smem_u32(sm.vo[0]), 8192, ks), idesc_bf16(128, 128, 0, 1), 1);
+        umma_commit(&bb.b_done);
+        umma_commit(&bb.empty[st]);
+      }
+      role_wait(&bb.epi2, ph.epi2, abort);  // the epilogue's last state hand-off
+    }
+    return !*abort;
+  }
+  // -------------------------------------------------------------------- epilogue warps 0-7
+  const uint32_t lane_base = (uint32_t)(32 * cx.q4) << 16;
+  const int i = 16 * cx.q4 + cx.lane;  // row of M = 64 accumulators (lanes < 16)
+  e_handoff(cx.tid, &bb.epi2);          // S(gc0) is staged
+  auto staging = [&](int j) {
+    const int gc = gc0 + j, st = j & 1;
+    const bool out = gc >= gc_out;
+    role_wait(&bb.full[st], ph.full[st], abort);
+    role_wait(&bb.fullq, ph.fullq, abort);
+    const float* gm = sm.gam[st];
+    if (out) {
+      for (int e = cx.tid; e < 2 * 64 * 8; e += 256) {
+        const int b = e >> 9, r = (e >> 3) & 63, cj = e & 7;
+        const uint32_t off = r * 128 + ((cj ^ (r & 7)) << 4);
+        uint4 raw = *reinterpret_cast<const uint4*>(sm.q[b] + off);
+        const float sc = __expf(gm[r]) * p.scale;
+        __nv_bfloat162* x = reinterpret_cast<__nv_bfloat162*>(&raw);
+        uint32_t w[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          float2 f = __bfloat1622float2(x[u]);
+          w[u] = pack_bf16x2(f.x * sc, f.y * sc);
+        }
+        *reinterpret_cast<uint4*>(sm.qw[b] + off) = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+    }
+    role_wait(&bb.pre_done, ph.pre_done, abort);
+#pragma unroll
+    for (int hc = 0; hc < 2; ++hc) {
+      float v[32];
+      tmem_ld16(cx.tmem + kTmW + lane_base + 64 * cx.half + 32 * hc, v);
+      tmem_ld16(cx.tmem + kTmW + lane_base + 64 * cx.half + 32 * hc + 16, v + 16);
+      tmem_ld_wait();
+      if (cx.lane < 16) {
+        const int r = 64 + i;
+#pragma unroll
+        for (int cj4 = 0; cj4 < 4; ++cj4) {
+          const int cj = 4 * hc + cj4;
+          const float* x = v + 8 * cj4;
+          *reinterpret_cast<uint4*>(sm.qw[cx.half] + r * 128 + ((cj ^ (r & 7)) << 4)) =
+              make_uint4(pack_bf16x2(-x[0], -x[1]), pack_bf16x2(-x[2], -x[3]), pack_bf16x2(-x[4], -x[5]),
+                         pack_bf16x2(-x[6], -x[7]));
+        }
+      }
+    }
+    if (out) {
+      const int nn = clen[gc];
+      float v[32];
+      tmem_ld16(cx.tmem + kTmG + lane_base + 32 * cx.half, v);
+      tmem_ld16(cx.tmem + kTmG + lane_base + 32 * cx.half + 16, v + 16);
+      tmem_ld_wait();
+      if (cx.lane < 16) {
+        const float gi = gm[i];
+        uint8_t* pb = sm.pt[j & 1];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          float pv[8];
+#pragma unroll
+          for (int x = 0; x < 8; ++x) {
+            const int jj = 32 * cx.half + 8 * u + x;
+            pv[x] = (jj <= i && i < nn) ? __expf(gi - gm[jj]) * p.scale * v[8 * u + x] : 0.f;
+          }
+          const int cj = 4 * cx.half + u;
+          *reinterpret_cast<uint4*>(pb + i * 128 + ((cj ^ (i & 7)) << 4)) =
+              make_uint4(pack_bf16x2(pv[0], pv[1]), pack_bf16x2(pv[2], pv[3]), pack_bf16x2(pv[4], pv[5]),
+                         pack_bf16x2(pv[6], pv[7]));
+        }
+      }
+    }
+    e_handoff(cx.tid, &bb.staged, &bb.emptyq);
+  };
+  staging(0);
+  for (int j = 0; j < n; ++j) {
+    const int gc = gc0 + j, st = j & 1;
+    const bool out = gc >= gc_out;
+    role_wait(&bb.a_done, ph.a_done, abort);
+    const float* gm = sm.gam[st];
+    const float gC = gm[63];
+    if (cx.q4 >= 2) {
+      // V' = U - W S, rows t = lanes 64-127
+      const int t = 32 * (cx.q4 - 2) + cx.lane;
+      const float sc = __expf(gC - gm[t]);
+#pragma unroll
+      for (int hc = 0; hc < 2; ++hc) {
+        float v[32];
+        tmem_ld16(cx.tmem + kTmD1 + lane_base + 64 * cx.half + 32 * hc, v);
+        tmem_ld16(cx.tmem + kTmD1 + lane_base + 64 * cx.half + 32 * hc + 16, v + 16);
+        if (kWithU) {
+          float u[32];
+          tmem_ld16(cx.tmem + kTmD2 + lane_base + 64 * cx.half + 32 * hc, u);
+          tmem_ld16(cx.tmem + kTmD2 + lane_base + 64 * cx.half + 32 * hc + 16, u + 16);
+          tmem_ld_wait();
+#pragma unroll
+          for (int x = 0; x < 32; ++x) v[x] += u[x];
+        } else {
+          tmem_ld_wait();
+        }
+#pragma unroll
+        for (int cj4 = 0; cj4 < 4; ++cj4) {
+          const int cj = 4 * hc + cj4;
+          const uint32_t off = t * 128 + ((cj ^ (t & 7)) << 4);
+          const float* x = v + 8 * cj4;
+          *reinterpret_cast<uint4*>(sm.vo[cx.half] + off) =
+              make_uint4(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]), pack_bf16x2(x[4], x[5]), pack_bf16x2(x[6], x[7]));
+          *reinterpret_cast<uint4*>(sm.vs[cx.half] + off) =
+              make_uint4(pack_bf16x2(x[0] * sc, x[1] * sc), pack_bf16x2(x[2] * sc, x[3] * sc),
+                         pack_bf16x2(x[4] * sc, x[5] * sc), pack_bf16x2(x[6] * sc, x[7] * sc));
+        }
+      }
+    }
+    e_handoff(cx.tid, &bb.epi1);
+    if (j + 1 < n) staging(j + 1);
+    role_wait(&bb.b_done, ph.b_done, abort);
+    {
+      const float GC = __expf(gC);
+#pragma unroll
+      for (int hc = 0; hc < 2; ++hc) {
+        float v[32];
+        tmem_ld16(cx.tmem + kTmD2 + lane_base + 64 * cx.half + 32 * hc, v);
+        tmem_ld16(cx.tmem + kTmD2 + lane_base + 64 * cx.half + 32 * hc + 16, v + 16);
+        tmem_ld_wait();
+#pragma unroll
+        for (int x = 0; x < 32; ++x) S[32 * hc + x] = GC * S[32 * hc + x] + v[x];
+      }
+      store_state_bf16_to(sm, cx, S);
+    }
+    if (out && cx.q4 < 2) {
+      const int t = 32 * cx.q4 + cx.lane;
+      const int nn = clen[gc];
+      uint4* dst = reinterpret_cast<uint4*>(p.out + ((size_t)(ctok[gc] + t) * Hv + h) * kDim + 64 * cx.half);
+#pragma unroll
+      for (int hc = 0; hc < 2; ++hc) {
+        float v[32];
+        tmem_ld16(cx.tmem + kTmD1 + lane_base + 64 * cx.half + 32 * hc, v);
+        tmem_ld16(cx.tmem + kTmD1 + lane_base + 64 * cx.half + 32 * hc + 16, v + 16);
+        tmem_ld_wait();
+        if (t < nn) {
+#pragma unroll
+          for (int cj4 = 0; cj4 < 4; ++cj4) {
+            const float* x = v + 8 * cj4;
+            dst[4 * hc + cj4] = make_uint4(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]), pack_bf16x2(x[4], x[5]),
+                                           pack_bf16x2(x[6], x[7]));
+          }
+        }
+      }
+    }
+    e_handoff(cx.tid, &bb.epi2, &bb.empty[st]);
+  }
+  return !*abort;
 }
 
 __device__ __forceinline__ void publish(int* flag) {
@@ -763,16 +1072,25 @@ __device__ __forceinline__ void publish(int* flag) {
   }
 }
 
-template <int kMode>
-__global__ void __launch_bounds__(256, 1) chain_kernel(const __grid_constant__ FwdParams p) {
+// kRec: the backward's recompute (per-chunk path with records and compensated arithmetic, 256
+// threads); otherwise the warp-specialized forward (320 threads).
+constexpr int kTransWindow = 12;  // chunks of the transition evaluated first (see pass 1, part 0)
+
+template <int kMode, bool kRec>
+__global__ void __launch_bounds__(kRec ? 256 : kWsThreads, 1) chain_kernel(const __grid_constant__ FwdParams p) {
   extern __shared__ uint8_t smem_raw[];
-  ChainSmem* smp = reinterpret_cast<ChainSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  ChainSmem* smp = reinterpret_cast<ChainSmem*>(base);
+  WsSmem* wss = reinterpret_cast<WsSmem*>(base);
   __shared__ uint64_t bar_ld, bar_mma;
+  __shared__ WsBars wbars;
   __shared__ uint32_t tmem_holder;
-  __shared__ int s_item, s_ok;
+  __shared__ int s_item, s_ok, s_abort;
   Header* hd = ws_ptr<Header>(p, p.L.header);
+  constexpr bool rec = kRec;
   ChainCtx cx;
   cx.sm = smp;
+  cx.base = base;
   cx.bar_ld = &bar_ld;
   cx.bar_mma = &bar_mma;
   cx.tid = threadIdx.x;
@@ -782,6 +1100,9 @@ __global__ void __launch_bounds__(256, 1) chain_kernel(const __grid_constant__ F
   cx.half = cx.warp >> 2;
   cx.ph_ld = 0;
   cx.ph_mma = 0;
+  const bool epi = cx.warp < 8;  // threads that hold state rows
+  WsPhase ph;
+  memset(&ph, 0, sizeof(ph));
   const int Hv = p.d.Hv, G = p.d.Hv / p.d.Hk;
   const int n_items = (kMode == kModeOut ? hd->n_segs : hd->n_p1) * Hv;
   if (blockIdx.x >= n_items || get_status(hd) != 0) return;
@@ -789,15 +1110,31 @@ __global__ void __launch_bounds__(256, 1) chain_kernel(const __grid_constant__ F
   if (cx.tid == 0) {
     mbar_init(&bar_ld, 1);
     mbar_init(&bar_mma, 1);
+    if (!rec) {
+      mbar_init(&wbars.full[0], 1);
+      mbar_init(&wbars.full[1], 1);
+      mbar_init(&wbars.fullq, 1);
+      mbar_init(&wbars.empty[0], 2);
+      mbar_init(&wbars.empty[1], 2);
+      mbar_init(&wbars.emptyq, 2);
+      mbar_init(&wbars.a_done, 1);
+      mbar_init(&wbars.pre_done, 1);
+      mbar_init(&wbars.b_done, 1);
+      mbar_init(&wbars.epi1, 1);
+      mbar_init(&wbars.staged, 1);
+      mbar_init(&wbars.epi2, 1);
+    }
+    s_abort = 0;
     fence_mbar_init();
   }
-  // zero blocks: sm.z always; sm.qw rows 0-63 stay zero in pass 1 (no Q~)
-  for (int e = cx.tid; e < 8192 / 16; e += 256) {
-    reinterpret_cast<uint4*>(smp->z)[e] = make_uint4(0, 0, 0, 0);
-    reinterpret_cast<uint4*>(smp->z2)[e] = make_uint4(0, 0, 0, 0);
+  if constexpr (rec) {
+    for (int e = cx.tid; e < 8192 / 16; e += 256) {
+      reinterpret_cast<uint4*>(smp->z)[e] = make_uint4(0, 0, 0, 0);
+      reinterpret_cast<uint4*>(smp->z2)[e] = make_uint4(0, 0, 0, 0);
+    }
+    if (kMode == kModeP1)
+      for (int e = cx.tid; e < 2 * 16384 / 16; e += 256) reinterpret_cast<uint4*>(smp->qw)[e] = make_uint4(0, 0, 0, 0);
   }
-  if (kMode == kModeP1)
-    for (int e = cx.tid; e < 2 * 16384 / 16; e += 256) reinterpret_cast<uint4*>(smp->qw)[e] = make_uint4(0, 0, 0, 0);
   if (cx.warp == 0) tmem_alloc(&tmem_holder, 512);
   sync_generic_to_async();
   cx.tmem = tmem_holder;
@@ -809,8 +1146,39 @@ __global__ void __launch_bounds__(256, 1) chain_kernel(const __grid_constant__ F
   const int32_t* clen = ws_ptr<int32_t>(p, p.L.chunk_len);
   int* flags_seg = ws_ptr<int>(p, p.L.flags_seg);
   int* flags_fin = ws_ptr<int>(p, p.L.flags_fin);
+  int* mzero = ws_ptr<int>(p, p.L.mzero);
   const size_t st_elems = (size_t)kDim * kDim;
   float S[64];
+  auto store_s = [&]() {
+    if constexpr (rec)
+      store_state_bf16_to(*smp, cx, S);
+    else if (epi)
+      store_state_bf16_to(*wss, cx, S);
+  };
+  auto set_zero = [&]() {
+    for (int c = 0; c < 64; ++c) S[c] = 0.f;
+  };
+  auto set_identity = [&]() {
+    const int r = 32 * cx.q4 + cx.lane;
+    for (int c = 0; c < 64; ++c) S[c] = (r == 64 * cx.half + c) ? 1.f : 0.f;
+  };
+  auto all_zero = [&]() -> bool {
+    bool mine = true;
+    if (epi)
+      for (int x = 0; x < 64; ++x) mine = mine && (S[x] == 0.f);
+    return __syncthreads_and(mine) != 0;
+  };
+  // forward chain over [g0, g1) with outputs from g_out (warp-specialized path)
+  auto run_fast = [&](int g0, int g1, int g_out, int h, int hk, bool with_u) -> bool {
+    bool ok2;
+    if (with_u)
+      ok2 = run_ws<true>(p, cx, wbars, ph, &s_abort, S, g0, g1, g_out, h, hk);
+    else
+      ok2 = run_ws<false>(p, cx, wbars, ph, &s_abort, S, g0, g1, g_out, h, hk);
+    (void)ok2;
+    __syncthreads();
+    return s_abort == 0;
+  };
 
   for (;;) {
     if (cx.tid == 0) {
@@ -828,35 +1196,73 @@ __global__ void __launch_bounds__(256, 1) chain_kernel(const __grid_constant__ F
       const int s = p1[2 * unit], part = p1[2 * unit + 1];
       const int seq = si[4 * s], c0 = si[4 * s + 1], nch = si[4 * s + 2];
       const int sl = slot[s];
-      // start: identity (part 0), zero (part 1) or the known start state (part 2)
+      float* mdst = ws_ptr<float>(p, p.L.mmat) + ((size_t)sl * Hv + h) * st_elems;
+      bool m_zero = false;
       if (part == 0) {
-        const int r = 32 * cx.q4 + cx.lane;
-        for (int c = 0; c < 64; ++c) S[c] = (r == 64 * cx.half + c) ? 1.f : 0.f;
-      } else if (part == 1) {
-        for (int c = 0; c < 64; ++c) S[c] = 0.f;
+        if constexpr (rec) {
+          set_identity();
+          store_s();
+          sync_generic_to_async();
+          for (int c = 0; c < nch && ok && !m_zero; ++c) {
+            const int gc = c0 + c;
+            ok = chain_chunk<false, false, false, true>(p, cx, S, gc, h, hk, ctok[gc], clen[gc]);
+            m_zero = all_zero();
+          }
+          if (!ok) break;
+          save_state(cx, mdst, S);
+        } else {
+          // Transition M = Phi_last ... Phi_first, evaluated as Y X with Y the product over the
+          // last kTransWindow chunks (a chain from I). When Y is exactly zero so is M, and the
+          // segment boundary needs no start state; otherwise X (chain from I over the first
+          // chunks) and M = Y X.
+          const int w = nch < kTransWindow ? nch : kTransWindow;
+          set_identity();
+          store_s();
+          sync_generic_to_async();
+          if (!run_fast(c0 + nch - w, c0 + nch, c0 + nch, h, hk, false)) break;
+          m_zero = all_zero();
+          if (epi) save_state(cx, mdst, S);
+          if (!m_zero && w < nch) {
+            set_identity();
+            store_s();
+            sync_generic_to_async();
+            if (!run_fast(c0, c0 + nch - w, c0 + nch, h, hk, false)) break;
+            __syncthreads();  // Y is in global memory
+            store_s();        // X (bf16) for the product
+            sync_generic_to_async();
+            if (!affine_apply(p, cx, *wss, mdst, nullptr, S, mdst)) {
+              set_status(hd, kErrTimeout);
+              break;
+            }
+          }
+        }
       } else {
-        const int x = p.init_idx ? p.init_idx[seq] : -1;
-        if (x >= 0 && x < p.d.n_init)
-          load_state(cx, p.initial_state + ((size_t)x * Hv + h) * st_elems, S, false);
-        else
-          for (int c = 0; c < 64; ++c) S[c] = 0.f;
+        if (part == 1) {
+          set_zero();
+        } else {
+          const int x = p.init_idx ? p.init_idx[seq] : -1;
+          if (epi && x >= 0 && x < p.d.n_init)
+            load_state(cx, p.initial_state + ((size_t)x * Hv + h) * st_elems, S, false);
+          else
+            set_zero();
+        }
+        store_s();
+        sync_generic_to_async();
+        if constexpr (rec) {
+          for (int c = 0; c < nch && ok; ++c) {
+            const int gc = c0 + c;
+            ok = chain_chunk<false, true, false, true>(p, cx, S, gc, h, hk, ctok[gc], clen[gc]);
+          }
+        } else {
+          ok = run_fast(c0, c0 + nch, c0 + nch, h, hk, true);
+        }
+        if (!ok) break;
+        float* dst = (part == 1) ? ws_ptr<float>(p, p.L.bmat) : ws_ptr<float>(p, p.L.pub);
+        if (epi) save_state(cx, dst + ((size_t)sl * Hv + h) * st_elems, S);
       }
-      store_state_bf16(cx, S);
-      sync_generic_to_async();
-      for (int c = 0; c < nch && ok; ++c) {
-        const int gc = c0 + c;
-        const bool comp = p.st_img != nullptr;  // backward recompute: compensated arithmetic
-        if (part == 0)
-          ok = comp ? chain_chunk<false, false, false, true>(p, cx, S, gc, h, hk, ctok[gc], clen[gc])
-                    : chain_chunk<false, false>(p, cx, S, gc, h, hk, ctok[gc], clen[gc]);
-        else
-          ok = comp ? chain_chunk<false, true, false, true>(p, cx, S, gc, h, hk, ctok[gc], clen[gc])
-                    : chain_chunk<false, true>(p, cx, S, gc, h, hk, ctok[gc], clen[gc]);
-      }
-      if (!ok) break;
-      float* dst = (part == 0) ? ws_ptr<float>(p, p.L.mmat) : (part == 1) ? ws_ptr<float>(p, p.L.bmat)
-                                                                          : ws_ptr<float>(p, p.L.pub);
-      save_state(cx, dst + ((size_t)sl * Hv + h) * st_elems, S);
+      // A transition that is exactly zero makes the segment's end state its local end state B:
+      // the next segment can start without waiting for this segment's start state.
+      if (part == 0 && m_zero && cx.tid == 0) mzero[sl * Hv + h] = 1;
       if (part == 2) publish(&flags_seg[s * Hv + h]);
       __syncthreads();
       continue;
@@ -870,10 +1276,10 @@ __global__ void __launch_bounds__(256, 1) chain_kernel(const __grid_constant__ F
     bool have_start = true;
     if (dep == -1) {
       const int x = p.init_idx ? p.init_idx[seq] : -1;
-      if (x >= 0 && x < p.d.n_init)
+      if (epi && x >= 0 && x < p.d.n_init)
         load_state(cx, p.initial_state + ((size_t)x * Hv + h) * st_elems, S, false);
       else
-        for (int c = 0; c < 64; ++c) S[c] = 0.f;
+        set_zero();
     } else if (dep <= -2) {
       const int j = dep_fork_seq(dep);
       if (cx.tid == 0) {
@@ -882,15 +1288,22 @@ __global__ void __launch_bounds__(256, 1) chain_kernel(const __grid_constant__ F
       }
       __syncthreads();
       have_start = s_ok != 0;
-      if (have_start) load_state(cx, p.final_state + ((size_t)j * Hv + h) * st_elems, S, true);
+      if (have_start && epi) load_state(cx, p.final_state + ((size_t)j * Hv + h) * st_elems, S, true);
     } else if (p.d.mode == 0) {
-      if (cx.tid == 0) {
-        s_ok = wait_flag(&flags_seg[dep * Hv + h], hd) ? 1 : 0;
-        __threadfence();
+      const int dsl = slot[dep];
+      if (__ldcg(&mzero[dsl * Hv + h])) {
+        // the previous segment's transition is exactly zero: its end state is its local B
+        if (epi) load_state(cx, ws_ptr<float>(p, p.L.bmat) + ((size_t)dsl * Hv + h) * st_elems, S, true);
+      } else {
+        if (cx.tid == 0) {
+          s_ok = wait_flag(&flags_seg[dep * Hv + h], hd) ? 1 : 0;
+          __threadfence();
+        }
+        __syncthreads();
+        have_start = s_ok != 0;
+        if (have_start && epi)
+          load_state(cx, ws_ptr<float>(p, p.L.pub) + ((size_t)dsl * Hv + h) * st_elems, S, true);
       }
-      __syncthreads();
-      have_start = s_ok != 0;
-      if (have_start) load_state(cx, ws_ptr<float>(p, p.L.pub) + ((size_t)slot[dep] * Hv + h) * st_elems, S, true);
     } else {
       // truncation: fewest preceding whole chunks of this document whose summed log-decay is
       // below the threshold; from zero, or from the document's start state if the window reaches it
@@ -903,13 +1316,14 @@ __global__ void __launch_bounds__(256, 1) chain_kernel(const __grid_constant__ F
         acc += gam[((size_t)w * Hv + h) * 64 + 63];
       }
       first_chunk = w;
-      for (int c = 0; c < 64; ++c) S[c] = 0.f;
+      set_zero();
       if (w == doc_c0 && acc >= p.trunc_thr) {
         const int s0 = seq_seg0[seq];
         const int d0 = si[4 * s0 + 3];
         if (d0 == -1) {
           const int x = p.init_idx ? p.init_idx[seq] : -1;
-          if (x >= 0 && x < p.d.n_init) load_state(cx, p.initial_state + ((size_t)x * Hv + h) * st_elems, S, false);
+          if (epi && x >= 0 && x < p.d.n_init)
+            load_state(cx, p.initial_state + ((size_t)x * Hv + h) * st_elems, S, false);
         } else {
           const int j = dep_fork_seq(d0);
           if (cx.tid == 0) {
@@ -918,43 +1332,52 @@ __global__ void __launch_bounds__(256, 1) chain_kernel(const __grid_constant__ F
           }
           __syncthreads();
           have_start = s_ok != 0;
-          if (have_start) load_state(cx, p.final_state + ((size_t)j * Hv + h) * st_elems, S, true);
+          if (have_start && epi) load_state(cx, p.final_state + ((size_t)j * Hv + h) * st_elems, S, true);
         }
       }
     }
     if (!have_start) break;
-    store_state_bf16(cx, S);
+    store_s();
     sync_generic_to_async();
-    // early publication of this segment's end state (exact split)
-    if (p.d.mode == 0 && slot[s] >= 0 && dep != -1) {
+    // early publication of this segment's end state (exact split), unless its transition is zero
+    if (p.d.mode == 0 && slot[s] >= 0 && dep != -1 && !__ldcg(&mzero[slot[s] * Hv + h])) {
       const size_t off = ((size_t)slot[s] * Hv + h) * st_elems;
-      if (!affine_apply(p, cx, ws_ptr<float>(p, p.L.mmat) + off, ws_ptr<float>(p, p.L.bmat) + off, S,
-                        ws_ptr<float>(p, p.L.pub) + off)) {
+      bool okp;
+      if constexpr (rec)
+        okp = affine_apply(p, cx, *smp, ws_ptr<float>(p, p.L.mmat) + off, ws_ptr<float>(p, p.L.bmat) + off, S,
+                           ws_ptr<float>(p, p.L.pub) + off);
+      else
+        okp = affine_apply(p, cx, *wss, ws_ptr<float>(p, p.L.mmat) + off, ws_ptr<float>(p, p.L.bmat) + off, S,
+                           ws_ptr<float>(p, p.L.pub) + off);
+      if (!okp) {
         set_status(hd, kErrTimeout);
         break;
       }
       publish(&flags_seg[s * Hv + h]);
+      store_s();  // affine_apply used the staging buffers
+      sync_generic_to_async();
     }
-    for (int gc = first_chunk; gc < c0 && ok; ++gc)
-      ok = p.st_img ? chain_chunk<false, true, false, true>(p, cx, S, gc, h, hk, ctok[gc], clen[gc])
-                    : chain_chunk<false, true>(p, cx, S, gc, h, hk, ctok[gc], clen[gc]);
-    for (int c = 0; c < nch && ok; ++c) {
-      const int gc = c0 + c;
-      if (p.st_img)
+    if constexpr (!rec) {
+      ok = run_fast(first_chunk, c0 + nch, c0, h, hk, true);
+    } else {
+      for (int gc = first_chunk; gc < c0 && ok; ++gc)
+        ok = chain_chunk<false, true, false, true>(p, cx, S, gc, h, hk, ctok[gc], clen[gc]);
+      for (int c = 0; c < nch && ok; ++c) {
+        const int gc = c0 + c;
         ok = chain_chunk<false, true, true>(p, cx, S, gc, h, hk, ctok[gc], clen[gc]);
-      else
-        ok = chain_chunk<true, true>(p, cx, S, gc, h, hk, ctok[gc], clen[gc]);
+      }
     }
     if (!ok) {
       set_status(hd, kErrTimeout);
       break;
     }
     if (last) {
-      save_state(cx, p.final_state + ((size_t)seq * Hv + h) * st_elems, S);
+      if (epi) save_state(cx, p.final_state + ((size_t)seq * Hv + h) * st_elems, S);
       publish(&flags_fin[seq * Hv + h]);
     }
     __syncthreads();
   }
+  if (s_abort && cx.tid == 0) set_status(hd, kErrTimeout);
   // drain: make sure no MMA is in flight before releasing tensor memory
   if (cx.tid == 0) {
     umma_commit(&bar_mma);
@@ -974,11 +1397,14 @@ int launch_fwd(const FwdParams& p, cudaStream_t stream, cudaEvent_t* ev) {
     if (cudaFuncSetAttribute(kkt_solve_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)(sizeof(KktSmem) + 1024)) != cudaSuccess)
       return kErrCuda;
-    if (cudaFuncSetAttribute(chain_kernel<kModeOut>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kChainSmemBytes) != cudaSuccess)
-      return kErrCuda;
-    if (cudaFuncSetAttribute(chain_kernel<kModeP1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kChainSmemBytes) != cudaSuccess)
+    if (cudaFuncSetAttribute(chain_kernel<kModeOut, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kSmemBytes) != cudaSuccess ||
+        cudaFuncSetAttribute(chain_kernel<kModeP1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kSmemBytes) != cudaSuccess ||
+        cudaFuncSetAttribute(chain_kernel<kModeOut, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kSmemBytes) != cudaSuccess ||
+        cudaFuncSetAttribute(chain_kernel<kModeP1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kSmemBytes) != cudaSuccess)
       return kErrCuda;
     attr_done = true;
   }
@@ -999,14 +1425,20 @@ int launch_fwd(const FwdParams& p, cudaStream_t stream, cudaEvent_t* ev) {
   if (p.d.mode == 0 && p.L.slots > 0 && p.d.T > 0) {
     const int64_t units = (2 * p.L.slots + 1) * p.d.Hv;
     const int grid = (int)(units < items_cap ? units : items_cap);
-    chain_kernel<kModeP1><<<grid, 256, kChainSmemBytes, stream>>>(p);
+    if (p.st_img)
+      chain_kernel<kModeP1, true><<<grid, 256, kSmemBytes, stream>>>(p);
+    else
+      chain_kernel<kModeP1, false><<<grid, kWsThreads, kSmemBytes, stream>>>(p);
   }
   mark(5);
   mark(6);
   {
     const int64_t items = p.L.smax * p.d.Hv;
     const int grid = (int)(items < items_cap ? items : items_cap);
-    chain_kernel<kModeOut><<<grid, 256, kChainSmemBytes, stream>>>(p);
+    if (p.st_img)
+      chain_kernel<kModeOut, true><<<grid, 256, kSmemBytes, stream>>>(p);
+    else
+      chain_kernel<kModeOut, false><<<grid, kWsThreads, kSmemBytes, stream>>>(p);
   }
   mark(7);
   return cudaGetLastError() == cudaSuccess ? kOk : kErrCuda;
