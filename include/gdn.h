@@ -101,7 +101,7 @@ void gdn_default_options(gdn_options* opt);
  * Returns 0 for invalid sizes. The value depends on the current device's SM count. */
 size_t gdn_fwd_workspace_size(int N, int T, int H_k, int H_v, const gdn_options* opt);
 
-/* Workspace bytes gdn_chunk_bwd needs. */
+/* Workspace bytes gdn_chunk_bwd needs (opt->mode is ignored: the backward is exact). */
 size_t gdn_bwd_workspace_size(int N, int T, int H_k, int H_v, const gdn_options* opt);
 
 /*
@@ -125,6 +125,9 @@ int gdn_chunk_fwd(const void* q, const void* k, const void* v, const float* g, c
  * (summed over every document that starts from the same pool entry; NULL allowed when n_init == 0).
  * A document forked from document j of the same call sends its gradient back into j
  * ("Musings on long-context fine-tuning", section "Backward through P").
+ * The backward is always that of the exact forward: opt->mode is ignored (truncation is a
+ * forward-only option), the other options apply. Long documents are split into segments in
+ * both directions, with an exact fix-up of the state and of its gradient at each boundary.
  */
 int gdn_chunk_bwd(const void* q, const void* k, const void* v, const float* g, const float* beta,
                   const int32_t* cu_seqlens, int N, int T, int H_k, int H_v, int head_dim,

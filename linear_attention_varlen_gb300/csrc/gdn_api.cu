@@ -118,8 +118,9 @@ size_t gdn_fwd_workspace_size(int N, int T, int H_k, int H_v, const gdn_options*
 
 size_t gdn_bwd_workspace_size(int N, int T, int H_k, int H_v, const gdn_options* opt) {
   if (!sizes_ok(N, T, H_k, H_v)) return 0;
-  const gdn_options o = resolve(opt);
+  gdn_options o = resolve(opt);
   if (!valid_options(o)) return 0;
+  o.mode = GDN_MODE_EXACT;  // the backward is always exact
   return bwd_layout(make_dims(N, T, H_k, H_v, 0, o, current_sm_count())).total;
 }
 
@@ -217,7 +218,9 @@ int gdn_chunk_bwd(const void* q, const void* k, const void* v, const float* g, c
   a.dinit = dinitial_state;
   a.ws = workspace;
   a.ws_bytes = ws_bytes;
-  a.d = make_dims(N, T, H_k, H_v, n_init, o, current_sm_count());
+  gdn_options oe = o;
+  oe.mode = GDN_MODE_EXACT;  // the backward recomputes and differentiates the exact forward
+  a.d = make_dims(N, T, H_k, H_v, n_init, oe, current_sm_count());
   a.trunc_thr = o.trunc_log_threshold;
   a.scale = o.scale;
   return launch_bwd(a, (cudaStream_t)stream, reinterpret_cast<cudaEvent_t*>(o.stage_events));

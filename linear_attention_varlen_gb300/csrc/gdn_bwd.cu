@@ -140,11 +140,14 @@ __device__ __forceinline__ void rev_store_ds(const Ctx& cx, RevSmem& sm, const f
   for (int cj = 0; cj < 8; ++cj) *reinterpret_cast<uint4*>(blk + r * 128 + ((cj ^ (r & 7)) << 4)) = pack8(dS + 8 * cj);
 }
 
+// One chunk of the reverse chain: dS (this thread's row of dL/dS at the chunk end, fp32) becomes
+// dL/dS at the chunk start. kRecord: also store dL/dS at the chunk end and dV' (bf16 images) for
+// the gradient kernels.
+template <bool kRecord>
 __device__ bool rev_chunk(const BwdParams& p, Ctx& cx, RevSmem& sm, float* dS, int gc, int h, int hk, int tok0,
                           int n) {
   const int Hv = p.d.Hv;
-  // record dL/dS at this chunk's end
-  copy_smem_to_global(p.ws + p.L.ds_img + ((size_t)gc * Hv + h) * 32768, sm.ds[0], 32768, cx.tid);
+  if (kRecord) copy_smem_to_global(p.ws + p.L.ds_img + ((size_t)gc * Hv + h) * 32768, sm.ds[0], 32768, cx.tid);
   if (cx.tid == 0) {
     mbar_arrive_expect_tx(cx.bar_ld, 6 * 8192 + 8192 + 256);
     tma_load_3d(sm.k[0], &p.tm_k, 0, hk, tok0, cx.bar_ld);
@@ -245,7 +248,7 @@ __device__ bool rev_chunk(const BwdParams& p, Ctx& cx, RevSmem& sm, float* dS, i
     }
   }
   sync_generic_to_async();
-  copy_smem_to_global(p.ws + p.L.dvp_img + ((size_t)gc * Hv + h) * 16384, sm.dvp[0], 16384, cx.tid);
+  if (kRecord) copy_smem_to_global(p.ws + p.L.dvp_img + ((size_t)gc * Hv + h) * 16384, sm.dvp[0], 16384, cx.tid);
   // dS_c = e^{gamma_C} dS + Q~^T dO - W^T dV'
   if (cx.tid == 0) {
     for (int ks = 0; ks < 4; ++ks)
@@ -270,6 +273,124 @@ __device__ bool rev_chunk(const BwdParams& p, Ctx& cx, RevSmem& sm, float* dS, i
   return true;
 }
 
+// This thread's row piece (row 32 q4 + lane, columns 64 half ... +63) of a 128x128 fp32 matrix.
+__device__ __forceinline__ void rev_load(const Ctx& cx, const float* src, float* dS, bool add) {
+  const float* row = src + (size_t)(32 * cx.q4 + cx.lane) * kDim + 64 * cx.half;
+  for (int c = 0; c < 64; c += 4) {
+    const float4 f = __ldcg(reinterpret_cast<const float4*>(row + c));
+    if (add) {
+      dS[c] += f.x;
+      dS[c + 1] += f.y;
+      dS[c + 2] += f.z;
+      dS[c + 3] += f.w;
+    } else {
+      dS[c] = f.x;
+      dS[c + 1] = f.y;
+      dS[c + 2] = f.z;
+      dS[c + 3] = f.w;
+    }
+  }
+}
+__device__ __forceinline__ void rev_save(const Ctx& cx, float* dst, const float* dS) {
+  float* row = dst + (size_t)(32 * cx.q4 + cx.lane) * kDim + 64 * cx.half;
+  for (int c = 0; c < 64; c += 4) *reinterpret_cast<float4*>(row + c) = make_float4(dS[c], dS[c + 1], dS[c + 2], dS[c + 3]);
+}
+
+// out = M^T dS + B on the tensor cores with compensated bf16 operands (x = hi + lo):
+// M hi^T dS hi + M hi^T dS lo + M lo^T dS hi. M is the forward transition of a segment (fp32,
+// row-major [dk][dk]); the reverse chain carries dL/dS through M^T. M's rows go unchanged into
+// MN-major A blocks (row k of M = row k of the block, 64 m-values per block), which is M^T as
+// the A operand. dS hi is in sm.ds (rev_store_ds). Staging: M hi in q|k, M lo in qt|kt, dS lo
+// in dout|dvp (each pair is one contiguous 32 KB region of two 16 KB blocks).
+__device__ bool rev_affine(Ctx& cx, RevSmem& sm, const float* Mm, const float* Bm, const float* dS, float* out) {
+  uint8_t* mhi = sm.q[0];
+  uint8_t* mlo = sm.qt[0];
+  uint8_t* dlo = sm.dout[0];
+  {
+    const int r = cx.tid >> 1, c0 = (cx.tid & 1) * 64;
+    const float* row = Mm + (size_t)r * kDim + c0;
+    uint8_t* bhi = mhi + (c0 >> 6) * 16384;
+    uint8_t* blo = mlo + (c0 >> 6) * 16384;
+    for (int cj = 0; cj < 8; ++cj) {
+      float x[8], lo[8];
+      const float4 a = __ldcg(reinterpret_cast<const float4*>(row + 8 * cj));
+      const float4 b = __ldcg(reinterpret_cast<const float4*>(row + 8 * cj + 4));
+      x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+      for (int u = 0; u < 8; ++u) lo[u] = x[u] - __bfloat162float(__float2bfloat16_rn(x[u]));
+      const uint32_t off = r * 128 + ((cj ^ (r & 7)) << 4);
+      *reinterpret_cast<uint4*>(bhi + off) = pack8(x);
+      *reinterpret_cast<uint4*>(blo + off) = pack8(lo);
+    }
+    const int rr = 32 * cx.q4 + cx.lane;
+    uint8_t* dl = dlo + cx.half * 16384;
+    for (int cj = 0; cj < 8; ++cj) {
+      float lo[8];
+      for (int u = 0; u < 8; ++u) lo[u] = dS[8 * cj + u] - __bfloat162float(__float2bfloat16_rn(dS[8 * cj + u]));
+      *reinterpret_cast<uint4*>(dl + rr * 128 + ((cj ^ (rr & 7)) << 4)) = pack8(lo);
+    }
+  }
+  sync_generic_to_async();
+  if (cx.tid == 0) {
+    for (int ks = 0; ks < 8; ++ks)
+      umma_bf16(cx.tmem + kRtC, mnmajor_desc(smem_u32(mhi), 16384, ks), mnmajor_desc(smem_u32(sm.ds[0]), 16384, ks),
+                idesc_bf16(128, 128, 1, 1), ks > 0);
+    for (int ks = 0; ks < 8; ++ks)
+      umma_bf16(cx.tmem + kRtC, mnmajor_desc(smem_u32(mhi), 16384, ks), mnmajor_desc(smem_u32(dlo), 16384, ks),
+                idesc_bf16(128, 128, 1, 1), 1);
+    for (int ks = 0; ks < 8; ++ks)
+      umma_bf16(cx.tmem + kRtC, mnmajor_desc(smem_u32(mlo), 16384, ks), mnmajor_desc(smem_u32(sm.ds[0]), 16384, ks),
+                idesc_bf16(128, 128, 1, 1), 1);
+  }
+  if (!cx.commit_wait()) return false;
+  {
+    const int r = 32 * cx.q4 + cx.lane;
+    for (int cc = 0; cc < 64; cc += 16) {
+      float v[16];
+      tmem_ld16(cx.tmem + kRtC + cx.lane_base() + 64 * cx.half + cc, v);
+      tmem_ld_wait();
+      const size_t o = (size_t)r * kDim + 64 * cx.half + cc;
+      for (int x = 0; x < 16; x += 4) {
+        const float4 b = __ldcg(reinterpret_cast<const float4*>(Bm + o + x));
+        *reinterpret_cast<float4*>(out + o + x) = make_float4(v[x] + b.x, v[x + 1] + b.y, v[x + 2] + b.z, v[x + 3] + b.w);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  return true;
+}
+
+// Does some later document of the call start from document seq's final state (a fork)?
+__device__ __forceinline__ bool doc_has_forks(const BwdParams& p, int seq) {
+  if (!p.init_idx) return false;
+  for (int x = seq + 1; x < p.d.N; ++x)
+    if (p.init_idx[x] == p.d.n_init + seq) return true;
+  return false;
+}
+
+__device__ __forceinline__ void rev_publish(int* flag) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    st_release(flag, 1);
+  }
+  __syncthreads();
+}
+
+// Reverse chain over the segments of the forward plan, exact split (the mirror of the forward's):
+// with M_s the forward transition of segment s (S_end = M_s S_start + B_s), the gradient obeys
+//   dL/dS_start(s) = M_s^T dL/dS_end(s) + Br_s,   Br_s = the reverse chain over s from zero.
+//   kPass 1, per (segment, value head), no dependencies: Br_s for the inner segments of a split
+//            document (neither first nor last); for its last segment, when no document forks from
+//            it, dL/dS at the segment start directly (published at once).
+//   kPass 2, per (segment, value head) in descending segment order: the end gradient is dfinal
+//            (+ the forked documents' start gradients) for a last segment, else the published start
+//            gradient of segment s + 1 (or Br_{s+1} when M_{s+1} is exactly zero); an inner segment
+//            publishes its start gradient M_s^T dS_end + Br_s before it runs; then the chunks in
+//            reverse with records; a first segment writes dL/dS at the document start.
+// Every wait is on an item with a smaller ticket, so the queue cannot deadlock.
+template <int kPass>
 __global__ void __launch_bounds__(256, 1) rev_chain_kernel(const __grid_constant__ BwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   RevSmem& sm = *reinterpret_cast<RevSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -279,7 +400,8 @@ __global__ void __launch_bounds__(256, 1) rev_chain_kernel(const __grid_constant
   Header* hd = reinterpret_cast<Header*>(p.ws + p.L.f.header);
   Header* h2 = reinterpret_cast<Header*>(p.ws + p.L.hdr2);
   const int N = p.d.N, Hv = p.d.Hv, G = p.d.Hv / p.d.Hk;
-  const int n_items = N * Hv;
+  const int n_segs = hd->n_segs;
+  const int n_items = n_segs * Hv;
   if (blockIdx.x >= n_items || get_status(hd) != 0) return;
   Ctx cx;
   ctx_init(cx, &bar_ld, &bar_mma);
@@ -291,68 +413,117 @@ __global__ void __launch_bounds__(256, 1) rev_chain_kernel(const __grid_constant
   if (cx.warp == 0) tmem_alloc(&tmem_holder, 512);
   sync_generic_to_async();
   cx.tmem = tmem_holder;
-  const int32_t* seq_chunk0 = reinterpret_cast<const int32_t*>(p.ws + p.L.f.seq_chunk0);
+  const int32_t* seq_seg0 = reinterpret_cast<const int32_t*>(p.ws + p.L.f.seq_seg0);
+  const int32_t* si = reinterpret_cast<const int32_t*>(p.ws + p.L.f.seg_info);
+  const int32_t* slot = reinterpret_cast<const int32_t*>(p.ws + p.L.f.seg_slot);
   const int32_t* ctok = reinterpret_cast<const int32_t*>(p.ws + p.L.f.chunk_tok0);
   const int32_t* clen = reinterpret_cast<const int32_t*>(p.ws + p.L.f.chunk_len);
+  const int* mzero = reinterpret_cast<const int*>(p.ws + p.L.f.mzero);
+  const float* mmat = reinterpret_cast<const float*>(p.ws + p.L.f.mmat);
   float* ds0 = reinterpret_cast<float*>(p.ws + p.L.ds0);
+  float* rpub = reinterpret_cast<float*>(p.ws + p.L.rpub);
+  float* rb = reinterpret_cast<float*>(p.ws + p.L.rb);
   int* flags = reinterpret_cast<int*>(p.ws + p.L.flags_ds0);
+  int* rflags = reinterpret_cast<int*>(p.ws + p.L.flags_rseg);
   const size_t st = (size_t)kDim * kDim;
   float dS[64];
+  // wait for `flag` (uniform outcome)
+  auto wait_uniform = [&](const int* flag) -> bool {
+    if (cx.tid == 0) {
+      s_ok = wait_flag(flag, hd) ? 1 : 0;
+      __threadfence();
+    }
+    __syncthreads();
+    const bool ok = s_ok != 0;
+    __syncthreads();
+    return ok;
+  };
+  // dL/dS at a document's end: dfinal plus the start gradients of the documents forked from it
+  auto doc_end_grad = [&](int seq, int h) -> bool {
+    if (p.dfinal)
+      rev_load(cx, p.dfinal + ((size_t)seq * Hv + h) * st, dS, false);
+    else
+      for (int c = 0; c < 64; ++c) dS[c] = 0.f;
+    if (p.init_idx)
+      for (int x = seq + 1; x < N; ++x) {
+        if (p.init_idx[x] != p.d.n_init + seq) continue;
+        if (!wait_uniform(&flags[x * Hv + h])) return false;
+        rev_load(cx, ds0 + ((size_t)x * Hv + h) * st, dS, true);
+      }
+    return true;
+  };
+  auto run = [&](int c0, int nch, int h, int hk, bool record) -> bool {
+    rev_store_ds(cx, sm, dS);
+    sync_generic_to_async();
+    bool ok = true;
+    for (int gc = c0 + nch - 1; gc >= c0 && ok; --gc)
+      ok = record ? rev_chunk<true>(p, cx, sm, dS, gc, h, hk, ctok[gc], clen[gc])
+                  : rev_chunk<false>(p, cx, sm, dS, gc, h, hk, ctok[gc], clen[gc]);
+    return ok;
+  };
   for (;;) {
     if (cx.tid == 0) {
-      const int it = (int)atomicAdd(&h2->q_chain, 1u);
+      const int it = (int)atomicAdd(kPass == 1 ? &h2->q_p1 : &h2->q_chain, 1u);
       s_item = (get_status(hd) != 0) ? n_items : it;
     }
     __syncthreads();
     const int item = s_item;
+    __syncthreads();  // s_item is rewritten by the next ticket
     if (item >= n_items) break;
-    const int seq = N - 1 - item / Hv, h = item % Hv, hk = h / G;
-    const int r = 32 * cx.q4 + cx.lane;
-    if (p.dfinal) {
-      const float* src = p.dfinal + ((size_t)seq * Hv + h) * st + (size_t)r * kDim + 64 * cx.half;
-      for (int c = 0; c < 64; ++c) dS[c] = src[c];
-    } else {
-      for (int c = 0; c < 64; ++c) dS[c] = 0.f;
-    }
-    // documents that started from this one's final state send their gradient back (in order)
+    const int s = (kPass == 1) ? item / Hv : n_segs - 1 - item / Hv;
+    const int h = item % Hv, hk = h / G;
+    const int seq = si[4 * s], c0 = si[4 * s + 1], nch = si[4 * s + 2];
+    const int first = seq_seg0[seq], last = seq_seg0[seq + 1] - 1;
     bool ok = true;
-    if (p.init_idx) {
-      for (int x = seq + 1; x < N && ok; ++x) {
-        if (p.init_idx[x] != p.d.n_init + seq) continue;
-        if (cx.tid == 0) {
-          s_ok = wait_flag(&flags[x * Hv + h], hd) ? 1 : 0;
-          __threadfence();
-        }
+    if (kPass == 1) {
+      if (first == last || s == first) continue;  // nothing to precompute
+      if (s < last) {
+        for (int c = 0; c < 64; ++c) dS[c] = 0.f;
+        ok = run(c0, nch, h, hk, false);
+        if (!ok) break;
+        rev_save(cx, rb + ((size_t)slot[s] * Hv + h) * st, dS);
         __syncthreads();
-        ok = s_ok != 0;
-        if (ok) {
-          const float* src = ds0 + ((size_t)x * Hv + h) * st + (size_t)r * kDim + 64 * cx.half;
-          for (int c = 0; c < 64; c += 4) {
-            const float4 f = __ldcg(reinterpret_cast<const float4*>(src + c));
-            dS[c] += f.x;
-            dS[c + 1] += f.y;
-            dS[c + 2] += f.z;
-            dS[c + 3] += f.w;
-          }
-        }
-        __syncthreads();
+        continue;
       }
+      if (doc_has_forks(p, seq)) continue;  // its end gradient waits for the forked documents
+      ok = doc_end_grad(seq, h) && run(c0, nch, h, hk, false);
+      if (!ok) break;
+      rev_save(cx, rpub + ((size_t)slot[s - 1] * Hv + h) * st, dS);
+      rev_publish(&rflags[s * Hv + h]);
+      continue;
+    }
+    // ----------------------------------------------------------------- pass 2
+    if (s == last) {
+      ok = doc_end_grad(seq, h);
+    } else if (s + 1 != last && mzero[slot[s + 1] * Hv + h]) {
+      rev_load(cx, rb + ((size_t)slot[s + 1] * Hv + h) * st, dS, false);  // M_{s+1} = 0: no wait
+    } else {
+      ok = wait_uniform(&rflags[(s + 1) * Hv + h]);
+      if (ok) rev_load(cx, rpub + ((size_t)slot[s] * Hv + h) * st, dS, false);
     }
     if (!ok) break;
-    rev_store_ds(cx, sm, dS);
-    sync_generic_to_async();
-    const int c0 = seq_chunk0[seq], c1 = seq_chunk0[seq + 1];
-    for (int gc = c1 - 1; gc >= c0 && ok; --gc) ok = rev_chunk(p, cx, sm, dS, gc, h, hk, ctok[gc], clen[gc]);
-    if (!ok) {
+    if (first < s && s < last && !mzero[slot[s] * Hv + h]) {
+      // early publication of this segment's start gradient
+      rev_store_ds(cx, sm, dS);
+      sync_generic_to_async();
+      const size_t o = ((size_t)slot[s] * Hv + h) * st;
+      if (!rev_affine(cx, sm, mmat + o, rb + o, dS, rpub + ((size_t)slot[s - 1] * Hv + h) * st)) {
+        set_status(hd, kErrTimeout);
+        break;
+      }
+      rev_publish(&rflags[s * Hv + h]);
+    }
+    if (!run(c0, nch, h, hk, true)) {
       set_status(hd, kErrTimeout);
       break;
     }
-    float* dst = ds0 + ((size_t)seq * Hv + h) * st + (size_t)r * kDim + 64 * cx.half;
-    for (int c = 0; c < 64; c += 4) *reinterpret_cast<float4*>(dst + c) = make_float4(dS[c], dS[c + 1], dS[c + 2], dS[c + 3]);
-    __syncthreads();
-    if (cx.tid == 0) {
-      __threadfence();
-      st_release(&flags[seq * Hv + h], 1);
+    if (first < s && s == last && doc_has_forks(p, seq)) {
+      rev_save(cx, rpub + ((size_t)slot[s - 1] * Hv + h) * st, dS);
+      rev_publish(&rflags[s * Hv + h]);
+    }
+    if (s == first) {
+      rev_save(cx, ds0 + ((size_t)seq * Hv + h) * st, dS);
+      rev_publish(&flags[seq * Hv + h]);
     }
     __syncthreads();
   }
@@ -955,8 +1126,10 @@ __global__ void __launch_bounds__(256) dinit_reduce_kernel(const __grid_constant
 int launch_bwd(const BwdArgs& a, cudaStream_t stream, cudaEvent_t* ev) {
   static bool attr_done = false;
   if (!attr_done) {
-    if (cudaFuncSetAttribute(rev_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRevSmemBytes) !=
-        cudaSuccess)
+    if (cudaFuncSetAttribute(rev_chain_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRevSmemBytes) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(rev_chain_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRevSmemBytes) !=
+            cudaSuccess)
       return kErrCuda;
     if (cudaFuncSetAttribute(grad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGradSmemBytes) !=
         cudaSuccess)
@@ -1026,11 +1199,13 @@ int launch_bwd(const BwdArgs& a, cudaStream_t stream, cudaEvent_t* ev) {
   };
   if (cudaMemsetAsync(ws + p.L.flags_ds0, 0, (size_t)d.N * d.Hv * 4, stream) != cudaSuccess) return kErrCuda;
   if (cudaMemsetAsync(ws + p.L.hdr2, 0, sizeof(Header), stream) != cudaSuccess) return kErrCuda;
+  if (cudaMemsetAsync(ws + p.L.flags_rseg, 0, (size_t)p.L.f.smax * d.Hv * 4, stream) != cudaSuccess) return kErrCuda;
   mark(8);
   {
-    const int items = d.N * d.Hv;
-    const int grid = items < d.num_sms ? items : d.num_sms;
-    rev_chain_kernel<<<grid, 256, kRevSmemBytes, stream>>>(p);
+    const int64_t items = p.L.f.smax * d.Hv;
+    const int grid = (int)(items < d.num_sms ? items : d.num_sms);
+    if (p.L.f.slots > 0 && d.T > 0) rev_chain_kernel<1><<<grid, 256, kRevSmemBytes, stream>>>(p);
+    rev_chain_kernel<2><<<grid, 256, kRevSmemBytes, stream>>>(p);
   }
   mark(9);
   mark(10);

@@ -35,6 +35,9 @@ struct BwdLayout {
   size_t fin;       // final states of the recompute, fp32 [N][Hv][128][128]
   size_t ds0;       // dL/dS at each document start, fp32 [N][Hv][128][128]
   size_t flags_ds0; // int32 [N][Hv]
+  size_t rpub;      // reverse split: dL/dS at the start of segment s, published at slot[s-1], fp32
+  size_t rb;        // reverse split: dL/dS at the start of segment s from a zero end gradient, at slot[s]
+  size_t flags_rseg;// int32 [smax][Hv]: rpub of segment s is ready
   size_t hdr2;      // Header of the reverse pass (queue, status mirror)
   size_t total;
 };
@@ -62,6 +65,9 @@ inline BwdLayout bwd_layout(const PlanDims& d) {
   L.fin = take((size_t)d.N * d.Hv * state);
   L.ds0 = take((size_t)d.N * d.Hv * state);
   L.flags_ds0 = take((size_t)d.N * d.Hv * 4);
+  L.rpub = take((size_t)L.f.slots * d.Hv * state);
+  L.rb = take((size_t)L.f.slots * d.Hv * state);
+  L.flags_rseg = take((size_t)L.f.smax * d.Hv * 4);
   L.hdr2 = take(sizeof(Header));
   L.total = o;
   return L;

@@ -46,10 +46,6 @@ def check_bwd(p, options=None, record=None, stress=False):
         for k, (rel, mx) in res.items():
             record(f"{k}_rel_l2", rel)
             record(f"{k}_max_abs", mx)
-    if record is not None:
-        for k, (rel, mx) in res.items():
-            record(f"{k}_rel_l2", rel)
-            record(f"{k}_max_abs", mx)
     return got, ref
 
 
@@ -108,3 +104,34 @@ def test_bwd_deterministic():
 def test_bwd_workload_train_full(record_property):
     """Full-size training step: 4 documents x 16384 tokens, 8 value heads over 2 key heads."""
     check_bwd(synth.workload_train(), record=record_property)
+
+
+def test_bwd_split_document_with_forks():
+    """A document split into segments whose final state two later (also split) documents fork
+    from: its last segment's end gradient waits for the forks' start gradients."""
+    lens = [64 * 10 + 5, 64 * 7, 300]
+    p = synth.make_problem("bwd_split_forks", 350, lens, 2, 4, init_idx=[-1, 0, 0], with_dout=True)
+    check_bwd(p, gdn.Options(segment_chunks=3))
+
+
+def test_bwd_split_zero_transitions():
+    """A decay fast enough that segment transitions are exactly zero in fp32: the reverse split
+    takes the local start gradient without waiting for the next segment."""
+    p = synth.make_problem("bwd_fast_decay", 351, [64 * 12 + 17, 64 * 9], 1, 2, with_dout=True, g_mean=-3.0)
+    check_bwd(p, gdn.Options(segment_chunks=2))
+
+
+def test_bwd_ignores_truncation_mode():
+    """The backward is that of the exact forward whatever the mode option says."""
+    p = synth.make_problem("bwd_trunc_opt", 352, [64 * 20 + 3], 1, 2, with_dout=True)
+    a = run_bwd(p, gdn.Options(segment_chunks=4))
+    b = run_bwd(p, gdn.Options(segment_chunks=4, mode="truncate"))
+    for key in KEYS:
+        np.testing.assert_array_equal(a[key], b[key])
+
+
+def test_bwd_workload_long_full(record_property):
+    """Full-size long prefill shape: one 32768-token document, 8 value heads over 2 key heads,
+    automatic exact split in both directions."""
+    p = synth.make_problem("bwd_long_T32768_H8", synth.SEEDS[2], [32768], 2, 8, with_dout=True)
+    check_bwd(p, record=record_property)
