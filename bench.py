@@ -45,10 +45,37 @@ def algorithmic_fwd(T, Hk, Hv, N):
 
 
 def algorithmic_bwd(T, Hk, Hv, N):
-    # read q, k, v, g, beta, dO; write dq, dk, dv, dg, dbeta
-    bytes_ = T * (2 * Hk * D * 2 + Hv * D * 2 + 2 * Hv * 4 + Hv * D * 2 + 2 * Hk * D * 2 + Hv * D * 2 + 2 * Hv * 4)
+    # read q, k, v, g, beta, dO; write dq, dk, dv (fp32), dg, dbeta
+    bytes_ = T * (2 * Hk * D * 2 + 2 * Hv * D * 2 + 2 * Hv * 4) + T * (2 * Hk * D * 4 + Hv * D * 4 + 2 * Hv * 4)
     flops = T * (Hk * 4 * 64 * D + Hv * (16 * D * D + 26 * 64 * D))
     return bytes_, flops
+
+
+def kernel_counts(T, Hk, Hv, N):
+    """Algorithmic (bytes, FLOPs) per launch of the kernels that can dominate a step: inputs a
+    kernel must read and outputs it must write (no intermediates), and the FLOPs of the matrix
+    products its math needs (compensation products not counted)."""
+    C = 64
+    n_ch = T / C
+    fb, ff = algorithmic_fwd(T, Hk, Hv, N)
+    # chain (forward output pass): q, k, v in; o, final state out; W S, K~^T V', Q S, P V'
+    chain = (fb - T * 2 * Hv * 4, n_ch * Hv * 2 * (3 * C * D * D + C * C * D))
+    # grad_kernel: q, k, v, dO, g, beta in; dk, dv, dg, dbeta out (fp32)
+    grad_b = T * (2 * Hk * D * 2 + 2 * Hv * D * 2 + 2 * Hv * 4) + T * (Hk * D * 4 + Hv * D * 4 + 2 * Hv * 4)
+    # per value head: K dS, Q S, dV' S^T, V'_s dS^T (C D^2 each); dO V'^T, dV' V^T, dW K^T, P Q,
+    # T_u^T dV', T_w^T dW, dKK K (C^2 D each); dT T^T, T^T R (C^3 each); per key head K K^T, Q K^T
+    grad_f = n_ch * (Hk * 2 * 2 * C * C * D + Hv * 2 * (4 * C * D * D + 7 * C * C * D + 2 * C * C * C))
+    # dq_kernel: k, dO, g in; dq out (fp32); dO S^T, dO V'^T, (dQK o E) K
+    dq_b = T * (Hk * D * 2 + Hv * D * 2 + Hv * 4) + T * Hk * D * 4
+    dq_f = n_ch * Hv * 2 * (C * D * D + 2 * C * C * D)
+    # reverse chain: k, q, dO in; K~ dS, P^T dO, Q~^T dO, W^T dV'
+    rev_b = T * (2 * Hk * D * 2 + Hv * D * 2)
+    rev_f = n_ch * Hv * 2 * (3 * C * D * D + C * C * D)
+    # kkt_solve: k, g, beta in; K K^T and the 64x64 solve per value head
+    kkt_b = T * (Hk * D * 2 + 2 * Hv * 4)
+    kkt_f = n_ch * (Hk * 2 * C * C * D + Hv * C * C * C / 3)
+    return {"chain_kernel<out>": chain, "chain_kernel<out,record>": chain, "grad_kernel": (grad_b, grad_f),
+            "dq_kernel": (dq_b, dq_f), "rev_chain_kernel": (rev_b, rev_f), "kkt_solve_kernel": (kkt_b, kkt_f)}
 
 
 def load_peaks():
@@ -120,6 +147,13 @@ class ClockSampler:
 # ----------------------------------------------------------------------------- reference arm (fp64 oracle)
 
 
+def _oracle_step(p, f, cores):
+    """One forward + backward of the fp64 oracle on problem p (the bench step's work)."""
+    import oracle
+    oracle.fwd(f["q"], f["k"], f["v"], f["g"], f["beta"], p.cu_seqlens, threads=cores)
+    oracle.bwd(f["q"], f["k"], f["v"], f["g"], f["beta"], p.cu_seqlens, f["dout"], threads=cores)
+
+
 def run_reference(args, rank):
     if rank != 0:
         return None
@@ -128,64 +162,71 @@ def run_reference(args, rank):
     import oracle
     import synth
     oracle.build()
-    T_sample = 2048
-    p = synth.workload_long(T=T_sample)
+    T_sample = 1024
+    p = synth.make_problem(f"long_sample_T{T_sample}", synth.SEEDS[2], [T_sample], 2, 8, with_dout=True)
     f = p.as_f64()
     cores = oracle.hw_threads()
     for _ in range(args.warmup):
-        oracle.fwd(f["q"], f["k"], f["v"], f["g"], f["beta"], p.cu_seqlens, threads=cores)
+        _oracle_step(p, f, cores)
     ts = []
     for _ in range(args.steps):
         t0 = time.perf_counter()
-        oracle.fwd(f["q"], f["k"], f["v"], f["g"], f["beta"], p.cu_seqlens, threads=cores)
+        _oracle_step(p, f, cores)
         ts.append(time.perf_counter() - t0)
     sec = float(np.mean(ts))
     value = T_sample / sec / 1e6
-    sample = f"first {T_sample} tokens of the 32768-token, 8-head workload per step (fp64 oracle forward)"
+    sample = (f"a {T_sample}-token single sequence with the 32768-token workload's shapes and distributions "
+              f"(H_v=8, H_k=2), fp64 oracle forward + backward per step")
     return {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": "GDN fwd, single sequence, H_v=8, H_k=2, d=128 (oracle on host cores)",
+        "config": {"workload": "GDN fwd+bwd, single sequence, H_v=8, H_k=2, d=128 (fp64 oracle on host cores)",
                    "T": T_sample, "H_v": 8, "H_k": 2},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
 
-def cpu_baseline():
-    """The fp64 oracle on the full workload, repeated until about 10 s of CPU work."""
+def cpu_baseline(T_full):
+    """The fp64 oracle's forward + backward on a bounded sample of the workload (the first 4096
+    tokens' shape), repeated until about 10 s of CPU work."""
     import oracle
     import synth
     oracle.build()
-    p = synth.workload_long()
+    T_s = min(4096, T_full)
+    p = synth.make_problem(f"long_sample_T{T_s}", synth.SEEDS[2], [T_s], 2, 8, with_dout=True)
     f = p.as_f64()
     cores = oracle.hw_threads()
     total, runs = 0.0, 0
-    while runs < 1 or (total < 10.0 and runs < 4):
+    while runs < 1 or (total < 10.0 and runs < 8):
         t0 = time.perf_counter()
-        oracle.fwd(f["q"], f["k"], f["v"], f["g"], f["beta"], p.cu_seqlens, threads=cores)
+        _oracle_step(p, f, cores)
         total += time.perf_counter() - t0
         runs += 1
-    return {"value": p.T * runs / total / 1e6, "unit": UNIT, "cores": cores,
-            "kind": "oracle", "sample": f"full 32768-token x 8-head forward, {runs} run(s), {total:.1f} s"}
+    return {"value": p.T * runs / total / 1e6, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{T_s}-token single sequence, 8 value heads over 2 key heads, forward + backward, "
+                      f"{runs} run(s), {total:.1f} s"}
 
 
 # ----------------------------------------------------------------------------- our arm
 
 
-def traffic_record(kernel_src):
-    """DRAM bytes per launch of the dominant kernel from a committed ncu summary, if it was
-    taken on the current source of that kernel (else None)."""
+def traffic_record(kernel):
+    """DRAM bytes per launch of `kernel` from the committed ncu summaries (profiles/traffic.json:
+    one record per kernel), if the record was taken on the current source of that kernel."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
     try:
-        rec = json.load(open(path))
-        sha = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()
+        recs = json.load(open(path))
+        rec = recs.get(kernel) if isinstance(recs, dict) else None
+        if not rec:
+            return None
+        sha = hashlib.sha256(open(os.path.join(ROOT, rec["source"]), "rb").read()).hexdigest()
         if rec.get("source_sha256") == sha:
             return rec
-    except (OSError, ValueError):
+    except (OSError, ValueError, KeyError):
         pass
     return None
 
@@ -203,7 +244,7 @@ def run_ours(args, rank, world, local_rank):
     gdn.load()
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
-    p = synth.workload_long()
+    p = synth.workload_long(T=args.tokens)
     d = to_device(p, dev)
     T, Hk, Hv, N = p.T, p.Hk, p.Hv, p.N
     stream = torch.cuda.current_stream()
@@ -266,7 +307,7 @@ def run_ours(args, rank, world, local_rank):
         stops[i].synchronize()
         for s_ in range(gdn.NUM_STAGES):
             stage_f[i, s_] = ev_f[2 * s_].elapsed_time(ev_f[2 * s_ + 1])
-            if has_bwd and s_ <= gdn.STAGE_DINIT:
+            if has_bwd:
                 stage_b[i, s_] = ev_b[2 * s_].elapsed_time(ev_b[2 * s_ + 1])
     torch.cuda.synchronize()
     if world > 1:
@@ -320,48 +361,57 @@ def run_ours(args, rank, world, local_rank):
     if rank != 0:
         return None
     peaks = load_peaks()
-    names = {gdn.STAGE_PLAN: "plan_kernel", gdn.STAGE_KKT_SOLVE: "kkt_solve_kernel",
-             gdn.STAGE_SPLIT: "chain_kernel<pass1>", gdn.STAGE_CHAIN: "chain_kernel<out>"}
+    fnames = {gdn.STAGE_PLAN: "plan_kernel", gdn.STAGE_KKT_SOLVE: "kkt_solve_kernel",
+              gdn.STAGE_SPLIT: "chain_kernel<pass1>", gdn.STAGE_CHAIN: "chain_kernel<out>"}
     bnames = {gdn.STAGE_PLAN: "plan_kernel", gdn.STAGE_KKT_SOLVE: "kkt_solve_kernel",
               gdn.STAGE_SPLIT: "chain_kernel<pass1,record>", gdn.STAGE_CHAIN: "chain_kernel<out,record>",
-              gdn.STAGE_REV_CHAIN: "rev_chain_kernel", gdn.STAGE_GRADS: "grad_kernel+dq_kernel",
-              gdn.STAGE_DINIT: "dinit_reduce_kernel"}
+              gdn.STAGE_REV_CHAIN: "rev_chain_kernel", gdn.STAGE_GRADS: "grad_kernel",
+              gdn.STAGE_DQ: "dq_kernel", gdn.STAGE_DINIT: "dinit_reduce_kernel"}
     avg = stage_f.mean(axis=0)
     bavg = stage_b.mean(axis=0)
-    dom = int(np.argmax(avg[:4]))
-    fb, ff = algorithmic_fwd(T, Hk, Hv, N)
-    # The chain kernel reads q, k, v and writes o and the final state: the forward's algorithmic bytes.
-    hbm_t = fb / (peaks["hbm"] * 1e9)
-    tc_t = ff / (peaks["tc_sus"] * 1e12)
-    bound = "hbm" if hbm_t >= tc_t else "tensor"
-    kern_s = avg[dom] * 1e-3
-    if bound == "hbm":
-        achieved, peak, unit_r = fb / kern_s / 1e9, peaks["hbm"], "GB/s"
+    fwd_ms = float(sum(avg[s_] for s_ in fnames))
+    bwd_ms = float(sum(bavg[s_] for s_ in bnames)) if has_bwd else 0.0
+    # the dominant kernel of the step (one launch per stage, except the two-pass reverse chain)
+    cands = [(avg[s_], fnames[s_]) for s_ in fnames]
+    if has_bwd:
+        cands += [(bavg[s_], bnames[s_]) for s_ in bnames]
+    counts = kernel_counts(T, Hk, Hv, N)
+    dom_ms, dom = max((c for c in cands if c[1] in counts), key=lambda c: c[0])
+    kb, kf = counts[dom]
+    kern_s = dom_ms * 1e-3
+    # binding roofline of that kernel at the measured peaks (sustained TC: it runs inside a long step)
+    if kb / (peaks["hbm"] * 1e9) >= kf / (peaks["tc_sus"] * 1e12):
+        bound, achieved, peak, unit_r = "hbm", kb / kern_s / 1e9, peaks["hbm"], "GB/s"
     else:
-        achieved, peak, unit_r = ff / kern_s / 1e12, peaks["tc_sus"], "TFLOP/s"
-    tr = traffic_record(os.path.join(ROOT, "linear_attention_varlen_gb300", "csrc", "gdn_fwd.cu"))
+        bound, achieved, peak, unit_r = "tensor", kf / kern_s / 1e12, peaks["tc_sus"], "TFLOP/s"
+    tr = traffic_record(dom)
     launches_per_step = 3 + (1 if split_launched else 0)
-    if has_bwd:  # recompute (same launches as the forward) + reverse chain, grad, dq kernels
-        launches_per_step += 3 + (1 if split_launched else 0) + 3
-    fwd_ms = float(avg[:4].sum())
+    if has_bwd:  # recompute (same launches as the forward) + two reverse passes (one unsplit), grad, dq
+        launches_per_step += 3 + (1 if split_launched else 0) + (2 if split_launched else 1) + 2
+    fb, ff = algorithmic_fwd(T, Hk, Hv, N)
+    bb, bf = algorithmic_bwd(T, Hk, Hv, N) if has_bwd else (0, 0)
+    step_alg_s = max(fb / (peaks["hbm"] * 1e9), ff / (peaks["tc_sus"] * 1e12))
+    if has_bwd:
+        step_alg_s += max(bb / (peaks["hbm"] * 1e9), bf / (peaks["tc_sus"] * 1e12))
     res = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": value / PAGE_FWD_MTOK_S if not has_bwd else None,
         "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": "GDN " + ("fwd+bwd" if has_bwd else "fwd") + ", one 32768-token sequence, H_v=8, "
+        "config": {"workload": "GDN " + ("fwd+bwd" if has_bwd else "fwd") + f", one {T}-token sequence, H_v=8, "
                    "H_k=2, d_k=d_v=128, chunk 64, " + args.mode + " mode", "T": T, "H_v": Hv, "H_k": Hk,
                    "mode": args.mode, "pass": "fwd+bwd" if has_bwd else "fwd",
                    "l2": "flushed between timed steps (512 MiB write outside the timed events)"},
-        "roofline": {"bound": bound, "kernel": names[dom], "achieved": achieved, "peak": peak, "unit": unit_r,
+        "roofline": {"bound": bound, "kernel": dom, "achieved": achieved, "peak": peak, "unit": unit_r,
                      "frac": achieved / peak, "traffic": (tr["bytes_per_launch"] if tr else None),
                      "peak_source": peaks["src"] + (" hbm_gbs" if bound == "hbm" else " bf16_tflops_sustained"),
-                     "algorithmic_bytes": fb, "algorithmic_flops": ff},
-        "step_roofline": {"bound": bound, "frac": (max(hbm_t, tc_t) / (fwd_ms * 1e-3)),
-                          "note": "forward algorithmic time at measured peaks / whole forward time"},
-        "stages_ms": {names[s_]: float(avg[s_]) for s_ in range(4)},
-        "bwd_stages_ms": ({bnames[s_]: float(bavg[s_]) for s_ in range(7)} if has_bwd else None),
-        "fwd_ms": fwd_ms, "bwd_ms": (float(bavg[:7].sum()) if has_bwd else None),
+                     "algorithmic_bytes": kb, "algorithmic_flops": kf, "ms_per_launch": dom_ms},
+        "step_roofline": {"frac": step_alg_s / (ms * 1e-3),
+                          "note": "sum over forward and backward of max(algorithmic bytes / HBM peak, algorithmic "
+                                  "FLOPs / sustained bf16 peak), divided by the measured step time"},
+        "stages_ms": {fnames[s_]: float(avg[s_]) for s_ in fnames},
+        "bwd_stages_ms": ({bnames[s_]: float(bavg[s_]) for s_ in bnames} if has_bwd else None),
+        "fwd_ms": fwd_ms, "bwd_ms": (bwd_ms if has_bwd else None),
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
         "gpu_launches": int(launches_per_step * args.steps),
         "clocks": clk,
@@ -369,7 +419,7 @@ def run_ours(args, rank, world, local_rank):
     if not has_bwd:
         res["vs_baseline_note"] = "value / FlashQLA forward on H200 (0.31 ms for 32K at TP8), context only"
     if world == 1 and not args.no_cpu_baseline:
-        res["cpu_baseline"] = cpu_baseline()
+        res["cpu_baseline"] = cpu_baseline(T)
     return res
 
 
@@ -381,6 +431,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--mode", choices=["exact", "truncate"], default="exact")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--tokens", type=int, default=32768,
+                    help="sequence length (32768 = the benchmark; smaller only for profiler captures)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -81,16 +81,17 @@ typedef struct gdn_options {
                                 stage s (both at the same point when the stage has nothing to launch) */
 } gdn_options;
 
-/* Stages of a call, in launch order (indices into gdn_options.stage_events). A backward call
- * runs stages 0-3 (the forward recompute) and then 4-6. */
+/* Stages of a call (indices into gdn_options.stage_events). A backward call runs stages 0-3
+ * (the forward recompute), then 4, 5, 7 and 6 in that order. */
 enum gdn_fwd_stage {
   GDN_STAGE_PLAN = 0,      /* chunk / segment maps */
   GDN_STAGE_KKT_SOLVE = 1, /* intra-chunk K K^T, triangular solve, WY factors */
   GDN_STAGE_SPLIT = 2,     /* exact split, pass 1: segment transitions and local end states */
   GDN_STAGE_CHAIN = 3,     /* state chain fused with the output (records states in the backward) */
   GDN_STAGE_REV_CHAIN = 4, /* backward: reverse state-gradient chain */
-  GDN_STAGE_GRADS = 5,     /* backward: per-chunk dq, dk, dv, dg, dbeta */
+  GDN_STAGE_GRADS = 5,     /* backward: per-chunk dk, dv, dg, dbeta */
   GDN_STAGE_DINIT = 6,     /* backward: d(initial_state) sums over documents sharing a pool entry */
+  GDN_STAGE_DQ = 7,        /* backward: per-chunk dq */
   GDN_NUM_STAGES = 8
 };
 

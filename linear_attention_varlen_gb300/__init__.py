@@ -44,7 +44,7 @@ class COptions(ctypes.Structure):
 
 
 NUM_STAGES = 8
-STAGE_PLAN, STAGE_KKT_SOLVE, STAGE_SPLIT, STAGE_CHAIN, STAGE_REV_CHAIN, STAGE_GRADS, STAGE_DINIT = range(7)
+STAGE_PLAN, STAGE_KKT_SOLVE, STAGE_SPLIT, STAGE_CHAIN, STAGE_REV_CHAIN, STAGE_GRADS, STAGE_DINIT, STAGE_DQ = range(8)
 
 
 @dataclass

@@ -15,6 +15,14 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// 1024-byte aligned start of the dynamic shared memory. It is derived from the __shared__ array
+// by pointer arithmetic (not through an integer round trip), so the compiler still knows that
+// accesses through it are shared-memory accesses and emits LDS/STS instead of generic loads.
+__device__ __forceinline__ uint8_t* smem_align1024(uint8_t* raw) {
+  const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(raw));
+  return raw + ((1024u - (a & 1023u)) & 1023u);
+}
+
 // ------------------------------------------------------------------------------------------ mbarrier
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {

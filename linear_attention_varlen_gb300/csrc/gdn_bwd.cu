@@ -393,7 +393,7 @@ __device__ __forceinline__ void rev_publish(int* flag) {
 template <int kPass>
 __global__ void __launch_bounds__(256, 1) rev_chain_kernel(const __grid_constant__ BwdParams p) {
   extern __shared__ uint8_t smem_raw[];
-  RevSmem& sm = *reinterpret_cast<RevSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  RevSmem& sm = *reinterpret_cast<RevSmem*>(smem_align1024(smem_raw));
   __shared__ uint64_t bar_ld, bar_mma;
   __shared__ uint32_t tmem_holder;
   __shared__ int s_item, s_ok;
@@ -542,26 +542,54 @@ __global__ void __launch_bounds__(256, 1) rev_chain_kernel(const __grid_constant
 struct GradSmem {
   uint8_t q[2][8192];
   uint8_t k[2][8192];
-  float kkf[64][64];       // K K^T
-  float qkf[64][64];       // scale Q K^T
-  uint8_t bS[2][16384];    // S_c image       | phase 2: T fp32 [0, 16K), T bf16 [16K, 24K)
+  float kkf[4096];         // K K^T                (fz layout)
+  float qkf[4096];         // scale Q K^T          (fz layout)
+  uint8_t bS[2][16384];    // S_c image       | phase 2: T fp32 [0, 16K) (fz), T bf16 [16K, 24K)
   uint8_t bdS[2][16384];   // dS_{c+1} image  | phase 2: T_w [0, 8K), T_u [8K, 16K), dT [16K, 24K), R [24K, 32K)
-  uint8_t bVp[2][8192];    // V' -> V'_s      | fp32 64x64 scratch (vy products, then dA)
+  uint8_t bVp[2][8192];    // V' -> V'_s      | fp32 64x64 scratch (vy products, then L o KK)
   uint8_t bdVp[2][8192];   // dV'             | fp32 64x64 scratch (kx products)
   uint8_t bdO[2][8192];    // dO              | phase 2: V
   uint8_t bW[2][8192];     // fp32 scratch (dEg) | dW rows t
-  uint8_t bP[8192];        // scale dQK, then dKK + dKK^T
+  uint8_t bP[8192];        // scale dQK, then L = dA o diag(beta) E (strictly lower)
   float gam[64], beta[64], Gm[64];
   float part[8][64];
-  float vy[64], kx[64], rA[64], cA[64], db3[64];
-  float red[256];
+  float vy[64], kx[64], cA[64], db3[2][64];
+  float red4[2][4][64];    // partial column sums (two matrices x four row quarters)
+  float red[8];
 };
 constexpr size_t kGradSmemBytes = sizeof(GradSmem) + 1024;
 constexpr uint32_t kGtK = 128, kGt1 = 256, kGt2 = 384;
 
+// Column sums of one or two fp32 64x64 fz matrices over rows [0, 64) with all 256 threads:
+// out[j] = sum_i X[i][j]. Ends with the result visible to every thread.
+__device__ __forceinline__ void col_sums(GradSmem& sm, const float* X, const float* Y, float* outx, float* outy,
+                                         int tid) {
+  const int j = tid & 63, q = tid >> 6;
+  float a = 0.f, b = 0.f;
+#pragma unroll 4
+  for (int i = 16 * q; i < 16 * q + 16; ++i) {
+    a += X[fz(i, j)];
+    if (Y) b += Y[fz(i, j)];
+  }
+  sm.red4[0][q][j] = a;
+  sm.red4[1][q][j] = b;
+  __syncthreads();
+  if (tid < 64) {
+    outx[tid] = (sm.red4[0][0][tid] + sm.red4[0][1][tid]) + (sm.red4[0][2][tid] + sm.red4[0][3][tid]);
+    if (Y) outy[tid] = (sm.red4[1][0][tid] + sm.red4[1][1][tid]) + (sm.red4[1][2][tid] + sm.red4[1][3][tid]);
+  }
+  __syncthreads();
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
 __global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ BwdParams p) {
   extern __shared__ uint8_t smem_raw[];
-  GradSmem& sm = *reinterpret_cast<GradSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  GradSmem& sm = *reinterpret_cast<GradSmem*>(smem_align1024(smem_raw));
   __shared__ uint64_t bar_ld, bar_mma;
   __shared__ uint32_t tmem_holder;
   Header* hd = reinterpret_cast<Header*>(p.ws + p.L.f.header);
@@ -614,8 +642,9 @@ __global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ Bw
       tmem_ld_wait();
       if (has_row)
         for (int x = 0; x < 16; ++x) {
-          sm.kkf[i_row][32 * cx.half + cc + x] = a[x];
-          sm.qkf[i_row][32 * cx.half + cc + x] = b[x] * p.scale;
+          const int j = 32 * cx.half + cc + x;
+          sm.kkf[fz(i_row, j)] = a[x];
+          sm.qkf[fz(i_row, j)] = b[x] * p.scale;
         }
     }
   }
@@ -654,6 +683,7 @@ __global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ Bw
     if (!(ok = cx.commit_wait())) break;
     {
       float rs = 0.f;
+      const float gi = has_row ? sm.gam[i_row] : 0.f;
       for (int cc = 0; cc < 32; cc += 16) {
         float v[16];
         tmem_ld16(tm + kGt1 + cx.lane_base() + 32 * cx.half + cc, v);
@@ -661,13 +691,14 @@ __global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ Bw
         if (has_row) {
           const int i = i_row;
           float dq8[16];
+#pragma unroll
           for (int x = 0; x < 16; ++x) {
             const int j = 32 * cx.half + cc + x;
-            const float e = (j <= i && i < n) ? __expf(sm.gam[i] - sm.gam[j]) : 0.f;
+            const float e = (j <= i && i < n) ? __expf(gi - sm.gam[j]) : 0.f;
             const float dqk = v[x] * e;
             dq8[x] = dqk * p.scale;
-            const float eg = dqk * sm.qkf[i][j];
-            dEg[i * 64 + j] = eg;
+            const float eg = dqk * sm.qkf[fz(i, j)];
+            dEg[fz(i, j)] = eg;
             rs += eg;
           }
 #pragma unroll
@@ -689,12 +720,7 @@ __global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ Bw
       if (has_row) sm.part[2 + cx.half][i_row] = kt;
     }
     __syncthreads();
-    if (tid < 64) {
-      float s = 0.f;
-      for (int i = 0; i < 64; ++i) s += dEg[i * 64 + tid];
-      sm.part[4][tid] = s;
-    }
-    __syncthreads();
+    col_sums(sm, dEg, nullptr, sm.part[4], nullptr, tid);
     // ---------------- (b) Q S ; dV' S^T (-> dW) ; <dS, S>
     if (tid == 0) {
       for (int ks = 0; ks < 8; ++ks)
@@ -717,7 +743,8 @@ __global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ Bw
           fr += fa.x * fb.x + fa.y * fb.y;
         }
       }
-      sm.red[tid] = fr;
+      fr = warp_sum(fr);
+      if (cx.lane == 0) sm.red[cx.warp] = fr;
     }
     if (!(ok = cx.commit_wait())) break;
     {
@@ -754,9 +781,7 @@ __global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ Bw
                   idesc_bf16(64, 128, 1, 1), 1);
     }
     first_k = false;
-    float fro = 0.f;
-    if (tid == 0)
-      for (int x = 0; x < 256; ++x) fro += sm.red[x];
+    const float fro = ((sm.red[0] + sm.red[1]) + (sm.red[2] + sm.red[3])) + ((sm.red[4] + sm.red[5]) + (sm.red[6] + sm.red[7]));
     if (!(ok = cx.commit_wait())) break;
     // ---------------- phase 2 loads: V, T, T_w, T_u
     if (tid == 0) {
@@ -776,8 +801,9 @@ __global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ Bw
     uint8_t* Rt = sm.bdS[1] + 8192;
     for (int e = tid; e < 64 * 8; e += 256) {
       const int r = e >> 3, cj = e & 7;
-      float x[8];
-      for (int u = 0; u < 8; ++u) x[u] = Tf[r * 64 + cj * 8 + u];
+      const float4 t0 = *reinterpret_cast<const float4*>(Tf + fz(r, 8 * cj));
+      const float4 t1 = *reinterpret_cast<const float4*>(Tf + fz(r, 8 * cj + 4));
+      const float x[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
       *reinterpret_cast<uint4*>(Tb + r * 128 + ((cj ^ (r & 7)) << 4)) = pack8(x);
     }
     sync_generic_to_async();
@@ -817,11 +843,21 @@ __global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ Bw
         if (has_row) {
           const int i = i_row;
           float dt[16];
-          for (int x = 0; x < 16; ++x) {
-            const int j = 32 * cx.half + cc + x;
-            dt[x] = d1[x] * sm.beta[j] + d2[x] * sm.beta[j] * sm.Gm[j];
-            vyM[i * 64 + j] = Tf[i * 64 + j] * d1[x];
-            kxM[i * 64 + j] = Tf[i * 64 + j] * d2[x];
+#pragma unroll
+          for (int x4 = 0; x4 < 16; x4 += 4) {
+            const int j0 = 32 * cx.half + cc + x4;
+            const float4 tf = *reinterpret_cast<const float4*>(Tf + fz(i, j0));
+            const float tv[4] = {tf.x, tf.y, tf.z, tf.w};
+            float vy4[4], kx4[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int x = x4 + u, j = j0 + u;
+              dt[x] = d1[x] * sm.beta[j] + d2[x] * sm.beta[j] * sm.Gm[j];
+              vy4[u] = tv[u] * d1[x];
+              kx4[u] = tv[u] * d2[x];
+            }
+            *reinterpret_cast<float4*>(vyM + fz(i, j0)) = make_float4(vy4[0], vy4[1], vy4[2], vy4[3]);
+            *reinterpret_cast<float4*>(kxM + fz(i, j0)) = make_float4(kx4[0], kx4[1], kx4[2], kx4[3]);
           }
 #pragma unroll
           for (int u = 0; u < 2; ++u) {
@@ -832,20 +868,12 @@ __global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ Bw
       }
     }
     sync_generic_to_async();
-    if (tid < 64) {
-      float a = 0.f, b = 0.f;
-      for (int i = 0; i < 64; ++i) {
-        a += vyM[i * 64 + tid];
-        b += kxM[i * 64 + tid];
-      }
-      sm.vy[tid] = a;
-      sm.kx[tid] = b;
-    }
-    // ---------------- (e) R = dT T^T
+    // ---------------- (e) R = dT T^T (the column sums of vy / kx run meanwhile)
     if (tid == 0)
       for (int ks = 0; ks < 4; ++ks)
         umma_bf16(tm + kGt1, kmajor_desc(smem_u32(dTt), 8192, ks), kmajor_desc(smem_u32(Tb), 8192, ks),
                   idesc_bf16(64, 64, 0, 0), ks > 0);
+    col_sums(sm, vyM, kxM, sm.vy, sm.kx, tid);
     if (!(ok = cx.commit_wait())) break;
     for (int cc = 0; cc < 32; cc += 16) {
       float v[16];
@@ -860,87 +888,98 @@ __global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ Bw
       }
     }
     sync_generic_to_async();
-    // ---------------- (f) dA = -(T^T R), strictly lower and inside the chunk
+    // ---------------- (f) dA = -(T^T R), strictly lower and inside the chunk. With E_ij = e^{gamma_i -
+    // gamma_j}: L = dA o diag(beta) E (bf16, for dk += (L + L^T) K), the row sums of dA o E o KK
+    // (dbeta) and the matrix L o KK for its column sums (dgamma).
     if (tid == 0)
       for (int ks = 0; ks < 4; ++ks)
         umma_bf16(tm + kGt1, mnmajor_desc(smem_u32(Tb), 8192, ks), mnmajor_desc(smem_u32(Rt), 8192, ks),
                   idesc_bf16(64, 64, 1, 1), ks > 0);
     if (!(ok = cx.commit_wait())) break;
-    float* dA = vyM;  // vy column sums are done
-    for (int cc = 0; cc < 32; cc += 16) {
-      float v[16];
-      tmem_ld16(tm + kGt1 + cx.lane_base() + 32 * cx.half + cc, v);
-      tmem_ld_wait();
-      if (has_row)
-        for (int x = 0; x < 16; ++x) {
-          const int j = 32 * cx.half + cc + x;
-          dA[i_row * 64 + j] = (j < i_row && i_row < n) ? -v[x] : 0.f;
+    float* LK = vyM;  // vy / kx column sums are done
+    {
+      const int i = i_row;
+      const float gi = has_row ? sm.gam[i] : 0.f, bi = has_row ? sm.beta[i] : 0.f;
+      float b3 = 0.f;
+      for (int cc = 0; cc < 32; cc += 16) {
+        float v[16];
+        tmem_ld16(tm + kGt1 + cx.lane_base() + 32 * cx.half + cc, v);
+        tmem_ld_wait();
+        if (has_row) {
+          float l16[16];
+#pragma unroll
+          for (int x4 = 0; x4 < 16; x4 += 4) {
+            const int j0 = 32 * cx.half + cc + x4;
+            const float4 kk4 = *reinterpret_cast<const float4*>(sm.kkf + fz(i, j0));
+            const float kv[4] = {kk4.x, kk4.y, kk4.z, kk4.w};
+            float lk[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int x = x4 + u, j = j0 + u;
+              const bool in = (j < i && i < n);
+              const float da = in ? -v[x] : 0.f;
+              const float e = in ? __expf(gi - sm.gam[j]) : 0.f;
+              const float dae = da * e;
+              b3 += dae * kv[u];
+              l16[x] = dae * bi;
+              lk[u] = l16[x] * kv[u];
+            }
+            *reinterpret_cast<float4*>(LK + fz(i, j0)) = make_float4(lk[0], lk[1], lk[2], lk[3]);
+          }
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int cj = ((32 * cx.half + cc) >> 3) + u;
+            *reinterpret_cast<uint4*>(sm.bP + i * 128 + ((cj ^ (i & 7)) << 4)) = pack8(l16 + 8 * u);
+          }
         }
-    }
-    __syncthreads();
-    // dKK + dKK^T (dKK_ij = dA_ij beta_i E_ij), row and column sums for dbeta and dgamma
-    for (int e = tid; e < 64 * 8; e += 256) {
-      const int i = e >> 3, cj = e & 7;
-      float x[8];
-      for (int u = 0; u < 8; ++u) {
-        const int j = cj * 8 + u;
-        float s = 0.f;
-        if (j < i) s += dA[i * 64 + j] * sm.beta[i] * __expf(sm.gam[i] - sm.gam[j]);
-        if (i < j) s += dA[j * 64 + i] * sm.beta[j] * __expf(sm.gam[j] - sm.gam[i]);
-        x[u] = s;
       }
-      *reinterpret_cast<uint4*>(sm.bP + i * 128 + ((cj ^ (i & 7)) << 4)) = pack8(x);
-    }
-    if (tid < 64) {
-      const int i = tid;
-      float b3 = 0.f, ra = 0.f;
-      for (int j = 0; j < i; ++j) {
-        const float ekk = __expf(sm.gam[i] - sm.gam[j]) * sm.kkf[i][j];
-        b3 += dA[i * 64 + j] * ekk;
-        ra += dA[i * 64 + j] * sm.beta[i] * ekk;
-      }
-      sm.db3[i] = b3;
-      sm.rA[i] = ra;
-    } else if (tid < 128) {
-      const int j = tid - 64;
-      float ca = 0.f;
-      for (int i = j + 1; i < 64; ++i) ca += dA[i * 64 + j] * sm.beta[i] * __expf(sm.gam[i] - sm.gam[j]) * sm.kkf[i][j];
-      sm.cA[j] = ca;
+      if (has_row) sm.db3[cx.half][i] = b3;
     }
     sync_generic_to_async();
-    // ---------------- (g) dk += (dKK + dKK^T) K
-    if (tid == 0)
+    // ---------------- (g) dk += (L + L^T) K: the image of L read K-major (L) and MN-major (L^T)
+    if (tid == 0) {
       for (int ks = 0; ks < 4; ++ks)
         umma_bf16(tm + kGtK, kmajor_desc(smem_u32(sm.bP), 8192, ks), mnmajor_desc(smem_u32(sm.k[0]), 8192, ks),
                   idesc_bf16(64, 128, 0, 1), 1);
-    if (!(ok = cx.commit_wait())) break;
-    // ---------------- (h) dgamma -> dg (reverse cumulative sum in the chunk), dbeta
-    if (tid == 0) {
-      float ktsum = 0.f;
-      for (int i = 0; i < n; ++i) ktsum += __expf(gC - sm.gam[i]) * (sm.part[2][i] + sm.part[3][i]);
-      sm.red[0] = ktsum;
-      sm.red[1] = fro;
+      for (int ks = 0; ks < 4; ++ks)
+        umma_bf16(tm + kGtK, mnmajor_desc(smem_u32(sm.bP), 8192, ks), mnmajor_desc(smem_u32(sm.k[0]), 8192, ks),
+                  idesc_bf16(64, 128, 1, 1), 1);
     }
-    __syncthreads();
+    col_sums(sm, LK, nullptr, sm.cA, nullptr, tid);
+    // ---------------- (h) dgamma -> dg (reverse cumulative sum in the chunk), dbeta
     if (tid < 64) {
       const int i = tid;
+      const float ktd = (i < n) ? __expf(gC - sm.gam[i]) * (sm.part[2][i] + sm.part[3][i]) : 0.f;
+      const float kts = warp_sum(ktd);
+      if (cx.lane == 0) sm.red[cx.warp] = kts;  // warps 0 and 1 (the Frobenius partials are consumed)
       float dgam = 0.f;
       if (i < n) {
-        const float ktd = __expf(gC - sm.gam[i]) * (sm.part[2][i] + sm.part[3][i]);
+        const float b3 = sm.db3[0][i] + sm.db3[1][i];
         dgam = sm.part[0][i] + sm.part[1][i] - sm.part[4][i] + sm.part[5][i] + sm.part[6][i] - ktd +
-               sm.beta[i] * sm.Gm[i] * sm.kx[i] + sm.rA[i] - sm.cA[i];
-        if (i == n - 1) dgam += GC * sm.red[1] + sm.red[0];
+               sm.beta[i] * sm.Gm[i] * sm.kx[i] + sm.beta[i] * b3 - sm.cA[i];
       }
       sm.part[7][i] = dgam;
     }
     __syncthreads();
-    if (tid < n) {
-      float s = 0.f;
-      for (int i = n - 1; i >= tid; --i) s += sm.part[7][i];
-      p.dg[(size_t)(tok0 + tid) * Hv + h] = s;
-      p.dbeta[(size_t)(tok0 + tid) * Hv + h] = sm.vy[tid] + sm.Gm[tid] * sm.kx[tid] + sm.db3[tid];
+    if (tid < 64) {
+      // suffix sums over the chunk (two warps), the last token also takes the chunk-end terms
+      const int i = tid;
+      float x = sm.part[7][i];
+      if (i == n - 1) x += GC * fro + (sm.red[0] + sm.red[1]);
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float y = __shfl_down_sync(0xffffffffu, x, o);
+        if (cx.lane + o < 32) x += y;
+      }
+      sm.red4[0][0][i] = x;
     }
     __syncthreads();
+    if (tid < n) {
+      const float s = sm.red4[0][0][tid] + (tid < 32 ? sm.red4[0][0][32] : 0.f);
+      p.dg[(size_t)(tok0 + tid) * Hv + h] = s;
+      p.dbeta[(size_t)(tok0 + tid) * Hv + h] = sm.vy[tid] + sm.Gm[tid] * sm.kx[tid] + sm.db3[0][tid] + sm.db3[1][tid];
+    }
+    if (!(ok = cx.commit_wait())) break;  // (g) done before the next head reuses bP
   }
   if (ok) {
     // dk: sum over the value heads of this key head
@@ -986,7 +1025,7 @@ constexpr uint32_t kDtP = 0, kDt1 = 128, kDt2 = 256;
 
 __global__ void __launch_bounds__(256, 1) dq_kernel(const __grid_constant__ BwdParams p) {
   extern __shared__ uint8_t smem_raw[];
-  DqSmem& sm = *reinterpret_cast<DqSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  DqSmem& sm = *reinterpret_cast<DqSmem*>(smem_align1024(smem_raw));
   __shared__ uint64_t bar_ld, bar_mma;
   __shared__ uint32_t tmem_holder;
   Header* hd = reinterpret_cast<Header*>(p.ws + p.L.f.header);
@@ -1209,11 +1248,11 @@ int launch_bwd(const BwdArgs& a, cudaStream_t stream, cudaEvent_t* ev) {
   }
   mark(9);
   mark(10);
-  if (d.T > 0) {
-    grad_kernel<<<dim3((unsigned)p.L.f.cmax, (unsigned)d.Hk), 256, kGradSmemBytes, stream>>>(p);
-    dq_kernel<<<dim3((unsigned)p.L.f.cmax, (unsigned)d.Hk), 256, kDqSmemBytes, stream>>>(p);
-  }
+  if (d.T > 0) grad_kernel<<<dim3((unsigned)p.L.f.cmax, (unsigned)d.Hk), 256, kGradSmemBytes, stream>>>(p);
   mark(11);
+  mark(14);
+  if (d.T > 0) dq_kernel<<<dim3((unsigned)p.L.f.cmax, (unsigned)d.Hk), 256, kDqSmemBytes, stream>>>(p);
+  mark(15);
   mark(12);
   if (d.n_init > 0) dinit_reduce_kernel<<<d.n_init * d.Hv, 256, 0, stream>>>(p);
   mark(13);

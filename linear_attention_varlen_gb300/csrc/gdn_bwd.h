@@ -27,7 +27,7 @@ struct BwdLayout {
   FwdLayout f;
   size_t st_img;    // S at each chunk start, bf16 image [cmax][Hv][32 KB]
   size_t vp_img;    // V' per chunk, bf16 image [cmax][Hv][16 KB]
-  size_t t_f32;     // T per chunk, fp32 [cmax][Hv][64][64]
+  size_t t_f32;     // T per chunk, fp32 [cmax][Hv][64 x 64] in the fz layout
   size_t ds_img;    // dL/dS at each chunk end, bf16 image [cmax][Hv][32 KB]
   size_t dvp_img;   // dL/dV' per chunk, bf16 image [cmax][Hv][16 KB]
   size_t tw_lo, tu_lo;    // low parts of the WY factors, bf16 images [cmax][Hv][8 KB]

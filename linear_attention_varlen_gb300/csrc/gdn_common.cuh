@@ -128,6 +128,12 @@ GDN_HD int plan_check_doc(int i, const int32_t* cu, const int32_t* init_idx, int
   return kOk;
 }
 
+// fp32 64x64 scratch layout shared by the gradient kernels and the T records of kkt_solve:
+// element (i, j) at i*64 + 4*((j/4 XOR i) mod 16) + j mod 4. Sixteen threads that each own a row
+// and read the same column hit distinct 16-byte granules (at most two to a bank), and a warp that
+// reads a row (consecutive j) stays conflict-free; 4-element groups stay contiguous and aligned.
+GDN_HD int fz(int i, int j) { return i * 64 + ((((j >> 2) ^ i) & 15) << 2) + (j & 3); }
+
 GDN_HD int doc_chunks(int i, const int32_t* cu) { return (cu[i + 1] - cu[i] + kChunk - 1) / kChunk; }
 
 // Segment length in chunks (0 = no split) from the totals of this call.

@@ -168,22 +168,39 @@ __global__ void __launch_bounds__(1024) plan_kernel(const __grid_constant__ FwdP
 
 // ======================================================================================= kkt_solve
 
-// Shared memory of kkt_solve (after 1024-byte alignment).
+// kkt_solve: one CTA of 256 threads per (chunk, key head). K K^T runs once on the tensor cores;
+// the value heads of the group are then processed four at a time, one group of 64 threads per
+// value head: the chunk-local cumulative gate gamma, A = diag(beta) (e^{gamma_i - gamma_j} o K K^T)
+// (strictly lower), T = (I + A)^{-1} by forward substitution with one thread per column of T
+// (x_r = [r == c] - sum_{m<r} A_rm x_m, unrolled, x in registers), and the outputs T diag(beta
+// e^gamma), T diag(beta) as bf16 images (plus T in fp32 and the low bf16 parts in record mode).
+constexpr int kKktHeads = 4;   // value heads solved concurrently
+constexpr int kAStride = 68;   // fp32 row stride of A / T (16-byte aligned rows for vector loads)
 struct KktSmem {
-  uint8_t k_tile[2][8192];  // K rows of the chunk, two 64-wide dk blocks, SW128
-  float kk[64][65];
-  float a[64][65];
-  float t[64][65];
-  float y[3][16][16];
-  float gam[64];
-  float beta[64];
+  uint8_t k_tile[2][8192];               // K rows of the chunk, two 64-wide dk blocks, SW128
+  float kk[64][65];                      // K K^T
+  float a[kKktHeads][64][kAStride];      // A, then T (per concurrent value head)
+  float gam[kKktHeads][64];
+  float beta[kKktHeads][64];
 };
 
-__global__ void __launch_bounds__(128) kkt_solve_kernel(const __grid_constant__ FwdParams p) {
+// Named barrier of one 64-thread value-head group (ids 1-4; literal ids keep the count of
+// hardware barriers the kernel reserves at five).
+__device__ __forceinline__ void group_sync(int group) {
+  switch (group) {
+    case 0: asm volatile("bar.sync 1, 64;" ::: "memory"); break;
+    case 1: asm volatile("bar.sync 2, 64;" ::: "memory"); break;
+    case 2: asm volatile("bar.sync 3, 64;" ::: "memory"); break;
+    default: asm volatile("bar.sync 4, 64;" ::: "memory"); break;
+  }
+}
+
+__global__ void __launch_bounds__(256) kkt_solve_kernel(const __grid_constant__ FwdParams p) {
   extern __shared__ uint8_t smem_raw[];
-  KktSmem& sm = *reinterpret_cast<KktSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  KktSmem& sm = *reinterpret_cast<KktSmem*>(smem_align1024(smem_raw));
   __shared__ uint64_t bar_ld, bar_mma;
   __shared__ uint32_t tmem_holder;
+  __shared__ int s_ld_ok;
   Header* hd = ws_ptr<Header>(p, p.L.header);
   const int chunk = blockIdx.x, hk = blockIdx.y;
   if (chunk >= hd->n_chunks || get_status(hd) != 0) return;
@@ -191,6 +208,7 @@ __global__ void __launch_bounds__(128) kkt_solve_kernel(const __grid_constant__ 
   const int tok0 = ws_ptr<int32_t>(p, p.L.chunk_tok0)[chunk];
   const int n = ws_ptr<int32_t>(p, p.L.chunk_len)[chunk];
   const int Hv = p.d.Hv, G = p.d.Hv / p.d.Hk;
+  const int grp = tid >> 6, t = tid & 63;  // value-head group and its thread (token / column)
 
   if (tid == 0) {
     mbar_init(&bar_ld, 1);
@@ -216,26 +234,22 @@ __global__ void __launch_bounds__(128) kkt_solve_kernel(const __grid_constant__ 
         umma_bf16(tmem, kmajor_desc(kt, 8192, ks), kmajor_desc(kt, 8192, ks), idesc_bf16(64, 64, 0, 0), ks > 0);
       umma_commit(&bar_mma);
     }
+    s_ld_ok = ok ? 1 : 0;
   }
-  // zero T (upper blocks stay zero)
-  for (int e = tid; e < 64 * 65; e += 128) (&sm.t[0][0])[e] = 0.f;
-  __shared__ int s_ld_ok;
-  if (tid == 0) s_ld_ok = ok ? 1 : 0;
   __syncthreads();
   bool ok_mma = false;
   if (s_ld_ok) ok_mma = wait_all(&bar_mma, 0);
   tc_fence_after();
   if (!ok_mma) {
     if (tid == 0) set_status(hd, kErrTimeout);
-  } else {
+  } else if (warp < 4) {
     // K K^T readback (M = 64: row 16q + l sits in lane 32q + l, l < 16)
-    const int q4 = warp & 3;
     for (int c = 0; c < 64; c += 16) {
       float v[16];
-      tmem_ld16(tmem + ((uint32_t)(32 * q4) << 16) + c, v);
+      tmem_ld16(tmem + ((uint32_t)(32 * warp) << 16) + c, v);
       tmem_ld_wait();
       if (lane < 16)
-        for (int i = 0; i < 16; ++i) sm.kk[16 * q4 + lane][c + i] = v[i];
+        for (int i = 0; i < 16; ++i) sm.kk[16 * warp + lane][c + i] = v[i];
     }
   }
   tc_fence_before();
@@ -246,100 +260,96 @@ __global__ void __launch_bounds__(128) kkt_solve_kernel(const __grid_constant__ 
   float* gam_ws = ws_ptr<float>(p, p.L.gam);
   uint8_t* tw_ws = ws_ptr<uint8_t>(p, p.L.tw);
   uint8_t* tu_ws = ws_ptr<uint8_t>(p, p.L.tu);
-  for (int hh = 0; hh < G; ++hh) {
-    const int h = hk * G + hh;
-    // chunk-local cumulative gate (inclusive scan over 64 tokens in two warps)
-    if (tid < 64) {
-      const float gi = (tid < n) ? p.g[(size_t)(tok0 + tid) * Hv + h] : 0.f;
-      const float bi = (tid < n) ? p.beta[(size_t)(tok0 + tid) * Hv + h] : 0.f;
-      float s = gi;
+  float(*A)[kAStride] = sm.a[grp];
+  float* gam = sm.gam[grp];
+  float* bet = sm.beta[grp];
+  for (int hb = 0; hb < G; hb += kKktHeads) {
+    if (hb + grp >= G) break;  // whole group leaves together
+    const int h = hk * G + hb + grp;
+    const size_t rec = (size_t)chunk * Hv + h;
+    // chunk-local cumulative gate: inclusive scan over the 64 tokens in the group's two warps
+    {
+      const float gi = (t < n) ? p.g[(size_t)(tok0 + t) * Hv + h] : 0.f;
+      const float bi = (t < n) ? p.beta[(size_t)(tok0 + t) * Hv + h] : 0.f;
+      float sc = gi;
       for (int off = 1; off < 32; off <<= 1) {
-        const float o = __shfl_up_sync(0xffffffffu, s, off);
-        if (lane >= off) s += o;
+        const float o = __shfl_up_sync(0xffffffffu, sc, off);
+        if (lane >= off) sc += o;
       }
-      sm.gam[tid] = s;
-      sm.beta[tid] = bi;
+      gam[t] = sc;
+      bet[t] = bi;
+      group_sync(grp);
+      if (t >= 32) gam[t] = sc + gam[31];
+      group_sync(grp);
+      gam_ws[rec * 64 + t] = gam[t];
     }
-    __syncthreads();
-    if (tid >= 32 && tid < 64) sm.gam[tid] += sm.gam[31];
-    __syncthreads();
-    if (tid < 64) gam_ws[((size_t)chunk * Hv + h) * 64 + tid] = sm.gam[tid];
-    // A (strictly lower)
-    for (int e = tid; e < 64 * 64; e += 128) {
-      const int i = e >> 6, j = e & 63;
-      sm.a[i][j] = (j < i) ? sm.beta[i] * __expf(sm.gam[i] - sm.gam[j]) * sm.kk[i][j] : 0.f;
+    // A, column t (rows below the diagonal)
+    {
+      const float gt = gam[t];
+      for (int r = t + 1; r < 64; ++r) A[r][t] = bet[r] * __expf(gam[r] - gt) * sm.kk[r][t];
     }
-    __syncthreads();
-    // (I + A)^{-1}: diagonal 16x16 blocks by forward substitution, one warp per block
-    if (lane < 16) {
-      const int b = warp, c = lane;
-      float x[16];
+    group_sync(grp);
+    // T = (I + A)^{-1}, column t: forward substitution (entries above the diagonal come out 0)
+    float x[64];
 #pragma unroll
-      for (int r = 0; r < 16; ++r) {
-        float s = (r == c) ? 1.f : 0.f;
+    for (int r = 0; r < 64; ++r) {
+      // four independent partial sums keep the FMA chain of row r about r/4 long
+      float a0 = (r == t) ? 1.f : 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll
-        for (int m = 0; m < r; ++m) s -= sm.a[16 * b + r][16 * b + m] * x[m];
-        x[r] = s;
+      for (int m = 0; m + 4 <= r; m += 4) {
+        const float4 av = *reinterpret_cast<const float4*>(&A[r][m]);
+        a0 -= av.x * x[m];
+        a1 -= av.y * x[m + 1];
+        a2 -= av.z * x[m + 2];
+        a3 -= av.w * x[m + 3];
       }
 #pragma unroll
-      for (int r = 0; r < 16; ++r) sm.t[16 * b + r][16 * b + c] = x[r];
+      for (int m = r & ~3; m < r; ++m) a0 -= A[r][m] * x[m];
+      x[r] = (a0 + a1) + (a2 + a3);
     }
-    __syncthreads();
-    // off-diagonal blocks by block distance: T_ij = -T_ii sum_{k=j}^{i-1} A_ik T_kj
-    for (int dd = 1; dd < 4; ++dd) {
-      const int nb = 4 - dd;
-      for (int e = tid; e < nb * 256; e += 128) {
-        const int bi = e >> 8, r = (e >> 4) & 15, cc = e & 15;
-        const int i = dd + bi, j = i - dd;
-        float s = 0.f;
-        for (int kb = j; kb < i; ++kb)
+    group_sync(grp);  // every thread is done reading A
 #pragma unroll
-          for (int m = 0; m < 16; ++m) s += sm.a[16 * i + r][16 * kb + m] * sm.t[16 * kb + m][16 * j + cc];
-        sm.y[bi][r][cc] = s;
+    for (int r = 0; r < 64; ++r) A[r][t] = x[r];
+    group_sync(grp);
+    // outputs, row by row (8 threads per 128-byte row of the bf16 images)
+    uint8_t* dw = tw_ws + rec * 8192;
+    uint8_t* du = tu_ws + rec * 8192;
+    float* tdst = p.t_f32 ? p.t_f32 + rec * 4096 : nullptr;
+    for (int e = t; e < 64 * 8; e += 64) {
+      const int r = e >> 3, cj = e & 7;
+      const float4 t0 = *reinterpret_cast<const float4*>(&A[r][8 * cj]);
+      const float4 t1 = *reinterpret_cast<const float4*>(&A[r][8 * cj + 4]);
+      const float tv[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
+      if (tdst) {  // fz layout (the gradient kernel's fp32 scratch layout)
+        *reinterpret_cast<float4*>(tdst + fz(r, 8 * cj)) = t0;
+        *reinterpret_cast<float4*>(tdst + fz(r, 8 * cj + 4)) = t1;
       }
-      __syncthreads();
-      for (int e = tid; e < nb * 256; e += 128) {
-        const int bi = e >> 8, r = (e >> 4) & 15, cc = e & 15;
-        const int i = dd + bi, j = i - dd;
-        float s = 0.f;
+      float xw[8], xu[8];
 #pragma unroll
-        for (int m = 0; m < 16; ++m) s += sm.t[16 * i + r][16 * i + m] * sm.y[bi][m][cc];
-        sm.t[16 * i + r][16 * j + cc] = -s;
+      for (int u = 0; u < 8; ++u) {
+        const int j = 8 * cj + u;
+        xu[u] = tv[u] * bet[j];
+        xw[u] = xu[u] * __expf(gam[j]);
       }
-      __syncthreads();
-    }
-    if (p.t_f32) {
-      float* tdst = p.t_f32 + ((size_t)chunk * Hv + h) * 4096;
-      for (int e = tid; e < 4096; e += 128) tdst[e] = sm.t[e >> 6][e & 63];
-    }
-    // T diag(beta e^gamma) and T diag(beta), bf16, stored as the SW128 K-major smem image
-    uint8_t* dw = tw_ws + ((size_t)chunk * Hv + h) * 8192;
-    uint8_t* du = tu_ws + ((size_t)chunk * Hv + h) * 8192;
-    for (int e = tid; e < 2 * 64 * 8; e += 128) {
-      const int mat = e >> 9, r = (e >> 3) & 63, cj = e & 7;
-      uint32_t w[4], wl[4];
+      const uint32_t off = r * 128 + ((cj ^ (r & 7)) << 4);
+      uint32_t w[4], wl[4], uu[4], ul[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        const int j0 = cj * 8 + 2 * u;
-        float s0 = sm.beta[j0], s1 = sm.beta[j0 + 1];
-        if (mat == 0) {
-          s0 *= __expf(sm.gam[j0]);
-          s1 *= __expf(sm.gam[j0 + 1]);
-        }
-        const float x0 = sm.t[r][j0] * s0, x1 = sm.t[r][j0 + 1] * s1;
-        w[u] = pack_bf16x2(x0, x1);
-        const __nv_bfloat162 hb = *reinterpret_cast<const __nv_bfloat162*>(&w[u]);
-        const float2 hf = __bfloat1622float2(hb);
-        wl[u] = pack_bf16x2(x0 - hf.x, x1 - hf.y);
+        w[u] = pack_bf16x2(xw[2 * u], xw[2 * u + 1]);
+        uu[u] = pack_bf16x2(xu[2 * u], xu[2 * u + 1]);
+        const float2 hw = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[u]));
+        const float2 hu = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&uu[u]));
+        wl[u] = pack_bf16x2(xw[2 * u] - hw.x, xw[2 * u + 1] - hw.y);
+        ul[u] = pack_bf16x2(xu[2 * u] - hu.x, xu[2 * u + 1] - hu.y);
       }
-      uint8_t* dst = (mat == 0 ? dw : du) + r * 128 + ((cj ^ (r & 7)) << 4);
-      *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+      *reinterpret_cast<uint4*>(dw + off) = make_uint4(w[0], w[1], w[2], w[3]);
+      *reinterpret_cast<uint4*>(du + off) = make_uint4(uu[0], uu[1], uu[2], uu[3]);
       if (p.tw_lo) {
-        uint8_t* lo = (mat == 0 ? p.tw_lo : p.tu_lo) + ((size_t)chunk * Hv + h) * 8192 + r * 128 + ((cj ^ (r & 7)) << 4);
-        *reinterpret_cast<uint4*>(lo) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+        *reinterpret_cast<uint4*>(p.tw_lo + rec * 8192 + off) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+        *reinterpret_cast<uint4*>(p.tu_lo + rec * 8192 + off) = make_uint4(ul[0], ul[1], ul[2], ul[3]);
       }
     }
-    __syncthreads();
+    group_sync(grp);  // A / gam / beta are rewritten by the next head of this group
   }
 }
 
@@ -1079,7 +1089,7 @@ constexpr int kTransWindow = 12;  // chunks of the transition evaluated first (s
 template <int kMode, bool kRec>
 __global__ void __launch_bounds__(kRec ? 256 : kWsThreads, 1) chain_kernel(const __grid_constant__ FwdParams p) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* base = smem_align1024(smem_raw);
   ChainSmem* smp = reinterpret_cast<ChainSmem*>(base);
   WsSmem* wss = reinterpret_cast<WsSmem*>(base);
   __shared__ uint64_t bar_ld, bar_mma;
@@ -1417,7 +1427,7 @@ int launch_fwd(const FwdParams& p, cudaStream_t stream, cudaEvent_t* ev) {
   mark(2);
   if (p.d.T > 0) {
     dim3 grid((unsigned)p.L.cmax, (unsigned)p.d.Hk);
-    kkt_solve_kernel<<<grid, 128, sizeof(KktSmem) + 1024, stream>>>(p);
+    kkt_solve_kernel<<<grid, 256, sizeof(KktSmem) + 1024, stream>>>(p);
   }
   mark(3);
   const int64_t items_cap = (int64_t)p.d.num_sms;

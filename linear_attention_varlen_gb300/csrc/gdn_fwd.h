@@ -27,7 +27,7 @@ struct FwdParams {
   // Backward recompute only (all NULL for a plain forward): per (chunk, value head) records
   uint8_t* st_img;  // S at each chunk start, bf16, 128B-swizzled smem image [cmax][Hv][32 KB]
   uint8_t* vp_img;  // V' = U - W S of each chunk, bf16 smem image [cmax][Hv][16 KB]
-  float* t_f32;     // T = (I + A)^{-1}, fp32 [cmax][Hv][64][64]
+  float* t_f32;     // T = (I + A)^{-1}, fp32 [cmax][Hv][64 x 64] in the fz layout
   // Compensated bf16 (x = hi + lo, both bf16) for the backward recompute: the low parts of
   // T diag(beta e^gamma) and T diag(beta) (written by kkt_solve, read by the chain), and of
   // S and V' (written by the chain for the gradient kernels).
