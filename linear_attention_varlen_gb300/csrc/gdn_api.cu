@@ -161,7 +161,8 @@ int gdn_chunk_fwd(const void* q, const void* k, const void* v, const float* g, c
     const uint64_t row_k = (uint64_t)H_k * kDim * 2, row_v = (uint64_t)H_v * kDim * 2;
     if (!make_tmap_bf16_3d(&p.tm_q, q, kDim, H_k, T, kDim * 2, row_k, 64, 1, 64) ||
         !make_tmap_bf16_3d(&p.tm_k, k, kDim, H_k, T, kDim * 2, row_k, 64, 1, 64) ||
-        !make_tmap_bf16_3d(&p.tm_v, v, kDim, H_v, T, kDim * 2, row_v, 64, 1, 64))
+        !make_tmap_bf16_3d(&p.tm_v, v, kDim, H_v, T, kDim * 2, row_v, 64, 1, 64) ||
+        !make_tmap_bf16_3d(&p.tm_o, out, kDim, H_v, T, kDim * 2, row_v, 64, 1, 64))
       return GDN_ERR_CUDA;
   }
   p.g = g;
@@ -174,6 +175,7 @@ int gdn_chunk_fwd(const void* q, const void* k, const void* v, const float* g, c
   p.ws = reinterpret_cast<uint8_t*>(workspace);
   p.trunc_thr = o.trunc_log_threshold;
   p.scale = o.scale;
+  p.p_img = p.ws + p.L.pimg;
   return launch_fwd(p, (cudaStream_t)stream, reinterpret_cast<cudaEvent_t*>(o.stage_events));
 }
 

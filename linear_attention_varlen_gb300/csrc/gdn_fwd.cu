@@ -174,14 +174,22 @@ __global__ void __launch_bounds__(1024) plan_kernel(const __grid_constant__ FwdP
 // (strictly lower), T = (I + A)^{-1} by forward substitution with one thread per column of T
 // (x_r = [r == c] - sum_{m<r} A_rm x_m, unrolled, x in registers), and the outputs T diag(beta
 // e^gamma), T diag(beta) as bf16 images (plus T in fp32 and the low bf16 parts in record mode).
+// A plain forward also computes Q K^T once per key head (tensor cores) and writes P = scale
+// (Q K^T o E) per value head as a bf16 image, so that the state chain never forms it.
+// The decay factors e^{gamma_i - gamma_j} (j <= i) are taken as e^{gamma_i} e^{-gamma_j} when the
+// chunk's total decay is above -80 (both factors then stay finite in fp32), else one exp each.
 constexpr int kKktHeads = 4;   // value heads solved concurrently
 constexpr int kAStride = 68;   // fp32 row stride of A / T (16-byte aligned rows for vector loads)
+constexpr float kFactorMin = -80.f;
 struct KktSmem {
-  uint8_t k_tile[2][8192];               // K rows of the chunk, two 64-wide dk blocks, SW128
+  uint8_t k_tile[2][8192];               // K rows, two 64-wide dk blocks, SW128; then Q K^T fp32 (fz)
+  float a[kKktHeads][64][kAStride];      // A, then T (per concurrent value head); before the solve
+                                         // the first 16 KB hold the Q tile (forward: Q K^T)
   float kk[64][65];                      // K K^T
-  float a[kKktHeads][64][kAStride];      // A, then T (per concurrent value head)
   float gam[kKktHeads][64];
   float beta[kKktHeads][64];
+  float eg[kKktHeads][64];               // e^{gamma}
+  float egi[kKktHeads][64];              // e^{-gamma} (factored path only)
 };
 
 // Named barrier of one 64-thread value-head group (ids 1-4; literal ids keep the count of
@@ -215,16 +223,22 @@ __global__ void __launch_bounds__(256) kkt_solve_kernel(const __grid_constant__ 
     mbar_init(&bar_mma, 1);
     fence_mbar_init();
   }
-  if (warp == 0) tmem_alloc(&tmem_holder, 64);
+  const bool want_p = p.p_img != nullptr;
+  if (warp == 0) tmem_alloc(&tmem_holder, 128);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_holder;
   bool ok = true;
+  uint8_t* q_tile = reinterpret_cast<uint8_t*>(&sm.a[0][0][0]);
   if (tid == 0) {
-    mbar_arrive_expect_tx(&bar_ld, 16384);
+    mbar_arrive_expect_tx(&bar_ld, want_p ? 32768 : 16384);
     tma_load_3d(sm.k_tile[0], &p.tm_k, 0, hk, tok0, &bar_ld);
     tma_load_3d(sm.k_tile[1], &p.tm_k, 64, hk, tok0, &bar_ld);
+    if (want_p) {
+      tma_load_3d(q_tile, &p.tm_q, 0, hk, tok0, &bar_ld);
+      tma_load_3d(q_tile + 8192, &p.tm_q, 64, hk, tok0, &bar_ld);
+    }
     ok = mbar_wait(&bar_ld, 0, kWaitBudget);
     if (!ok) mbar_wait(&bar_ld, 0, kWaitBudget);  // let a late copy land before the CTA can exit
     if (ok) {
@@ -232,6 +246,10 @@ __global__ void __launch_bounds__(256) kkt_solve_kernel(const __grid_constant__ 
       const uint32_t kt = smem_u32(sm.k_tile[0]);
       for (int ks = 0; ks < 8; ++ks)
         umma_bf16(tmem, kmajor_desc(kt, 8192, ks), kmajor_desc(kt, 8192, ks), idesc_bf16(64, 64, 0, 0), ks > 0);
+      if (want_p)
+        for (int ks = 0; ks < 8; ++ks)
+          umma_bf16(tmem + 64, kmajor_desc(smem_u32(q_tile), 8192, ks), kmajor_desc(kt, 8192, ks),
+                    idesc_bf16(64, 64, 0, 0), ks > 0);
       umma_commit(&bar_mma);
     }
     s_ld_ok = ok ? 1 : 0;
@@ -240,21 +258,31 @@ __global__ void __launch_bounds__(256) kkt_solve_kernel(const __grid_constant__ 
   bool ok_mma = false;
   if (s_ld_ok) ok_mma = wait_all(&bar_mma, 0);
   tc_fence_after();
+  float* qk = reinterpret_cast<float*>(sm.k_tile[0]);  // the K tile is dead once the products are done
   if (!ok_mma) {
     if (tid == 0) set_status(hd, kErrTimeout);
-  } else if (warp < 4) {
-    // K K^T readback (M = 64: row 16q + l sits in lane 32q + l, l < 16)
-    for (int c = 0; c < 64; c += 16) {
-      float v[16];
-      tmem_ld16(tmem + ((uint32_t)(32 * warp) << 16) + c, v);
-      tmem_ld_wait();
-      if (lane < 16)
-        for (int i = 0; i < 16; ++i) sm.kk[16 * warp + lane][c + i] = v[i];
-    }
+  } else {
+    // readback (M = 64: row 16q + l sits in lane 32q + l, l < 16): warps 0-3 K K^T, warps 4-7 Q K^T
+    const int q4 = warp & 3;
+    if (warp < 4 || want_p)
+      for (int c = 0; c < 64; c += 16) {
+        float v[16];
+        tmem_ld16(tmem + ((uint32_t)(32 * q4) << 16) + (warp < 4 ? 0 : 64) + c, v);
+        tmem_ld_wait();
+        if (lane < 16) {
+          const int r = 16 * q4 + lane;
+          if (warp < 4)
+            for (int i = 0; i < 16; ++i) sm.kk[r][c + i] = v[i];
+          else
+            for (int i = 0; i < 16; i += 4)
+              *reinterpret_cast<float4*>(qk + fz(r, c + i)) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+        }
+      }
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) tmem_dealloc(tmem, 64);
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(tmem, 128);
   if (!ok_mma) return;
 
   float* gam_ws = ws_ptr<float>(p, p.L.gam);
@@ -263,93 +291,150 @@ __global__ void __launch_bounds__(256) kkt_solve_kernel(const __grid_constant__ 
   float(*A)[kAStride] = sm.a[grp];
   float* gam = sm.gam[grp];
   float* bet = sm.beta[grp];
+  float* eg = sm.eg[grp];
+  float* egi = sm.egi[grp];
+  const int sub = t >> 5;  // warp of the group: columns 32 sub ..; rows and terms below 32 sub are zero
   for (int hb = 0; hb < G; hb += kKktHeads) {
-    if (hb + grp >= G) break;  // whole group leaves together
-    const int h = hk * G + hb + grp;
-    const size_t rec = (size_t)chunk * Hv + h;
-    // chunk-local cumulative gate: inclusive scan over the 64 tokens in the group's two warps
-    {
-      const float gi = (t < n) ? p.g[(size_t)(tok0 + t) * Hv + h] : 0.f;
-      const float bi = (t < n) ? p.beta[(size_t)(tok0 + t) * Hv + h] : 0.f;
-      float sc = gi;
-      for (int off = 1; off < 32; off <<= 1) {
-        const float o = __shfl_up_sync(0xffffffffu, sc, off);
-        if (lane >= off) sc += o;
+    if (hb + grp < G) {  // groups without a head this round skip to the CTA barrier below
+      const int h = hk * G + hb + grp;
+      const size_t rec = (size_t)chunk * Hv + h;
+      // chunk-local cumulative gate: inclusive scan over the 64 tokens in the group's two warps
+      {
+        const float gi = (t < n) ? p.g[(size_t)(tok0 + t) * Hv + h] : 0.f;
+        const float bi = (t < n) ? p.beta[(size_t)(tok0 + t) * Hv + h] : 0.f;
+        float sc = gi;
+        for (int off = 1; off < 32; off <<= 1) {
+          const float o = __shfl_up_sync(0xffffffffu, sc, off);
+          if (lane >= off) sc += o;
+        }
+        gam[t] = sc;
+        bet[t] = bi;
+        group_sync(grp);
+        if (t >= 32) sc += gam[31];
+        gam_ws[rec * 64 + t] = sc;
+        eg[t] = __expf(sc);
+        egi[t] = __expf(-sc);
+        group_sync(grp);
+        if (t >= 32) gam[t] = sc;
+        group_sync(grp);
       }
-      gam[t] = sc;
-      bet[t] = bi;
+      const bool factored = gam[63] > kFactorMin;  // gamma is nonincreasing: gam[63] is the minimum
+      // A, column t (rows below the diagonal)
+      {
+        const float gt = gam[t], et = egi[t];
+        if (factored) {
+#pragma unroll 4
+          for (int r = t + 1; r < 64; ++r) A[r][t] = bet[r] * eg[r] * et * sm.kk[r][t];
+        } else {
+#pragma unroll 4
+          for (int r = t + 1; r < 64; ++r) A[r][t] = bet[r] * __expf(gam[r] - gt) * sm.kk[r][t];
+        }
+      }
       group_sync(grp);
-      if (t >= 32) gam[t] = sc + gam[31];
+      // T = (I + A)^{-1}, column t: forward substitution (entries above the diagonal come out 0);
+      // the second warp of the group (columns 32-63) skips rows and terms below 32, which are zero
+      float x[64];
+      if (sub == 0) {
+#pragma unroll
+        for (int r = 0; r < 64; ++r) {
+          // four independent partial sums keep the FMA chain of row r about r/4 long
+          float a0 = (r == t) ? 1.f : 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+          for (int m = 0; m + 4 <= r; m += 4) {
+            const float4 av = *reinterpret_cast<const float4*>(&A[r][m]);
+            a0 -= av.x * x[m];
+            a1 -= av.y * x[m + 1];
+            a2 -= av.z * x[m + 2];
+            a3 -= av.w * x[m + 3];
+          }
+#pragma unroll
+          for (int m = r & ~3; m < r; ++m) a0 -= A[r][m] * x[m];
+          x[r] = (a0 + a1) + (a2 + a3);
+        }
+      } else {
+#pragma unroll
+        for (int r = 0; r < 32; ++r) x[r] = 0.f;
+#pragma unroll
+        for (int r = 32; r < 64; ++r) {
+          float a0 = (r == t) ? 1.f : 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+          for (int m = 32; m + 4 <= r; m += 4) {
+            const float4 av = *reinterpret_cast<const float4*>(&A[r][m]);
+            a0 -= av.x * x[m];
+            a1 -= av.y * x[m + 1];
+            a2 -= av.z * x[m + 2];
+            a3 -= av.w * x[m + 3];
+          }
+#pragma unroll
+          for (int m = r & ~3; m < r; ++m) a0 -= A[r][m] * x[m];
+          x[r] = (a0 + a1) + (a2 + a3);
+        }
+      }
+      group_sync(grp);  // every thread is done reading A
+#pragma unroll
+      for (int r = 0; r < 64; ++r) A[r][t] = x[r];
       group_sync(grp);
-      gam_ws[rec * 64 + t] = gam[t];
+      // outputs, row by row (8 threads per 128-byte row of the bf16 images)
+      uint8_t* dw = tw_ws + rec * 8192;
+      uint8_t* du = tu_ws + rec * 8192;
+      float* tdst = p.t_f32 ? p.t_f32 + rec * 4096 : nullptr;
+      for (int e = t; e < 64 * 8; e += 64) {
+        const int r = e >> 3, cj = e & 7;
+        const float4 t0 = *reinterpret_cast<const float4*>(&A[r][8 * cj]);
+        const float4 t1 = *reinterpret_cast<const float4*>(&A[r][8 * cj + 4]);
+        const float tv[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
+        if (tdst) {  // fz layout (the gradient kernel's fp32 scratch layout)
+          *reinterpret_cast<float4*>(tdst + fz(r, 8 * cj)) = t0;
+          *reinterpret_cast<float4*>(tdst + fz(r, 8 * cj + 4)) = t1;
+        }
+        float xw[8], xu[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int j = 8 * cj + u;
+          xu[u] = tv[u] * bet[j];
+          xw[u] = xu[u] * eg[j];
+        }
+        const uint32_t off = r * 128 + ((cj ^ (r & 7)) << 4);
+        uint32_t w[4], wl[4], uu[4], ul[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          w[u] = pack_bf16x2(xw[2 * u], xw[2 * u + 1]);
+          uu[u] = pack_bf16x2(xu[2 * u], xu[2 * u + 1]);
+          const float2 hw = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[u]));
+          const float2 hu = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&uu[u]));
+          wl[u] = pack_bf16x2(xw[2 * u] - hw.x, xw[2 * u + 1] - hw.y);
+          ul[u] = pack_bf16x2(xu[2 * u] - hu.x, xu[2 * u + 1] - hu.y);
+        }
+        *reinterpret_cast<uint4*>(dw + off) = make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<uint4*>(du + off) = make_uint4(uu[0], uu[1], uu[2], uu[3]);
+        if (p.tw_lo) {
+          *reinterpret_cast<uint4*>(p.tw_lo + rec * 8192 + off) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+          *reinterpret_cast<uint4*>(p.tu_lo + rec * 8192 + off) = make_uint4(ul[0], ul[1], ul[2], ul[3]);
+        }
+      }
+      // P = scale (Q K^T o E): rows i < n, j <= i, 8 threads per 128-byte row
+      if (want_p) {
+        uint8_t* dp = p.p_img + rec * 8192;
+        for (int e = t; e < 64 * 8; e += 64) {
+          const int i = e >> 3, cj = e & 7;
+          const float4 q0 = *reinterpret_cast<const float4*>(qk + fz(i, 8 * cj));
+          const float4 q1 = *reinterpret_cast<const float4*>(qk + fz(i, 8 * cj + 4));
+          const float qv[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+          const float gi = gam[i], ei = eg[i] * p.scale;
+          float pv[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const int j = 8 * cj + u;
+            const float e2 = factored ? ei * egi[j] : __expf(gi - gam[j]) * p.scale;
+            pv[u] = (j <= i && i < n) ? e2 * qv[u] : 0.f;
+          }
+          *reinterpret_cast<uint4*>(dp + i * 128 + ((cj ^ (i & 7)) << 4)) =
+              make_uint4(pack_bf16x2(pv[0], pv[1]), pack_bf16x2(pv[2], pv[3]), pack_bf16x2(pv[4], pv[5]),
+                         pack_bf16x2(pv[6], pv[7]));
+        }
+      }
+      group_sync(grp);  // A / gam / beta are rewritten by the next head of this group
     }
-    // A, column t (rows below the diagonal)
-    {
-      const float gt = gam[t];
-      for (int r = t + 1; r < 64; ++r) A[r][t] = bet[r] * __expf(gam[r] - gt) * sm.kk[r][t];
-    }
-    group_sync(grp);
-    // T = (I + A)^{-1}, column t: forward substitution (entries above the diagonal come out 0)
-    float x[64];
-#pragma unroll
-    for (int r = 0; r < 64; ++r) {
-      // four independent partial sums keep the FMA chain of row r about r/4 long
-      float a0 = (r == t) ? 1.f : 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-#pragma unroll
-      for (int m = 0; m + 4 <= r; m += 4) {
-        const float4 av = *reinterpret_cast<const float4*>(&A[r][m]);
-        a0 -= av.x * x[m];
-        a1 -= av.y * x[m + 1];
-        a2 -= av.z * x[m + 2];
-        a3 -= av.w * x[m + 3];
-      }
-#pragma unroll
-      for (int m = r & ~3; m < r; ++m) a0 -= A[r][m] * x[m];
-      x[r] = (a0 + a1) + (a2 + a3);
-    }
-    group_sync(grp);  // every thread is done reading A
-#pragma unroll
-    for (int r = 0; r < 64; ++r) A[r][t] = x[r];
-    group_sync(grp);
-    // outputs, row by row (8 threads per 128-byte row of the bf16 images)
-    uint8_t* dw = tw_ws + rec * 8192;
-    uint8_t* du = tu_ws + rec * 8192;
-    float* tdst = p.t_f32 ? p.t_f32 + rec * 4096 : nullptr;
-    for (int e = t; e < 64 * 8; e += 64) {
-      const int r = e >> 3, cj = e & 7;
-      const float4 t0 = *reinterpret_cast<const float4*>(&A[r][8 * cj]);
-      const float4 t1 = *reinterpret_cast<const float4*>(&A[r][8 * cj + 4]);
-      const float tv[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
-      if (tdst) {  // fz layout (the gradient kernel's fp32 scratch layout)
-        *reinterpret_cast<float4*>(tdst + fz(r, 8 * cj)) = t0;
-        *reinterpret_cast<float4*>(tdst + fz(r, 8 * cj + 4)) = t1;
-      }
-      float xw[8], xu[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int j = 8 * cj + u;
-        xu[u] = tv[u] * bet[j];
-        xw[u] = xu[u] * __expf(gam[j]);
-      }
-      const uint32_t off = r * 128 + ((cj ^ (r & 7)) << 4);
-      uint32_t w[4], wl[4], uu[4], ul[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        w[u] = pack_bf16x2(xw[2 * u], xw[2 * u + 1]);
-        uu[u] = pack_bf16x2(xu[2 * u], xu[2 * u + 1]);
-        const float2 hw = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[u]));
-        const float2 hu = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&uu[u]));
-        wl[u] = pack_bf16x2(xw[2 * u] - hw.x, xw[2 * u + 1] - hw.y);
-        ul[u] = pack_bf16x2(xu[2 * u] - hu.x, xu[2 * u + 1] - hu.y);
-      }
-      *reinterpret_cast<uint4*>(dw + off) = make_uint4(w[0], w[1], w[2], w[3]);
-      *reinterpret_cast<uint4*>(du + off) = make_uint4(uu[0], uu[1], uu[2], uu[3]);
-      if (p.tw_lo) {
-        *reinterpret_cast<uint4*>(p.tw_lo + rec * 8192 + off) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
-        *reinterpret_cast<uint4*>(p.tu_lo + rec * 8192 + off) = make_uint4(ul[0], ul[1], ul[2], ul[3]);
-      }
-    }
-    group_sync(grp);  // A / gam / beta are rewritten by the next head of this group
   }
 }
 
@@ -769,20 +854,23 @@ __device__ bool affine_apply(const FwdParams& p, ChainCtx& cx, SM& sm, const flo
 // =========================================================================== warp-specialized chain
 //
 // The forward chain with three roles in one CTA of 10 warps:
-//   warp 8      TMA producer: K, V, T_u and gamma of chunk j into stage j & 1; Q and T_w (one buffer).
+//   warp 8      TMA producer: K, V, T_u, P (from kkt_solve) and gamma of chunk j into stage j & 1;
+//               Q and T_w (one buffer).
 //   warp 9      MMA issuer (one lane), per chunk j:
-//                 U = [*; T_u] V -> D2 rows 64-127, D1 = [Q~; -W] S, then chunk j+1's W = T_w K and
-//                 Q K^T (staged by the epilogue while chunk j runs), then D2 = K^T V'_s, D1 += [P; *] V'.
-//   warps 0-7   epilogue: V' = U - W S, staging of chunk j+1 (-W, P, Q~), S += K^T V'_s, O.
+//                 U = [*; T_u] V -> D2 rows 64-127, D1 = [Q~; -W] S, then chunk j+1's W = T_w K
+//                 (staged by the epilogue while chunk j runs), then D2 = K^T V'_s, D1 += [P; *] V'.
+//   warps 0-7   epilogue: V' = U - W S, staging of chunk j+1 (-W, Q~), S += K^T V'_s, O.
 // Hand-offs are mbarriers only: tcgen05.commit from the issuer, one elected arrival from the
 // epilogue after a named barrier, TMA transaction counts from the producer. Rows 0-63 of the U
 // product and rows 64-127 of the P product are never read, so neither operand needs zero rows.
 
 struct WsSmem {
   uint8_t k[2][16384];   // [stage] K rows t, two dk blocks     (B K-major, B MN-major, A MN-major)
-  uint8_t v[2][16384];   // [stage] V rows t, two dv blocks     (B MN-major)
+  uint8_t v[1][16384];   // V rows t, two dv blocks (one buffer, refilled once U is done) (B MN-major)
+  uint8_t ostage[2][8192];  // O rows t, two dv blocks (bf16), the source of the TMA store; in a
+                            // run without outputs, the second V buffer
   uint8_t q[2][8192];    // Q rows t, two dk blocks (one buffer) (A K-major)
-  uint8_t pt[4][8192];   // P stage 0, P stage 1, T_u stage 0, T_u stage 1 (contiguous)
+  uint8_t pt[4][8192];   // P stage 0, P stage 1, T_u stage 0, T_u stage 1 (contiguous; TMA-loaded)
   uint8_t tw[8192];      // T diag(beta e^gamma) (one buffer)  (A, M = 64)
   uint8_t qw[2][16384];  // dk block b: rows 0-63 Q~, rows 64-127 -W   (A, M = 128)
   uint8_t vo[2][8192];   // V'                                  (B MN-major)
@@ -794,11 +882,15 @@ constexpr size_t kSmemBytes = (sizeof(WsSmem) > sizeof(ChainSmem) ? sizeof(WsSme
 constexpr int kWsThreads = 320;
 
 struct WsBars {
-  uint64_t full[2], fullq, empty[2], emptyq, a_done, pre_done, b_done, epi1, staged, epi2;
+  uint64_t full[2], fullq, empty[2], emptyq, a_done, pre_done, b_done, epi1, staged, epi2, vfree;
 };
 struct WsPhase {
-  uint32_t full[2], fullq, empty[2], emptyq, a_done, pre_done, b_done, epi1, staged, epi2;
+  uint32_t full[2], fullq, empty[2], emptyq, a_done, pre_done, b_done, epi1, staged, epi2, vfree;
 };
+// TMEM columns of D1 for chunk j: two accumulators in turn, so that the output of chunk j is
+// read while chunk j + 1 already runs (columns 384-511 hold Q K^T only in the record path).
+__device__ __forceinline__ uint32_t d1_col(int j) { return (j & 1) ? 384u : kTmD1; }
+__device__ __forceinline__ void o_sync() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
 
 __device__ __forceinline__ void e_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
@@ -834,6 +926,10 @@ __device__ bool run_ws(const FwdParams& p, ChainCtx& cx, WsBars& bb, WsPhase& ph
   const int Hv = p.d.Hv;
   const int32_t* ctok = ws_ptr<int32_t>(p, p.L.chunk_tok0);
   const int32_t* clen = ws_ptr<int32_t>(p, p.L.chunk_len);
+  // A run without outputs has no use for the O stage: V then alternates between sm.v and the O
+  // stage (released with the rest of the stage), else V has one buffer refilled after each U.
+  const bool dbl_v = gc_out >= gc1;
+  auto vbuf = [&](int j) -> uint8_t* { return (dbl_v && (j & 1)) ? sm.ostage[0] : sm.v[0]; };
 
   if (cx.warp == 8) {
     // ------------------------------------------------------------------ TMA producer
@@ -843,14 +939,11 @@ __device__ bool run_ws(const FwdParams& p, ChainCtx& cx, WsBars& bb, WsPhase& ph
         const bool out = gc >= gc_out;
         if (j >= 2) role_wait(&bb.empty[st], ph.empty[st], abort);
         if (*abort) break;
-        mbar_arrive_expect_tx(&bb.full[st], 16384 + 256 + (kWithU ? 16384 + 8192 : 0));
+        mbar_arrive_expect_tx(&bb.full[st], 16384 + 256 + (kWithU ? 16384 + 8192 : 0) + (out ? 8192 : 0));
+        if (out) bulk_load(sm.pt[st], p.p_img + ((size_t)gc * Hv + h) * 8192, 8192, &bb.full[st]);
         tma_load_3d(sm.k[st], &p.tm_k, 0, hk, tok0, &bb.full[st]);
         tma_load_3d(sm.k[st] + 8192, &p.tm_k, 64, hk, tok0, &bb.full[st]);
-        if (kWithU) {
-          tma_load_3d(sm.v[st], &p.tm_v, 0, h, tok0, &bb.full[st]);
-          tma_load_3d(sm.v[st] + 8192, &p.tm_v, 64, h, tok0, &bb.full[st]);
-          bulk_load(sm.pt[2 + st], p.ws + p.L.tu + ((size_t)gc * Hv + h) * 8192, 8192, &bb.full[st]);
-        }
+        if (kWithU) bulk_load(sm.pt[2 + st], p.ws + p.L.tu + ((size_t)gc * Hv + h) * 8192, 8192, &bb.full[st]);
         bulk_load(sm.gam[st], p.ws + p.L.gam + ((size_t)gc * Hv + h) * 256, 256, &bb.full[st]);
         if (j >= 1) role_wait(&bb.emptyq, ph.emptyq, abort);
         if (*abort) break;
@@ -860,10 +953,18 @@ __device__ bool run_ws(const FwdParams& p, ChainCtx& cx, WsBars& bb, WsPhase& ph
           tma_load_3d(sm.q[1], &p.tm_q, 64, hk, tok0, &bb.fullq);
         }
         bulk_load(sm.tw, p.ws + p.L.tw + ((size_t)gc * Hv + h) * 8192, 8192, &bb.fullq);
+        if (kWithU) {
+          // V of chunk j (counted in full[st]) once the U product of chunk j - 1 has read the buffer
+          if (!dbl_v && j >= 1) role_wait(&bb.vfree, ph.vfree, abort);
+          if (*abort) break;
+          tma_load_3d(vbuf(j), &p.tm_v, 0, h, tok0, &bb.full[st]);
+          tma_load_3d(vbuf(j) + 8192, &p.tm_v, 64, h, tok0, &bb.full[st]);
+        }
       }
       // drain: wait for the release of the last uses so that every phase is consumed
       for (int j = (n >= 2 ? n - 2 : 0); j < n; ++j) role_wait(&bb.empty[j & 1], ph.empty[j & 1], abort);
       role_wait(&bb.emptyq, ph.emptyq, abort);
+      if (kWithU && !dbl_v) role_wait(&bb.vfree, ph.vfree, abort);
     }
     return !*abort;
   }
@@ -877,10 +978,6 @@ __device__ bool run_ws(const FwdParams& p, ChainCtx& cx, WsBars& bb, WsPhase& ph
         for (int ks = 0; ks < 4; ++ks)
           umma_bf16(tm + kTmW, kmajor_desc(smem_u32(sm.tw), 8192, ks), mnmajor_desc(k0, 8192, ks),
                     idesc_bf16(64, 128, 0, 1), ks > 0);
-        if (gc0 + j >= gc_out)
-          for (int ks = 0; ks < 8; ++ks)
-            umma_bf16(tm + kTmG, kmajor_desc(smem_u32(sm.q[0]), 8192, ks), kmajor_desc(k0, 8192, ks),
-                      idesc_bf16(64, 64, 0, 0), ks > 0);
         umma_commit(&bb.pre_done);
         umma_commit(&bb.emptyq);
       };
@@ -893,14 +990,16 @@ __device__ bool run_ws(const FwdParams& p, ChainCtx& cx, WsBars& bb, WsPhase& ph
         role_wait(&bb.staged, ph.staged, abort);
         role_wait(&bb.epi2, ph.epi2, abort);
         if (*abort) break;
+        const uint32_t d1 = tm + d1_col(j);
         if (kWithU)
           for (int ks = 0; ks < 4; ++ks)
             umma_bf16(tm + kTmD2, kmajor_desc(smem_u32(sm.pt[1 + st]), 16384, ks),
-                      mnmajor_desc(smem_u32(sm.v[st]), 8192, ks), idesc_bf16(128, 128, 0, 1), ks > 0);
+                      mnmajor_desc(smem_u32(vbuf(j)), 8192, ks), idesc_bf16(128, 128, 0, 1), ks > 0);
         for (int ks = 0; ks < 8; ++ks)
-          umma_bf16(tm + kTmD1, kmajor_desc(smem_u32(sm.qw[0]), 16384, ks), mnmajor_desc(smem_u32(sm.s[0]), 16384, ks),
+          umma_bf16(d1, kmajor_desc(smem_u32(sm.qw[0]), 16384, ks), mnmajor_desc(smem_u32(sm.s[0]), 16384, ks),
                     idesc_bf16(128, 128, 0, 1), ks > 0);
         umma_commit(&bb.a_done);
+        if (kWithU && !dbl_v) umma_commit(&bb.vfree);
         if (j + 1 < n) {
           role_wait(&bb.full[st ^ 1], ph.full[st ^ 1], abort);
           role_wait(&bb.fullq, ph.fullq, abort);
@@ -914,7 +1013,7 @@ __device__ bool run_ws(const FwdParams& p, ChainCtx& cx, WsBars& bb, WsPhase& ph
                     idesc_bf16(128, 128, 1, 1), ks > 0);
         if (out)
           for (int ks = 0; ks < 4; ++ks)
-            umma_bf16(tm + kTmD1, kmajor_desc(smem_u32(sm.pt[j & 1]), 16384, ks),
+            umma_bf16(d1, kmajor_desc(smem_u32(sm.pt[j & 1]), 16384, ks),
                       mnmajor_desc(smem_u32(sm.vo[0]), 8192, ks), idesc_bf16(128, 128, 0, 1), 1);
         umma_commit(&bb.b_done);
         umma_commit(&bb.empty[st]);
@@ -968,30 +1067,6 @@ __device__ bool run_ws(const FwdParams& p, ChainCtx& cx, WsBars& bb, WsPhase& ph
         }
       }
     }
-    if (out) {
-      const int nn = clen[gc];
-      float v[32];
-      tmem_ld16(cx.tmem + kTmG + lane_base + 32 * cx.half, v);
-      tmem_ld16(cx.tmem + kTmG + lane_base + 32 * cx.half + 16, v + 16);
-      tmem_ld_wait();
-      if (cx.lane < 16) {
-        const float gi = gm[i];
-        uint8_t* pb = sm.pt[j & 1];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          float pv[8];
-#pragma unroll
-          for (int x = 0; x < 8; ++x) {
-            const int jj = 32 * cx.half + 8 * u + x;
-            pv[x] = (jj <= i && i < nn) ? __expf(gi - gm[jj]) * p.scale * v[8 * u + x] : 0.f;
-          }
-          const int cj = 4 * cx.half + u;
-          *reinterpret_cast<uint4*>(pb + i * 128 + ((cj ^ (i & 7)) << 4)) =
-              make_uint4(pack_bf16x2(pv[0], pv[1]), pack_bf16x2(pv[2], pv[3]), pack_bf16x2(pv[4], pv[5]),
-                         pack_bf16x2(pv[6], pv[7]));
-        }
-      }
-    }
     e_handoff(cx.tid, &bb.staged, &bb.emptyq);
   };
   staging(0);
@@ -1008,8 +1083,8 @@ __device__ bool run_ws(const FwdParams& p, ChainCtx& cx, WsBars& bb, WsPhase& ph
 #pragma unroll
       for (int hc = 0; hc < 2; ++hc) {
         float v[32];
-        tmem_ld16(cx.tmem + kTmD1 + lane_base + 64 * cx.half + 32 * hc, v);
-        tmem_ld16(cx.tmem + kTmD1 + lane_base + 64 * cx.half + 32 * hc + 16, v + 16);
+        tmem_ld16(cx.tmem + d1_col(j) + lane_base + 64 * cx.half + 32 * hc, v);
+        tmem_ld16(cx.tmem + d1_col(j) + lane_base + 64 * cx.half + 32 * hc + 16, v + 16);
         if (kWithU) {
           float u[32];
           tmem_ld16(cx.tmem + kTmD2 + lane_base + 64 * cx.half + 32 * hc, u);
@@ -1049,17 +1124,34 @@ __device__ bool run_ws(const FwdParams& p, ChainCtx& cx, WsBars& bb, WsPhase& ph
       }
       store_state_bf16_to(sm, cx, S);
     }
+    e_handoff(cx.tid, &bb.epi2, &bb.empty[st]);
+    // O of chunk j (rows 0-63 of D1[j], warps of lane quadrants 0-1), while chunk j + 1 runs:
+    // a whole chunk goes out by TMA store from a shared-memory stage, a partial one (the end of a
+    // document) row by row so that the next document's rows are not touched
     if (out && cx.q4 < 2) {
       const int t = 32 * cx.q4 + cx.lane;
       const int nn = clen[gc];
-      uint4* dst = reinterpret_cast<uint4*>(p.out + ((size_t)(ctok[gc] + t) * Hv + h) * kDim + 64 * cx.half);
+      if (nn == kChunk) {
+        if (cx.tid == 0) bulk_wait_read_all();  // the previous store has read the stage
+        o_sync();
+      }
 #pragma unroll
       for (int hc = 0; hc < 2; ++hc) {
         float v[32];
-        tmem_ld16(cx.tmem + kTmD1 + lane_base + 64 * cx.half + 32 * hc, v);
-        tmem_ld16(cx.tmem + kTmD1 + lane_base + 64 * cx.half + 32 * hc + 16, v + 16);
+        tmem_ld16(cx.tmem + d1_col(j) + lane_base + 64 * cx.half + 32 * hc, v);
+        tmem_ld16(cx.tmem + d1_col(j) + lane_base + 64 * cx.half + 32 * hc + 16, v + 16);
         tmem_ld_wait();
-        if (t < nn) {
+        if (nn == kChunk) {
+#pragma unroll
+          for (int cj4 = 0; cj4 < 4; ++cj4) {
+            const int cj = 4 * hc + cj4;
+            const float* x = v + 8 * cj4;
+            *reinterpret_cast<uint4*>(sm.ostage[cx.half] + t * 128 + ((cj ^ (t & 7)) << 4)) =
+                make_uint4(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]), pack_bf16x2(x[4], x[5]),
+                           pack_bf16x2(x[6], x[7]));
+          }
+        } else if (t < nn) {
+          uint4* dst = reinterpret_cast<uint4*>(p.out + ((size_t)(ctok[gc] + t) * Hv + h) * kDim + 64 * cx.half);
 #pragma unroll
           for (int cj4 = 0; cj4 < 4; ++cj4) {
             const float* x = v + 8 * cj4;
@@ -1068,9 +1160,18 @@ __device__ bool run_ws(const FwdParams& p, ChainCtx& cx, WsBars& bb, WsPhase& ph
           }
         }
       }
+      if (nn == kChunk) {
+        fence_proxy_async_smem();
+        o_sync();
+        if (cx.tid == 0) {
+          tma_store_3d(&p.tm_o, sm.ostage[0], 0, h, ctok[gc]);
+          tma_store_3d(&p.tm_o, sm.ostage[1], 64, h, ctok[gc]);
+          bulk_commit_group();
+        }
+      }
     }
-    e_handoff(cx.tid, &bb.epi2, &bb.empty[st]);
   }
+  if (cx.tid == 0) bulk_wait_all();  // every output store has landed before the buffers are reused
   return !*abort;
 }
 
@@ -1133,6 +1234,7 @@ __global__ void __launch_bounds__(kRec ? 256 : kWsThreads, 1) chain_kernel(const
       mbar_init(&wbars.epi1, 1);
       mbar_init(&wbars.staged, 1);
       mbar_init(&wbars.epi2, 1);
+      mbar_init(&wbars.vfree, 1);
     }
     s_abort = 0;
     fence_mbar_init();

@@ -12,6 +12,7 @@ struct FwdParams {
   CUtensorMap tm_q;  // bf16 [T][Hk][128], box 64 x 1 x 64, 128B swizzle
   CUtensorMap tm_k;  // same shape as q
   CUtensorMap tm_v;  // bf16 [T][Hv][128]
+  CUtensorMap tm_o;  // the output, same shape as v (plain forward only)
   const float* g;
   const float* beta;
   const int32_t* cu;
@@ -24,6 +25,9 @@ struct FwdParams {
   FwdLayout L;
   float trunc_thr;
   float scale;
+  // Plain forward only (NULL in the backward's recompute): P = scale (Q K^T o E) per (chunk, value
+  // head), E_ij = e^{gamma_i - gamma_j} for j <= i inside the chunk, bf16 smem image [cmax][Hv][8 KB]
+  uint8_t* p_img;
   // Backward recompute only (all NULL for a plain forward): per (chunk, value head) records
   uint8_t* st_img;  // S at each chunk start, bf16, 128B-swizzled smem image [cmax][Hv][32 KB]
   uint8_t* vp_img;  // V' = U - W S of each chunk, bf16 smem image [cmax][Hv][16 KB]
