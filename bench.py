@@ -199,7 +199,7 @@ def cpu_baseline(T_full):
     f = p.as_f64()
     cores = oracle.hw_threads()
     total, runs = 0.0, 0
-    while runs < 1 or (total < 10.0 and runs < 8):
+    while runs < 1 or (total < 10.0 and runs < 200):
         t0 = time.perf_counter()
         _oracle_step(p, f, cores)
         total += time.perf_counter() - t0
