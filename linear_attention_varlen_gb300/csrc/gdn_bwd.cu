@@ -307,19 +307,29 @@ __device__ bool rev_affine(Ctx& cx, RevSmem& sm, const float* Mm, const float* B
   uint8_t* mlo = sm.qt[0];
   uint8_t* dlo = sm.dout[0];
   {
-    const int r = cx.tid >> 1, c0 = (cx.tid & 1) * 64;
-    const float* row = Mm + (size_t)r * kDim + c0;
-    uint8_t* bhi = mhi + (c0 >> 6) * 16384;
-    uint8_t* blo = mlo + (c0 >> 6) * 16384;
-    for (int cj = 0; cj < 8; ++cj) {
-      float x[8], lo[8];
-      const float4 a = __ldcg(reinterpret_cast<const float4*>(row + 8 * cj));
-      const float4 b = __ldcg(reinterpret_cast<const float4*>(row + 8 * cj + 4));
-      x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
-      for (int u = 0; u < 8; ++u) lo[u] = x[u] - __bfloat162float(__float2bfloat16_rn(x[u]));
-      const uint32_t off = r * 128 + ((cj ^ (r & 7)) << 4);
-      *reinterpret_cast<uint4*>(bhi + off) = pack8(x);
-      *reinterpret_cast<uint4*>(blo + off) = pack8(lo);
+    // M hi / lo from coalesced loads (16 threads per 512-byte row), four 32-byte pieces in flight
+#pragma unroll
+    for (int k0 = 0; k0 < 8; k0 += 4) {
+      float4 mv[8];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int e = cx.tid + 256 * (k0 + k);
+        const float* src = Mm + (size_t)(e >> 4) * kDim + 8 * (e & 15);
+        mv[2 * k] = __ldcg(reinterpret_cast<const float4*>(src));
+        mv[2 * k + 1] = __ldcg(reinterpret_cast<const float4*>(src + 4));
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int e = cx.tid + 256 * (k0 + k), r = e >> 4, c8 = e & 15, cj = c8 & 7;
+        const float x[8] = {mv[2 * k].x, mv[2 * k].y, mv[2 * k].z, mv[2 * k].w,
+                            mv[2 * k + 1].x, mv[2 * k + 1].y, mv[2 * k + 1].z, mv[2 * k + 1].w};
+        float lo[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) lo[u] = x[u] - __bfloat162float(__float2bfloat16_rn(x[u]));
+        const uint32_t off = (c8 >> 3) * 16384 + r * 128 + ((cj ^ (r & 7)) << 4);
+        *reinterpret_cast<uint4*>(mhi + off) = pack8(x);
+        *reinterpret_cast<uint4*>(mlo + off) = pack8(lo);
+      }
     }
     const int rr = 32 * cx.q4 + cx.lane;
     uint8_t* dl = dlo + cx.half * 16384;
@@ -342,23 +352,51 @@ __device__ bool rev_affine(Ctx& cx, RevSmem& sm, const float* Mm, const float* B
                 idesc_bf16(128, 128, 1, 1), 1);
   }
   if (!cx.commit_wait()) return false;
-  {
-    const int r = 32 * cx.q4 + cx.lane;
-    for (int cc = 0; cc < 64; cc += 16) {
-      float v[16];
-      tmem_ld16(cx.tmem + kRtC + cx.lane_base() + 64 * cx.half + cc, v);
-      tmem_ld_wait();
-      const size_t o = (size_t)r * kDim + 64 * cx.half + cc;
-      for (int x = 0; x < 16; x += 4) {
-        const float4 b = __ldcg(reinterpret_cast<const float4*>(Bm + o + x));
-        *reinterpret_cast<float4*>(out + o + x) = make_float4(v[x] + b.x, v[x + 1] + b.y, v[x + 2] + b.z, v[x + 3] + b.w);
+  // the product goes through a 32 KB fp32 stage (wn | p | tw, idle here), 64 rows at a time, with
+  // granule g of local row rl at rl * 128 + 4 (g XOR rl mod 32), so that B is read and out
+  // written with coalesced accesses
+  float* stg = reinterpret_cast<float*>(sm.wn[0]);
+  for (int pass = 0; pass < 2; ++pass) {
+    if ((cx.q4 >> 1) == pass) {
+      const int rl = 32 * (cx.q4 & 1) + cx.lane;
+#pragma unroll
+      for (int cc = 0; cc < 64; cc += 16) {
+        float v[16];
+        tmem_ld16(cx.tmem + kRtC + cx.lane_base() + 64 * cx.half + cc, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+          const int g = (64 * cx.half + cc) / 4 + x;
+          *reinterpret_cast<float4*>(stg + rl * 128 + 4 * ((g ^ rl) & 31)) =
+              make_float4(v[4 * x], v[4 * x + 1], v[4 * x + 2], v[4 * x + 3]);
+        }
       }
     }
+    __syncthreads();
+    float4 b[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int e = cx.tid + 256 * k, r = 64 * pass + (e >> 5), g = e & 31;
+      b[k] = __ldcg(reinterpret_cast<const float4*>(Bm + (size_t)r * kDim + 4 * g));
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int e = cx.tid + 256 * k, rl = e >> 5, g = e & 31;
+      const float4 v = *reinterpret_cast<const float4*>(stg + rl * 128 + 4 * ((g ^ rl) & 31));
+      *reinterpret_cast<float4*>(out + (size_t)(64 * pass + rl) * kDim + 4 * g) =
+          make_float4(v.x + b[k].x, v.y + b[k].y, v.z + b[k].z, v.w + b[k].w);
+    }
+    __syncthreads();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   return true;
+}
+
+// Bring a 128x128 fp32 matrix into L2 ahead of its use (every thread of the CTA takes a share).
+__device__ __forceinline__ void prefetch_state_l2(const float* m, int tid) {
+  for (int l = tid; l < kDim * kDim * 4 / 128; l += 256) prefetch_l2(reinterpret_cast<const uint8_t*>(m) + 128 * l);
 }
 
 // Does some later document of the call start from document seq's final state (a fork)?
@@ -493,6 +531,11 @@ __global__ void __launch_bounds__(256, 1) rev_chain_kernel(const __grid_constant
       continue;
     }
     // ----------------------------------------------------------------- pass 2
+    if (first < s && s < last && !mzero[slot[s] * Hv + h]) {  // early publication below
+      const size_t o = ((size_t)slot[s] * Hv + h) * st;
+      prefetch_state_l2(mmat + o, cx.tid);
+      prefetch_state_l2(rb + o, cx.tid);
+    }
     if (s == last) {
       ok = doc_end_grad(seq, h);
     } else if (s + 1 != last && mzero[slot[s + 1] * Hv + h]) {

@@ -780,25 +780,38 @@ __device__ __forceinline__ void save_state(const ChainCtx& cx, float* dst, const
 // out = M S_start + B (B may be null) on the tensor cores with compensated bf16 operands (x = hi + lo):
 // M hi S hi + M hi S lo + M lo S hi. At the start of an item every staging buffer except sm.s
 // (S_start hi) is idle: M hi goes to sm.qw, M lo to sm.q / sm.vo, S lo to sm.v / sm.vs.
+// 32 KB idle during affine_apply in each shared-memory layout.
+__device__ __forceinline__ float* affine_stage(ChainSmem& sm) { return reinterpret_cast<float*>(sm.tu_lo); }
+
 template <class SM>
 __device__ bool affine_apply(const FwdParams& p, ChainCtx& cx, SM& sm, const float* Mm, const float* Bm,
                              const float* S, float* out) {
   if (cx.tid < 256) {
-    const int r = cx.tid >> 1, c0 = (cx.tid & 1) * 64;
-    const float* row = Mm + (size_t)r * kDim + c0;
-    uint8_t* bhi = sm.qw[c0 >> 6];
-    uint8_t* blo = (c0 == 0) ? sm.q[0] : sm.vo[0];
-    for (int cj = 0; cj < 8; ++cj) {
-      float x[8], lo[8];
-      const float4 a = __ldcg(reinterpret_cast<const float4*>(row + 8 * cj));
-      const float4 b = __ldcg(reinterpret_cast<const float4*>(row + 8 * cj + 4));
-      x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
-      for (int u = 0; u < 8; ++u) lo[u] = x[u] - __bfloat162float(__float2bfloat16_rn(x[u]));
-      const uint32_t off = r * 128 + ((cj ^ (r & 7)) << 4);
-      *reinterpret_cast<uint4*>(bhi + off) = make_uint4(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]),
-                                                        pack_bf16x2(x[4], x[5]), pack_bf16x2(x[6], x[7]));
-      *reinterpret_cast<uint4*>(blo + off) = make_uint4(pack_bf16x2(lo[0], lo[1]), pack_bf16x2(lo[2], lo[3]),
-                                                        pack_bf16x2(lo[4], lo[5]), pack_bf16x2(lo[6], lo[7]));
+    // M hi / lo from coalesced loads (16 threads per 512-byte row), four 32-byte pieces in flight
+#pragma unroll
+    for (int k0 = 0; k0 < 8; k0 += 4) {
+      float4 mv[8];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int e = cx.tid + 256 * (k0 + k);
+        const float* src = Mm + (size_t)(e >> 4) * kDim + 8 * (e & 15);
+        mv[2 * k] = __ldcg(reinterpret_cast<const float4*>(src));
+        mv[2 * k + 1] = __ldcg(reinterpret_cast<const float4*>(src + 4));
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int e = cx.tid + 256 * (k0 + k), r = e >> 4, c8 = e & 15, cj = c8 & 7;
+        const float x[8] = {mv[2 * k].x, mv[2 * k].y, mv[2 * k].z, mv[2 * k].w,
+                            mv[2 * k + 1].x, mv[2 * k + 1].y, mv[2 * k + 1].z, mv[2 * k + 1].w};
+        float lo[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) lo[u] = x[u] - __bfloat162float(__float2bfloat16_rn(x[u]));
+        const uint32_t off = r * 128 + ((cj ^ (r & 7)) << 4);
+        *reinterpret_cast<uint4*>(sm.qw[c8 >> 3] + off) = make_uint4(
+            pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]), pack_bf16x2(x[4], x[5]), pack_bf16x2(x[6], x[7]));
+        *reinterpret_cast<uint4*>(((c8 >> 3) == 0 ? sm.q[0] : sm.vo[0]) + off) = make_uint4(
+            pack_bf16x2(lo[0], lo[1]), pack_bf16x2(lo[2], lo[3]), pack_bf16x2(lo[4], lo[5]), pack_bf16x2(lo[6], lo[7]));
+      }
     }
     // S lo (this thread's row of S_start, 64 columns of dv block `half`)
     const int rr = 32 * cx.q4 + cx.lane;  // (threads below 256 only)
@@ -829,20 +842,44 @@ __device__ bool affine_apply(const FwdParams& p, ChainCtx& cx, SM& sm, const flo
   if (!wait_all(cx.bar_mma, cx.ph_mma)) return false;
   cx.ph_mma ^= 1;
   tc_fence_after();
-  if (cx.tid < 256) {
-    const uint32_t lane_base = (uint32_t)(32 * cx.q4) << 16;
-    const int r = 32 * cx.q4 + cx.lane;
-    for (int cc = 0; cc < 64; cc += 16) {
-      float v[16];
-      tmem_ld16(cx.tmem + kTmD2 + lane_base + 64 * cx.half + cc, v);
-      tmem_ld_wait();
-      float* orow = out + (size_t)r * kDim + 64 * cx.half + cc;
-      for (int x = 0; x < 16; x += 4) {
-        float4 b = Bm ? __ldcg(reinterpret_cast<const float4*>(Bm + (size_t)r * kDim + 64 * cx.half + cc + x))
-                      : make_float4(0.f, 0.f, 0.f, 0.f);
-        *reinterpret_cast<float4*>(orow + x) = make_float4(v[x] + b.x, v[x + 1] + b.y, v[x + 2] + b.z, v[x + 3] + b.w);
+  // M S_start + B: the product goes through a 32 KB fp32 stage, 64 rows at a time (granule g of
+  // local row rl at rl * 128 + 4 (g XOR rl mod 32): conflict-free both for a thread per row and for
+  // a warp per row), so that B is read and out written with coalesced accesses.
+  float* stg = affine_stage(sm);
+  for (int pass = 0; pass < 2; ++pass) {
+    if (cx.tid < 256 && (cx.q4 >> 1) == pass) {
+      const uint32_t lane_base = (uint32_t)(32 * cx.q4) << 16;
+      const int rl = 32 * (cx.q4 & 1) + cx.lane;
+#pragma unroll
+      for (int cc = 0; cc < 64; cc += 16) {
+        float v[16];
+        tmem_ld16(cx.tmem + kTmD2 + lane_base + 64 * cx.half + cc, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+          const int g = (64 * cx.half + cc) / 4 + x;
+          *reinterpret_cast<float4*>(stg + rl * 128 + 4 * ((g ^ rl) & 31)) =
+              make_float4(v[4 * x], v[4 * x + 1], v[4 * x + 2], v[4 * x + 3]);
+        }
       }
     }
+    __syncthreads();
+    if (cx.tid < 256) {
+      float4 b[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int e = cx.tid + 256 * k, r = 64 * pass + (e >> 5), g = e & 31;
+        b[k] = Bm ? __ldcg(reinterpret_cast<const float4*>(Bm + (size_t)r * kDim + 4 * g)) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int e = cx.tid + 256 * k, rl = e >> 5, g = e & 31;
+        const float4 v = *reinterpret_cast<const float4*>(stg + rl * 128 + 4 * ((g ^ rl) & 31));
+        *reinterpret_cast<float4*>(out + (size_t)(64 * pass + rl) * kDim + 4 * g) =
+            make_float4(v.x + b[k].x, v.y + b[k].y, v.z + b[k].z, v.w + b[k].w);
+      }
+    }
+    __syncthreads();
   }
   tc_fence_before();
   __syncthreads();
@@ -850,6 +887,10 @@ __device__ bool affine_apply(const FwdParams& p, ChainCtx& cx, SM& sm, const flo
   return true;
 }
 
+// Bring a 128x128 fp32 matrix into L2 ahead of its use (every thread of the CTA takes a share).
+__device__ __forceinline__ void prefetch_state_l2(const float* m, int tid, int nthreads) {
+  for (int l = tid; l < kDim * kDim * 4 / 128; l += nthreads) prefetch_l2(reinterpret_cast<const uint8_t*>(m) + 128 * l);
+}
 
 // =========================================================================== warp-specialized chain
 //
@@ -880,6 +921,7 @@ struct WsSmem {
 };
 constexpr size_t kSmemBytes = (sizeof(WsSmem) > sizeof(ChainSmem) ? sizeof(WsSmem) : sizeof(ChainSmem)) + 1024;
 constexpr int kWsThreads = 320;
+__device__ __forceinline__ float* affine_stage(WsSmem& sm) { return reinterpret_cast<float*>(sm.k[0]); }
 
 struct WsBars {
   uint64_t full[2], fullq, empty[2], emptyq, a_done, pre_done, b_done, epi1, staged, epi2, vfree;
@@ -1386,6 +1428,11 @@ __global__ void __launch_bounds__(kRec ? 256 : kWsThreads, 1) chain_kernel(const
     const bool last = (s + 1 == seq_seg0[seq + 1]);
     int first_chunk = c0;  // truncation mode may start earlier (warmup)
     bool have_start = true;
+    if (p.d.mode == 0 && slot[s] >= 0 && dep != -1) {  // this item publishes its end state early
+      const size_t off = ((size_t)slot[s] * Hv + h) * st_elems;
+      prefetch_state_l2(ws_ptr<float>(p, p.L.mmat) + off, cx.tid, blockDim.x);
+      prefetch_state_l2(ws_ptr<float>(p, p.L.bmat) + off, cx.tid, blockDim.x);
+    }
     if (dep == -1) {
       const int x = p.init_idx ? p.init_idx[seq] : -1;
       if (epi && x >= 0 && x < p.d.n_init)
