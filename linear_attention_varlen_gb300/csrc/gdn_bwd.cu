@@ -116,166 +116,328 @@ __device__ __forceinline__ void ctx_init(Ctx& c, uint64_t* bl, uint64_t* bm) {
 }
 
 // ===================================================================================== reverse chain
+//
+// The reverse chain per (segment, value head) in one CTA of 10 warps, chunks in reverse order:
+//   warp 8      TMA producer: K, Q, dO, T diag(beta e^gamma) and gamma of chunk j into stage j & 1.
+//   warp 9      MMA issuer (one lane): chunk j + 1's W = T_w K and G = Q K^T as soon as their
+//               operands have landed; A: Q~^T dO into the dS accumulator (M = 128) and
+//               dV' = K~ dS + P^T dO (M = 64); B: dS accumulator += -W^T dV' (M = 128).
+//   warps 0-7   epilogue: Q~, K~, P of chunk j + 1 and -W of chunk j + 1 staged while chunk j runs;
+//               dV' (zero rows beyond the chunk) in bf16, dS = e^{gamma_C} dS + accumulator in fp32
+//               registers (row 32 q4 + lane, columns 64 half ..), its bf16 copy the next chunk's
+//               operand; records (dL/dS at each chunk end, dV') go out by bulk stores.
+// Hand-offs are mbarriers: tcgen05.commit from the issuer, one elected arrival after a named
+// barrier from the epilogue, TMA transaction counts from the producer.
 
 struct RevSmem {
-  uint8_t q[2][8192];     // Q tile (A K-major: Q K^T)
-  uint8_t k[2][8192];     // K tile (B K-major: Q K^T; B MN-major: T_w K)
-  uint8_t qt[2][8192];    // Q~ = scale diag(e^gamma) Q, rows >= n zero (A MN-major: Q~^T dO)
-  uint8_t kt[2][8192];    // K~ = diag(e^{gamma_C - gamma}) K            (A K-major: K~ dS)
-  uint8_t wn[2][8192];    // -W rows t                                    (A MN-major: -W^T dV')
+  uint8_t k[2][16384];    // [stage] K rows t, two dk blocks (B K-major: Q K^T; B MN-major: T_w K)
+  uint8_t q[2][16384];    // [stage] Q rows t                 (A K-major: Q K^T)
+  uint8_t dout[2][16384]; // [stage] dO rows t, two dv blocks (B MN-major)
+  uint8_t tw[2][8192];    // [stage] T diag(beta e^gamma)     (A K-major: W = T_w K)
+  uint8_t qt[16384];      // Q~ = scale diag(e^gamma) Q, rows >= n zero (A MN-major: Q~^T dO)
+  uint8_t kt[16384];      // K~ = diag(e^{gamma_C - gamma}) K            (A K-major: K~ dS)
+  uint8_t wn[16384];      // -W rows t                                    (A MN-major: -W^T dV')
   uint8_t p[8192];        // P = scale (Q K^T) o E                        (A MN-major: P^T dO)
-  uint8_t tw[8192];       // T diag(beta e^gamma)                         (A K-major: W = T_w K)
-  uint8_t dout[2][8192];  // dO rows t, dv blocks                         (B MN-major)
-  uint8_t dvp[2][8192];   // dV' rows t, dv blocks                        (B MN-major)
-  uint8_t ds[2][16384];   // dS bf16 rows dk, dv blocks                   (B MN-major)
-  float gam[64];
+  uint8_t dvp[16384];     // dV' rows t, two dv blocks                    (B MN-major)
+  uint8_t ds[32768];      // dS bf16 rows dk, two dv blocks               (B MN-major)
+  float gam[2][64];
 };
 constexpr size_t kRevSmemBytes = sizeof(RevSmem) + 1024;
+static_assert(kRevSmemBytes <= 227 * 1024, "shared memory of the reverse chain");
+constexpr int kRevThreads = 320;
 constexpr uint32_t kRtW = 0, kRtG = 128, kRtA = 256, kRtC = 384;
 
+struct RevBars {
+  uint64_t full[2], empty[2], pre_done, staged1, staged2, a_done, epi1, b_done, epi2;
+};
+struct RevPhase {
+  uint32_t full[2], empty[2], pre_done, staged1, staged2, a_done, epi1, b_done, epi2;
+};
+
+// Bounded wait that never diverges: after the first failure (recorded in *abort) every later
+// wait returns at once, so all threads keep executing the same barriers.
+__device__ __forceinline__ void rrole_wait(uint64_t* bar, uint32_t& ph, volatile int* abort) {
+  if (!*abort && !mbar_wait(bar, ph, kWaitBudget)) *abort = 1;
+  ph ^= 1;
+  tc_fence_after();
+}
+__device__ __forceinline__ void r_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+// Epilogue hand-off: shared-memory writes visible to the async proxy, TMEM reads ordered, the 256
+// epilogue threads meet, one of them arrives.
+__device__ __forceinline__ void r_handoff(int tid, uint64_t* b1, uint64_t* b2 = nullptr) {
+  fence_proxy_async_smem();
+  tc_fence_before();
+  r_sync();
+  if (tid == 0) {
+    mbar_arrive(b1);
+    if (b2) mbar_arrive(b2);
+  }
+  __syncwarp();
+}
+
+// Write this thread's 64 dS values (row 32 q4 + lane, columns 64 half ..) as bf16 into sm.ds.
 __device__ __forceinline__ void rev_store_ds(const Ctx& cx, RevSmem& sm, const float* dS) {
   const int r = 32 * cx.q4 + cx.lane;
-  uint8_t* blk = sm.ds[cx.half];
+  uint8_t* blk = sm.ds + cx.half * 16384;
 #pragma unroll
   for (int cj = 0; cj < 8; ++cj) *reinterpret_cast<uint4*>(blk + r * 128 + ((cj ^ (r & 7)) << 4)) = pack8(dS + 8 * cj);
 }
 
-// One chunk of the reverse chain: dS (this thread's row of dL/dS at the chunk end, fp32) becomes
-// dL/dS at the chunk start. kRecord: also store dL/dS at the chunk end and dV' (bf16 images) for
-// the gradient kernels.
+// Chunks [gc0, gc1) of one document for value head h, in reverse, from dS (epilogue registers;
+// its bf16 copy is already in sm.ds): dS becomes dL/dS at the start of chunk gc0. kRecord: also
+// store dL/dS at each chunk end and dV' (bf16 images) for the gradient kernels. All 320 threads
+// call this; returns false after a failed wait.
 template <bool kRecord>
-__device__ bool rev_chunk(const BwdParams& p, Ctx& cx, RevSmem& sm, float* dS, int gc, int h, int hk, int tok0,
-                          int n) {
+__device__ bool run_rev_ws(const BwdParams& p, Ctx& cx, RevSmem& sm, RevBars& bb, RevPhase& ph, volatile int* abort,
+                           float* dS, int gc0, int gc1, int h, int hk) {
+  const int n = gc1 - gc0;
+  if (n <= 0) return true;
   const int Hv = p.d.Hv;
-  if (kRecord) copy_smem_to_global(p.ws + p.L.ds_img + ((size_t)gc * Hv + h) * 32768, sm.ds[0], 32768, cx.tid);
-  if (cx.tid == 0) {
-    mbar_arrive_expect_tx(cx.bar_ld, 6 * 8192 + 8192 + 256);
-    tma_load_3d(sm.k[0], &p.tm_k, 0, hk, tok0, cx.bar_ld);
-    tma_load_3d(sm.k[1], &p.tm_k, 64, hk, tok0, cx.bar_ld);
-    tma_load_3d(sm.q[0], &p.tm_q, 0, hk, tok0, cx.bar_ld);
-    tma_load_3d(sm.q[1], &p.tm_q, 64, hk, tok0, cx.bar_ld);
-    tma_load_3d(sm.dout[0], &p.tm_do, 0, h, tok0, cx.bar_ld);
-    tma_load_3d(sm.dout[1], &p.tm_do, 64, h, tok0, cx.bar_ld);
-    bulk_load(sm.tw, p.ws + p.L.f.tw + ((size_t)gc * Hv + h) * 8192, 8192, cx.bar_ld);
-    bulk_load(sm.gam, p.ws + p.L.f.gam + ((size_t)gc * Hv + h) * 256, 256, cx.bar_ld);
-  }
-  if (!cx.wait_ld()) return false;
-  if (cx.tid == 0) {
-    for (int ks = 0; ks < 4; ++ks)
-      umma_bf16(cx.tmem + kRtW, kmajor_desc(smem_u32(sm.tw), 8192, ks), mnmajor_desc(smem_u32(sm.k[0]), 8192, ks),
-                idesc_bf16(64, 128, 0, 1), ks > 0);
-    for (int ks = 0; ks < 8; ++ks)
-      umma_bf16(cx.tmem + kRtG, kmajor_desc(smem_u32(sm.q[0]), 8192, ks), kmajor_desc(smem_u32(sm.k[0]), 8192, ks),
-                idesc_bf16(64, 64, 0, 0), ks > 0);
-  }
-  const float gC = sm.gam[63];
-  // Q~ and K~ (rows >= n of Q~ are zeroed: they belong to the next document)
-  for (int e = cx.tid; e < 2 * 2 * 64 * 8; e += 256) {
-    const int which = e >> 10, b = (e >> 9) & 1, r = (e >> 3) & 63, cj = e & 7;
-    const uint32_t off = r * 128 + ((cj ^ (r & 7)) << 4);
-    const float sc = which == 0 ? ((r < n) ? __expf(sm.gam[r]) * p.scale : 0.f) : __expf(gC - sm.gam[r]);
-    uint4 raw = *reinterpret_cast<const uint4*>((which == 0 ? sm.q[b] : sm.k[b]) + off);
-    __nv_bfloat162* x = reinterpret_cast<__nv_bfloat162*>(&raw);
-    uint32_t w[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      float2 f = __bfloat1622float2(x[u]);
-      w[u] = pack_bf16x2(f.x * sc, f.y * sc);
+  const int32_t* ctok = reinterpret_cast<const int32_t*>(p.ws + p.L.f.chunk_tok0);
+  const int32_t* clen = reinterpret_cast<const int32_t*>(p.ws + p.L.f.chunk_len);
+  const uint32_t tm = cx.tmem;
+  auto chunk_of = [&](int j) { return gc1 - 1 - j; };
+
+  if (cx.warp == 8) {
+    // ------------------------------------------------------------------ TMA producer
+    if (cx.lane == 0) {
+      for (int j = 0; j < n; ++j) {
+        const int gc = chunk_of(j), st = j & 1, tok0 = ctok[gc];
+        const size_t rec = (size_t)gc * Hv + h;
+        if (j >= 2) rrole_wait(&bb.empty[st], ph.empty[st], abort);
+        if (*abort) break;
+        mbar_arrive_expect_tx(&bb.full[st], 3 * 16384 + 8192 + 256);
+        tma_load_3d(sm.k[st], &p.tm_k, 0, hk, tok0, &bb.full[st]);
+        tma_load_3d(sm.k[st] + 8192, &p.tm_k, 64, hk, tok0, &bb.full[st]);
+        tma_load_3d(sm.q[st], &p.tm_q, 0, hk, tok0, &bb.full[st]);
+        tma_load_3d(sm.q[st] + 8192, &p.tm_q, 64, hk, tok0, &bb.full[st]);
+        tma_load_3d(sm.dout[st], &p.tm_do, 0, h, tok0, &bb.full[st]);
+        tma_load_3d(sm.dout[st] + 8192, &p.tm_do, 64, h, tok0, &bb.full[st]);
+        bulk_load(sm.tw[st], p.ws + p.L.f.tw + rec * 8192, 8192, &bb.full[st]);
+        bulk_load(sm.gam[st], p.ws + p.L.f.gam + rec * 256, 256, &bb.full[st]);
+      }
+      for (int j = (n >= 2 ? n - 2 : 0); j < n; ++j) rrole_wait(&bb.empty[j & 1], ph.empty[j & 1], abort);
     }
-    *reinterpret_cast<uint4*>((which == 0 ? sm.qt[b] : sm.kt[b]) + off) = make_uint4(w[0], w[1], w[2], w[3]);
+    return !*abort;
   }
-  if (!cx.commit_wait()) return false;
-  {
-    const int i = 16 * cx.q4 + cx.lane;
-    for (int cc = 0; cc < 64; cc += 16) {
-      float v[16];
-      tmem_ld16(cx.tmem + kRtW + cx.lane_base() + 64 * cx.half + cc, v);
-      tmem_ld_wait();
-      if (cx.lane < 16) {
-        for (int x = 0; x < 16; ++x) v[x] = -v[x];
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int cj = (cc >> 3) + u;
-          *reinterpret_cast<uint4*>(sm.wn[cx.half] + i * 128 + ((cj ^ (i & 7)) << 4)) = pack8(v + 8 * u);
+  if (cx.warp == 9) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (cx.lane == 0) {
+      auto prep = [&](int j) {  // W = T_w K, G = Q K^T of chunk j
+        const int st = j & 1;
+        for (int ks = 0; ks < 4; ++ks)
+          umma_bf16(tm + kRtW, kmajor_desc(smem_u32(sm.tw[st]), 8192, ks), mnmajor_desc(smem_u32(sm.k[st]), 8192, ks),
+                    idesc_bf16(64, 128, 0, 1), ks > 0);
+        for (int ks = 0; ks < 8; ++ks)
+          umma_bf16(tm + kRtG, kmajor_desc(smem_u32(sm.q[st]), 8192, ks), kmajor_desc(smem_u32(sm.k[st]), 8192, ks),
+                    idesc_bf16(64, 64, 0, 0), ks > 0);
+        umma_commit(&bb.pre_done);
+      };
+      rrole_wait(&bb.full[0], ph.full[0], abort);
+      if (!*abort) prep(0);
+      for (int j = 0; j < n && !*abort; ++j) {
+        const int st = j & 1;
+        // A: needs Q~, K~, P of chunk j (staged1), dS of chunk j (epi2 of j - 1, or the initial
+        // hand-off) and the dV' accumulator read (epi1 of j - 1)
+        rrole_wait(&bb.staged1, ph.staged1, abort);
+        rrole_wait(&bb.epi2, ph.epi2, abort);
+        if (*abort) break;
+        // Q~^T dO first: a_done then also covers it, so that the epilogue may restage Q~ right after
+        for (int ks = 0; ks < 4; ++ks)
+          umma_bf16(tm + kRtC, mnmajor_desc(smem_u32(sm.qt), 8192, ks), mnmajor_desc(smem_u32(sm.dout[st]), 8192, ks),
+                    idesc_bf16(128, 128, 1, 1), ks > 0);
+        for (int ks = 0; ks < 8; ++ks)
+          umma_bf16(tm + kRtA, kmajor_desc(smem_u32(sm.kt), 8192, ks), mnmajor_desc(smem_u32(sm.ds), 16384, ks),
+                    idesc_bf16(64, 128, 0, 1), ks > 0);
+        for (int ks = 0; ks < 4; ++ks)
+          umma_bf16(tm + kRtA, mnmajor_desc(smem_u32(sm.p), 8192, ks), mnmajor_desc(smem_u32(sm.dout[st]), 8192, ks),
+                    idesc_bf16(64, 128, 1, 1), 1);
+        umma_commit(&bb.a_done);
+        // B as soon as dV' and -W are staged; chunk j + 1's W, G as soon as its operands have
+        // landed and W, G of chunk j have been read (staged2 of j), whichever comes first
+        bool need_prep = j + 1 < n, b_issued = false, w_read = false;
+        const long long t0 = clock64();
+        while (!b_issued && !*abort) {
+          if (!w_read && mbar_test(&bb.staged2, ph.staged2)) {
+            ph.staged2 ^= 1;
+            tc_fence_after();
+            w_read = true;
+          }
+          if (need_prep && w_read && mbar_test(&bb.full[st ^ 1], ph.full[st ^ 1])) {
+            ph.full[st ^ 1] ^= 1;
+            tc_fence_after();
+            prep(j + 1);
+            need_prep = false;
+          }
+          if (w_read && mbar_test(&bb.epi1, ph.epi1)) {
+            ph.epi1 ^= 1;
+            tc_fence_after();
+            for (int ks = 0; ks < 4; ++ks)
+              umma_bf16(tm + kRtC, mnmajor_desc(smem_u32(sm.wn), 8192, ks), mnmajor_desc(smem_u32(sm.dvp), 8192, ks),
+                        idesc_bf16(128, 128, 1, 1), 1);
+            umma_commit(&bb.b_done);
+            umma_commit(&bb.empty[st]);
+            b_issued = true;
+          } else if (clock64() - t0 > kWaitBudget) {
+            *abort = 1;
+          }
+        }
+        if (*abort) break;
+        if (need_prep) {
+          rrole_wait(&bb.full[st ^ 1], ph.full[st ^ 1], abort);
+          if (*abort) break;
+          prep(j + 1);
         }
       }
+      rrole_wait(&bb.epi2, ph.epi2, abort);  // the epilogue's last dS hand-off
     }
-    for (int cc = 0; cc < 32; cc += 16) {
-      float v[16];
-      tmem_ld16(cx.tmem + kRtG + cx.lane_base() + 32 * cx.half + cc, v);
+    return !*abort;
+  }
+  // -------------------------------------------------------------------- epilogue warps 0-7
+  const uint32_t lane_base = (uint32_t)(32 * cx.q4) << 16;
+  const int i = 16 * cx.q4 + cx.lane;  // row of M = 64 accumulators (lanes < 16)
+  // Q~, K~ (from the stage) and P (from G) of chunk j
+  auto staging1 = [&](int j) {
+    const int gc = chunk_of(j), st = j & 1, nn = clen[gc];
+    rrole_wait(&bb.full[st], ph.full[st], abort);
+    const float* gm = sm.gam[st];
+    const float gC = gm[63];
+    for (int e = cx.tid; e < 2 * 2 * 64 * 8; e += 256) {
+      const int which = e >> 10, b = (e >> 9) & 1, r = (e >> 3) & 63, cj = e & 7;
+      const uint32_t off = b * 8192 + r * 128 + ((cj ^ (r & 7)) << 4);
+      const float sc = which == 0 ? ((r < nn) ? __expf(gm[r]) * p.scale : 0.f) : __expf(gC - gm[r]);
+      uint4 raw = *reinterpret_cast<const uint4*>((which == 0 ? sm.q[st] : sm.k[st]) + off);
+      __nv_bfloat162* x = reinterpret_cast<__nv_bfloat162*>(&raw);
+      uint32_t w[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        float2 f = __bfloat1622float2(x[u]);
+        w[u] = pack_bf16x2(f.x * sc, f.y * sc);
+      }
+      *reinterpret_cast<uint4*>((which == 0 ? sm.qt : sm.kt) + off) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    rrole_wait(&bb.pre_done, ph.pre_done, abort);
+    {
+      float v[32];
+      tmem_ld16(tm + kRtG + lane_base + 32 * cx.half, v);
+      tmem_ld16(tm + kRtG + lane_base + 32 * cx.half + 16, v + 16);
       tmem_ld_wait();
       if (cx.lane < 16) {
-        const float gi = sm.gam[i];
+        const float gi = gm[i];
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
+        for (int u = 0; u < 4; ++u) {
           float pv[8];
+#pragma unroll
           for (int x = 0; x < 8; ++x) {
-            const int j = 32 * cx.half + cc + 8 * u + x;
-            pv[x] = (j <= i && i < n) ? __expf(gi - sm.gam[j]) * p.scale * v[8 * u + x] : 0.f;
+            const int jj = 32 * cx.half + 8 * u + x;
+            pv[x] = (jj <= i && i < nn) ? __expf(gi - gm[jj]) * p.scale * v[8 * u + x] : 0.f;
           }
-          const int cj = ((32 * cx.half + cc) >> 3) + u;
+          const int cj = 4 * cx.half + u;
           *reinterpret_cast<uint4*>(sm.p + i * 128 + ((cj ^ (i & 7)) << 4)) = pack8(pv);
         }
       }
     }
-  }
-  sync_generic_to_async();
-  // dV' = K~ dS + P^T dO
-  if (cx.tid == 0) {
-    for (int ks = 0; ks < 8; ++ks)
-      umma_bf16(cx.tmem + kRtA, kmajor_desc(smem_u32(sm.kt[0]), 8192, ks), mnmajor_desc(smem_u32(sm.ds[0]), 16384, ks),
-                idesc_bf16(64, 128, 0, 1), ks > 0);
-    for (int ks = 0; ks < 4; ++ks)
-      umma_bf16(cx.tmem + kRtA, mnmajor_desc(smem_u32(sm.p), 8192, ks), mnmajor_desc(smem_u32(sm.dout[0]), 8192, ks),
-                idesc_bf16(64, 128, 1, 1), 1);
-  }
-  if (!cx.commit_wait()) return false;
-  {
-    const int t = 16 * cx.q4 + cx.lane;
-    for (int cc = 0; cc < 64; cc += 16) {
-      float v[16];
-      tmem_ld16(cx.tmem + kRtA + cx.lane_base() + 64 * cx.half + cc, v);
+    r_handoff(cx.tid, &bb.staged1);
+  };
+  // -W of chunk j (W is ready: staging1 of j waited for it)
+  auto staging2 = [&]() {
+#pragma unroll
+    for (int hc = 0; hc < 2; ++hc) {
+      float v[32];
+      tmem_ld16(tm + kRtW + lane_base + 64 * cx.half + 32 * hc, v);
+      tmem_ld16(tm + kRtW + lane_base + 64 * cx.half + 32 * hc + 16, v + 16);
       tmem_ld_wait();
       if (cx.lane < 16) {
-        if (t >= n)
-          for (int x = 0; x < 16; ++x) v[x] = 0.f;
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int cj = (cc >> 3) + u;
-          *reinterpret_cast<uint4*>(sm.dvp[cx.half] + t * 128 + ((cj ^ (t & 7)) << 4)) = pack8(v + 8 * u);
+        for (int x = 0; x < 32; ++x) v[x] = -v[x];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int cj = 4 * hc + u;
+          *reinterpret_cast<uint4*>(sm.wn + cx.half * 8192 + i * 128 + ((cj ^ (i & 7)) << 4)) = pack8(v + 8 * u);
         }
       }
     }
-  }
-  sync_generic_to_async();
-  if (kRecord) copy_smem_to_global(p.ws + p.L.dvp_img + ((size_t)gc * Hv + h) * 16384, sm.dvp[0], 16384, cx.tid);
-  // dS_c = e^{gamma_C} dS + Q~^T dO - W^T dV'
-  if (cx.tid == 0) {
-    for (int ks = 0; ks < 4; ++ks)
-      umma_bf16(cx.tmem + kRtC, mnmajor_desc(smem_u32(sm.qt[0]), 8192, ks), mnmajor_desc(smem_u32(sm.dout[0]), 8192, ks),
-                idesc_bf16(128, 128, 1, 1), ks > 0);
-    for (int ks = 0; ks < 4; ++ks)
-      umma_bf16(cx.tmem + kRtC, mnmajor_desc(smem_u32(sm.wn[0]), 8192, ks), mnmajor_desc(smem_u32(sm.dvp[0]), 8192, ks),
-                idesc_bf16(128, 128, 1, 1), 1);
-  }
-  if (!cx.commit_wait()) return false;
-  {
-    const float GC = __expf(gC);
-    for (int cc = 0; cc < 64; cc += 16) {
-      float v[16];
-      tmem_ld16(cx.tmem + kRtC + cx.lane_base() + 64 * cx.half + cc, v);
-      tmem_ld_wait();
-      for (int x = 0; x < 16; ++x) dS[cc + x] = GC * dS[cc + x] + v[x];
+    r_handoff(cx.tid, &bb.staged2);
+  };
+  // dL/dS at the end of chunk j (the bf16 image in sm.ds) goes to the records
+  auto record_ds = [&](int j) {
+    if (kRecord && cx.tid == 0) {
+      bulk_wait_read_all();
+      bulk_store(p.ws + p.L.ds_img + ((size_t)chunk_of(j) * Hv + h) * 32768, sm.ds, 32768);
+      bulk_commit_group();
     }
-    rev_store_ds(cx, sm, dS);
+    __syncwarp();
+  };
+  r_handoff(cx.tid, &bb.epi2);  // dS of the first chunk is staged
+  staging1(0);
+  staging2();
+  record_ds(0);
+  for (int j = 0; j < n; ++j) {
+    const int gc = chunk_of(j), st = j & 1, nn = clen[gc];
+    const float gC = sm.gam[st][63];
+    rrole_wait(&bb.a_done, ph.a_done, abort);
+    // dV' (rows beyond the chunk are zero), bf16
+    if (kRecord && cx.tid == 0) bulk_wait_read_all();  // the previous dV' record has read sm.dvp
+    __syncwarp();
+    r_sync();
+    {
+      const int t = i;
+#pragma unroll
+      for (int hc = 0; hc < 2; ++hc) {
+        float v[32];
+        tmem_ld16(tm + kRtA + lane_base + 64 * cx.half + 32 * hc, v);
+        tmem_ld16(tm + kRtA + lane_base + 64 * cx.half + 32 * hc + 16, v + 16);
+        tmem_ld_wait();
+        if (cx.lane < 16) {
+          if (t >= nn)
+#pragma unroll
+            for (int x = 0; x < 32; ++x) v[x] = 0.f;
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int cj = 4 * hc + u;
+            *reinterpret_cast<uint4*>(sm.dvp + cx.half * 8192 + t * 128 + ((cj ^ (t & 7)) << 4)) = pack8(v + 8 * u);
+          }
+        }
+      }
+    }
+    r_handoff(cx.tid, &bb.epi1);
+    if (kRecord && cx.tid == 0) {
+      bulk_store(p.ws + p.L.dvp_img + ((size_t)gc * Hv + h) * 16384, sm.dvp, 16384);
+      bulk_commit_group();
+    }
+    __syncwarp();
+    if (j + 1 < n) staging1(j + 1);
+    rrole_wait(&bb.b_done, ph.b_done, abort);
+    {
+      const float GC = __expf(gC);
+#pragma unroll
+      for (int hc = 0; hc < 2; ++hc) {
+        float v[32];
+        tmem_ld16(tm + kRtC + lane_base + 64 * cx.half + 32 * hc, v);
+        tmem_ld16(tm + kRtC + lane_base + 64 * cx.half + 32 * hc + 16, v + 16);
+        tmem_ld_wait();
+#pragma unroll
+        for (int x = 0; x < 32; ++x) dS[32 * hc + x] = GC * dS[32 * hc + x] + v[x];
+      }
+      if (kRecord && cx.tid == 0) bulk_wait_read_all();  // the dS record of chunk j has read sm.ds
+      __syncwarp();
+      r_sync();
+      rev_store_ds(cx, sm, dS);
+    }
+    r_handoff(cx.tid, &bb.epi2, &bb.empty[st]);
+    if (j + 1 < n) {
+      staging2();
+      record_ds(j + 1);
+    }
   }
-  sync_generic_to_async();
-  return true;
+  if (kRecord && cx.tid == 0) bulk_wait_all();
+  return !*abort;
 }
 
 // This thread's row piece (row 32 q4 + lane, columns 64 half ... +63) of a 128x128 fp32 matrix.
 __device__ __forceinline__ void rev_load(const Ctx& cx, const float* src, float* dS, bool add) {
   const float* row = src + (size_t)(32 * cx.q4 + cx.lane) * kDim + 64 * cx.half;
+#pragma unroll
   for (int c = 0; c < 64; c += 4) {
     const float4 f = __ldcg(reinterpret_cast<const float4*>(row + c));
     if (add) {
@@ -293,6 +455,7 @@ __device__ __forceinline__ void rev_load(const Ctx& cx, const float* src, float*
 }
 __device__ __forceinline__ void rev_save(const Ctx& cx, float* dst, const float* dS) {
   float* row = dst + (size_t)(32 * cx.q4 + cx.lane) * kDim + 64 * cx.half;
+#pragma unroll
   for (int c = 0; c < 64; c += 4) *reinterpret_cast<float4*>(row + c) = make_float4(dS[c], dS[c + 1], dS[c + 2], dS[c + 3]);
 }
 
@@ -300,13 +463,14 @@ __device__ __forceinline__ void rev_save(const Ctx& cx, float* dst, const float*
 // M hi^T dS hi + M hi^T dS lo + M lo^T dS hi. M is the forward transition of a segment (fp32,
 // row-major [dk][dk]); the reverse chain carries dL/dS through M^T. M's rows go unchanged into
 // MN-major A blocks (row k of M = row k of the block, 64 m-values per block), which is M^T as
-// the A operand. dS hi is in sm.ds (rev_store_ds). Staging: M hi in q|k, M lo in qt|kt, dS lo
-// in dout|dvp (each pair is one contiguous 32 KB region of two 16 KB blocks).
+// the A operand. dS hi is in sm.ds (rev_store_ds). Staging (idle at the start of an item): M hi in
+// sm.q, M lo in sm.k, dS lo in sm.dout (two 16 KB blocks each), the fp32 product in qt | kt. The
+// epilogue threads (tid < 256) hold dS; all threads of the CTA call this.
 __device__ bool rev_affine(Ctx& cx, RevSmem& sm, const float* Mm, const float* Bm, const float* dS, float* out) {
   uint8_t* mhi = sm.q[0];
-  uint8_t* mlo = sm.qt[0];
+  uint8_t* mlo = sm.k[0];
   uint8_t* dlo = sm.dout[0];
-  {
+  if (cx.tid < 256) {
     // M hi / lo from coalesced loads (16 threads per 512-byte row), four 32-byte pieces in flight
 #pragma unroll
     for (int k0 = 0; k0 < 8; k0 += 4) {
@@ -333,8 +497,10 @@ __device__ bool rev_affine(Ctx& cx, RevSmem& sm, const float* Mm, const float* B
     }
     const int rr = 32 * cx.q4 + cx.lane;
     uint8_t* dl = dlo + cx.half * 16384;
+#pragma unroll
     for (int cj = 0; cj < 8; ++cj) {
       float lo[8];
+#pragma unroll
       for (int u = 0; u < 8; ++u) lo[u] = dS[8 * cj + u] - __bfloat162float(__float2bfloat16_rn(dS[8 * cj + u]));
       *reinterpret_cast<uint4*>(dl + rr * 128 + ((cj ^ (rr & 7)) << 4)) = pack8(lo);
     }
@@ -342,22 +508,21 @@ __device__ bool rev_affine(Ctx& cx, RevSmem& sm, const float* Mm, const float* B
   sync_generic_to_async();
   if (cx.tid == 0) {
     for (int ks = 0; ks < 8; ++ks)
-      umma_bf16(cx.tmem + kRtC, mnmajor_desc(smem_u32(mhi), 16384, ks), mnmajor_desc(smem_u32(sm.ds[0]), 16384, ks),
+      umma_bf16(cx.tmem + kRtC, mnmajor_desc(smem_u32(mhi), 16384, ks), mnmajor_desc(smem_u32(sm.ds), 16384, ks),
                 idesc_bf16(128, 128, 1, 1), ks > 0);
     for (int ks = 0; ks < 8; ++ks)
       umma_bf16(cx.tmem + kRtC, mnmajor_desc(smem_u32(mhi), 16384, ks), mnmajor_desc(smem_u32(dlo), 16384, ks),
                 idesc_bf16(128, 128, 1, 1), 1);
     for (int ks = 0; ks < 8; ++ks)
-      umma_bf16(cx.tmem + kRtC, mnmajor_desc(smem_u32(mlo), 16384, ks), mnmajor_desc(smem_u32(sm.ds[0]), 16384, ks),
+      umma_bf16(cx.tmem + kRtC, mnmajor_desc(smem_u32(mlo), 16384, ks), mnmajor_desc(smem_u32(sm.ds), 16384, ks),
                 idesc_bf16(128, 128, 1, 1), 1);
   }
   if (!cx.commit_wait()) return false;
-  // the product goes through a 32 KB fp32 stage (wn | p | tw, idle here), 64 rows at a time, with
-  // granule g of local row rl at rl * 128 + 4 (g XOR rl mod 32), so that B is read and out
-  // written with coalesced accesses
-  float* stg = reinterpret_cast<float*>(sm.wn[0]);
+  // the product goes through a 32 KB fp32 stage, 64 rows at a time, with granule g of local row
+  // rl at rl * 128 + 4 (g XOR rl mod 32), so that B is read and out written with coalesced accesses
+  float* stg = reinterpret_cast<float*>(sm.qt);
   for (int pass = 0; pass < 2; ++pass) {
-    if ((cx.q4 >> 1) == pass) {
+    if (cx.tid < 256 && (cx.q4 >> 1) == pass) {
       const int rl = 32 * (cx.q4 & 1) + cx.lane;
 #pragma unroll
       for (int cc = 0; cc < 64; cc += 16) {
@@ -373,18 +538,20 @@ __device__ bool rev_affine(Ctx& cx, RevSmem& sm, const float* Mm, const float* B
       }
     }
     __syncthreads();
-    float4 b[8];
+    if (cx.tid < 256) {
+      float4 b[8];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const int e = cx.tid + 256 * k, r = 64 * pass + (e >> 5), g = e & 31;
-      b[k] = __ldcg(reinterpret_cast<const float4*>(Bm + (size_t)r * kDim + 4 * g));
-    }
+      for (int k = 0; k < 8; ++k) {
+        const int e = cx.tid + 256 * k, r = 64 * pass + (e >> 5), g = e & 31;
+        b[k] = __ldcg(reinterpret_cast<const float4*>(Bm + (size_t)r * kDim + 4 * g));
+      }
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const int e = cx.tid + 256 * k, rl = e >> 5, g = e & 31;
-      const float4 v = *reinterpret_cast<const float4*>(stg + rl * 128 + 4 * ((g ^ rl) & 31));
-      *reinterpret_cast<float4*>(out + (size_t)(64 * pass + rl) * kDim + 4 * g) =
-          make_float4(v.x + b[k].x, v.y + b[k].y, v.z + b[k].z, v.w + b[k].w);
+      for (int k = 0; k < 8; ++k) {
+        const int e = cx.tid + 256 * k, rl = e >> 5, g = e & 31;
+        const float4 v = *reinterpret_cast<const float4*>(stg + rl * 128 + 4 * ((g ^ rl) & 31));
+        *reinterpret_cast<float4*>(out + (size_t)(64 * pass + rl) * kDim + 4 * g) =
+            make_float4(v.x + b[k].x, v.y + b[k].y, v.z + b[k].z, v.w + b[k].w);
+      }
     }
     __syncthreads();
   }
@@ -396,7 +563,7 @@ __device__ bool rev_affine(Ctx& cx, RevSmem& sm, const float* Mm, const float* B
 
 // Bring a 128x128 fp32 matrix into L2 ahead of its use (every thread of the CTA takes a share).
 __device__ __forceinline__ void prefetch_state_l2(const float* m, int tid) {
-  for (int l = tid; l < kDim * kDim * 4 / 128; l += 256) prefetch_l2(reinterpret_cast<const uint8_t*>(m) + 128 * l);
+  for (int l = tid; l < kDim * kDim * 4 / 128; l += kRevThreads) prefetch_l2(reinterpret_cast<const uint8_t*>(m) + 128 * l);
 }
 
 // Does some later document of the call start from document seq's final state (a fork)?
@@ -429,12 +596,13 @@ __device__ __forceinline__ void rev_publish(int* flag) {
 //            reverse with records; a first segment writes dL/dS at the document start.
 // Every wait is on an item with a smaller ticket, so the queue cannot deadlock.
 template <int kPass>
-__global__ void __launch_bounds__(256, 1) rev_chain_kernel(const __grid_constant__ BwdParams p) {
+__global__ void __launch_bounds__(kRevThreads, 1) rev_chain_kernel(const __grid_constant__ BwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   RevSmem& sm = *reinterpret_cast<RevSmem*>(smem_align1024(smem_raw));
   __shared__ uint64_t bar_ld, bar_mma;
+  __shared__ RevBars rbars;
   __shared__ uint32_t tmem_holder;
-  __shared__ int s_item, s_ok;
+  __shared__ int s_item, s_ok, s_abort;
   Header* hd = reinterpret_cast<Header*>(p.ws + p.L.f.header);
   Header* h2 = reinterpret_cast<Header*>(p.ws + p.L.hdr2);
   const int N = p.d.N, Hv = p.d.Hv, G = p.d.Hv / p.d.Hk;
@@ -443,9 +611,24 @@ __global__ void __launch_bounds__(256, 1) rev_chain_kernel(const __grid_constant
   if (blockIdx.x >= n_items || get_status(hd) != 0) return;
   Ctx cx;
   ctx_init(cx, &bar_ld, &bar_mma);
+  const bool epi = cx.tid < 256;  // threads that hold dS rows
+  RevPhase ph;
+  memset(&ph, 0, sizeof(ph));
   if (cx.tid == 0) {
     mbar_init(&bar_ld, 1);
     mbar_init(&bar_mma, 1);
+    mbar_init(&rbars.full[0], 1);
+    mbar_init(&rbars.full[1], 1);
+    mbar_init(&rbars.empty[0], 2);
+    mbar_init(&rbars.empty[1], 2);
+    mbar_init(&rbars.pre_done, 1);
+    mbar_init(&rbars.staged1, 1);
+    mbar_init(&rbars.staged2, 1);
+    mbar_init(&rbars.a_done, 1);
+    mbar_init(&rbars.epi1, 1);
+    mbar_init(&rbars.b_done, 1);
+    mbar_init(&rbars.epi2, 1);
+    s_abort = 0;
     fence_mbar_init();
   }
   if (cx.warp == 0) tmem_alloc(&tmem_holder, 512);
@@ -454,8 +637,6 @@ __global__ void __launch_bounds__(256, 1) rev_chain_kernel(const __grid_constant
   const int32_t* seq_seg0 = reinterpret_cast<const int32_t*>(p.ws + p.L.f.seq_seg0);
   const int32_t* si = reinterpret_cast<const int32_t*>(p.ws + p.L.f.seg_info);
   const int32_t* slot = reinterpret_cast<const int32_t*>(p.ws + p.L.f.seg_slot);
-  const int32_t* ctok = reinterpret_cast<const int32_t*>(p.ws + p.L.f.chunk_tok0);
-  const int32_t* clen = reinterpret_cast<const int32_t*>(p.ws + p.L.f.chunk_len);
   const int* mzero = reinterpret_cast<const int*>(p.ws + p.L.f.mzero);
   const float* mmat = reinterpret_cast<const float*>(p.ws + p.L.f.mmat);
   float* ds0 = reinterpret_cast<float*>(p.ws + p.L.ds0);
@@ -478,26 +659,29 @@ __global__ void __launch_bounds__(256, 1) rev_chain_kernel(const __grid_constant
   };
   // dL/dS at a document's end: dfinal plus the start gradients of the documents forked from it
   auto doc_end_grad = [&](int seq, int h) -> bool {
-    if (p.dfinal)
-      rev_load(cx, p.dfinal + ((size_t)seq * Hv + h) * st, dS, false);
-    else
-      for (int c = 0; c < 64; ++c) dS[c] = 0.f;
+    if (epi) {
+      if (p.dfinal)
+        rev_load(cx, p.dfinal + ((size_t)seq * Hv + h) * st, dS, false);
+      else
+        for (int c = 0; c < 64; ++c) dS[c] = 0.f;
+    }
     if (p.init_idx)
       for (int x = seq + 1; x < N; ++x) {
         if (p.init_idx[x] != p.d.n_init + seq) continue;
         if (!wait_uniform(&flags[x * Hv + h])) return false;
-        rev_load(cx, ds0 + ((size_t)x * Hv + h) * st, dS, true);
+        if (epi) rev_load(cx, ds0 + ((size_t)x * Hv + h) * st, dS, true);
       }
     return true;
   };
   auto run = [&](int c0, int nch, int h, int hk, bool record) -> bool {
-    rev_store_ds(cx, sm, dS);
+    if (epi) rev_store_ds(cx, sm, dS);
     sync_generic_to_async();
-    bool ok = true;
-    for (int gc = c0 + nch - 1; gc >= c0 && ok; --gc)
-      ok = record ? rev_chunk<true>(p, cx, sm, dS, gc, h, hk, ctok[gc], clen[gc])
-                  : rev_chunk<false>(p, cx, sm, dS, gc, h, hk, ctok[gc], clen[gc]);
-    return ok;
+    if (record)
+      run_rev_ws<true>(p, cx, sm, rbars, ph, &s_abort, dS, c0, c0 + nch, h, hk);
+    else
+      run_rev_ws<false>(p, cx, sm, rbars, ph, &s_abort, dS, c0, c0 + nch, h, hk);
+    __syncthreads();
+    return s_abort == 0;
   };
   for (;;) {
     if (cx.tid == 0) {
@@ -516,17 +700,18 @@ __global__ void __launch_bounds__(256, 1) rev_chain_kernel(const __grid_constant
     if (kPass == 1) {
       if (first == last || s == first) continue;  // nothing to precompute
       if (s < last) {
-        for (int c = 0; c < 64; ++c) dS[c] = 0.f;
+        if (epi)
+          for (int c = 0; c < 64; ++c) dS[c] = 0.f;
         ok = run(c0, nch, h, hk, false);
         if (!ok) break;
-        rev_save(cx, rb + ((size_t)slot[s] * Hv + h) * st, dS);
+        if (epi) rev_save(cx, rb + ((size_t)slot[s] * Hv + h) * st, dS);
         __syncthreads();
         continue;
       }
       if (doc_has_forks(p, seq)) continue;  // its end gradient waits for the forked documents
       ok = doc_end_grad(seq, h) && run(c0, nch, h, hk, false);
       if (!ok) break;
-      rev_save(cx, rpub + ((size_t)slot[s - 1] * Hv + h) * st, dS);
+      if (epi) rev_save(cx, rpub + ((size_t)slot[s - 1] * Hv + h) * st, dS);
       rev_publish(&rflags[s * Hv + h]);
       continue;
     }
@@ -539,15 +724,15 @@ __global__ void __launch_bounds__(256, 1) rev_chain_kernel(const __grid_constant
     if (s == last) {
       ok = doc_end_grad(seq, h);
     } else if (s + 1 != last && mzero[slot[s + 1] * Hv + h]) {
-      rev_load(cx, rb + ((size_t)slot[s + 1] * Hv + h) * st, dS, false);  // M_{s+1} = 0: no wait
+      if (epi) rev_load(cx, rb + ((size_t)slot[s + 1] * Hv + h) * st, dS, false);  // M_{s+1} = 0: no wait
     } else {
       ok = wait_uniform(&rflags[(s + 1) * Hv + h]);
-      if (ok) rev_load(cx, rpub + ((size_t)slot[s] * Hv + h) * st, dS, false);
+      if (ok && epi) rev_load(cx, rpub + ((size_t)slot[s] * Hv + h) * st, dS, false);
     }
     if (!ok) break;
     if (first < s && s < last && !mzero[slot[s] * Hv + h]) {
       // early publication of this segment's start gradient
-      rev_store_ds(cx, sm, dS);
+      if (epi) rev_store_ds(cx, sm, dS);
       sync_generic_to_async();
       const size_t o = ((size_t)slot[s] * Hv + h) * st;
       if (!rev_affine(cx, sm, mmat + o, rb + o, dS, rpub + ((size_t)slot[s - 1] * Hv + h) * st)) {
@@ -561,15 +746,16 @@ __global__ void __launch_bounds__(256, 1) rev_chain_kernel(const __grid_constant
       break;
     }
     if (first < s && s == last && doc_has_forks(p, seq)) {
-      rev_save(cx, rpub + ((size_t)slot[s - 1] * Hv + h) * st, dS);
+      if (epi) rev_save(cx, rpub + ((size_t)slot[s - 1] * Hv + h) * st, dS);
       rev_publish(&rflags[s * Hv + h]);
     }
     if (s == first) {
-      rev_save(cx, ds0 + ((size_t)seq * Hv + h) * st, dS);
+      if (epi) rev_save(cx, ds0 + ((size_t)seq * Hv + h) * st, dS);
       rev_publish(&flags[seq * Hv + h]);
     }
     __syncthreads();
   }
+  if (s_abort && cx.tid == 0) set_status(hd, kErrTimeout);
   if (cx.tid == 0) {
     umma_commit(&bar_mma);
     mbar_wait(&bar_mma, cx.ph_mma, kWaitBudget);
@@ -1286,8 +1472,8 @@ int launch_bwd(const BwdArgs& a, cudaStream_t stream, cudaEvent_t* ev) {
   {
     const int64_t items = p.L.f.smax * d.Hv;
     const int grid = (int)(items < d.num_sms ? items : d.num_sms);
-    if (p.L.f.slots > 0 && d.T > 0) rev_chain_kernel<1><<<grid, 256, kRevSmemBytes, stream>>>(p);
-    rev_chain_kernel<2><<<grid, 256, kRevSmemBytes, stream>>>(p);
+    if (p.L.f.slots > 0 && d.T > 0) rev_chain_kernel<1><<<grid, kRevThreads, kRevSmemBytes, stream>>>(p);
+    rev_chain_kernel<2><<<grid, kRevThreads, kRevSmemBytes, stream>>>(p);
   }
   mark(9);
   mark(10);
