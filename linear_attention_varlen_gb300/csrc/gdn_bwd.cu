@@ -118,11 +118,12 @@ __device__ __forceinline__ void ctx_init(Ctx& c, uint64_t* bl, uint64_t* bm) {
 // ===================================================================================== reverse chain
 //
 // The reverse chain per (segment, value head) in one CTA of 10 warps, chunks in reverse order:
-//   warp 8      TMA producer: K, Q, dO, T diag(beta e^gamma) and gamma of chunk j into stage j & 1.
-//   warp 9      MMA issuer (one lane): chunk j + 1's W = T_w K and G = Q K^T as soon as their
-//               operands have landed; A: Q~^T dO into the dS accumulator (M = 128) and
-//               dV' = K~ dS + P^T dO (M = 64); B: dS accumulator += -W^T dV' (M = 128).
-//   warps 0-7   epilogue: Q~, K~, P of chunk j + 1 and -W of chunk j + 1 staged while chunk j runs;
+//   warp 8      TMA producer: K, Q, dO, T diag(beta e^gamma), P = scale (Q K^T o E) (formed by
+//               kkt_solve) and gamma of chunk j into stage j & 1.
+//   warp 9      MMA issuer (one lane): chunk j + 1's W = T_w K as soon as its operands have
+//               landed; A: Q~^T dO into the dS accumulator (M = 128) and dV' = K~ dS + P^T dO
+//               (M = 64); B: dS accumulator += -W^T dV' (M = 128).
+//   warps 0-7   epilogue: Q~, K~ and -W of chunk j + 1 staged while chunk j runs;
 //               dV' (zero rows beyond the chunk) in bf16, dS = e^{gamma_C} dS + accumulator in fp32
 //               registers (row 32 q4 + lane, columns 64 half ..), its bf16 copy the next chunk's
 //               operand; records (dL/dS at each chunk end, dV') go out by bulk stores.
@@ -137,15 +138,16 @@ struct RevSmem {
   uint8_t qt[16384];      // Q~ = scale diag(e^gamma) Q, rows >= n zero (A MN-major: Q~^T dO)
   uint8_t kt[16384];      // K~ = diag(e^{gamma_C - gamma}) K            (A K-major: K~ dS)
   uint8_t wn[16384];      // -W rows t                                    (A MN-major: -W^T dV')
-  uint8_t p[8192];        // P = scale (Q K^T) o E                        (A MN-major: P^T dO)
+  uint8_t p[2][8192];     // [stage] P = scale (Q K^T) o E                (A MN-major: P^T dO)
   uint8_t dvp[16384];     // dV' rows t, two dv blocks                    (B MN-major)
   uint8_t ds[32768];      // dS bf16 rows dk, two dv blocks               (B MN-major)
   float gam[2][64];
+  float fsc[2][64];       // row factors of Q~ (scale e^gamma, zero beyond the chunk) and K~ (e^{gamma_C - gamma})
 };
 constexpr size_t kRevSmemBytes = sizeof(RevSmem) + 1024;
 static_assert(kRevSmemBytes <= 227 * 1024, "shared memory of the reverse chain");
 constexpr int kRevThreads = 320;
-constexpr uint32_t kRtW = 0, kRtG = 128, kRtA = 256, kRtC = 384;
+constexpr uint32_t kRtW = 0, kRtA = 256, kRtC = 384;  // TMEM columns: W (M = 64), dV' (M = 64), dS (M = 128)
 
 struct RevBars {
   uint64_t full[2], empty[2], pre_done, staged1, staged2, a_done, epi1, b_done, epi2;
@@ -206,7 +208,7 @@ __device__ bool run_rev_ws(const BwdParams& p, Ctx& cx, RevSmem& sm, RevBars& bb
         const size_t rec = (size_t)gc * Hv + h;
         if (j >= 2) rrole_wait(&bb.empty[st], ph.empty[st], abort);
         if (*abort) break;
-        mbar_arrive_expect_tx(&bb.full[st], 3 * 16384 + 8192 + 256);
+        mbar_arrive_expect_tx(&bb.full[st], 3 * 16384 + 2 * 8192 + 256);
         tma_load_3d(sm.k[st], &p.tm_k, 0, hk, tok0, &bb.full[st]);
         tma_load_3d(sm.k[st] + 8192, &p.tm_k, 64, hk, tok0, &bb.full[st]);
         tma_load_3d(sm.q[st], &p.tm_q, 0, hk, tok0, &bb.full[st]);
@@ -214,6 +216,7 @@ __device__ bool run_rev_ws(const BwdParams& p, Ctx& cx, RevSmem& sm, RevBars& bb
         tma_load_3d(sm.dout[st], &p.tm_do, 0, h, tok0, &bb.full[st]);
         tma_load_3d(sm.dout[st] + 8192, &p.tm_do, 64, h, tok0, &bb.full[st]);
         bulk_load(sm.tw[st], p.ws + p.L.f.tw + rec * 8192, 8192, &bb.full[st]);
+        bulk_load(sm.p[st], p.ws + p.L.f.pimg + rec * 8192, 8192, &bb.full[st]);
         bulk_load(sm.gam[st], p.ws + p.L.f.gam + rec * 256, 256, &bb.full[st]);
       }
       for (int j = (n >= 2 ? n - 2 : 0); j < n; ++j) rrole_wait(&bb.empty[j & 1], ph.empty[j & 1], abort);
@@ -223,21 +226,18 @@ __device__ bool run_rev_ws(const BwdParams& p, Ctx& cx, RevSmem& sm, RevBars& bb
   if (cx.warp == 9) {
     // ------------------------------------------------------------------ MMA issuer
     if (cx.lane == 0) {
-      auto prep = [&](int j) {  // W = T_w K, G = Q K^T of chunk j
+      auto prep = [&](int j) {  // W = T_w K of chunk j
         const int st = j & 1;
         for (int ks = 0; ks < 4; ++ks)
           umma_bf16(tm + kRtW, kmajor_desc(smem_u32(sm.tw[st]), 8192, ks), mnmajor_desc(smem_u32(sm.k[st]), 8192, ks),
                     idesc_bf16(64, 128, 0, 1), ks > 0);
-        for (int ks = 0; ks < 8; ++ks)
-          umma_bf16(tm + kRtG, kmajor_desc(smem_u32(sm.q[st]), 8192, ks), kmajor_desc(smem_u32(sm.k[st]), 8192, ks),
-                    idesc_bf16(64, 64, 0, 0), ks > 0);
         umma_commit(&bb.pre_done);
       };
       rrole_wait(&bb.full[0], ph.full[0], abort);
       if (!*abort) prep(0);
       for (int j = 0; j < n && !*abort; ++j) {
         const int st = j & 1;
-        // A: needs Q~, K~, P of chunk j (staged1), dS of chunk j (epi2 of j - 1, or the initial
+        // A: needs Q~, K~ of chunk j (staged1), dS of chunk j (epi2 of j - 1, or the initial
         // hand-off) and the dV' accumulator read (epi1 of j - 1)
         rrole_wait(&bb.staged1, ph.staged1, abort);
         rrole_wait(&bb.epi2, ph.epi2, abort);
@@ -250,11 +250,11 @@ __device__ bool run_rev_ws(const BwdParams& p, Ctx& cx, RevSmem& sm, RevBars& bb
           umma_bf16(tm + kRtA, kmajor_desc(smem_u32(sm.kt), 8192, ks), mnmajor_desc(smem_u32(sm.ds), 16384, ks),
                     idesc_bf16(64, 128, 0, 1), ks > 0);
         for (int ks = 0; ks < 4; ++ks)
-          umma_bf16(tm + kRtA, mnmajor_desc(smem_u32(sm.p), 8192, ks), mnmajor_desc(smem_u32(sm.dout[st]), 8192, ks),
+          umma_bf16(tm + kRtA, mnmajor_desc(smem_u32(sm.p[st]), 8192, ks), mnmajor_desc(smem_u32(sm.dout[st]), 8192, ks),
                     idesc_bf16(64, 128, 1, 1), 1);
         umma_commit(&bb.a_done);
-        // B as soon as dV' and -W are staged; chunk j + 1's W, G as soon as its operands have
-        // landed and W, G of chunk j have been read (staged2 of j), whichever comes first
+        // B as soon as dV' and -W are staged; chunk j + 1's W as soon as its operands have landed
+        // and W of chunk j has been read (staged2 of j), whichever comes first
         bool need_prep = j + 1 < n, b_issued = false, w_read = false;
         const long long t0 = clock64();
         while (!b_issued && !*abort) {
@@ -280,6 +280,8 @@ __device__ bool run_rev_ws(const BwdParams& p, Ctx& cx, RevSmem& sm, RevBars& bb
             b_issued = true;
           } else if (clock64() - t0 > kWaitBudget) {
             *abort = 1;
+          } else {
+            __nanosleep(64);  // leave the issue slots of this SM sub-partition to the epilogue warps
           }
         }
         if (*abort) break;
@@ -296,16 +298,20 @@ __device__ bool run_rev_ws(const BwdParams& p, Ctx& cx, RevSmem& sm, RevBars& bb
   // -------------------------------------------------------------------- epilogue warps 0-7
   const uint32_t lane_base = (uint32_t)(32 * cx.q4) << 16;
   const int i = 16 * cx.q4 + cx.lane;  // row of M = 64 accumulators (lanes < 16)
-  // Q~, K~ (from the stage) and P (from G) of chunk j
+  // Q~, K~ of chunk j (from the stage)
   auto staging1 = [&](int j) {
     const int gc = chunk_of(j), st = j & 1, nn = clen[gc];
     rrole_wait(&bb.full[st], ph.full[st], abort);
-    const float* gm = sm.gam[st];
-    const float gC = gm[63];
+    if (cx.tid < 128) {
+      const float* gm = sm.gam[st];
+      const int r = cx.tid & 63;
+      sm.fsc[cx.tid >> 6][r] = (cx.tid < 64) ? ((r < nn) ? __expf(gm[r]) * p.scale : 0.f) : __expf(gm[63] - gm[r]);
+    }
+    r_sync();
     for (int e = cx.tid; e < 2 * 2 * 64 * 8; e += 256) {
       const int which = e >> 10, b = (e >> 9) & 1, r = (e >> 3) & 63, cj = e & 7;
       const uint32_t off = b * 8192 + r * 128 + ((cj ^ (r & 7)) << 4);
-      const float sc = which == 0 ? ((r < nn) ? __expf(gm[r]) * p.scale : 0.f) : __expf(gC - gm[r]);
+      const float sc = sm.fsc[which][r];
       uint4 raw = *reinterpret_cast<const uint4*>((which == 0 ? sm.q[st] : sm.k[st]) + off);
       __nv_bfloat162* x = reinterpret_cast<__nv_bfloat162*>(&raw);
       uint32_t w[4];
@@ -316,31 +322,11 @@ __device__ bool run_rev_ws(const BwdParams& p, Ctx& cx, RevSmem& sm, RevBars& bb
       }
       *reinterpret_cast<uint4*>((which == 0 ? sm.qt : sm.kt) + off) = make_uint4(w[0], w[1], w[2], w[3]);
     }
-    rrole_wait(&bb.pre_done, ph.pre_done, abort);
-    {
-      float v[32];
-      tmem_ld16(tm + kRtG + lane_base + 32 * cx.half, v);
-      tmem_ld16(tm + kRtG + lane_base + 32 * cx.half + 16, v + 16);
-      tmem_ld_wait();
-      if (cx.lane < 16) {
-        const float gi = gm[i];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          float pv[8];
-#pragma unroll
-          for (int x = 0; x < 8; ++x) {
-            const int jj = 32 * cx.half + 8 * u + x;
-            pv[x] = (jj <= i && i < nn) ? __expf(gi - gm[jj]) * p.scale * v[8 * u + x] : 0.f;
-          }
-          const int cj = 4 * cx.half + u;
-          *reinterpret_cast<uint4*>(sm.p + i * 128 + ((cj ^ (i & 7)) << 4)) = pack8(pv);
-        }
-      }
-    }
     r_handoff(cx.tid, &bb.staged1);
   };
-  // -W of chunk j (W is ready: staging1 of j waited for it)
+  // -W of chunk j
   auto staging2 = [&]() {
+    rrole_wait(&bb.pre_done, ph.pre_done, abort);
 #pragma unroll
     for (int hc = 0; hc < 2; ++hc) {
       float v[32];
@@ -1442,6 +1428,7 @@ int launch_bwd(const BwdArgs& a, cudaStream_t stream, cudaEvent_t* ev) {
   f.scale = a.scale;
   f.st_img = ws + p.L.st_img;
   f.vp_img = ws + p.L.vp_img;
+  f.p_img = ws + p.L.f.pimg;  // kkt_solve also forms P = scale (Q K^T o E) for the reverse chain
   f.t_f32 = reinterpret_cast<float*>(ws + p.L.t_f32);
   f.tw_lo = ws + p.L.tw_lo;
   f.tu_lo = ws + p.L.tu_lo;
