@@ -805,7 +805,7 @@ __device__ __forceinline__ float warp_sum(float v) {
 __global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ BwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   GradSmem& sm = *reinterpret_cast<GradSmem*>(smem_align1024(smem_raw));
-  __shared__ uint64_t bar_ld, bar_mma;
+  __shared__ uint64_t bar_ld, bar_mma, bar_p1, bar_v, bar_tw;
   __shared__ uint32_t tmem_holder;
   Header* hd = reinterpret_cast<Header*>(p.ws + p.L.f.header);
   const int chunk = blockIdx.x, hk = blockIdx.y;
@@ -819,8 +819,36 @@ __global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ Bw
   if (tid == 0) {
     mbar_init(&bar_ld, 1);
     mbar_init(&bar_mma, 1);
+    mbar_init(&bar_p1, 1);
+    mbar_init(&bar_v, 1);
+    mbar_init(&bar_tw, 1);
     fence_mbar_init();
   }
+  uint32_t ph_p1 = 0, ph_v = 0, ph_tw = 0;
+  // bounded wait of every thread on one of the load barriers (uniform outcome)
+  auto wait_bar = [&](uint64_t* bar, uint32_t& ph) -> bool {
+    if (!wait_all(bar, ph)) return false;
+    ph ^= 1;
+    tc_fence_after();
+    return true;
+  };
+  // Loads of one value head's records, in the order their buffers become free. The phase-1 set
+  // (S, dS, V', dV', dO images and gamma) lands on bar_p1: its transaction count is armed by the
+  // first piece, the other pieces follow as the previous head releases their buffers.
+  const uint32_t kP1Bytes = 32768 * 2 + 16384 * 2 + 2 * 8192 + 256;
+  auto rec_of = [&](int hh2) { return (size_t)chunk * Hv + hk * G + hh2; };
+  auto load_do_gam = [&](int hh2) {  // thread 0; arms bar_p1
+    mbar_arrive_expect_tx(&bar_p1, kP1Bytes);
+    tma_load_3d(sm.bdO[0], &p.tm_do, 0, hk * G + hh2, tok0, &bar_p1);
+    tma_load_3d(sm.bdO[1], &p.tm_do, 64, hk * G + hh2, tok0, &bar_p1);
+    bulk_load(sm.gam, p.ws + p.L.f.gam + rec_of(hh2) * 256, 256, &bar_p1);
+  };
+  auto load_dvp = [&](int hh2) { bulk_load(sm.bdVp[0], p.ws + p.L.dvp_img + rec_of(hh2) * 16384, 16384, &bar_p1); };
+  auto load_s_ds = [&](int hh2) {
+    bulk_load(sm.bS[0], p.ws + p.L.st_img + rec_of(hh2) * 32768, 32768, &bar_p1);
+    bulk_load(sm.bdS[0], p.ws + p.L.ds_img + rec_of(hh2) * 32768, 32768, &bar_p1);
+  };
+  auto load_vp = [&](int hh2) { bulk_load(sm.bVp[0], p.ws + p.L.vp_img + rec_of(hh2) * 16384, 16384, &bar_p1); };
   if (cx.warp == 0) tmem_alloc(&tmem_holder, 512);
   sync_generic_to_async();
   cx.tmem = tmem_holder;
@@ -865,23 +893,19 @@ __global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ Bw
   }
   __syncthreads();
 
+  if (tid == 0 && ok) {
+    load_do_gam(0);
+    load_dvp(0);
+    load_s_ds(0);
+    load_vp(0);
+  }
   bool first_k = true;
   for (int hh = 0; hh < G && ok; ++hh) {
     const int h = hk * G + hh;
     const size_t rec = (size_t)chunk * Hv + h;
-    // ---------------- phase 1 loads
-    if (tid == 0) {
-      mbar_arrive_expect_tx(&bar_ld, 32768 * 2 + 16384 * 2 + 2 * 8192 + 256);
-      bulk_load(sm.bS[0], p.ws + p.L.st_img + rec * 32768, 32768, &bar_ld);
-      bulk_load(sm.bdS[0], p.ws + p.L.ds_img + rec * 32768, 32768, &bar_ld);
-      bulk_load(sm.bVp[0], p.ws + p.L.vp_img + rec * 16384, 16384, &bar_ld);
-      bulk_load(sm.bdVp[0], p.ws + p.L.dvp_img + rec * 16384, 16384, &bar_ld);
-      tma_load_3d(sm.bdO[0], &p.tm_do, 0, h, tok0, &bar_ld);
-      tma_load_3d(sm.bdO[1], &p.tm_do, 64, h, tok0, &bar_ld);
-      bulk_load(sm.gam, p.ws + p.L.f.gam + rec * 256, 256, &bar_ld);
-    }
+    const bool next = hh + 1 < G;
     if (tid < 64) sm.beta[tid] = (tid < n) ? p.beta[(size_t)(tok0 + tid) * Hv + h] : 0.f;
-    if (!(ok = cx.wait_ld())) break;
+    if (!(ok = wait_bar(&bar_p1, ph_p1))) break;
     if (tid < 64) sm.Gm[tid] = __expf(sm.gam[tid]);
     __syncthreads();
     const float gC = sm.gam[63], GC = __expf(gC);
@@ -962,6 +986,10 @@ __global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ Bw
       if (cx.lane == 0) sm.red[cx.warp] = fr;
     }
     if (!(ok = cx.commit_wait())) break;
+    if (tid == 0) {  // S is read: T (fp32) into its buffer (phase 2)
+      mbar_arrive_expect_tx(&bar_v, 16384 + 2 * 8192);
+      bulk_load(sm.bS[0], p.ws + p.L.t_f32 + rec * 16384, 16384, &bar_v);
+    }
     {
       float qs = 0.f;
       for (int cc = 0; cc < 64; cc += 16) {
@@ -984,6 +1012,10 @@ __global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ Bw
     // ---------------- (c) V'_s = diag(e^{gamma_C - gamma}) V' ; dk accumulation (dq has its own kernel)
     if (tid < 64) sm.cA[tid] = __expf(gC - sm.gam[tid]);
     __syncthreads();
+    if (tid == 0) {  // dO is read: V into its buffer (phase 2)
+      tma_load_3d(sm.bdO[0], &p.tm_v, 0, h, tok0, &bar_v);
+      tma_load_3d(sm.bdO[1], &p.tm_v, 64, h, tok0, &bar_v);
+    }
     scale_rows(sm.bVp[0], sm.cA, tid);
     scale_rows(sm.bVp[1], sm.cA, tid);
     sync_generic_to_async();
@@ -998,16 +1030,14 @@ __global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ Bw
     first_k = false;
     const float fro = ((sm.red[0] + sm.red[1]) + (sm.red[2] + sm.red[3])) + ((sm.red[4] + sm.red[5]) + (sm.red[6] + sm.red[7]));
     if (!(ok = cx.commit_wait())) break;
-    // ---------------- phase 2 loads: V, T, T_w, T_u
+    // ---------------- phase 2 loads: T_w, T_u (dS is read); V and T were issued earlier
     if (tid == 0) {
-      mbar_arrive_expect_tx(&bar_ld, 2 * 8192 + 16384 + 2 * 8192);
-      tma_load_3d(sm.bdO[0], &p.tm_v, 0, h, tok0, &bar_ld);
-      tma_load_3d(sm.bdO[1], &p.tm_v, 64, h, tok0, &bar_ld);
-      bulk_load(sm.bS[0], p.ws + p.L.t_f32 + rec * 16384, 16384, &bar_ld);
-      bulk_load(sm.bdS[0], p.ws + p.L.f.tw + rec * 8192, 8192, &bar_ld);
-      bulk_load(sm.bdS[0] + 8192, p.ws + p.L.f.tu + rec * 8192, 8192, &bar_ld);
+      mbar_arrive_expect_tx(&bar_tw, 2 * 8192);
+      bulk_load(sm.bdS[0], p.ws + p.L.f.tw + rec * 8192, 8192, &bar_tw);
+      bulk_load(sm.bdS[0] + 8192, p.ws + p.L.f.tu + rec * 8192, 8192, &bar_tw);
     }
-    if (!(ok = cx.wait_ld())) break;
+    if (!(ok = wait_bar(&bar_v, ph_v))) break;
+    if (!(ok = wait_bar(&bar_tw, ph_tw))) break;
     const float* Tf = reinterpret_cast<const float*>(sm.bS[0]);
     uint8_t* Tb = sm.bS[1];                 // T bf16 image (bytes [16K, 24K) of bS)
     uint8_t* Tw = sm.bdS[0];
@@ -1038,6 +1068,11 @@ __global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ Bw
                   idesc_bf16(64, 128, 1, 1), 1);
     }
     if (!(ok = cx.commit_wait())) break;
+    if (tid == 0 && next) {  // V is read: the next head's dO (gamma follows once (h) is done)
+      mbar_arrive_expect_tx(&bar_p1, kP1Bytes);
+      tma_load_3d(sm.bdO[0], &p.tm_do, 0, h + 1, tok0, &bar_p1);
+      tma_load_3d(sm.bdO[1], &p.tm_do, 64, h + 1, tok0, &bar_p1);
+    }
     float* vyM = reinterpret_cast<float*>(sm.bVp[0]);
     float* kxM = reinterpret_cast<float*>(sm.bdVp[0]);
     {
@@ -1089,6 +1124,7 @@ __global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ Bw
         umma_bf16(tm + kGt1, kmajor_desc(smem_u32(dTt), 8192, ks), kmajor_desc(smem_u32(Tb), 8192, ks),
                   idesc_bf16(64, 64, 0, 0), ks > 0);
     col_sums(sm, vyM, kxM, sm.vy, sm.kx, tid);
+    if (tid == 0 && next) load_dvp(hh + 1);  // the kx scratch is summed: the next head's dV'
     if (!(ok = cx.commit_wait())) break;
     for (int cc = 0; cc < 32; cc += 16) {
       float v[16];
@@ -1111,6 +1147,7 @@ __global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ Bw
         umma_bf16(tm + kGt1, mnmajor_desc(smem_u32(Tb), 8192, ks), mnmajor_desc(smem_u32(Rt), 8192, ks),
                   idesc_bf16(64, 64, 1, 1), ks > 0);
     if (!(ok = cx.commit_wait())) break;
+    if (tid == 0 && next) load_s_ds(hh + 1);  // T, R, T_w, T_u, dT are read: the next head's S, dS
     float* LK = vyM;  // vy / kx column sums are done
     {
       const int i = i_row;
@@ -1161,6 +1198,7 @@ __global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ Bw
                   idesc_bf16(64, 128, 1, 1), 1);
     }
     col_sums(sm, LK, nullptr, sm.cA, nullptr, tid);
+    if (tid == 0 && next) load_vp(hh + 1);  // the L o KK scratch is summed: the next head's V'
     // ---------------- (h) dgamma -> dg (reverse cumulative sum in the chunk), dbeta
     if (tid < 64) {
       const int i = tid;
@@ -1194,6 +1232,8 @@ __global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ Bw
       p.dg[(size_t)(tok0 + tid) * Hv + h] = s;
       p.dbeta[(size_t)(tok0 + tid) * Hv + h] = sm.vy[tid] + sm.Gm[tid] * sm.kx[tid] + sm.db3[0][tid] + sm.db3[1][tid];
     }
+    __syncthreads();  // gamma of this head is no longer read
+    if (tid == 0 && next) bulk_load(sm.gam, p.ws + p.L.f.gam + rec_of(hh + 1) * 256, 256, &bar_p1);
     if (!(ok = cx.commit_wait())) break;  // (g) done before the next head reuses bP
   }
   if (ok) {
