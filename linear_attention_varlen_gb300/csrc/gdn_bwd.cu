@@ -766,13 +766,16 @@ struct GradSmem {
   uint8_t bdO[2][8192];    // dO              | phase 2: V
   uint8_t bW[2][8192];     // fp32 scratch (dEg) | dW rows t
   uint8_t bP[8192];        // scale dQK, then L = dA o diag(beta) E (strictly lower)
-  float gam[64], beta[64], Gm[64];
+  float gam[64], beta[64], Gm[64], Gi[64];  // gamma, beta, e^{gamma}, e^{-gamma}
   float part[8][64];
   float vy[64], kx[64], cA[64], db3[2][64];
   float red4[2][4][64];    // partial column sums (two matrices x four row quarters)
   float red[8];
 };
 constexpr size_t kGradSmemBytes = sizeof(GradSmem) + 1024;
+// Chunk decay above which e^{gamma_i} and e^{-gamma_j} both stay finite in fp32 (gamma is the
+// chunk-local cumulative log-decay, nonincreasing, so gamma_63 is its minimum).
+constexpr float kFactorMin = -80.f;
 constexpr uint32_t kGtK = 128, kGt1 = 256, kGt2 = 384;
 
 // Column sums of one or two fp32 64x64 fz matrices over rows [0, 64) with all 256 threads:
@@ -906,7 +909,10 @@ __global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ Bw
     const bool next = hh + 1 < G;
     if (tid < 64) sm.beta[tid] = (tid < n) ? p.beta[(size_t)(tok0 + tid) * Hv + h] : 0.f;
     if (!(ok = wait_bar(&bar_p1, ph_p1))) break;
-    if (tid < 64) sm.Gm[tid] = __expf(sm.gam[tid]);
+    if (tid < 64) {
+      sm.Gm[tid] = __expf(sm.gam[tid]);
+      sm.Gi[tid] = __expf(-sm.gam[tid]);
+    }
     __syncthreads();
     const float gC = sm.gam[63], GC = __expf(gC);
     float* dEg = reinterpret_cast<float*>(sm.bW[0]);
@@ -922,7 +928,9 @@ __global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ Bw
     if (!(ok = cx.commit_wait())) break;
     {
       float rs = 0.f;
-      const float gi = has_row ? sm.gam[i_row] : 0.f;
+      const float gi = has_row ? sm.gam[i_row] : 0.f, ei = has_row ? sm.Gm[i_row] : 0.f;
+      // e^{gamma_i - gamma_j} as e^{gamma_i} e^{-gamma_j} while both factors stay finite
+      const bool factored = sm.gam[63] > kFactorMin;
       for (int cc = 0; cc < 32; cc += 16) {
         float v[16];
         tmem_ld16(tm + kGt1 + cx.lane_base() + 32 * cx.half + cc, v);
@@ -933,7 +941,7 @@ __global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ Bw
 #pragma unroll
           for (int x = 0; x < 16; ++x) {
             const int j = 32 * cx.half + cc + x;
-            const float e = (j <= i && i < n) ? __expf(gi - sm.gam[j]) : 0.f;
+            const float e = (j <= i && i < n) ? (factored ? ei * sm.Gi[j] : __expf(gi - sm.gam[j])) : 0.f;
             const float dqk = v[x] * e;
             dq8[x] = dqk * p.scale;
             const float eg = dqk * sm.qkf[fz(i, j)];
@@ -1152,6 +1160,8 @@ __global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ Bw
     {
       const int i = i_row;
       const float gi = has_row ? sm.gam[i] : 0.f, bi = has_row ? sm.beta[i] : 0.f;
+      const float ei = has_row ? sm.Gm[i] : 0.f;
+      const bool factored = sm.gam[63] > kFactorMin;
       float b3 = 0.f;
       for (int cc = 0; cc < 32; cc += 16) {
         float v[16];
@@ -1170,7 +1180,7 @@ __global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ Bw
               const int x = x4 + u, j = j0 + u;
               const bool in = (j < i && i < n);
               const float da = in ? -v[x] : 0.f;
-              const float e = in ? __expf(gi - sm.gam[j]) : 0.f;
+              const float e = in ? (factored ? ei * sm.Gi[j] : __expf(gi - sm.gam[j])) : 0.f;
               const float dae = da * e;
               b3 += dae * kv[u];
               l16[x] = dae * bi;
@@ -1274,6 +1284,7 @@ struct DqSmem {
   uint8_t qh[8192];      // scale dQK high part     (A K-major)
   uint8_t ql[8192];      // scale dQK low part
   float gam[64];
+  float eg[64], egi[64]; // e^{gamma}, e^{-gamma}
 };
 constexpr size_t kDqSmemBytes = sizeof(DqSmem) + 1024;
 constexpr uint32_t kDtP = 0, kDt1 = 128, kDt2 = 256;
@@ -1324,6 +1335,10 @@ __global__ void __launch_bounds__(256, 1) dq_kernel(const __grid_constant__ BwdP
       bulk_load(sm.gam, p.ws + p.L.f.gam + rec * 256, 256, &bar_ld);
     }
     if (!(ok = cx.wait_ld())) break;
+    if (tid < 64) {
+      sm.eg[tid] = __expf(sm.gam[tid]);
+      sm.egi[tid] = __expf(-sm.gam[tid]);
+    }
     // dP = dO V'^T (hi + lo)
     if (tid == 0) {
       for (int ks = 0; ks < 8; ++ks)
@@ -1333,16 +1348,21 @@ __global__ void __launch_bounds__(256, 1) dq_kernel(const __grid_constant__ BwdP
         umma_bf16(tm + kDtP, kmajor_desc(smem_u32(sm.dout[0]), 8192, ks), kmajor_desc(smem_u32(sm.vl[0]), 8192, ks),
                   idesc_bf16(64, 64, 0, 0), 1);
     }
-    if (!(ok = cx.commit_wait())) break;
+    if (!(ok = cx.commit_wait())) break;  // (its barrier also publishes eg / egi)
+    // e^{gamma_i - gamma_j} as e^{gamma_i} e^{-gamma_j} while both factors stay finite
+    const bool factored = sm.gam[63] > kFactorMin;
     for (int cc = 0; cc < 32; cc += 16) {
       float v[16];
       tmem_ld16(tm + kDtP + cx.lane_base() + 32 * cx.half + cc, v);
       tmem_ld_wait();
       if (has_row) {
         float hi[16], lo[16];
+        const float es = sm.eg[i_row] * p.scale;
+#pragma unroll
         for (int x = 0; x < 16; ++x) {
           const int j = 32 * cx.half + cc + x;
-          const float d = (j <= i_row && i_row < n) ? v[x] * __expf(sm.gam[i_row] - sm.gam[j]) * p.scale : 0.f;
+          const float e = factored ? es * sm.egi[j] : __expf(sm.gam[i_row] - sm.gam[j]) * p.scale;
+          const float d = (j <= i_row && i_row < n) ? v[x] * e : 0.f;
           hi[x] = __bfloat162float(__float2bfloat16_rn(d));
           lo[x] = d - hi[x];
         }
