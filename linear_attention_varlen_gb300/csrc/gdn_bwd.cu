@@ -937,11 +937,18 @@ __global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ Bw
         tmem_ld_wait();
         if (has_row) {
           const int i = i_row;
-          float dq8[16];
+          float dq8[16], ev[16];
+          if (factored) {
+#pragma unroll
+            for (int x = 0; x < 16; ++x) ev[x] = ei * sm.Gi[32 * cx.half + cc + x];
+          } else {
+#pragma unroll
+            for (int x = 0; x < 16; ++x) ev[x] = __expf(gi - sm.gam[32 * cx.half + cc + x]);
+          }
 #pragma unroll
           for (int x = 0; x < 16; ++x) {
             const int j = 32 * cx.half + cc + x;
-            const float e = (j <= i && i < n) ? (factored ? ei * sm.Gi[j] : __expf(gi - sm.gam[j])) : 0.f;
+            const float e = (j <= i && i < n) ? ev[x] : 0.f;
             const float dqk = v[x] * e;
             dq8[x] = dqk * p.scale;
             const float eg = dqk * sm.qkf[fz(i, j)];
@@ -1168,7 +1175,14 @@ __global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ Bw
         tmem_ld16(tm + kGt1 + cx.lane_base() + 32 * cx.half + cc, v);
         tmem_ld_wait();
         if (has_row) {
-          float l16[16];
+          float l16[16], ev[16];
+          if (factored) {
+#pragma unroll
+            for (int x = 0; x < 16; ++x) ev[x] = ei * sm.Gi[32 * cx.half + cc + x];
+          } else {
+#pragma unroll
+            for (int x = 0; x < 16; ++x) ev[x] = __expf(gi - sm.gam[32 * cx.half + cc + x]);
+          }
 #pragma unroll
           for (int x4 = 0; x4 < 16; x4 += 4) {
             const int j0 = 32 * cx.half + cc + x4;
@@ -1180,7 +1194,7 @@ __global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ Bw
               const int x = x4 + u, j = j0 + u;
               const bool in = (j < i && i < n);
               const float da = in ? -v[x] : 0.f;
-              const float e = in ? (factored ? ei * sm.Gi[j] : __expf(gi - sm.gam[j])) : 0.f;
+              const float e = in ? ev[x] : 0.f;
               const float dae = da * e;
               b3 += dae * kv[u];
               l16[x] = dae * bi;
@@ -1358,11 +1372,18 @@ __global__ void __launch_bounds__(256, 1) dq_kernel(const __grid_constant__ BwdP
       if (has_row) {
         float hi[16], lo[16];
         const float es = sm.eg[i_row] * p.scale;
+        float ev[16];
+        if (factored) {
+#pragma unroll
+          for (int x = 0; x < 16; ++x) ev[x] = es * sm.egi[32 * cx.half + cc + x];
+        } else {
+#pragma unroll
+          for (int x = 0; x < 16; ++x) ev[x] = __expf(sm.gam[i_row] - sm.gam[32 * cx.half + cc + x]) * p.scale;
+        }
 #pragma unroll
         for (int x = 0; x < 16; ++x) {
           const int j = 32 * cx.half + cc + x;
-          const float e = factored ? es * sm.egi[j] : __expf(sm.gam[i_row] - sm.gam[j]) * p.scale;
-          const float d = (j <= i_row && i_row < n) ? v[x] * e : 0.f;
+          const float d = (j <= i_row && i_row < n) ? v[x] * ev[x] : 0.f;
           hi[x] = __bfloat162float(__float2bfloat16_rn(d));
           lo[x] = d - hi[x];
         }

@@ -422,11 +422,18 @@ __global__ void __launch_bounds__(256) kkt_solve_kernel(const __grid_constant__ 
           const float qv[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
           const float gi = gam[i], ei = eg[i] * p.scale;
           float pv[8];
+          if (factored) {
 #pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            const int j = 8 * cj + u;
-            const float e2 = factored ? ei * egi[j] : __expf(gi - gam[j]) * p.scale;
-            pv[u] = (j <= i && i < n) ? e2 * qv[u] : 0.f;
+            for (int u = 0; u < 8; ++u) {
+              const int j = 8 * cj + u;
+              pv[u] = (j <= i && i < n) ? ei * egi[j] * qv[u] : 0.f;
+            }
+          } else {
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              const int j = 8 * cj + u;
+              pv[u] = (j <= i && i < n) ? __expf(gi - gam[j]) * p.scale * qv[u] : 0.f;
+            }
           }
           *reinterpret_cast<uint4*>(dp + i * 128 + ((cj ^ (i & 7)) << 4)) =
               make_uint4(pack_bf16x2(pv[0], pv[1]), pack_bf16x2(pv[2], pv[3]), pack_bf16x2(pv[4], pv[5]),
