@@ -153,7 +153,33 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
 #pragma unroll
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
+// 16 TMEM lanes (taddr's lane field: the first of them) x 32 columns over the whole warp:
+// thread t gets rows t/4 and t/4 + 8 of the 16 and columns 8k + 2(t%4) + {0, 1}, k = 0..3, in
+// the order v[4k] = (t/4, c), v[4k+1] = (t/4, c+1), v[4k+2] = (t/4+8, c), v[4k+3] = (t/4+8, c+1)
+// with c = 8k + 2(t%4) (shape 16x256b, repeated 4 times). This is how an M = 64 accumulator
+// (16 valid lanes per 32-lane quarter) is read with all 32 threads of a warp.
+__device__ __forceinline__ void tmem_ld16x256_x4(uint32_t taddr, float* v) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x256b.x4.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Sum over the four threads of a row group of the 16x256b layout (lanes 4g .. 4g + 3).
+__device__ __forceinline__ float quad_sum(float x) {
+  x += __shfl_xor_sync(0xffffffffu, x, 1);
+  x += __shfl_xor_sync(0xffffffffu, x, 2);
+  return x;
+}
+// Byte offset of the bf16 pair (row r, columns c, c + 1; c even) in a 64-column SW128 block.
+__device__ __forceinline__ uint32_t sw128_pair(int r, int c) {
+  return r * 128 + ((((c >> 3) ^ r) & 7) << 4) + ((c & 7) << 1);
+}
 
 // ------------------------------------------------------------------------------------------ UMMA
 

@@ -927,51 +927,70 @@ __global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ Bw
     }
     if (!(ok = cx.commit_wait())) break;
     {
-      float rs = 0.f;
-      const float gi = has_row ? sm.gam[i_row] : 0.f, ei = has_row ? sm.Gm[i_row] : 0.f;
+      // all 32 lanes: rows r0 = 16 q4 + lane / 4 and r0 + 8, column pairs (tmem_ld16x256_x4)
+      const int c2 = 2 * (cx.lane & 3);
+      const int rw[2] = {16 * cx.q4 + (cx.lane >> 2), 16 * cx.q4 + (cx.lane >> 2) + 8};
       // e^{gamma_i - gamma_j} as e^{gamma_i} e^{-gamma_j} while both factors stay finite
       const bool factored = sm.gam[63] > kFactorMin;
-      for (int cc = 0; cc < 32; cc += 16) {
-        float v[16];
-        tmem_ld16(tm + kGt1 + cx.lane_base() + 32 * cx.half + cc, v);
-        tmem_ld_wait();
-        if (has_row) {
-          const int i = i_row;
-          float dq8[16], ev[16];
-          if (factored) {
+      float rs[2] = {0.f, 0.f};
+      {
+        float v[16], ev[16];
+        tmem_ld16x256_x4(tm + kGt1 + cx.lane_base() + 32 * cx.half, v);
+        if (factored) {
 #pragma unroll
-            for (int x = 0; x < 16; ++x) ev[x] = ei * sm.Gi[32 * cx.half + cc + x];
-          } else {
+          for (int k = 0; k < 4; ++k)
 #pragma unroll
-            for (int x = 0; x < 16; ++x) ev[x] = __expf(gi - sm.gam[32 * cx.half + cc + x]);
-          }
+            for (int q = 0; q < 4; ++q)
+              ev[4 * k + q] = sm.Gm[rw[q >> 1]] * sm.Gi[32 * cx.half + 8 * k + c2 + (q & 1)];
+        } else {
 #pragma unroll
-          for (int x = 0; x < 16; ++x) {
-            const int j = 32 * cx.half + cc + x;
-            const float e = (j <= i && i < n) ? ev[x] : 0.f;
-            const float dqk = v[x] * e;
-            dq8[x] = dqk * p.scale;
-            const float eg = dqk * sm.qkf[fz(i, j)];
-            dEg[fz(i, j)] = eg;
-            rs += eg;
-          }
+          for (int k = 0; k < 4; ++k)
 #pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int cj = ((32 * cx.half + cc) >> 3) + u;
-            *reinterpret_cast<uint4*>(sm.bP + i * 128 + ((cj ^ (i & 7)) << 4)) = pack8(dq8 + 8 * u);
-          }
+            for (int q = 0; q < 4; ++q)
+              ev[4 * k + q] = __expf(sm.gam[rw[q >> 1]] - sm.gam[32 * cx.half + 8 * k + c2 + (q & 1)]);
         }
-      }
-      if (has_row) sm.part[0 + cx.half][i_row] = rs;
-      float kt = 0.f;
-      for (int cc = 0; cc < 64; cc += 16) {
-        float v[16];
-        tmem_ld16(tm + kGt2 + cx.lane_base() + 64 * cx.half + cc, v);
         tmem_ld_wait();
-        if (has_row)
-          for (int x = 0; x < 16; ++x) kt += bf16_at(sm.bVp[cx.half], i_row, cc + x) * v[x];
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+#pragma unroll
+          for (int rr = 0; rr < 2; ++rr) {
+            const int r = rw[rr], j = 32 * cx.half + 8 * k + c2;
+            const float d0 = (j <= r && r < n) ? v[4 * k + 2 * rr] * ev[4 * k + 2 * rr] : 0.f;
+            const float d1 = (j + 1 <= r && r < n) ? v[4 * k + 2 * rr + 1] * ev[4 * k + 2 * rr + 1] : 0.f;
+            *reinterpret_cast<uint32_t*>(sm.bP + sw128_pair(r, j)) = pack_bf16x2(d0 * p.scale, d1 * p.scale);
+            const float2 qk = *reinterpret_cast<const float2*>(sm.qkf + fz(r, j));
+            const float e0 = d0 * qk.x, e1 = d1 * qk.y;
+            *reinterpret_cast<float2*>(dEg + fz(r, j)) = make_float2(e0, e1);
+            rs[rr] += e0 + e1;
+          }
       }
-      if (has_row) sm.part[2 + cx.half][i_row] = kt;
+      rs[0] = quad_sum(rs[0]);
+      rs[1] = quad_sum(rs[1]);
+      if ((cx.lane & 3) == 0) {
+        sm.part[0 + cx.half][rw[0]] = rs[0];
+        sm.part[0 + cx.half][rw[1]] = rs[1];
+      }
+      float kt[2] = {0.f, 0.f};
+#pragma unroll
+      for (int cc = 0; cc < 64; cc += 32) {
+        float v[16];
+        tmem_ld16x256_x4(tm + kGt2 + cx.lane_base() + 64 * cx.half + cc, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+#pragma unroll
+          for (int rr = 0; rr < 2; ++rr) {
+            const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(
+                sm.bVp[cx.half] + sw128_pair(rw[rr], cc + 8 * k + c2)));
+            kt[rr] += a.x * v[4 * k + 2 * rr] + a.y * v[4 * k + 2 * rr + 1];
+          }
+      }
+      kt[0] = quad_sum(kt[0]);
+      kt[1] = quad_sum(kt[1]);
+      if ((cx.lane & 3) == 0) {
+        sm.part[2 + cx.half][rw[0]] = kt[0];
+        sm.part[2 + cx.half][rw[1]] = kt[1];
+      }
     }
     __syncthreads();
     col_sums(sm, dEg, nullptr, sm.part[4], nullptr, tid);
@@ -1091,43 +1110,41 @@ __global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ Bw
     float* vyM = reinterpret_cast<float*>(sm.bVp[0]);
     float* kxM = reinterpret_cast<float*>(sm.bdVp[0]);
     {
-      float* dvrow = p.dv + ((size_t)(tok0 + i_row) * Hv + h) * kDim + 64 * cx.half;
-      for (int cc = 0; cc < 64; cc += 16) {
+      // all 32 lanes: rows r0 = 16 q4 + lane / 4 and r0 + 8, column pairs (tmem_ld16x256_x4)
+      const int c2 = 2 * (cx.lane & 3);
+      const int rw[2] = {16 * cx.q4 + (cx.lane >> 2), 16 * cx.q4 + (cx.lane >> 2) + 8};
+#pragma unroll
+      for (int cc = 0; cc < 64; cc += 32) {
         float v[16];
-        tmem_ld16(tm + kGt1 + cx.lane_base() + 64 * cx.half + cc, v);
+        tmem_ld16x256_x4(tm + kGt1 + cx.lane_base() + 64 * cx.half + cc, v);
         tmem_ld_wait();
-        if (has_row && i_row < n)
-          for (int x = 0; x < 16; x += 4)
-            *reinterpret_cast<float4*>(dvrow + cc + x) = make_float4(v[x], v[x + 1], v[x + 2], v[x + 3]);
-      }
-      for (int cc = 0; cc < 32; cc += 16) {
-        float d1[16], d2[16];
-        tmem_ld16(tm + kGt2 + cx.lane_base() + 32 * cx.half + cc, d1);
-        tmem_ld16(tm + kGt2 + 64 + cx.lane_base() + 32 * cx.half + cc, d2);
-        tmem_ld_wait();
-        if (has_row) {
-          const int i = i_row;
-          float dt[16];
 #pragma unroll
-          for (int x4 = 0; x4 < 16; x4 += 4) {
-            const int j0 = 32 * cx.half + cc + x4;
-            const float4 tf = *reinterpret_cast<const float4*>(Tf + fz(i, j0));
-            const float tv[4] = {tf.x, tf.y, tf.z, tf.w};
-            float vy4[4], kx4[4];
+        for (int rr = 0; rr < 2; ++rr)
+          if (rw[rr] < n) {
+            float* dvrow = p.dv + ((size_t)(tok0 + rw[rr]) * Hv + h) * kDim + 64 * cx.half + cc + c2;
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const int x = x4 + u, j = j0 + u;
-              dt[x] = d1[x] * sm.beta[j] + d2[x] * sm.beta[j] * sm.Gm[j];
-              vy4[u] = tv[u] * d1[x];
-              kx4[u] = tv[u] * d2[x];
-            }
-            *reinterpret_cast<float4*>(vyM + fz(i, j0)) = make_float4(vy4[0], vy4[1], vy4[2], vy4[3]);
-            *reinterpret_cast<float4*>(kxM + fz(i, j0)) = make_float4(kx4[0], kx4[1], kx4[2], kx4[3]);
+            for (int k = 0; k < 4; ++k)
+              *reinterpret_cast<float2*>(dvrow + 8 * k) = make_float2(v[4 * k + 2 * rr], v[4 * k + 2 * rr + 1]);
           }
+      }
+      {
+        float d1[16], d2[16];
+        tmem_ld16x256_x4(tm + kGt2 + cx.lane_base() + 32 * cx.half, d1);
+        tmem_ld16x256_x4(tm + kGt2 + 64 + cx.lane_base() + 32 * cx.half, d2);
+        tmem_ld_wait();
 #pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int cj = ((32 * cx.half + cc) >> 3) + u;
-            *reinterpret_cast<uint4*>(dTt + i * 128 + ((cj ^ (i & 7)) << 4)) = pack8(dt + 8 * u);
+        for (int k = 0; k < 4; ++k) {
+          const int j = 32 * cx.half + 8 * k + c2;
+          const float b0 = sm.beta[j], b1 = sm.beta[j + 1];
+          const float bg0 = b0 * sm.Gm[j], bg1 = b1 * sm.Gm[j + 1];
+#pragma unroll
+          for (int rr = 0; rr < 2; ++rr) {
+            const int r = rw[rr], x = 4 * k + 2 * rr;
+            const float2 tf = *reinterpret_cast<const float2*>(Tf + fz(r, j));
+            *reinterpret_cast<uint32_t*>(dTt + sw128_pair(r, j)) =
+                pack_bf16x2(d1[x] * b0 + d2[x] * bg0, d1[x + 1] * b1 + d2[x + 1] * bg1);
+            *reinterpret_cast<float2*>(vyM + fz(r, j)) = make_float2(tf.x * d1[x], tf.y * d1[x + 1]);
+            *reinterpret_cast<float2*>(kxM + fz(r, j)) = make_float2(tf.x * d2[x], tf.y * d2[x + 1]);
           }
         }
       }
@@ -1165,51 +1182,47 @@ __global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ Bw
     if (tid == 0 && next) load_s_ds(hh + 1);  // T, R, T_w, T_u, dT are read: the next head's S, dS
     float* LK = vyM;  // vy / kx column sums are done
     {
-      const int i = i_row;
-      const float gi = has_row ? sm.gam[i] : 0.f, bi = has_row ? sm.beta[i] : 0.f;
-      const float ei = has_row ? sm.Gm[i] : 0.f;
+      // all 32 lanes: rows r0 = 16 q4 + lane / 4 and r0 + 8, column pairs (tmem_ld16x256_x4)
+      const int c2 = 2 * (cx.lane & 3);
+      const int rw[2] = {16 * cx.q4 + (cx.lane >> 2), 16 * cx.q4 + (cx.lane >> 2) + 8};
       const bool factored = sm.gam[63] > kFactorMin;
-      float b3 = 0.f;
-      for (int cc = 0; cc < 32; cc += 16) {
-        float v[16];
-        tmem_ld16(tm + kGt1 + cx.lane_base() + 32 * cx.half + cc, v);
-        tmem_ld_wait();
-        if (has_row) {
-          float l16[16], ev[16];
-          if (factored) {
+      float v[16], ev[16];
+      tmem_ld16x256_x4(tm + kGt1 + cx.lane_base() + 32 * cx.half, v);
+      if (factored) {
 #pragma unroll
-            for (int x = 0; x < 16; ++x) ev[x] = ei * sm.Gi[32 * cx.half + cc + x];
-          } else {
+        for (int k = 0; k < 4; ++k)
 #pragma unroll
-            for (int x = 0; x < 16; ++x) ev[x] = __expf(gi - sm.gam[32 * cx.half + cc + x]);
-          }
+          for (int q = 0; q < 4; ++q) ev[4 * k + q] = sm.Gm[rw[q >> 1]] * sm.Gi[32 * cx.half + 8 * k + c2 + (q & 1)];
+      } else {
 #pragma unroll
-          for (int x4 = 0; x4 < 16; x4 += 4) {
-            const int j0 = 32 * cx.half + cc + x4;
-            const float4 kk4 = *reinterpret_cast<const float4*>(sm.kkf + fz(i, j0));
-            const float kv[4] = {kk4.x, kk4.y, kk4.z, kk4.w};
-            float lk[4];
+        for (int k = 0; k < 4; ++k)
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const int x = x4 + u, j = j0 + u;
-              const bool in = (j < i && i < n);
-              const float da = in ? -v[x] : 0.f;
-              const float e = in ? ev[x] : 0.f;
-              const float dae = da * e;
-              b3 += dae * kv[u];
-              l16[x] = dae * bi;
-              lk[u] = l16[x] * kv[u];
-            }
-            *reinterpret_cast<float4*>(LK + fz(i, j0)) = make_float4(lk[0], lk[1], lk[2], lk[3]);
-          }
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int cj = ((32 * cx.half + cc) >> 3) + u;
-            *reinterpret_cast<uint4*>(sm.bP + i * 128 + ((cj ^ (i & 7)) << 4)) = pack8(l16 + 8 * u);
-          }
-        }
+          for (int q = 0; q < 4; ++q)
+            ev[4 * k + q] = __expf(sm.gam[rw[q >> 1]] - sm.gam[32 * cx.half + 8 * k + c2 + (q & 1)]);
       }
-      if (has_row) sm.db3[cx.half][i] = b3;
+      tmem_ld_wait();
+      float b3[2] = {0.f, 0.f};
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+#pragma unroll
+        for (int rr = 0; rr < 2; ++rr) {
+          const int r = rw[rr], j = 32 * cx.half + 8 * k + c2, x = 4 * k + 2 * rr;
+          const float bi = sm.beta[r];
+          const float2 kk = *reinterpret_cast<const float2*>(sm.kkf + fz(r, j));
+          // dA = -v, strictly lower and inside the chunk; L = dA o diag(beta) E
+          const float dae0 = (j < r && r < n) ? -v[x] * ev[x] : 0.f;
+          const float dae1 = (j + 1 < r && r < n) ? -v[x + 1] * ev[x + 1] : 0.f;
+          b3[rr] += dae0 * kk.x + dae1 * kk.y;
+          const float l0 = dae0 * bi, l1 = dae1 * bi;
+          *reinterpret_cast<float2*>(LK + fz(r, j)) = make_float2(l0 * kk.x, l1 * kk.y);
+          *reinterpret_cast<uint32_t*>(sm.bP + sw128_pair(r, j)) = pack_bf16x2(l0, l1);
+        }
+      b3[0] = quad_sum(b3[0]);
+      b3[1] = quad_sum(b3[1]);
+      if ((cx.lane & 3) == 0) {
+        sm.db3[cx.half][rw[0]] = b3[0];
+        sm.db3[cx.half][rw[1]] = b3[1];
+      }
     }
     sync_generic_to_async();
     // ---------------- (g) dk += (L + L^T) K: the image of L read K-major (L) and MN-major (L^T)
