@@ -1025,23 +1025,33 @@ __global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ Bw
       bulk_load(sm.bS[0], p.ws + p.L.t_f32 + rec * 16384, 16384, &bar_v);
     }
     {
-      float qs = 0.f;
-      for (int cc = 0; cc < 64; cc += 16) {
-        float v[16], w[16];
-        tmem_ld16(tm + kGt1 + cx.lane_base() + 64 * cx.half + cc, v);
-        tmem_ld16(tm + kGt2 + cx.lane_base() + 64 * cx.half + cc, w);
-        tmem_ld_wait();
-        if (has_row) {
-          for (int x = 0; x < 16; ++x) qs += bf16_at(sm.bdO[cx.half], i_row, cc + x) * v[x];
-          for (int x = 0; x < 16; ++x) w[x] = -w[x];
+      // all 32 lanes: rows r0 = 16 q4 + lane / 4 and r0 + 8, column pairs (tmem_ld16x256_x4)
+      const int c2 = 2 * (cx.lane & 3);
+      const int rw[2] = {16 * cx.q4 + (cx.lane >> 2), 16 * cx.q4 + (cx.lane >> 2) + 8};
+      float qs[2] = {0.f, 0.f};
 #pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int cj = (cc >> 3) + u;
-            *reinterpret_cast<uint4*>(sm.bW[cx.half] + i_row * 128 + ((cj ^ (i_row & 7)) << 4)) = pack8(w + 8 * u);
+      for (int cc = 0; cc < 64; cc += 32) {
+        float v[16], w[16];
+        tmem_ld16x256_x4(tm + kGt1 + cx.lane_base() + 64 * cx.half + cc, v);
+        tmem_ld16x256_x4(tm + kGt2 + cx.lane_base() + 64 * cx.half + cc, w);
+        tmem_ld_wait();
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+#pragma unroll
+          for (int rr = 0; rr < 2; ++rr) {
+            const int c = cc + 8 * k + c2, x = 4 * k + 2 * rr;
+            const uint32_t off = sw128_pair(rw[rr], c);
+            const float2 d = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(sm.bdO[cx.half] + off));
+            qs[rr] += d.x * v[x] + d.y * v[x + 1];
+            *reinterpret_cast<uint32_t*>(sm.bW[cx.half] + off) = pack_bf16x2(-w[x], -w[x + 1]);
           }
-        }
       }
-      if (has_row) sm.part[5 + cx.half][i_row] = qs * sm.Gm[i_row] * p.scale;
+      qs[0] = quad_sum(qs[0]);
+      qs[1] = quad_sum(qs[1]);
+      if ((cx.lane & 3) == 0) {
+        sm.part[5 + cx.half][rw[0]] = qs[0] * sm.Gm[rw[0]] * p.scale;
+        sm.part[5 + cx.half][rw[1]] = qs[1] * sm.Gm[rw[1]] * p.scale;
+      }
     }
     // ---------------- (c) V'_s = diag(e^{gamma_C - gamma}) V' ; dk accumulation (dq has its own kernel)
     if (tid < 64) sm.cA[tid] = __expf(gC - sm.gam[tid]);
@@ -1158,16 +1168,16 @@ __global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ Bw
     col_sums(sm, vyM, kxM, sm.vy, sm.kx, tid);
     if (tid == 0 && next) load_dvp(hh + 1);  // the kx scratch is summed: the next head's dV'
     if (!(ok = cx.commit_wait())) break;
-    for (int cc = 0; cc < 32; cc += 16) {
+    {
+      const int c2 = 2 * (cx.lane & 3), r0 = 16 * cx.q4 + (cx.lane >> 2);
       float v[16];
-      tmem_ld16(tm + kGt1 + cx.lane_base() + 32 * cx.half + cc, v);
+      tmem_ld16x256_x4(tm + kGt1 + cx.lane_base() + 32 * cx.half, v);
       tmem_ld_wait();
-      if (has_row) {
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int cj = ((32 * cx.half + cc) >> 3) + u;
-          *reinterpret_cast<uint4*>(Rt + i_row * 128 + ((cj ^ (i_row & 7)) << 4)) = pack8(v + 8 * u);
-        }
+      for (int k = 0; k < 4; ++k) {
+        const int j = 32 * cx.half + 8 * k + c2;
+        *reinterpret_cast<uint32_t*>(Rt + sw128_pair(r0, j)) = pack_bf16x2(v[4 * k], v[4 * k + 1]);
+        *reinterpret_cast<uint32_t*>(Rt + sw128_pair(r0 + 8, j)) = pack_bf16x2(v[4 * k + 2], v[4 * k + 3]);
       }
     }
     sync_generic_to_async();
@@ -1339,10 +1349,12 @@ __global__ void __launch_bounds__(256, 1) dq_kernel(const __grid_constant__ BwdP
   sync_generic_to_async();
   const uint32_t tm = tmem_holder;
   cx.tmem = tm;
-  const int i_row = 16 * cx.q4 + cx.lane;
-  const bool has_row = cx.lane < 16;
-  float dq[64];
-  for (int c = 0; c < 64; ++c) dq[c] = 0.f;
+  // all 32 lanes of each warp: rows rw[0] = 16 q4 + lane / 4 and rw[1] = rw[0] + 8 of the M = 64
+  // accumulators, column pairs c2 + 8k of each 32-column group (tmem_ld16x256_x4)
+  const int c2 = 2 * (cx.lane & 3);
+  const int rw[2] = {16 * cx.q4 + (cx.lane >> 2), 16 * cx.q4 + (cx.lane >> 2) + 8};
+  float dq[32];  // [32-column group ci][16 values in the tmem_ld16x256_x4 order]
+  for (int c = 0; c < 32; ++c) dq[c] = 0.f;
   bool ok = true;
   for (int hh = 0; hh < G && ok; ++hh) {
     const int h = hk * G + hh;
@@ -1378,36 +1390,36 @@ __global__ void __launch_bounds__(256, 1) dq_kernel(const __grid_constant__ BwdP
     if (!(ok = cx.commit_wait())) break;  // (its barrier also publishes eg / egi)
     // e^{gamma_i - gamma_j} as e^{gamma_i} e^{-gamma_j} while both factors stay finite
     const bool factored = sm.gam[63] > kFactorMin;
-    for (int cc = 0; cc < 32; cc += 16) {
-      float v[16];
-      tmem_ld16(tm + kDtP + cx.lane_base() + 32 * cx.half + cc, v);
-      tmem_ld_wait();
-      if (has_row) {
-        float hi[16], lo[16];
-        const float es = sm.eg[i_row] * p.scale;
-        float ev[16];
-        if (factored) {
+    {
+      // all 32 lanes: rows rw[0], rw[1], column pairs (tmem_ld16x256_x4)
+      float v[16], ev[16];
+      tmem_ld16x256_x4(tm + kDtP + cx.lane_base() + 32 * cx.half, v);
+      if (factored) {
 #pragma unroll
-          for (int x = 0; x < 16; ++x) ev[x] = es * sm.egi[32 * cx.half + cc + x];
-        } else {
+        for (int k = 0; k < 4; ++k)
 #pragma unroll
-          for (int x = 0; x < 16; ++x) ev[x] = __expf(sm.gam[i_row] - sm.gam[32 * cx.half + cc + x]) * p.scale;
-        }
+          for (int q = 0; q < 4; ++q)
+            ev[4 * k + q] = sm.eg[rw[q >> 1]] * p.scale * sm.egi[32 * cx.half + 8 * k + c2 + (q & 1)];
+      } else {
 #pragma unroll
-        for (int x = 0; x < 16; ++x) {
-          const int j = 32 * cx.half + cc + x;
-          const float d = (j <= i_row && i_row < n) ? v[x] * ev[x] : 0.f;
-          hi[x] = __bfloat162float(__float2bfloat16_rn(d));
-          lo[x] = d - hi[x];
-        }
+        for (int k = 0; k < 4; ++k)
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int cj = ((32 * cx.half + cc) >> 3) + u;
-          const uint32_t off = i_row * 128 + ((cj ^ (i_row & 7)) << 4);
-          *reinterpret_cast<uint4*>(sm.qh + off) = pack8(hi + 8 * u);
-          *reinterpret_cast<uint4*>(sm.ql + off) = pack8(lo + 8 * u);
-        }
+          for (int q = 0; q < 4; ++q)
+            ev[4 * k + q] = __expf(sm.gam[rw[q >> 1]] - sm.gam[32 * cx.half + 8 * k + c2 + (q & 1)]) * p.scale;
       }
+      tmem_ld_wait();
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+#pragma unroll
+        for (int rr = 0; rr < 2; ++rr) {
+          const int r = rw[rr], j = 32 * cx.half + 8 * k + c2, x = 4 * k + 2 * rr;
+          const float d0 = (j <= r && r < n) ? v[x] * ev[x] : 0.f;
+          const float d1 = (j + 1 <= r && r < n) ? v[x + 1] * ev[x + 1] : 0.f;
+          const float h0 = __bfloat162float(__float2bfloat16_rn(d0)), h1 = __bfloat162float(__float2bfloat16_rn(d1));
+          const uint32_t off = sw128_pair(r, j);
+          *reinterpret_cast<uint32_t*>(sm.qh + off) = pack_bf16x2(h0, h1);
+          *reinterpret_cast<uint32_t*>(sm.ql + off) = pack_bf16x2(d0 - h0, d1 - h1);
+        }
     }
     sync_generic_to_async();
     // dO S^T (hi + lo) and dQK K (hi + lo)
@@ -1427,13 +1439,15 @@ __global__ void __launch_bounds__(256, 1) dq_kernel(const __grid_constant__ BwdP
     }
     if (!(ok = cx.commit_wait())) break;
     {
-      const float sc = has_row ? __expf(sm.gam[i_row]) * p.scale : 0.f;
-      for (int cc = 0; cc < 64; cc += 16) {
+      const float sc0 = sm.eg[rw[0]] * p.scale, sc1 = sm.eg[rw[1]] * p.scale;
+#pragma unroll
+      for (int ci = 0; ci < 2; ++ci) {
         float a[16], b[16];
-        tmem_ld16(tm + kDt1 + cx.lane_base() + 64 * cx.half + cc, a);
-        tmem_ld16(tm + kDt2 + cx.lane_base() + 64 * cx.half + cc, b);
+        tmem_ld16x256_x4(tm + kDt1 + cx.lane_base() + 64 * cx.half + 32 * ci, a);
+        tmem_ld16x256_x4(tm + kDt2 + cx.lane_base() + 64 * cx.half + 32 * ci, b);
         tmem_ld_wait();
-        for (int x = 0; x < 16; ++x) dq[cc + x] += sc * a[x] + b[x];
+#pragma unroll
+        for (int x = 0; x < 16; ++x) dq[16 * ci + x] += ((x & 2) ? sc1 : sc0) * a[x] + b[x];
       }
     }
     tc_fence_before();
@@ -1441,10 +1455,17 @@ __global__ void __launch_bounds__(256, 1) dq_kernel(const __grid_constant__ BwdP
     tc_fence_after();
   }
   if (ok) {
-    if (has_row && i_row < n) {
-      float* row = p.dq + ((size_t)(tok0 + i_row) * Hk + hk) * kDim + 64 * cx.half;
-      for (int c = 0; c < 64; c += 4) *reinterpret_cast<float4*>(row + c) = make_float4(dq[c], dq[c + 1], dq[c + 2], dq[c + 3]);
-    }
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr)
+      if (rw[rr] < n) {
+        float* row = p.dq + ((size_t)(tok0 + rw[rr]) * Hk + hk) * kDim + 64 * cx.half + c2;
+#pragma unroll
+        for (int ci = 0; ci < 2; ++ci)
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            *reinterpret_cast<float2*>(row + 32 * ci + 8 * k) =
+                make_float2(dq[16 * ci + 4 * k + 2 * rr], dq[16 * ci + 4 * k + 2 * rr + 1]);
+      }
   } else if (tid == 0) {
     set_status(hd, kErrTimeout);
   }
