@@ -327,20 +327,19 @@ __device__ bool run_rev_ws(const BwdParams& p, Ctx& cx, RevSmem& sm, RevBars& bb
   // -W of chunk j
   auto staging2 = [&]() {
     rrole_wait(&bb.pre_done, ph.pre_done, abort);
+    // all 32 lanes: rows r0 = 16 q4 + lane / 4 and r0 + 8 of W (M = 64), column pairs
+    const int c2 = 2 * (cx.lane & 3), r0 = 16 * cx.q4 + (cx.lane >> 2);
 #pragma unroll
     for (int hc = 0; hc < 2; ++hc) {
-      float v[32];
-      tmem_ld16(tm + kRtW + lane_base + 64 * cx.half + 32 * hc, v);
-      tmem_ld16(tm + kRtW + lane_base + 64 * cx.half + 32 * hc + 16, v + 16);
+      float v[16];
+      tmem_ld16x256_x4(tm + kRtW + lane_base + 64 * cx.half + 32 * hc, v);
       tmem_ld_wait();
-      if (cx.lane < 16) {
 #pragma unroll
-        for (int x = 0; x < 32; ++x) v[x] = -v[x];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int cj = 4 * hc + u;
-          *reinterpret_cast<uint4*>(sm.wn + cx.half * 8192 + i * 128 + ((cj ^ (i & 7)) << 4)) = pack8(v + 8 * u);
-        }
+      for (int k = 0; k < 4; ++k) {
+        const int c = 32 * hc + 8 * k + c2;
+        *reinterpret_cast<uint32_t*>(sm.wn + cx.half * 8192 + sw128_pair(r0, c)) = pack_bf16x2(-v[4 * k], -v[4 * k + 1]);
+        *reinterpret_cast<uint32_t*>(sm.wn + cx.half * 8192 + sw128_pair(r0 + 8, c)) =
+            pack_bf16x2(-v[4 * k + 2], -v[4 * k + 3]);
       }
     }
     r_handoff(cx.tid, &bb.staged2);
@@ -367,22 +366,21 @@ __device__ bool run_rev_ws(const BwdParams& p, Ctx& cx, RevSmem& sm, RevBars& bb
     __syncwarp();
     r_sync();
     {
-      const int t = i;
+      // all 32 lanes: rows t0 = 16 q4 + lane / 4 and t0 + 8 of dV' (M = 64), column pairs
+      const int c2 = 2 * (cx.lane & 3), t0 = 16 * cx.q4 + (cx.lane >> 2);
+      const float m0 = t0 < nn ? 1.f : 0.f, m1 = t0 + 8 < nn ? 1.f : 0.f;
 #pragma unroll
       for (int hc = 0; hc < 2; ++hc) {
-        float v[32];
-        tmem_ld16(tm + kRtA + lane_base + 64 * cx.half + 32 * hc, v);
-        tmem_ld16(tm + kRtA + lane_base + 64 * cx.half + 32 * hc + 16, v + 16);
+        float v[16];
+        tmem_ld16x256_x4(tm + kRtA + lane_base + 64 * cx.half + 32 * hc, v);
         tmem_ld_wait();
-        if (cx.lane < 16) {
-          if (t >= nn)
 #pragma unroll
-            for (int x = 0; x < 32; ++x) v[x] = 0.f;
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int cj = 4 * hc + u;
-            *reinterpret_cast<uint4*>(sm.dvp + cx.half * 8192 + t * 128 + ((cj ^ (t & 7)) << 4)) = pack8(v + 8 * u);
-          }
+        for (int k = 0; k < 4; ++k) {
+          const int c = 32 * hc + 8 * k + c2;
+          *reinterpret_cast<uint32_t*>(sm.dvp + cx.half * 8192 + sw128_pair(t0, c)) =
+              pack_bf16x2(v[4 * k] * m0, v[4 * k + 1] * m0);
+          *reinterpret_cast<uint32_t*>(sm.dvp + cx.half * 8192 + sw128_pair(t0 + 8, c)) =
+              pack_bf16x2(v[4 * k + 2] * m1, v[4 * k + 3] * m1);
         }
       }
     }

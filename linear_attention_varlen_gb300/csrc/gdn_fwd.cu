@@ -1098,21 +1098,21 @@ __device__ bool run_ws(const FwdParams& p, ChainCtx& cx, WsBars& bb, WsPhase& ph
       }
     }
     role_wait(&bb.pre_done, ph.pre_done, abort);
+    {
+      // all 32 lanes: rows r0 = 16 q4 + lane / 4 and r0 + 8 of W (M = 64) go to rows 64 + r of the
+      // stacked operand, column pairs
+      const int c2 = 2 * (cx.lane & 3), r0 = 64 + 16 * cx.q4 + (cx.lane >> 2);
 #pragma unroll
-    for (int hc = 0; hc < 2; ++hc) {
-      float v[32];
-      tmem_ld16(cx.tmem + kTmW + lane_base + 64 * cx.half + 32 * hc, v);
-      tmem_ld16(cx.tmem + kTmW + lane_base + 64 * cx.half + 32 * hc + 16, v + 16);
-      tmem_ld_wait();
-      if (cx.lane < 16) {
-        const int r = 64 + i;
+      for (int hc = 0; hc < 2; ++hc) {
+        float v[16];
+        tmem_ld16x256_x4(cx.tmem + kTmW + lane_base + 64 * cx.half + 32 * hc, v);
+        tmem_ld_wait();
 #pragma unroll
-        for (int cj4 = 0; cj4 < 4; ++cj4) {
-          const int cj = 4 * hc + cj4;
-          const float* x = v + 8 * cj4;
-          *reinterpret_cast<uint4*>(sm.qw[cx.half] + r * 128 + ((cj ^ (r & 7)) << 4)) =
-              make_uint4(pack_bf16x2(-x[0], -x[1]), pack_bf16x2(-x[2], -x[3]), pack_bf16x2(-x[4], -x[5]),
-                         pack_bf16x2(-x[6], -x[7]));
+        for (int k = 0; k < 4; ++k) {
+          const int c = 32 * hc + 8 * k + c2;
+          *reinterpret_cast<uint32_t*>(sm.qw[cx.half] + sw128_pair(r0, c)) = pack_bf16x2(-v[4 * k], -v[4 * k + 1]);
+          *reinterpret_cast<uint32_t*>(sm.qw[cx.half] + sw128_pair(r0 + 8, c)) =
+              pack_bf16x2(-v[4 * k + 2], -v[4 * k + 3]);
         }
       }
     }
