@@ -297,7 +297,6 @@ __device__ bool run_rev_ws(const BwdParams& p, Ctx& cx, RevSmem& sm, RevBars& bb
   }
   // -------------------------------------------------------------------- epilogue warps 0-7
   const uint32_t lane_base = (uint32_t)(32 * cx.q4) << 16;
-  const int i = 16 * cx.q4 + cx.lane;  // row of M = 64 accumulators (lanes < 16)
   // Q~, K~ of chunk j (from the stage)
   auto staging1 = [&](int j) {
     const int gc = chunk_of(j), st = j & 1, nn = clen[gc];

@@ -449,37 +449,13 @@ __global__ void __launch_bounds__(256) kkt_solve_kernel(const __grid_constant__ 
 
 enum ChainMode { kModeOut = 0, kModeP1 = 1 };
 
-// Shared memory of the chain kernel (after 1024-byte alignment). Every operand block is a
-// 128B-swizzled image (rows of 64 bf16); see bw_prims.cuh for the descriptor conventions.
-struct ChainSmem {
-  uint8_t q[2][8192];     // Q rows t, dk blocks                      (A, K-major: P = Q K^T)
-  uint8_t k[2][8192];     // K rows t, dk blocks                      (B K-major / B MN-major / A MN-major)
-  uint8_t v[2][8192];     // V rows t, dv blocks                      (B, MN-major: U)
-  uint8_t p[8192];        // P = (Q K^T) o E, rows t                  ([P; 0] A operand)
-  uint8_t z[8192];        // zeros                                    ([0; T_u] A operand)
-  uint8_t tu[8192];       // T diag(beta)
-  uint8_t tw[8192];       // T diag(beta e^gamma)                     (A, M=64: W = T_w K)
-  uint8_t qw[2][16384];   // dk block b: rows 0-63 Q~ = diag(e^gamma) Q, rows 64-127 -W   (A, M=128)
-  uint8_t vo[2][8192];    // V' rows t, dv blocks                     (B, MN-major: P V')
-  uint8_t vs[2][8192];    // diag(e^{gamma_C - gamma}) V'             (B, MN-major: K^T V's)
-  uint8_t s[2][16384];    // S in bf16: rows dk, dv blocks            (B, MN-major: [Q~; -W] S)
-  // record mode only (compensated bf16: x = hi + lo)
-  uint8_t z2[8192];       // zeros                                    ([0; T_u lo] A operand)
-  uint8_t tu_lo[8192];    // low part of T diag(beta)
-  uint8_t tw_lo[8192];    // low part of T diag(beta e^gamma)
-  uint8_t vs_lo[2][8192]; // low part of diag(e^{gamma_C - gamma}) V'
-  float gam[64];
-};
-
-// TMEM columns.
+// TMEM columns of the forward chain.
 constexpr uint32_t kTmD1 = 0;    // [Q~ S + P V' ; U - W S]   (M = 128, 128 cols)
 constexpr uint32_t kTmD2 = 128;  // K^T V's                   (M = 128, 128 cols)
 constexpr uint32_t kTmW = 256;   // W                         (M = 64, 128 cols)
-constexpr uint32_t kTmG = 384;   // Q K^T                     (M = 64, 64 cols)
 
 struct ChainCtx {
-  ChainSmem* sm;   // record-mode layout
-  uint8_t* base;   // 1024-aligned dynamic shared memory (both layouts start here)
+  uint8_t* base;   // 1024-aligned dynamic shared memory (every layout starts here)
   uint64_t* bar_ld;
   uint64_t* bar_mma;
   uint32_t tmem;
@@ -499,273 +475,12 @@ __device__ __forceinline__ void store_state_bf16_to(SM& sm, const ChainCtx& cx, 
     *reinterpret_cast<uint4*>(blk + r * 128 + ((cj ^ (r & 7)) << 4)) = w;
   }
 }
-__device__ __forceinline__ void store_state_bf16(ChainCtx& cx, const float* S) { store_state_bf16_to(*cx.sm, cx, S); }
 
-template <bool kOut, bool kWithU, bool kStore = false, bool kComp = kStore>
-__device__ bool chain_chunk(const FwdParams& p, ChainCtx& cx, float* S, int gc, int h, int hk, int tok0, int n) {
-  ChainSmem& sm = *cx.sm;
-  const int Hv = p.d.Hv;
-  if (cx.tid == 0) {
-    uint32_t bytes = 2 * 8192 /*K*/ + 8192 /*Tw*/ + 256;
-    if (kOut) bytes += 2 * 8192;
-    if (kWithU) bytes += 2 * 8192 + 8192;
-    if (kComp) bytes += kWithU ? 2 * 8192 : 8192;
-    mbar_arrive_expect_tx(cx.bar_ld, bytes);
-    tma_load_3d(sm.k[0], &p.tm_k, 0, hk, tok0, cx.bar_ld);
-    tma_load_3d(sm.k[1], &p.tm_k, 64, hk, tok0, cx.bar_ld);
-    if (kOut) {
-      tma_load_3d(sm.q[0], &p.tm_q, 0, hk, tok0, cx.bar_ld);
-      tma_load_3d(sm.q[1], &p.tm_q, 64, hk, tok0, cx.bar_ld);
-    }
-    if (kWithU) {
-      tma_load_3d(sm.v[0], &p.tm_v, 0, h, tok0, cx.bar_ld);
-      tma_load_3d(sm.v[1], &p.tm_v, 64, h, tok0, cx.bar_ld);
-      bulk_load(sm.tu, p.ws + p.L.tu + ((size_t)gc * Hv + h) * 8192, 8192, cx.bar_ld);
-    }
-    bulk_load(sm.tw, p.ws + p.L.tw + ((size_t)gc * Hv + h) * 8192, 8192, cx.bar_ld);
-    bulk_load(sm.gam, p.ws + p.L.gam + ((size_t)gc * Hv + h) * 256, 256, cx.bar_ld);
-    if (kComp) {
-      bulk_load(sm.tw_lo, p.tw_lo + ((size_t)gc * Hv + h) * 8192, 8192, cx.bar_ld);
-      if (kWithU) bulk_load(sm.tu_lo, p.tu_lo + ((size_t)gc * Hv + h) * 8192, 8192, cx.bar_ld);
-    }
-  }
-  if (!wait_all(cx.bar_ld, cx.ph_ld)) return false;
-  cx.ph_ld ^= 1;
-  tc_fence_after();
-  if (kStore) copy_smem_to_global(p.st_img + ((size_t)gc * Hv + h) * 32768, sm.s[0], 32768, cx.tid);
-  if (kComp) {
-    // low part S - bf16(S), same image layout as sm.s. In this mode Q and V'-out are idle when
-    // W S is formed: they hold the two dv blocks of S lo.
-    const int r = 32 * cx.q4 + cx.lane;
-    uint8_t* dst = kStore ? p.st_lo_img + ((size_t)gc * Hv + h) * 32768 + cx.half * 16384 : nullptr;
-    uint8_t* slo = cx.half == 0 ? sm.q[0] : sm.vo[0];
-#pragma unroll
-    for (int cj = 0; cj < 8; ++cj) {
-      float lo[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) lo[u] = S[8 * cj + u] - __bfloat162float(__float2bfloat16_rn(S[8 * cj + u]));
-      const uint4 w = make_uint4(pack_bf16x2(lo[0], lo[1]), pack_bf16x2(lo[2], lo[3]), pack_bf16x2(lo[4], lo[5]),
-                                 pack_bf16x2(lo[6], lo[7]));
-      if (kStore) *reinterpret_cast<uint4*>(dst + r * 128 + ((cj ^ (r & 7)) << 4)) = w;
-      *reinterpret_cast<uint4*>(slo + r * 128 + ((cj ^ (r & 7)) << 4)) = w;
-    }
-  }
-
-  // -- MMA group 1: W = T_w K (M=64), P-raw = Q K^T (M=64)
-  if (cx.tid == 0) {
-    const uint32_t k0 = smem_u32(sm.k[0]);
-    for (int ks = 0; ks < 4; ++ks)
-      umma_bf16(cx.tmem + kTmW, kmajor_desc(smem_u32(sm.tw), 8192, ks), mnmajor_desc(k0, 8192, ks),
-                idesc_bf16(64, 128, 0, 1), ks > 0);
-    if (kComp)
-      for (int ks = 0; ks < 4; ++ks)
-        umma_bf16(cx.tmem + kTmW, kmajor_desc(smem_u32(sm.tw_lo), 8192, ks), mnmajor_desc(k0, 8192, ks),
-                  idesc_bf16(64, 128, 0, 1), 1);
-    if (kOut)
-      for (int ks = 0; ks < 8; ++ks)
-        umma_bf16(cx.tmem + kTmG, kmajor_desc(smem_u32(sm.q[0]), 8192, ks), kmajor_desc(k0, 8192, ks),
-                  idesc_bf16(64, 64, 0, 0), ks > 0);
-    umma_commit(cx.bar_mma);
-  }
-  const float gC = sm.gam[63];
-  if (kOut) {
-    // Q~ = diag(e^gamma) Q into rows 0-63 of sm.qw
-    for (int e = cx.tid; e < 2 * 64 * 8; e += 256) {
-      const int b = e >> 9, r = (e >> 3) & 63, cj = e & 7;
-      const uint32_t off = r * 128 + ((cj ^ (r & 7)) << 4);
-      uint4 raw = *reinterpret_cast<const uint4*>(sm.q[b] + off);
-      const float sc = __expf(sm.gam[r]) * p.scale;
-      __nv_bfloat162* x = reinterpret_cast<__nv_bfloat162*>(&raw);
-      uint32_t w[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        float2 f = __bfloat1622float2(x[u]);
-        w[u] = pack_bf16x2(f.x * sc, f.y * sc);
-      }
-      *reinterpret_cast<uint4*>(sm.qw[b] + off) = make_uint4(w[0], w[1], w[2], w[3]);
-    }
-  }
-  if (!wait_all(cx.bar_mma, cx.ph_mma)) return false;
-  cx.ph_mma ^= 1;
-  tc_fence_after();
-  {
-    const uint32_t lane_base = (uint32_t)(32 * cx.q4) << 16;
-    const int i = 16 * cx.q4 + cx.lane;  // row for lanes < 16 (M = 64 layout)
-    // -W into rows 64-127 of sm.qw (dk block = half)
-    for (int cc = 0; cc < 64; cc += 16) {
-      float v[16];
-      tmem_ld16(cx.tmem + kTmW + lane_base + 64 * cx.half + cc, v);
-      tmem_ld_wait();
-      if (cx.lane < 16) {
-        const int r = 64 + i;
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int cj = (cc >> 3) + u;
-          uint4 w = make_uint4(pack_bf16x2(-v[8 * u + 0], -v[8 * u + 1]), pack_bf16x2(-v[8 * u + 2], -v[8 * u + 3]),
-                               pack_bf16x2(-v[8 * u + 4], -v[8 * u + 5]), pack_bf16x2(-v[8 * u + 6], -v[8 * u + 7]));
-          *reinterpret_cast<uint4*>(sm.qw[cx.half] + r * 128 + ((cj ^ (r & 7)) << 4)) = w;
-          if (kComp) {
-            // -W lo in rows 0-63 (the Q~ rows, idle in this mode)
-            const __nv_bfloat162* hb = reinterpret_cast<const __nv_bfloat162*>(&w);
-            float lo[8];
-#pragma unroll
-            for (int x = 0; x < 4; ++x) {
-              const float2 hf = __bfloat1622float2(hb[x]);
-              lo[2 * x] = -v[8 * u + 2 * x] - hf.x;
-              lo[2 * x + 1] = -v[8 * u + 2 * x + 1] - hf.y;
-            }
-            *reinterpret_cast<uint4*>(sm.qw[cx.half] + i * 128 + ((cj ^ (i & 7)) << 4)) =
-                make_uint4(pack_bf16x2(lo[0], lo[1]), pack_bf16x2(lo[2], lo[3]), pack_bf16x2(lo[4], lo[5]),
-                           pack_bf16x2(lo[6], lo[7]));
-          }
-        }
-      }
-    }
-    if (kOut) {
-      // P = (Q K^T) o E, masked causal and to the chunk's valid tokens (32 columns per half)
-      for (int cc = 0; cc < 32; cc += 16) {
-        float v[16];
-        tmem_ld16(cx.tmem + kTmG + lane_base + 32 * cx.half + cc, v);
-        tmem_ld_wait();
-        if (cx.lane < 16) {
-          const float gi = sm.gam[i];
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            float pv[8];
-#pragma unroll
-            for (int x = 0; x < 8; ++x) {
-              const int j = 32 * cx.half + cc + 8 * u + x;
-              pv[x] = (j <= i && i < n) ? __expf(gi - sm.gam[j]) * p.scale * v[8 * u + x] : 0.f;
-            }
-            const int cj = ((32 * cx.half + cc) >> 3) + u;
-            uint4 w = make_uint4(pack_bf16x2(pv[0], pv[1]), pack_bf16x2(pv[2], pv[3]), pack_bf16x2(pv[4], pv[5]),
-                                 pack_bf16x2(pv[6], pv[7]));
-            *reinterpret_cast<uint4*>(sm.p + i * 128 + ((cj ^ (i & 7)) << 4)) = w;
-          }
-        }
-      }
-    }
-  }
-  sync_generic_to_async();
-
-  // -- MMA group 2: D1 = [0; T_u] V + [Q~; -W] S
-  if (cx.tid == 0) {
-    if (kWithU)
-      for (int ks = 0; ks < 4; ++ks)
-        umma_bf16(cx.tmem + kTmD1, kmajor_desc(smem_u32(sm.z), 16384, ks), mnmajor_desc(smem_u32(sm.v[0]), 8192, ks),
-                  idesc_bf16(128, 128, 0, 1), ks > 0);
-    if (kComp && kWithU)
-      for (int ks = 0; ks < 4; ++ks)
-        umma_bf16(cx.tmem + kTmD1, kmajor_desc(smem_u32(sm.z2), 16384, ks), mnmajor_desc(smem_u32(sm.v[0]), 8192, ks),
-                  idesc_bf16(128, 128, 0, 1), 1);
-    for (int ks = 0; ks < 8; ++ks)
-      umma_bf16(cx.tmem + kTmD1, kmajor_desc(smem_u32(sm.qw[0]), 16384, ks),
-                mnmajor_desc(smem_u32(sm.s[0]), 16384, ks), idesc_bf16(128, 128, 0, 1), (kWithU || ks > 0) ? 1 : 0);
-    if (kComp) {
-      // compensated W S: + (-W hi) S lo + (-W lo) S hi. The second A operand starts 8 KB before
-      // sm.qw so that its rows 64-127 are the -W lo rows; its rows 0-63 feed unused accumulator rows.
-      const uint32_t slo_lbo = smem_u32(sm.vo[0]) - smem_u32(sm.q[0]);
-      for (int ks = 0; ks < 8; ++ks)
-        umma_bf16(cx.tmem + kTmD1, kmajor_desc(smem_u32(sm.qw[0]), 16384, ks),
-                  mnmajor_desc(smem_u32(sm.q[0]), slo_lbo, ks), idesc_bf16(128, 128, 0, 1), 1);
-      for (int ks = 0; ks < 8; ++ks)
-        umma_bf16(cx.tmem + kTmD1, kmajor_desc(smem_u32(sm.qw[0]) - 8192, 16384, ks),
-                  mnmajor_desc(smem_u32(sm.s[0]), 16384, ks), idesc_bf16(128, 128, 0, 1), 1);
-    }
-    umma_commit(cx.bar_mma);
-  }
-  if (!wait_all(cx.bar_mma, cx.ph_mma)) return false;
-  cx.ph_mma ^= 1;
-  tc_fence_after();
-  // V' = rows 64-127 of D1 (lanes 64-127: quarters 2 and 3)
-  if (cx.q4 >= 2) {
-    const int t = 32 * (cx.q4 - 2) + cx.lane;
-    const float sc = __expf(gC - sm.gam[t]);
-    const uint32_t lane_base = (uint32_t)(32 * cx.q4) << 16;
-    for (int cc = 0; cc < 64; cc += 16) {
-      float v[16];
-      tmem_ld16(cx.tmem + kTmD1 + lane_base + 64 * cx.half + cc, v);
-      tmem_ld_wait();
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int cj = (cc >> 3) + u;
-        const uint32_t off = t * 128 + ((cj ^ (t & 7)) << 4);
-        const float* x = v + 8 * u;
-        *reinterpret_cast<uint4*>(sm.vo[cx.half] + off) =
-            make_uint4(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]), pack_bf16x2(x[4], x[5]), pack_bf16x2(x[6], x[7]));
-        *reinterpret_cast<uint4*>(sm.vs[cx.half] + off) =
-            make_uint4(pack_bf16x2(x[0] * sc, x[1] * sc), pack_bf16x2(x[2] * sc, x[3] * sc),
-                       pack_bf16x2(x[4] * sc, x[5] * sc), pack_bf16x2(x[6] * sc, x[7] * sc));
-        if (kComp) {
-          float lo[8], los[8];
-#pragma unroll
-          for (int u2 = 0; u2 < 8; ++u2) {
-            const float xs = x[u2] * sc;
-            lo[u2] = x[u2] - __bfloat162float(__float2bfloat16_rn(x[u2]));
-            los[u2] = xs - __bfloat162float(__float2bfloat16_rn(xs));
-          }
-          *reinterpret_cast<uint4*>(sm.vs_lo[cx.half] + off) =
-              make_uint4(pack_bf16x2(los[0], los[1]), pack_bf16x2(los[2], los[3]), pack_bf16x2(los[4], los[5]),
-                         pack_bf16x2(los[6], los[7]));
-          if (kStore)
-            *reinterpret_cast<uint4*>(p.vp_lo_img + ((size_t)gc * Hv + h) * 16384 + cx.half * 8192 + off) =
-                make_uint4(pack_bf16x2(lo[0], lo[1]), pack_bf16x2(lo[2], lo[3]), pack_bf16x2(lo[4], lo[5]),
-                           pack_bf16x2(lo[6], lo[7]));
-        }
-      }
-    }
-  }
-  sync_generic_to_async();
-  if (kStore) copy_smem_to_global(p.vp_img + ((size_t)gc * Hv + h) * 16384, sm.vo[0], 16384, cx.tid);
-
-  // -- MMA group 3: D2 = K^T V's ; D1 += [P; 0] V'
-  if (cx.tid == 0) {
-    for (int ks = 0; ks < 4; ++ks)
-      umma_bf16(cx.tmem + kTmD2, mnmajor_desc(smem_u32(sm.k[0]), 8192, ks), mnmajor_desc(smem_u32(sm.vs[0]), 8192, ks),
-                idesc_bf16(128, 128, 1, 1), ks > 0);
-    if (kComp)
-      for (int ks = 0; ks < 4; ++ks)
-        umma_bf16(cx.tmem + kTmD2, mnmajor_desc(smem_u32(sm.k[0]), 8192, ks),
-                  mnmajor_desc(smem_u32(sm.vs_lo[0]), 8192, ks), idesc_bf16(128, 128, 1, 1), 1);
-    if (kOut)
-      for (int ks = 0; ks < 4; ++ks)
-        umma_bf16(cx.tmem + kTmD1, kmajor_desc(smem_u32(sm.p), 16384, ks), mnmajor_desc(smem_u32(sm.vo[0]), 8192, ks),
-                  idesc_bf16(128, 128, 0, 1), 1);
-    umma_commit(cx.bar_mma);
-  }
-  if (!wait_all(cx.bar_mma, cx.ph_mma)) return false;
-  cx.ph_mma ^= 1;
-  tc_fence_after();
-  {
-    const uint32_t lane_base = (uint32_t)(32 * cx.q4) << 16;
-    const float GC = __expf(gC);
-    for (int cc = 0; cc < 64; cc += 16) {
-      float v[16];
-      tmem_ld16(cx.tmem + kTmD2 + lane_base + 64 * cx.half + cc, v);
-      tmem_ld_wait();
-#pragma unroll
-      for (int x = 0; x < 16; ++x) S[cc + x] = GC * S[cc + x] + v[x];
-    }
-    store_state_bf16(cx, S);
-    if (kOut && cx.q4 < 2) {
-      const int t = 32 * cx.q4 + cx.lane;
-      __nv_bfloat16* orow = p.out + ((size_t)(tok0 + t) * Hv + h) * kDim + 64 * cx.half;
-      for (int cc = 0; cc < 64; cc += 16) {
-        float v[16];
-        tmem_ld16(cx.tmem + kTmD1 + lane_base + 64 * cx.half + cc, v);
-        tmem_ld_wait();
-        if (t < n) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + cc);
-          dst[0] = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
-                              pack_bf16x2(v[6], v[7]));
-          dst[1] = make_uint4(pack_bf16x2(v[8], v[9]), pack_bf16x2(v[10], v[11]), pack_bf16x2(v[12], v[13]),
-                              pack_bf16x2(v[14], v[15]));
-        }
-      }
-    }
-  }
-  sync_generic_to_async();
-  return true;
+// Compensated bf16 pair: hi = bf16(a, b), lo = bf16 of what the rounding left out.
+__device__ __forceinline__ float bf16_round(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
+__device__ __forceinline__ void split_pair(float a, float b, uint32_t& hi, uint32_t& lo) {
+  hi = pack_bf16x2(a, b);
+  lo = pack_bf16x2(a - bf16_round(a), b - bf16_round(b));
 }
 
 // Load a 128x128 fp32 state (row-major [dk][dv]) into this thread's registers.
@@ -784,15 +499,22 @@ __device__ __forceinline__ void save_state(const ChainCtx& cx, float* dst, const
   for (int c = 0; c < 64; c += 4) *reinterpret_cast<float4*>(row + c) = make_float4(S[c], S[c + 1], S[c + 2], S[c + 3]);
 }
 
-// out = M S_start + B (B may be null) on the tensor cores with compensated bf16 operands (x = hi + lo):
-// M hi S hi + M hi S lo + M lo S hi. At the start of an item every staging buffer except sm.s
-// (S_start hi) is idle: M hi goes to sm.qw, M lo to sm.q / sm.vo, S lo to sm.v / sm.vs.
-// 32 KB idle during affine_apply in each shared-memory layout.
-__device__ __forceinline__ float* affine_stage(ChainSmem& sm) { return reinterpret_cast<float*>(sm.tu_lo); }
+// Shared-memory buffers that affine_apply borrows; at the start of an item every staging buffer
+// of the chain except S hi is idle.
+struct AffineBufs {
+  uint8_t* mhi;         // M hi: two dk blocks of 128 rows, 16 KB apart (A K-major, M = 128)
+  uint8_t* mlo;         // M lo, dk block 0 (block 1 at mlo + mlo_stride)
+  uint32_t mlo_stride;
+  uint8_t* slo;         // S_start lo, dv block 0 (block 1 at slo + slo_stride) (B MN-major)
+  uint32_t slo_stride;
+  uint8_t* shi;         // S_start hi as staged by the chain: two dv blocks, 16 KB apart
+  float* stage;         // 32 KB of fp32 staging for the product
+};
 
-template <class SM>
-__device__ bool affine_apply(const FwdParams& p, ChainCtx& cx, SM& sm, const float* Mm, const float* Bm,
-                             const float* S, float* out) {
+// out = M S_start + B (B may be null) on the tensor cores with compensated bf16 operands (x = hi + lo):
+// M hi S hi + M hi S lo + M lo S hi.
+__device__ bool affine_apply(const FwdParams& p, ChainCtx& cx, const AffineBufs& sm, const float* Mm,
+                             const float* Bm, const float* S, float* out) {
   if (cx.tid < 256) {
     // M hi / lo from coalesced loads (16 threads per 512-byte row), four 32-byte pieces in flight
 #pragma unroll
@@ -814,15 +536,15 @@ __device__ bool affine_apply(const FwdParams& p, ChainCtx& cx, SM& sm, const flo
 #pragma unroll
         for (int u = 0; u < 8; ++u) lo[u] = x[u] - __bfloat162float(__float2bfloat16_rn(x[u]));
         const uint32_t off = r * 128 + ((cj ^ (r & 7)) << 4);
-        *reinterpret_cast<uint4*>(sm.qw[c8 >> 3] + off) = make_uint4(
+        *reinterpret_cast<uint4*>(sm.mhi + (c8 >> 3) * 16384 + off) = make_uint4(
             pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]), pack_bf16x2(x[4], x[5]), pack_bf16x2(x[6], x[7]));
-        *reinterpret_cast<uint4*>(((c8 >> 3) == 0 ? sm.q[0] : sm.vo[0]) + off) = make_uint4(
+        *reinterpret_cast<uint4*>(sm.mlo + (c8 >> 3) * sm.mlo_stride + off) = make_uint4(
             pack_bf16x2(lo[0], lo[1]), pack_bf16x2(lo[2], lo[3]), pack_bf16x2(lo[4], lo[5]), pack_bf16x2(lo[6], lo[7]));
       }
     }
     // S lo (this thread's row of S_start, 64 columns of dv block `half`)
     const int rr = 32 * cx.q4 + cx.lane;  // (threads below 256 only)
-    uint8_t* slo = cx.half == 0 ? sm.v[0] : sm.vs[0];
+    uint8_t* slo = sm.slo + cx.half * sm.slo_stride;
     for (int cj = 0; cj < 8; ++cj) {
       float lo[8];
       for (int u = 0; u < 8; ++u) lo[u] = S[8 * cj + u] - __bfloat162float(__float2bfloat16_rn(S[8 * cj + u]));
@@ -833,17 +555,15 @@ __device__ bool affine_apply(const FwdParams& p, ChainCtx& cx, SM& sm, const flo
   }
   sync_generic_to_async();
   if (cx.tid == 0) {
-    const uint32_t m_lo_stride = smem_u32(sm.vo[0]) - smem_u32(sm.q[0]);
-    const uint32_t s_lo_lbo = smem_u32(sm.vs[0]) - smem_u32(sm.v[0]);
     for (int ks = 0; ks < 8; ++ks)
-      umma_bf16(cx.tmem + kTmD2, kmajor_desc(smem_u32(sm.qw[0]), 16384, ks), mnmajor_desc(smem_u32(sm.s[0]), 16384, ks),
+      umma_bf16(cx.tmem + kTmD2, kmajor_desc(smem_u32(sm.mhi), 16384, ks), mnmajor_desc(smem_u32(sm.shi), 16384, ks),
                 idesc_bf16(128, 128, 0, 1), ks > 0);
     for (int ks = 0; ks < 8; ++ks)
-      umma_bf16(cx.tmem + kTmD2, kmajor_desc(smem_u32(sm.qw[0]), 16384, ks),
-                mnmajor_desc(smem_u32(sm.v[0]), s_lo_lbo, ks), idesc_bf16(128, 128, 0, 1), 1);
+      umma_bf16(cx.tmem + kTmD2, kmajor_desc(smem_u32(sm.mhi), 16384, ks),
+                mnmajor_desc(smem_u32(sm.slo), sm.slo_stride, ks), idesc_bf16(128, 128, 0, 1), 1);
     for (int ks = 0; ks < 8; ++ks)
-      umma_bf16(cx.tmem + kTmD2, kmajor_desc(smem_u32(sm.q[0]), m_lo_stride, ks),
-                mnmajor_desc(smem_u32(sm.s[0]), 16384, ks), idesc_bf16(128, 128, 0, 1), 1);
+      umma_bf16(cx.tmem + kTmD2, kmajor_desc(smem_u32(sm.mlo), sm.mlo_stride, ks),
+                mnmajor_desc(smem_u32(sm.shi), 16384, ks), idesc_bf16(128, 128, 0, 1), 1);
     umma_commit(cx.bar_mma);
   }
   if (!wait_all(cx.bar_mma, cx.ph_mma)) return false;
@@ -852,7 +572,7 @@ __device__ bool affine_apply(const FwdParams& p, ChainCtx& cx, SM& sm, const flo
   // M S_start + B: the product goes through a 32 KB fp32 stage, 64 rows at a time (granule g of
   // local row rl at rl * 128 + 4 (g XOR rl mod 32): conflict-free both for a thread per row and for
   // a warp per row), so that B is read and out written with coalesced accesses.
-  float* stg = affine_stage(sm);
+  float* stg = sm.stage;
   for (int pass = 0; pass < 2; ++pass) {
     if (cx.tid < 256 && (cx.q4 >> 1) == pass) {
       const uint32_t lane_base = (uint32_t)(32 * cx.q4) << 16;
@@ -926,15 +646,17 @@ struct WsSmem {
   uint8_t s[2][16384];   // S bf16 rows dk                      (B MN-major)
   float gam[2][64];      // [stage] chunk-local cumulative gate
 };
-constexpr size_t kSmemBytes = (sizeof(WsSmem) > sizeof(ChainSmem) ? sizeof(WsSmem) : sizeof(ChainSmem)) + 1024;
 constexpr int kWsThreads = 320;
-__device__ __forceinline__ float* affine_stage(WsSmem& sm) { return reinterpret_cast<float*>(sm.k[0]); }
+__device__ __forceinline__ AffineBufs affine_bufs(WsSmem& sm) {
+  return {sm.qw[0], sm.q[0], (uint32_t)(sm.vo[0] - sm.q[0]), sm.v[0], (uint32_t)(sm.vs[0] - sm.v[0]),
+          sm.s[0], reinterpret_cast<float*>(sm.k[0])};
+}
 
 struct WsBars {
-  uint64_t full[2], fullq, empty[2], emptyq, a_done, pre_done, b_done, epi1, staged, epi2, vfree;
+  uint64_t full[2], fullq, fullu, empty[2], emptyq, a_done, pre_done, b_done, epi1, staged, epi2, vfree;
 };
 struct WsPhase {
-  uint32_t full[2], fullq, empty[2], emptyq, a_done, pre_done, b_done, epi1, staged, epi2, vfree;
+  uint32_t full[2], fullq, fullu, empty[2], emptyq, a_done, pre_done, b_done, epi1, staged, epi2, vfree;
 };
 // TMEM columns of D1 for chunk j: two accumulators in turn, so that the output of chunk j is
 // read while chunk j + 1 already runs (columns 384-511 hold Q K^T only in the record path).
@@ -1073,8 +795,7 @@ __device__ bool run_ws(const FwdParams& p, ChainCtx& cx, WsBars& bb, WsPhase& ph
   }
   // -------------------------------------------------------------------- epilogue warps 0-7
   const uint32_t lane_base = (uint32_t)(32 * cx.q4) << 16;
-  const int i = 16 * cx.q4 + cx.lane;  // row of M = 64 accumulators (lanes < 16)
-  e_handoff(cx.tid, &bb.epi2);          // S(gc0) is staged
+  e_handoff(cx.tid, &bb.epi2);  // S(gc0) is staged
   auto staging = [&](int j) {
     const int gc = gc0 + j, st = j & 1;
     const bool out = gc >= gc_out;
@@ -1224,6 +945,260 @@ __device__ bool run_ws(const FwdParams& p, ChainCtx& cx, WsBars& bb, WsPhase& ph
   return !*abort;
 }
 
+// ============================================================== warp-specialized record chain
+//
+// The backward's recompute of the forward chain: the same recurrence with compensated bf16
+// operands (x = hi + lo for T_w, T_u, W, S and V'_s; K and V are exact in bf16), optionally
+// writing the per-chunk records that the gradient kernels read (chunk-start S hi / lo and V'
+// hi / lo as 128B-swizzled images). No output. Roles in one CTA of 10 warps:
+//   warp 8      TMA producer: K and gamma of chunk j into stage j & 1; T_w hi / lo (one buffer,
+//               released by the W product); V and T_u hi / lo (one buffer, released by the U
+//               product).
+//   warp 9      MMA issuer, per chunk j: D_V = T_u V - W S (M = 64; W S as W hi S hi + W hi S lo +
+//               W lo S hi), then chunk j+1's W = T_w K (M = 64), then D2 = K^T (V'_s hi + V'_s lo)
+//               (M = 128).
+//   warps 0-7   epilogue: -W hi / lo staging, V' (records, V'_s hi / lo), S = e^{gamma_C} S + D2
+//               with its hi / lo staging. A chunk-start state reaches its record by bulk store
+//               straight from the staged images.
+struct RecSmem {
+  uint8_t k[2][16384];    // [stage] K rows t, two dk blocks (B MN-major for W, A MN-major for K^T V'_s)
+  uint8_t v[16384];       // V rows t, two dv blocks (B MN-major)
+  uint8_t tu[2][8192];    // T diag(beta) hi, lo (A K-major, M = 64)
+  uint8_t tw[2][8192];    // T diag(beta e^gamma) hi, lo (A K-major, M = 64)
+  uint8_t wn[2][16384];   // -W hi, -W lo: two dk blocks of 64 rows each (A K-major, M = 64)
+  uint8_t s[2][16384];    // S hi rows dk, two dv blocks (B MN-major)
+  uint8_t slo[2][16384];  // S lo
+  uint8_t vs[2][8192];    // V'_s = diag(e^{gamma_C - gamma}) V' hi, two dv blocks (B MN-major)
+  uint8_t vslo[2][8192];  // V'_s lo
+  float gam[2][64];       // [stage] chunk-local cumulative gate
+};
+constexpr size_t kSmemBytes = (sizeof(WsSmem) > sizeof(RecSmem) ? sizeof(WsSmem) : sizeof(RecSmem)) + 1024;
+static_assert(kSmemBytes <= 232448, "chain shared memory");
+__device__ __forceinline__ AffineBufs affine_bufs(RecSmem& sm) {
+  return {sm.wn[0], sm.k[0], 16384u, sm.slo[0], 16384u, sm.s[0], reinterpret_cast<float*>(sm.tu[0])};
+}
+
+// TMEM columns of the record chain.
+constexpr uint32_t kRtW = 0;     // W                          (M = 64, 128 cols)
+constexpr uint32_t kRtV = 128;   // D_V = U - W S              (M = 64, 128 cols)
+constexpr uint32_t kRtD2 = 256;  // K^T V'_s                   (M = 128, 128 cols)
+
+// This thread's 64 state values (row dk = 32 q4 + lane, dv block `half`) as bf16 hi / lo images.
+__device__ __forceinline__ void store_state_comp(RecSmem& sm, const ChainCtx& cx, const float* S) {
+  const int r = 32 * cx.q4 + cx.lane;
+#pragma unroll
+  for (int cj = 0; cj < 8; ++cj) {
+    uint32_t hi[4], lo[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) split_pair(S[8 * cj + 2 * u], S[8 * cj + 2 * u + 1], hi[u], lo[u]);
+    const uint32_t off = r * 128 + ((cj ^ (r & 7)) << 4);
+    *reinterpret_cast<uint4*>(sm.s[cx.half] + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+    *reinterpret_cast<uint4*>(sm.slo[cx.half] + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+  }
+}
+
+// Run chunks [gc0, gc1) of one document for value head h from S (epilogue registers; its hi / lo
+// images are already in sm.s / sm.slo). kWithU = false runs the transition chain (no U term).
+// kStore writes the records of every chunk of the run. All 320 threads call this; returns false
+// after a failed wait.
+template <bool kWithU, bool kStore>
+__device__ bool run_ws_rec(const FwdParams& p, ChainCtx& cx, WsBars& bb, WsPhase& ph, volatile int* abort,
+                           float* S, int gc0, int gc1, int h, int hk) {
+  RecSmem& sm = *reinterpret_cast<RecSmem*>(cx.base);
+  const int n = gc1 - gc0;
+  if (n <= 0) return true;
+  const int Hv = p.d.Hv;
+  const int32_t* ctok = ws_ptr<int32_t>(p, p.L.chunk_tok0);
+  auto rec = [&](int gc) { return (size_t)gc * Hv + h; };
+
+  if (cx.warp == 8) {
+    // ------------------------------------------------------------------ TMA producer
+    if (cx.lane == 0) {
+      for (int j = 0; j < n; ++j) {
+        const int gc = gc0 + j, st = j & 1, tok0 = ctok[gc];
+        if (j >= 2) role_wait(&bb.empty[st], ph.empty[st], abort);
+        if (*abort) break;
+        mbar_arrive_expect_tx(&bb.full[st], 16384 + 256);
+        tma_load_3d(sm.k[st], &p.tm_k, 0, hk, tok0, &bb.full[st]);
+        tma_load_3d(sm.k[st] + 8192, &p.tm_k, 64, hk, tok0, &bb.full[st]);
+        bulk_load(sm.gam[st], p.ws + p.L.gam + rec(gc) * 256, 256, &bb.full[st]);
+        if (j >= 1) role_wait(&bb.emptyq, ph.emptyq, abort);
+        if (*abort) break;
+        mbar_arrive_expect_tx(&bb.fullq, 16384);
+        bulk_load(sm.tw[0], p.ws + p.L.tw + rec(gc) * 8192, 8192, &bb.fullq);
+        bulk_load(sm.tw[1], p.tw_lo + rec(gc) * 8192, 8192, &bb.fullq);
+        if (kWithU) {
+          if (j >= 1) role_wait(&bb.vfree, ph.vfree, abort);
+          if (*abort) break;
+          mbar_arrive_expect_tx(&bb.fullu, 32768);
+          tma_load_3d(sm.v, &p.tm_v, 0, h, tok0, &bb.fullu);
+          tma_load_3d(sm.v + 8192, &p.tm_v, 64, h, tok0, &bb.fullu);
+          bulk_load(sm.tu[0], p.ws + p.L.tu + rec(gc) * 8192, 8192, &bb.fullu);
+          bulk_load(sm.tu[1], p.tu_lo + rec(gc) * 8192, 8192, &bb.fullu);
+        }
+      }
+      // drain: wait for the release of the last uses so that every phase is consumed
+      for (int j = (n >= 2 ? n - 2 : 0); j < n; ++j) role_wait(&bb.empty[j & 1], ph.empty[j & 1], abort);
+      role_wait(&bb.emptyq, ph.emptyq, abort);
+      if (kWithU) role_wait(&bb.vfree, ph.vfree, abort);
+    }
+    return !*abort;
+  }
+  if (cx.warp == 9) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (cx.lane == 0) {
+      const uint32_t tm = cx.tmem;
+      constexpr uint32_t i64 = idesc_bf16(64, 128, 0, 1);
+      auto prep = [&](int j) {
+        const uint32_t k0 = smem_u32(sm.k[j & 1]);
+        for (int ks = 0; ks < 4; ++ks)
+          umma_bf16(tm + kRtW, kmajor_desc(smem_u32(sm.tw[0]), 8192, ks), mnmajor_desc(k0, 8192, ks), i64, ks > 0);
+        for (int ks = 0; ks < 4; ++ks)
+          umma_bf16(tm + kRtW, kmajor_desc(smem_u32(sm.tw[1]), 8192, ks), mnmajor_desc(k0, 8192, ks), i64, 1);
+        umma_commit(&bb.pre_done);
+        umma_commit(&bb.emptyq);
+      };
+      role_wait(&bb.full[0], ph.full[0], abort);
+      role_wait(&bb.fullq, ph.fullq, abort);
+      if (!*abort) prep(0);
+      for (int j = 0; j < n && !*abort; ++j) {
+        const int st = j & 1;
+        role_wait(&bb.staged, ph.staged, abort);
+        role_wait(&bb.epi2, ph.epi2, abort);
+        if (kWithU) role_wait(&bb.fullu, ph.fullu, abort);
+        if (*abort) break;
+        const uint32_t dv = tm + kRtV;
+        if (kWithU) {
+          for (int ks = 0; ks < 4; ++ks)
+            umma_bf16(dv, kmajor_desc(smem_u32(sm.tu[0]), 8192, ks), mnmajor_desc(smem_u32(sm.v), 8192, ks), i64, ks > 0);
+          for (int ks = 0; ks < 4; ++ks)
+            umma_bf16(dv, kmajor_desc(smem_u32(sm.tu[1]), 8192, ks), mnmajor_desc(smem_u32(sm.v), 8192, ks), i64, 1);
+        }
+        for (int ks = 0; ks < 8; ++ks)
+          umma_bf16(dv, kmajor_desc(smem_u32(sm.wn[0]), 8192, ks), mnmajor_desc(smem_u32(sm.s[0]), 16384, ks), i64,
+                    (kWithU || ks > 0) ? 1 : 0);
+        for (int ks = 0; ks < 8; ++ks)
+          umma_bf16(dv, kmajor_desc(smem_u32(sm.wn[0]), 8192, ks), mnmajor_desc(smem_u32(sm.slo[0]), 16384, ks), i64, 1);
+        for (int ks = 0; ks < 8; ++ks)
+          umma_bf16(dv, kmajor_desc(smem_u32(sm.wn[1]), 8192, ks), mnmajor_desc(smem_u32(sm.s[0]), 16384, ks), i64, 1);
+        umma_commit(&bb.a_done);
+        if (kWithU) umma_commit(&bb.vfree);
+        if (j + 1 < n) {
+          role_wait(&bb.full[st ^ 1], ph.full[st ^ 1], abort);
+          role_wait(&bb.fullq, ph.fullq, abort);
+          if (*abort) break;
+          prep(j + 1);
+        }
+        role_wait(&bb.epi1, ph.epi1, abort);
+        if (*abort) break;
+        const uint32_t k0 = smem_u32(sm.k[st]);
+        for (int ks = 0; ks < 4; ++ks)
+          umma_bf16(tm + kRtD2, mnmajor_desc(k0, 8192, ks), mnmajor_desc(smem_u32(sm.vs[0]), 8192, ks),
+                    idesc_bf16(128, 128, 1, 1), ks > 0);
+        for (int ks = 0; ks < 4; ++ks)
+          umma_bf16(tm + kRtD2, mnmajor_desc(k0, 8192, ks), mnmajor_desc(smem_u32(sm.vslo[0]), 8192, ks),
+                    idesc_bf16(128, 128, 1, 1), 1);
+        umma_commit(&bb.b_done);
+        umma_commit(&bb.empty[st]);
+      }
+      role_wait(&bb.epi2, ph.epi2, abort);  // the epilogue's last state hand-off
+    }
+    return !*abort;
+  }
+  // -------------------------------------------------------------------- epilogue warps 0-7
+  const uint32_t lane_base = (uint32_t)(32 * cx.q4) << 16;
+  // M = 64 accumulators, all 32 lanes: rows r0 = 16 q4 + lane / 4 and r0 + 8, column pairs c2 + 8k
+  const int c2 = 2 * (cx.lane & 3), r0 = 16 * cx.q4 + (cx.lane >> 2);
+  auto store_s_record = [&](int gc) {  // thread 0: the staged chunk-start state to its records
+    bulk_store(p.st_img + rec(gc) * 32768, sm.s[0], 32768);
+    bulk_store(p.st_lo_img + rec(gc) * 32768, sm.slo[0], 32768);
+    bulk_commit_group();
+  };
+  e_handoff(cx.tid, &bb.epi2);  // S(gc0) is staged
+  if (kStore && cx.tid == 0) store_s_record(gc0);
+  auto staging = [&](int j) {
+    role_wait(&bb.full[j & 1], ph.full[j & 1], abort);
+    role_wait(&bb.pre_done, ph.pre_done, abort);
+#pragma unroll
+    for (int hc = 0; hc < 2; ++hc) {
+      float v[16];
+      tmem_ld16x256_x4(cx.tmem + kRtW + lane_base + 64 * cx.half + 32 * hc, v);
+      tmem_ld_wait();
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int c = 32 * hc + 8 * k + c2;
+#pragma unroll
+        for (int rr = 0; rr < 2; ++rr) {
+          const uint32_t off = cx.half * 8192 + sw128_pair(r0 + 8 * rr, c);
+          uint32_t hi, lo;
+          split_pair(-v[4 * k + 2 * rr], -v[4 * k + 2 * rr + 1], hi, lo);
+          *reinterpret_cast<uint32_t*>(sm.wn[0] + off) = hi;
+          *reinterpret_cast<uint32_t*>(sm.wn[1] + off) = lo;
+        }
+      }
+    }
+    e_handoff(cx.tid, &bb.staged);
+  };
+  staging(0);
+  for (int j = 0; j < n; ++j) {
+    const int gc = gc0 + j, st = j & 1;
+    role_wait(&bb.a_done, ph.a_done, abort);
+    const float* gm = sm.gam[st];
+    const float gC = gm[63];
+    if (kStore && cx.tid == 0) bulk_wait_read_all();  // the start-state record has read sm.s / sm.slo
+    {
+      // V' = D_V: its records (hi / lo) and V'_s = e^{gamma_C - gamma_t} V' (hi / lo) for K^T V'_s
+      const float sc[2] = {__expf(gC - gm[r0]), __expf(gC - gm[r0 + 8])};
+      uint8_t* vph = kStore ? p.vp_img + rec(gc) * 16384 + cx.half * 8192 : nullptr;
+      uint8_t* vpl = kStore ? p.vp_lo_img + rec(gc) * 16384 + cx.half * 8192 : nullptr;
+#pragma unroll
+      for (int hc = 0; hc < 2; ++hc) {
+        float v[16];
+        tmem_ld16x256_x4(cx.tmem + kRtV + lane_base + 64 * cx.half + 32 * hc, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int c = 32 * hc + 8 * k + c2;
+#pragma unroll
+          for (int rr = 0; rr < 2; ++rr) {
+            const float x0 = v[4 * k + 2 * rr], x1 = v[4 * k + 2 * rr + 1];
+            const uint32_t off = sw128_pair(r0 + 8 * rr, c);
+            uint32_t hi, lo;
+            split_pair(x0 * sc[rr], x1 * sc[rr], hi, lo);
+            *reinterpret_cast<uint32_t*>(sm.vs[cx.half] + off) = hi;
+            *reinterpret_cast<uint32_t*>(sm.vslo[cx.half] + off) = lo;
+            if (kStore) {
+              split_pair(x0, x1, hi, lo);
+              *reinterpret_cast<uint32_t*>(vph + off) = hi;
+              *reinterpret_cast<uint32_t*>(vpl + off) = lo;
+            }
+          }
+        }
+      }
+    }
+    e_handoff(cx.tid, &bb.epi1);
+    if (j + 1 < n) staging(j + 1);
+    role_wait(&bb.b_done, ph.b_done, abort);
+    {
+      const float GC = __expf(gC);
+#pragma unroll
+      for (int hc = 0; hc < 2; ++hc) {
+        float v[32];
+        tmem_ld16(cx.tmem + kRtD2 + lane_base + 64 * cx.half + 32 * hc, v);
+        tmem_ld16(cx.tmem + kRtD2 + lane_base + 64 * cx.half + 32 * hc + 16, v + 16);
+        tmem_ld_wait();
+#pragma unroll
+        for (int x = 0; x < 32; ++x) S[32 * hc + x] = GC * S[32 * hc + x] + v[x];
+      }
+      store_state_comp(sm, cx, S);
+    }
+    e_handoff(cx.tid, &bb.epi2, &bb.empty[st]);
+    if (kStore && j + 1 < n && cx.tid == 0) store_s_record(gc + 1);
+  }
+  if (cx.tid == 0) bulk_wait_all();  // every record store has landed before the buffers are reused
+  return !*abort;
+}
+
 __device__ __forceinline__ void publish(int* flag) {
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -1232,16 +1207,16 @@ __device__ __forceinline__ void publish(int* flag) {
   }
 }
 
-// kRec: the backward's recompute (per-chunk path with records and compensated arithmetic, 256
-// threads); otherwise the warp-specialized forward (320 threads).
+// kRec: the backward's recompute (compensated arithmetic, records in the output pass); otherwise
+// the forward. Both warp-specialized, 320 threads.
 constexpr int kTransWindow = 12;  // chunks of the transition evaluated first (see pass 1, part 0)
 
 template <int kMode, bool kRec>
-__global__ void __launch_bounds__(kRec ? 256 : kWsThreads, 1) chain_kernel(const __grid_constant__ FwdParams p) {
+__global__ void __launch_bounds__(kWsThreads, 1) chain_kernel(const __grid_constant__ FwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = smem_align1024(smem_raw);
-  ChainSmem* smp = reinterpret_cast<ChainSmem*>(base);
   WsSmem* wss = reinterpret_cast<WsSmem*>(base);
+  RecSmem* rss = reinterpret_cast<RecSmem*>(base);
   __shared__ uint64_t bar_ld, bar_mma;
   __shared__ WsBars wbars;
   __shared__ uint32_t tmem_holder;
@@ -1249,7 +1224,6 @@ __global__ void __launch_bounds__(kRec ? 256 : kWsThreads, 1) chain_kernel(const
   Header* hd = ws_ptr<Header>(p, p.L.header);
   constexpr bool rec = kRec;
   ChainCtx cx;
-  cx.sm = smp;
   cx.base = base;
   cx.bar_ld = &bar_ld;
   cx.bar_mma = &bar_mma;
@@ -1270,31 +1244,22 @@ __global__ void __launch_bounds__(kRec ? 256 : kWsThreads, 1) chain_kernel(const
   if (cx.tid == 0) {
     mbar_init(&bar_ld, 1);
     mbar_init(&bar_mma, 1);
-    if (!rec) {
-      mbar_init(&wbars.full[0], 1);
-      mbar_init(&wbars.full[1], 1);
-      mbar_init(&wbars.fullq, 1);
-      mbar_init(&wbars.empty[0], 2);
-      mbar_init(&wbars.empty[1], 2);
-      mbar_init(&wbars.emptyq, 2);
-      mbar_init(&wbars.a_done, 1);
-      mbar_init(&wbars.pre_done, 1);
-      mbar_init(&wbars.b_done, 1);
-      mbar_init(&wbars.epi1, 1);
-      mbar_init(&wbars.staged, 1);
-      mbar_init(&wbars.epi2, 1);
-      mbar_init(&wbars.vfree, 1);
-    }
+    mbar_init(&wbars.full[0], 1);
+    mbar_init(&wbars.full[1], 1);
+    mbar_init(&wbars.fullq, 1);
+    mbar_init(&wbars.fullu, 1);
+    mbar_init(&wbars.empty[0], 2);
+    mbar_init(&wbars.empty[1], 2);
+    mbar_init(&wbars.emptyq, rec ? 1 : 2);  // the forward's epilogue also releases Q
+    mbar_init(&wbars.a_done, 1);
+    mbar_init(&wbars.pre_done, 1);
+    mbar_init(&wbars.b_done, 1);
+    mbar_init(&wbars.epi1, 1);
+    mbar_init(&wbars.staged, 1);
+    mbar_init(&wbars.epi2, 1);
+    mbar_init(&wbars.vfree, 1);
     s_abort = 0;
     fence_mbar_init();
-  }
-  if constexpr (rec) {
-    for (int e = cx.tid; e < 8192 / 16; e += 256) {
-      reinterpret_cast<uint4*>(smp->z)[e] = make_uint4(0, 0, 0, 0);
-      reinterpret_cast<uint4*>(smp->z2)[e] = make_uint4(0, 0, 0, 0);
-    }
-    if (kMode == kModeP1)
-      for (int e = cx.tid; e < 2 * 16384 / 16; e += 256) reinterpret_cast<uint4*>(smp->qw)[e] = make_uint4(0, 0, 0, 0);
   }
   if (cx.warp == 0) tmem_alloc(&tmem_holder, 512);
   sync_generic_to_async();
@@ -1303,18 +1268,18 @@ __global__ void __launch_bounds__(kRec ? 256 : kWsThreads, 1) chain_kernel(const
   const int32_t* si = ws_ptr<int32_t>(p, p.L.seg_info);
   const int32_t* slot = ws_ptr<int32_t>(p, p.L.seg_slot);
   const int32_t* seq_seg0 = ws_ptr<int32_t>(p, p.L.seq_seg0);
-  const int32_t* ctok = ws_ptr<int32_t>(p, p.L.chunk_tok0);
-  const int32_t* clen = ws_ptr<int32_t>(p, p.L.chunk_len);
   int* flags_seg = ws_ptr<int>(p, p.L.flags_seg);
   int* flags_fin = ws_ptr<int>(p, p.L.flags_fin);
   int* mzero = ws_ptr<int>(p, p.L.mzero);
   const size_t st_elems = (size_t)kDim * kDim;
   float S[64];
   auto store_s = [&]() {
-    if constexpr (rec)
-      store_state_bf16_to(*smp, cx, S);
-    else if (epi)
-      store_state_bf16_to(*wss, cx, S);
+    if (epi) {
+      if constexpr (rec)
+        store_state_comp(*rss, cx, S);
+      else
+        store_state_bf16_to(*wss, cx, S);
+    }
   };
   auto set_zero = [&]() {
     for (int c = 0; c < 64; ++c) S[c] = 0.f;
@@ -1329,16 +1294,32 @@ __global__ void __launch_bounds__(kRec ? 256 : kWsThreads, 1) chain_kernel(const
       for (int x = 0; x < 64; ++x) mine = mine && (S[x] == 0.f);
     return __syncthreads_and(mine) != 0;
   };
-  // forward chain over [g0, g1) with outputs from g_out (warp-specialized path)
+  // chain over [g0, g1): outputs from g_out (forward), records from g_out (recompute)
   auto run_fast = [&](int g0, int g1, int g_out, int h, int hk, bool with_u) -> bool {
-    bool ok2;
-    if (with_u)
-      ok2 = run_ws<true>(p, cx, wbars, ph, &s_abort, S, g0, g1, g_out, h, hk);
-    else
-      ok2 = run_ws<false>(p, cx, wbars, ph, &s_abort, S, g0, g1, g_out, h, hk);
-    (void)ok2;
+    if constexpr (rec) {
+      if (!with_u) {
+        run_ws_rec<false, false>(p, cx, wbars, ph, &s_abort, S, g0, g1, h, hk);
+      } else {
+        // the state after the first part is staged by its last chunk
+        const int gm = g_out < g0 ? g0 : (g_out > g1 ? g1 : g_out);
+        if (gm > g0) run_ws_rec<true, false>(p, cx, wbars, ph, &s_abort, S, g0, gm, h, hk);
+        if (gm > g0 && g1 > gm) __syncthreads();
+        if (g1 > gm && s_abort == 0) run_ws_rec<true, true>(p, cx, wbars, ph, &s_abort, S, gm, g1, h, hk);
+      }
+    } else {
+      if (with_u)
+        run_ws<true>(p, cx, wbars, ph, &s_abort, S, g0, g1, g_out, h, hk);
+      else
+        run_ws<false>(p, cx, wbars, ph, &s_abort, S, g0, g1, g_out, h, hk);
+    }
     __syncthreads();
     return s_abort == 0;
+  };
+  auto affine = [&](const float* Mm, const float* Bm, float* out) -> bool {
+    if constexpr (rec)
+      return affine_apply(p, cx, affine_bufs(*rss), Mm, Bm, S, out);
+    else
+      return affine_apply(p, cx, affine_bufs(*wss), Mm, Bm, S, out);
   };
 
   for (;;) {
@@ -1360,41 +1341,28 @@ __global__ void __launch_bounds__(kRec ? 256 : kWsThreads, 1) chain_kernel(const
       float* mdst = ws_ptr<float>(p, p.L.mmat) + ((size_t)sl * Hv + h) * st_elems;
       bool m_zero = false;
       if (part == 0) {
-        if constexpr (rec) {
+        // Transition M = Phi_last ... Phi_first, evaluated as Y X with Y the product over the
+        // last kTransWindow chunks (a chain from I). When Y is exactly zero so is M, and the
+        // segment boundary needs no start state; otherwise X (chain from I over the first
+        // chunks) and M = Y X.
+        const int w = nch < kTransWindow ? nch : kTransWindow;
+        set_identity();
+        store_s();
+        sync_generic_to_async();
+        if (!run_fast(c0 + nch - w, c0 + nch, c0 + nch, h, hk, false)) break;
+        m_zero = all_zero();
+        if (epi) save_state(cx, mdst, S);
+        if (!m_zero && w < nch) {
           set_identity();
           store_s();
           sync_generic_to_async();
-          for (int c = 0; c < nch && ok && !m_zero; ++c) {
-            const int gc = c0 + c;
-            ok = chain_chunk<false, false, false, true>(p, cx, S, gc, h, hk, ctok[gc], clen[gc]);
-            m_zero = all_zero();
-          }
-          if (!ok) break;
-          save_state(cx, mdst, S);
-        } else {
-          // Transition M = Phi_last ... Phi_first, evaluated as Y X with Y the product over the
-          // last kTransWindow chunks (a chain from I). When Y is exactly zero so is M, and the
-          // segment boundary needs no start state; otherwise X (chain from I over the first
-          // chunks) and M = Y X.
-          const int w = nch < kTransWindow ? nch : kTransWindow;
-          set_identity();
-          store_s();
+          if (!run_fast(c0, c0 + nch - w, c0 + nch, h, hk, false)) break;
+          __syncthreads();  // Y is in global memory
+          store_s();        // X for the product
           sync_generic_to_async();
-          if (!run_fast(c0 + nch - w, c0 + nch, c0 + nch, h, hk, false)) break;
-          m_zero = all_zero();
-          if (epi) save_state(cx, mdst, S);
-          if (!m_zero && w < nch) {
-            set_identity();
-            store_s();
-            sync_generic_to_async();
-            if (!run_fast(c0, c0 + nch - w, c0 + nch, h, hk, false)) break;
-            __syncthreads();  // Y is in global memory
-            store_s();        // X (bf16) for the product
-            sync_generic_to_async();
-            if (!affine_apply(p, cx, *wss, mdst, nullptr, S, mdst)) {
-              set_status(hd, kErrTimeout);
-              break;
-            }
+          if (!affine(mdst, nullptr, mdst)) {
+            set_status(hd, kErrTimeout);
+            break;
           }
         }
       } else {
@@ -1409,15 +1377,7 @@ __global__ void __launch_bounds__(kRec ? 256 : kWsThreads, 1) chain_kernel(const
         }
         store_s();
         sync_generic_to_async();
-        if constexpr (rec) {
-          for (int c = 0; c < nch && ok; ++c) {
-            const int gc = c0 + c;
-            ok = chain_chunk<false, true, false, true>(p, cx, S, gc, h, hk, ctok[gc], clen[gc]);
-          }
-        } else {
-          ok = run_fast(c0, c0 + nch, c0 + nch, h, hk, true);
-        }
-        if (!ok) break;
+        if (!run_fast(c0, c0 + nch, c0 + nch, h, hk, true)) break;
         float* dst = (part == 1) ? ws_ptr<float>(p, p.L.bmat) : ws_ptr<float>(p, p.L.pub);
         if (epi) save_state(cx, dst + ((size_t)sl * Hv + h) * st_elems, S);
       }
@@ -1508,14 +1468,7 @@ __global__ void __launch_bounds__(kRec ? 256 : kWsThreads, 1) chain_kernel(const
     // early publication of this segment's end state (exact split), unless its transition is zero
     if (p.d.mode == 0 && slot[s] >= 0 && dep != -1 && !__ldcg(&mzero[slot[s] * Hv + h])) {
       const size_t off = ((size_t)slot[s] * Hv + h) * st_elems;
-      bool okp;
-      if constexpr (rec)
-        okp = affine_apply(p, cx, *smp, ws_ptr<float>(p, p.L.mmat) + off, ws_ptr<float>(p, p.L.bmat) + off, S,
-                           ws_ptr<float>(p, p.L.pub) + off);
-      else
-        okp = affine_apply(p, cx, *wss, ws_ptr<float>(p, p.L.mmat) + off, ws_ptr<float>(p, p.L.bmat) + off, S,
-                           ws_ptr<float>(p, p.L.pub) + off);
-      if (!okp) {
+      if (!affine(ws_ptr<float>(p, p.L.mmat) + off, ws_ptr<float>(p, p.L.bmat) + off, ws_ptr<float>(p, p.L.pub) + off)) {
         set_status(hd, kErrTimeout);
         break;
       }
@@ -1523,16 +1476,7 @@ __global__ void __launch_bounds__(kRec ? 256 : kWsThreads, 1) chain_kernel(const
       store_s();  // affine_apply used the staging buffers
       sync_generic_to_async();
     }
-    if constexpr (!rec) {
-      ok = run_fast(first_chunk, c0 + nch, c0, h, hk, true);
-    } else {
-      for (int gc = first_chunk; gc < c0 && ok; ++gc)
-        ok = chain_chunk<false, true, false, true>(p, cx, S, gc, h, hk, ctok[gc], clen[gc]);
-      for (int c = 0; c < nch && ok; ++c) {
-        const int gc = c0 + c;
-        ok = chain_chunk<false, true, true>(p, cx, S, gc, h, hk, ctok[gc], clen[gc]);
-      }
-    }
+    ok = run_fast(first_chunk, c0 + nch, c0, h, hk, true);
     if (!ok) {
       set_status(hd, kErrTimeout);
       break;
@@ -1592,7 +1536,7 @@ int launch_fwd(const FwdParams& p, cudaStream_t stream, cudaEvent_t* ev) {
     const int64_t units = (2 * p.L.slots + 1) * p.d.Hv;
     const int grid = (int)(units < items_cap ? units : items_cap);
     if (p.st_img)
-      chain_kernel<kModeP1, true><<<grid, 256, kSmemBytes, stream>>>(p);
+      chain_kernel<kModeP1, true><<<grid, kWsThreads, kSmemBytes, stream>>>(p);
     else
       chain_kernel<kModeP1, false><<<grid, kWsThreads, kSmemBytes, stream>>>(p);
   }
@@ -1602,7 +1546,7 @@ int launch_fwd(const FwdParams& p, cudaStream_t stream, cudaEvent_t* ev) {
     const int64_t items = p.L.smax * p.d.Hv;
     const int grid = (int)(items < items_cap ? items : items_cap);
     if (p.st_img)
-      chain_kernel<kModeOut, true><<<grid, 256, kSmemBytes, stream>>>(p);
+      chain_kernel<kModeOut, true><<<grid, kWsThreads, kSmemBytes, stream>>>(p);
     else
       chain_kernel<kModeOut, false><<<grid, kWsThreads, kSmemBytes, stream>>>(p);
   }
