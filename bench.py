@@ -18,6 +18,7 @@ the data path) launched by torchrun.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import os
@@ -74,8 +75,12 @@ def kernel_counts(T, Hk, Hv, N):
     # kkt_solve: k, g, beta in; K K^T and the 64x64 solve per value head
     kkt_b = T * (Hk * D * 2 + 2 * Hv * 4)
     kkt_f = n_ch * (Hk * 2 * C * C * D + Hv * C * C * C / 3)
+    # out_kernel (o from the records of a training forward): q in, o out; Q S, P V' per value head
+    out_b = T * (Hk * D * 2 + Hv * D * 2)
+    out_f = n_ch * Hv * 2 * (C * D * D + C * C * D)
     return {"chain_kernel<out>": chain, "chain_kernel<out,record>": chain, "grad_kernel": (grad_b, grad_f),
-            "dq_kernel": (dq_b, dq_f), "rev_chain_kernel": (rev_b, rev_f), "kkt_solve_kernel": (kkt_b, kkt_f)}
+            "dq_kernel": (dq_b, dq_f), "rev_chain_kernel": (rev_b, rev_f), "kkt_solve_kernel": (kkt_b, kkt_f),
+            "kkt_solve_kernel<record>": (kkt_b, kkt_f), "out_kernel": (out_b, out_f)}
 
 
 def load_peaks():
@@ -253,8 +258,6 @@ def run_ours(args, rank, world, local_rank):
     for e in ev_f + ev_b:
         e.record(stream)
     opts = gdn.Options(mode=args.mode)
-    opts_f = gdn.Options(mode=args.mode, stage_events=ev_f)
-    opts_b = gdn.Options(mode=args.mode, stage_events=ev_b)
     ws = torch.empty(max(gdn.fwd_workspace_size(N, T, Hk, Hv, opts), gdn.bwd_workspace_size(N, T, Hk, Hv, opts)),
                      dtype=torch.uint8, device=dev)
     out = torch.empty((T, Hv, D), dtype=torch.bfloat16, device=dev)
@@ -273,6 +276,14 @@ def run_ours(args, rank, world, local_rank):
             raise
         has_bwd = False
 
+    # A training step (exact mode) keeps the forward's records for its backward: the forward runs the
+    # backward's recompute and forms o from the records, the backward skips the recompute.
+    train = has_bwd and args.mode == "exact"
+    o_fwd = gdn.Options(mode=args.mode, save_for_backward=train)
+    o_bwd = gdn.Options(mode=args.mode, reuse_forward=train)
+    opts_f = dataclasses.replace(o_fwd, stage_events=ev_f)
+    opts_b = dataclasses.replace(o_bwd, stage_events=ev_b)
+
     def step(of, ob):
         fwd(of)
         if has_bwd:
@@ -280,7 +291,7 @@ def run_ours(args, rank, world, local_rank):
 
     flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)  # > 129 MB L2
     for _ in range(args.warmup):
-        step(opts, opts)
+        step(o_fwd, o_bwd)
     torch.cuda.synchronize()
     st = gdn.workspace_status(ws)
     if st != gdn.GDN_OK:
@@ -321,6 +332,23 @@ def run_ours(args, rank, world, local_rank):
         ms = float(t.item())
     value = T * world / (ms * 1e-3) / 1e6
 
+    # context, outside the timed region: the inference forward and the backward that recomputes
+    ctx = None
+    if train:
+        ctx_n = max(3, min(args.steps, 10))
+        ctx_f = np.zeros((ctx_n, gdn.NUM_STAGES))
+        ctx_b = np.zeros((ctx_n, gdn.NUM_STAGES))
+        for i in range(ctx_n):
+            flush.zero_()
+            fwd(dataclasses.replace(opts, stage_events=ev_f))
+            gdn.chunk_bwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"], dout,
+                          options=dataclasses.replace(opts, stage_events=ev_b), workspace=ws)
+            torch.cuda.synchronize()
+            for s_ in range(gdn.NUM_STAGES):
+                ctx_f[i, s_] = ev_f[2 * s_].elapsed_time(ev_f[2 * s_ + 1])
+                ctx_b[i, s_] = ev_b[2 * s_].elapsed_time(ev_b[2 * s_ + 1])
+        ctx = (ctx_f.mean(axis=0), ctx_b.mean(axis=0))
+
     # e2e: the same step through the public API from pinned host buffers, copies inside the timed
     # region: inputs (and the output gradient) host->device, outputs (and the gradients) device->host
     host = {k: v.detach().cpu().pin_memory() for k, v in d.items() if v is not None}
@@ -345,12 +373,12 @@ def run_ours(args, rank, world, local_rank):
         for k2, v2 in host.items():
             dev_in[k2].copy_(v2, non_blocking=True)
         gdn.chunk_fwd(dev_in["q"], dev_in["k"], dev_in["v"], dev_in["g"], dev_in["beta"], dev_in["cu_seqlens"], None,
-                      None, options=opts, out=out, final_state=fin, workspace=ws)
+                      None, options=o_fwd, out=out, final_state=fin, workspace=ws)
         out_h.copy_(out, non_blocking=True)
         fin_h.copy_(fin, non_blocking=True)
         if has_bwd:
             gr = gdn.chunk_bwd(dev_in["q"], dev_in["k"], dev_in["v"], dev_in["g"], dev_in["beta"],
-                               dev_in["cu_seqlens"], dev_in["dout"], options=opts, workspace=ws)
+                               dev_in["cu_seqlens"], dev_in["dout"], options=o_bwd, workspace=ws)
             for k2, v2 in grad_h.items():
                 v2.copy_(gr[k2], non_blocking=True)
     eb.record(stream)
@@ -361,12 +389,20 @@ def run_ours(args, rank, world, local_rank):
     if rank != 0:
         return None
     peaks = load_peaks()
-    fnames = {gdn.STAGE_PLAN: "plan_kernel", gdn.STAGE_KKT_SOLVE: "kkt_solve_kernel",
-              gdn.STAGE_SPLIT: "chain_kernel<pass1>", gdn.STAGE_CHAIN: "chain_kernel<out>"}
-    bnames = {gdn.STAGE_PLAN: "plan_kernel", gdn.STAGE_KKT_SOLVE: "kkt_solve_kernel",
-              gdn.STAGE_SPLIT: "chain_kernel<pass1,record>", gdn.STAGE_CHAIN: "chain_kernel<out,record>",
-              gdn.STAGE_REV_CHAIN: "rev_chain_kernel", gdn.STAGE_GRADS: "grad_kernel",
-              gdn.STAGE_DQ: "dq_kernel", gdn.STAGE_DINIT: "dinit_reduce_kernel"}
+    infer_f = {gdn.STAGE_PLAN: "plan_kernel", gdn.STAGE_KKT_SOLVE: "kkt_solve_kernel",
+               gdn.STAGE_SPLIT: "chain_kernel<pass1>", gdn.STAGE_CHAIN: "chain_kernel<out>"}
+    recomp_b = {gdn.STAGE_PLAN: "plan_kernel", gdn.STAGE_KKT_SOLVE: "kkt_solve_kernel<record>",
+                gdn.STAGE_SPLIT: "chain_kernel<pass1,record>", gdn.STAGE_CHAIN: "chain_kernel<out,record>",
+                gdn.STAGE_REV_CHAIN: "rev_chain_kernel", gdn.STAGE_GRADS: "grad_kernel",
+                gdn.STAGE_DQ: "dq_kernel", gdn.STAGE_DINIT: "dinit_reduce_kernel"}
+    if train:
+        fnames = {gdn.STAGE_PLAN: "plan_kernel", gdn.STAGE_KKT_SOLVE: "kkt_solve_kernel<record>",
+                  gdn.STAGE_SPLIT: "chain_kernel<pass1,record>", gdn.STAGE_CHAIN: "chain_kernel<out,record>",
+                  gdn.STAGE_OUT: "out_kernel"}
+        bnames = {gdn.STAGE_PLAN: "plan_kernel", gdn.STAGE_REV_CHAIN: "rev_chain_kernel",
+                  gdn.STAGE_GRADS: "grad_kernel", gdn.STAGE_DQ: "dq_kernel", gdn.STAGE_DINIT: "dinit_reduce_kernel"}
+    else:
+        fnames, bnames = infer_f, recomp_b
     avg = stage_f.mean(axis=0)
     bavg = stage_b.mean(axis=0)
     fwd_ms = float(sum(avg[s_] for s_ in fnames))
@@ -386,7 +422,9 @@ def run_ours(args, rank, world, local_rank):
         bound, achieved, peak, unit_r = "tensor", kf / kern_s / 1e12, peaks["tc_sus"], "TFLOP/s"
     tr = traffic_record(dom)
     launches_per_step = 3 + (1 if split_launched else 0)
-    if has_bwd:  # recompute (same launches as the forward) + two reverse passes (one unsplit), grad, dq
+    if train:  # + o from the records; backward: plan, two reverse passes (one unsplit), grad, dq
+        launches_per_step += 1 + 1 + (2 if split_launched else 1) + 2
+    elif has_bwd:  # recompute (same launches as the forward) + two reverse passes (one unsplit), grad, dq
         launches_per_step += 3 + (1 if split_launched else 0) + (2 if split_launched else 1) + 2
     fb, ff = algorithmic_fwd(T, Hk, Hv, N)
     bb, bf = algorithmic_bwd(T, Hk, Hv, N) if has_bwd else (0, 0)
@@ -401,6 +439,9 @@ def run_ours(args, rank, world, local_rank):
         "config": {"workload": "GDN " + ("fwd+bwd" if has_bwd else "fwd") + f", one {T}-token sequence, H_v=8, "
                    "H_k=2, d_k=d_v=128, chunk 64, " + args.mode + " mode", "T": T, "H_v": Hv, "H_k": Hk,
                    "mode": args.mode, "pass": "fwd+bwd" if has_bwd else "fwd",
+                   "step": ("training step: forward keeping its records (save_for_backward), backward reusing "
+                            "them (reuse_forward)" if train else
+                            ("forward, then a backward that recomputes the forward" if has_bwd else "forward")),
                    "l2": "flushed between timed steps (512 MiB write outside the timed events)"},
         "roofline": {"bound": bound, "kernel": dom, "achieved": achieved, "peak": peak, "unit": unit_r,
                      "frac": achieved / peak, "traffic": (tr["bytes_per_launch"] if tr else None),
@@ -416,6 +457,13 @@ def run_ours(args, rank, world, local_rank):
         "gpu_launches": int(launches_per_step * args.steps),
         "clocks": clk,
     }
+    if ctx is not None:
+        res["context"] = {
+            "note": "outside the timed region: the inference forward and the backward that recomputes the forward",
+            "fwd_inference_ms": float(sum(ctx[0][s_] for s_ in infer_f)),
+            "bwd_recompute_ms": float(sum(ctx[1][s_] for s_ in recomp_b)),
+            "fwd_inference_stages_ms": {infer_f[s_]: float(ctx[0][s_]) for s_ in infer_f},
+            "bwd_recompute_stages_ms": {recomp_b[s_]: float(ctx[1][s_]) for s_ in recomp_b}}
     if not has_bwd:
         res["vs_baseline_note"] = "value / FlashQLA forward on H200 (0.31 ms for 32K at TP8), context only"
     if world == 1 and not args.no_cpu_baseline:

@@ -65,6 +65,21 @@ enum gdn_status_code {
   GDN_ERR_WORKSPACE = -5    /* the workspace is smaller than the size query returned */
 };
 
+/* gdn_options.flags: a training step keeps the forward's per-chunk records for its backward. */
+enum gdn_flags {
+  GDN_FLAG_SAVE_FOR_BWD = 1, /* forward: also leave in the workspace everything the backward recomputes
+                                (the intra-chunk factors, the chunk-start states and V' = U - W S, in the
+                                compensated precision of the backward's recompute), and form o from those
+                                records. The workspace must then be of gdn_bwd_workspace_size() bytes
+                                (gdn_fwd_workspace_size() returns that size when this flag is set).
+                                Exact mode only. */
+  GDN_FLAG_REUSE_FWD = 2     /* backward: the workspace holds the records of a forward run with
+                                GDN_FLAG_SAVE_FOR_BWD on the same inputs, options and stream order, and
+                                nothing has written it since; the backward then skips its recompute
+                                (it rebuilds only the chunk and segment maps). Records that do not
+                                belong to these inputs give wrong gradients, not a fault. */
+};
+
 enum gdn_mode {
   GDN_MODE_EXACT = 0,   /* default: long documents split into segments, exact cross-segment fix-up */
   GDN_MODE_TRUNCATE = 1 /* opt-in: segment carries rebuilt from a warmup window ("Lever 1") */
@@ -75,14 +90,15 @@ typedef struct gdn_options {
   float trunc_log_threshold; /* truncation mode: warmup window ends once the summed log-decay < this (-10) */
   int32_t segment_chunks;    /* segment length in 64-token chunks; 0 = automatic, < 0 = never split */
   float scale;               /* multiplies q (1.0: inputs already scaled) */
-  int32_t reserved;          /* must be 0 */
+  int32_t flags;             /* gdn_flags, 0 = none */
   void* stage_events;        /* optional profiling hook: NULL, or a cudaEvent_t[2 * GDN_NUM_STAGES] array;
                                 events 2s and 2s+1 are recorded on `stream` right before and right after
                                 stage s (both at the same point when the stage has nothing to launch) */
 } gdn_options;
 
 /* Stages of a call (indices into gdn_options.stage_events). A backward call runs stages 0-3
- * (the forward recompute), then 4, 5, 7 and 6 in that order. */
+ * (the forward recompute; stage 0 alone with GDN_FLAG_REUSE_FWD), then 4, 5, 7 and 6 in that order.
+ * A forward with GDN_FLAG_SAVE_FOR_BWD runs stages 0-3 and 8. */
 enum gdn_fwd_stage {
   GDN_STAGE_PLAN = 0,      /* chunk / segment maps */
   GDN_STAGE_KKT_SOLVE = 1, /* intra-chunk K K^T, triangular solve, WY factors */
@@ -92,14 +108,17 @@ enum gdn_fwd_stage {
   GDN_STAGE_GRADS = 5,     /* backward: per-chunk dk, dv, dg, dbeta */
   GDN_STAGE_DINIT = 6,     /* backward: d(initial_state) sums over documents sharing a pool entry */
   GDN_STAGE_DQ = 7,        /* backward: per-chunk dq */
-  GDN_NUM_STAGES = 8
+  GDN_STAGE_OUT = 8,       /* forward with GDN_FLAG_SAVE_FOR_BWD: o from the records */
+  GDN_NUM_STAGES = 9
 };
 
-/* Fill `opt` with the defaults: exact mode, threshold -10, automatic segments, scale 1, no events. */
+/* Fill `opt` with the defaults: exact mode, threshold -10, automatic segments, scale 1, no flags,
+ * no events. */
 void gdn_default_options(gdn_options* opt);
 
-/* Workspace bytes gdn_chunk_fwd needs for these sizes (opt may be NULL for defaults).
- * Returns 0 for invalid sizes. The value depends on the current device's SM count. */
+/* Workspace bytes gdn_chunk_fwd needs for these sizes (opt may be NULL for defaults; with
+ * GDN_FLAG_SAVE_FOR_BWD the backward's size). Returns 0 for invalid sizes. The value depends on the
+ * current device's SM count. */
 size_t gdn_fwd_workspace_size(int N, int T, int H_k, int H_v, const gdn_options* opt);
 
 /* Workspace bytes gdn_chunk_bwd needs (opt->mode is ignored: the backward is exact). */
@@ -111,6 +130,9 @@ size_t gdn_bwd_workspace_size(int N, int T, int H_k, int H_v, const gdn_options*
  * n_init: number of pool entries in initial_state (0 allowed).
  * head_dim must be 128. workspace: device memory of at least gdn_fwd_workspace_size() bytes,
  * 256-byte aligned; its contents need no initialisation.
+ * opt->flags: GDN_FLAG_SAVE_FOR_BWD runs the forward of a training step (the backward's recompute,
+ * with o formed from its records) and needs exact mode; GDN_FLAG_REUSE_FWD is rejected
+ * (GDN_ERR_INVALID_ARG).
  */
 int gdn_chunk_fwd(const void* q, const void* k, const void* v, const float* g, const float* beta,
                   const int32_t* cu_seqlens, int N, int T, int H_k, int H_v, int head_dim,
@@ -129,6 +151,8 @@ int gdn_chunk_fwd(const void* q, const void* k, const void* v, const float* g, c
  * The backward is always that of the exact forward: opt->mode is ignored (truncation is a
  * forward-only option), the other options apply. Long documents are split into segments in
  * both directions, with an exact fix-up of the state and of its gradient at each boundary.
+ * opt->flags: GDN_FLAG_REUSE_FWD skips the recompute (see gdn_flags); GDN_FLAG_SAVE_FOR_BWD is
+ * rejected (GDN_ERR_INVALID_ARG).
  */
 int gdn_chunk_bwd(const void* q, const void* k, const void* v, const float* g, const float* beta,
                   const int32_t* cu_seqlens, int N, int T, int H_k, int H_v, int head_dim,

@@ -39,22 +39,28 @@ class GdnError(RuntimeError):
 
 class COptions(ctypes.Structure):
     _fields_ = [("mode", ctypes.c_int32), ("trunc_log_threshold", ctypes.c_float),
-                ("segment_chunks", ctypes.c_int32), ("scale", ctypes.c_float), ("reserved", ctypes.c_int32),
+                ("segment_chunks", ctypes.c_int32), ("scale", ctypes.c_float), ("flags", ctypes.c_int32),
                 ("stage_events", ctypes.c_void_p)]
 
 
-NUM_STAGES = 8
-STAGE_PLAN, STAGE_KKT_SOLVE, STAGE_SPLIT, STAGE_CHAIN, STAGE_REV_CHAIN, STAGE_GRADS, STAGE_DINIT, STAGE_DQ = range(8)
+NUM_STAGES = 9
+(STAGE_PLAN, STAGE_KKT_SOLVE, STAGE_SPLIT, STAGE_CHAIN, STAGE_REV_CHAIN, STAGE_GRADS, STAGE_DINIT, STAGE_DQ,
+ STAGE_OUT) = range(9)
+FLAG_SAVE_FOR_BWD = 1  # forward of a training step: keep the records for the backward
+FLAG_REUSE_FWD = 2     # backward: use the records of a FLAG_SAVE_FOR_BWD forward instead of recomputing
 
 
 @dataclass
 class Options:
-    """Mirror of gdn_options. mode: "exact" (default) or "truncate"."""
+    """Mirror of gdn_options. mode: "exact" (default) or "truncate". save_for_backward (forward) and
+    reuse_forward (backward) set the two gdn_flags of a training step that shares one workspace."""
     mode: str = "exact"
     trunc_log_threshold: float = -10.0
     segment_chunks: int = 0
     scale: float = 1.0
     stage_events: Optional[object] = None  # optional list of 2 * NUM_STAGES timing torch.cuda.Event
+    save_for_backward: bool = False
+    reuse_forward: bool = False
 
     def c(self) -> COptions:
         m = {"exact": MODE_EXACT, "truncate": MODE_TRUNCATE}[self.mode]
@@ -65,7 +71,8 @@ class Options:
                 raise ValueError("stage_events: 2 * NUM_STAGES recorded timing events are required")
             self._ev_array = (ctypes.c_void_p * len(handles))(*handles)
             ev = ctypes.cast(self._ev_array, ctypes.c_void_p)
-        return COptions(m, float(self.trunc_log_threshold), int(self.segment_chunks), float(self.scale), 0, ev)
+        flags = (FLAG_SAVE_FOR_BWD if self.save_for_backward else 0) | (FLAG_REUSE_FWD if self.reuse_forward else 0)
+        return COptions(m, float(self.trunc_log_threshold), int(self.segment_chunks), float(self.scale), flags, ev)
 
 
 _lock = threading.Lock()
@@ -192,7 +199,9 @@ def chunk_fwd(q, k, v, g, beta, cu_seqlens, init_idx=None, initial_state=None, o
               out=None, final_state=None, workspace=None, stream=None):
     """Forward over a packed batch. Shapes: q, k [T, Hk, 128] bf16; v [T, Hv, 128] bf16;
     g, beta [T, Hv] fp32; cu_seqlens [N+1] int32 (device); init_idx [N] int32 or None;
-    initial_state [n_init, Hv, 128, 128] fp32 or None. Returns (out, final_state)."""
+    initial_state [n_init, Hv, 128, 128] fp32 or None. Returns (out, final_state).
+    With options.save_for_backward the workspace (allocated here when not given, of the backward's
+    size) keeps the records for chunk_bwd(..., options with reuse_forward, workspace=the same)."""
     torch = _torch()
     T, Hk, D = q.shape
     Hv = v.shape[1]
@@ -228,8 +237,12 @@ def chunk_fwd(q, k, v, g, beta, cu_seqlens, init_idx=None, initial_state=None, o
 
 def chunk_bwd(q, k, v, g, beta, cu_seqlens, dout, dfinal_state=None, init_idx=None, initial_state=None,
               options: Optional[Options] = None, workspace=None, stream=None):
-    """Backward. Returns dict of fp32 gradients dq, dk, dv, dg, dbeta and dinit (None without a pool)."""
+    """Backward. Returns dict of fp32 gradients dq, dk, dv, dg, dbeta and dinit (None without a pool).
+    With options.reuse_forward, `workspace` must be the one a save_for_backward forward of the same
+    inputs used."""
     torch = _torch()
+    if options is not None and options.reuse_forward and workspace is None:
+        raise ValueError("reuse_forward needs the workspace of the save_for_backward forward")
     T, Hk, D = q.shape
     Hv = v.shape[1]
     N = cu_seqlens.shape[0] - 1

@@ -54,7 +54,8 @@ gdn_options resolve(const gdn_options* opt) {
 }
 
 bool valid_options(const gdn_options& o) {
-  return (o.mode == GDN_MODE_EXACT || o.mode == GDN_MODE_TRUNCATE) && o.reserved == 0 && o.scale == o.scale;
+  return (o.mode == GDN_MODE_EXACT || o.mode == GDN_MODE_TRUNCATE) &&
+         (o.flags & ~(GDN_FLAG_SAVE_FOR_BWD | GDN_FLAG_REUSE_FWD)) == 0 && o.scale == o.scale;
 }
 
 PlanDims make_dims(int N, int T, int H_k, int H_v, int n_init, const gdn_options& o, int sms) {
@@ -86,7 +87,7 @@ void gdn_default_options(gdn_options* opt) {
   opt->trunc_log_threshold = -10.0f;
   opt->segment_chunks = 0;
   opt->scale = 1.0f;
-  opt->reserved = 0;
+  opt->flags = 0;
   opt->stage_events = nullptr;
 }
 
@@ -113,6 +114,7 @@ size_t gdn_fwd_workspace_size(int N, int T, int H_k, int H_v, const gdn_options*
   if (!sizes_ok(N, T, H_k, H_v)) return 0;
   const gdn_options o = resolve(opt);
   if (!valid_options(o)) return 0;
+  if (o.flags & GDN_FLAG_SAVE_FOR_BWD) return gdn_bwd_workspace_size(N, T, H_k, H_v, opt);
   return fwd_layout(make_dims(N, T, H_k, H_v, 0, o, current_sm_count())).total;
 }
 
@@ -147,11 +149,31 @@ int gdn_chunk_fwd(const void* q, const void* k, const void* v, const float* g, c
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) || !aligned(final_state, 16) ||
       !aligned(initial_state, 16) || !aligned(workspace, 256))
     return GDN_ERR_INVALID_ARG;
+  if (o.flags & GDN_FLAG_REUSE_FWD) return GDN_ERR_INVALID_ARG;  // a backward option
+  if ((o.flags & GDN_FLAG_SAVE_FOR_BWD) && o.mode != GDN_MODE_EXACT) return GDN_ERR_INVALID_ARG;
   const int dev = select_device_of(workspace);
   if (dev != kOk) return dev;
   const int arch = check_arch();
   if (arch != kOk) return arch;
   const int sms = current_sm_count();
+  if (o.flags & GDN_FLAG_SAVE_FOR_BWD) {
+    BwdArgs a;
+    std::memset(&a, 0, sizeof(a));
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.g = g;
+    a.beta = beta;
+    a.cu = cu_seqlens;
+    a.init_idx = init_idx;
+    a.initial_state = initial_state;
+    a.ws = workspace;
+    a.ws_bytes = ws_bytes;
+    a.d = make_dims(N, T, H_k, H_v, n_init, o, sms);
+    a.trunc_thr = o.trunc_log_threshold;
+    a.scale = o.scale;
+    return launch_fwd_save(a, out, final_state, (cudaStream_t)stream, reinterpret_cast<cudaEvent_t*>(o.stage_events));
+  }
   FwdParams p;
   std::memset(&p, 0, sizeof(p));
   p.d = make_dims(N, T, H_k, H_v, n_init, o, sms);
@@ -197,6 +219,7 @@ int gdn_chunk_bwd(const void* q, const void* k, const void* v, const float* g, c
       !aligned(dk, 16) || !aligned(dv, 16) || !aligned(initial_state, 16) || !aligned(dfinal_state, 16) ||
       !aligned(dinitial_state, 16) || !aligned(workspace, 256))
     return GDN_ERR_INVALID_ARG;
+  if (o.flags & GDN_FLAG_SAVE_FOR_BWD) return GDN_ERR_INVALID_ARG;  // a forward option
   const int dev = select_device_of(workspace);
   if (dev != kOk) return dev;
   const int arch = check_arch();
@@ -225,7 +248,8 @@ int gdn_chunk_bwd(const void* q, const void* k, const void* v, const float* g, c
   a.d = make_dims(N, T, H_k, H_v, n_init, oe, current_sm_count());
   a.trunc_thr = o.trunc_log_threshold;
   a.scale = o.scale;
-  return launch_bwd(a, (cudaStream_t)stream, reinterpret_cast<cudaEvent_t*>(o.stage_events));
+  return launch_bwd(a, (o.flags & GDN_FLAG_REUSE_FWD) != 0, (cudaStream_t)stream,
+                    reinterpret_cast<cudaEvent_t*>(o.stage_events));
 }
 
 int gdn_plan_host(const int32_t* cu, int N, int T, int H_v, const int32_t* init_idx, int n_init,

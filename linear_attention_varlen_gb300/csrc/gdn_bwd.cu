@@ -1489,7 +1489,62 @@ __global__ void __launch_bounds__(256) dinit_reduce_kernel(const __grid_constant
 
 // ============================================================================================ launch
 
-int launch_bwd(const BwdArgs& a, cudaStream_t stream, cudaEvent_t* ev) {
+namespace {
+
+// The recording forward over the backward's workspace layout: tensor maps of the inputs, the
+// inputs, and the record pointers. Shared by the backward's recompute and by a forward that keeps
+// its records for the backward.
+int setup_record_fwd(const BwdArgs& a, const BwdLayout& L, FwdParams& f) {
+  std::memset(&f, 0, sizeof(f));
+  const PlanDims& d = a.d;
+  f.d = d;
+  f.L = L.f;
+  if (d.T > 0) {
+    const uint64_t row_k = (uint64_t)d.Hk * kDim * 2, row_v = (uint64_t)d.Hv * kDim * 2;
+    if (!make_tmap_bf16_3d(&f.tm_q, a.q, kDim, d.Hk, d.T, kDim * 2, row_k, 64, 1, 64) ||
+        !make_tmap_bf16_3d(&f.tm_k, a.k, kDim, d.Hk, d.T, kDim * 2, row_k, 64, 1, 64) ||
+        !make_tmap_bf16_3d(&f.tm_v, a.v, kDim, d.Hv, d.T, kDim * 2, row_v, 64, 1, 64))
+      return kErrCuda;
+  }
+  uint8_t* ws = reinterpret_cast<uint8_t*>(a.ws);
+  f.g = a.g;
+  f.beta = a.beta;
+  f.cu = a.cu;
+  f.init_idx = a.init_idx;
+  f.initial_state = a.initial_state;
+  f.out = nullptr;
+  f.final_state = reinterpret_cast<float*>(ws + L.fin);
+  f.ws = ws;
+  f.trunc_thr = a.trunc_thr;
+  f.scale = a.scale;
+  f.st_img = ws + L.st_img;
+  f.vp_img = ws + L.vp_img;
+  f.p_img = ws + L.f.pimg;  // kkt_solve also forms P = scale (Q K^T o E) for the reverse chain
+  f.t_f32 = reinterpret_cast<float*>(ws + L.t_f32);
+  f.tw_lo = ws + L.tw_lo;
+  f.tu_lo = ws + L.tu_lo;
+  f.st_lo_img = ws + L.st_lo;
+  f.vp_lo_img = ws + L.vp_lo;
+  return kOk;
+}
+
+}  // namespace
+
+int launch_fwd_save(const BwdArgs& a, void* out, float* final_state, cudaStream_t stream, cudaEvent_t* ev) {
+  const BwdLayout L = bwd_layout(a.d);
+  if (a.ws_bytes < L.total) return kErrWorkspace;
+  FwdParams f;
+  const int rc = setup_record_fwd(a, L, f);
+  if (rc != kOk) return rc;
+  if (a.d.T > 0 && !make_tmap_bf16_3d(&f.tm_o, out, kDim, a.d.Hv, a.d.T, kDim * 2, (uint64_t)a.d.Hv * kDim * 2,
+                                      64, 1, 64))
+    return kErrCuda;
+  f.out = reinterpret_cast<__nv_bfloat16*>(out);
+  f.final_state = final_state;
+  return launch_fwd(f, stream, ev);
+}
+
+int launch_bwd(const BwdArgs& a, bool reuse, cudaStream_t stream, cudaEvent_t* ev) {
   static bool attr_done = false;
   if (!attr_done) {
     if (cudaFuncSetAttribute(rev_chain_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRevSmemBytes) !=
@@ -1512,41 +1567,16 @@ int launch_bwd(const BwdArgs& a, cudaStream_t stream, cudaEvent_t* ev) {
   p.L = bwd_layout(d);
   if (a.ws_bytes < p.L.total) return kErrWorkspace;
   uint8_t* ws = reinterpret_cast<uint8_t*>(a.ws);
-  // forward recompute with per-chunk records
+  // the forward with per-chunk records (only its maps when a forward left the records here)
   FwdParams f;
-  std::memset(&f, 0, sizeof(f));
-  f.d = d;
-  f.L = p.L.f;
-  if (d.T > 0) {
-    const uint64_t row_k = (uint64_t)d.Hk * kDim * 2, row_v = (uint64_t)d.Hv * kDim * 2;
-    if (!make_tmap_bf16_3d(&f.tm_q, a.q, kDim, d.Hk, d.T, kDim * 2, row_k, 64, 1, 64) ||
-        !make_tmap_bf16_3d(&f.tm_k, a.k, kDim, d.Hk, d.T, kDim * 2, row_k, 64, 1, 64) ||
-        !make_tmap_bf16_3d(&f.tm_v, a.v, kDim, d.Hv, d.T, kDim * 2, row_v, 64, 1, 64) ||
-        !make_tmap_bf16_3d(&p.tm_do, a.dout, kDim, d.Hv, d.T, kDim * 2, row_v, 64, 1, 64))
-      return kErrCuda;
-  }
+  int rc = setup_record_fwd(a, p.L, f);
+  if (rc != kOk) return rc;
+  if (d.T > 0 && !make_tmap_bf16_3d(&p.tm_do, a.dout, kDim, d.Hv, d.T, kDim * 2, (uint64_t)d.Hv * kDim * 2, 64, 1, 64))
+    return kErrCuda;
   p.tm_q = f.tm_q;
   p.tm_k = f.tm_k;
   p.tm_v = f.tm_v;
-  f.g = a.g;
-  f.beta = a.beta;
-  f.cu = a.cu;
-  f.init_idx = a.init_idx;
-  f.initial_state = a.initial_state;
-  f.out = nullptr;
-  f.final_state = reinterpret_cast<float*>(ws + p.L.fin);
-  f.ws = ws;
-  f.trunc_thr = a.trunc_thr;
-  f.scale = a.scale;
-  f.st_img = ws + p.L.st_img;
-  f.vp_img = ws + p.L.vp_img;
-  f.p_img = ws + p.L.f.pimg;  // kkt_solve also forms P = scale (Q K^T o E) for the reverse chain
-  f.t_f32 = reinterpret_cast<float*>(ws + p.L.t_f32);
-  f.tw_lo = ws + p.L.tw_lo;
-  f.tu_lo = ws + p.L.tu_lo;
-  f.st_lo_img = ws + p.L.st_lo;
-  f.vp_lo_img = ws + p.L.vp_lo;
-  int rc = launch_fwd(f, stream, ev);
+  rc = launch_fwd(f, stream, ev, reuse);
   if (rc != kOk) return rc;
   p.g = a.g;
   p.beta = a.beta;

@@ -73,6 +73,10 @@ inline BwdLayout bwd_layout(const PlanDims& d) {
   return L;
 }
 
-int launch_bwd(const BwdArgs& a, cudaStream_t stream, cudaEvent_t* events);
+// reuse: the workspace holds the records of a forward launched with launch_fwd_save on the same
+// inputs; only the maps are rebuilt.
+int launch_bwd(const BwdArgs& a, bool reuse, cudaStream_t stream, cudaEvent_t* events);
+// Forward (o and final states) that leaves its records in a backward workspace for launch_bwd.
+int launch_fwd_save(const BwdArgs& a, void* out, float* final_state, cudaStream_t stream, cudaEvent_t* events);
 
 }  // namespace gdn

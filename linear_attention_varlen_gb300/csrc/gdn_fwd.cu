@@ -31,7 +31,9 @@ using namespace bw;
 
 // ============================================================================================ plan
 
-__global__ void __launch_bounds__(1024) plan_kernel(const __grid_constant__ FwdParams p) {
+// keep_mzero: a backward that reuses a forward's records keeps that forward's pass-1 findings
+// (which segment transitions are exactly zero); the maps it rebuilds are the same.
+__global__ void __launch_bounds__(1024) plan_kernel(const __grid_constant__ FwdParams p, int keep_mzero) {
   Header* hd = ws_ptr<Header>(p, p.L.header);
   int32_t* seq_chunk0 = ws_ptr<int32_t>(p, p.L.seq_chunk0);
   int32_t* seq_seg0 = ws_ptr<int32_t>(p, p.L.seq_seg0);
@@ -124,7 +126,8 @@ __global__ void __launch_bounds__(1024) plan_kernel(const __grid_constant__ FwdP
   for (int e = tid; e < total_segs * p.d.Hv; e += nt) fs[e] = 0;
   for (int e = tid; e < N * p.d.Hv; e += nt) ff[e] = 0;
   int32_t* mz = ws_ptr<int32_t>(p, p.L.mzero);
-  for (int e = tid; e < (int)p.L.slots * p.d.Hv; e += nt) mz[e] = 0;
+  if (!keep_mzero)
+    for (int e = tid; e < (int)p.L.slots * p.d.Hv; e += nt) mz[e] = 0;
   __syncthreads();
   // slots and pass-1 units (serial: only split segments get them)
   if (tid == 0) {
@@ -1499,9 +1502,131 @@ __global__ void __launch_bounds__(kWsThreads, 1) chain_kernel(const __grid_const
   if (cx.warp == 0) tmem_dealloc(cx.tmem, 512);
 }
 
+// ================================================================================ output from records
+//
+// o of one chunk and value head from the recompute's records (the forward of a training step):
+// O = diag(scale e^gamma) Q S + P V', with S the chunk-start state and V' = U - W S (bf16 hi images
+// written by the record chain) and P = scale (Q K^T o E) (bf16 image from kkt_solve). One CTA of
+// 128 threads per (chunk, value head): TMA and bulk loads on one barrier, Q~ formed in place, one
+// M = 64 accumulator, O staged over Q~ and written by TMA store (a partial chunk row by row).
+struct OutSmem {
+  uint8_t q[2][8192];   // Q rows t, two dk blocks -> Q~ in place (A K-major, M = 64); then the O stage
+  uint8_t s[2][16384];  // S hi rows dk, two dv blocks (B MN-major)
+  uint8_t vp[2][8192];  // V' hi rows t, two dv blocks (B MN-major)
+  uint8_t p[8192];      // P rows t (A K-major, M = 64, K = 64)
+  float gam[64];
+};
+constexpr int kOutThreads = 128;
+constexpr size_t kOutSmemBytes = sizeof(OutSmem) + 1024;
+
+__global__ void __launch_bounds__(kOutThreads) out_kernel(const __grid_constant__ FwdParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  OutSmem& sm = *reinterpret_cast<OutSmem*>(smem_align1024(smem_raw));
+  __shared__ uint64_t bar_ld, bar_mma;
+  __shared__ uint32_t tmem_holder;
+  Header* hd = ws_ptr<Header>(p, p.L.header);
+  const int gc = blockIdx.x, h = blockIdx.y, Hv = p.d.Hv, hk = h / (Hv / p.d.Hk);
+  if (gc >= hd->n_chunks || get_status(hd) != 0) return;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tok0 = ws_ptr<int32_t>(p, p.L.chunk_tok0)[gc], nn = ws_ptr<int32_t>(p, p.L.chunk_len)[gc];
+  const size_t rec = (size_t)gc * Hv + h;
+  if (tid == 0) {
+    mbar_init(&bar_ld, 1);
+    mbar_init(&bar_mma, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (tid == 0) {
+    mbar_arrive_expect_tx(&bar_ld, 16384 + 32768 + 16384 + 8192 + 256);
+    tma_load_3d(sm.q[0], &p.tm_q, 0, hk, tok0, &bar_ld);
+    tma_load_3d(sm.q[1], &p.tm_q, 64, hk, tok0, &bar_ld);
+    bulk_load(sm.s[0], p.st_img + rec * 32768, 32768, &bar_ld);
+    bulk_load(sm.vp[0], p.vp_img + rec * 16384, 16384, &bar_ld);
+    bulk_load(sm.p, p.p_img + rec * 8192, 8192, &bar_ld);
+    bulk_load(sm.gam, p.ws + p.L.gam + rec * 256, 256, &bar_ld);
+  }
+  if (warp == 0) tmem_alloc(&tmem_holder, 128);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tm = tmem_holder;
+  bool ok = wait_all(&bar_ld, 0);
+  if (ok) {
+    // Q~ = diag(scale e^gamma) Q, in place
+    for (int e = tid; e < 2 * 64 * 8; e += kOutThreads) {
+      const int b = e >> 9, r = (e >> 3) & 63, cj = e & 7;
+      const uint32_t off = r * 128 + ((cj ^ (r & 7)) << 4);
+      uint4 raw = *reinterpret_cast<const uint4*>(sm.q[b] + off);
+      const float sc = __expf(sm.gam[r]) * p.scale;
+      __nv_bfloat162* x = reinterpret_cast<__nv_bfloat162*>(&raw);
+      uint32_t w[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float2 f = __bfloat1622float2(x[u]);
+        w[u] = pack_bf16x2(f.x * sc, f.y * sc);
+      }
+      *reinterpret_cast<uint4*>(sm.q[b] + off) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    sync_generic_to_async();
+    if (tid == 0) {
+      constexpr uint32_t i64 = idesc_bf16(64, 128, 0, 1);
+      for (int ks = 0; ks < 8; ++ks)
+        umma_bf16(tm, kmajor_desc(smem_u32(sm.q[0]), 8192, ks), mnmajor_desc(smem_u32(sm.s[0]), 16384, ks), i64,
+                  ks > 0);
+      for (int ks = 0; ks < 4; ++ks)
+        umma_bf16(tm, kmajor_desc(smem_u32(sm.p), 8192, ks), mnmajor_desc(smem_u32(sm.vp[0]), 8192, ks), i64, 1);
+      umma_commit(&bar_mma);
+    }
+    ok = wait_all(&bar_mma, 0);
+  }
+  if (ok) {
+    tc_fence_after();
+    // M = 64 accumulator, all 32 lanes: rows r0 = 16 warp + lane / 4 and r0 + 8, column pairs
+    const int c2 = 2 * (lane & 3), r0 = 16 * warp + (lane >> 2);
+    const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
+#pragma unroll
+    for (int cb = 0; cb < 4; ++cb) {
+      float v[16];
+      tmem_ld16x256_x4(tm + lane_base + 32 * cb, v);
+      tmem_ld_wait();
+      uint8_t* blk = sm.q[cb >> 1];  // dv block (the MMA has finished reading Q~)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int c = 32 * (cb & 1) + 8 * k + c2;
+        *reinterpret_cast<uint32_t*>(blk + sw128_pair(r0, c)) = pack_bf16x2(v[4 * k], v[4 * k + 1]);
+        *reinterpret_cast<uint32_t*>(blk + sw128_pair(r0 + 8, c)) = pack_bf16x2(v[4 * k + 2], v[4 * k + 3]);
+      }
+    }
+    if (nn == kChunk) {
+      fence_proxy_async_smem();
+      __syncthreads();
+      if (tid == 0) {
+        tma_store_3d(&p.tm_o, sm.q[0], 0, h, tok0);
+        tma_store_3d(&p.tm_o, sm.q[1], 64, h, tok0);
+        bulk_commit_group();
+        bulk_wait_all();
+      }
+    } else {
+      // the end of a document: only its rows, so that the next document's rows are not touched
+      __syncthreads();
+      for (int e = tid; e < nn * 16; e += kOutThreads) {
+        const int t = e >> 4, u = e & 15, cj = u & 7;
+        const uint4 val = *reinterpret_cast<const uint4*>(sm.q[u >> 3] + t * 128 + ((cj ^ (t & 7)) << 4));
+        reinterpret_cast<uint4*>(p.out + ((size_t)(tok0 + t) * Hv + h) * kDim)[u] = val;
+      }
+    }
+  } else if (tid == 0) {
+    set_status(hd, kErrTimeout);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(tm, 128);
+}
+
 // ========================================================================================= launch
 
-int launch_fwd(const FwdParams& p, cudaStream_t stream, cudaEvent_t* ev) {
+int launch_fwd(const FwdParams& p, cudaStream_t stream, cudaEvent_t* ev, bool plan_only) {
   static bool attr_done = false;
   if (!attr_done) {
     if (cudaFuncSetAttribute(kkt_solve_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1514,7 +1639,9 @@ int launch_fwd(const FwdParams& p, cudaStream_t stream, cudaEvent_t* ev) {
         cudaFuncSetAttribute(chain_kernel<kModeOut, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kSmemBytes) != cudaSuccess ||
         cudaFuncSetAttribute(chain_kernel<kModeP1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kSmemBytes) != cudaSuccess)
+                             (int)kSmemBytes) != cudaSuccess ||
+        cudaFuncSetAttribute(out_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kOutSmemBytes) !=
+            cudaSuccess)
       return kErrCuda;
     attr_done = true;
   }
@@ -1522,8 +1649,14 @@ int launch_fwd(const FwdParams& p, cudaStream_t stream, cudaEvent_t* ev) {
     if (ev) cudaEventRecord(ev[i], stream);
   };
   mark(0);
-  plan_kernel<<<1, 1024, 0, stream>>>(p);
+  plan_kernel<<<1, 1024, 0, stream>>>(p, plan_only ? 1 : 0);
   mark(1);
+  if (plan_only) {
+    for (int i = 2; i < 8; ++i) mark(i);
+    mark(16);
+    mark(17);
+    return cudaGetLastError() == cudaSuccess ? kOk : kErrCuda;
+  }
   mark(2);
   if (p.d.T > 0) {
     dim3 grid((unsigned)p.L.cmax, (unsigned)p.d.Hk);
@@ -1551,6 +1684,11 @@ int launch_fwd(const FwdParams& p, cudaStream_t stream, cudaEvent_t* ev) {
       chain_kernel<kModeOut, false><<<grid, kWsThreads, kSmemBytes, stream>>>(p);
   }
   mark(7);
+  // a forward that keeps its records for the backward forms o from them
+  mark(16);
+  if (p.st_img && p.out && p.d.T > 0)
+    out_kernel<<<dim3((unsigned)p.L.cmax, (unsigned)p.d.Hv), kOutThreads, kOutSmemBytes, stream>>>(p);
+  mark(17);
   return cudaGetLastError() == cudaSuccess ? kOk : kErrCuda;
 }
 

@@ -12,7 +12,7 @@ struct FwdParams {
   CUtensorMap tm_q;  // bf16 [T][Hk][128], box 64 x 1 x 64, 128B swizzle
   CUtensorMap tm_k;  // same shape as q
   CUtensorMap tm_v;  // bf16 [T][Hv][128]
-  CUtensorMap tm_o;  // the output, same shape as v (plain forward only)
+  CUtensorMap tm_o;  // the output, same shape as v (forwards that write o)
   const float* g;
   const float* beta;
   const int32_t* cu;
@@ -25,10 +25,12 @@ struct FwdParams {
   FwdLayout L;
   float trunc_thr;
   float scale;
-  // Plain forward only (NULL in the backward's recompute): P = scale (Q K^T o E) per (chunk, value
-  // head), E_ij = e^{gamma_i - gamma_j} for j <= i inside the chunk, bf16 smem image [cmax][Hv][8 KB]
+  // P = scale (Q K^T o E) per (chunk, value head), E_ij = e^{gamma_i - gamma_j} for j <= i inside
+  // the chunk, bf16 smem image [cmax][Hv][8 KB], formed by kkt_solve
   uint8_t* p_img;
-  // Backward recompute only (all NULL for a plain forward): per (chunk, value head) records
+  // Recording forward only (the backward's recompute, or a forward that keeps its records for the
+  // backward; all NULL for a plain forward): per (chunk, value head) records. With `out` set, o is
+  // formed from them after the chain.
   uint8_t* st_img;  // S at each chunk start, bf16, 128B-swizzled smem image [cmax][Hv][32 KB]
   uint8_t* vp_img;  // V' = U - W S of each chunk, bf16 smem image [cmax][Hv][16 KB]
   float* t_f32;     // T = (I + A)^{-1}, fp32 [cmax][Hv][64 x 64] in the fz layout
@@ -41,7 +43,8 @@ struct FwdParams {
   uint8_t* vp_lo_img;  // [cmax][Hv][16 KB]
 };
 
-// events: NULL or cudaEvent_t[2 * 8], recorded around each stage (see gdn_fwd_stage).
-int launch_fwd(const FwdParams& p, cudaStream_t stream, cudaEvent_t* events);
+// events: NULL or cudaEvent_t[2 * 9], recorded around each stage (see gdn_fwd_stage).
+// plan_only: the chunk and segment maps only (a backward that reuses a forward's records).
+int launch_fwd(const FwdParams& p, cudaStream_t stream, cudaEvent_t* events, bool plan_only = false);
 
 }  // namespace gdn

@@ -61,6 +61,8 @@ extern "C" int gdn_chunk_fwd_noalloc(const void* q, const void* k, const void* v
                                      float* final_state, const gdn_options* opt, gdn_stream_t stream) {
   if (head_dim != 128) return GDN_ERR_UNSUPPORTED;
   if (!out) return GDN_ERR_INVALID_ARG;
+  // records kept for a backward need a workspace that the caller can hand to it
+  if (opt && (opt->flags & GDN_FLAG_SAVE_FOR_BWD)) return GDN_ERR_INVALID_ARG;
   // the tensors decide the GPU, as for gdn_chunk_fwd
   cudaPointerAttributes attr;
   const void* any = T > 0 ? out : static_cast<const void*>(final_state);

@@ -92,3 +92,30 @@ def run_bwd(p: synth.Problem, options=None):
     out = {k: gr[k].double().cpu().numpy() for k in ("dq", "dk", "dv", "dg", "dbeta")}
     out["dinit"] = None if gr["dinit"] is None else gr["dinit"].double().cpu().numpy()
     return out
+
+
+def run_train(p: synth.Problem, options=None):
+    """Training step through the library: a forward that keeps its records (save_for_backward),
+    then the backward on the same workspace (reuse_forward). Returns (out, final_state, grads) as
+    fp64 numpy arrays."""
+    import dataclasses
+
+    import linear_attention_varlen_gb300 as gdn
+    import torch
+    base = options or gdn.Options()
+    fo = dataclasses.replace(base, save_for_backward=True, reuse_forward=False)
+    bo = dataclasses.replace(base, save_for_backward=False, reuse_forward=True)
+    d = to_device(p)
+    ws = torch.empty(gdn.fwd_workspace_size(p.N, p.T, p.Hk, p.Hv, fo), dtype=torch.uint8, device="cuda")
+    assert ws.numel() == gdn.bwd_workspace_size(p.N, p.T, p.Hk, p.Hv, base)
+    out, fin = gdn.chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"], d["init_idx"],
+                             d["initial_state"], options=fo, workspace=ws)
+    st = gdn.workspace_status(ws)
+    assert st == 0, f"device status {gdn.status_string(st)}"
+    gr = gdn.chunk_bwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"], d["dout"], d.get("dfinal_state"),
+                       d["init_idx"], d["initial_state"], options=bo, workspace=ws)
+    st = gdn.workspace_status(ws)
+    assert st == 0, f"device status {gdn.status_string(st)}"
+    grads = {k: gr[k].double().cpu().numpy() for k in ("dq", "dk", "dv", "dg", "dbeta")}
+    grads["dinit"] = None if gr["dinit"] is None else gr["dinit"].double().cpu().numpy()
+    return bf16_to_f64(out), fin.double().cpu().numpy(), grads

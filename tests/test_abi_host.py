@@ -44,7 +44,7 @@ def test_status_strings(lib):
 def test_default_options(lib):
     o = gdn.COptions()
     lib.gdn_default_options(ctypes.byref(o))
-    assert (o.mode, o.trunc_log_threshold, o.segment_chunks, o.scale, o.reserved) == (0, -10.0, 0, 1.0, 0)
+    assert (o.mode, o.trunc_log_threshold, o.segment_chunks, o.scale, o.flags) == (0, -10.0, 0, 1.0, 0)
     assert o.stage_events is None
 
 
@@ -57,11 +57,11 @@ def test_workspace_size_queries(lib):
     assert gdn.bwd_workspace_size(4, 65536, 2, 8) > 0
 
 
-def _fwd_raw(lib, **kw):
+def _fwd_raw(lib, mode=0, flags=0, **kw):
     args = dict(q=1 << 20, k=1 << 20, v=1 << 20, g=1 << 20, beta=1 << 20, cu=1 << 20, N=1, T=64, Hk=1, Hv=1, D=128,
                 init=None, h0=None, n_init=0, out=1 << 20, fin=1 << 20, ws=1 << 20, ws_bytes=1 << 30)
     args.update(kw)
-    o = gdn.COptions(0, -10.0, 0, 1.0, 0, None)
+    o = gdn.COptions(mode, -10.0, 0, 1.0, flags, None)
     P = ctypes.c_void_p
     return lib.gdn_chunk_fwd(P(args["q"]), P(args["k"]), P(args["v"]), P(args["g"]), P(args["beta"]), P(args["cu"]),
                              args["N"], args["T"], args["Hk"], args["Hv"], args["D"], P(args["init"]), P(args["h0"]),
@@ -80,6 +80,39 @@ def test_host_argument_checks(lib):
     assert _fwd_raw(lib, q=(1 << 20) + 8) == gdn.GDN_ERR_INVALID_ARG      # 16-byte alignment
     assert _fwd_raw(lib, ws=(1 << 20) + 128) == gdn.GDN_ERR_INVALID_ARG   # 256-byte workspace alignment
     assert _fwd_raw(lib, T=-1) == gdn.GDN_ERR_INVALID_ARG
+
+
+def _bwd_raw(lib, flags=0):
+    P, a = ctypes.c_void_p, 1 << 20
+    o = gdn.COptions(0, -10.0, 0, 1.0, flags, None)
+    return lib.gdn_chunk_bwd(P(a), P(a), P(a), P(a), P(a), P(a), 1, 64, 1, 1, 128, None, None, 0, P(a), None,
+                             P(a), P(a), P(a), P(a), P(a), None, P(a), 1 << 30, ctypes.byref(o), None)
+
+
+def test_training_flags_host_checks(lib):
+    # rejected before the library touches the GPU
+    assert _fwd_raw(lib, flags=gdn.FLAG_REUSE_FWD) == gdn.GDN_ERR_INVALID_ARG       # a backward flag
+    assert _fwd_raw(lib, flags=gdn.FLAG_SAVE_FOR_BWD, mode=1) == gdn.GDN_ERR_INVALID_ARG  # exact mode only
+    assert _fwd_raw(lib, flags=4) == gdn.GDN_ERR_INVALID_ARG                         # unknown bit
+    assert _bwd_raw(lib, flags=gdn.FLAG_SAVE_FOR_BWD) == gdn.GDN_ERR_INVALID_ARG     # a forward flag
+    assert _bwd_raw(lib, flags=8) == gdn.GDN_ERR_INVALID_ARG
+    # a forward that keeps its records needs the backward's workspace
+    save = gdn.Options(save_for_backward=True)
+    for N, T, Hk, Hv in [(1, 512, 2, 2), (1, 32768, 2, 8), (12, 16384, 2, 8)]:
+        assert gdn.fwd_workspace_size(N, T, Hk, Hv, save) == gdn.bwd_workspace_size(N, T, Hk, Hv)
+        assert gdn.fwd_workspace_size(N, T, Hk, Hv, save) > gdn.fwd_workspace_size(N, T, Hk, Hv)
+    P = ctypes.c_void_p
+    o = gdn.COptions(0, -10.0, 0, 1.0, gdn.FLAG_SAVE_FOR_BWD, None)
+    assert lib.gdn_chunk_fwd_noalloc(P(1 << 20), P(1 << 20), P(1 << 20), P(1 << 20), P(1 << 20), P(1 << 20), 1, 64, 1,
+                                     1, 128, None, None, 0, P(1 << 20), P(1 << 20), ctypes.byref(o),
+                                     None) == gdn.GDN_ERR_INVALID_ARG
+
+
+def test_reuse_needs_the_forward_workspace():
+    torch = pytest.importorskip("torch")
+    with pytest.raises(ValueError):
+        z = torch.zeros(1)
+        gdn.chunk_bwd(z, z, z, z, z, z, z, options=gdn.Options(reuse_forward=True))
 
 
 # ----------------------------------------------------------------------------- planner
