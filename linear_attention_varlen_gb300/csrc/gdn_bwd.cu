@@ -622,6 +622,9 @@ __global__ void __launch_bounds__(kRevThreads, 1) rev_chain_kernel(const __grid_
   const int32_t* slot = reinterpret_cast<const int32_t*>(p.ws + p.L.f.seg_slot);
   const int* mzero = reinterpret_cast<const int*>(p.ws + p.L.f.mzero);
   const float* mmat = reinterpret_cast<const float*>(p.ws + p.L.f.mmat);
+  const float* gam_ws = reinterpret_cast<const float*>(p.ws + p.L.f.gam);
+  const int32_t* contr = reinterpret_cast<const int32_t*>(p.ws + p.L.f.contr);
+  const int32_t* dch = reinterpret_cast<const int32_t*>(p.ws + p.L.f.seq_chunk0);
   float* ds0 = reinterpret_cast<float*>(p.ws + p.L.ds0);
   float* rpub = reinterpret_cast<float*>(p.ws + p.L.rpub);
   float* rb = reinterpret_cast<float*>(p.ws + p.L.rb);
@@ -680,8 +683,11 @@ __global__ void __launch_bounds__(kRevThreads, 1) rev_chain_kernel(const __grid_
     const int seq = si[4 * s], c0 = si[4 * s + 1], nch = si[4 * s + 2];
     const int first = seq_seg0[seq], last = seq_seg0[seq + 1] - 1;
     bool ok = true;
+    // exact split, reversed: the previous segment's item needs this segment's start gradient only
+    // when it cannot warm up over this segment's first chunks; this item warms up the same way
+    const bool prev_warms = s > first && warm_fwd(gam_ws, contr, Hv, h, c0, dch[seq + 1]) >= 0;
     if (kPass == 1) {
-      if (first == last || s == first) continue;  // nothing to precompute
+      if (first == last || s == first || prev_warms) continue;  // nothing to precompute
       if (s < last) {
         if (epi)
           for (int c = 0; c < 64; ++c) dS[c] = 0.f;
@@ -699,13 +705,21 @@ __global__ void __launch_bounds__(kRevThreads, 1) rev_chain_kernel(const __grid_
       continue;
     }
     // ----------------------------------------------------------------- pass 2
-    if (first < s && s < last && !mzero[slot[s] * Hv + h]) {  // early publication below
+    const bool pub_prev = first < s && s < last && !prev_warms && !mzero[slot[s] * Hv + h];
+    if (pub_prev) {  // early publication below
       const size_t o = ((size_t)slot[s] * Hv + h) * st;
       prefetch_state_l2(mmat + o, cx.tid);
       prefetch_state_l2(rb + o, cx.tid);
     }
+    const int wf = s < last ? warm_fwd(gam_ws, contr, Hv, h, c0 + nch, dch[seq + 1]) : -1;
     if (s == last) {
       ok = doc_end_grad(seq, h);
+    } else if (wf >= 0) {
+      // the decay over chunks [c0 + nch, wf) leaves the later gradient below fp32 resolution:
+      // warm up from zero over them
+      if (epi)
+        for (int c = 0; c < 64; ++c) dS[c] = 0.f;
+      ok = run(c0 + nch, wf - (c0 + nch), h, hk, false);
     } else if (s + 1 != last && mzero[slot[s + 1] * Hv + h]) {
       if (epi) rev_load(cx, rb + ((size_t)slot[s + 1] * Hv + h) * st, dS, false);  // M_{s+1} = 0: no wait
     } else {
@@ -713,7 +727,7 @@ __global__ void __launch_bounds__(kRevThreads, 1) rev_chain_kernel(const __grid_
       if (ok && epi) rev_load(cx, rpub + ((size_t)slot[s] * Hv + h) * st, dS, false);
     }
     if (!ok) break;
-    if (first < s && s < last && !mzero[slot[s] * Hv + h]) {
+    if (pub_prev) {
       // early publication of this segment's start gradient
       if (epi) rev_store_ds(cx, sm, dS);
       sync_generic_to_async();
@@ -728,7 +742,7 @@ __global__ void __launch_bounds__(kRevThreads, 1) rev_chain_kernel(const __grid_
       set_status(hd, kErrTimeout);
       break;
     }
-    if (first < s && s == last && doc_has_forks(p, seq)) {
+    if (first < s && s == last && !prev_warms && doc_has_forks(p, seq)) {
       if (epi) rev_save(cx, rpub + ((size_t)slot[s - 1] * Hv + h) * st, dS);
       rev_publish(&rflags[s * Hv + h]);
     }

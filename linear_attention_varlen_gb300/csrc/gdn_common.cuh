@@ -76,7 +76,7 @@ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // Forward workspace layout (byte offsets from the workspace base).
 struct FwdLayout {
   size_t header, seq_chunk0, seq_seg0, chunk_seq, chunk_tok0, chunk_len, seg_info, seg_slot, p1_list;
-  size_t flags_seg, flags_fin, mzero, gam, tw, tu, pimg, pub, mmat, bmat, total;
+  size_t flags_seg, flags_fin, mzero, gam, contr, tw, tu, pimg, pub, mmat, bmat, total;
   int64_t cmax, smax, slots;
 };
 
@@ -105,6 +105,7 @@ inline FwdLayout fwd_layout(const PlanDims& d) {
   L.flags_fin = take(sizeof(int32_t) * (size_t)(d.N + 1) * d.Hv);
   L.mzero = take(sizeof(int32_t) * ((size_t)L.slots * d.Hv + 1));
   L.gam = take(sizeof(float) * (size_t)L.cmax * d.Hv * kChunk);
+  L.contr = take(sizeof(int32_t) * (size_t)L.cmax * d.Hv);
   L.tw = take((size_t)L.cmax * d.Hv * kChunk * kChunk * 2);
   L.tu = take((size_t)L.cmax * d.Hv * kChunk * kChunk * 2);
   L.pimg = take((size_t)L.cmax * d.Hv * kChunk * kChunk * 2);

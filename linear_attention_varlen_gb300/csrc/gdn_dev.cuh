@@ -49,6 +49,53 @@ __device__ __forceinline__ bool wait_all(uint64_t* bar, uint32_t parity) {
   return true;
 }
 
+// Exact split: a segment boundary needs no published state when the decay between the state it
+// neglects and the chunk it starts at is below fp32 resolution. Per token the transition is
+// e^{g_t} (I - beta_t k_t k_t^T), whose spectral norm is at most e^{g_t} while
+// 0 <= beta_t |k_t|^2 <= 2 (the chunk's flag in `contr`, written by kkt_solve). Over a window
+// whose summed log-decay is below kExactCut the neglected term is therefore below
+// e^{-120} (about 2^-173) times the norm of the state it neglects: the chain can start from zero
+// at the window's far end (a warm-up) instead of waiting for the neighbouring segment.
+constexpr float kExactCut = -120.f;
+constexpr int kWarmCap = 32;  // longest warm-up window, chunks: one per lane of the warp that evaluates it
+
+// One warp evaluates a window in one round trip: lane i takes chunk `first + step * i`, an
+// inclusive prefix sum of the chunks' log-decays gives the window ending at lane i, and the window
+// is the shortest one below kExactCut whose chunks all lie in [lo, hi) and contract. Every lane
+// returns the same value; call with the whole warp (the chain kernels call it with all threads).
+__device__ __forceinline__ int warm_window(const float* gam, const int32_t* contr, int Hv, int h, int first, int step,
+                                           int lo, int hi) {
+  const int lane = threadIdx.x & 31;
+  const int w = first + step * lane;
+  const bool in = w >= lo && w < hi;
+  float acc = in ? __ldg(gam + ((size_t)w * Hv + h) * kChunk + kChunk - 1) : 0.f;
+  const bool good = in && __ldg(contr + (size_t)w * Hv + h) != 0;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float t = __shfl_up_sync(0xffffffffu, acc, o);
+    if (lane >= o) acc += t;
+  }
+  const unsigned bad = __ballot_sync(0xffffffffu, !good);
+  const unsigned hit = __ballot_sync(0xffffffffu, good && acc < kExactCut);
+  if (!hit) return -1;
+  const int i = __ffs(hit) - 1;
+  const unsigned upto = (i == 31) ? 0xffffffffu : ((1u << (i + 1)) - 1u);
+  return (bad & upto) ? -1 : w - step * lane + step * i;
+}
+
+// Backward-looking window for a forward chain that starts at chunk c (document chunks from dc0):
+// the first chunk of the warm-up, or -1 when no window of at most kWarmCap chunks qualifies.
+__device__ __forceinline__ int warm_back(const float* gam, const int32_t* contr, int Hv, int h, int c, int dc0) {
+  return warm_window(gam, contr, Hv, h, c - 1, -1, dc0, c);
+}
+
+// Forward-looking window for a reverse chain that ends at chunk c (exclusive; document chunks up
+// to dcn): one past the last chunk of the warm-up, or -1.
+__device__ __forceinline__ int warm_fwd(const float* gam, const int32_t* contr, int Hv, int h, int c, int dcn) {
+  const int w = warm_window(gam, contr, Hv, h, c, 1, c, dcn);
+  return w < 0 ? -1 : w + 1;
+}
+
 template <class T, class P>
 __device__ __forceinline__ T* ws_ptr(const P& p, size_t off) {
   return reinterpret_cast<T*>(p.ws + off);

@@ -193,6 +193,7 @@ struct KktSmem {
   float beta[kKktHeads][64];
   float eg[kKktHeads][64];               // e^{gamma}
   float egi[kKktHeads][64];              // e^{-gamma} (factored path only)
+  int contr[kKktHeads][2];               // per warp of a group: every token has 0 <= beta |k|^2 <= 2
 };
 
 // Named barrier of one 64-thread value-head group (ids 1-4; literal ids keep the count of
@@ -312,7 +313,12 @@ __global__ void __launch_bounds__(256) kkt_solve_kernel(const __grid_constant__ 
         }
         gam[t] = sc;
         bet[t] = bi;
+        // contraction check of the chunk's token transitions (padding rows have beta = 0)
+        const float bk = bi * sm.kk[t][t];
+        const int all_ok = __all_sync(0xffffffffu, bk >= 0.f && bk <= 2.f);
+        if (lane == 0) sm.contr[grp][sub] = all_ok;
         group_sync(grp);
+        if (t == 0) ws_ptr<int32_t>(p, p.L.contr)[rec] = (sm.contr[grp][0] && sm.contr[grp][1]) ? 1 : 0;
         if (t >= 32) sc += gam[31];
         gam_ws[rec * 64 + t] = sc;
         eg[t] = __expf(sc);
@@ -1272,6 +1278,8 @@ __global__ void __launch_bounds__(kWsThreads, 1) chain_kernel(const __grid_const
   const int32_t* slot = ws_ptr<int32_t>(p, p.L.seg_slot);
   const int32_t* seq_seg0 = ws_ptr<int32_t>(p, p.L.seq_seg0);
   int* flags_seg = ws_ptr<int>(p, p.L.flags_seg);
+  const float* gam_ws = ws_ptr<float>(p, p.L.gam);
+  const int32_t* contr = ws_ptr<int32_t>(p, p.L.contr);
   int* flags_fin = ws_ptr<int>(p, p.L.flags_fin);
   int* mzero = ws_ptr<int>(p, p.L.mzero);
   const size_t st_elems = (size_t)kDim * kDim;
@@ -1341,6 +1349,18 @@ __global__ void __launch_bounds__(kWsThreads, 1) chain_kernel(const __grid_const
       const int s = p1[2 * unit], part = p1[2 * unit + 1];
       const int seq = si[4 * s], c0 = si[4 * s + 1], nch = si[4 * s + 2];
       const int sl = slot[s];
+      // The unit serves the next segment's start, unless that segment warms up; the transition also
+      // serves the reverse chain's publication of this segment's start gradient (record mode).
+      {
+        const int32_t* dch = ws_ptr<int32_t>(p, p.L.seq_chunk0);
+        const bool next_warms = warm_back(gam_ws, contr, Hv, h, c0 + nch, dch[seq]) >= 0;
+        const bool rev_needs_m =
+            rec && part == 0 && s != seq_seg0[seq] && warm_fwd(gam_ws, contr, Hv, h, c0, dch[seq + 1]) < 0;
+        if (next_warms && !rev_needs_m) {
+          __syncthreads();  // every thread has read s_item before the next ticket
+          continue;
+        }
+      }
       float* mdst = ws_ptr<float>(p, p.L.mmat) + ((size_t)sl * Hv + h) * st_elems;
       bool m_zero = false;
       if (part == 0) {
@@ -1396,9 +1416,15 @@ __global__ void __launch_bounds__(kWsThreads, 1) chain_kernel(const __grid_const
     const int s = item / Hv;
     const int seq = si[4 * s], c0 = si[4 * s + 1], nch = si[4 * s + 2], dep = si[4 * s + 3];
     const bool last = (s + 1 == seq_seg0[seq + 1]);
-    int first_chunk = c0;  // truncation mode may start earlier (warmup)
+    int first_chunk = c0;  // a warm-up may start earlier
     bool have_start = true;
-    if (p.d.mode == 0 && slot[s] >= 0 && dep != -1) {  // this item publishes its end state early
+    // exact split: this segment warms up instead of waiting, and the next one needs this item's
+    // published end state only when it cannot warm up itself
+    const int32_t* dch = ws_ptr<int32_t>(p, p.L.seq_chunk0);
+    const int wb = (p.d.mode == 0 && dep >= 0) ? warm_back(gam_ws, contr, Hv, h, c0, dch[seq]) : -1;
+    const bool pub_next = p.d.mode == 0 && slot[s] >= 0 && dep != -1 &&
+                          warm_back(gam_ws, contr, Hv, h, c0 + nch, dch[seq]) < 0;
+    if (pub_next) {  // this item publishes its end state early
       const size_t off = ((size_t)slot[s] * Hv + h) * st_elems;
       prefetch_state_l2(ws_ptr<float>(p, p.L.mmat) + off, cx.tid, blockDim.x);
       prefetch_state_l2(ws_ptr<float>(p, p.L.bmat) + off, cx.tid, blockDim.x);
@@ -1420,7 +1446,11 @@ __global__ void __launch_bounds__(kWsThreads, 1) chain_kernel(const __grid_const
       if (have_start && epi) load_state(cx, p.final_state + ((size_t)j * Hv + h) * st_elems, S, true);
     } else if (p.d.mode == 0) {
       const int dsl = slot[dep];
-      if (__ldcg(&mzero[dsl * Hv + h])) {
+      if (wb >= 0) {
+        // the decay since chunk wb leaves the earlier state below fp32 resolution: warm up from zero
+        first_chunk = wb;
+        set_zero();
+      } else if (__ldcg(&mzero[dsl * Hv + h])) {
         // the previous segment's transition is exactly zero: its end state is its local B
         if (epi) load_state(cx, ws_ptr<float>(p, p.L.bmat) + ((size_t)dsl * Hv + h) * st_elems, S, true);
       } else {
@@ -1469,7 +1499,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) chain_kernel(const __grid_const
     store_s();
     sync_generic_to_async();
     // early publication of this segment's end state (exact split), unless its transition is zero
-    if (p.d.mode == 0 && slot[s] >= 0 && dep != -1 && !__ldcg(&mzero[slot[s] * Hv + h])) {
+    if (pub_next && !__ldcg(&mzero[slot[s] * Hv + h])) {
       const size_t off = ((size_t)slot[s] * Hv + h) * st_elems;
       if (!affine(ws_ptr<float>(p, p.L.mmat) + off, ws_ptr<float>(p, p.L.bmat) + off, ws_ptr<float>(p, p.L.pub) + off)) {
         set_status(hd, kErrTimeout);
