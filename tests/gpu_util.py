@@ -119,3 +119,24 @@ def run_train(p: synth.Problem, options=None):
     grads = {k: gr[k].double().cpu().numpy() for k in ("dq", "dk", "dv", "dg", "dbeta")}
     grads["dinit"] = None if gr["dinit"] is None else gr["dinit"].double().cpu().numpy()
     return bf16_to_f64(out), fin.double().cpu().numpy(), grads
+
+
+def mixed_decay_problem(name, seed, nchunks=30, Hk=1, Hv=2, with_dout=False, beta_boost=None):
+    """One document whose gates change regime along it: slow decay (u ~ N(6, 1)) in its first
+    third, fast (u ~ N(-3, 1)) in the second, the workloads' (u ~ N(2, 1)) in the last. With
+    beta_boost, beta in the middle third is multiplied by it, so that beta |k|^2 exceeds 2 there:
+    chunks whose token transitions do not contract."""
+    T = 64 * nchunks + 5
+    p = synth.make_problem(name, seed, [T], Hk, Hv, with_dout=with_dout, g_mean=6.0)
+    fast = synth.make_problem(name, seed + 1, [T], Hk, Hv, g_mean=-3.0)
+    mid = synth.make_problem(name, seed + 2, [T], Hk, Hv, g_mean=2.0)
+    a, b = T // 3, 2 * T // 3
+    g = p.g.copy()
+    g[a:b] = fast.g[a:b]
+    g[b:] = mid.g[b:]
+    p.g = g.astype(np.float32)
+    if beta_boost:
+        beta = p.beta.copy()
+        beta[a:b] *= beta_boost
+        p.beta = beta.astype(np.float32)
+    return p

@@ -6,7 +6,7 @@ import pytest
 
 import oracle
 import synth
-from tests.gpu_util import assert_close, errors, run_bwd
+from tests.gpu_util import assert_close, errors, mixed_decay_problem, run_bwd
 
 pytestmark = pytest.mark.gpu
 
@@ -119,6 +119,13 @@ def test_bwd_split_zero_transitions():
     takes the local start gradient without waiting for the next segment."""
     p = synth.make_problem("bwd_fast_decay", 351, [64 * 12 + 17, 64 * 9], 1, 2, with_dout=True, g_mean=-3.0)
     check_bwd(p, gdn.Options(segment_chunks=2))
+
+
+@pytest.mark.parametrize("boost", [None, 3.0])
+def test_bwd_split_mixed_decay(boost):
+    """Reverse split over regimes that warm up and regimes that wait for a publication."""
+    p = mixed_decay_problem(f"bwd_mixed_b{boost}", 360, with_dout=True, beta_boost=boost)
+    check_bwd(p, gdn.Options(segment_chunks=3), stress=True)
 
 
 def test_bwd_ignores_truncation_mode():

@@ -8,7 +8,7 @@ import pytest
 import oracle
 import synth
 from tests import chunked_ref as cr
-from tests.gpu_util import assert_close, errors, head_slice, run_fwd, to_device
+from tests.gpu_util import assert_close, errors, head_slice, mixed_decay_problem, run_fwd, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -75,6 +75,15 @@ def test_exact_split_forced_segments(seg, g_mean):
     """Slow decay (g_mean = 6, about -0.0025 per token) makes the carried state matter."""
     p = synth.make_problem(f"split_s{seg}_g{g_mean}", 120 + seg, [64 * 23 + 17], 2, 4, g_mean=g_mean)
     check_problem(p, gdn.Options(segment_chunks=seg))
+
+
+@pytest.mark.parametrize("boost", [None, 3.0])
+def test_exact_split_mixed_decay(boost):
+    """Segment boundaries in slow-decay stretches take the published state, those after fast
+    decay warm up from zero; with boost, the fast stretch's chunks do not contract and its
+    boundaries take the published state too."""
+    p = mixed_decay_problem(f"split_mixed_b{boost}", 150, beta_boost=boost)
+    check_problem(p, gdn.Options(segment_chunks=3))
 
 
 def test_exact_split_with_initial_state_and_fork():

@@ -8,7 +8,7 @@ import pytest
 
 import oracle
 import synth
-from tests.gpu_util import assert_close, errors, run_bwd, run_train
+from tests.gpu_util import assert_close, errors, mixed_decay_problem, run_bwd, run_train
 
 pytestmark = pytest.mark.gpu
 
@@ -88,6 +88,16 @@ def test_train_gradients_equal_recompute(seg):
     p = synth.make_problem(f"train_eq{seg}", 440 + seg, [64 * 10 + 5, 64 * 7, 300], 2, 4, init_idx=[-1, 0, 0],
                            with_dout=True)
     opts = gdn.Options(segment_chunks=seg)
+    _, _, a = run_train(p, opts)
+    b = run_bwd(p, opts)
+    for key in KEYS:
+        np.testing.assert_array_equal(a[key], b[key])
+
+
+def test_train_split_mixed_decay_equals_recompute():
+    p = mixed_decay_problem("train_mixed", 460, with_dout=True, beta_boost=3.0)
+    opts = gdn.Options(segment_chunks=3)
+    check_train(p, opts, stress=True)
     _, _, a = run_train(p, opts)
     b = run_bwd(p, opts)
     for key in KEYS:
