@@ -113,6 +113,18 @@ __device__ __forceinline__ void bulk_store(void* dst, const void* src, uint32_t 
 }
 
 // Ask for the 128-byte line holding p to be brought into L2.
+// Bring a tiled TMA box (3-D map, same coordinates as a load) into L2 ahead of its load.
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
+}
+// Bring `bytes` (16-byte aligned address, multiple of 16) of global memory into L2.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)), "r"(bytes)
+               : "memory");
+}
 __device__ __forceinline__ void prefetch_l2(const void* p) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(p)));
 }
@@ -177,6 +189,34 @@ __device__ __forceinline__ float quad_sum(float x) {
   return x;
 }
 // Byte offset of the bf16 pair (row r, columns c, c + 1; c even) in a 64-column SW128 block.
+// 4 x 4 transpose across the four lanes of a group (qa = lane & 3): lane qa's x[m] becomes the
+// x[qa] of lane m. Two exchange rounds (lane ^ 1, lane ^ 2) of two shuffles each.
+__device__ __forceinline__ void quad_transpose4(uint32_t* x, int qa) {
+  {
+    const bool o = qa & 1;
+    const uint32_t r0 = __shfl_xor_sync(0xffffffffu, o ? x[0] : x[1], 1);
+    const uint32_t r1 = __shfl_xor_sync(0xffffffffu, o ? x[2] : x[3], 1);
+    if (o) {
+      x[0] = r0;
+      x[2] = r1;
+    } else {
+      x[1] = r0;
+      x[3] = r1;
+    }
+  }
+  {
+    const bool o = qa & 2;
+    const uint32_t r0 = __shfl_xor_sync(0xffffffffu, o ? x[0] : x[2], 2);
+    const uint32_t r1 = __shfl_xor_sync(0xffffffffu, o ? x[1] : x[3], 2);
+    if (o) {
+      x[0] = r0;
+      x[1] = r1;
+    } else {
+      x[2] = r0;
+      x[3] = r1;
+    }
+  }
+}
 __device__ __forceinline__ uint32_t sw128_pair(int r, int c) {
   return r * 128 + ((((c >> 3) ^ r) & 7) << 4) + ((c & 7) << 1);
 }
@@ -233,6 +273,13 @@ __host__ __device__ __forceinline__ uint32_t sw128_off(uint32_t row, uint32_t co
 __device__ __forceinline__ uint64_t kmajor_desc(uint32_t base, uint32_t kblk_stride, int ks) {
   return sdesc_sw128(base + (uint32_t)(ks >> 2) * kblk_stride + (uint32_t)(ks & 3) * 32u, 16u, 1024u);
 }
+// Descriptor of k-step ks from that of k-step 0 (no address arithmetic in the issue loop): the
+// start-address field holds bits 4-17 of the address, and every operand lies below 256 KB of
+// shared memory, so adding the step's offset never carries out of the field.
+__device__ __forceinline__ uint64_t kmajor_step(uint64_t d0, uint32_t kblk_stride, int ks) {
+  return d0 + (((uint32_t)(ks >> 2) * kblk_stride + (uint32_t)(ks & 3) * 32u) >> 4);
+}
+__device__ __forceinline__ uint64_t mnmajor_step(uint64_t d0, int ks) { return d0 + (uint64_t)ks * (2048u >> 4); }
 // MN-major operand: rows = K index (128 bytes per row = 64 MN elements), MN blocks of 64
 // elements `mn_stride` bytes apart. Descriptor for k-step ks (16 rows of K each).
 __device__ __forceinline__ uint64_t mnmajor_desc(uint32_t base, uint32_t mn_stride, int ks) {

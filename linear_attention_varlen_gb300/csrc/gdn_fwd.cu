@@ -662,10 +662,10 @@ __device__ __forceinline__ AffineBufs affine_bufs(WsSmem& sm) {
 }
 
 struct WsBars {
-  uint64_t full[2], fullq, fullu, empty[2], emptyq, a_done, pre_done, b_done, epi1, staged, epi2, vfree;
+  uint64_t full[3], fullq, fullu, empty[3], emptyq, a_done, pre_done, b_done, epi1, staged, epi2, vfree;
 };
 struct WsPhase {
-  uint32_t full[2], fullq, fullu, empty[2], emptyq, a_done, pre_done, b_done, epi1, staged, epi2, vfree;
+  uint32_t full[3], fullq, fullu, empty[3], emptyq, a_done, pre_done, b_done, epi1, staged, epi2, vfree;
 };
 // TMEM columns of D1 for chunk j: two accumulators in turn, so that the output of chunk j is
 // read while chunk j + 1 already runs (columns 384-511 hold Q K^T only in the record path).
@@ -960,7 +960,7 @@ __device__ bool run_ws(const FwdParams& p, ChainCtx& cx, WsBars& bb, WsPhase& ph
 // operands (x = hi + lo for T_w, T_u, W, S and V'_s; K and V are exact in bf16), optionally
 // writing the per-chunk records that the gradient kernels read (chunk-start S hi / lo and V'
 // hi / lo as 128B-swizzled images). No output. Roles in one CTA of 10 warps:
-//   warp 8      TMA producer: K and gamma of chunk j into stage j & 1; T_w hi / lo (one buffer,
+//   warp 8      TMA producer: K and gamma of chunk j into stage j % 3; T_w hi / lo (one buffer,
 //               released by the W product); V and T_u hi / lo (one buffer, released by the U
 //               product).
 //   warp 9      MMA issuer, per chunk j: D_V = T_u V - W S (M = 64; W S as W hi S hi + W hi S lo +
@@ -969,8 +969,9 @@ __device__ bool run_ws(const FwdParams& p, ChainCtx& cx, WsBars& bb, WsPhase& ph
 //   warps 0-7   epilogue: -W hi / lo staging, V' (records, V'_s hi / lo), S = e^{gamma_C} S + D2
 //               with its hi / lo staging. A chunk-start state reaches its record by bulk store
 //               straight from the staged images.
+constexpr int kRecStages = 3;  // K is loaded up to two chunks ahead
 struct RecSmem {
-  uint8_t k[2][16384];    // [stage] K rows t, two dk blocks (B MN-major for W, A MN-major for K^T V'_s)
+  uint8_t k[kRecStages][16384];  // [stage] K rows t, two dk blocks (B MN-major for W, A MN-major for K^T V'_s)
   uint8_t v[16384];       // V rows t, two dv blocks (B MN-major)
   uint8_t tu[2][8192];    // T diag(beta) hi, lo (A K-major, M = 64)
   uint8_t tw[2][8192];    // T diag(beta e^gamma) hi, lo (A K-major, M = 64)
@@ -979,7 +980,7 @@ struct RecSmem {
   uint8_t slo[2][16384];  // S lo
   uint8_t vs[2][8192];    // V'_s = diag(e^{gamma_C - gamma}) V' hi, two dv blocks (B MN-major)
   uint8_t vslo[2][8192];  // V'_s lo
-  float gam[2][64];       // [stage] chunk-local cumulative gate
+  float gam[kRecStages][64];  // [stage] chunk-local cumulative gate
 };
 constexpr size_t kSmemBytes = (sizeof(WsSmem) > sizeof(RecSmem) ? sizeof(WsSmem) : sizeof(RecSmem)) + 1024;
 static_assert(kSmemBytes <= 232448, "chain shared memory");
@@ -1024,8 +1025,8 @@ __device__ bool run_ws_rec(const FwdParams& p, ChainCtx& cx, WsBars& bb, WsPhase
     // ------------------------------------------------------------------ TMA producer
     if (cx.lane == 0) {
       for (int j = 0; j < n; ++j) {
-        const int gc = gc0 + j, st = j & 1, tok0 = ctok[gc];
-        if (j >= 2) role_wait(&bb.empty[st], ph.empty[st], abort);
+        const int gc = gc0 + j, st = j % kRecStages, tok0 = ctok[gc];
+        if (j >= kRecStages) role_wait(&bb.empty[st], ph.empty[st], abort);
         if (*abort) break;
         mbar_arrive_expect_tx(&bb.full[st], 16384 + 256);
         tma_load_3d(sm.k[st], &p.tm_k, 0, hk, tok0, &bb.full[st]);
@@ -1047,7 +1048,8 @@ __device__ bool run_ws_rec(const FwdParams& p, ChainCtx& cx, WsBars& bb, WsPhase
         }
       }
       // drain: wait for the release of the last uses so that every phase is consumed
-      for (int j = (n >= 2 ? n - 2 : 0); j < n; ++j) role_wait(&bb.empty[j & 1], ph.empty[j & 1], abort);
+      for (int j = (n >= kRecStages ? n - kRecStages : 0); j < n; ++j)
+        role_wait(&bb.empty[j % kRecStages], ph.empty[j % kRecStages], abort);
       role_wait(&bb.emptyq, ph.emptyq, abort);
       if (kWithU) role_wait(&bb.vfree, ph.vfree, abort);
     }
@@ -1058,12 +1060,23 @@ __device__ bool run_ws_rec(const FwdParams& p, ChainCtx& cx, WsBars& bb, WsPhase
     if (cx.lane == 0) {
       const uint32_t tm = cx.tmem;
       constexpr uint32_t i64 = idesc_bf16(64, 128, 0, 1);
+      // k-step-0 descriptors of every operand (the buffers do not move)
+      const uint64_t d_tw[2] = {kmajor_desc(smem_u32(sm.tw[0]), 8192, 0), kmajor_desc(smem_u32(sm.tw[1]), 8192, 0)};
+      const uint64_t d_tu[2] = {kmajor_desc(smem_u32(sm.tu[0]), 8192, 0), kmajor_desc(smem_u32(sm.tu[1]), 8192, 0)};
+      const uint64_t d_wn[2] = {kmajor_desc(smem_u32(sm.wn[0]), 8192, 0), kmajor_desc(smem_u32(sm.wn[1]), 8192, 0)};
+      const uint64_t d_kb[kRecStages] = {mnmajor_desc(smem_u32(sm.k[0]), 8192, 0), mnmajor_desc(smem_u32(sm.k[1]), 8192, 0),
+                                         mnmajor_desc(smem_u32(sm.k[2]), 8192, 0)};
+      const uint64_t d_v = mnmajor_desc(smem_u32(sm.v), 8192, 0);
+      const uint64_t d_s = mnmajor_desc(smem_u32(sm.s[0]), 16384, 0);
+      const uint64_t d_slo = mnmajor_desc(smem_u32(sm.slo[0]), 16384, 0);
+      const uint64_t d_vs[2] = {mnmajor_desc(smem_u32(sm.vs[0]), 8192, 0), mnmajor_desc(smem_u32(sm.vslo[0]), 8192, 0)};
+      constexpr uint32_t i128 = idesc_bf16(128, 128, 1, 1);
       auto prep = [&](int j) {
-        const uint32_t k0 = smem_u32(sm.k[j & 1]);
-        for (int ks = 0; ks < 4; ++ks)
-          umma_bf16(tm + kRtW, kmajor_desc(smem_u32(sm.tw[0]), 8192, ks), mnmajor_desc(k0, 8192, ks), i64, ks > 0);
-        for (int ks = 0; ks < 4; ++ks)
-          umma_bf16(tm + kRtW, kmajor_desc(smem_u32(sm.tw[1]), 8192, ks), mnmajor_desc(k0, 8192, ks), i64, 1);
+        const uint64_t kb = d_kb[j % kRecStages];
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) umma_bf16(tm + kRtW, kmajor_step(d_tw[0], 8192, ks), mnmajor_step(kb, ks), i64, ks > 0);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) umma_bf16(tm + kRtW, kmajor_step(d_tw[1], 8192, ks), mnmajor_step(kb, ks), i64, 1);
         umma_commit(&bb.pre_done);
         umma_commit(&bb.emptyq);
       };
@@ -1071,42 +1084,40 @@ __device__ bool run_ws_rec(const FwdParams& p, ChainCtx& cx, WsBars& bb, WsPhase
       role_wait(&bb.fullq, ph.fullq, abort);
       if (!*abort) prep(0);
       for (int j = 0; j < n && !*abort; ++j) {
-        const int st = j & 1;
+        const int st = j % kRecStages, st1 = (j + 1) % kRecStages;
         role_wait(&bb.staged, ph.staged, abort);
         role_wait(&bb.epi2, ph.epi2, abort);
         if (kWithU) role_wait(&bb.fullu, ph.fullu, abort);
         if (*abort) break;
         const uint32_t dv = tm + kRtV;
         if (kWithU) {
-          for (int ks = 0; ks < 4; ++ks)
-            umma_bf16(dv, kmajor_desc(smem_u32(sm.tu[0]), 8192, ks), mnmajor_desc(smem_u32(sm.v), 8192, ks), i64, ks > 0);
-          for (int ks = 0; ks < 4; ++ks)
-            umma_bf16(dv, kmajor_desc(smem_u32(sm.tu[1]), 8192, ks), mnmajor_desc(smem_u32(sm.v), 8192, ks), i64, 1);
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks) umma_bf16(dv, kmajor_step(d_tu[0], 8192, ks), mnmajor_step(d_v, ks), i64, ks > 0);
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks) umma_bf16(dv, kmajor_step(d_tu[1], 8192, ks), mnmajor_step(d_v, ks), i64, 1);
         }
+#pragma unroll
         for (int ks = 0; ks < 8; ++ks)
-          umma_bf16(dv, kmajor_desc(smem_u32(sm.wn[0]), 8192, ks), mnmajor_desc(smem_u32(sm.s[0]), 16384, ks), i64,
-                    (kWithU || ks > 0) ? 1 : 0);
-        for (int ks = 0; ks < 8; ++ks)
-          umma_bf16(dv, kmajor_desc(smem_u32(sm.wn[0]), 8192, ks), mnmajor_desc(smem_u32(sm.slo[0]), 16384, ks), i64, 1);
-        for (int ks = 0; ks < 8; ++ks)
-          umma_bf16(dv, kmajor_desc(smem_u32(sm.wn[1]), 8192, ks), mnmajor_desc(smem_u32(sm.s[0]), 16384, ks), i64, 1);
+          umma_bf16(dv, kmajor_step(d_wn[0], 8192, ks), mnmajor_step(d_s, ks), i64, (kWithU || ks > 0) ? 1 : 0);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) umma_bf16(dv, kmajor_step(d_wn[0], 8192, ks), mnmajor_step(d_slo, ks), i64, 1);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) umma_bf16(dv, kmajor_step(d_wn[1], 8192, ks), mnmajor_step(d_s, ks), i64, 1);
         umma_commit(&bb.a_done);
         if (kWithU) umma_commit(&bb.vfree);
         if (j + 1 < n) {
-          role_wait(&bb.full[st ^ 1], ph.full[st ^ 1], abort);
+          role_wait(&bb.full[st1], ph.full[st1], abort);
           role_wait(&bb.fullq, ph.fullq, abort);
           if (*abort) break;
           prep(j + 1);
         }
         role_wait(&bb.epi1, ph.epi1, abort);
         if (*abort) break;
-        const uint32_t k0 = smem_u32(sm.k[st]);
-        for (int ks = 0; ks < 4; ++ks)
-          umma_bf16(tm + kRtD2, mnmajor_desc(k0, 8192, ks), mnmajor_desc(smem_u32(sm.vs[0]), 8192, ks),
-                    idesc_bf16(128, 128, 1, 1), ks > 0);
-        for (int ks = 0; ks < 4; ++ks)
-          umma_bf16(tm + kRtD2, mnmajor_desc(k0, 8192, ks), mnmajor_desc(smem_u32(sm.vslo[0]), 8192, ks),
-                    idesc_bf16(128, 128, 1, 1), 1);
+        const uint64_t ka = d_kb[st];
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) umma_bf16(tm + kRtD2, mnmajor_step(ka, ks), mnmajor_step(d_vs[0], ks), i128, ks > 0);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) umma_bf16(tm + kRtD2, mnmajor_step(ka, ks), mnmajor_step(d_vs[1], ks), i128, 1);
         umma_commit(&bb.b_done);
         umma_commit(&bb.empty[st]);
       }
@@ -1126,7 +1137,7 @@ __device__ bool run_ws_rec(const FwdParams& p, ChainCtx& cx, WsBars& bb, WsPhase
   e_handoff(cx.tid, &bb.epi2);  // S(gc0) is staged
   if (kStore && cx.tid == 0) store_s_record(gc0);
   auto staging = [&](int j) {
-    role_wait(&bb.full[j & 1], ph.full[j & 1], abort);
+    role_wait(&bb.full[j % kRecStages], ph.full[j % kRecStages], abort);
     role_wait(&bb.pre_done, ph.pre_done, abort);
 #pragma unroll
     for (int hc = 0; hc < 2; ++hc) {
@@ -1150,7 +1161,7 @@ __device__ bool run_ws_rec(const FwdParams& p, ChainCtx& cx, WsBars& bb, WsPhase
   };
   staging(0);
   for (int j = 0; j < n; ++j) {
-    const int gc = gc0 + j, st = j & 1;
+    const int gc = gc0 + j, st = j % kRecStages;
     role_wait(&bb.a_done, ph.a_done, abort);
     const float* gm = sm.gam[st];
     const float gC = gm[63];
@@ -1160,11 +1171,13 @@ __device__ bool run_ws_rec(const FwdParams& p, ChainCtx& cx, WsBars& bb, WsPhase
       const float sc[2] = {__expf(gC - gm[r0]), __expf(gC - gm[r0 + 8])};
       uint8_t* vph = kStore ? p.vp_img + rec(gc) * 16384 + cx.half * 8192 : nullptr;
       uint8_t* vpl = kStore ? p.vp_lo_img + rec(gc) * 16384 + cx.half * 8192 : nullptr;
+      const int qa = cx.lane & 3;
 #pragma unroll
       for (int hc = 0; hc < 2; ++hc) {
         float v[16];
         tmem_ld16x256_x4(cx.tmem + kRtV + lane_base + 64 * cx.half + 32 * hc, v);
         tmem_ld_wait();
+        uint32_t rh[2][4], rl[2][4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const int c = 32 * hc + 8 * k + c2;
@@ -1176,11 +1189,20 @@ __device__ bool run_ws_rec(const FwdParams& p, ChainCtx& cx, WsBars& bb, WsPhase
             split_pair(x0 * sc[rr], x1 * sc[rr], hi, lo);
             *reinterpret_cast<uint32_t*>(sm.vs[cx.half] + off) = hi;
             *reinterpret_cast<uint32_t*>(sm.vslo[cx.half] + off) = lo;
-            if (kStore) {
-              split_pair(x0, x1, hi, lo);
-              *reinterpret_cast<uint32_t*>(vph + off) = hi;
-              *reinterpret_cast<uint32_t*>(vpl + off) = lo;
-            }
+            if (kStore) split_pair(x0, x1, rh[rr][k], rl[rr][k]);
+          }
+        }
+        if (kStore) {
+          // a 4x4 transpose inside each group of four lanes leaves lane qa with the whole 16-byte
+          // unit 4 hc + qa of its rows: one 16-byte store per unit instead of four 4-byte ones
+#pragma unroll
+          for (int rr = 0; rr < 2; ++rr) {
+            quad_transpose4(rh[rr], qa);
+            quad_transpose4(rl[rr], qa);
+            const int r = r0 + 8 * rr, cj = 4 * hc + qa;
+            const uint32_t off = r * 128 + ((cj ^ (r & 7)) << 4);
+            *reinterpret_cast<uint4*>(vph + off) = make_uint4(rh[rr][0], rh[rr][1], rh[rr][2], rh[rr][3]);
+            *reinterpret_cast<uint4*>(vpl + off) = make_uint4(rl[rr][0], rl[rr][1], rl[rr][2], rl[rr][3]);
           }
         }
       }
@@ -1255,10 +1277,12 @@ __global__ void __launch_bounds__(kWsThreads, 1) chain_kernel(const __grid_const
     mbar_init(&bar_mma, 1);
     mbar_init(&wbars.full[0], 1);
     mbar_init(&wbars.full[1], 1);
+    mbar_init(&wbars.full[2], 1);
     mbar_init(&wbars.fullq, 1);
     mbar_init(&wbars.fullu, 1);
     mbar_init(&wbars.empty[0], 2);
     mbar_init(&wbars.empty[1], 2);
+    mbar_init(&wbars.empty[2], 2);
     mbar_init(&wbars.emptyq, rec ? 1 : 2);  // the forward's epilogue also releases Q
     mbar_init(&wbars.a_done, 1);
     mbar_init(&wbars.pre_done, 1);
