@@ -918,6 +918,24 @@ __global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ Bw
     const int h = hk * G + hh;
     const size_t rec = (size_t)chunk * Hv + h;
     const bool next = hh + 1 < G;
+    if (tid == 0) {
+      // this head's later loads and the next head's records into L2 now: each buffer is refilled
+      // only once the previous use frees it, and the fill then waits on L2 instead of HBM
+      bulk_prefetch_l2(p.ws + p.L.t_f32 + rec * 16384, 16384);
+      bulk_prefetch_l2(p.ws + p.L.f.tw + rec * 8192, 8192);
+      bulk_prefetch_l2(p.ws + p.L.f.tu + rec * 8192, 8192);
+      tma_prefetch_3d(&p.tm_v, 0, h, tok0);
+      tma_prefetch_3d(&p.tm_v, 64, h, tok0);
+      if (next) {
+        const size_t r1 = rec + 1;
+        tma_prefetch_3d(&p.tm_do, 0, h + 1, tok0);
+        tma_prefetch_3d(&p.tm_do, 64, h + 1, tok0);
+        bulk_prefetch_l2(p.ws + p.L.dvp_img + r1 * 16384, 16384);
+        bulk_prefetch_l2(p.ws + p.L.st_img + r1 * 32768, 32768);
+        bulk_prefetch_l2(p.ws + p.L.ds_img + r1 * 32768, 32768);
+        bulk_prefetch_l2(p.ws + p.L.vp_img + r1 * 16384, 16384);
+      }
+    }
     if (tid < 64) sm.beta[tid] = (tid < n) ? p.beta[(size_t)(tok0 + tid) * Hv + h] : 0.f;
     if (!(ok = wait_bar(&bar_p1, ph_p1))) break;
     if (tid < 64) {
@@ -1383,6 +1401,16 @@ __global__ void __launch_bounds__(256, 1) dq_kernel(const __grid_constant__ BwdP
       bulk_load(sm.vh[0], p.ws + p.L.vp_img + rec * 16384, 16384, &bar_ld);
       bulk_load(sm.vl[0], p.ws + p.L.vp_lo + rec * 16384, 16384, &bar_ld);
       bulk_load(sm.gam, p.ws + p.L.f.gam + rec * 256, 256, &bar_ld);
+      if (hh + 1 < G) {  // the next head's records into L2 while this head runs
+        const size_t r1 = rec + 1;
+        tma_prefetch_3d(&p.tm_do, 0, h + 1, tok0);
+        tma_prefetch_3d(&p.tm_do, 64, h + 1, tok0);
+        bulk_prefetch_l2(p.ws + p.L.st_img + r1 * 32768, 32768);
+        bulk_prefetch_l2(p.ws + p.L.st_lo + r1 * 32768, 32768);
+        bulk_prefetch_l2(p.ws + p.L.vp_img + r1 * 16384, 16384);
+        bulk_prefetch_l2(p.ws + p.L.vp_lo + r1 * 16384, 16384);
+        bulk_prefetch_l2(p.ws + p.L.f.gam + r1 * 256, 256);
+      }
     }
     if (!(ok = cx.wait_ld())) break;
     if (tid < 64) {
