@@ -206,6 +206,19 @@ __device__ bool run_rev_ws(const BwdParams& p, Ctx& cx, RevSmem& sm, RevBars& bb
       for (int j = 0; j < n; ++j) {
         const int gc = chunk_of(j), st = j & 1, tok0 = ctok[gc];
         const size_t rec = (size_t)gc * Hv + h;
+        if (j + 2 < n) {  // chunk j + 2 into L2 while its stage is still in use
+          const int g2 = chunk_of(j + 2), t2 = ctok[g2];
+          const size_t r2 = (size_t)g2 * Hv + h;
+          tma_prefetch_3d(&p.tm_k, 0, hk, t2);
+          tma_prefetch_3d(&p.tm_k, 64, hk, t2);
+          tma_prefetch_3d(&p.tm_q, 0, hk, t2);
+          tma_prefetch_3d(&p.tm_q, 64, hk, t2);
+          tma_prefetch_3d(&p.tm_do, 0, h, t2);
+          tma_prefetch_3d(&p.tm_do, 64, h, t2);
+          bulk_prefetch_l2(p.ws + p.L.f.tw + r2 * 8192, 8192);
+          bulk_prefetch_l2(p.ws + p.L.f.pimg + r2 * 8192, 8192);
+          bulk_prefetch_l2(p.ws + p.L.f.gam + r2 * 256, 256);
+        }
         if (j >= 2) rrole_wait(&bb.empty[st], ph.empty[st], abort);
         if (*abort) break;
         mbar_arrive_expect_tx(&bb.full[st], 3 * 16384 + 2 * 8192 + 256);

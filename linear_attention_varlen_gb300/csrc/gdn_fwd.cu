@@ -717,6 +717,24 @@ __device__ bool run_ws(const FwdParams& p, ChainCtx& cx, WsBars& bb, WsPhase& ph
       for (int j = 0; j < n; ++j) {
         const int gc = gc0 + j, st = j & 1, tok0 = ctok[gc];
         const bool out = gc >= gc_out;
+        if (j + 2 < n) {  // chunk j + 2 into L2 while its stage is still in use
+          const int g2 = gc + 2, t2 = ctok[g2];
+          const size_t r2 = (size_t)g2 * Hv + h;
+          tma_prefetch_3d(&p.tm_k, 0, hk, t2);
+          tma_prefetch_3d(&p.tm_k, 64, hk, t2);
+          bulk_prefetch_l2(p.ws + p.L.gam + r2 * 256, 256);
+          bulk_prefetch_l2(p.ws + p.L.tw + r2 * 8192, 8192);
+          if (kWithU) {
+            tma_prefetch_3d(&p.tm_v, 0, h, t2);
+            tma_prefetch_3d(&p.tm_v, 64, h, t2);
+            bulk_prefetch_l2(p.ws + p.L.tu + r2 * 8192, 8192);
+          }
+          if (g2 >= gc_out) {
+            tma_prefetch_3d(&p.tm_q, 0, hk, t2);
+            tma_prefetch_3d(&p.tm_q, 64, hk, t2);
+            bulk_prefetch_l2(p.p_img + r2 * 8192, 8192);
+          }
+        }
         if (j >= 2) role_wait(&bb.empty[st], ph.empty[st], abort);
         if (*abort) break;
         mbar_arrive_expect_tx(&bb.full[st], 16384 + 256 + (kWithU ? 16384 + 8192 : 0) + (out ? 8192 : 0));
