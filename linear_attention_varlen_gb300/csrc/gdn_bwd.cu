@@ -931,7 +931,7 @@ __global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ Bw
     const int h = hk * G + hh;
     const size_t rec = (size_t)chunk * Hv + h;
     const bool next = hh + 1 < G;
-    if (tid == 0) {
+    if (tid == 224) {  // a thread that issues neither loads nor MMAs
       // this head's later loads and the next head's records into L2 now: each buffer is refilled
       // only once the previous use frees it, and the fill then waits on L2 instead of HBM
       bulk_prefetch_l2(p.ws + p.L.t_f32 + rec * 16384, 16384);
