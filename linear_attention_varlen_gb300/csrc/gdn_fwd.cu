@@ -188,7 +188,7 @@ struct KktSmem {
   uint8_t k_tile[2][8192];               // K rows, two 64-wide dk blocks, SW128; then Q K^T fp32 (fz)
   float a[kKktHeads][64][kAStride];      // A, then T (per concurrent value head); before the solve
                                          // the first 16 KB hold the Q tile (forward: Q K^T)
-  float kk[64][65];                      // K K^T
+  float kk[64][kAStride];                // K K^T (16-byte aligned rows for vector loads)
   float gam[kKktHeads][64];
   float beta[kKktHeads][64];
   float eg[kKktHeads][64];               // e^{gamma}
@@ -207,7 +207,7 @@ __device__ __forceinline__ void group_sync(int group) {
   }
 }
 
-__global__ void __launch_bounds__(256) kkt_solve_kernel(const __grid_constant__ FwdParams p) {
+__global__ void __launch_bounds__(256, 2) kkt_solve_kernel(const __grid_constant__ FwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   KktSmem& sm = *reinterpret_cast<KktSmem*>(smem_align1024(smem_raw));
   __shared__ uint64_t bar_ld, bar_mma;
@@ -328,61 +328,104 @@ __global__ void __launch_bounds__(256) kkt_solve_kernel(const __grid_constant__ 
         group_sync(grp);
       }
       const bool factored = gam[63] > kFactorMin;  // gamma is nonincreasing: gam[63] is the minimum
-      // A, column t (rows below the diagonal)
-      {
-        const float gt = gam[t], et = egi[t];
-        if (factored) {
-#pragma unroll 4
-          for (int r = t + 1; r < 64; ++r) A[r][t] = bet[r] * eg[r] * et * sm.kk[r][t];
+      if (factored) {
+        // T = (I + A)^{-1}, column t, with A_rm = (beta_r e^{gamma_r}) (K K^T)_rm e^{-gamma_m} for
+        // m < r: forward substitution on y_m = e^{-gamma_m} x_m reads K K^T itself (no A matrix).
+        // T goes to A's buffer row by row; the second warp of the group (columns 32-63) starts
+        // at row 32 (rows and terms below are zero).
+        float y[64];
+        if (sub == 0) {
+#pragma unroll
+          for (int r = 0; r < 64; ++r) {
+            float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+            for (int m = 0; m + 4 <= r; m += 4) {
+              const float4 kv = *reinterpret_cast<const float4*>(&sm.kk[r][m]);
+              a0 += kv.x * y[m];
+              a1 += kv.y * y[m + 1];
+              a2 += kv.z * y[m + 2];
+              a3 += kv.w * y[m + 3];
+            }
+#pragma unroll
+            for (int m = r & ~3; m < r; ++m) a0 += sm.kk[r][m] * y[m];
+            const float xr = ((r == t) ? 1.f : 0.f) - bet[r] * eg[r] * ((a0 + a1) + (a2 + a3));
+            A[r][t] = xr;
+            y[r] = egi[r] * xr;
+          }
         } else {
+#pragma unroll
+          for (int r = 0; r < 32; ++r) A[r][t] = 0.f;
+#pragma unroll
+          for (int r = 32; r < 64; ++r) {
+            float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+            for (int m = 32; m + 4 <= r; m += 4) {
+              const float4 kv = *reinterpret_cast<const float4*>(&sm.kk[r][m]);
+              a0 += kv.x * y[m];
+              a1 += kv.y * y[m + 1];
+              a2 += kv.z * y[m + 2];
+              a3 += kv.w * y[m + 3];
+            }
+#pragma unroll
+            for (int m = r & ~3; m < r; ++m) a0 += sm.kk[r][m] * y[m];
+            const float xr = ((r == t) ? 1.f : 0.f) - bet[r] * eg[r] * ((a0 + a1) + (a2 + a3));
+            A[r][t] = xr;
+            y[r] = egi[r] * xr;
+          }
+        }
+        group_sync(grp);
+      } else {
+        // A, column t (rows below the diagonal), one exponential per entry
+        {
+          const float gt = gam[t];
 #pragma unroll 4
           for (int r = t + 1; r < 64; ++r) A[r][t] = bet[r] * __expf(gam[r] - gt) * sm.kk[r][t];
         }
-      }
-      group_sync(grp);
-      // T = (I + A)^{-1}, column t: forward substitution (entries above the diagonal come out 0);
-      // the second warp of the group (columns 32-63) skips rows and terms below 32, which are zero
-      float x[64];
-      if (sub == 0) {
+        group_sync(grp);
+        // T = (I + A)^{-1}, column t: forward substitution (entries above the diagonal come out 0);
+        // the second warp of the group (columns 32-63) skips rows and terms below 32, which are zero
+        float x[64];
+        if (sub == 0) {
 #pragma unroll
-        for (int r = 0; r < 64; ++r) {
-          // four independent partial sums keep the FMA chain of row r about r/4 long
-          float a0 = (r == t) ? 1.f : 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+          for (int r = 0; r < 64; ++r) {
+            // four independent partial sums keep the FMA chain of row r about r/4 long
+            float a0 = (r == t) ? 1.f : 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll
-          for (int m = 0; m + 4 <= r; m += 4) {
-            const float4 av = *reinterpret_cast<const float4*>(&A[r][m]);
-            a0 -= av.x * x[m];
-            a1 -= av.y * x[m + 1];
-            a2 -= av.z * x[m + 2];
-            a3 -= av.w * x[m + 3];
+            for (int m = 0; m + 4 <= r; m += 4) {
+              const float4 av = *reinterpret_cast<const float4*>(&A[r][m]);
+              a0 -= av.x * x[m];
+              a1 -= av.y * x[m + 1];
+              a2 -= av.z * x[m + 2];
+              a3 -= av.w * x[m + 3];
+            }
+#pragma unroll
+            for (int m = r & ~3; m < r; ++m) a0 -= A[r][m] * x[m];
+            x[r] = (a0 + a1) + (a2 + a3);
           }
+        } else {
 #pragma unroll
-          for (int m = r & ~3; m < r; ++m) a0 -= A[r][m] * x[m];
-          x[r] = (a0 + a1) + (a2 + a3);
-        }
-      } else {
+          for (int r = 0; r < 32; ++r) x[r] = 0.f;
 #pragma unroll
-        for (int r = 0; r < 32; ++r) x[r] = 0.f;
+          for (int r = 32; r < 64; ++r) {
+            float a0 = (r == t) ? 1.f : 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll
-        for (int r = 32; r < 64; ++r) {
-          float a0 = (r == t) ? 1.f : 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+            for (int m = 32; m + 4 <= r; m += 4) {
+              const float4 av = *reinterpret_cast<const float4*>(&A[r][m]);
+              a0 -= av.x * x[m];
+              a1 -= av.y * x[m + 1];
+              a2 -= av.z * x[m + 2];
+              a3 -= av.w * x[m + 3];
+            }
 #pragma unroll
-          for (int m = 32; m + 4 <= r; m += 4) {
-            const float4 av = *reinterpret_cast<const float4*>(&A[r][m]);
-            a0 -= av.x * x[m];
-            a1 -= av.y * x[m + 1];
-            a2 -= av.z * x[m + 2];
-            a3 -= av.w * x[m + 3];
+            for (int m = r & ~3; m < r; ++m) a0 -= A[r][m] * x[m];
+            x[r] = (a0 + a1) + (a2 + a3);
           }
-#pragma unroll
-          for (int m = r & ~3; m < r; ++m) a0 -= A[r][m] * x[m];
-          x[r] = (a0 + a1) + (a2 + a3);
         }
-      }
-      group_sync(grp);  // every thread is done reading A
+        group_sync(grp);  // every thread is done reading A
 #pragma unroll
-      for (int r = 0; r < 64; ++r) A[r][t] = x[r];
-      group_sync(grp);
+        for (int r = 0; r < 64; ++r) A[r][t] = x[r];
+        group_sync(grp);
+      }
       // outputs, row by row (8 threads per 128-byte row of the bf16 images)
       uint8_t* dw = tw_ws + rec * 8192;
       uint8_t* du = tu_ws + rec * 8192;
