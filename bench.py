@@ -109,7 +109,7 @@ class ClockSampler:
     def start(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "50"], stdout=subprocess.PIPE,
+                                          "--format=csv,noheader,nounits", "-lms", "20"], stdout=subprocess.PIPE,
                                          stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
@@ -281,8 +281,6 @@ def run_ours(args, rank, world, local_rank):
     train = has_bwd and args.mode == "exact"
     o_fwd = gdn.Options(mode=args.mode, save_for_backward=train)
     o_bwd = gdn.Options(mode=args.mode, reuse_forward=train)
-    opts_f = dataclasses.replace(o_fwd, stage_events=ev_f)
-    opts_b = dataclasses.replace(o_bwd, stage_events=ev_b)
 
     def step(of, ob):
         fwd(of)
@@ -310,17 +308,26 @@ def run_ours(args, rank, world, local_rank):
     stops = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     stage_f = np.zeros((args.steps, gdn.NUM_STAGES))
     stage_b = np.zeros((args.steps, gdn.NUM_STAGES))
+    # every step gets its own events, so that the host enqueues ahead of the device and no step
+    # waits for the host (events are read once all steps have run)
+    evs = [([torch.cuda.Event(enable_timing=True) for _ in range(2 * gdn.NUM_STAGES)],
+            [torch.cuda.Event(enable_timing=True) for _ in range(2 * gdn.NUM_STAGES)]) for _ in range(args.steps)]
+    for ef, eb in evs:  # creates the CUDA events (the library records them again inside each call)
+        for e in ef + eb:
+            e.record(stream)
+    torch.cuda.synchronize()
     for i in range(args.steps):
         flush.zero_()
         starts[i].record(stream)
-        step(opts_f, opts_b)
+        step(dataclasses.replace(o_fwd, stage_events=evs[i][0]), dataclasses.replace(o_bwd, stage_events=evs[i][1]))
         stops[i].record(stream)
-        stops[i].synchronize()
-        for s_ in range(gdn.NUM_STAGES):
-            stage_f[i, s_] = ev_f[2 * s_].elapsed_time(ev_f[2 * s_ + 1])
-            if has_bwd:
-                stage_b[i, s_] = ev_b[2 * s_].elapsed_time(ev_b[2 * s_ + 1])
     torch.cuda.synchronize()
+    for i in range(args.steps):
+        ef, eb = evs[i]
+        for s_ in range(gdn.NUM_STAGES):
+            stage_f[i, s_] = ef[2 * s_].elapsed_time(ef[2 * s_ + 1])
+            if has_bwd:
+                stage_b[i, s_] = eb[2 * s_].elapsed_time(eb[2 * s_ + 1])
     if world > 1:
         torch.distributed.barrier()
     clk = clocks.stop() if clocks else None
