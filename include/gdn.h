@@ -93,7 +93,8 @@ typedef struct gdn_options {
   int32_t flags;             /* gdn_flags, 0 = none */
   void* stage_events;        /* optional profiling hook: NULL, or a cudaEvent_t[2 * GDN_NUM_STAGES] array;
                                 events 2s and 2s+1 are recorded on `stream` right before and right after
-                                stage s (both at the same point when the stage has nothing to launch) */
+                                stage s (both at the same point when the stage has nothing to launch);
+                                NULL entries are skipped */
 } gdn_options;
 
 /* Stages of a call (indices into gdn_options.stage_events). A backward call runs stages 0-3

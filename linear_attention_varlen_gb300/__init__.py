@@ -58,7 +58,7 @@ class Options:
     trunc_log_threshold: float = -10.0
     segment_chunks: int = 0
     scale: float = 1.0
-    stage_events: Optional[object] = None  # optional list of 2 * NUM_STAGES timing torch.cuda.Event
+    stage_events: Optional[object] = None  # optional list of 2 * NUM_STAGES timing torch.cuda.Event (or None)
     save_for_backward: bool = False
     reuse_forward: bool = False
 
@@ -66,9 +66,11 @@ class Options:
         m = {"exact": MODE_EXACT, "truncate": MODE_TRUNCATE}[self.mode]
         ev = None
         if self.stage_events is not None:
-            handles = [int(e.cuda_event) for e in self.stage_events]
-            if len(handles) != 2 * NUM_STAGES or not all(handles):
-                raise ValueError("stage_events: 2 * NUM_STAGES recorded timing events are required")
+            # None entries are not recorded (each recorded event costs a few microseconds of stream time)
+            handles = [0 if e is None else int(e.cuda_event) for e in self.stage_events]
+            given = [e for e in self.stage_events if e is not None]
+            if len(handles) != 2 * NUM_STAGES or not all(int(e.cuda_event) for e in given):
+                raise ValueError("stage_events: 2 * NUM_STAGES entries, each None or a recorded timing event")
             self._ev_array = (ctypes.c_void_p * len(handles))(*handles)
             ev = ctypes.cast(self._ev_array, ctypes.c_void_p)
         flags = (FLAG_SAVE_FOR_BWD if self.save_for_backward else 0) | (FLAG_REUSE_FWD if self.reuse_forward else 0)

@@ -1647,7 +1647,7 @@ int launch_bwd(const BwdArgs& a, bool reuse, cudaStream_t stream, cudaEvent_t* e
   p.ws = ws;
   p.scale = a.scale;
   auto mark = [&](int i) {
-    if (ev) cudaEventRecord(ev[i], stream);
+    if (ev && ev[i]) cudaEventRecord(ev[i], stream);
   };
   if (cudaMemsetAsync(ws + p.L.flags_ds0, 0, (size_t)d.N * d.Hv * 4, stream) != cudaSuccess) return kErrCuda;
   if (cudaMemsetAsync(ws + p.L.hdr2, 0, sizeof(Header), stream) != cudaSuccess) return kErrCuda;

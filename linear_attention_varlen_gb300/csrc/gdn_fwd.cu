@@ -1761,7 +1761,7 @@ int launch_fwd(const FwdParams& p, cudaStream_t stream, cudaEvent_t* ev, bool pl
     attr_done = true;
   }
   auto mark = [&](int i) {
-    if (ev) cudaEventRecord(ev[i], stream);
+    if (ev && ev[i]) cudaEventRecord(ev[i], stream);
   };
   mark(0);
   plan_kernel<<<1, 1024, 0, stream>>>(p, plan_only ? 1 : 0);
