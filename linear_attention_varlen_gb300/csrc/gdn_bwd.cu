@@ -1355,14 +1355,14 @@ __global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ Bw
 
 struct DqSmem {
   uint8_t k[2][8192];    // K tile                  (B MN-major: dQK K)
-  uint8_t dout[2][8192]; // dO tile                 (A K-major)
+  uint8_t dout[2][2][8192];  // [head parity] dO tile (A K-major)
   uint8_t sh[2][16384];  // S_c high part           (B K-major: dO S^T)
   uint8_t sl[2][16384];  // S_c low part
   uint8_t vh[2][8192];   // V' high part            (B K-major: dO V'^T)
   uint8_t vl[2][8192];   // V' low part
   uint8_t qh[8192];      // scale dQK high part     (A K-major)
   uint8_t ql[8192];      // scale dQK low part
-  float gam[64];
+  float gam[2][64];      // [head parity]
   float eg[64], egi[64]; // e^{gamma}, e^{-gamma}
 };
 constexpr size_t kDqSmemBytes = sizeof(DqSmem) + 1024;
@@ -1371,7 +1371,7 @@ constexpr uint32_t kDtP = 0, kDt1 = 128, kDt2 = 256;
 __global__ void __launch_bounds__(256, 1) dq_kernel(const __grid_constant__ BwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   DqSmem& sm = *reinterpret_cast<DqSmem*>(smem_align1024(smem_raw));
-  __shared__ uint64_t bar_ld, bar_mma;
+  __shared__ uint64_t bar_ld, bar_mma, bar_a, bar_b;
   __shared__ uint32_t tmem_holder;
   Header* hd = reinterpret_cast<Header*>(p.ws + p.L.f.header);
   const int chunk = blockIdx.x, hk = blockIdx.y;
@@ -1385,6 +1385,8 @@ __global__ void __launch_bounds__(256, 1) dq_kernel(const __grid_constant__ BwdP
   if (tid == 0) {
     mbar_init(&bar_ld, 1);
     mbar_init(&bar_mma, 1);
+    mbar_init(&bar_a, 1);
+    mbar_init(&bar_b, 1);
     fence_mbar_init();
   }
   if (cx.warp == 0) tmem_alloc(&tmem_holder, 512);
@@ -1398,50 +1400,67 @@ __global__ void __launch_bounds__(256, 1) dq_kernel(const __grid_constant__ BwdP
   float dq[32];  // [32-column group ci][16 values in the tmem_ld16x256_x4 order]
   for (int c = 0; c < 32; ++c) dq[c] = 0.f;
   bool ok = true;
-  for (int hh = 0; hh < G && ok; ++hh) {
-    const int h = hk * G + hh;
-    const size_t rec = (size_t)chunk * Hv + h;
-    if (tid == 0) {
-      mbar_arrive_expect_tx(&bar_ld, (hh == 0 ? 2 * 8192 : 0) + 2 * 8192 + 2 * 32768 + 2 * 16384 + 256);
-      if (hh == 0) {
-        tma_load_3d(sm.k[0], &p.tm_k, 0, hk, tok0, &bar_ld);
-        tma_load_3d(sm.k[1], &p.tm_k, 64, hk, tok0, &bar_ld);
-      }
-      tma_load_3d(sm.dout[0], &p.tm_do, 0, h, tok0, &bar_ld);
-      tma_load_3d(sm.dout[1], &p.tm_do, 64, h, tok0, &bar_ld);
-      bulk_load(sm.sh[0], p.ws + p.L.st_img + rec * 32768, 32768, &bar_ld);
-      bulk_load(sm.sl[0], p.ws + p.L.st_lo + rec * 32768, 32768, &bar_ld);
-      bulk_load(sm.vh[0], p.ws + p.L.vp_img + rec * 16384, 16384, &bar_ld);
-      bulk_load(sm.vl[0], p.ws + p.L.vp_lo + rec * 16384, 16384, &bar_ld);
-      bulk_load(sm.gam, p.ws + p.L.f.gam + rec * 256, 256, &bar_ld);
-      if (hh + 1 < G) {  // the next head's records into L2 while this head runs
-        const size_t r1 = rec + 1;
-        tma_prefetch_3d(&p.tm_do, 0, h + 1, tok0);
-        tma_prefetch_3d(&p.tm_do, 64, h + 1, tok0);
-        bulk_prefetch_l2(p.ws + p.L.st_img + r1 * 32768, 32768);
-        bulk_prefetch_l2(p.ws + p.L.st_lo + r1 * 32768, 32768);
-        bulk_prefetch_l2(p.ws + p.L.vp_img + r1 * 16384, 16384);
-        bulk_prefetch_l2(p.ws + p.L.vp_lo + r1 * 16384, 16384);
-        bulk_prefetch_l2(p.ws + p.L.f.gam + r1 * 256, 256);
-      }
+  // Two load groups per value head, each issued as soon as the previous head frees its buffers:
+  // A (dO into the head's parity buffer, V' hi / lo, gamma) once dP = dO V'^T has run, B (S hi / lo)
+  // once dO S^T has run. Head hh + 1's A then lands during head hh's second half, and its B
+  // during its own dP and epilogue.
+  uint32_t ph_a = 0, ph_b = 0;
+  auto issue_a = [&](int hh2) {  // thread 0
+    const int h2 = hk * G + hh2, b2 = hh2 & 1;
+    const size_t r2 = (size_t)chunk * Hv + h2;
+    mbar_arrive_expect_tx(&bar_a, (hh2 == 0 ? 2 * 8192 : 0) + 2 * 8192 + 2 * 16384 + 256);
+    if (hh2 == 0) {
+      tma_load_3d(sm.k[0], &p.tm_k, 0, hk, tok0, &bar_a);
+      tma_load_3d(sm.k[1], &p.tm_k, 64, hk, tok0, &bar_a);
     }
-    if (!(ok = cx.wait_ld())) break;
+    tma_load_3d(sm.dout[b2][0], &p.tm_do, 0, h2, tok0, &bar_a);
+    tma_load_3d(sm.dout[b2][1], &p.tm_do, 64, h2, tok0, &bar_a);
+    bulk_load(sm.vh[0], p.ws + p.L.vp_img + r2 * 16384, 16384, &bar_a);
+    bulk_load(sm.vl[0], p.ws + p.L.vp_lo + r2 * 16384, 16384, &bar_a);
+    bulk_load(sm.gam[b2], p.ws + p.L.f.gam + r2 * 256, 256, &bar_a);
+  };
+  auto issue_b = [&](int hh2) {  // thread 0
+    const size_t r2 = (size_t)chunk * Hv + hk * G + hh2;
+    mbar_arrive_expect_tx(&bar_b, 2 * 32768);
+    bulk_load(sm.sh[0], p.ws + p.L.st_img + r2 * 32768, 32768, &bar_b);
+    bulk_load(sm.sl[0], p.ws + p.L.st_lo + r2 * 32768, 32768, &bar_b);
+  };
+  if (tid == 0) {
+    issue_a(0);
+    issue_b(0);
+  }
+  for (int hh = 0; hh < G && ok; ++hh) {
+    const int h = hk * G + hh, bp = hh & 1;
+    const size_t rec = (size_t)chunk * Hv + h;
+    if (tid == 224 && hh + 1 < G) {  // the next head's records into L2 (a thread off the load path)
+      const size_t r1 = rec + 1;
+      tma_prefetch_3d(&p.tm_do, 0, h + 1, tok0);
+      tma_prefetch_3d(&p.tm_do, 64, h + 1, tok0);
+      bulk_prefetch_l2(p.ws + p.L.st_img + r1 * 32768, 32768);
+      bulk_prefetch_l2(p.ws + p.L.st_lo + r1 * 32768, 32768);
+      bulk_prefetch_l2(p.ws + p.L.vp_img + r1 * 16384, 16384);
+      bulk_prefetch_l2(p.ws + p.L.vp_lo + r1 * 16384, 16384);
+    }
+    if (!(ok = wait_all(&bar_a, ph_a))) break;
+    ph_a ^= 1;
+    tc_fence_after();
     if (tid < 64) {
-      sm.eg[tid] = __expf(sm.gam[tid]);
-      sm.egi[tid] = __expf(-sm.gam[tid]);
+      sm.eg[tid] = __expf(sm.gam[bp][tid]);
+      sm.egi[tid] = __expf(-sm.gam[bp][tid]);
     }
     // dP = dO V'^T (hi + lo)
     if (tid == 0) {
       for (int ks = 0; ks < 8; ++ks)
-        umma_bf16(tm + kDtP, kmajor_desc(smem_u32(sm.dout[0]), 8192, ks), kmajor_desc(smem_u32(sm.vh[0]), 8192, ks),
+        umma_bf16(tm + kDtP, kmajor_desc(smem_u32(sm.dout[bp][0]), 8192, ks), kmajor_desc(smem_u32(sm.vh[0]), 8192, ks),
                   idesc_bf16(64, 64, 0, 0), ks > 0);
       for (int ks = 0; ks < 8; ++ks)
-        umma_bf16(tm + kDtP, kmajor_desc(smem_u32(sm.dout[0]), 8192, ks), kmajor_desc(smem_u32(sm.vl[0]), 8192, ks),
+        umma_bf16(tm + kDtP, kmajor_desc(smem_u32(sm.dout[bp][0]), 8192, ks), kmajor_desc(smem_u32(sm.vl[0]), 8192, ks),
                   idesc_bf16(64, 64, 0, 0), 1);
     }
     if (!(ok = cx.commit_wait())) break;  // (its barrier also publishes eg / egi)
+    if (tid == 0 && hh + 1 < G) issue_a(hh + 1);  // V' is read; the other dO buffer is free
     // e^{gamma_i - gamma_j} as e^{gamma_i} e^{-gamma_j} while both factors stay finite
-    const bool factored = sm.gam[63] > kFactorMin;
+    const bool factored = sm.gam[bp][63] > kFactorMin;
     {
       // all 32 lanes: rows rw[0], rw[1], column pairs (tmem_ld16x256_x4)
       float v[16], ev[16];
@@ -1457,7 +1476,7 @@ __global__ void __launch_bounds__(256, 1) dq_kernel(const __grid_constant__ BwdP
         for (int k = 0; k < 4; ++k)
 #pragma unroll
           for (int q = 0; q < 4; ++q)
-            ev[4 * k + q] = __expf(sm.gam[rw[q >> 1]] - sm.gam[32 * cx.half + 8 * k + c2 + (q & 1)]) * p.scale;
+            ev[4 * k + q] = __expf(sm.gam[bp][rw[q >> 1]] - sm.gam[bp][32 * cx.half + 8 * k + c2 + (q & 1)]) * p.scale;
       }
       tmem_ld_wait();
 #pragma unroll
@@ -1474,13 +1493,16 @@ __global__ void __launch_bounds__(256, 1) dq_kernel(const __grid_constant__ BwdP
         }
     }
     sync_generic_to_async();
+    if (!(ok = wait_all(&bar_b, ph_b))) break;
+    ph_b ^= 1;
+    tc_fence_after();
     // dO S^T (hi + lo) and dQK K (hi + lo)
     if (tid == 0) {
       for (int ks = 0; ks < 8; ++ks)
-        umma_bf16(tm + kDt1, kmajor_desc(smem_u32(sm.dout[0]), 8192, ks), kmajor_desc(smem_u32(sm.sh[0]), 16384, ks),
+        umma_bf16(tm + kDt1, kmajor_desc(smem_u32(sm.dout[bp][0]), 8192, ks), kmajor_desc(smem_u32(sm.sh[0]), 16384, ks),
                   idesc_bf16(64, 128, 0, 0), ks > 0);
       for (int ks = 0; ks < 8; ++ks)
-        umma_bf16(tm + kDt1, kmajor_desc(smem_u32(sm.dout[0]), 8192, ks), kmajor_desc(smem_u32(sm.sl[0]), 16384, ks),
+        umma_bf16(tm + kDt1, kmajor_desc(smem_u32(sm.dout[bp][0]), 8192, ks), kmajor_desc(smem_u32(sm.sl[0]), 16384, ks),
                   idesc_bf16(64, 128, 0, 0), 1);
       for (int ks = 0; ks < 4; ++ks)
         umma_bf16(tm + kDt2, kmajor_desc(smem_u32(sm.qh), 8192, ks), mnmajor_desc(smem_u32(sm.k[0]), 8192, ks),
@@ -1490,6 +1512,7 @@ __global__ void __launch_bounds__(256, 1) dq_kernel(const __grid_constant__ BwdP
                   idesc_bf16(64, 128, 0, 1), 1);
     }
     if (!(ok = cx.commit_wait())) break;
+    if (tid == 0 && hh + 1 < G) issue_b(hh + 1);  // S is read
     {
       const float sc0 = sm.eg[rw[0]] * p.scale, sc1 = sm.eg[rw[1]] * p.scale;
 #pragma unroll
