@@ -785,12 +785,14 @@ struct GradSmem {
   float qkf[4096];         // scale Q K^T          (fz layout)
   uint8_t bS[2][16384];    // S_c image       | phase 2: T fp32 [0, 16K) (fz), T bf16 [16K, 24K)
   uint8_t bdS[2][16384];   // dS_{c+1} image  | phase 2: T_w [0, 8K), T_u [8K, 16K), dT [16K, 24K), R [24K, 32K)
-  uint8_t bVp[2][8192];    // V' -> V'_s      | fp32 64x64 scratch (vy products, then L o KK)
+  uint8_t bVp[2][8192];    // V' -> V'_s (then the next head's V')
   uint8_t bdVp[2][8192];   // dV'             | fp32 64x64 scratch (kx products)
   uint8_t bdO[2][8192];    // dO              | phase 2: V
   uint8_t bW[2][8192];     // fp32 scratch (dEg) | dW rows t
   uint8_t bP[8192];        // scale dQK, then L = dA o diag(beta) E (strictly lower)
-  float gam[64], beta[64], Gm[64], Gi[64];  // gamma, beta, e^{gamma}, e^{-gamma}
+  float scr[4096];         // fp32 64x64 scratch (fz): vy products, then L o KK
+  float gam[2][64];        // [head parity] gamma
+  float beta[64], Gm[64], Gi[64];  // beta, e^{gamma}, e^{-gamma}
   float part[8][64];
   float vy[64], kx[64], cA[64], db3[2][64];
   float red4[2][4][64];    // partial column sums (two matrices x four row quarters)
@@ -862,20 +864,24 @@ __global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ Bw
   // Loads of one value head's records, in the order their buffers become free. The phase-1 set
   // (S, dS, V', dV', dO images and gamma) lands on bar_p1: its transaction count is armed by the
   // first piece, the other pieces follow as the previous head releases their buffers.
-  const uint32_t kP1Bytes = 32768 * 2 + 16384 * 2 + 2 * 8192 + 256;
+  const uint32_t kP1Bytes = 32768 * 2 + 16384 + 2 * 8192;  // gamma and V' are counted where issued
   auto rec_of = [&](int hh2) { return (size_t)chunk * Hv + hk * G + hh2; };
   auto load_do_gam = [&](int hh2) {  // thread 0; arms bar_p1
+    mbar_expect_tx(&bar_p1, 256);
+    bulk_load(sm.gam[hh2 & 1], p.ws + p.L.f.gam + rec_of(hh2) * 256, 256, &bar_p1);
     mbar_arrive_expect_tx(&bar_p1, kP1Bytes);
     tma_load_3d(sm.bdO[0], &p.tm_do, 0, hk * G + hh2, tok0, &bar_p1);
     tma_load_3d(sm.bdO[1], &p.tm_do, 64, hk * G + hh2, tok0, &bar_p1);
-    bulk_load(sm.gam, p.ws + p.L.f.gam + rec_of(hh2) * 256, 256, &bar_p1);
   };
   auto load_dvp = [&](int hh2) { bulk_load(sm.bdVp[0], p.ws + p.L.dvp_img + rec_of(hh2) * 16384, 16384, &bar_p1); };
   auto load_s_ds = [&](int hh2) {
     bulk_load(sm.bS[0], p.ws + p.L.st_img + rec_of(hh2) * 32768, 32768, &bar_p1);
     bulk_load(sm.bdS[0], p.ws + p.L.ds_img + rec_of(hh2) * 32768, 32768, &bar_p1);
   };
-  auto load_vp = [&](int hh2) { bulk_load(sm.bVp[0], p.ws + p.L.vp_img + rec_of(hh2) * 16384, 16384, &bar_p1); };
+  auto load_vp = [&](int hh2) {
+    mbar_expect_tx(&bar_p1, 16384);
+    bulk_load(sm.bVp[0], p.ws + p.L.vp_img + rec_of(hh2) * 16384, 16384, &bar_p1);
+  };
   if (cx.warp == 0) tmem_alloc(&tmem_holder, 512);
   sync_generic_to_async();
   cx.tmem = tmem_holder;
@@ -951,12 +957,17 @@ __global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ Bw
     }
     if (tid < 64) sm.beta[tid] = (tid < n) ? p.beta[(size_t)(tok0 + tid) * Hv + h] : 0.f;
     if (!(ok = wait_bar(&bar_p1, ph_p1))) break;
+    const float* gam = sm.gam[hh & 1];
+    if (tid == 0 && next) {  // the next head's gamma, into the other buffer, on the next phase
+      mbar_expect_tx(&bar_p1, 256);
+      bulk_load(sm.gam[(hh + 1) & 1], p.ws + p.L.f.gam + rec_of(hh + 1) * 256, 256, &bar_p1);
+    }
     if (tid < 64) {
-      sm.Gm[tid] = __expf(sm.gam[tid]);
-      sm.Gi[tid] = __expf(-sm.gam[tid]);
+      sm.Gm[tid] = __expf(gam[tid]);
+      sm.Gi[tid] = __expf(-gam[tid]);
     }
     __syncthreads();
-    const float gC = sm.gam[63], GC = __expf(gC);
+    const float gC = gam[63], GC = __expf(gC);
     float* dEg = reinterpret_cast<float*>(sm.bW[0]);
     // ---------------- (a) dP = dO V'^T ; K dS
     if (tid == 0) {
@@ -973,7 +984,7 @@ __global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ Bw
       const int c2 = 2 * (cx.lane & 3);
       const int rw[2] = {16 * cx.q4 + (cx.lane >> 2), 16 * cx.q4 + (cx.lane >> 2) + 8};
       // e^{gamma_i - gamma_j} as e^{gamma_i} e^{-gamma_j} while both factors stay finite
-      const bool factored = sm.gam[63] > kFactorMin;
+      const bool factored = gam[63] > kFactorMin;
       float rs[2] = {0.f, 0.f};
       {
         float v[16], ev[16];
@@ -989,7 +1000,7 @@ __global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ Bw
           for (int k = 0; k < 4; ++k)
 #pragma unroll
             for (int q = 0; q < 4; ++q)
-              ev[4 * k + q] = __expf(sm.gam[rw[q >> 1]] - sm.gam[32 * cx.half + 8 * k + c2 + (q & 1)]);
+              ev[4 * k + q] = __expf(gam[rw[q >> 1]] - gam[32 * cx.half + 8 * k + c2 + (q & 1)]);
         }
         tmem_ld_wait();
 #pragma unroll
@@ -1096,7 +1107,7 @@ __global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ Bw
       }
     }
     // ---------------- (c) V'_s = diag(e^{gamma_C - gamma}) V' ; dk accumulation (dq has its own kernel)
-    if (tid < 64) sm.cA[tid] = __expf(gC - sm.gam[tid]);
+    if (tid < 64) sm.cA[tid] = __expf(gC - gam[tid]);
     __syncthreads();
     if (tid == 0) {  // dO is read: V into its buffer (phase 2)
       tma_load_3d(sm.bdO[0], &p.tm_v, 0, h, tok0, &bar_v);
@@ -1116,6 +1127,7 @@ __global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ Bw
     first_k = false;
     const float fro = ((sm.red[0] + sm.red[1]) + (sm.red[2] + sm.red[3])) + ((sm.red[4] + sm.red[5]) + (sm.red[6] + sm.red[7]));
     if (!(ok = cx.commit_wait())) break;
+    if (tid == 0 && next) load_vp(hh + 1);  // V'_s is read: the next head's V'
     // ---------------- phase 2 loads: T_w, T_u (dS is read); V and T were issued earlier
     if (tid == 0) {
       mbar_arrive_expect_tx(&bar_tw, 2 * 8192);
@@ -1159,7 +1171,7 @@ __global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ Bw
       tma_load_3d(sm.bdO[0], &p.tm_do, 0, h + 1, tok0, &bar_p1);
       tma_load_3d(sm.bdO[1], &p.tm_do, 64, h + 1, tok0, &bar_p1);
     }
-    float* vyM = reinterpret_cast<float*>(sm.bVp[0]);
+    float* vyM = sm.scr;
     float* kxM = reinterpret_cast<float*>(sm.bdVp[0]);
     {
       // all 32 lanes: rows r0 = 16 q4 + lane / 4 and r0 + 8, column pairs (tmem_ld16x256_x4)
@@ -1237,7 +1249,7 @@ __global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ Bw
       // all 32 lanes: rows r0 = 16 q4 + lane / 4 and r0 + 8, column pairs (tmem_ld16x256_x4)
       const int c2 = 2 * (cx.lane & 3);
       const int rw[2] = {16 * cx.q4 + (cx.lane >> 2), 16 * cx.q4 + (cx.lane >> 2) + 8};
-      const bool factored = sm.gam[63] > kFactorMin;
+      const bool factored = gam[63] > kFactorMin;
       float v[16], ev[16];
       tmem_ld16x256_x4(tm + kGt1 + cx.lane_base() + 32 * cx.half, v);
       if (factored) {
@@ -1250,7 +1262,7 @@ __global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ Bw
         for (int k = 0; k < 4; ++k)
 #pragma unroll
           for (int q = 0; q < 4; ++q)
-            ev[4 * k + q] = __expf(sm.gam[rw[q >> 1]] - sm.gam[32 * cx.half + 8 * k + c2 + (q & 1)]);
+            ev[4 * k + q] = __expf(gam[rw[q >> 1]] - gam[32 * cx.half + 8 * k + c2 + (q & 1)]);
       }
       tmem_ld_wait();
       float b3[2] = {0.f, 0.f};
@@ -1287,11 +1299,10 @@ __global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ Bw
                   idesc_bf16(64, 128, 1, 1), 1);
     }
     col_sums(sm, LK, nullptr, sm.cA, nullptr, tid);
-    if (tid == 0 && next) load_vp(hh + 1);  // the L o KK scratch is summed: the next head's V'
     // ---------------- (h) dgamma -> dg (reverse cumulative sum in the chunk), dbeta
     if (tid < 64) {
       const int i = tid;
-      const float ktd = (i < n) ? __expf(gC - sm.gam[i]) * (sm.part[2][i] + sm.part[3][i]) : 0.f;
+      const float ktd = (i < n) ? __expf(gC - gam[i]) * (sm.part[2][i] + sm.part[3][i]) : 0.f;
       const float kts = warp_sum(ktd);
       if (cx.lane == 0) sm.red[cx.warp] = kts;  // warps 0 and 1 (the Frobenius partials are consumed)
       float dgam = 0.f;
@@ -1321,8 +1332,7 @@ __global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ Bw
       p.dg[(size_t)(tok0 + tid) * Hv + h] = s;
       p.dbeta[(size_t)(tok0 + tid) * Hv + h] = sm.vy[tid] + sm.Gm[tid] * sm.kx[tid] + sm.db3[0][tid] + sm.db3[1][tid];
     }
-    __syncthreads();  // gamma of this head is no longer read
-    if (tid == 0 && next) bulk_load(sm.gam, p.ws + p.L.f.gam + rec_of(hh + 1) * 256, 256, &bar_p1);
+    __syncthreads();
     if (!(ok = cx.commit_wait())) break;  // (g) done before the next head reuses bP
   }
   if (ok) {
