@@ -33,7 +33,8 @@ using namespace bw;
 
 // keep_mzero: a backward that reuses a forward's records keeps that forward's pass-1 findings
 // (which segment transitions are exactly zero); the maps it rebuilds are the same.
-__global__ void __launch_bounds__(1024) plan_kernel(const __grid_constant__ FwdParams p, int keep_mzero) {
+constexpr int kPlanThreads = 256;  // one block; the scans run in tiles of this many documents / segments
+__global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constant__ FwdParams p, int keep_mzero) {
   Header* hd = ws_ptr<Header>(p, p.L.header);
   int32_t* seq_chunk0 = ws_ptr<int32_t>(p, p.L.seq_chunk0);
   int32_t* seq_seg0 = ws_ptr<int32_t>(p, p.L.seq_seg0);
@@ -41,7 +42,7 @@ __global__ void __launch_bounds__(1024) plan_kernel(const __grid_constant__ FwdP
   const int tid = threadIdx.x, nt = blockDim.x;
   __shared__ int s_bad, s_L, s_longest;
   __shared__ int s_carry[2];
-  __shared__ int s_scan[1024];
+  __shared__ int s_scan[kPlanThreads];
   if (tid == 0) {
     s_bad = 0;
     s_longest = 0;
@@ -129,41 +130,64 @@ __global__ void __launch_bounds__(1024) plan_kernel(const __grid_constant__ FwdP
   if (!keep_mzero)
     for (int e = tid; e < (int)p.L.slots * p.d.Hv; e += nt) mz[e] = 0;
   __syncthreads();
-  // slots and pass-1 units (serial: only split segments get them)
+  // slots and pass-1 units: only split segments other than the last of their document get them
+  // (exact mode); a block scan over the segments numbers them in segment order
+  int32_t* slot = ws_ptr<int32_t>(p, p.L.seg_slot);
+  int32_t* p1 = ws_ptr<int32_t>(p, p.L.p1_list);
   if (tid == 0) {
-    int32_t* slot = ws_ptr<int32_t>(p, p.L.seg_slot);
-    int32_t* p1 = ws_ptr<int32_t>(p, p.L.p1_list);
-    int ns = 0, nu = 0, out_of_slots = 0;
-    for (int s = 0; s < total_segs; ++s) {
+    s_carry[0] = 0;
+    s_carry[1] = 0;
+  }
+  __syncthreads();
+  for (int base = 0; base < total_segs; base += nt) {
+    const int s = base + tid;
+    int need = 0, units = 0;
+    if (s < total_segs) {
       const int i = si[4 * s];
       const bool last = (s + 1 == seq_seg0[i + 1]);
       const bool split = (seq_seg0[i + 1] - seq_seg0[i]) > 1;
-      slot[s] = -1;
-      if (split && !last && p.d.mode == 0) {
-        if (ns >= p.L.slots) {
-          out_of_slots = 1;
-          break;
-        }
-        slot[s] = ns++;
-        if (si[4 * s + 3] == -1) {
-          p1[2 * nu] = s;
-          p1[2 * nu + 1] = 2;  // end state from the known start, published directly
-          ++nu;
+      need = (split && !last && p.d.mode == 0) ? 1 : 0;
+      units = need ? (si[4 * s + 3] == -1 ? 1 : 2) : 0;
+    }
+    const int mine = (need << 16) | units;  // a tile holds at most nt segments: no carry between the halves
+    s_scan[tid] = mine;
+    __syncthreads();
+    for (int off = 1; off < nt; off <<= 1) {
+      const int v = (tid >= off) ? s_scan[tid - off] : 0;
+      __syncthreads();
+      s_scan[tid] += v;
+      __syncthreads();
+    }
+    const int excl = s_scan[tid] - mine;
+    if (s < total_segs) {
+      const int sl = s_carry[0] + (excl >> 16), u = s_carry[1] + (excl & 0xFFFF);
+      slot[s] = (need && sl < p.L.slots) ? sl : -1;
+      if (need && sl < p.L.slots) {
+        if (units == 1) {
+          p1[2 * u] = s;
+          p1[2 * u + 1] = 2;  // end state from the known start, published directly
         } else {
-          p1[2 * nu] = s;
-          p1[2 * nu + 1] = 0;  // transition M
-          ++nu;
-          p1[2 * nu] = s;
-          p1[2 * nu + 1] = 1;  // end state from zero B
-          ++nu;
+          p1[2 * u] = s;
+          p1[2 * u + 1] = 0;  // transition M
+          p1[2 * u + 2] = s;
+          p1[2 * u + 3] = 1;  // end state from zero B
         }
       }
     }
+    __syncthreads();
+    if (tid == nt - 1) {
+      s_carry[0] += s_scan[tid] >> 16;
+      s_carry[1] += s_scan[tid] & 0xFFFF;
+    }
+    __syncthreads();
+  }
+  if (tid == 0) {
+    const int out_of_slots = s_carry[0] > p.L.slots ? 1 : 0;
     hd->status = out_of_slots ? kErrWorkspace : 0;
     hd->n_chunks = out_of_slots ? 0 : total_chunks;
     hd->n_segs = out_of_slots ? 0 : total_segs;
     hd->seg_chunks = L;
-    hd->n_p1 = out_of_slots ? 0 : nu;
+    hd->n_p1 = out_of_slots ? 0 : s_carry[1];
     hd->q_p1 = 0;
     hd->q_chain = 0;
   }
@@ -1764,7 +1788,7 @@ int launch_fwd(const FwdParams& p, cudaStream_t stream, cudaEvent_t* ev, bool pl
     if (ev && ev[i]) cudaEventRecord(ev[i], stream);
   };
   mark(0);
-  plan_kernel<<<1, 1024, 0, stream>>>(p, plan_only ? 1 : 0);
+  plan_kernel<<<1, kPlanThreads, 0, stream>>>(p, plan_only ? 1 : 0);
   mark(1);
   if (plan_only) {
     for (int i = 2; i < 8; ++i) mark(i);
