@@ -83,6 +83,18 @@ def kernel_counts(T, Hk, Hv, N):
             "kkt_solve_kernel<record>": (kkt_b, kkt_f), "out_kernel": (out_b, out_f)}
 
 
+def whole_job(ms, tokens_per_rank, world, device=None):
+    """Replicas: the slowest rank's mean step time (max over ranks) and the whole-job rate in
+    Mtokens/s (every rank's tokens over that time). One process per GPU, no collective on the
+    data path; this reduction runs once, after the timed steps."""
+    if world > 1:
+        import torch
+        t = torch.tensor([float(ms)], device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    return ms, tokens_per_rank * world / (ms * 1e-3) / 1e6
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -372,12 +384,7 @@ def run_ours(args, rank, world, local_rank):
         torch.distributed.barrier()
     clk = clocks.stop() if clocks else None
     step_ms = np.array([a.elapsed_time(b) for a, b in zip(starts, stops)])
-    ms = float(step_ms.mean())
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
-    value = T * world / (ms * 1e-3) / 1e6
+    ms, value = whole_job(float(step_ms.mean()), T, world, dev)
 
     # context, outside the timed region: the inference forward and the backward that recomputes
     ctx = None
