@@ -187,11 +187,12 @@ __device__ __forceinline__ void rev_store_ds(const Ctx& cx, RevSmem& sm, const f
 
 // Chunks [gc0, gc1) of one document for value head h, in reverse, from dS (epilogue registers;
 // its bf16 copy is already in sm.ds): dS becomes dL/dS at the start of chunk gc0. kRecord: also
-// store dL/dS at each chunk end and dV' (bf16 images) for the gradient kernels. All 320 threads
-// call this; returns false after a failed wait.
+// store dL/dS at each chunk end and dV' (bf16 images) for the gradient kernels, for the chunks
+// below gc_rec (the ones above are a warm-up). All 320 threads call this; returns false after a
+// failed wait.
 template <bool kRecord>
 __device__ bool run_rev_ws(const BwdParams& p, Ctx& cx, RevSmem& sm, RevBars& bb, RevPhase& ph, volatile int* abort,
-                           float* dS, int gc0, int gc1, int h, int hk) {
+                           float* dS, int gc0, int gc1, int h, int hk, int gc_rec) {
   const int n = gc1 - gc0;
   if (n <= 0) return true;
   const int Hv = p.d.Hv;
@@ -358,7 +359,7 @@ __device__ bool run_rev_ws(const BwdParams& p, Ctx& cx, RevSmem& sm, RevBars& bb
   };
   // dL/dS at the end of chunk j (the bf16 image in sm.ds) goes to the records
   auto record_ds = [&](int j) {
-    if (kRecord && cx.tid == 0) {
+    if (kRecord && cx.tid == 0 && chunk_of(j) < gc_rec) {
       bulk_wait_read_all();
       bulk_store(p.ws + p.L.ds_img + ((size_t)chunk_of(j) * Hv + h) * 32768, sm.ds, 32768);
       bulk_commit_group();
@@ -397,7 +398,7 @@ __device__ bool run_rev_ws(const BwdParams& p, Ctx& cx, RevSmem& sm, RevBars& bb
       }
     }
     r_handoff(cx.tid, &bb.epi1);
-    if (kRecord && cx.tid == 0) {
+    if (kRecord && cx.tid == 0 && gc < gc_rec) {
       bulk_store(p.ws + p.L.dvp_img + ((size_t)gc * Hv + h) * 16384, sm.dvp, 16384);
       bulk_commit_group();
     }
@@ -672,13 +673,14 @@ __global__ void __launch_bounds__(kRevThreads, 1) rev_chain_kernel(const __grid_
       }
     return true;
   };
-  auto run = [&](int c0, int nch, int h, int hk, bool record) -> bool {
+  // chunks [c0, c0 + nch) in reverse; with `record`, records for the chunks below rec_end
+  auto run = [&](int c0, int nch, int h, int hk, bool record, int rec_end) -> bool {
     if (epi) rev_store_ds(cx, sm, dS);
     sync_generic_to_async();
     if (record)
-      run_rev_ws<true>(p, cx, sm, rbars, ph, &s_abort, dS, c0, c0 + nch, h, hk);
+      run_rev_ws<true>(p, cx, sm, rbars, ph, &s_abort, dS, c0, c0 + nch, h, hk, rec_end);
     else
-      run_rev_ws<false>(p, cx, sm, rbars, ph, &s_abort, dS, c0, c0 + nch, h, hk);
+      run_rev_ws<false>(p, cx, sm, rbars, ph, &s_abort, dS, c0, c0 + nch, h, hk, c0);
     __syncthreads();
     return s_abort == 0;
   };
@@ -704,14 +706,14 @@ __global__ void __launch_bounds__(kRevThreads, 1) rev_chain_kernel(const __grid_
       if (s < last) {
         if (epi)
           for (int c = 0; c < 64; ++c) dS[c] = 0.f;
-        ok = run(c0, nch, h, hk, false);
+        ok = run(c0, nch, h, hk, false, c0);
         if (!ok) break;
         if (epi) rev_save(cx, rb + ((size_t)slot[s] * Hv + h) * st, dS);
         __syncthreads();
         continue;
       }
       if (doc_has_forks(p, seq)) continue;  // its end gradient waits for the forked documents
-      ok = doc_end_grad(seq, h) && run(c0, nch, h, hk, false);
+      ok = doc_end_grad(seq, h) && run(c0, nch, h, hk, false, c0);
       if (!ok) break;
       if (epi) rev_save(cx, rpub + ((size_t)slot[s - 1] * Hv + h) * st, dS);
       rev_publish(&rflags[s * Hv + h]);
@@ -729,10 +731,11 @@ __global__ void __launch_bounds__(kRevThreads, 1) rev_chain_kernel(const __grid_
       ok = doc_end_grad(seq, h);
     } else if (wf >= 0) {
       // the decay over chunks [c0 + nch, wf) leaves the later gradient below fp32 resolution:
-      // warm up from zero over them
+      // warm up from zero over them (a run of its own: a lighter path than the recording one,
+      // and the early publication below needs dL/dS at the segment end)
       if (epi)
         for (int c = 0; c < 64; ++c) dS[c] = 0.f;
-      ok = run(c0 + nch, wf - (c0 + nch), h, hk, false);
+      ok = run(c0 + nch, wf - (c0 + nch), h, hk, false, c0);
     } else if (s + 1 != last && mzero[slot[s + 1] * Hv + h]) {
       if (epi) rev_load(cx, rb + ((size_t)slot[s + 1] * Hv + h) * st, dS, false);  // M_{s+1} = 0: no wait
     } else {
@@ -751,7 +754,7 @@ __global__ void __launch_bounds__(kRevThreads, 1) rev_chain_kernel(const __grid_
       }
       rev_publish(&rflags[s * Hv + h]);
     }
-    if (!run(c0, nch, h, hk, true)) {
+    if (!run(c0, nch, h, hk, true, c0 + nch)) {
       set_status(hd, kErrTimeout);
       break;
     }

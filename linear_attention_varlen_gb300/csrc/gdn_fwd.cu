@@ -1094,11 +1094,11 @@ __device__ __forceinline__ void store_state_comp(RecSmem& sm, const ChainCtx& cx
 
 // Run chunks [gc0, gc1) of one document for value head h from S (epilogue registers; its hi / lo
 // images are already in sm.s / sm.slo). kWithU = false runs the transition chain (no U term).
-// kStore writes the records of every chunk of the run. All 320 threads call this; returns false
-// after a failed wait.
+// kStore writes the records of the chunks from gc_rec on (the ones before are a warm-up). All 320
+// threads call this; returns false after a failed wait.
 template <bool kWithU, bool kStore>
 __device__ bool run_ws_rec(const FwdParams& p, ChainCtx& cx, WsBars& bb, WsPhase& ph, volatile int* abort,
-                           float* S, int gc0, int gc1, int h, int hk) {
+                           float* S, int gc0, int gc1, int h, int hk, int gc_rec) {
   RecSmem& sm = *reinterpret_cast<RecSmem*>(cx.base);
   const int n = gc1 - gc0;
   if (n <= 0) return true;
@@ -1220,7 +1220,7 @@ __device__ bool run_ws_rec(const FwdParams& p, ChainCtx& cx, WsBars& bb, WsPhase
     bulk_commit_group();
   };
   e_handoff(cx.tid, &bb.epi2);  // S(gc0) is staged
-  if (kStore && cx.tid == 0) store_s_record(gc0);
+  if (kStore && cx.tid == 0 && gc0 >= gc_rec) store_s_record(gc0);
   auto staging = [&](int j) {
     role_wait(&bb.full[j % kRecStages], ph.full[j % kRecStages], abort);
     role_wait(&bb.pre_done, ph.pre_done, abort);
@@ -1254,8 +1254,9 @@ __device__ bool run_ws_rec(const FwdParams& p, ChainCtx& cx, WsBars& bb, WsPhase
     {
       // V' = D_V: its records (hi / lo) and V'_s = e^{gamma_C - gamma_t} V' (hi / lo) for K^T V'_s
       const float sc[2] = {__expf(gC - gm[r0]), __expf(gC - gm[r0 + 8])};
-      uint8_t* vph = kStore ? p.vp_img + rec(gc) * 16384 + cx.half * 8192 : nullptr;
-      uint8_t* vpl = kStore ? p.vp_lo_img + rec(gc) * 16384 + cx.half * 8192 : nullptr;
+      const bool recj = kStore && gc >= gc_rec;
+      uint8_t* vph = recj ? p.vp_img + rec(gc) * 16384 + cx.half * 8192 : nullptr;
+      uint8_t* vpl = recj ? p.vp_lo_img + rec(gc) * 16384 + cx.half * 8192 : nullptr;
       const int qa = cx.lane & 3;
 #pragma unroll
       for (int hc = 0; hc < 2; ++hc) {
@@ -1274,10 +1275,10 @@ __device__ bool run_ws_rec(const FwdParams& p, ChainCtx& cx, WsBars& bb, WsPhase
             split_pair(x0 * sc[rr], x1 * sc[rr], hi, lo);
             *reinterpret_cast<uint32_t*>(sm.vs[cx.half] + off) = hi;
             *reinterpret_cast<uint32_t*>(sm.vslo[cx.half] + off) = lo;
-            if (kStore) split_pair(x0, x1, rh[rr][k], rl[rr][k]);
+            if (recj) split_pair(x0, x1, rh[rr][k], rl[rr][k]);
           }
         }
-        if (kStore) {
+        if (recj) {
           // a 4x4 transpose inside each group of four lanes leaves lane qa with the whole 16-byte
           // unit 4 hc + qa of its rows: one 16-byte store per unit instead of four 4-byte ones
 #pragma unroll
@@ -1309,7 +1310,7 @@ __device__ bool run_ws_rec(const FwdParams& p, ChainCtx& cx, WsBars& bb, WsPhase
       store_state_comp(sm, cx, S);
     }
     e_handoff(cx.tid, &bb.epi2, &bb.empty[st]);
-    if (kStore && j + 1 < n && cx.tid == 0) store_s_record(gc + 1);
+    if (kStore && j + 1 < n && gc + 1 >= gc_rec && cx.tid == 0) store_s_record(gc + 1);
   }
   if (cx.tid == 0) bulk_wait_all();  // every record store has landed before the buffers are reused
   return !*abort;
@@ -1418,13 +1419,13 @@ __global__ void __launch_bounds__(kWsThreads, 1) chain_kernel(const __grid_const
   auto run_fast = [&](int g0, int g1, int g_out, int h, int hk, bool with_u) -> bool {
     if constexpr (rec) {
       if (!with_u) {
-        run_ws_rec<false, false>(p, cx, wbars, ph, &s_abort, S, g0, g1, h, hk);
+        run_ws_rec<false, false>(p, cx, wbars, ph, &s_abort, S, g0, g1, h, hk, g1);
       } else {
-        // the state after the first part is staged by its last chunk
+        // records from g_out on; the chunks before (a warm-up) run without the record path
         const int gm = g_out < g0 ? g0 : (g_out > g1 ? g1 : g_out);
-        if (gm > g0) run_ws_rec<true, false>(p, cx, wbars, ph, &s_abort, S, g0, gm, h, hk);
+        if (gm > g0) run_ws_rec<true, false>(p, cx, wbars, ph, &s_abort, S, g0, gm, h, hk, gm);
         if (gm > g0 && g1 > gm) __syncthreads();
-        if (g1 > gm && s_abort == 0) run_ws_rec<true, true>(p, cx, wbars, ph, &s_abort, S, gm, g1, h, hk);
+        if (g1 > gm && s_abort == 0) run_ws_rec<true, true>(p, cx, wbars, ph, &s_abort, S, gm, g1, h, hk, gm);
       }
     } else {
       if (with_u)
@@ -1607,8 +1608,17 @@ __global__ void __launch_bounds__(kWsThreads, 1) chain_kernel(const __grid_const
     if (!have_start) break;
     store_s();
     sync_generic_to_async();
+    const bool publishes = pub_next && !__ldcg(&mzero[slot[s] * Hv + h]);
+    if (publishes && first_chunk < c0) {
+      // the publication below needs the state at the segment start: warm up first
+      if (!run_fast(first_chunk, c0, c0, h, hk, true)) {
+        set_status(hd, kErrTimeout);
+        break;
+      }
+      first_chunk = c0;
+    }
     // early publication of this segment's end state (exact split), unless its transition is zero
-    if (pub_next && !__ldcg(&mzero[slot[s] * Hv + h])) {
+    if (publishes) {
       const size_t off = ((size_t)slot[s] * Hv + h) * st_elems;
       if (!affine(ws_ptr<float>(p, p.L.mmat) + off, ws_ptr<float>(p, p.L.bmat) + off, ws_ptr<float>(p, p.L.pub) + off)) {
         set_status(hd, kErrTimeout);

@@ -140,3 +140,17 @@ def mixed_decay_problem(name, seed, nchunks=30, Hk=1, Hv=2, with_dout=False, bet
         beta[a:b] *= beta_boost
         p.beta = beta.astype(np.float32)
     return p
+
+
+def fast_then_slow_problem(name, seed, fast_chunks=8, slow_chunks=40, Hk=1, Hv=2, with_dout=False):
+    """One document: fast decay (u ~ N(-3, 1)) over its first chunks, then slow decay (u ~ N(6, 1))
+    for longer than a warm-up window can reach back. With short segments, a segment a little
+    under a window after the fast stretch warms up while the next one cannot and waits for the
+    state it publishes."""
+    T = 64 * (fast_chunks + slow_chunks) + 5
+    p = synth.make_problem(name, seed, [T], Hk, Hv, with_dout=with_dout, g_mean=6.0)
+    fast = synth.make_problem(name, seed + 1, [T], Hk, Hv, g_mean=-3.0)
+    g = p.g.copy()
+    g[:64 * fast_chunks] = fast.g[:64 * fast_chunks]
+    p.g = g.astype(np.float32)
+    return p

@@ -8,7 +8,8 @@ import pytest
 import oracle
 import synth
 from tests import chunked_ref as cr
-from tests.gpu_util import assert_close, errors, head_slice, mixed_decay_problem, run_fwd, to_device
+from tests.gpu_util import (assert_close, errors, fast_then_slow_problem, head_slice, mixed_decay_problem, run_fwd,
+                            to_device)
 
 pytestmark = pytest.mark.gpu
 
@@ -84,6 +85,13 @@ def test_exact_split_mixed_decay(boost):
     boundaries take the published state too."""
     p = mixed_decay_problem(f"split_mixed_b{boost}", 150, beta_boost=boost)
     check_problem(p, gdn.Options(segment_chunks=3))
+
+
+def test_exact_split_warm_segment_publishes_for_the_next():
+    """A segment that warms up (fast decay before it) whose successor cannot (slow decay for
+    longer than a window) publishes its end state from its warmed-up start state."""
+    p = fast_then_slow_problem("split_warm_pub", 160)
+    check_problem(p, gdn.Options(segment_chunks=4))
 
 
 def test_exact_split_with_initial_state_and_fork():

@@ -8,7 +8,7 @@ import pytest
 
 import oracle
 import synth
-from tests.gpu_util import assert_close, errors, mixed_decay_problem, run_bwd, run_train
+from tests.gpu_util import assert_close, errors, fast_then_slow_problem, mixed_decay_problem, run_bwd, run_train
 
 pytestmark = pytest.mark.gpu
 
@@ -102,6 +102,12 @@ def test_train_split_mixed_decay_equals_recompute():
     b = run_bwd(p, opts)
     for key in KEYS:
         np.testing.assert_array_equal(a[key], b[key])
+
+
+def test_train_split_warm_segment_publishes():
+    """Forward and reverse: segments that warm up next to segments that wait for a publication."""
+    p = fast_then_slow_problem("train_warm_pub", 470, with_dout=True)
+    check_train(p, gdn.Options(segment_chunks=4), stress=True)
 
 
 def test_train_rejects_truncation_mode():
