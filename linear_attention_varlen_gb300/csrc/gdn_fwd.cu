@@ -217,6 +217,7 @@ struct KktSmem {
   float beta[kKktHeads][64];
   float eg[kKktHeads][64];               // e^{gamma}
   float egi[kKktHeads][64];              // e^{-gamma} (factored path only)
+  float be[kKktHeads][64];               // beta e^{gamma}
   int contr[kKktHeads][2];               // per warp of a group: every token has 0 <= beta |k|^2 <= 2
 };
 
@@ -321,6 +322,7 @@ __global__ void __launch_bounds__(256, 2) kkt_solve_kernel(const __grid_constant
   float* bet = sm.beta[grp];
   float* eg = sm.eg[grp];
   float* egi = sm.egi[grp];
+  float* be = sm.be[grp];
   const int sub = t >> 5;  // warp of the group: columns 32 sub ..; rows and terms below 32 sub are zero
   for (int hb = 0; hb < G; hb += kKktHeads) {
     if (hb + grp < G) {  // groups without a head this round skip to the CTA barrier below
@@ -347,6 +349,7 @@ __global__ void __launch_bounds__(256, 2) kkt_solve_kernel(const __grid_constant
         gam_ws[rec * 64 + t] = sc;
         eg[t] = __expf(sc);
         egi[t] = __expf(-sc);
+        be[t] = bi * eg[t];
         group_sync(grp);
         if (t >= 32) gam[t] = sc;
         group_sync(grp);
@@ -358,45 +361,48 @@ __global__ void __launch_bounds__(256, 2) kkt_solve_kernel(const __grid_constant
         // T goes to A's buffer row by row; the second warp of the group (columns 32-63) starts
         // at row 32 (rows and terms below are zero).
         float y[64];
+        // rows in groups of four: their beta e^{gamma} and e^{-gamma} come in two vector loads
+#define GDN_KKT_ROW(R, M0)                                                                 \
+  {                                                                                        \
+    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;                                          \
+    _Pragma("unroll") for (int m = (M0); m + 4 <= (R); m += 4) {                           \
+      const float4 kv = *reinterpret_cast<const float4*>(&sm.kk[(R)][m]);                  \
+      a0 += kv.x * y[m];                                                                   \
+      a1 += kv.y * y[m + 1];                                                               \
+      a2 += kv.z * y[m + 2];                                                               \
+      a3 += kv.w * y[m + 3];                                                               \
+    }                                                                                      \
+    _Pragma("unroll") for (int m = (R) & ~3; m < (R); ++m) a0 += sm.kk[(R)][m] * y[m];    \
+    const float xr = (((R) == t) ? 1.f : 0.f) - cq[(R) & 3] * ((a0 + a1) + (a2 + a3));     \
+    A[(R)][t] = xr;                                                                        \
+    y[(R)] = eq[(R) & 3] * xr;                                                             \
+  }
         if (sub == 0) {
 #pragma unroll
-          for (int r = 0; r < 64; ++r) {
-            float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-#pragma unroll
-            for (int m = 0; m + 4 <= r; m += 4) {
-              const float4 kv = *reinterpret_cast<const float4*>(&sm.kk[r][m]);
-              a0 += kv.x * y[m];
-              a1 += kv.y * y[m + 1];
-              a2 += kv.z * y[m + 2];
-              a3 += kv.w * y[m + 3];
-            }
-#pragma unroll
-            for (int m = r & ~3; m < r; ++m) a0 += sm.kk[r][m] * y[m];
-            const float xr = ((r == t) ? 1.f : 0.f) - bet[r] * eg[r] * ((a0 + a1) + (a2 + a3));
-            A[r][t] = xr;
-            y[r] = egi[r] * xr;
+          for (int rb = 0; rb < 64; rb += 4) {
+            const float4 c4 = *reinterpret_cast<const float4*>(&be[rb]);
+            const float4 e4 = *reinterpret_cast<const float4*>(&egi[rb]);
+            const float cq[4] = {c4.x, c4.y, c4.z, c4.w}, eq[4] = {e4.x, e4.y, e4.z, e4.w};
+            GDN_KKT_ROW(rb, 0)
+            GDN_KKT_ROW(rb + 1, 0)
+            GDN_KKT_ROW(rb + 2, 0)
+            GDN_KKT_ROW(rb + 3, 0)
           }
         } else {
 #pragma unroll
           for (int r = 0; r < 32; ++r) A[r][t] = 0.f;
 #pragma unroll
-          for (int r = 32; r < 64; ++r) {
-            float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-#pragma unroll
-            for (int m = 32; m + 4 <= r; m += 4) {
-              const float4 kv = *reinterpret_cast<const float4*>(&sm.kk[r][m]);
-              a0 += kv.x * y[m];
-              a1 += kv.y * y[m + 1];
-              a2 += kv.z * y[m + 2];
-              a3 += kv.w * y[m + 3];
-            }
-#pragma unroll
-            for (int m = r & ~3; m < r; ++m) a0 += sm.kk[r][m] * y[m];
-            const float xr = ((r == t) ? 1.f : 0.f) - bet[r] * eg[r] * ((a0 + a1) + (a2 + a3));
-            A[r][t] = xr;
-            y[r] = egi[r] * xr;
+          for (int rb = 32; rb < 64; rb += 4) {
+            const float4 c4 = *reinterpret_cast<const float4*>(&be[rb]);
+            const float4 e4 = *reinterpret_cast<const float4*>(&egi[rb]);
+            const float cq[4] = {c4.x, c4.y, c4.z, c4.w}, eq[4] = {e4.x, e4.y, e4.z, e4.w};
+            GDN_KKT_ROW(rb, 32)
+            GDN_KKT_ROW(rb + 1, 32)
+            GDN_KKT_ROW(rb + 2, 32)
+            GDN_KKT_ROW(rb + 3, 32)
           }
         }
+#undef GDN_KKT_ROW
         group_sync(grp);
       } else {
         // A, column t (rows below the diagonal), one exponential per entry
