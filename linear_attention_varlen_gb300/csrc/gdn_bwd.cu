@@ -1,16 +1,19 @@
 // Backward of the chunked Gated DeltaNet (sm_103a).
 //
-// The backward recomputes the forward chunk states instead of keeping them from the forward
-// call ("How to Speed Up GDN Kernels for Qwen Models", section "Lever 2": the backward pass
-// recomputes hidden states in one dedicated pass), then runs the state-gradient chain in
-// reverse and the per-chunk gradients in parallel:
+// The backward recomputes the forward chunk states ("How to Speed Up GDN Kernels for Qwen
+// Models", section "Lever 2": the backward pass recomputes hidden states in one dedicated pass),
+// or finds them in the workspace when the forward of a training step kept them (the same
+// recompute, run by the forward, which then forms o from the records), then runs the
+// state-gradient chain in reverse and the per-chunk gradients in parallel:
 //
 //   1. forward recompute (plan, kkt_solve, chain in record mode): for every chunk c and value
 //      head, S_c (state at the chunk start, bf16), V'_c = U - W S_c (bf16) and T_c (fp32).
 //   2. rev_chain_kernel, per (document, value head), chunks in reverse:
 //        dV' = K~ dS_{c+1} + P^T dO,    dS_c = e^{gamma_C} dS_{c+1} + Q~^T dO - W^T dV'
 //      (K~ = diag(e^{gamma_C - gamma}) K, Q~ = diag(e^{gamma}) Q, P = (Q K^T) o E); records
-//      dS_{c+1} and dV' per chunk, and dL/dS at the document start. A document whose final
+//      dS_{c+1} and dV' per chunk, and dL/dS at the document start; segments warm up from zero
+//      over the following chunks when the decay there provably hides the later gradient, as in
+//      the forward. A document whose final
 //      state was forked first collects the d(initial state) of every document that started from
 //      it ("Musings on long-context fine-tuning", section "Backward through P": the gradients of
 //      the branches add up at the shared state).

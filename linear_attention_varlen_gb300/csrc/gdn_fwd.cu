@@ -1,22 +1,30 @@
 // Forward kernels of the chunked Gated DeltaNet over packed varlen batches (sm_103a).
 //
 //   plan_kernel       chunk map, segment map, dependencies, queue and flag reset (device planner)
-//   kkt_solve_kernel  per (chunk, key head): K K^T on tcgen05, then per value head of the group the
-//                     chunk-local cumulative gate gamma, A = diag(beta) (e^{gamma_i-gamma_j} o K K^T)
-//                     (strictly lower), T = (I + A)^{-1} by blocked forward substitution, and
-//                     T diag(beta e^gamma), T diag(beta) in bf16 ("How to Speed Up GDN Kernels for Qwen
-//                     Models", sections "What GDN actually computes" (kkt_solve, one 64x64 system per
-//                     chunk per head) and "Lever 2" (gate cumsum once per chunk, triangular inverse
-//                     solved once and reused by the output path and the state update)).
+//   kkt_solve_kernel  per (chunk, key head): K K^T (and Q K^T) on tcgen05, then per value head of
+//                     the group the chunk-local cumulative gate gamma, T = (I + A)^{-1} with
+//                     A = diag(beta) (e^{gamma_i-gamma_j} o K K^T) (strictly lower) by forward
+//                     substitution, T diag(beta e^gamma), T diag(beta) and P = scale (Q K^T o E) in
+//                     bf16, and a per-chunk flag for the warm-up bound below ("How to Speed Up GDN
+//                     Kernels for Qwen Models", sections "What GDN actually computes" (kkt_solve, one
+//                     64x64 system per chunk per head) and "Lever 2" (gate cumsum once per chunk,
+//                     triangular inverse solved once and reused by the output path and the state
+//                     update)).
 //   chain_kernel<OUT> persistent over (segment, value head) items in dependency order: the state S
 //                     (fp32, 128x128) lives in registers across 8 warps; per chunk, tcgen05 MMAs compute
-//                     W = T_w K, P = Q K^T, then [Q~; -W] S + [0; U] (U = T_u V preloaded into the same
-//                     accumulator), V' = U - W S, S += K^T diag(e^{gamma_C - gamma}) V', O = Q~ S + P V'.
+//                     W = T_w K, then [Q~; -W] S + [0; U] (U = T_u V), V' = U - W S,
+//                     S += K^T diag(e^{gamma_C - gamma}) V', O = Q~ S + P V'. A segment starts from the
+//                     state published by the previous one, or from a warm-up from zero when the decay
+//                     in between provably leaves the earlier state below fp32 resolution.
 //   chain_kernel<P1>  pass 1 of the exact segment split: per segment, the end state from zero (B) and
 //                     the segment transition (M, started from I) -- or, for a first segment with a known
 //                     start, its end state directly -- so that segment end states can be published as
 //                     soon as the start state is known ("Lever 1": a sequence is split into segments
-//                     that run in parallel; here the carry is exact instead of truncated).
+//                     that run in parallel; here the carry is exact instead of truncated). Units that
+//                     no segment reads (the next one warms up) are skipped.
+//   chain_kernel<·, record> the same chain in compensated bf16 writing per-chunk records (chunk-start
+//                     S, V') for the backward: its recompute, or the forward of a training step,
+//                     which then forms o from the records in out_kernel.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
