@@ -787,9 +787,8 @@ __global__ void __launch_bounds__(kRevThreads, 1) rev_chain_kernel(const __grid_
 struct GradSmem {
   uint8_t q[2][8192];
   uint8_t k[2][8192];
-  float kkf[4096];         // K K^T                (fz layout)
-  float qkf[4096];         // scale Q K^T          (fz layout)
-  uint8_t bS[2][16384];    // S_c image       | phase 2: T fp32 [0, 16K) (fz), T bf16 [16K, 24K)
+  uint8_t tb[24576];       // T fp32 [0, 16K) (fz layout), T bf16 image [16K, 24K)
+  uint8_t bS[2][16384];    // S_c image (the next head's once (b) has read it)
   uint8_t bdS[2][16384];   // dS_{c+1} image  | phase 2: T_w [0, 8K), T_u [8K, 16K), dT [16K, 24K), R [24K, 32K)
   uint8_t bVp[2][8192];    // V' -> V'_s (then the next head's V')
   uint8_t bdVp[2][8192];   // dV'             | fp32 64x64 scratch (kx products)
@@ -808,7 +807,8 @@ constexpr size_t kGradSmemBytes = sizeof(GradSmem) + 1024;
 // Chunk decay above which e^{gamma_i} and e^{-gamma_j} both stay finite in fp32 (gamma is the
 // chunk-local cumulative log-decay, nonincreasing, so gamma_63 is its minimum).
 constexpr float kFactorMin = -80.f;
-constexpr uint32_t kGtK = 128, kGt1 = 256, kGt2 = 384;
+// TMEM: K K^T and Q K^T of the key head (kept for the whole CTA), dk, two working accumulators
+constexpr uint32_t kGtC = 0, kGtK = 128, kGt1 = 256, kGt2 = 384;
 
 // Column sums of one or two fp32 64x64 fz matrices over rows [0, 64) with all 256 threads:
 // out[j] = sum_i X[i][j]. Ends with the result visible to every thread.
@@ -870,7 +870,7 @@ __global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ Bw
   // Loads of one value head's records, in the order their buffers become free. The phase-1 set
   // (S, dS, V', dV', dO images and gamma) lands on bar_p1: its transaction count is armed by the
   // first piece, the other pieces follow as the previous head releases their buffers.
-  const uint32_t kP1Bytes = 32768 * 2 + 16384 + 2 * 8192;  // gamma and V' are counted where issued
+  const uint32_t kP1Bytes = 32768 + 16384 + 2 * 8192;  // gamma, V' and S are counted where issued
   auto rec_of = [&](int hh2) { return (size_t)chunk * Hv + hk * G + hh2; };
   auto load_do_gam = [&](int hh2) {  // thread 0; arms bar_p1
     mbar_expect_tx(&bar_p1, 256);
@@ -880,10 +880,11 @@ __global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ Bw
     tma_load_3d(sm.bdO[1], &p.tm_do, 64, hk * G + hh2, tok0, &bar_p1);
   };
   auto load_dvp = [&](int hh2) { bulk_load(sm.bdVp[0], p.ws + p.L.dvp_img + rec_of(hh2) * 16384, 16384, &bar_p1); };
-  auto load_s_ds = [&](int hh2) {
+  auto load_s = [&](int hh2) {
+    mbar_expect_tx(&bar_p1, 32768);
     bulk_load(sm.bS[0], p.ws + p.L.st_img + rec_of(hh2) * 32768, 32768, &bar_p1);
-    bulk_load(sm.bdS[0], p.ws + p.L.ds_img + rec_of(hh2) * 32768, 32768, &bar_p1);
   };
+  auto load_ds = [&](int hh2) { bulk_load(sm.bdS[0], p.ws + p.L.ds_img + rec_of(hh2) * 32768, 32768, &bar_p1); };
   auto load_vp = [&](int hh2) {
     mbar_expect_tx(&bar_p1, 16384);
     bulk_load(sm.bVp[0], p.ws + p.L.vp_img + rec_of(hh2) * 16384, 16384, &bar_p1);
@@ -908,35 +909,23 @@ __global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ Bw
   if (ok) {
     if (tid == 0) {
       for (int ks = 0; ks < 8; ++ks) {
-        umma_bf16(tm + kGt1, kmajor_desc(smem_u32(sm.k[0]), 8192, ks), kmajor_desc(smem_u32(sm.k[0]), 8192, ks),
+        umma_bf16(tm + kGtC, kmajor_desc(smem_u32(sm.k[0]), 8192, ks), kmajor_desc(smem_u32(sm.k[0]), 8192, ks),
                   idesc_bf16(64, 64, 0, 0), ks > 0);
-        umma_bf16(tm + kGt1 + 64, kmajor_desc(smem_u32(sm.q[0]), 8192, ks), kmajor_desc(smem_u32(sm.k[0]), 8192, ks),
+        umma_bf16(tm + kGtC + 64, kmajor_desc(smem_u32(sm.q[0]), 8192, ks), kmajor_desc(smem_u32(sm.k[0]), 8192, ks),
                   idesc_bf16(64, 64, 0, 0), ks > 0);
       }
     }
-    ok = cx.commit_wait();
-  }
-  if (ok) {
-    for (int cc = 0; cc < 32; cc += 16) {
-      float a[16], b[16];
-      tmem_ld16(tm + kGt1 + cx.lane_base() + 32 * cx.half + cc, a);
-      tmem_ld16(tm + kGt1 + 64 + cx.lane_base() + 32 * cx.half + cc, b);
-      tmem_ld_wait();
-      if (has_row)
-        for (int x = 0; x < 16; ++x) {
-          const int j = 32 * cx.half + cc + x;
-          sm.kkf[fz(i_row, j)] = a[x];
-          sm.qkf[fz(i_row, j)] = b[x] * p.scale;
-        }
-    }
+    ok = cx.commit_wait();  // K K^T and Q K^T stay in TMEM, read where needed
   }
   __syncthreads();
 
   if (tid == 0 && ok) {
+    // the pieces with their own expect_tx first: the arrival in load_do_gam must come last
+    load_s(0);
+    load_vp(0);
     load_do_gam(0);
     load_dvp(0);
-    load_s_ds(0);
-    load_vp(0);
+    load_ds(0);
   }
   bool first_k = true;
   for (int hh = 0; hh < G && ok; ++hh) {
@@ -993,8 +982,9 @@ __global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ Bw
       const bool factored = gam[63] > kFactorMin;
       float rs[2] = {0.f, 0.f};
       {
-        float v[16], ev[16];
+        float v[16], ev[16], qkv[16];
         tmem_ld16x256_x4(tm + kGt1 + cx.lane_base() + 32 * cx.half, v);
+        tmem_ld16x256_x4(tm + kGtC + 64 + cx.lane_base() + 32 * cx.half, qkv);
         if (factored) {
 #pragma unroll
           for (int k = 0; k < 4; ++k)
@@ -1017,8 +1007,7 @@ __global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ Bw
             const float d0 = (j <= r && r < n) ? v[4 * k + 2 * rr] * ev[4 * k + 2 * rr] : 0.f;
             const float d1 = (j + 1 <= r && r < n) ? v[4 * k + 2 * rr + 1] * ev[4 * k + 2 * rr + 1] : 0.f;
             *reinterpret_cast<uint32_t*>(sm.bP + sw128_pair(r, j)) = pack_bf16x2(d0 * p.scale, d1 * p.scale);
-            const float2 qk = *reinterpret_cast<const float2*>(sm.qkf + fz(r, j));
-            const float e0 = d0 * qk.x, e1 = d1 * qk.y;
+            const float e0 = d0 * qkv[4 * k + 2 * rr] * p.scale, e1 = d1 * qkv[4 * k + 2 * rr + 1] * p.scale;
             *reinterpret_cast<float2*>(dEg + fz(r, j)) = make_float2(e0, e1);
             rs[rr] += e0 + e1;
           }
@@ -1079,9 +1068,10 @@ __global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ Bw
       if (cx.lane == 0) sm.red[cx.warp] = fr;
     }
     if (!(ok = cx.commit_wait())) break;
-    if (tid == 0) {  // S is read: T (fp32) into its buffer (phase 2)
+    if (tid == 0) {  // T (fp32) into its buffer (phase 2); S is read: the next head's S
       mbar_arrive_expect_tx(&bar_v, 16384 + 2 * 8192);
-      bulk_load(sm.bS[0], p.ws + p.L.t_f32 + rec * 16384, 16384, &bar_v);
+      bulk_load(sm.tb, p.ws + p.L.t_f32 + rec * 16384, 16384, &bar_v);
+      if (next) load_s(hh + 1);
     }
     {
       // all 32 lanes: rows r0 = 16 q4 + lane / 4 and r0 + 8, column pairs (tmem_ld16x256_x4)
@@ -1142,8 +1132,8 @@ __global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ Bw
     }
     if (!(ok = wait_bar(&bar_v, ph_v))) break;
     if (!(ok = wait_bar(&bar_tw, ph_tw))) break;
-    const float* Tf = reinterpret_cast<const float*>(sm.bS[0]);
-    uint8_t* Tb = sm.bS[1];                 // T bf16 image (bytes [16K, 24K) of bS)
+    const float* Tf = reinterpret_cast<const float*>(sm.tb);
+    uint8_t* Tb = sm.tb + 16384;            // T bf16 image
     uint8_t* Tw = sm.bdS[0];
     uint8_t* Tu = sm.bdS[0] + 8192;
     uint8_t* dTt = sm.bdS[1];
@@ -1249,15 +1239,16 @@ __global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ Bw
         umma_bf16(tm + kGt1, mnmajor_desc(smem_u32(Tb), 8192, ks), mnmajor_desc(smem_u32(Rt), 8192, ks),
                   idesc_bf16(64, 64, 1, 1), ks > 0);
     if (!(ok = cx.commit_wait())) break;
-    if (tid == 0 && next) load_s_ds(hh + 1);  // T, R, T_w, T_u, dT are read: the next head's S, dS
+    if (tid == 0 && next) load_ds(hh + 1);  // R, T_w, T_u, dT are read: the next head's dS
     float* LK = vyM;  // vy / kx column sums are done
     {
       // all 32 lanes: rows r0 = 16 q4 + lane / 4 and r0 + 8, column pairs (tmem_ld16x256_x4)
       const int c2 = 2 * (cx.lane & 3);
       const int rw[2] = {16 * cx.q4 + (cx.lane >> 2), 16 * cx.q4 + (cx.lane >> 2) + 8};
       const bool factored = gam[63] > kFactorMin;
-      float v[16], ev[16];
+      float v[16], ev[16], kkv[16];
       tmem_ld16x256_x4(tm + kGt1 + cx.lane_base() + 32 * cx.half, v);
+      tmem_ld16x256_x4(tm + kGtC + cx.lane_base() + 32 * cx.half, kkv);
       if (factored) {
 #pragma unroll
         for (int k = 0; k < 4; ++k)
@@ -1278,7 +1269,7 @@ __global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ Bw
         for (int rr = 0; rr < 2; ++rr) {
           const int r = rw[rr], j = 32 * cx.half + 8 * k + c2, x = 4 * k + 2 * rr;
           const float bi = sm.beta[r];
-          const float2 kk = *reinterpret_cast<const float2*>(sm.kkf + fz(r, j));
+          const float2 kk = make_float2(kkv[x], kkv[x + 1]);
           // dA = -v, strictly lower and inside the chunk; L = dA o diag(beta) E
           const float dae0 = (j < r && r < n) ? -v[x] * ev[x] : 0.f;
           const float dae1 = (j + 1 < r && r < n) ? -v[x + 1] * ev[x + 1] : 0.f;
