@@ -195,3 +195,12 @@ def test_split_layout_fills_the_sms(lib):
     assert L == 27 and len(segs) * 8 >= 152 - 8 and len(segs) * 8 <= 152 + 8
     _, segs, L = gdn.plan_host([0, 2048], 8, num_sms=152)
     assert L == 4
+
+
+def test_stage_events_allow_skipped_entries():
+    n = 2 * gdn.NUM_STAGES
+    o = gdn.Options(stage_events=[None] * n).c()  # every entry skipped
+    arr = ctypes.cast(o.stage_events, ctypes.POINTER(ctypes.c_void_p))
+    assert all(arr[i] is None for i in range(n))
+    with pytest.raises(ValueError):
+        gdn.Options(stage_events=[None] * (n - 1)).c()
