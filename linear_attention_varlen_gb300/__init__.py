@@ -238,10 +238,10 @@ def chunk_fwd(q, k, v, g, beta, cu_seqlens, init_idx=None, initial_state=None, o
 
 
 def chunk_bwd(q, k, v, g, beta, cu_seqlens, dout, dfinal_state=None, init_idx=None, initial_state=None,
-              options: Optional[Options] = None, workspace=None, stream=None):
+              options: Optional[Options] = None, workspace=None, stream=None, grads=None):
     """Backward. Returns dict of fp32 gradients dq, dk, dv, dg, dbeta and dinit (None without a pool).
     With options.reuse_forward, `workspace` must be the one a save_for_backward forward of the same
-    inputs used."""
+    inputs used. `grads` may hold preallocated fp32 outputs (keys dq, dk, dv, dg, dbeta, dinit)."""
     torch = _torch()
     if options is not None and options.reuse_forward and workspace is None:
         raise ValueError("reuse_forward needs the workspace of the save_for_backward forward")
@@ -253,12 +253,20 @@ def chunk_bwd(q, k, v, g, beta, cu_seqlens, dout, dfinal_state=None, init_idx=No
         _check(dfinal_state, "dfinal_state", torch.float32, (N, Hv, D, D))
     n_init = 0 if initial_state is None else initial_state.shape[0]
     dev = q.device
-    dq = torch.empty(q.shape, dtype=torch.float32, device=dev)
-    dk = torch.empty(k.shape, dtype=torch.float32, device=dev)
-    dv = torch.empty(v.shape, dtype=torch.float32, device=dev)
-    dg = torch.empty((T, Hv), dtype=torch.float32, device=dev)
-    db = torch.empty((T, Hv), dtype=torch.float32, device=dev)
-    dinit = torch.empty_like(initial_state) if n_init > 0 else None
+    grads = grads or {}
+    f32 = torch.float32
+
+    def out_buf(key, shape):
+        t = grads.get(key)
+        if t is None:
+            return torch.empty(shape, dtype=f32, device=dev)
+        return _check(t, key, f32, shape)
+    dq = out_buf("dq", q.shape)
+    dk = out_buf("dk", k.shape)
+    dv = out_buf("dv", v.shape)
+    dg = out_buf("dg", (T, Hv))
+    db = out_buf("dbeta", (T, Hv))
+    dinit = out_buf("dinit", initial_state.shape) if n_init > 0 else None
     o = _opts(options)
     need = int(load().gdn_bwd_workspace_size(N, T, Hk, Hv, ctypes.byref(o)))
     if workspace is None:
