@@ -21,7 +21,8 @@
 //      (summed over the group in tensor memory), dv, dbeta and dg from S_c, dS_{c+1}, V', dV'
 //      and T, through the reverse mode of the chunk algebra (T = (I + A)^{-1}, W = T diag(beta
 //      e^gamma) K, U = T diag(beta) V, O = Q~ S + P V', S_{c+1} = e^{gamma_C} S + K~^T V').
-//      dq_kernel computes dq the same way with compensated bf16 operands (see there).
+//      dq_kernel computes dq the same way with compensated bf16 operands (see there), and adds
+//      to dg its term through the state part of o, which needs S_c at that accuracy.
 //   4. dinit_reduce_kernel: d(initial_state) of each pool entry = the sum, in document order,
 //      over the documents that start from it.
 //
@@ -1042,11 +1043,8 @@ __global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ Bw
     }
     __syncthreads();
     col_sums(sm, dEg, nullptr, sm.part[4], nullptr, tid);
-    // ---------------- (b) Q S ; dV' S^T (-> dW) ; <dS, S>
+    // ---------------- (b) dV' S^T (-> dW) ; <dS, S>  (the term of dgamma in q S dO is dq_kernel's)
     if (tid == 0) {
-      for (int ks = 0; ks < 8; ++ks)
-        umma_bf16(tm + kGt1, kmajor_desc(smem_u32(sm.q[0]), 8192, ks), mnmajor_desc(smem_u32(sm.bS[0]), 16384, ks),
-                  idesc_bf16(64, 128, 0, 1), ks > 0);
       for (int ks = 0; ks < 8; ++ks)
         umma_bf16(tm + kGt2, kmajor_desc(smem_u32(sm.bdVp[0]), 8192, ks), kmajor_desc(smem_u32(sm.bS[0]), 16384, ks),
                   idesc_bf16(64, 128, 0, 0), ks > 0);
@@ -1077,11 +1075,9 @@ __global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ Bw
       // all 32 lanes: rows r0 = 16 q4 + lane / 4 and r0 + 8, column pairs (tmem_ld16x256_x4)
       const int c2 = 2 * (cx.lane & 3);
       const int rw[2] = {16 * cx.q4 + (cx.lane >> 2), 16 * cx.q4 + (cx.lane >> 2) + 8};
-      float qs[2] = {0.f, 0.f};
 #pragma unroll
       for (int cc = 0; cc < 64; cc += 32) {
-        float v[16], w[16];
-        tmem_ld16x256_x4(tm + kGt1 + cx.lane_base() + 64 * cx.half + cc, v);
+        float w[16];
         tmem_ld16x256_x4(tm + kGt2 + cx.lane_base() + 64 * cx.half + cc, w);
         tmem_ld_wait();
 #pragma unroll
@@ -1089,17 +1085,8 @@ __global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ Bw
 #pragma unroll
           for (int rr = 0; rr < 2; ++rr) {
             const int c = cc + 8 * k + c2, x = 4 * k + 2 * rr;
-            const uint32_t off = sw128_pair(rw[rr], c);
-            const float2 d = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(sm.bdO[cx.half] + off));
-            qs[rr] += d.x * v[x] + d.y * v[x + 1];
-            *reinterpret_cast<uint32_t*>(sm.bW[cx.half] + off) = pack_bf16x2(-w[x], -w[x + 1]);
+            *reinterpret_cast<uint32_t*>(sm.bW[cx.half] + sw128_pair(rw[rr], c)) = pack_bf16x2(-w[x], -w[x + 1]);
           }
-      }
-      qs[0] = quad_sum(qs[0]);
-      qs[1] = quad_sum(qs[1]);
-      if ((cx.lane & 3) == 0) {
-        sm.part[5 + cx.half][rw[0]] = qs[0] * sm.Gm[rw[0]] * p.scale;
-        sm.part[5 + cx.half][rw[1]] = qs[1] * sm.Gm[rw[1]] * p.scale;
       }
     }
     // ---------------- (c) V'_s = diag(e^{gamma_C - gamma}) V' ; dk accumulation (dq has its own kernel)
@@ -1305,7 +1292,7 @@ __global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ Bw
       float dgam = 0.f;
       if (i < n) {
         const float b3 = sm.db3[0][i] + sm.db3[1][i];
-        dgam = sm.part[0][i] + sm.part[1][i] - sm.part[4][i] + sm.part[5][i] + sm.part[6][i] - ktd +
+        dgam = sm.part[0][i] + sm.part[1][i] - sm.part[4][i] - ktd +
                sm.beta[i] * sm.Gm[i] * sm.kx[i] + sm.beta[i] * b3 - sm.cA[i];
       }
       sm.part[7][i] = dgam;
@@ -1359,6 +1346,11 @@ __global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ Bw
 // with S_c and V' in compensated bf16 (hi + lo, two MMAs each) so that dq, whose entries reach
 // O(10) at these shapes, keeps the accuracy of the other gradients; the per-row e^gamma scaling is
 // applied in fp32 and the sum over value heads is kept in fp32 registers.
+//
+// The same compensated dO S^T also gives the term of dgamma_t through the state part of o_t,
+// scale e^{gamma_t} q_t . (S_c dO_t): its suffix sums over the chunk are added to dg, which
+// grad_kernel (launched before, on the same stream) has written with all the other terms. With
+// S_c in bf16 alone this term dominated the error of dg on long slowly decaying documents.
 
 struct DqSmem {
   uint8_t k[2][8192];    // K tile                  (B MN-major: dQK K)
@@ -1369,8 +1361,10 @@ struct DqSmem {
   uint8_t vl[2][8192];   // V' low part
   uint8_t qh[8192];      // scale dQK high part     (A K-major)
   uint8_t ql[8192];      // scale dQK low part
+  uint8_t q[2][8192];    // Q tile (read by the threads: the dgamma term)
   float gam[2][64];      // [head parity]
   float eg[64], egi[64]; // e^{gamma}, e^{-gamma}
+  float qd[2][2][64];    // [head parity][column half] row partials of the dgamma term
 };
 constexpr size_t kDqSmemBytes = sizeof(DqSmem) + 1024;
 constexpr uint32_t kDtP = 0, kDt1 = 128, kDt2 = 256;
@@ -1415,10 +1409,12 @@ __global__ void __launch_bounds__(256, 1) dq_kernel(const __grid_constant__ BwdP
   auto issue_a = [&](int hh2) {  // thread 0
     const int h2 = hk * G + hh2, b2 = hh2 & 1;
     const size_t r2 = (size_t)chunk * Hv + h2;
-    mbar_arrive_expect_tx(&bar_a, (hh2 == 0 ? 2 * 8192 : 0) + 2 * 8192 + 2 * 16384 + 256);
+    mbar_arrive_expect_tx(&bar_a, (hh2 == 0 ? 4 * 8192 : 0) + 2 * 8192 + 2 * 16384 + 256);
     if (hh2 == 0) {
       tma_load_3d(sm.k[0], &p.tm_k, 0, hk, tok0, &bar_a);
       tma_load_3d(sm.k[1], &p.tm_k, 64, hk, tok0, &bar_a);
+      tma_load_3d(sm.q[0], &p.tm_q, 0, hk, tok0, &bar_a);
+      tma_load_3d(sm.q[1], &p.tm_q, 64, hk, tok0, &bar_a);
     }
     tma_load_3d(sm.dout[b2][0], &p.tm_do, 0, h2, tok0, &bar_a);
     tma_load_3d(sm.dout[b2][1], &p.tm_do, 64, h2, tok0, &bar_a);
@@ -1439,6 +1435,10 @@ __global__ void __launch_bounds__(256, 1) dq_kernel(const __grid_constant__ BwdP
   for (int hh = 0; hh < G && ok; ++hh) {
     const int h = hk * G + hh, bp = hh & 1;
     const size_t rec = (size_t)chunk * Hv + h;
+    // warps 2-3 add the dgamma term of this head to dg at its end: grad_kernel's value, read now
+    const int gi = tid - 64;
+    float dg_old = 0.f;
+    if (gi >= 0 && gi < 64 && gi < n) dg_old = p.dg[(size_t)(tok0 + gi) * Hv + h];
     if (tid == 224 && hh + 1 < G) {  // the next head's records into L2 (a thread off the load path)
       const size_t r1 = rec + 1;
       tma_prefetch_3d(&p.tm_do, 0, h + 1, tok0);
@@ -1522,6 +1522,7 @@ __global__ void __launch_bounds__(256, 1) dq_kernel(const __grid_constant__ BwdP
     if (tid == 0 && hh + 1 < G) issue_b(hh + 1);  // S is read
     {
       const float sc0 = sm.eg[rw[0]] * p.scale, sc1 = sm.eg[rw[1]] * p.scale;
+      float qd[2] = {0.f, 0.f};  // q_t . (S_c dO_t) over this thread's columns, rows rw[0], rw[1]
 #pragma unroll
       for (int ci = 0; ci < 2; ++ci) {
         float a[16], b[16];
@@ -1530,11 +1531,40 @@ __global__ void __launch_bounds__(256, 1) dq_kernel(const __grid_constant__ BwdP
         tmem_ld_wait();
 #pragma unroll
         for (int x = 0; x < 16; ++x) dq[16 * ci + x] += ((x & 2) ? sc1 : sc0) * a[x] + b[x];
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+#pragma unroll
+          for (int rr = 0; rr < 2; ++rr) {
+            const float2 qv = __bfloat1622float2(
+                *reinterpret_cast<const __nv_bfloat162*>(sm.q[cx.half] + sw128_pair(rw[rr], 32 * ci + 8 * k + c2)));
+            qd[rr] += qv.x * a[4 * k + 2 * rr] + qv.y * a[4 * k + 2 * rr + 1];
+          }
+      }
+      qd[0] = quad_sum(qd[0]);
+      qd[1] = quad_sum(qd[1]);
+      if ((cx.lane & 3) == 0) {
+        sm.qd[bp][cx.half][rw[0]] = qd[0] * sc0;
+        sm.qd[bp][cx.half][rw[1]] = qd[1] * sc1;
       }
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    if (gi >= 0 && gi < 64) {
+      // dg += suffix sums of the term over the chunk: warp 2 rows 0-31 (plus the total of rows
+      // 32-63), warp 3 rows 32-63; the other warps go on to the next head, which writes the other
+      // parity of qd
+      const int i = gi;
+      float x = (i < n) ? sm.qd[bp][0][i] + sm.qd[bp][1][i] : 0.f;
+      float tail = 0.f;
+      if (cx.warp == 2) tail = warp_sum((i + 32 < n) ? sm.qd[bp][0][i + 32] + sm.qd[bp][1][i + 32] : 0.f);
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float y = __shfl_down_sync(0xffffffffu, x, o);
+        if (cx.lane + o < 32) x += y;
+      }
+      if (i < n) p.dg[(size_t)(tok0 + i) * Hv + h] = dg_old + (x + tail);
+    }
   }
   if (ok) {
 #pragma unroll
