@@ -1,7 +1,8 @@
 // Backward of the chunked Gated DeltaNet (sm_103a).
 //
 // The backward recomputes the forward chunk states ("How to Speed Up GDN Kernels for Qwen
-// Models", section "Lever 2": the backward pass recomputes hidden states in one dedicated pass),
+// Models", section "Lever 2": the per-chunk states are rebuilt by a single pass of their own
+// rather than kept from the forward),
 // or finds them in the workspace when the forward of a training step kept them (the same
 // recompute, run by the forward, which then forms o from the records), then runs the
 // state-gradient chain in reverse and the per-chunk gradients in parallel:

@@ -7,9 +7,8 @@
 //                     substitution, T diag(beta e^gamma), T diag(beta) and P = scale (Q K^T o E) in
 //                     bf16, and a per-chunk flag for the warm-up bound below ("How to Speed Up GDN
 //                     Kernels for Qwen Models", sections "What GDN actually computes" (kkt_solve, one
-//                     64x64 system per chunk per head) and "Lever 2" (gate cumsum once per chunk,
-//                     triangular inverse solved once and reused by the output path and the state
-//                     update)).
+//                     64x64 system per chunk per head) and "Lever 2" (gate cumsum once per chunk;
+//                     one inverse per chunk serves both o and the state recurrence)).
 //   chain_kernel<OUT> persistent over (segment, value head) items in dependency order: the state S
 //                     (fp32, 128x128) lives in registers across 8 warps; per chunk, tcgen05 MMAs compute
 //                     W = T_w K, then [Q~; -W] S + [0; U] (U = T_u V), V' = U - W S,
