@@ -106,9 +106,9 @@ enum gdn_fwd_stage {
   GDN_STAGE_SPLIT = 2,     /* exact split, pass 1: segment transitions and local end states */
   GDN_STAGE_CHAIN = 3,     /* state chain fused with the output (records states in the backward) */
   GDN_STAGE_REV_CHAIN = 4, /* backward: reverse state-gradient chain */
-  GDN_STAGE_GRADS = 5,     /* backward: per-chunk dk, dv, dg, dbeta */
+  GDN_STAGE_GRADS = 5,     /* backward: per-chunk dk, dv, dbeta, dg (all but its q S dO term) */
   GDN_STAGE_DINIT = 6,     /* backward: d(initial_state) sums over documents sharing a pool entry */
-  GDN_STAGE_DQ = 7,        /* backward: per-chunk dq */
+  GDN_STAGE_DQ = 7,        /* backward: per-chunk dq; adds the q S dO term of dg */
   GDN_STAGE_OUT = 8,       /* forward with GDN_FLAG_SAVE_FOR_BWD: o from the records */
   GDN_NUM_STAGES = 9
 };
