@@ -51,3 +51,28 @@ def test_all_documents_empty_backward(path):
     df = p.dfinal.astype(np.float64)
     np.testing.assert_allclose(got["dinit"][1], df[0] + df[3], rtol=1e-6, atol=1e-6)
     np.testing.assert_array_equal(got["dinit"][0], df[2])
+
+
+def _many_documents_problem(with_dout=False):
+    # 600 documents of 0-90 tokens (some empty, most shorter than a chunk): the planner's scans
+    # over documents and segments run in several tiles, and most chunks are partial
+    rng = np.random.default_rng(5252)
+    lens = [int(x) for x in rng.integers(0, 91, size=600)]
+    lens[::37] = [0] * len(lens[::37])
+    return synth.make_problem("many_docs", 5252, lens, 1, 2, with_dout=with_dout)
+
+
+def test_many_short_documents_forward():
+    p = _many_documents_problem()
+    out, fin = run_fwd(p)
+    ro, rf = oracle.fwd_problem(p)
+    assert_close("many_docs out", out, ro)
+    assert_close("many_docs final_state", fin, rf)
+
+
+def test_many_short_documents_backward():
+    p = _many_documents_problem(with_dout=True)
+    got = run_bwd(p)
+    ref = oracle.bwd_problem(p)
+    for key in ("dq", "dk", "dv", "dg", "dbeta"):
+        assert_close(f"many_docs {key}", got[key], ref[key])
