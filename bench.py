@@ -48,7 +48,7 @@ def algorithmic_fwd(T, Hk, Hv, N):
 def algorithmic_bwd(T, Hk, Hv, N):
     # read q, k, v, g, beta, dO; write dq, dk, dv (fp32), dg, dbeta
     bytes_ = T * (2 * Hk * D * 2 + 2 * Hv * D * 2 + 2 * Hv * 4) + T * (2 * Hk * D * 4 + Hv * D * 4 + 2 * Hv * 4)
-    flops = T * (Hk * 4 * 64 * D + Hv * (16 * D * D + 26 * 64 * D))
+    flops = T * (Hk * 4 * 64 * D + Hv * (14 * D * D + 26 * 64 * D))
     return bytes_, flops
 
 
@@ -63,11 +63,12 @@ def kernel_counts(T, Hk, Hv, N):
     chain = (fb - T * 2 * Hv * 4, n_ch * Hv * 2 * (3 * C * D * D + C * C * D))
     # grad_kernel: q, k, v, dO, g, beta in; dk, dv, dg, dbeta out (fp32)
     grad_b = T * (2 * Hk * D * 2 + 2 * Hv * D * 2 + 2 * Hv * 4) + T * (Hk * D * 4 + Hv * D * 4 + 2 * Hv * 4)
-    # per value head: K dS, Q S, dV' S^T, V'_s dS^T (C D^2 each); dO V'^T, dV' V^T, dW K^T, P Q,
-    # T_u^T dV', T_w^T dW, dKK K (C^2 D each); dT T^T, T^T R (C^3 each); per key head K K^T, Q K^T
-    grad_f = n_ch * (Hk * 2 * 2 * C * C * D + Hv * 2 * (4 * C * D * D + 7 * C * C * D + 2 * C * C * C))
-    # dq_kernel: k, dO, g in; dq out (fp32); dO S^T, dO V'^T, (dQK o E) K
-    dq_b = T * (Hk * D * 2 + Hv * D * 2 + Hv * 4) + T * Hk * D * 4
+    # per value head: K dS, dV' S^T, V'_s dS^T (C D^2 each); dO V'^T, dV' V^T, dW K^T, P Q,
+    # T_u^T dV', T_w^T dW, dKK K (C^2 D each); dT T^T, T^T R (C^3 each); per key head K K^T, Q K^T.
+    # The term of dgamma through q S dO needs no product of its own: dq_kernel forms it from dO S^T.
+    grad_f = n_ch * (Hk * 2 * 2 * C * C * D + Hv * 2 * (3 * C * D * D + 7 * C * C * D + 2 * C * C * C))
+    # dq_kernel: q, k, dO, g in; dq out (fp32); dO S^T, dO V'^T, (dQK o E) K
+    dq_b = T * (2 * Hk * D * 2 + Hv * D * 2 + Hv * 4) + T * Hk * D * 4
     dq_f = n_ch * Hv * 2 * (C * D * D + 2 * C * C * D)
     # reverse chain: k, q, dO in; K~ dS, P^T dO, Q~^T dO, W^T dV'
     rev_b = T * (2 * Hk * D * 2 + Hv * D * 2)
