@@ -172,6 +172,17 @@ def _oracle_step(p, f, cores):
     oracle.bwd(f["q"], f["k"], f["v"], f["g"], f["beta"], p.cu_seqlens, f["dout"], threads=cores)
 
 
+def workload_config(T, Hv, Hk, mode, has_bwd, train):
+    """The `config` object of the bench line; the reference arm reports the same one."""
+    return {"workload": "GDN " + ("fwd+bwd" if has_bwd else "fwd") + f", one {T}-token sequence, H_v={Hv}, "
+            f"H_k={Hk}, d_k=d_v=128, chunk 64, " + mode + " mode", "T": T, "H_v": Hv, "H_k": Hk,
+            "mode": mode, "pass": "fwd+bwd" if has_bwd else "fwd",
+            "step": ("training step: forward keeping its records (save_for_backward), backward reusing "
+                     "them (reuse_forward)" if train else
+                     ("forward, then a backward that recomputes the forward" if has_bwd else "forward")),
+            "l2": "flushed between timed steps (512 MiB write outside the timed events)"}
+
+
 def run_reference(args, rank):
     if rank != 0:
         return None
@@ -199,8 +210,8 @@ def run_reference(args, rank):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": "GDN fwd+bwd, single sequence, H_v=8, H_k=2, d=128 (fp64 oracle on host cores)",
-                   "T": T_sample, "H_v": 8, "H_k": 2},
+        "config": dict(workload_config(args.tokens, 8, 2, args.mode, True, args.mode == "exact"),
+                       l2="not applicable: the fp64 oracle on the host cores, one sample per step"),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -484,13 +495,7 @@ def run_ours(args, rank, world, local_rank):
         "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": value / PAGE_FWD_MTOK_S if not has_bwd else None,
         "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": "GDN " + ("fwd+bwd" if has_bwd else "fwd") + f", one {T}-token sequence, H_v=8, "
-                   "H_k=2, d_k=d_v=128, chunk 64, " + args.mode + " mode", "T": T, "H_v": Hv, "H_k": Hk,
-                   "mode": args.mode, "pass": "fwd+bwd" if has_bwd else "fwd",
-                   "step": ("training step: forward keeping its records (save_for_backward), backward reusing "
-                            "them (reuse_forward)" if train else
-                            ("forward, then a backward that recomputes the forward" if has_bwd else "forward")),
-                   "l2": "flushed between timed steps (512 MiB write outside the timed events)"},
+        "config": workload_config(T, Hv, Hk, args.mode, has_bwd, train),
         "roofline": {"bound": bound, "kernel": dom, "achieved": achieved, "peak": peak, "unit": unit_r,
                      "frac": achieved / peak, "traffic": (tr["bytes_per_launch"] if tr else None),
                      "peak_source": peaks["src"] + (" hbm_gbs" if bound == "hbm" else " bf16_tflops_sustained"),

@@ -4,6 +4,7 @@ CPU; the reference arm runs on rank 0 only."""
 import os
 import socket
 import sys
+import time
 
 import pytest
 
@@ -58,3 +59,17 @@ def test_reference_arm_runs_on_rank_zero_only():
     class A:
         steps, warmup = 1, 0
     assert bench.run_reference(A(), rank=1) is None
+
+
+def test_reference_arm_reports_our_arm_config(monkeypatch):
+    """The reference arm's line names the same workload as ours (same metric, unit and config);
+    only the timing note differs. The oracle step itself is replaced here: this checks the line."""
+    monkeypatch.setattr(bench, "_oracle_step", lambda p, f, cores: time.sleep(0.001))
+
+    class A:
+        steps, warmup, tokens, mode = 2, 1, 32768, "exact"
+    res = bench.run_reference(A(), rank=0)
+    ours = bench.workload_config(32768, 8, 2, "exact", True, True)
+    assert res["impl"] == "reference" and res["metric"] == bench.METRIC and res["unit"] == bench.UNIT
+    assert {k: v for k, v in res["config"].items() if k != "l2"} == {k: v for k, v in ours.items() if k != "l2"}
+    assert res["cpu_baseline"]["kind"] == "oracle" and res["e2e"]["h2d_bytes_per_step"] == 0
