@@ -204,3 +204,34 @@ def test_stage_events_allow_skipped_entries():
     assert all(arr[i] is None for i in range(n))
     with pytest.raises(ValueError):
         gdn.Options(stage_events=[None] * (n - 1)).c()
+
+
+def test_no_cpu_fallback(lib):
+    """Host memory is refused, never computed on: the binding rejects host tensors, the C ABI
+    returns an error for host buffers and leaves the outputs untouched, and a missing library
+    raises instead of falling back."""
+    torch = pytest.importorskip("torch")
+    import synth
+    from tests.gpu_util import to_device
+    p = synth.make_problem("host", 3, [70], 1, 2, with_dout=True)
+    d = to_device(p, "cpu")
+    with pytest.raises(ValueError):
+        gdn.chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"])
+    with pytest.raises(ValueError):
+        gdn.chunk_bwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"], d["dout"])
+    # the C ABI on host buffers (aligned, well-formed): an argument error before any launch
+    T, N = p.T, p.N
+    need = gdn.fwd_workspace_size(N, T, 1, 2)
+    raw = np.zeros(need + 256, dtype=np.uint8)
+    ws = raw[(-raw.ctypes.data) % 256:][:need]
+    out = np.full((T, 2, 128), 0x7FC0, dtype=np.uint16)
+    fin = np.full((N, 2, 128, 128), 7.0, dtype=np.float32)
+    o = gdn.COptions(0, -10.0, 0, 1.0, 0, None)
+    P = ctypes.c_void_p
+    rc = lib.gdn_chunk_fwd(P(p.q.ctypes.data), P(p.k.ctypes.data), P(p.v.ctypes.data), P(p.g.ctypes.data),
+                           P(p.beta.ctypes.data), P(p.cu_seqlens.ctypes.data), N, T, 1, 2, 128, None, None, 0,
+                           P(out.ctypes.data), P(fin.ctypes.data), P(ws.ctypes.data), need, ctypes.byref(o), None)
+    assert rc == gdn.GDN_ERR_INVALID_ARG
+    assert (out == 0x7FC0).all() and (fin == 7.0).all()
+    with pytest.raises(RuntimeError):
+        gdn.load("/nonexistent/libgdn_gb300.so")
