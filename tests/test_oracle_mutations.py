@@ -16,6 +16,8 @@ FWD_PINS = [pins.test_hand_worked_cases, pins.test_gqa_head_map_contiguous_group
             pins.test_reset_at_boundaries_equals_separate_runs, pins.test_empty_documents_pass_the_state_through,
             lambda: pins.test_brute_force_quadratic_form(17, 8, 5)]
 BWD_PINS = [pins.test_backward_matches_finite_differences]
+# the block recompute of the backward only runs past its first block on documents over 64 tokens
+CKPT_PINS = [pins.test_backward_finite_differences_across_checkpoints]
 
 # (name, original text, mutated text, which pins)
 MUTANTS = [
@@ -30,6 +32,12 @@ MUTANTS = [
     ("dk drops prediction term", "acc += Sp[(size_t)r * w + c] * dp[c];", "acc += 0.0;", BWD_PINS),
     ("dbeta uses v", "dbt += ddel[c] * vp[c];", "dbt += ddel[c] * vt[c];", BWD_PINS),
     ("decay not carried into dS", "for (size_t e = 0; e < SZ; ++e) dS[e] *= a;", "(void)a;", BWD_PINS),
+    ("block restarts from the previous checkpoint", "std::copy(ckpt[bi].begin(), ckpt[bi].end(), states.begin());",
+     "std::copy(ckpt[bi ? bi - 1 : 0].begin(), ckpt[bi ? bi - 1 : 0].end(), states.begin());", CKPT_PINS),
+    ("block edge off by one", "const int64_t tb = t0 + bi * CK, te = std::min(t1, tb + CK);",
+     "const int64_t tb = t0 + bi * CK - (bi > 0 ? 1 : 0), te = std::min(t1, tb + CK);", CKPT_PINS),
+    ("checkpoint repeats the previous one", "ckpt[bi] = S;\n        for (int64_t t = t0 + bi * CK;",
+     "ckpt[bi] = bi ? ckpt[bi - 1] : S;\n        for (int64_t t = t0 + bi * CK;", CKPT_PINS),
 ]
 
 
@@ -50,3 +58,6 @@ def test_pins_catch_mutant(name, orig, mut, which, tmp_path, monkeypatch):
         except AssertionError:
             failed.append(getattr(pin, "__name__", "pin"))
     assert failed, f"no pin caught the '{name}' mutant"
+    if which is CKPT_PINS:
+        # only the pin that crosses a checkpoint sees these: the short-document pin passes
+        pins.test_backward_matches_finite_differences()

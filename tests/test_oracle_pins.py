@@ -265,6 +265,48 @@ def test_backward_matches_finite_differences():
         assert err < 1e-6, f"{gname}: rel err {err:.3e}"
 
 
+def test_backward_finite_differences_across_checkpoints():
+    """The oracle's backward rebuilds each document in 64-token blocks from saved states; here
+    documents of 130 and 70 tokens cross that interval (the 130-token one twice, the second one
+    forked from the first), with a slow decay so that the state carries across the block edges.
+    Central differences on a seeded sample of entries of every input, always including the tokens
+    on both sides of each block edge, must match the hand-written reverse mode."""
+    Hk, Hv, Dk, Dv = 1, 2, 3, 2
+    lens = [130, 70]
+    p = rand_problem(61, lens, Hk, Hv, Dk, Dv, n_init=1, init_idx=[0, 1], g_lo=-0.08, g_hi=-0.002)
+    r = rng(62)
+    T = sum(lens)
+    dout = r.standard_normal((T, Hv, Dv))
+    dfinal = r.standard_normal((len(lens), Hv, Dk, Dv))
+    gr = oracle.bwd(p["q"], p["k"], p["v"], p["g"], p["beta"], p["cu_seqlens"], dout, dfinal,
+                    p["init_idx"], p["initial_state"])
+    edges = [0, 63, 64, 65, 127, 128, 129, 130, 130 + 63, 130 + 64, T - 1]  # block edges of both documents
+    eps = 1e-6
+    names = dict(q="dq", k="dk", v="dv", g="dg", beta="dbeta", initial_state="dinit")
+    for name, gname in names.items():
+        x = p[name]
+        if name == "initial_state":
+            picks = [tuple(i) for i in np.ndindex(x.shape)]
+        else:
+            rest = x.shape[1:]
+            picks = [(t,) + tuple(i) for t in edges for i in np.ndindex(rest)]
+            flat = r.choice(x.size, size=min(40, x.size), replace=False)
+            picks += [tuple(int(c) for c in np.unravel_index(f, x.shape)) for f in flat]
+        ana = gr[gname]
+        num = np.array([0.0] * len(picks))
+        for n_, idx in enumerate(picks):
+            old = x[idx]
+            x[idx] = old + eps
+            lp = _loss(p, dout, dfinal)
+            x[idx] = old - eps
+            lm = _loss(p, dout, dfinal)
+            x[idx] = old
+            num[n_] = (lp - lm) / (2 * eps)
+        got = np.array([ana[idx] for idx in picks])
+        err = np.abs(got - num).max() / max(1.0, np.abs(num).max())
+        assert err < 1e-6, f"{gname}: rel err {err:.3e}"
+
+
 def test_backward_gradient_sums_at_shared_state():
     """d(shared initial state) = sum over the documents that start from it."""
     Hk, Hv, Dk, Dv = 1, 2, 6, 4
