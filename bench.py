@@ -211,7 +211,11 @@ def run_reference(args, rank):
         "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": dict(workload_config(args.tokens, 8, 2, args.mode, True, args.mode == "exact"),
-                       l2="not applicable: the fp64 oracle on the host cores, one sample per step"),
+                       l2="not applicable: the fp64 oracle on the host cores, one sample per step",
+                       sample_tokens_per_step=T_sample,
+                       sample=f"each step runs the oracle on the first {T_sample} tokens' worth of the workload "
+                              f"(same shapes and distributions); Mtokens/s of the token-by-token recurrence is "
+                              f"independent of the sequence length"),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -267,7 +271,7 @@ def run_ours(args, rank, world, local_rank):
     import linear_attention_varlen_gb300 as gdn
     import synth
     from linear_attention_varlen_gb300 import build as gdn_build
-    from tests.gpu_util import to_device
+    from synth import to_device
 
     gdn_build.build()
     gdn.load()
@@ -467,6 +471,37 @@ def run_ours(args, rank, world, local_rank):
     e2e_ms = ea.elapsed_time(ev_out[-1]) / e2e_steps
     e2e_value = T * world / (e2e_ms * 1e-3) / 1e6
 
+    # The inference forward alone (exact mode, the spec prefill) and the truncation mode, each
+    # timed with one event pair around the whole call (L2 flushed before each), outside the step
+    # loop; truncation's deviation from the exact forward on the same inputs.
+    def time_forward(mode, reps):
+        of = gdn.Options(mode=mode)
+        for _ in range(3):
+            fwd(of)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        torch.cuda.synchronize()
+        for a_, b_ in evs:
+            flush.zero_()
+            a_.record(stream)
+            fwd(of)
+            b_.record(stream)
+        torch.cuda.synchronize()
+        return float(np.median([a_.elapsed_time(b_) for a_, b_ in evs]))
+
+    fwd_reps = max(10, min(args.steps, 50))
+    fwd_exact_ms = time_forward("exact", fwd_reps)
+    o_exact, f_exact = out.double().clone(), fin.double().clone()
+    fwd_trunc_ms = time_forward("truncate", fwd_reps)
+    o_trunc, f_trunc = out.double().clone(), fin.double().clone()
+
+    def deviation(a_, b_):
+        n_ = float(torch.linalg.vector_norm(b_))
+        return {"rel_l2": float(torch.linalg.vector_norm(a_ - b_)) / n_ if n_ > 0 else 0.0,
+                "max_abs": float((a_ - b_).abs().max())}
+    trunc_dev = {"out": deviation(o_trunc, o_exact), "final_state": deviation(f_trunc, f_exact)}
+    if world > 1:
+        torch.distributed.barrier()
+
     if rank != 0:
         return None
     peaks = load_peaks()
@@ -521,6 +556,29 @@ def run_ours(args, rank, world, local_rank):
             "bwd_recompute_ms": float(sum(ctx[1][s_] for s_ in recomp_b)),
             "fwd_inference_stages_ms": {infer_f[s_]: float(ctx[0][s_]) for s_ in infer_f},
             "bwd_recompute_stages_ms": {recomp_b[s_]: float(ctx[1][s_]) for s_ in recomp_b}}
+    fb_inf, ff_inf = algorithmic_fwd(T, Hk, Hv, N)
+
+    def fwd_object(ms_):
+        t_ = ms_ * 1e-3
+        hbm_t, tc_t = fb_inf / (peaks["hbm"] * 1e9), ff_inf / (peaks["tc"] * 1e12)
+        bound_ = "hbm" if hbm_t >= tc_t else "tensor"
+        ach = fb_inf / t_ / 1e9 if bound_ == "hbm" else ff_inf / t_ / 1e12
+        pk = peaks["hbm"] if bound_ == "hbm" else peaks["tc"]
+        return {"ms": ms_, "value": T / t_ / 1e6, "unit": UNIT,
+                "roofline": {"bound": bound_, "achieved": ach, "peak": pk, "unit": "GB/s" if bound_ == "hbm" else
+                             "TFLOP/s", "frac": ach / pk, "algorithmic_bytes": fb_inf, "algorithmic_flops": ff_inf,
+                             "peak_source": peaks["src"] + (" hbm_gbs" if bound_ == "hbm" else " bf16_tflops")}}
+    res["fwd"] = dict(fwd_object(fwd_exact_ms), mode="exact",
+                      note=f"inference forward alone (o and final state), {T} tokens x {Hv} value heads, median of "
+                           f"{fwd_reps} calls with one event pair around each and L2 flushed before it; roofline "
+                           f"over the whole call (q, k, v, g, beta read once, o and the final state written once)")
+    res["truncate"] = dict(fwd_object(fwd_trunc_ms), mode="truncate",
+                           threshold=float(opts.trunc_log_threshold),
+                           deviation_from_exact=trunc_dev,
+                           note="the opt-in truncation mode (segment carries rebuilt from a window whose summed "
+                                "log-decay is below the threshold), timed like `fwd`; deviation_from_exact compares "
+                                "its o and final state with the exact forward's on the same inputs (the tests bound "
+                                "both modes against the fp64 oracle)")
     if not has_bwd:
         res["vs_baseline_note"] = "value / FlashQLA forward on H200 (0.31 ms for 32K at TP8), context only"
     if world == 1 and not args.no_cpu_baseline:

@@ -42,7 +42,11 @@
  *  - GPUs: built for sm_103a (GB300) only; any other GPU returns
  *    GDN_ERR_UNSUPPORTED ("Using it, and the fine print": the kernels refuse
  *    hardware they were not built for). The device is the one that holds the
- *    workspace.
+ *    workspace. Every non-null pointer must be device memory of that GPU (or
+ *    managed memory); a host, pinned-host or unregistered pointer, or one on
+ *    another GPU, returns GDN_ERR_INVALID_ARG before anything is launched.
+ *    An entry point may switch to the workspace's GPU while it enqueues work,
+ *    and always gives the calling thread its own current device back.
  */
 #ifndef GDN_H_
 #define GDN_H_
@@ -73,6 +77,11 @@ enum gdn_flags {
                                 records. The workspace must then be of gdn_bwd_workspace_size() bytes
                                 (gdn_fwd_workspace_size() returns that size when this flag is set).
                                 Exact mode only. */
+  GDN_FLAG_TEST_WITHHOLD_FORK = 4, /* forward, for testing the bounded waits only: no document of the call
+                                      publishes its final state to the documents that fork from it, so
+                                      their waits run out (after gdn_options.flag_wait_us) and the call
+                                      reports GDN_ERR_TIMEOUT through the status word; outputs are then
+                                      unspecified. Rejected by the backward (GDN_ERR_INVALID_ARG). */
   GDN_FLAG_REUSE_FWD = 2     /* backward: the workspace holds the records of a forward run with
                                 GDN_FLAG_SAVE_FOR_BWD on the same inputs, options and stream order, and
                                 nothing has written it since; the backward then skips its recompute
@@ -95,6 +104,10 @@ typedef struct gdn_options {
                                 events 2s and 2s+1 are recorded on `stream` right before and right after
                                 stage s (both at the same point when the stage has nothing to launch);
                                 NULL entries are skipped */
+  int32_t flag_wait_us;      /* limit of each wait of one work item for a state another item publishes
+                                (a fork source's final state, a previous segment's end state), in
+                                microseconds at the maximum SM clock; 0 = about two seconds. A wait that
+                                runs out stops the call with GDN_ERR_TIMEOUT in the status word. */
 } gdn_options;
 
 /* Stages of a call (indices into gdn_options.stage_events). A backward call runs stages 0-3
@@ -114,7 +127,7 @@ enum gdn_fwd_stage {
 };
 
 /* Fill `opt` with the defaults: exact mode, threshold -10, automatic segments, scale 1, no flags,
- * no events. */
+ * no events, the default wait limit. */
 void gdn_default_options(gdn_options* opt);
 
 /* Workspace bytes gdn_chunk_fwd needs for these sizes (opt may be NULL for defaults; with
@@ -166,12 +179,13 @@ int gdn_chunk_bwd(const void* q, const void* k, const void* v, const float* g, c
  * program with no device allocator of its own, or a plugin inside a framework whose memory pool
  * owns all device memory). The pages have no counterpart to this entry point. It runs the same
  * kernels as gdn_chunk_fwd with the scratch in a fixed array of gdn_noalloc_scratch_bytes() bytes
- * (128 MiB) compiled into the library: every GPU that loads the library holds that array until the
- * process exits, and every call shares it. Problems whose gdn_fwd_workspace_size() exceeds it return
- * GDN_ERR_WORKSPACE. Calls that overlap on the GPU race on the array: order them on one stream.
- * The array needs no clearing (the forward rewrites everything it reads). The first call on each
- * device looks up the array's device address; make it before any stream capture. Device-side
- * status: gdn_workspace_status() cannot name this array, so check results through the outputs. */
+ * (160 MiB: room for one 32768-token document at 8 value heads) compiled into the library: every
+ * GPU that loads the library holds that array until the process exits, and every call shares it.
+ * Problems whose gdn_fwd_workspace_size() exceeds it return GDN_ERR_WORKSPACE before any launch.
+ * The tensors' GPU is used (same pointer rules as gdn_chunk_fwd). Calls that overlap on the GPU
+ * race on the array: order them on one stream. The array needs no clearing (the forward rewrites
+ * everything it reads). The first call on each device looks up the array's device address; make
+ * it before any stream capture. Device-side errors: read them with gdn_noalloc_status(). */
 int gdn_chunk_fwd_noalloc(const void* q, const void* k, const void* v, const float* g, const float* beta,
                           const int32_t* cu_seqlens, int N, int T, int H_k, int H_v, int head_dim,
                           const int32_t* init_idx, const float* initial_state, int n_init, void* out,
@@ -180,9 +194,30 @@ int gdn_chunk_fwd_noalloc(const void* q, const void* k, const void* v, const flo
 /* Size in bytes of the array gdn_chunk_fwd_noalloc uses. */
 size_t gdn_noalloc_scratch_bytes(void);
 
+/* Device status word of the last gdn_chunk_fwd_noalloc call on CUDA device `device` (synchronises
+ * `stream`, which must belong to that device): GDN_OK or its first device-side error, as
+ * gdn_workspace_status() reports for a caller's workspace. GDN_ERR_INVALID_ARG if no such call has
+ * run on that device. */
+int gdn_noalloc_status(int device, gdn_stream_t stream);
+
 /* Copy the workspace's device status word to the host (synchronises `stream`) and return it:
  * GDN_OK or the first device-side error of the last call that used this workspace. */
 int gdn_workspace_status(const void* workspace, gdn_stream_t stream);
+
+/* Every host-side check gdn_chunk_fwd / gdn_chunk_bwd makes before its first launch (sizes,
+ * options, null pointers, alignment, the memory kind and GPU of each pointer, the GPU's
+ * architecture, the workspace size), with the same arguments minus the stream; returns the status
+ * the entry point would return at that point, GDN_OK when it would go on to launch. Launches
+ * nothing, reads and writes no buffer, leaves the caller's current device as it was. */
+int gdn_fwd_check_args(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                       const int32_t* cu_seqlens, int N, int T, int H_k, int H_v, int head_dim,
+                       const int32_t* init_idx, const float* initial_state, int n_init, void* out,
+                       float* final_state, void* workspace, size_t ws_bytes, const gdn_options* opt);
+int gdn_bwd_check_args(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                       const int32_t* cu_seqlens, int N, int T, int H_k, int H_v, int head_dim,
+                       const int32_t* init_idx, const float* initial_state, int n_init, const void* dout,
+                       const float* dfinal_state, float* dq, float* dk, float* dv, float* dg, float* dbeta,
+                       float* dinitial_state, void* workspace, size_t ws_bytes, const gdn_options* opt);
 
 /* Human-readable name of a status code (static string). */
 const char* gdn_status_string(int status);

@@ -28,7 +28,7 @@ CHUNK = 64
 # Every symbol include/gdn.h declares.
 EXPORTS = ("gdn_default_options", "gdn_fwd_workspace_size", "gdn_bwd_workspace_size", "gdn_chunk_fwd",
            "gdn_chunk_bwd", "gdn_workspace_status", "gdn_status_string", "gdn_plan_host", "gdn_chunk_fwd_noalloc",
-           "gdn_noalloc_scratch_bytes")
+           "gdn_noalloc_scratch_bytes", "gdn_noalloc_status", "gdn_fwd_check_args", "gdn_bwd_check_args")
 
 
 class GdnError(RuntimeError):
@@ -40,7 +40,7 @@ class GdnError(RuntimeError):
 class COptions(ctypes.Structure):
     _fields_ = [("mode", ctypes.c_int32), ("trunc_log_threshold", ctypes.c_float),
                 ("segment_chunks", ctypes.c_int32), ("scale", ctypes.c_float), ("flags", ctypes.c_int32),
-                ("stage_events", ctypes.c_void_p)]
+                ("stage_events", ctypes.c_void_p), ("flag_wait_us", ctypes.c_int32)]
 
 
 NUM_STAGES = 9
@@ -48,6 +48,7 @@ NUM_STAGES = 9
  STAGE_OUT) = range(9)
 FLAG_SAVE_FOR_BWD = 1  # forward of a training step: keep the records for the backward
 FLAG_REUSE_FWD = 2     # backward: use the records of a FLAG_SAVE_FOR_BWD forward instead of recomputing
+FLAG_TEST_WITHHOLD_FORK = 4  # forward, tests of the bounded waits only: forked documents never get their start
 
 
 @dataclass
@@ -61,6 +62,8 @@ class Options:
     stage_events: Optional[object] = None  # optional list of 2 * NUM_STAGES timing torch.cuda.Event (or None)
     save_for_backward: bool = False
     reuse_forward: bool = False
+    flag_wait_us: int = 0            # limit of a wait for another item's published state (0 = about 2 s)
+    test_withhold_fork: bool = False  # tests only: make the waits of forked documents run out
 
     def c(self) -> COptions:
         m = {"exact": MODE_EXACT, "truncate": MODE_TRUNCATE}[self.mode]
@@ -73,8 +76,10 @@ class Options:
                 raise ValueError("stage_events: 2 * NUM_STAGES entries, each None or a recorded timing event")
             self._ev_array = (ctypes.c_void_p * len(handles))(*handles)
             ev = ctypes.cast(self._ev_array, ctypes.c_void_p)
-        flags = (FLAG_SAVE_FOR_BWD if self.save_for_backward else 0) | (FLAG_REUSE_FWD if self.reuse_forward else 0)
-        return COptions(m, float(self.trunc_log_threshold), int(self.segment_chunks), float(self.scale), flags, ev)
+        flags = ((FLAG_SAVE_FOR_BWD if self.save_for_backward else 0) | (FLAG_REUSE_FWD if self.reuse_forward else 0)
+                 | (FLAG_TEST_WITHHOLD_FORK if self.test_withhold_fork else 0))
+        return COptions(m, float(self.trunc_log_threshold), int(self.segment_chunks), float(self.scale), flags, ev,
+                        int(self.flag_wait_us))
 
 
 _lock = threading.Lock()
@@ -117,6 +122,12 @@ def load(path: Optional[str] = None):
         lib.gdn_chunk_fwd_noalloc.restype = I
         lib.gdn_noalloc_scratch_bytes.argtypes = []
         lib.gdn_noalloc_scratch_bytes.restype = Z
+        lib.gdn_noalloc_status.argtypes = [I, P]
+        lib.gdn_noalloc_status.restype = I
+        lib.gdn_fwd_check_args.argtypes = [P, P, P, P, P, P, I, I, I, I, I, P, P, I, P, P, P, Z, OP]
+        lib.gdn_fwd_check_args.restype = I
+        lib.gdn_bwd_check_args.argtypes = [P, P, P, P, P, P, I, I, I, I, I, P, P, I, P, P, P, P, P, P, P, P, P, Z, OP]
+        lib.gdn_bwd_check_args.restype = I
         if path is None:
             _lib = lib
         return lib

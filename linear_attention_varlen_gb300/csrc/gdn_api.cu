@@ -10,25 +10,59 @@
 #include "../../include/gdn.h"
 #include "gdn_bwd.h"
 #include "gdn_common.cuh"
+#include "gdn_dev.cuh"
 #include "gdn_fwd.h"
+#include "gdn_host.h"
 #include "tmap.h"
 
 using namespace gdn;
 
+namespace gdn {
+
+int device_of(const void* anchor, const void* const* ptrs, int n, int* device) {
+  // 1 = device memory, 2 = managed memory, 0 = refused (host, pinned host, unregistered, error)
+  auto kind = [](const void* p, int* dev) -> int {
+    cudaPointerAttributes attr;
+    if (cudaPointerGetAttributes(&attr, p) != cudaSuccess) {
+      cudaGetLastError();
+      return 0;
+    }
+    *dev = attr.device;
+    if (attr.type == cudaMemoryTypeDevice) return 1;
+    if (attr.type == cudaMemoryTypeManaged) return 2;
+    return 0;
+  };
+  int chosen = -1, managed = -1;
+  if (anchor) {
+    int dv = -1;
+    if (kind(anchor, &dv) == 0) return kErrInvalid;
+    chosen = dv;
+  }
+  for (int i = 0; i < n; ++i) {
+    if (!ptrs[i]) continue;
+    int dv = -1;
+    const int k = kind(ptrs[i], &dv);
+    if (k == 0) return kErrInvalid;
+    if (k == 2) {
+      if (managed < 0) managed = dv;
+      continue;
+    }
+    if (chosen < 0)
+      chosen = dv;
+    else if (dv != chosen)
+      return kErrInvalid;
+  }
+  if (chosen < 0) chosen = managed;
+  if (chosen < 0) return kErrInvalid;
+  *device = chosen;
+  return kOk;
+}
+
+}  // namespace gdn
+
 namespace {
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
-
-// Make the device that owns `ptr` current (the caller's tensors decide the GPU).
-int select_device_of(const void* ptr) {
-  cudaPointerAttributes attr;
-  if (cudaPointerGetAttributes(&attr, ptr) != cudaSuccess) {
-    cudaGetLastError();
-    return kErrInvalid;
-  }
-  if (attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged) return kErrInvalid;
-  return cudaSetDevice(attr.device) == cudaSuccess ? kOk : kErrCuda;
-}
 
 int current_sm_count() {
   int dev = 0, n = 0;
@@ -55,7 +89,14 @@ gdn_options resolve(const gdn_options* opt) {
 
 bool valid_options(const gdn_options& o) {
   return (o.mode == GDN_MODE_EXACT || o.mode == GDN_MODE_TRUNCATE) &&
-         (o.flags & ~(GDN_FLAG_SAVE_FOR_BWD | GDN_FLAG_REUSE_FWD)) == 0 && o.scale == o.scale;
+         (o.flags & ~(GDN_FLAG_SAVE_FOR_BWD | GDN_FLAG_REUSE_FWD | GDN_FLAG_TEST_WITHHOLD_FORK)) == 0 &&
+         o.scale == o.scale && o.flag_wait_us >= 0;
+}
+
+// Wait limit of the cross-item waits in SM clock cycles (about 2 cycles per nanosecond at the
+// maximum clock; slower clocks make the wait longer, never shorter than asked).
+long long flag_budget(const gdn_options& o) {
+  return o.flag_wait_us > 0 ? (long long)o.flag_wait_us * 2070LL : kWaitBudget;
 }
 
 PlanDims make_dims(int N, int T, int H_k, int H_v, int n_init, const gdn_options& o, int sms) {
@@ -89,6 +130,7 @@ void gdn_default_options(gdn_options* opt) {
   opt->scale = 1.0f;
   opt->flags = 0;
   opt->stage_events = nullptr;
+  opt->flag_wait_us = 0;
 }
 
 const char* gdn_status_string(int status) {
@@ -128,6 +170,10 @@ size_t gdn_bwd_workspace_size(int N, int T, int H_k, int H_v, const gdn_options*
 
 int gdn_workspace_status(const void* workspace, gdn_stream_t stream) {
   if (!workspace) return GDN_ERR_INVALID_ARG;
+  int dev = 0;
+  if (device_of(workspace, nullptr, 0, &dev) != kOk) return GDN_ERR_INVALID_ARG;
+  DeviceGuard guard;
+  if (!guard.set(dev)) return GDN_ERR_CUDA;
   int32_t st = 0;
   if (cudaMemcpyAsync(&st, workspace, sizeof(st), cudaMemcpyDeviceToHost, (cudaStream_t)stream) != cudaSuccess)
     return GDN_ERR_CUDA;
@@ -135,26 +181,109 @@ int gdn_workspace_status(const void* workspace, gdn_stream_t stream) {
   return st;
 }
 
-int gdn_chunk_fwd(const void* q, const void* k, const void* v, const float* g, const float* beta,
-                  const int32_t* cu_seqlens, int N, int T, int H_k, int H_v, int head_dim,
-                  const int32_t* init_idx, const float* initial_state, int n_init, void* out, float* final_state,
-                  void* workspace, size_t ws_bytes, const gdn_options* opt, gdn_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// Every host-side check of a forward call, in order, up to the launch: sizes, options, null and
+// alignment rules, the memory kind and GPU of every pointer, the GPU's architecture and the
+// workspace size. On GDN_OK the workspace's GPU is current (through `guard`) and *o holds the
+// resolved options.
+int prepare_fwd(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                const int32_t* cu_seqlens, int N, int T, int H_k, int H_v, int head_dim, const int32_t* init_idx,
+                const float* initial_state, int n_init, void* out, float* final_state, void* workspace,
+                size_t ws_bytes, const gdn_options* opt, gdn_options* o, DeviceGuard& guard) {
   if (head_dim != kDim) return GDN_ERR_UNSUPPORTED;
   if (!sizes_ok(N, T, H_k, H_v) || n_init < 0) return GDN_ERR_INVALID_ARG;
-  const gdn_options o = resolve(opt);
-  if (!valid_options(o)) return GDN_ERR_INVALID_ARG;
+  *o = resolve(opt);
+  if (!valid_options(*o)) return GDN_ERR_INVALID_ARG;
   if (!cu_seqlens || !final_state || !workspace) return GDN_ERR_INVALID_ARG;
   if (T > 0 && (!q || !k || !v || !g || !beta || !out)) return GDN_ERR_INVALID_ARG;
   if (n_init > 0 && !initial_state) return GDN_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) || !aligned(final_state, 16) ||
       !aligned(initial_state, 16) || !aligned(workspace, 256))
     return GDN_ERR_INVALID_ARG;
-  if (o.flags & GDN_FLAG_REUSE_FWD) return GDN_ERR_INVALID_ARG;  // a backward option
-  if ((o.flags & GDN_FLAG_SAVE_FOR_BWD) && o.mode != GDN_MODE_EXACT) return GDN_ERR_INVALID_ARG;
-  const int dev = select_device_of(workspace);
-  if (dev != kOk) return dev;
+  if (o->flags & GDN_FLAG_REUSE_FWD) return GDN_ERR_INVALID_ARG;  // a backward option
+  if ((o->flags & GDN_FLAG_SAVE_FOR_BWD) && o->mode != GDN_MODE_EXACT) return GDN_ERR_INVALID_ARG;
+  const void* ptrs[] = {q, k, v, g, beta, cu_seqlens, init_idx, initial_state, out, final_state};
+  int dev = 0;
+  if (device_of(workspace, ptrs, (int)(sizeof(ptrs) / sizeof(ptrs[0])), &dev) != kOk) return GDN_ERR_INVALID_ARG;
+  if (!guard.set(dev)) return GDN_ERR_CUDA;
   const int arch = check_arch();
   if (arch != kOk) return arch;
+  const PlanDims d = make_dims(N, T, H_k, H_v, n_init, *o, current_sm_count());
+  const size_t need = (o->flags & GDN_FLAG_SAVE_FOR_BWD) ? bwd_layout(d).total : fwd_layout(d).total;
+  if (ws_bytes < need) return GDN_ERR_WORKSPACE;
+  return GDN_OK;
+}
+
+// Same for a backward call.
+int prepare_bwd(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                const int32_t* cu_seqlens, int N, int T, int H_k, int H_v, int head_dim, const int32_t* init_idx,
+                const float* initial_state, int n_init, const void* dout, const float* dfinal_state, float* dq,
+                float* dk, float* dv, float* dg, float* dbeta, float* dinitial_state, void* workspace,
+                size_t ws_bytes, const gdn_options* opt, gdn_options* o, DeviceGuard& guard) {
+  if (head_dim != kDim) return GDN_ERR_UNSUPPORTED;
+  if (!sizes_ok(N, T, H_k, H_v) || n_init < 0) return GDN_ERR_INVALID_ARG;
+  *o = resolve(opt);
+  if (!valid_options(*o)) return GDN_ERR_INVALID_ARG;
+  if (!cu_seqlens || !workspace) return GDN_ERR_INVALID_ARG;
+  if (T > 0 && (!q || !k || !v || !g || !beta || !dout || !dq || !dk || !dv || !dg || !dbeta))
+    return GDN_ERR_INVALID_ARG;
+  if (n_init > 0 && (!initial_state || !dinitial_state)) return GDN_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(dout, 16) || !aligned(dq, 16) ||
+      !aligned(dk, 16) || !aligned(dv, 16) || !aligned(initial_state, 16) || !aligned(dfinal_state, 16) ||
+      !aligned(dinitial_state, 16) || !aligned(workspace, 256))
+    return GDN_ERR_INVALID_ARG;
+  if (o->flags & (GDN_FLAG_SAVE_FOR_BWD | GDN_FLAG_TEST_WITHHOLD_FORK)) return GDN_ERR_INVALID_ARG;  // forward options
+  const void* ptrs[] = {q,    k,  v,  g,  beta, cu_seqlens, init_idx, initial_state, dout, dfinal_state,
+                        dq,   dk, dv, dg, dbeta, dinitial_state};
+  int dev = 0;
+  if (device_of(workspace, ptrs, (int)(sizeof(ptrs) / sizeof(ptrs[0])), &dev) != kOk) return GDN_ERR_INVALID_ARG;
+  if (!guard.set(dev)) return GDN_ERR_CUDA;
+  const int arch = check_arch();
+  if (arch != kOk) return arch;
+  gdn_options oe = *o;
+  oe.mode = GDN_MODE_EXACT;
+  if (ws_bytes < bwd_layout(make_dims(N, T, H_k, H_v, n_init, oe, current_sm_count())).total)
+    return GDN_ERR_WORKSPACE;
+  return GDN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int gdn_fwd_check_args(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                       const int32_t* cu_seqlens, int N, int T, int H_k, int H_v, int head_dim,
+                       const int32_t* init_idx, const float* initial_state, int n_init, void* out,
+                       float* final_state, void* workspace, size_t ws_bytes, const gdn_options* opt) {
+  gdn_options o;
+  DeviceGuard guard;
+  return prepare_fwd(q, k, v, g, beta, cu_seqlens, N, T, H_k, H_v, head_dim, init_idx, initial_state, n_init, out,
+                     final_state, workspace, ws_bytes, opt, &o, guard);
+}
+
+int gdn_bwd_check_args(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                       const int32_t* cu_seqlens, int N, int T, int H_k, int H_v, int head_dim,
+                       const int32_t* init_idx, const float* initial_state, int n_init, const void* dout,
+                       const float* dfinal_state, float* dq, float* dk, float* dv, float* dg, float* dbeta,
+                       float* dinitial_state, void* workspace, size_t ws_bytes, const gdn_options* opt) {
+  gdn_options o;
+  DeviceGuard guard;
+  return prepare_bwd(q, k, v, g, beta, cu_seqlens, N, T, H_k, H_v, head_dim, init_idx, initial_state, n_init, dout,
+                     dfinal_state, dq, dk, dv, dg, dbeta, dinitial_state, workspace, ws_bytes, opt, &o, guard);
+}
+
+int gdn_chunk_fwd(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                  const int32_t* cu_seqlens, int N, int T, int H_k, int H_v, int head_dim,
+                  const int32_t* init_idx, const float* initial_state, int n_init, void* out, float* final_state,
+                  void* workspace, size_t ws_bytes, const gdn_options* opt, gdn_stream_t stream) {
+  gdn_options o;
+  DeviceGuard guard;
+  const int rc = prepare_fwd(q, k, v, g, beta, cu_seqlens, N, T, H_k, H_v, head_dim, init_idx, initial_state, n_init,
+                             out, final_state, workspace, ws_bytes, opt, &o, guard);
+  if (rc != GDN_OK) return rc;
   const int sms = current_sm_count();
   if (o.flags & GDN_FLAG_SAVE_FOR_BWD) {
     BwdArgs a;
@@ -172,6 +301,8 @@ int gdn_chunk_fwd(const void* q, const void* k, const void* v, const float* g, c
     a.d = make_dims(N, T, H_k, H_v, n_init, o, sms);
     a.trunc_thr = o.trunc_log_threshold;
     a.scale = o.scale;
+    a.flag_budget = flag_budget(o);
+    a.withhold_fin = (o.flags & GDN_FLAG_TEST_WITHHOLD_FORK) ? 1 : 0;
     return launch_fwd_save(a, out, final_state, (cudaStream_t)stream, reinterpret_cast<cudaEvent_t*>(o.stage_events));
   }
   FwdParams p;
@@ -197,6 +328,8 @@ int gdn_chunk_fwd(const void* q, const void* k, const void* v, const float* g, c
   p.ws = reinterpret_cast<uint8_t*>(workspace);
   p.trunc_thr = o.trunc_log_threshold;
   p.scale = o.scale;
+  p.flag_budget = flag_budget(o);
+  p.withhold_fin = (o.flags & GDN_FLAG_TEST_WITHHOLD_FORK) ? 1 : 0;
   p.p_img = p.ws + p.L.pimg;
   return launch_fwd(p, (cudaStream_t)stream, reinterpret_cast<cudaEvent_t*>(o.stage_events));
 }
@@ -207,23 +340,12 @@ int gdn_chunk_bwd(const void* q, const void* k, const void* v, const float* g, c
                   const float* dfinal_state, float* dq, float* dk, float* dv, float* dg, float* dbeta,
                   float* dinitial_state, void* workspace, size_t ws_bytes, const gdn_options* opt,
                   gdn_stream_t stream) {
-  if (head_dim != kDim) return GDN_ERR_UNSUPPORTED;
-  if (!sizes_ok(N, T, H_k, H_v) || n_init < 0) return GDN_ERR_INVALID_ARG;
-  const gdn_options o = resolve(opt);
-  if (!valid_options(o)) return GDN_ERR_INVALID_ARG;
-  if (!cu_seqlens || !workspace) return GDN_ERR_INVALID_ARG;
-  if (T > 0 && (!q || !k || !v || !g || !beta || !dout || !dq || !dk || !dv || !dg || !dbeta))
-    return GDN_ERR_INVALID_ARG;
-  if (n_init > 0 && (!initial_state || !dinitial_state)) return GDN_ERR_INVALID_ARG;
-  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(dout, 16) || !aligned(dq, 16) ||
-      !aligned(dk, 16) || !aligned(dv, 16) || !aligned(initial_state, 16) || !aligned(dfinal_state, 16) ||
-      !aligned(dinitial_state, 16) || !aligned(workspace, 256))
-    return GDN_ERR_INVALID_ARG;
-  if (o.flags & GDN_FLAG_SAVE_FOR_BWD) return GDN_ERR_INVALID_ARG;  // a forward option
-  const int dev = select_device_of(workspace);
-  if (dev != kOk) return dev;
-  const int arch = check_arch();
-  if (arch != kOk) return arch;
+  gdn_options o;
+  DeviceGuard guard;
+  const int rc = prepare_bwd(q, k, v, g, beta, cu_seqlens, N, T, H_k, H_v, head_dim, init_idx, initial_state, n_init,
+                             dout, dfinal_state, dq, dk, dv, dg, dbeta, dinitial_state, workspace, ws_bytes, opt, &o,
+                             guard);
+  if (rc != GDN_OK) return rc;
   BwdArgs a;
   a.q = q;
   a.k = k;
@@ -248,6 +370,8 @@ int gdn_chunk_bwd(const void* q, const void* k, const void* v, const float* g, c
   a.d = make_dims(N, T, H_k, H_v, n_init, oe, current_sm_count());
   a.trunc_thr = o.trunc_log_threshold;
   a.scale = o.scale;
+  a.flag_budget = flag_budget(o);
+  a.withhold_fin = 0;
   return launch_bwd(a, (o.flags & GDN_FLAG_REUSE_FWD) != 0, (cudaStream_t)stream,
                     reinterpret_cast<cudaEvent_t*>(o.stage_events));
 }

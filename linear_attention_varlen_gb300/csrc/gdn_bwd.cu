@@ -41,6 +41,7 @@
 #include "gdn_common.cuh"
 #include "gdn_dev.cuh"
 #include "gdn_fwd.h"
+#include "gdn_host.h"
 #include "tmap.h"
 
 namespace gdn {
@@ -63,6 +64,7 @@ struct BwdParams {
   PlanDims d;
   BwdLayout L;
   float scale;
+  long long flag_budget;  // limit of a wait on another item's publication flag, SM clock cycles
 };
 
 __device__ __forceinline__ uint4 pack8(const float* x) {
@@ -654,7 +656,7 @@ __global__ void __launch_bounds__(kRevThreads, 1) rev_chain_kernel(const __grid_
   // wait for `flag` (uniform outcome)
   auto wait_uniform = [&](const int* flag) -> bool {
     if (cx.tid == 0) {
-      s_ok = wait_flag(flag, hd) ? 1 : 0;
+      s_ok = wait_flag(flag, hd, p.flag_budget) ? 1 : 0;
       __threadfence();
     }
     __syncthreads();
@@ -1633,6 +1635,8 @@ int setup_record_fwd(const BwdArgs& a, const BwdLayout& L, FwdParams& f) {
   f.ws = ws;
   f.trunc_thr = a.trunc_thr;
   f.scale = a.scale;
+  f.flag_budget = a.flag_budget;
+  f.withhold_fin = a.withhold_fin;
   f.st_img = ws + L.st_img;
   f.vp_img = ws + L.vp_img;
   f.p_img = ws + L.f.pimg;  // kkt_solve also forms P = scale (Q K^T o E) for the reverse chain
@@ -1661,8 +1665,10 @@ int launch_fwd_save(const BwdArgs& a, void* out, float* final_state, cudaStream_
 }
 
 int launch_bwd(const BwdArgs& a, bool reuse, cudaStream_t stream, cudaEvent_t* ev) {
-  static bool attr_done = false;
-  if (!attr_done) {
+  static PerDevice attr_done;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return kErrCuda;
+  if (!attr_done.done(dev)) {
     if (cudaFuncSetAttribute(rev_chain_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRevSmemBytes) !=
             cudaSuccess ||
         cudaFuncSetAttribute(rev_chain_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRevSmemBytes) !=
@@ -1674,7 +1680,7 @@ int launch_bwd(const BwdArgs& a, bool reuse, cudaStream_t stream, cudaEvent_t* e
     if (cudaFuncSetAttribute(dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kDqSmemBytes) !=
         cudaSuccess)
       return kErrCuda;
-    attr_done = true;
+    attr_done.mark(dev);
   }
   const PlanDims& d = a.d;
   BwdParams p;
@@ -1707,6 +1713,7 @@ int launch_bwd(const BwdArgs& a, bool reuse, cudaStream_t stream, cudaEvent_t* e
   p.dinit = a.dinit;
   p.ws = ws;
   p.scale = a.scale;
+  p.flag_budget = a.flag_budget;
   auto mark = [&](int i) {
     if (ev && ev[i]) cudaEventRecord(ev[i], stream);
   };

@@ -20,6 +20,8 @@ struct BwdArgs {
   size_t ws_bytes;
   PlanDims d;
   float trunc_thr, scale;
+  long long flag_budget;  // limit of a wait on another item's publication flag, SM clock cycles
+  int withhold_fin;       // forward of a training step: test hook of gdn_chunk_fwd
 };
 
 // Backward workspace: the forward recompute's workspace first, then the per-chunk records.

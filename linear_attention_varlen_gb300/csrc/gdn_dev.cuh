@@ -23,12 +23,13 @@ __device__ __forceinline__ int get_status(const Header* hd) {
   return *reinterpret_cast<const volatile int*>(&hd->status);
 }
 
-// Bounded wait on a publication flag; false on timeout (status set) or on an earlier error.
-__device__ __forceinline__ bool wait_flag(const int* flag, Header* hd) {
+// Bounded wait (`budget` clock cycles) on a publication flag; false on timeout (status set) or on
+// an earlier error.
+__device__ __forceinline__ bool wait_flag(const int* flag, Header* hd, long long budget) {
   const long long t0 = clock64();
   while (ld_acquire(flag) == 0) {
     if (get_status(hd) != 0) return false;
-    if (clock64() - t0 > kWaitBudget) {
+    if (clock64() - t0 > budget) {
       set_status(hd, kErrTimeout);
       return false;
     }

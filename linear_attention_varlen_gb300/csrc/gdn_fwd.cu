@@ -32,6 +32,7 @@
 #include "gdn_common.cuh"
 #include "gdn_dev.cuh"
 #include "gdn_fwd.h"
+#include "gdn_host.h"
 
 namespace gdn {
 using namespace bw;
@@ -1561,7 +1562,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) chain_kernel(const __grid_const
     } else if (dep <= -2) {
       const int j = dep_fork_seq(dep);
       if (cx.tid == 0) {
-        s_ok = wait_flag(&flags_fin[j * Hv + h], hd) ? 1 : 0;
+        s_ok = wait_flag(&flags_fin[j * Hv + h], hd, p.flag_budget) ? 1 : 0;
         __threadfence();
       }
       __syncthreads();
@@ -1578,7 +1579,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) chain_kernel(const __grid_const
         if (epi) load_state(cx, ws_ptr<float>(p, p.L.bmat) + ((size_t)dsl * Hv + h) * st_elems, S, true);
       } else {
         if (cx.tid == 0) {
-          s_ok = wait_flag(&flags_seg[dep * Hv + h], hd) ? 1 : 0;
+          s_ok = wait_flag(&flags_seg[dep * Hv + h], hd, p.flag_budget) ? 1 : 0;
           __threadfence();
         }
         __syncthreads();
@@ -1609,7 +1610,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) chain_kernel(const __grid_const
         } else {
           const int j = dep_fork_seq(d0);
           if (cx.tid == 0) {
-            s_ok = wait_flag(&flags_fin[j * Hv + h], hd) ? 1 : 0;
+            s_ok = wait_flag(&flags_fin[j * Hv + h], hd, p.flag_budget) ? 1 : 0;
             __threadfence();
           }
           __syncthreads();
@@ -1648,7 +1649,10 @@ __global__ void __launch_bounds__(kWsThreads, 1) chain_kernel(const __grid_const
     }
     if (last) {
       if (epi) save_state(cx, p.final_state + ((size_t)seq * Hv + h) * st_elems, S);
-      publish(&flags_fin[seq * Hv + h]);
+      if (!p.withhold_fin)
+        publish(&flags_fin[seq * Hv + h]);
+      else
+        __syncthreads();
     }
     __syncthreads();
   }
@@ -1789,8 +1793,10 @@ __global__ void __launch_bounds__(kOutThreads) out_kernel(const __grid_constant_
 // ========================================================================================= launch
 
 int launch_fwd(const FwdParams& p, cudaStream_t stream, cudaEvent_t* ev, bool plan_only) {
-  static bool attr_done = false;
-  if (!attr_done) {
+  static PerDevice attr_done;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return kErrCuda;
+  if (!attr_done.done(dev)) {
     if (cudaFuncSetAttribute(kkt_solve_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)(sizeof(KktSmem) + 1024)) != cudaSuccess)
       return kErrCuda;
@@ -1805,7 +1811,7 @@ int launch_fwd(const FwdParams& p, cudaStream_t stream, cudaEvent_t* ev, bool pl
         cudaFuncSetAttribute(out_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kOutSmemBytes) !=
             cudaSuccess)
       return kErrCuda;
-    attr_done = true;
+    attr_done.mark(dev);
   }
   auto mark = [&](int i) {
     if (ev && ev[i]) cudaEventRecord(ev[i], stream);

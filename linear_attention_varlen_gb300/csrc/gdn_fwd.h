@@ -25,6 +25,8 @@ struct FwdParams {
   FwdLayout L;
   float trunc_thr;
   float scale;
+  long long flag_budget;  // limit of a wait on another item's publication flag, SM clock cycles
+  int withhold_fin;       // test hook: final states are never published to forked documents
   // P = scale (Q K^T o E) per (chunk, value head), E_ij = e^{gamma_i - gamma_j} for j <= i inside
   // the chunk, bf16 smem image [cmax][Hv][8 KB], formed by kkt_solve
   uint8_t* p_img;

@@ -17,16 +17,21 @@
 //    array and give undefined results; order them on one stream.
 //  - The first call on a device looks up the array's device address (cudaGetSymbolAddress) and
 //    caches it per device; make that first call before any stream capture.
+//  - Errors found on the GPU (bad cu_seqlens or init_idx, an expired bounded wait) land in the
+//    array's status word: gdn_noalloc_status() reads it.
 #include <cuda_runtime.h>
 
 #include <cstdint>
 #include <mutex>
 
 #include "../../include/gdn.h"
+#include "gdn_common.cuh"
+#include "gdn_host.h"
 
 namespace {
 
-constexpr size_t kNoAllocScratchBytes = size_t(128) << 20;  // 128 MiB
+// 160 MiB: enough for a 32768-token document at 8 value heads (about 129 MiB with 148-152 SMs).
+constexpr size_t kNoAllocScratchBytes = size_t(160) << 20;
 constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) uint8_t g_scratch[kNoAllocScratchBytes];
@@ -60,17 +65,15 @@ extern "C" int gdn_chunk_fwd_noalloc(const void* q, const void* k, const void* v
                                      const int32_t* init_idx, const float* initial_state, int n_init, void* out,
                                      float* final_state, const gdn_options* opt, gdn_stream_t stream) {
   if (head_dim != 128) return GDN_ERR_UNSUPPORTED;
-  if (!out) return GDN_ERR_INVALID_ARG;
   // records kept for a backward need a workspace that the caller can hand to it
   if (opt && (opt->flags & GDN_FLAG_SAVE_FOR_BWD)) return GDN_ERR_INVALID_ARG;
-  // the tensors decide the GPU, as for gdn_chunk_fwd
-  cudaPointerAttributes attr;
-  const void* any = T > 0 ? out : static_cast<const void*>(final_state);
-  if (!any || cudaPointerGetAttributes(&attr, any) != cudaSuccess || attr.type != cudaMemoryTypeDevice) {
-    cudaGetLastError();
+  // the tensors decide the GPU (the same pointer rules as gdn_chunk_fwd, which checks them again)
+  const void* ptrs[] = {out, final_state, q, k, v, g, beta, cu_seqlens, init_idx, initial_state};
+  int dev = 0;
+  if (gdn::device_of(nullptr, ptrs, (int)(sizeof(ptrs) / sizeof(ptrs[0])), &dev) != gdn::kOk)
     return GDN_ERR_INVALID_ARG;
-  }
-  if (cudaSetDevice(attr.device) != cudaSuccess) return GDN_ERR_CUDA;
+  gdn::DeviceGuard guard;
+  if (!guard.set(dev)) return GDN_ERR_CUDA;
   const size_t need = gdn_fwd_workspace_size(N, T, H_k, H_v, opt);
   if (need == 0) return GDN_ERR_INVALID_ARG;
   if (need > kNoAllocScratchBytes) return GDN_ERR_WORKSPACE;
@@ -79,4 +82,15 @@ extern "C" int gdn_chunk_fwd_noalloc(const void* q, const void* k, const void* v
   if (rc != GDN_OK) return rc;
   return gdn_chunk_fwd(q, k, v, g, beta, cu_seqlens, N, T, H_k, H_v, head_dim, init_idx, initial_state, n_init, out,
                        final_state, ws, kNoAllocScratchBytes, opt, stream);
+}
+
+extern "C" int gdn_noalloc_status(int device, gdn_stream_t stream) {
+  if (device < 0 || device >= kMaxDevices) return GDN_ERR_INVALID_ARG;
+  void* ws = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    ws = g_addr[device];
+  }
+  if (!ws) return GDN_ERR_INVALID_ARG;  // no allocation-free call has run on this device
+  return gdn_workspace_status(ws, stream);
 }

@@ -277,3 +277,23 @@ def workload_train(n_docs: int = 4, doc_len: int = 16384, Hk: int = 2, Hv: int =
                    seed: int = SEEDS[4]) -> Problem:
     """Forward + backward training step over equal-length packed documents, with dO."""
     return make_problem(f"train_{n_docs}x{doc_len}_H{Hv}", seed, [doc_len] * n_docs, Hk, Hv, with_dout=True)
+
+
+# ----------------------------------------------------------------------------- device copies
+
+
+def to_device(p: Problem, device="cuda"):
+    """The problem's arrays as torch tensors on `device` (bf16 bit patterns viewed as bfloat16,
+    fp32 and int32 as they are): plain copies, no arithmetic."""
+    import torch
+    bf = lambda a: torch.from_numpy(np.ascontiguousarray(a)).view(torch.bfloat16).to(device)
+    f32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(device)
+    d = dict(q=bf(p.q), k=bf(p.k), v=bf(p.v), g=f32(p.g), beta=f32(p.beta),
+             cu_seqlens=torch.from_numpy(p.cu_seqlens.astype(np.int32)).to(device))
+    d["init_idx"] = None if p.init_idx is None else torch.from_numpy(p.init_idx.astype(np.int32)).to(device)
+    d["initial_state"] = None if p.initial_state is None else f32(p.initial_state)
+    if p.dout is not None:
+        d["dout"] = bf(p.dout)
+    if p.dfinal is not None:
+        d["dfinal_state"] = f32(p.dfinal)
+    return d

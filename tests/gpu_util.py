@@ -11,19 +11,7 @@ REL_L2 = 1e-2
 MAX_ABS = 2e-2
 
 
-def to_device(p: synth.Problem, device="cuda"):
-    import torch
-    bf = lambda a: torch.from_numpy(np.ascontiguousarray(a)).view(torch.bfloat16).to(device)
-    f32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(device)
-    d = dict(q=bf(p.q), k=bf(p.k), v=bf(p.v), g=f32(p.g), beta=f32(p.beta),
-             cu_seqlens=torch.from_numpy(p.cu_seqlens.astype(np.int32)).to(device))
-    d["init_idx"] = None if p.init_idx is None else torch.from_numpy(p.init_idx.astype(np.int32)).to(device)
-    d["initial_state"] = None if p.initial_state is None else f32(p.initial_state)
-    if p.dout is not None:
-        d["dout"] = bf(p.dout)
-    if p.dfinal is not None:
-        d["dfinal_state"] = f32(p.dfinal)
-    return d
+to_device = synth.to_device  # the problem's arrays on the device (plain copies)
 
 
 def bf16_to_f64(t):

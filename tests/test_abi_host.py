@@ -44,7 +44,7 @@ def test_status_strings(lib):
 def test_default_options(lib):
     o = gdn.COptions()
     lib.gdn_default_options(ctypes.byref(o))
-    assert (o.mode, o.trunc_log_threshold, o.segment_chunks, o.scale, o.flags) == (0, -10.0, 0, 1.0, 0)
+    assert (o.mode, o.trunc_log_threshold, o.segment_chunks, o.scale, o.flags, o.flag_wait_us) == (0, -10.0, 0, 1.0, 0, 0)
     assert o.stage_events is None
 
 

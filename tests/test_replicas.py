@@ -63,7 +63,8 @@ def test_reference_arm_runs_on_rank_zero_only():
 
 def test_reference_arm_reports_our_arm_config(monkeypatch):
     """The reference arm's line names the same workload as ours (same metric, unit and config);
-    only the timing note differs. The oracle step itself is replaced here: this checks the line."""
+    only the timing note and the statement of the per-step sample differ. The oracle step itself
+    is replaced here: this checks the line."""
     monkeypatch.setattr(bench, "_oracle_step", lambda p, f, cores: time.sleep(0.001))
 
     class A:
@@ -71,5 +72,7 @@ def test_reference_arm_reports_our_arm_config(monkeypatch):
     res = bench.run_reference(A(), rank=0)
     ours = bench.workload_config(32768, 8, 2, "exact", True, True)
     assert res["impl"] == "reference" and res["metric"] == bench.METRIC and res["unit"] == bench.UNIT
-    assert {k: v for k, v in res["config"].items() if k != "l2"} == {k: v for k, v in ours.items() if k != "l2"}
+    own = ("l2", "sample_tokens_per_step", "sample")
+    assert {k: v for k, v in res["config"].items() if k not in own} == {k: v for k, v in ours.items() if k != "l2"}
+    assert res["config"]["sample_tokens_per_step"] == 1024 and "1024" in res["config"]["sample"]
     assert res["cpu_baseline"]["kind"] == "oracle" and res["e2e"]["h2d_bytes_per_step"] == 0
