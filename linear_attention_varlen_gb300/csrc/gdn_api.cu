@@ -331,6 +331,7 @@ int gdn_chunk_fwd(const void* q, const void* k, const void* v, const float* g, c
   p.flag_budget = flag_budget(o);
   p.withhold_fin = (o.flags & GDN_FLAG_TEST_WITHHOLD_FORK) ? 1 : 0;
   p.p_img = p.ws + p.L.pimg;
+  p.p_factored = 1;
   return launch_fwd(p, (cudaStream_t)stream, reinterpret_cast<cudaEvent_t*>(o.stage_events));
 }
 

@@ -502,8 +502,31 @@ __global__ void __launch_bounds__(256, 2) kkt_solve_kernel(const __grid_constant
           *reinterpret_cast<uint4*>(p.tu_lo + rec * 8192 + off) = make_uint4(ul[0], ul[1], ul[2], ul[3]);
         }
       }
-      // P = scale (Q K^T o E): rows i < n, j <= i, 8 threads per 128-byte row
-      if (want_p) {
+      // P = scale (Q K^T o E): rows i < n, j <= i, 8 threads per 128-byte row. In the factored
+      // form of the inference forward the row factor scale e^{gamma_i} is left to the chain, which
+      // applies it to (Q S + P'' V') as a whole: P''_ij = (Q K^T)_ij e^{-gamma_j}, finite for every
+      // row whose decay since the chunk start stays above kExactCut; a row below it keeps P and
+      // drops its Q S term in the chain (that term is below e^{kExactCut} of the chunk-start state).
+      if (want_p && p.p_factored) {
+        uint8_t* dp = p.p_img + rec * 8192;
+        for (int e = t; e < 64 * 8; e += 64) {
+          const int i = e >> 3, cj = e & 7;
+          const float4 q0 = *reinterpret_cast<const float4*>(qk + fz(i, 8 * cj));
+          const float4 q1 = *reinterpret_cast<const float4*>(qk + fz(i, 8 * cj + 4));
+          const float qv[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+          const float gi = gam[i];
+          const bool row_f = gi >= kExactCut;
+          float pv[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const int j = 8 * cj + u;
+            pv[u] = (j <= i && i < n) ? (row_f ? egi[j] * qv[u] : __expf(gi - gam[j]) * p.scale * qv[u]) : 0.f;
+          }
+          *reinterpret_cast<uint4*>(dp + i * 128 + ((cj ^ (i & 7)) << 4)) =
+              make_uint4(pack_bf16x2(pv[0], pv[1]), pack_bf16x2(pv[2], pv[3]), pack_bf16x2(pv[4], pv[5]),
+                         pack_bf16x2(pv[6], pv[7]));
+        }
+      } else if (want_p) {
         uint8_t* dp = p.p_img + rec * 8192;
         for (int e = t; e < 64 * 8; e += 64) {
           const int i = e >> 3, cj = e & 7;
@@ -712,41 +735,57 @@ __device__ __forceinline__ void prefetch_state_l2(const float* m, int tid, int n
 // =========================================================================== warp-specialized chain
 //
 // The forward chain with three roles in one CTA of 10 warps:
-//   warp 8      TMA producer: K, V, T_u, P (from kkt_solve) and gamma of chunk j into stage j & 1;
-//               Q and T_w (one buffer).
+//   warp 8      TMA producer: K, V, P'' (from kkt_solve) and gamma of chunk j into stage j & 1; T_u and
+//               T_w (one buffer each, refilled once their product has read them); Q straight into
+//               rows 64-127 of the stacked operand once the previous chunk's product has read it.
 //   warp 9      MMA issuer (one lane), per chunk j:
-//                 U = [*; T_u] V -> D2 rows 64-127, D1 = [Q~; -W] S, then chunk j+1's W = T_w K
-//                 (staged by the epilogue while chunk j runs), then D2 = K^T V'_s, D1 += [P; *] V'.
-//   warps 0-7   epilogue: V' = U - W S, staging of chunk j+1 (-W, Q~), S += K^T V'_s, O.
+//                 D1 = [T_u; 0] V (issued early: the tensor pipe is idle while the state is
+//                 staged), then D1 += [-W; Q] S (the state product, alone on the critical path), so
+//                 that D1 = [V'; Q S]; chunk j+1's W = T_w K as soon as its operands are in (tested
+//                 without blocking); D2 = K^T V'_s (the state update, committed on its own); then
+//                 D1 += [*; P''] V' for the output.
+//   warps 0-7   epilogue: V' (rows 0-63 of D1), staging of chunk j+1 (-W), S += K^T V'_s, O.
+// The query enters the product unscaled: D1 rows 64-127 = Q S + P'' V' with P''_ij = (Q K^T)_ij
+// e^{-gamma_j}, so O_i = scale e^{gamma_i} (Q S + P'' V')_i. A row whose decay since the chunk
+// start is below kExactCut keeps the plain P and has its query row zeroed instead: its Q S term is
+// below e^{kExactCut} of the chunk-start state (the cut of the exact split's warm-ups).
 // Hand-offs are mbarriers only: tcgen05.commit from the issuer, one elected arrival from the
-// epilogue after a named barrier, TMA transaction counts from the producer. Rows 0-63 of the U
-// product and rows 64-127 of the P product are never read, so neither operand needs zero rows.
+// epilogue after a named barrier, TMA transaction counts from the producer. The P'' product adds
+// to rows 0-63 of D1 (V', already read) whatever precedes P'' in shared memory.
 
 struct WsSmem {
   uint8_t k[2][16384];   // [stage] K rows t, two dk blocks     (B K-major, B MN-major, A MN-major)
-  uint8_t v[1][16384];   // V rows t, two dv blocks (one buffer, refilled once U is done) (B MN-major)
-  uint8_t ostage[2][8192];  // O rows t, two dv blocks (bf16), the source of the TMA store; in a
-                            // run without outputs, the second V buffer
-  uint8_t q[2][8192];    // Q rows t, two dk blocks (one buffer) (A K-major)
-  uint8_t pt[4][8192];   // P stage 0, P stage 1, T_u stage 0, T_u stage 1 (contiguous; TMA-loaded)
+  uint8_t v[2][16384];   // [stage] V rows t, two dv blocks     (B MN-major)
+  uint8_t ostage[2][8192];  // O rows t, two dv blocks (bf16), the source of the TMA store
+  uint8_t pt[4][8192];   // T_u (one buffer), a zero block, P'' stage 0, P'' stage 1: [T_u; 0] and
+                         // [*; P''] are M = 128 operands (contiguous, 1024-aligned)
   uint8_t tw[8192];      // T diag(beta e^gamma) (one buffer)  (A, M = 64)
-  uint8_t qw[2][16384];  // dk block b: rows 0-63 Q~, rows 64-127 -W   (A, M = 128)
+  uint8_t qw[2][16384];  // dk block b: rows 0-63 -W, rows 64-127 Q (TMA)   (A, M = 128)
   uint8_t vo[2][8192];   // V'                                  (B MN-major)
   uint8_t vs[2][8192];   // diag(e^{gamma_C - gamma}) V'        (B MN-major)
   uint8_t s[2][16384];   // S bf16 rows dk                      (B MN-major)
   float gam[2][64];      // [stage] chunk-local cumulative gate
 };
 constexpr int kWsThreads = 320;
+// Buffers affine_apply borrows (idle at the start of an item): M hi in the stacked operand, M lo in
+// the two V stages, S_start lo in V' and V'_s (contiguous), the fp32 stage in K. The zero block is
+// not touched.
 __device__ __forceinline__ AffineBufs affine_bufs(WsSmem& sm) {
-  return {sm.qw[0], sm.q[0], (uint32_t)(sm.vo[0] - sm.q[0]), sm.v[0], (uint32_t)(sm.vs[0] - sm.v[0]),
-          sm.s[0], reinterpret_cast<float*>(sm.k[0])};
+  return {sm.qw[0], sm.v[0], 16384u, sm.vo[0], (uint32_t)(sm.vs[0] - sm.vo[0]), sm.s[0],
+          reinterpret_cast<float*>(sm.k[0])};
+}
+// Zero the zero block once per CTA (nothing writes it afterwards).
+__device__ __forceinline__ void ws_zero_block(WsSmem& sm, int tid, int nthreads) {
+  for (int e = tid; e < 8192 / 16; e += nthreads) reinterpret_cast<uint4*>(sm.pt[1])[e] = make_uint4(0, 0, 0, 0);
 }
 
 struct WsBars {
-  uint64_t full[3], fullq, fullu, empty[3], emptyq, a_done, pre_done, b_done, epi1, staged, epi2, vfree;
+  uint64_t full[3], fullq, fullu, fullo, empty[3], emptyq, qfree, tufree, o_read[2], a_done, pre_done, b_done, o_done,
+      epi1, staged, epi2, vfree;
 };
 struct WsPhase {
-  uint32_t full[3], fullq, fullu, empty[3], emptyq, a_done, pre_done, b_done, epi1, staged, epi2, vfree;
+  uint32_t full[3], fullq, fullu, fullo, empty[3], emptyq, qfree, tufree, o_read[2], a_done, pre_done, b_done, o_done,
+      epi1, staged, epi2, vfree;
 };
 // TMEM columns of D1 for chunk j: two accumulators in turn, so that the output of chunk j is
 // read while chunk j + 1 already runs (columns 384-511 hold Q K^T only in the record path).
@@ -787,17 +826,15 @@ __device__ bool run_ws(const FwdParams& p, ChainCtx& cx, WsBars& bb, WsPhase& ph
   const int Hv = p.d.Hv;
   const int32_t* ctok = ws_ptr<int32_t>(p, p.L.chunk_tok0);
   const int32_t* clen = ws_ptr<int32_t>(p, p.L.chunk_len);
-  // A run without outputs has no use for the O stage: V then alternates between sm.v and the O
-  // stage (released with the rest of the stage), else V has one buffer refilled after each U.
-  const bool dbl_v = gc_out >= gc1;
-  auto vbuf = [&](int j) -> uint8_t* { return (dbl_v && (j & 1)) ? sm.ostage[0] : sm.v[0]; };
+  auto is_out = [&](int j) { return gc0 + j >= gc_out; };
 
   if (cx.warp == 8) {
     // ------------------------------------------------------------------ TMA producer
     if (cx.lane == 0) {
       for (int j = 0; j < n; ++j) {
         const int gc = gc0 + j, st = j & 1, tok0 = ctok[gc];
-        const bool out = gc >= gc_out;
+        const bool out = is_out(j);
+        const size_t r = (size_t)gc * Hv + h;
         if (j + 2 < n) {  // chunk j + 2 into L2 while its stage is still in use
           const int g2 = gc + 2, t2 = ctok[g2];
           const size_t r2 = (size_t)g2 * Hv + h;
@@ -818,32 +855,36 @@ __device__ bool run_ws(const FwdParams& p, ChainCtx& cx, WsBars& bb, WsPhase& ph
         }
         if (j >= 2) role_wait(&bb.empty[st], ph.empty[st], abort);
         if (*abort) break;
-        mbar_arrive_expect_tx(&bb.full[st], 16384 + 256 + (kWithU ? 16384 + 8192 : 0) + (out ? 8192 : 0));
-        if (out) bulk_load(sm.pt[st], p.p_img + ((size_t)gc * Hv + h) * 8192, 8192, &bb.full[st]);
+        mbar_arrive_expect_tx(&bb.full[st], 16384 + 256 + (kWithU ? 16384 : 0) + (out ? 8192 : 0));
+        if (out) bulk_load(sm.pt[2 + st], p.p_img + r * 8192, 8192, &bb.full[st]);
         tma_load_3d(sm.k[st], &p.tm_k, 0, hk, tok0, &bb.full[st]);
         tma_load_3d(sm.k[st] + 8192, &p.tm_k, 64, hk, tok0, &bb.full[st]);
-        if (kWithU) bulk_load(sm.pt[2 + st], p.ws + p.L.tu + ((size_t)gc * Hv + h) * 8192, 8192, &bb.full[st]);
-        bulk_load(sm.gam[st], p.ws + p.L.gam + ((size_t)gc * Hv + h) * 256, 256, &bb.full[st]);
-        if (j >= 1) role_wait(&bb.emptyq, ph.emptyq, abort);
-        if (*abort) break;
-        mbar_arrive_expect_tx(&bb.fullq, 8192 + (out ? 16384 : 0));
-        if (out) {
-          tma_load_3d(sm.q[0], &p.tm_q, 0, hk, tok0, &bb.fullq);
-          tma_load_3d(sm.q[1], &p.tm_q, 64, hk, tok0, &bb.fullq);
-        }
-        bulk_load(sm.tw, p.ws + p.L.tw + ((size_t)gc * Hv + h) * 8192, 8192, &bb.fullq);
+        bulk_load(sm.gam[st], p.ws + p.L.gam + r * 256, 256, &bb.full[st]);
         if (kWithU) {
-          // V of chunk j (counted in full[st]) once the U product of chunk j - 1 has read the buffer
-          if (!dbl_v && j >= 1) role_wait(&bb.vfree, ph.vfree, abort);
+          tma_load_3d(sm.v[st], &p.tm_v, 0, h, tok0, &bb.full[st]);
+          tma_load_3d(sm.v[st] + 8192, &p.tm_v, 64, h, tok0, &bb.full[st]);
+          if (j >= 1) role_wait(&bb.tufree, ph.tufree, abort);  // the previous U product has read T_u
           if (*abort) break;
-          tma_load_3d(vbuf(j), &p.tm_v, 0, h, tok0, &bb.full[st]);
-          tma_load_3d(vbuf(j) + 8192, &p.tm_v, 64, h, tok0, &bb.full[st]);
+          mbar_arrive_expect_tx(&bb.fullu, 8192);
+          bulk_load(sm.pt[0], p.ws + p.L.tu + r * 8192, 8192, &bb.fullu);
+        }
+        if (j >= 1) role_wait(&bb.emptyq, ph.emptyq, abort);  // the previous W product has read T_w
+        if (*abort) break;
+        mbar_arrive_expect_tx(&bb.fullq, 8192);
+        bulk_load(sm.tw, p.ws + p.L.tw + r * 8192, 8192, &bb.fullq);
+        if (out) {
+          // Q into rows 64-127 of the stacked operand once the product of chunk j - 1 has read it
+          if (j >= 1) role_wait(&bb.qfree, ph.qfree, abort);
+          if (*abort) break;
+          mbar_arrive_expect_tx(&bb.fullo, 16384);
+          tma_load_3d(sm.qw[0] + 8192, &p.tm_q, 0, hk, tok0, &bb.fullo);
+          tma_load_3d(sm.qw[1] + 8192, &p.tm_q, 64, hk, tok0, &bb.fullo);
         }
       }
       // drain: wait for the release of the last uses so that every phase is consumed
       for (int j = (n >= 2 ? n - 2 : 0); j < n; ++j) role_wait(&bb.empty[j & 1], ph.empty[j & 1], abort);
       role_wait(&bb.emptyq, ph.emptyq, abort);
-      if (kWithU && !dbl_v) role_wait(&bb.vfree, ph.vfree, abort);
+      if (kWithU) role_wait(&bb.tufree, ph.tufree, abort);
     }
     return !*abort;
   }
@@ -865,39 +906,63 @@ __device__ bool run_ws(const FwdParams& p, ChainCtx& cx, WsBars& bb, WsPhase& ph
       if (!*abort) prep(0);
       for (int j = 0; j < n && !*abort; ++j) {
         const int st = j & 1;
-        const bool out = gc0 + j >= gc_out;
+        const bool out = is_out(j);
+        const uint32_t d1 = tm + d1_col(j);
+        if (kWithU) {
+          // U = T_u V into rows 0-63 of D1 (rows 64-127 get zero) once the output of chunk j - 2 has
+          // left these columns; V(j) came with the stage prep(j) waited for. One o_read barrier per
+          // D1 buffer: the read of chunk j - 1 goes to the other one, so this wait is never two
+          // phases behind.
+          role_wait(&bb.fullu, ph.fullu, abort);
+          if (j >= 2 && is_out(j - 2)) role_wait(&bb.o_read[st], ph.o_read[st], abort);
+          if (*abort) break;
+          for (int ks = 0; ks < 4; ++ks)
+            umma_bf16(d1, kmajor_desc(smem_u32(sm.pt[0]), 16384, ks), mnmajor_desc(smem_u32(sm.v[st]), 8192, ks),
+                      idesc_bf16(128, 128, 0, 1), ks > 0);
+          umma_commit(&bb.tufree);
+        }
         role_wait(&bb.staged, ph.staged, abort);
         role_wait(&bb.epi2, ph.epi2, abort);
         if (*abort) break;
-        const uint32_t d1 = tm + d1_col(j);
-        if (kWithU)
-          for (int ks = 0; ks < 4; ++ks)
-            umma_bf16(tm + kTmD2, kmajor_desc(smem_u32(sm.pt[1 + st]), 16384, ks),
-                      mnmajor_desc(smem_u32(vbuf(j)), 8192, ks), idesc_bf16(128, 128, 0, 1), ks > 0);
         for (int ks = 0; ks < 8; ++ks)
           umma_bf16(d1, kmajor_desc(smem_u32(sm.qw[0]), 16384, ks), mnmajor_desc(smem_u32(sm.s[0]), 16384, ks),
-                    idesc_bf16(128, 128, 0, 1), ks > 0);
+                    idesc_bf16(128, 128, 0, 1), (kWithU || ks > 0) ? 1 : 0);
         umma_commit(&bb.a_done);
-        if (kWithU && !dbl_v) umma_commit(&bb.vfree);
-        if (j + 1 < n) {
+        if (j + 1 < n && is_out(j + 1)) umma_commit(&bb.qfree);  // the producer may load Q(j + 1)
+        // chunk j + 1's W now if its operands are in (the tensor pipe is idle during the V' epilogue),
+        // else after the state update
+        bool next_prepped = false;
+        if (j + 1 < n && mbar_test(&bb.full[st ^ 1], ph.full[st ^ 1]) && mbar_test(&bb.fullq, ph.fullq)) {
           role_wait(&bb.full[st ^ 1], ph.full[st ^ 1], abort);
           role_wait(&bb.fullq, ph.fullq, abort);
-          if (*abort) break;
           prep(j + 1);
+          next_prepped = true;
         }
         role_wait(&bb.epi1, ph.epi1, abort);
         if (*abort) break;
         for (int ks = 0; ks < 4; ++ks)
           umma_bf16(tm + kTmD2, mnmajor_desc(smem_u32(sm.k[st]), 8192, ks), mnmajor_desc(smem_u32(sm.vs[0]), 8192, ks),
                     idesc_bf16(128, 128, 1, 1), ks > 0);
-        if (out)
-          for (int ks = 0; ks < 4; ++ks)
-            umma_bf16(d1, kmajor_desc(smem_u32(sm.pt[j & 1]), 16384, ks),
-                      mnmajor_desc(smem_u32(sm.vo[0]), 8192, ks), idesc_bf16(128, 128, 0, 1), 1);
         umma_commit(&bb.b_done);
+        if (out) {
+          for (int ks = 0; ks < 4; ++ks)
+            umma_bf16(d1, kmajor_desc(smem_u32(sm.pt[1 + st]), 16384, ks), mnmajor_desc(smem_u32(sm.vo[0]), 8192, ks),
+                      idesc_bf16(128, 128, 0, 1), 1);
+          umma_commit(&bb.o_done);
+        }
         umma_commit(&bb.empty[st]);
+        if (j + 1 < n && !next_prepped) {
+          role_wait(&bb.full[st ^ 1], ph.full[st ^ 1], abort);
+          role_wait(&bb.fullq, ph.fullq, abort);
+          if (*abort) break;
+          prep(j + 1);
+        }
       }
       role_wait(&bb.epi2, ph.epi2, abort);  // the epilogue's last state hand-off
+      // the outputs of the last two chunks have been read (every phase consumed)
+      if (kWithU)
+        for (int j = (n >= 2 ? n - 2 : 0); j < n; ++j)
+          if (is_out(j)) role_wait(&bb.o_read[j & 1], ph.o_read[j & 1], abort);
     }
     return !*abort;
   }
@@ -905,32 +970,13 @@ __device__ bool run_ws(const FwdParams& p, ChainCtx& cx, WsBars& bb, WsPhase& ph
   const uint32_t lane_base = (uint32_t)(32 * cx.q4) << 16;
   e_handoff(cx.tid, &bb.epi2);  // S(gc0) is staged
   auto staging = [&](int j) {
-    const int gc = gc0 + j, st = j & 1;
-    const bool out = gc >= gc_out;
+    const int st = j & 1;
     role_wait(&bb.full[st], ph.full[st], abort);
-    role_wait(&bb.fullq, ph.fullq, abort);
-    const float* gm = sm.gam[st];
-    if (out) {
-      for (int e = cx.tid; e < 2 * 64 * 8; e += 256) {
-        const int b = e >> 9, r = (e >> 3) & 63, cj = e & 7;
-        const uint32_t off = r * 128 + ((cj ^ (r & 7)) << 4);
-        uint4 raw = *reinterpret_cast<const uint4*>(sm.q[b] + off);
-        const float sc = __expf(gm[r]) * p.scale;
-        __nv_bfloat162* x = reinterpret_cast<__nv_bfloat162*>(&raw);
-        uint32_t w[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          float2 f = __bfloat1622float2(x[u]);
-          w[u] = pack_bf16x2(f.x * sc, f.y * sc);
-        }
-        *reinterpret_cast<uint4*>(sm.qw[b] + off) = make_uint4(w[0], w[1], w[2], w[3]);
-      }
-    }
     role_wait(&bb.pre_done, ph.pre_done, abort);
     {
-      // all 32 lanes: rows r0 = 16 q4 + lane / 4 and r0 + 8 of W (M = 64) go to rows 64 + r of the
+      // all 32 lanes: rows r0 = 16 q4 + lane / 4 and r0 + 8 of W (M = 64) go to rows r of the
       // stacked operand, column pairs
-      const int c2 = 2 * (cx.lane & 3), r0 = 64 + 16 * cx.q4 + (cx.lane >> 2);
+      const int c2 = 2 * (cx.lane & 3), r0 = 16 * cx.q4 + (cx.lane >> 2);
 #pragma unroll
       for (int hc = 0; hc < 2; ++hc) {
         float v[16];
@@ -945,34 +991,42 @@ __device__ bool run_ws(const FwdParams& p, ChainCtx& cx, WsBars& bb, WsPhase& ph
         }
       }
     }
-    e_handoff(cx.tid, &bb.staged, &bb.emptyq);
+    if (is_out(j)) {
+      role_wait(&bb.fullo, ph.fullo, abort);  // Q(j) is in rows 64-127
+      const float* gm = sm.gam[st];
+      if (gm[63] < kExactCut) {  // gamma is nonincreasing: zero the query rows past the cut
+        for (int e = cx.tid; e < 2 * 64 * 8; e += 256) {
+          const int b = e >> 9, r = (e >> 3) & 63, cj = e & 7;
+          if (gm[r] < kExactCut)
+            *reinterpret_cast<uint4*>(sm.qw[b] + 8192 + r * 128 + (cj << 4)) = make_uint4(0, 0, 0, 0);
+        }
+      }
+    }
+    e_handoff(cx.tid, &bb.staged);
   };
   staging(0);
   for (int j = 0; j < n; ++j) {
     const int gc = gc0 + j, st = j & 1;
-    const bool out = gc >= gc_out;
+    const bool out = is_out(j);
     role_wait(&bb.a_done, ph.a_done, abort);
     const float* gm = sm.gam[st];
     const float gC = gm[63];
-    if (cx.q4 >= 2) {
-      // V' = U - W S, rows t = lanes 64-127
-      const int t = 32 * (cx.q4 - 2) + cx.lane;
+    // this thread's output row factor (read before the stage is released)
+    float of = 0.f;
+    if (out && cx.q4 >= 2) {
+      const float gt = gm[32 * (cx.q4 - 2) + cx.lane];
+      of = gt >= kExactCut ? p.scale * __expf(gt) : 1.f;
+    }
+    if (cx.q4 < 2) {
+      // V' = U - W S, rows t = lanes 0-63
+      const int t = 32 * cx.q4 + cx.lane;
       const float sc = __expf(gC - gm[t]);
 #pragma unroll
       for (int hc = 0; hc < 2; ++hc) {
         float v[32];
         tmem_ld16(cx.tmem + d1_col(j) + lane_base + 64 * cx.half + 32 * hc, v);
         tmem_ld16(cx.tmem + d1_col(j) + lane_base + 64 * cx.half + 32 * hc + 16, v + 16);
-        if (kWithU) {
-          float u[32];
-          tmem_ld16(cx.tmem + kTmD2 + lane_base + 64 * cx.half + 32 * hc, u);
-          tmem_ld16(cx.tmem + kTmD2 + lane_base + 64 * cx.half + 32 * hc + 16, u + 16);
-          tmem_ld_wait();
-#pragma unroll
-          for (int x = 0; x < 32; ++x) v[x] += u[x];
-        } else {
-          tmem_ld_wait();
-        }
+        tmem_ld_wait();
 #pragma unroll
         for (int cj4 = 0; cj4 < 4; ++cj4) {
           const int cj = 4 * hc + cj4;
@@ -986,7 +1040,9 @@ __device__ bool run_ws(const FwdParams& p, ChainCtx& cx, WsBars& bb, WsPhase& ph
         }
       }
     }
-    e_handoff(cx.tid, &bb.epi1);
+    // the epilogue reads nothing of stage st after this point (gamma is in registers): release it
+    // here, so that chunk j + 2's loads go out as soon as the issuer's last product has read it
+    e_handoff(cx.tid, &bb.epi1, &bb.empty[st]);
     if (j + 1 < n) staging(j + 1);
     role_wait(&bb.b_done, ph.b_done, abort);
     {
@@ -1002,28 +1058,38 @@ __device__ bool run_ws(const FwdParams& p, ChainCtx& cx, WsBars& bb, WsPhase& ph
       }
       store_state_bf16_to(sm, cx, S);
     }
-    e_handoff(cx.tid, &bb.epi2, &bb.empty[st]);
-    // O of chunk j (rows 0-63 of D1[j], warps of lane quadrants 0-1), while chunk j + 1 runs:
+    e_handoff(cx.tid, &bb.epi2);
+    // O of chunk j (rows 64-127 of D1[j], warps of lane quadrants 2-3), while chunk j + 1 runs:
     // a whole chunk goes out by TMA store from a shared-memory stage, a partial one (the end of a
     // document) row by row so that the next document's rows are not touched
-    if (out && cx.q4 < 2) {
-      const int t = 32 * cx.q4 + cx.lane;
+    if (out && cx.q4 >= 2) {
+      role_wait(&bb.o_done, ph.o_done, abort);
+      const int t = 32 * (cx.q4 - 2) + cx.lane;
       const int nn = clen[gc];
       if (nn == kChunk) {
-        if (cx.tid == 0) bulk_wait_read_all();  // the previous store has read the stage
+        if (cx.tid == 64) bulk_wait_read_all();  // the previous store has read the stage
         o_sync();
       }
+      float v[64];
 #pragma unroll
       for (int hc = 0; hc < 2; ++hc) {
-        float v[32];
-        tmem_ld16(cx.tmem + d1_col(j) + lane_base + 64 * cx.half + 32 * hc, v);
-        tmem_ld16(cx.tmem + d1_col(j) + lane_base + 64 * cx.half + 32 * hc + 16, v + 16);
-        tmem_ld_wait();
+        tmem_ld16(cx.tmem + d1_col(j) + lane_base + 64 * cx.half + 32 * hc, v + 32 * hc);
+        tmem_ld16(cx.tmem + d1_col(j) + lane_base + 64 * cx.half + 32 * hc + 16, v + 32 * hc + 16);
+      }
+      tmem_ld_wait();
+      // these TMEM columns may take the U product of chunk j + 2 from here on
+      tc_fence_before();
+      o_sync();
+      if (kWithU && cx.tid == 64) mbar_arrive(&bb.o_read[st]);
+#pragma unroll
+      for (int x = 0; x < 64; ++x) v[x] *= of;
+#pragma unroll
+      for (int hc = 0; hc < 2; ++hc) {
         if (nn == kChunk) {
 #pragma unroll
           for (int cj4 = 0; cj4 < 4; ++cj4) {
             const int cj = 4 * hc + cj4;
-            const float* x = v + 8 * cj4;
+            const float* x = v + 32 * hc + 8 * cj4;
             *reinterpret_cast<uint4*>(sm.ostage[cx.half] + t * 128 + ((cj ^ (t & 7)) << 4)) =
                 make_uint4(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]), pack_bf16x2(x[4], x[5]),
                            pack_bf16x2(x[6], x[7]));
@@ -1032,7 +1098,7 @@ __device__ bool run_ws(const FwdParams& p, ChainCtx& cx, WsBars& bb, WsPhase& ph
           uint4* dst = reinterpret_cast<uint4*>(p.out + ((size_t)(ctok[gc] + t) * Hv + h) * kDim + 64 * cx.half);
 #pragma unroll
           for (int cj4 = 0; cj4 < 4; ++cj4) {
-            const float* x = v + 8 * cj4;
+            const float* x = v + 32 * hc + 8 * cj4;
             dst[4 * hc + cj4] = make_uint4(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]), pack_bf16x2(x[4], x[5]),
                                            pack_bf16x2(x[6], x[7]));
           }
@@ -1041,7 +1107,7 @@ __device__ bool run_ws(const FwdParams& p, ChainCtx& cx, WsBars& bb, WsPhase& ph
       if (nn == kChunk) {
         fence_proxy_async_smem();
         o_sync();
-        if (cx.tid == 0) {
+        if (cx.tid == 64) {
           tma_store_3d(&p.tm_o, sm.ostage[0], 0, h, ctok[gc]);
           tma_store_3d(&p.tm_o, sm.ostage[1], 64, h, ctok[gc]);
           bulk_commit_group();
@@ -1049,7 +1115,7 @@ __device__ bool run_ws(const FwdParams& p, ChainCtx& cx, WsBars& bb, WsPhase& ph
       }
     }
   }
-  if (cx.tid == 0) bulk_wait_all();  // every output store has landed before the buffers are reused
+  if (cx.tid == 64) bulk_wait_all();  // every output store has landed before the buffers are reused
   return !*abort;
 }
 
@@ -1380,10 +1446,16 @@ __global__ void __launch_bounds__(kWsThreads, 1) chain_kernel(const __grid_const
     mbar_init(&wbars.full[2], 1);
     mbar_init(&wbars.fullq, 1);
     mbar_init(&wbars.fullu, 1);
+    mbar_init(&wbars.fullo, 1);
+    mbar_init(&wbars.qfree, 1);
+    mbar_init(&wbars.tufree, 1);
+    mbar_init(&wbars.o_read[0], 1);
+    mbar_init(&wbars.o_read[1], 1);
+    mbar_init(&wbars.o_done, 1);
     mbar_init(&wbars.empty[0], 2);
     mbar_init(&wbars.empty[1], 2);
     mbar_init(&wbars.empty[2], 2);
-    mbar_init(&wbars.emptyq, rec ? 1 : 2);  // the forward's epilogue also releases Q
+    mbar_init(&wbars.emptyq, 1);
     mbar_init(&wbars.a_done, 1);
     mbar_init(&wbars.pre_done, 1);
     mbar_init(&wbars.b_done, 1);
@@ -1395,6 +1467,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) chain_kernel(const __grid_const
     fence_mbar_init();
   }
   if (cx.warp == 0) tmem_alloc(&tmem_holder, 512);
+  if constexpr (!kRec) ws_zero_block(*wss, cx.tid, kWsThreads);
   sync_generic_to_async();
   cx.tmem = tmem_holder;
 

@@ -30,6 +30,9 @@ struct FwdParams {
   // P = scale (Q K^T o E) per (chunk, value head), E_ij = e^{gamma_i - gamma_j} for j <= i inside
   // the chunk, bf16 smem image [cmax][Hv][8 KB], formed by kkt_solve
   uint8_t* p_img;
+  // 1: kkt_solve writes P in the factored form the inference chain uses (row factor scale e^{gamma_i}
+  // taken out: P''_ij = (Q K^T)_ij e^{-gamma_j}; see kkt_solve); 0: P itself (the record paths)
+  int p_factored;
   // Recording forward only (the backward's recompute, or a forward that keeps its records for the
   // backward; all NULL for a plain forward): per (chunk, value head) records. With `out` set, o is
   // formed from them after the chain.
