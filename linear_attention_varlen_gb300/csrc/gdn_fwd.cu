@@ -42,15 +42,19 @@ using namespace bw;
 // keep_mzero: a backward that reuses a forward's records keeps that forward's pass-1 findings
 // (which segment transitions are exactly zero); the maps it rebuilds are the same.
 constexpr int kPlanThreads = 256;  // one block; the scans run in tiles of this many documents / segments
+constexpr int kPlanSmemDocs = 2048;  // per-document offsets kept in shared memory up to this many documents
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constant__ FwdParams p, int keep_mzero) {
   Header* hd = ws_ptr<Header>(p, p.L.header);
-  int32_t* seq_chunk0 = ws_ptr<int32_t>(p, p.L.seq_chunk0);
-  int32_t* seq_seg0 = ws_ptr<int32_t>(p, p.L.seq_seg0);
   const int N = p.d.N;
   const int tid = threadIdx.x, nt = blockDim.x;
   __shared__ int s_bad, s_L, s_longest;
   __shared__ int s_carry[2];
   __shared__ int s_scan[kPlanThreads];
+  __shared__ int32_t s_c0[kPlanSmemDocs + 1], s_s0[kPlanSmemDocs + 1];
+  // the lookups below read these offsets many times: from shared memory when they fit
+  const bool in_smem = N <= kPlanSmemDocs;
+  int32_t* seq_chunk0 = in_smem ? s_c0 : ws_ptr<int32_t>(p, p.L.seq_chunk0);
+  int32_t* seq_seg0 = in_smem ? s_s0 : ws_ptr<int32_t>(p, p.L.seq_seg0);
   if (tid == 0) {
     s_bad = 0;
     s_longest = 0;
@@ -121,6 +125,14 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
   const int total_segs = s_carry[1];
   if (tid == 0) seq_seg0[N] = total_segs;
   __syncthreads();
+  if (in_smem) {  // the other kernels read the offsets from the workspace
+    int32_t* gc0 = ws_ptr<int32_t>(p, p.L.seq_chunk0);
+    int32_t* gs0 = ws_ptr<int32_t>(p, p.L.seq_seg0);
+    for (int i = tid; i <= N; i += nt) {
+      gc0[i] = s_c0[i];
+      gs0[i] = s_s0[i];
+    }
+  }
   // chunk and segment tables
   int32_t* cs = ws_ptr<int32_t>(p, p.L.chunk_seq);
   int32_t* ct = ws_ptr<int32_t>(p, p.L.chunk_tok0);
@@ -137,7 +149,6 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
   int32_t* mz = ws_ptr<int32_t>(p, p.L.mzero);
   if (!keep_mzero)
     for (int e = tid; e < (int)p.L.slots * p.d.Hv; e += nt) mz[e] = 0;
-  __syncthreads();
   // slots and pass-1 units: only split segments other than the last of their document get them
   // (exact mode); a block scan over the segments numbers them in segment order
   int32_t* slot = ws_ptr<int32_t>(p, p.L.seg_slot);
@@ -151,11 +162,14 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
     const int s = base + tid;
     int need = 0, units = 0;
     if (s < total_segs) {
-      const int i = si[4 * s];
+      // the segment's document and dependency, recomputed (the table above is in global memory)
+      int32_t info[4];
+      plan_segment(s, seq_seg0, seq_chunk0, N, p.cu, L, p.init_idx, p.d.n_init, info);
+      const int i = info[0];
       const bool last = (s + 1 == seq_seg0[i + 1]);
       const bool split = (seq_seg0[i + 1] - seq_seg0[i]) > 1;
       need = (split && !last && p.d.mode == 0) ? 1 : 0;
-      units = need ? (si[4 * s + 3] == -1 ? 1 : 2) : 0;
+      units = need ? (info[3] == -1 ? 1 : 2) : 0;
     }
     const int mine = (need << 16) | units;  // a tile holds at most nt segments: no carry between the halves
     s_scan[tid] = mine;
@@ -515,12 +529,19 @@ __global__ void __launch_bounds__(256, 2) kkt_solve_kernel(const __grid_constant
           const float4 q1 = *reinterpret_cast<const float4*>(qk + fz(i, 8 * cj + 4));
           const float qv[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
           const float gi = gam[i];
-          const bool row_f = gi >= kExactCut;
           float pv[8];
+          if (gi >= kExactCut) {
+            const float4 e0 = *reinterpret_cast<const float4*>(egi + 8 * cj);
+            const float4 e1 = *reinterpret_cast<const float4*>(egi + 8 * cj + 4);
+            const float ev[8] = {e0.x, e0.y, e0.z, e0.w, e1.x, e1.y, e1.z, e1.w};
 #pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            const int j = 8 * cj + u;
-            pv[u] = (j <= i && i < n) ? (row_f ? egi[j] * qv[u] : __expf(gi - gam[j]) * p.scale * qv[u]) : 0.f;
+            for (int u = 0; u < 8; ++u) pv[u] = (8 * cj + u <= i && i < n) ? ev[u] * qv[u] : 0.f;
+          } else {
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              const int j = 8 * cj + u;
+              pv[u] = (j <= i && i < n) ? __expf(gi - gam[j]) * p.scale * qv[u] : 0.f;
+            }
           }
           *reinterpret_cast<uint4*>(dp + i * 128 + ((cj ^ (i & 7)) << 4)) =
               make_uint4(pack_bf16x2(pv[0], pv[1]), pack_bf16x2(pv[2], pv[3]), pack_bf16x2(pv[4], pv[5]),
@@ -1437,6 +1458,46 @@ __global__ void __launch_bounds__(kWsThreads, 1) chain_kernel(const __grid_const
   const int Hv = p.d.Hv, G = p.d.Hv / p.d.Hk;
   const int n_items = (kMode == kModeOut ? hd->n_segs : hd->n_p1) * Hv;
   if (blockIdx.x >= n_items || get_status(hd) != 0) return;
+  const int32_t* si = ws_ptr<int32_t>(p, p.L.seg_info);
+  const int32_t* slot = ws_ptr<int32_t>(p, p.L.seg_slot);
+  const int32_t* seq_seg0 = ws_ptr<int32_t>(p, p.L.seq_seg0);
+  const float* gam_ws = ws_ptr<float>(p, p.L.gam);
+  const int32_t* contr = ws_ptr<int32_t>(p, p.L.contr);
+
+  // Pass 1: a unit serves the next segment's start, unless that segment warms up; the transition
+  // also serves the reverse chain's publication of this segment's start gradient (record mode).
+  // All threads call this (the window evaluation is warp-wide).
+  auto p1_skips = [&](int item) -> bool {
+    const int32_t* p1 = ws_ptr<int32_t>(p, p.L.p1_list);
+    const int unit = item / Hv, h = item % Hv;
+    const int s = p1[2 * unit], part = p1[2 * unit + 1];
+    const int seq = si[4 * s], c0 = si[4 * s + 1], nch = si[4 * s + 2];
+    const int32_t* dch = ws_ptr<int32_t>(p, p.L.seq_chunk0);
+    const bool next_warms = warm_back(gam_ws, contr, Hv, h, c0 + nch, dch[seq]) >= 0;
+    const bool rev_needs_m =
+        kRec && part == 0 && s != seq_seg0[seq] && warm_fwd(gam_ws, contr, Hv, h, c0, dch[seq + 1]) < 0;
+    return next_warms && !rev_needs_m;
+  };
+  // Pass 1 claims its tickets before it sets anything up: when every unit it draws is skipped
+  // (each boundary warms up), the CTA leaves without touching tensor memory or barriers.
+  int first_item = -1;
+  if constexpr (kMode == kModeP1) {
+    for (;;) {
+      if (cx.tid == 0) {
+        const int it = (int)atomicAdd(&hd->q_p1, 1u);
+        s_item = (get_status(hd) != 0) ? n_items : it;
+      }
+      __syncthreads();
+      const int item = s_item;
+      if (item >= n_items) return;
+      const bool skip = p1_skips(item);
+      __syncthreads();  // every thread has read s_item before the next ticket
+      if (!skip) {
+        first_item = item;
+        break;
+      }
+    }
+  }
 
   if (cx.tid == 0) {
     mbar_init(&bar_ld, 1);
@@ -1471,12 +1532,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) chain_kernel(const __grid_const
   sync_generic_to_async();
   cx.tmem = tmem_holder;
 
-  const int32_t* si = ws_ptr<int32_t>(p, p.L.seg_info);
-  const int32_t* slot = ws_ptr<int32_t>(p, p.L.seg_slot);
-  const int32_t* seq_seg0 = ws_ptr<int32_t>(p, p.L.seq_seg0);
   int* flags_seg = ws_ptr<int>(p, p.L.flags_seg);
-  const float* gam_ws = ws_ptr<float>(p, p.L.gam);
-  const int32_t* contr = ws_ptr<int32_t>(p, p.L.contr);
   int* flags_fin = ws_ptr<int>(p, p.L.flags_fin);
   int* mzero = ws_ptr<int>(p, p.L.mzero);
   const size_t st_elems = (size_t)kDim * kDim;
@@ -1531,12 +1587,13 @@ __global__ void __launch_bounds__(kWsThreads, 1) chain_kernel(const __grid_const
   };
 
   for (;;) {
-    if (cx.tid == 0) {
+    if (first_item < 0 && cx.tid == 0) {
       const int it = (int)atomicAdd(kMode == kModeOut ? &hd->q_chain : &hd->q_p1, 1u);
       s_item = (get_status(hd) != 0) ? n_items : it;
     }
     __syncthreads();
-    const int item = s_item;
+    const int item = first_item >= 0 ? first_item : s_item;
+    first_item = -1;
     if (item >= n_items) break;
     const int h = item % Hv, hk = h / G;
     bool ok = true;
@@ -1546,17 +1603,9 @@ __global__ void __launch_bounds__(kWsThreads, 1) chain_kernel(const __grid_const
       const int s = p1[2 * unit], part = p1[2 * unit + 1];
       const int seq = si[4 * s], c0 = si[4 * s + 1], nch = si[4 * s + 2];
       const int sl = slot[s];
-      // The unit serves the next segment's start, unless that segment warms up; the transition also
-      // serves the reverse chain's publication of this segment's start gradient (record mode).
-      {
-        const int32_t* dch = ws_ptr<int32_t>(p, p.L.seq_chunk0);
-        const bool next_warms = warm_back(gam_ws, contr, Hv, h, c0 + nch, dch[seq]) >= 0;
-        const bool rev_needs_m =
-            rec && part == 0 && s != seq_seg0[seq] && warm_fwd(gam_ws, contr, Hv, h, c0, dch[seq + 1]) < 0;
-        if (next_warms && !rev_needs_m) {
-          __syncthreads();  // every thread has read s_item before the next ticket
-          continue;
-        }
+      if (p1_skips(item)) {
+        __syncthreads();  // every thread has read s_item before the next ticket
+        continue;
       }
       float* mdst = ws_ptr<float>(p, p.L.mmat) + ((size_t)sl * Hv + h) * st_elems;
       bool m_zero = false;
