@@ -499,6 +499,28 @@ def run_ours(args, rank, world, local_rank):
         return {"rel_l2": float(torch.linalg.vector_norm(a_ - b_)) / n_ if n_ > 0 else 0.0,
                 "max_abs": float((a_ - b_).abs().max())}
     trunc_dev = {"out": deviation(o_trunc, o_exact), "final_state": deviation(f_trunc, f_exact)}
+
+    # Decode: one token for each of DEC_B sequences at the same heads, in place on a pool of states
+    # (one entry per sequence); bound by reading and writing every state once.
+    DEC_B = 256
+    pdec = synth.make_problem("decode_bench", 2024, [1] * DEC_B, Hk, Hv, init_idx=list(range(DEC_B)), n_init=DEC_B)
+    ddec = to_device(pdec, dev)
+    dec_in = [ddec[x] for x in ("q", "k", "v", "g", "beta")]
+    dec_pool, dec_idx = ddec["initial_state"], ddec["init_idx"]
+    dec_out = torch.empty((DEC_B, Hv, D), dtype=torch.bfloat16, device=dev)
+    for _ in range(3):
+        gdn.decode_step(*dec_in, dec_pool, dec_idx, out=dec_out)
+    dec_reps = max(10, min(args.steps, 50))
+    dec_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(dec_reps)]
+    torch.cuda.synchronize()
+    for a_, b_ in dec_ev:
+        flush.zero_()
+        a_.record(stream)
+        gdn.decode_step(*dec_in, dec_pool, dec_idx, out=dec_out)
+        b_.record(stream)
+    torch.cuda.synchronize()
+    dec_ms = float(np.median([a_.elapsed_time(b_) for a_, b_ in dec_ev]))
+    dec_bytes = DEC_B * (Hv * 2 * D * D * 4 + Hk * 2 * D * 2 + Hv * 2 * D * 2 + Hv * 2 * 4 + 4)
     if world > 1:
         torch.distributed.barrier()
 
@@ -579,6 +601,15 @@ def run_ours(args, rank, world, local_rank):
                                 "log-decay is below the threshold), timed like `fwd`; deviation_from_exact compares "
                                 "its o and final state with the exact forward's on the same inputs (the tests bound "
                                 "both modes against the fp64 oracle)")
+    dec_ach = dec_bytes / (dec_ms * 1e-3) / 1e9
+    res["decode"] = {"ms": dec_ms, "value": DEC_B / (dec_ms * 1e-3) / 1e6, "unit": "Msequence-steps/s",
+                     "batch": DEC_B, "H_v": Hv, "H_k": Hk,
+                     "roofline": {"bound": "hbm", "achieved": dec_ach, "peak": peaks["hbm"], "unit": "GB/s",
+                                  "frac": dec_ach / peaks["hbm"], "algorithmic_bytes": dec_bytes,
+                                  "peak_source": peaks["src"] + " hbm_gbs"},
+                     "note": f"gdn_decode_step: one token for each of {DEC_B} sequences, in place on a pool of "
+                             f"{DEC_B} states (each read and written once), median of {dec_reps} steps with one "
+                             f"event pair around each and L2 flushed before it"}
     if not has_bwd:
         res["vs_baseline_note"] = "value / FlashQLA forward on H200 (0.31 ms for 32K at TP8), context only"
     if world == 1 and not args.no_cpu_baseline:

@@ -200,6 +200,26 @@ size_t gdn_noalloc_scratch_bytes(void);
  * run on that device. */
 int gdn_noalloc_status(int device, gdn_stream_t stream);
 
+/*
+ * Decode: advance B sequences by one token each, in place on a pool of states ("How to Speed Up
+ * GDN Kernels for Qwen Models", FAQ "Does this help decode too?"; the recurrence of section "What
+ * GDN actually computes"). For sequence b and value head h (key head h / (H_v / H_k)), with
+ * S = state_pool[state_idx[b], h]:
+ *     S' = exp(g) S,  p = S'^T k,  d = beta (v - p),  S = S' + k d^T  (stored back),  out = scale S^T q.
+ * This equals gdn_chunk_fwd on B one-token documents whose initial states are those pool entries.
+ *   q, k  : bf16 [B, H_k, 128];  v, out : bf16 [B, H_v, 128];  g, beta : fp32 [B, H_v]
+ *   state_idx  : int32 [B], pairwise distinct entries of [0, n_pool) (two sequences on one entry race)
+ *   state_pool : fp32 [n_pool, H_v, 128, 128], read and overwritten in place (16-byte aligned)
+ *   status     : device int32 or NULL; a sequence whose index is out of range is skipped (its out row
+ *                is zero, its pool entry untouched) and GDN_ERR_INVALID_ARG is written here (never
+ *                cleared: the caller zeroes it)
+ * opt may be NULL; only opt->scale is used. Same device rules as gdn_chunk_fwd (the pool's GPU);
+ * nothing is allocated, everything runs on `stream`. B = 0 is a no-op.
+ */
+int gdn_decode_step(const void* q, const void* k, const void* v, const float* g, const float* beta, int B, int H_k,
+                    int H_v, int head_dim, const int32_t* state_idx, float* state_pool, int n_pool, void* out,
+                    int32_t* status, const gdn_options* opt, gdn_stream_t stream);
+
 /* Copy the workspace's device status word to the host (synchronises `stream`) and return it:
  * GDN_OK or the first device-side error of the last call that used this workspace. */
 int gdn_workspace_status(const void* workspace, gdn_stream_t stream);

@@ -28,7 +28,8 @@ CHUNK = 64
 # Every symbol include/gdn.h declares.
 EXPORTS = ("gdn_default_options", "gdn_fwd_workspace_size", "gdn_bwd_workspace_size", "gdn_chunk_fwd",
            "gdn_chunk_bwd", "gdn_workspace_status", "gdn_status_string", "gdn_plan_host", "gdn_chunk_fwd_noalloc",
-           "gdn_noalloc_scratch_bytes", "gdn_noalloc_status", "gdn_fwd_check_args", "gdn_bwd_check_args")
+           "gdn_noalloc_scratch_bytes", "gdn_noalloc_status", "gdn_fwd_check_args", "gdn_bwd_check_args",
+           "gdn_decode_step")
 
 
 class GdnError(RuntimeError):
@@ -128,6 +129,8 @@ def load(path: Optional[str] = None):
         lib.gdn_fwd_check_args.restype = I
         lib.gdn_bwd_check_args.argtypes = [P, P, P, P, P, P, I, I, I, I, I, P, P, I, P, P, P, P, P, P, P, P, P, Z, OP]
         lib.gdn_bwd_check_args.restype = I
+        lib.gdn_decode_step.argtypes = [P, P, P, P, P, I, I, I, I, P, P, I, P, P, OP, P]
+        lib.gdn_decode_step.restype = I
         if path is None:
             _lib = lib
         return lib
@@ -289,6 +292,38 @@ def chunk_bwd(q, k, v, g, beta, cu_seqlens, dout, dfinal_state=None, init_idx=No
     if rc != GDN_OK:
         raise GdnError(rc, "gdn_chunk_bwd")
     return dict(dq=dq, dk=dk, dv=dv, dg=dg, dbeta=db, dinit=dinit)
+
+
+def decode_step(q, k, v, g, beta, state_pool, state_idx, options: Optional[Options] = None, out=None, status=None,
+                stream=None):
+    """One decode token per sequence, in place on the state pool. Shapes: q, k [B, Hk, 128] bf16;
+    v [B, Hv, 128] bf16; g, beta [B, Hv] fp32; state_pool [n_pool, Hv, 128, 128] fp32 (updated);
+    state_idx [B] int32 (distinct entries of the pool). Returns out [B, Hv, 128] bf16. `status`: an
+    optional int32 device tensor of one element that receives GDN_ERR_INVALID_ARG for out-of-range
+    indices (not cleared here)."""
+    torch = _torch()
+    B, Hk, D = q.shape
+    Hv = v.shape[1]
+    _check(q, "q", torch.bfloat16, (B, Hk, D))
+    _check(k, "k", torch.bfloat16, (B, Hk, D))
+    _check(v, "v", torch.bfloat16, (B, Hv, D))
+    _check(g, "g", torch.float32, (B, Hv))
+    _check(beta, "beta", torch.float32, (B, Hv))
+    _check(state_idx, "state_idx", torch.int32, (B,))
+    _check(state_pool, "state_pool", torch.float32)
+    if state_pool.dim() != 4 or tuple(state_pool.shape[1:]) != (Hv, D, D):
+        raise ValueError("state_pool: expected [n_pool, Hv, 128, 128]")
+    if status is not None:
+        _check(status, "status", torch.int32, (1,))
+    if out is None:
+        out = torch.empty((B, Hv, D), dtype=torch.bfloat16, device=q.device)
+    o = _opts(options)
+    rc = load().gdn_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), B, Hk, Hv, D, _ptr(state_idx),
+                                _ptr(state_pool), state_pool.shape[0], _ptr(out), _ptr(status), ctypes.byref(o),
+                                _stream_handle(stream))
+    if rc != GDN_OK:
+        raise GdnError(rc, "gdn_decode_step")
+    return out
 
 
 def workspace_status(workspace, stream=None) -> int:
