@@ -82,6 +82,13 @@ enum gdn_flags {
                                       their waits run out (after gdn_options.flag_wait_us) and the call
                                       reports GDN_ERR_TIMEOUT through the status word; outputs are then
                                       unspecified. Rejected by the backward (GDN_ERR_INVALID_ARG). */
+  GDN_FLAG_L2NORM_QK = 8,    /* q and k come unnormalised: each (token, key head) row is first scaled to unit
+                                L2 norm, y = x / sqrt(x . x + 1e-6) ("Musings on long-context fine-tuning",
+                                "Triton autotuning in the first backward pass": the normalisation the model
+                                applies right before the op), then opt->scale multiplies the normalised q.
+                                The backward's dq and dk are the gradients with respect to the unnormalised
+                                inputs. The workspace also holds the normalised copies (the size queries
+                                count them); forward and backward of a training step must both set it. */
   GDN_FLAG_REUSE_FWD = 2     /* backward: the workspace holds the records of a forward run with
                                 GDN_FLAG_SAVE_FOR_BWD on the same inputs, options and stream order, and
                                 nothing has written it since; the backward then skips its recompute
@@ -112,7 +119,8 @@ typedef struct gdn_options {
 
 /* Stages of a call (indices into gdn_options.stage_events). A backward call runs stages 0-3
  * (the forward recompute; stage 0 alone with GDN_FLAG_REUSE_FWD), then 4, 5, 7 and 6 in that order.
- * A forward with GDN_FLAG_SAVE_FOR_BWD runs stages 0-3 and 8. */
+ * A forward with GDN_FLAG_SAVE_FOR_BWD runs stages 0-3 and 8. With GDN_FLAG_L2NORM_QK stage 9 runs
+ * first in both directions and the backward ends with stage 10. */
 enum gdn_fwd_stage {
   GDN_STAGE_PLAN = 0,      /* chunk / segment maps */
   GDN_STAGE_KKT_SOLVE = 1, /* intra-chunk K K^T, triangular solve, WY factors */
@@ -123,7 +131,9 @@ enum gdn_fwd_stage {
   GDN_STAGE_DINIT = 6,     /* backward: d(initial_state) sums over documents sharing a pool entry */
   GDN_STAGE_DQ = 7,        /* backward: per-chunk dq; adds the q S dO term of dg */
   GDN_STAGE_OUT = 8,       /* forward with GDN_FLAG_SAVE_FOR_BWD: o from the records */
-  GDN_NUM_STAGES = 9
+  GDN_STAGE_L2NORM = 9,    /* GDN_FLAG_L2NORM_QK: the normalised copies of q and k (both directions) */
+  GDN_STAGE_L2NORM_BWD = 10, /* GDN_FLAG_L2NORM_QK, backward: dq, dk back to the unnormalised inputs */
+  GDN_NUM_STAGES = 11
 };
 
 /* Fill `opt` with the defaults: exact mode, threshold -10, automatic segments, scale 1, no flags,
@@ -213,7 +223,8 @@ int gdn_noalloc_status(int device, gdn_stream_t stream);
  *   status     : device int32 or NULL; a sequence whose index is out of range is skipped (its out row
  *                is zero, its pool entry untouched) and GDN_ERR_INVALID_ARG is written here (never
  *                cleared: the caller zeroes it)
- * opt may be NULL; only opt->scale is used. Same device rules as gdn_chunk_fwd (the pool's GPU);
+ * opt may be NULL; opt->scale and the GDN_FLAG_L2NORM_QK bit of opt->flags are used (q and k then
+ * come unnormalised and are scaled to unit norm in fp32 first). Same device rules as gdn_chunk_fwd (the pool's GPU);
  * nothing is allocated, everything runs on `stream`. B = 0 is a no-op.
  */
 int gdn_decode_step(const void* q, const void* k, const void* v, const float* g, const float* beta, int B, int H_k,

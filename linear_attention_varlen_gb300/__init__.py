@@ -44,12 +44,13 @@ class COptions(ctypes.Structure):
                 ("stage_events", ctypes.c_void_p), ("flag_wait_us", ctypes.c_int32)]
 
 
-NUM_STAGES = 9
+NUM_STAGES = 11
 (STAGE_PLAN, STAGE_KKT_SOLVE, STAGE_SPLIT, STAGE_CHAIN, STAGE_REV_CHAIN, STAGE_GRADS, STAGE_DINIT, STAGE_DQ,
- STAGE_OUT) = range(9)
+ STAGE_OUT, STAGE_L2NORM, STAGE_L2NORM_BWD) = range(11)
 FLAG_SAVE_FOR_BWD = 1  # forward of a training step: keep the records for the backward
 FLAG_REUSE_FWD = 2     # backward: use the records of a FLAG_SAVE_FOR_BWD forward instead of recomputing
 FLAG_TEST_WITHHOLD_FORK = 4  # forward, tests of the bounded waits only: forked documents never get their start
+FLAG_L2NORM_QK = 8     # q and k come unnormalised: the library scales each row to unit L2 norm (both directions)
 
 
 @dataclass
@@ -63,6 +64,7 @@ class Options:
     stage_events: Optional[object] = None  # optional list of 2 * NUM_STAGES timing torch.cuda.Event (or None)
     save_for_backward: bool = False
     reuse_forward: bool = False
+    l2norm_qk: bool = False          # q and k unnormalised: normalise each row first (forward and backward)
     flag_wait_us: int = 0            # limit of a wait for another item's published state (0 = about 2 s)
     test_withhold_fork: bool = False  # tests only: make the waits of forked documents run out
 
@@ -78,7 +80,8 @@ class Options:
             self._ev_array = (ctypes.c_void_p * len(handles))(*handles)
             ev = ctypes.cast(self._ev_array, ctypes.c_void_p)
         flags = ((FLAG_SAVE_FOR_BWD if self.save_for_backward else 0) | (FLAG_REUSE_FWD if self.reuse_forward else 0)
-                 | (FLAG_TEST_WITHHOLD_FORK if self.test_withhold_fork else 0))
+                 | (FLAG_TEST_WITHHOLD_FORK if self.test_withhold_fork else 0)
+                 | (FLAG_L2NORM_QK if self.l2norm_qk else 0))
         return COptions(m, float(self.trunc_log_threshold), int(self.segment_chunks), float(self.scale), flags, ev,
                         int(self.flag_wait_us))
 

@@ -13,6 +13,7 @@
 #include "gdn_dev.cuh"
 #include "gdn_fwd.h"
 #include "gdn_host.h"
+#include "gdn_l2norm.h"
 #include "tmap.h"
 
 using namespace gdn;
@@ -89,7 +90,8 @@ gdn_options resolve(const gdn_options* opt) {
 
 bool valid_options(const gdn_options& o) {
   return (o.mode == GDN_MODE_EXACT || o.mode == GDN_MODE_TRUNCATE) &&
-         (o.flags & ~(GDN_FLAG_SAVE_FOR_BWD | GDN_FLAG_REUSE_FWD | GDN_FLAG_TEST_WITHHOLD_FORK)) == 0 &&
+         (o.flags & ~(GDN_FLAG_SAVE_FOR_BWD | GDN_FLAG_REUSE_FWD | GDN_FLAG_TEST_WITHHOLD_FORK | GDN_FLAG_L2NORM_QK)) ==
+             0 &&
          o.scale == o.scale && o.flag_wait_us >= 0;
 }
 
@@ -157,7 +159,8 @@ size_t gdn_fwd_workspace_size(int N, int T, int H_k, int H_v, const gdn_options*
   const gdn_options o = resolve(opt);
   if (!valid_options(o)) return 0;
   if (o.flags & GDN_FLAG_SAVE_FOR_BWD) return gdn_bwd_workspace_size(N, T, H_k, H_v, opt);
-  return fwd_layout(make_dims(N, T, H_k, H_v, 0, o, current_sm_count())).total;
+  return fwd_layout(make_dims(N, T, H_k, H_v, 0, o, current_sm_count())).total +
+         ((o.flags & GDN_FLAG_L2NORM_QK) ? l2norm_bytes(T, H_k) : 0);
 }
 
 size_t gdn_bwd_workspace_size(int N, int T, int H_k, int H_v, const gdn_options* opt) {
@@ -165,7 +168,8 @@ size_t gdn_bwd_workspace_size(int N, int T, int H_k, int H_v, const gdn_options*
   gdn_options o = resolve(opt);
   if (!valid_options(o)) return 0;
   o.mode = GDN_MODE_EXACT;  // the backward is always exact
-  return bwd_layout(make_dims(N, T, H_k, H_v, 0, o, current_sm_count())).total;
+  return bwd_layout(make_dims(N, T, H_k, H_v, 0, o, current_sm_count())).total +
+         ((o.flags & GDN_FLAG_L2NORM_QK) ? l2norm_bytes(T, H_k) : 0);
 }
 
 int gdn_workspace_status(const void* workspace, gdn_stream_t stream) {
@@ -212,7 +216,8 @@ int prepare_fwd(const void* q, const void* k, const void* v, const float* g, con
   const int arch = check_arch();
   if (arch != kOk) return arch;
   const PlanDims d = make_dims(N, T, H_k, H_v, n_init, *o, current_sm_count());
-  const size_t need = (o->flags & GDN_FLAG_SAVE_FOR_BWD) ? bwd_layout(d).total : fwd_layout(d).total;
+  const size_t need = ((o->flags & GDN_FLAG_SAVE_FOR_BWD) ? bwd_layout(d).total : fwd_layout(d).total) +
+                      ((o->flags & GDN_FLAG_L2NORM_QK) ? l2norm_bytes(T, H_k) : 0);
   if (ws_bytes < need) return GDN_ERR_WORKSPACE;
   return GDN_OK;
 }
@@ -245,7 +250,8 @@ int prepare_bwd(const void* q, const void* k, const void* v, const float* g, con
   if (arch != kOk) return arch;
   gdn_options oe = *o;
   oe.mode = GDN_MODE_EXACT;
-  if (ws_bytes < bwd_layout(make_dims(N, T, H_k, H_v, n_init, oe, current_sm_count())).total)
+  if (ws_bytes < bwd_layout(make_dims(N, T, H_k, H_v, n_init, oe, current_sm_count())).total +
+                     ((o->flags & GDN_FLAG_L2NORM_QK) ? l2norm_bytes(T, H_k) : 0))
     return GDN_ERR_WORKSPACE;
   return GDN_OK;
 }
@@ -285,6 +291,22 @@ int gdn_chunk_fwd(const void* q, const void* k, const void* v, const float* g, c
                              out, final_state, workspace, ws_bytes, opt, &o, guard);
   if (rc != GDN_OK) return rc;
   const int sms = current_sm_count();
+  cudaEvent_t* ev = reinterpret_cast<cudaEvent_t*>(o.stage_events);
+  if (o.flags & GDN_FLAG_L2NORM_QK) {
+    // normalised copies of q and k after the layout; every later kernel reads them instead
+    const PlanDims d0 = make_dims(N, T, H_k, H_v, n_init, o, sms);
+    uint8_t* qn = reinterpret_cast<uint8_t*>(workspace) +
+                  ((o.flags & GDN_FLAG_SAVE_FOR_BWD) ? bwd_layout(d0).total : fwd_layout(d0).total);
+    uint8_t* kn = qn + (size_t)T * H_k * kDim * 2;
+    if (ev && ev[18]) cudaEventRecord(ev[18], (cudaStream_t)stream);
+    if (launch_l2norm_fwd(q, k, qn, kn, (int64_t)T * H_k, (cudaStream_t)stream) != kOk) return GDN_ERR_CUDA;
+    if (ev && ev[19]) cudaEventRecord(ev[19], (cudaStream_t)stream);
+    q = qn;
+    k = kn;
+  } else if (ev) {
+    for (int i = 18; i < 20; ++i)
+      if (ev[i]) cudaEventRecord(ev[i], (cudaStream_t)stream);
+  }
   if (o.flags & GDN_FLAG_SAVE_FOR_BWD) {
     BwdArgs a;
     std::memset(&a, 0, sizeof(a));
@@ -347,6 +369,24 @@ int gdn_chunk_bwd(const void* q, const void* k, const void* v, const float* g, c
                              dout, dfinal_state, dq, dk, dv, dg, dbeta, dinitial_state, workspace, ws_bytes, opt, &o,
                              guard);
   if (rc != GDN_OK) return rc;
+  cudaEvent_t* ev = reinterpret_cast<cudaEvent_t*>(o.stage_events);
+  gdn_options oe = o;
+  oe.mode = GDN_MODE_EXACT;  // the backward recomputes and differentiates the exact forward
+  const PlanDims dims = make_dims(N, T, H_k, H_v, n_init, oe, current_sm_count());
+  const void* q_raw = q;
+  const void* k_raw = k;
+  if (o.flags & GDN_FLAG_L2NORM_QK) {
+    uint8_t* qn = reinterpret_cast<uint8_t*>(workspace) + bwd_layout(dims).total;
+    uint8_t* kn = qn + (size_t)T * H_k * kDim * 2;
+    if (ev && ev[18]) cudaEventRecord(ev[18], (cudaStream_t)stream);
+    if (launch_l2norm_fwd(q, k, qn, kn, (int64_t)T * H_k, (cudaStream_t)stream) != kOk) return GDN_ERR_CUDA;
+    if (ev && ev[19]) cudaEventRecord(ev[19], (cudaStream_t)stream);
+    q = qn;
+    k = kn;
+  } else if (ev) {
+    for (int i = 18; i < 20; ++i)
+      if (ev[i]) cudaEventRecord(ev[i], (cudaStream_t)stream);
+  }
   BwdArgs a;
   a.q = q;
   a.k = k;
@@ -366,15 +406,24 @@ int gdn_chunk_bwd(const void* q, const void* k, const void* v, const float* g, c
   a.dinit = dinitial_state;
   a.ws = workspace;
   a.ws_bytes = ws_bytes;
-  gdn_options oe = o;
-  oe.mode = GDN_MODE_EXACT;  // the backward recomputes and differentiates the exact forward
-  a.d = make_dims(N, T, H_k, H_v, n_init, oe, current_sm_count());
+  a.d = dims;
   a.trunc_thr = o.trunc_log_threshold;
   a.scale = o.scale;
   a.flag_budget = flag_budget(o);
   a.withhold_fin = 0;
-  return launch_bwd(a, (o.flags & GDN_FLAG_REUSE_FWD) != 0, (cudaStream_t)stream,
-                    reinterpret_cast<cudaEvent_t*>(o.stage_events));
+  const int rb = launch_bwd(a, (o.flags & GDN_FLAG_REUSE_FWD) != 0, (cudaStream_t)stream, ev);
+  if (rb != GDN_OK) return rb;
+  if (!(o.flags & GDN_FLAG_L2NORM_QK)) {
+    if (ev)
+      for (int i = 20; i < 22; ++i)
+        if (ev[i]) cudaEventRecord(ev[i], (cudaStream_t)stream);
+    return GDN_OK;
+  }
+  // gradients with respect to the unnormalised q and k
+  if (ev && ev[20]) cudaEventRecord(ev[20], (cudaStream_t)stream);
+  if (launch_l2norm_bwd(q_raw, k_raw, dq, dk, (int64_t)T * H_k, (cudaStream_t)stream) != kOk) return GDN_ERR_CUDA;
+  if (ev && ev[21]) cudaEventRecord(ev[21], (cudaStream_t)stream);
+  return GDN_OK;
 }
 
 int gdn_plan_host(const int32_t* cu, int N, int T, int H_v, const int32_t* init_idx, int n_init,

@@ -30,6 +30,12 @@ constexpr int kChunk = 64;        // tokens per chunk
 constexpr int kDim = 128;         // d_k = d_v
 constexpr int kMinSegChunks = 4;  // shortest automatic segment (chunks)
 
+// q and k normalisation (GDN_FLAG_L2NORM_QK): y = x (x . x + kL2NormEps)^{-1/2} per row of 128.
+constexpr float kL2NormEps = 1e-6f;
+// Workspace bytes of the normalised copies of q and k (bf16, [T][Hk][128] each), placed after the
+// forward's or the backward's layout.
+inline size_t l2norm_bytes(int T, int Hk) { return ((size_t)2 * T * Hk * kDim * 2 + 255) / 256 * 256; }
+
 // Status codes (mirror include/gdn.h).
 constexpr int kOk = 0, kErrInvalid = -1, kErrUnsupported = -2, kErrCuda = -3, kErrTimeout = -4,
               kErrWorkspace = -5;

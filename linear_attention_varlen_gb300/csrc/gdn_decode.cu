@@ -5,7 +5,8 @@
 // query reads the updated state ("How to Speed Up GDN Kernels for Qwen Models", FAQ "Does this help
 // decode too?": decode is a separate kernel; section "What GDN actually computes": the state is a
 // fixed 128 x 128 matrix per head, with no cache that grows). For sequence b, value head h (key
-// head hk = h / (H_v / H_k)) and S = pool[state_idx[b], h]:
+// head hk = h / (H_v / H_k)) and S = pool[state_idx[b], h] (q and k first scaled to unit norm with
+// GDN_FLAG_L2NORM_QK, in fp32):
 //     S' = e^{g} S,  p = S'^T k,  d = beta (v - p),  S = S' + k d^T,  o = scale * S^T q.
 // It is the chunked forward's recurrence for a document of one token that starts from a pool entry
 // and whose final state replaces that entry.
@@ -35,7 +36,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const __nv_bfloat16
                                                              const float* __restrict__ g,
                                                              const float* __restrict__ beta,
                                                              const int32_t* __restrict__ state_idx, float* pool,
-                                                             int n_pool, int Hk, int Hv, float scale,
+                                                             int n_pool, int Hk, int Hv, float scale, int l2norm,
                                                              __nv_bfloat16* __restrict__ out, int32_t* status) {
   const int b = blockIdx.x / Hv, h = blockIdx.x % Hv, hk = h / (Hv / Hk);
   const int t = threadIdx.x, cg = t & 31, rg = t >> 5;  // columns 4 cg .. +3, rows 16 rg .. +15
@@ -49,7 +50,24 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const __nv_bfloat16
   }
   if (t < kDim) {
     s_k[t] = __bfloat162float(k[((size_t)b * Hk + hk) * kDim + t]);
-    s_q[t] = __bfloat162float(q[((size_t)b * Hk + hk) * kDim + t]) * scale;
+    s_q[t] = __bfloat162float(q[((size_t)b * Hk + hk) * kDim + t]);
+  }
+  __syncthreads();
+  if (t < 64) {
+    // warps 0-1: |q|^2 and |k|^2 (GDN_FLAG_L2NORM_QK) in s_red row 0; the scale
+    const float* xv = (t < 32) ? s_q : s_k;
+    const int l = t & 31;
+    float ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) ss += xv[l + 32 * i] * xv[l + 32 * i];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if (l == 0) s_red[0][t >> 5] = l2norm ? rsqrtf(ss + kL2NormEps) : 1.f;
+  }
+  __syncthreads();
+  if (t < kDim) {
+    s_q[t] *= s_red[0][0] * scale;
+    s_k[t] *= s_red[0][1];
   }
   const float a = __expf(g[(size_t)b * Hv + h]), bt = beta[(size_t)b * Hv + h];
   float* S = pool + ((size_t)x * Hv + h) * kDim * kDim;
@@ -139,6 +157,6 @@ extern "C" int gdn_decode_step(const void* q, const void* k, const void* v, cons
   gdn::decode_kernel<<<(unsigned)(B * H_v), gdn::kDecThreads, 0, (cudaStream_t)stream>>>(
       reinterpret_cast<const __nv_bfloat16*>(q), reinterpret_cast<const __nv_bfloat16*>(k),
       reinterpret_cast<const __nv_bfloat16*>(v), g, beta, state_idx, state_pool, n_pool, H_k, H_v, o.scale,
-      reinterpret_cast<__nv_bfloat16*>(out), status);
+      (o.flags & GDN_FLAG_L2NORM_QK) ? 1 : 0, reinterpret_cast<__nv_bfloat16*>(out), status);
   return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }

@@ -135,3 +135,28 @@ def bwd_problem(p, threads: Optional[int] = None):
     f = p.as_f64()
     return bwd(f["q"], f["k"], f["v"], f["g"], f["beta"], p.cu_seqlens, f["dout"], f.get("dfinal"), p.init_idx,
                f.get("initial_state"), threads=threads)
+
+
+# ----------------------------------------------------------------------------- q / k normalisation
+
+L2NORM_EPS = 1e-6
+
+
+def l2norm_rows(x, eps: float = L2NORM_EPS):
+    """y = x / sqrt(x . x + eps) over the last axis, in fp64: the unit-norm scaling of each (token,
+    head) row of q and k that the model applies right before the recurrence ("Musings on long-context
+    fine-tuning", section "Triton autotuning in the first backward pass"; the workloads' recipe
+    normalises q and k per token and head). eps guards a zero row."""
+    x = np.asarray(x, dtype=np.float64)
+    return x / np.sqrt(np.sum(x * x, axis=-1, keepdims=True) + eps)
+
+
+def l2norm_rows_bwd(x, dy, eps: float = L2NORM_EPS):
+    """Gradient with respect to x of sum(dy * l2norm_rows(x)), in fp64. With r = (x . x + eps)^{-1/2}
+    and y = r x, the derivative of y is r I - r^3 x x^T, so dx = r dy - r^3 (x . dy) x = r (dy - (y . dy) y)."""
+    x = np.asarray(x, dtype=np.float64)
+    dy = np.asarray(dy, dtype=np.float64)
+    r = 1.0 / np.sqrt(np.sum(x * x, axis=-1, keepdims=True) + eps)
+    y = r * x
+    return r * (dy - np.sum(y * dy, axis=-1, keepdims=True) * y)
+

@@ -4,6 +4,8 @@ checks that at least one pin in test_oracle_pins fails against it."""
 import os
 import subprocess
 
+import numpy as np
+
 import pytest
 
 import oracle
@@ -61,3 +63,23 @@ def test_pins_catch_mutant(name, orig, mut, which, tmp_path, monkeypatch):
     if which is CKPT_PINS:
         # only the pin that crosses a checkpoint sees these: the short-document pin passes
         pins.test_backward_matches_finite_differences()
+
+
+# The normalisation of q and k is plain numpy in oracle/__init__.py: its mutants are substituted
+# functions, and the finite-difference pin must reject each of them.
+L2_MUTANTS = [
+    ("projection term dropped", lambda x, dy, eps=1e-6: dy / np.sqrt(np.sum(x * x, -1, keepdims=True) + eps)),
+    ("r to the first power in the projection",
+     lambda x, dy, eps=1e-6: (lambda r: r * dy - r * np.sum(x * dy, -1, keepdims=True) * x)(
+         1.0 / np.sqrt(np.sum(x * x, -1, keepdims=True) + eps))),
+    ("projection sign", lambda x, dy, eps=1e-6: (lambda r, y: r * (dy + np.sum(y * dy, -1, keepdims=True) * y))(
+        1.0 / np.sqrt(np.sum(x * x, -1, keepdims=True) + eps),
+        x / np.sqrt(np.sum(x * x, -1, keepdims=True) + eps))),
+]
+
+
+@pytest.mark.parametrize("name,fn", L2_MUTANTS, ids=[m[0] for m in L2_MUTANTS])
+def test_l2norm_pin_catches_mutant(name, fn, monkeypatch):
+    monkeypatch.setattr(oracle, "l2norm_rows_bwd", fn)
+    with pytest.raises(AssertionError):
+        pins.test_l2norm_rows_bwd_matches_finite_differences()

@@ -342,3 +342,78 @@ def test_backward_fork_equals_two_calls():
     for key in ("dq", "dk", "dv", "dg", "dbeta"):
         np.testing.assert_allclose(full[key][sa], pre[key], rtol=1e-12, atol=1e-13)
         np.testing.assert_allclose(full[key][sb], br[key], rtol=1e-12, atol=1e-13)
+
+
+# ----------------------------------------------------------------------------- q / k normalisation
+
+
+def test_l2norm_rows_closed_forms():
+    """Rows come out with norm sqrt(s / (s + eps)) (1 up to eps), parallel to the input; a row that is
+    already a unit vector times c > 0 maps to (almost) the unit vector; a zero row stays zero."""
+    r = rng(81)
+    x = r.standard_normal((7, 3, 16)) * r.uniform(0.1, 5.0, (7, 3, 1))
+    y = oracle.l2norm_rows(x)
+    s_ = np.sum(x * x, axis=-1)
+    np.testing.assert_allclose(np.linalg.norm(y, axis=-1), np.sqrt(s_ / (s_ + oracle.L2NORM_EPS)), rtol=1e-14)
+    cos = np.sum(x * y, axis=-1) / (np.linalg.norm(x, axis=-1) * np.linalg.norm(y, axis=-1))
+    np.testing.assert_allclose(cos, 1.0, rtol=1e-14)
+    u = np.zeros((1, 1, 4))
+    u[0, 0, 2] = 3.0
+    np.testing.assert_allclose(oracle.l2norm_rows(u)[0, 0], [0, 0, 3.0 / np.sqrt(9.0 + 1e-6), 0], rtol=1e-15)
+    assert not np.any(oracle.l2norm_rows(np.zeros((2, 5))))
+
+
+def test_l2norm_rows_bwd_matches_finite_differences():
+    r = rng(82)
+    x = r.standard_normal((3, 2, 6)) * r.uniform(0.2, 3.0, (3, 2, 1))
+    dy = r.standard_normal(x.shape)
+    dx = oracle.l2norm_rows_bwd(x, dy)
+    eps = 1e-6
+    num = np.zeros_like(x)
+    for idx in np.ndindex(x.shape):
+        old = x[idx]
+        x[idx] = old + eps
+        lp = np.sum(dy * oracle.l2norm_rows(x))
+        x[idx] = old - eps
+        lm = np.sum(dy * oracle.l2norm_rows(x))
+        x[idx] = old
+        num[idx] = (lp - lm) / (2 * eps)
+    np.testing.assert_allclose(dx, num, rtol=0, atol=1e-8)
+    # the gradient is orthogonal to the row (scaling a row leaves the output unchanged, up to eps)
+    np.testing.assert_allclose(np.sum(dx * x, axis=-1), 0.0, atol=1e-6 * np.abs(dx).max())
+
+
+def test_normalised_recurrence_gradient_chain_rule():
+    """Through the recurrence: the gradient with respect to raw q and k, formed as l2norm_rows_bwd of
+    the oracle's gradient at the normalised inputs, matches central differences of the composed
+    forward."""
+    Hk, Hv, Dk, Dv = 1, 2, 4, 3
+    lens = [5, 3]
+    p = rand_problem(83, lens, Hk, Hv, Dk, Dv)
+    r = rng(84)
+    q_raw = p["q"] * r.uniform(0.5, 2.0, (sum(lens), Hk, 1))
+    k_raw = p["k"] * r.uniform(0.5, 2.0, (sum(lens), Hk, 1))
+    dout = r.standard_normal((sum(lens), Hv, Dv))
+
+    def loss(qr, kr):
+        out, _ = oracle.fwd(oracle.l2norm_rows(qr), oracle.l2norm_rows(kr), p["v"], p["g"], p["beta"],
+                            p["cu_seqlens"])
+        return float(np.sum(out * dout))
+
+    gr = oracle.bwd(oracle.l2norm_rows(q_raw), oracle.l2norm_rows(k_raw), p["v"], p["g"], p["beta"],
+                    p["cu_seqlens"], dout)
+    dq = oracle.l2norm_rows_bwd(q_raw, gr["dq"])
+    dk = oracle.l2norm_rows_bwd(k_raw, gr["dk"])
+    eps = 1e-6
+    for x, ana in ((q_raw, dq), (k_raw, dk)):
+        num = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            old = x[idx]
+            x[idx] = old + eps
+            lp = loss(q_raw, k_raw)
+            x[idx] = old - eps
+            lm = loss(q_raw, k_raw)
+            x[idx] = old
+            num[idx] = (lp - lm) / (2 * eps)
+        assert np.abs(ana - num).max() / max(1.0, np.abs(num).max()) < 1e-6
+
