@@ -500,6 +500,33 @@ def run_ours(args, rank, world, local_rank):
                 "max_abs": float((a_ - b_).abs().max())}
     trunc_dev = {"out": deviation(o_trunc, o_exact), "final_state": deviation(f_trunc, f_exact)}
 
+    # q / k normalisation (GDN_FLAG_L2NORM_QK) on the inference forward: the whole call, and the
+    # normalisation pass alone (its stage events), both with L2 flushed before each call
+    l2_reps = max(10, min(args.steps, 50))
+    l2_ws = torch.empty(gdn.fwd_workspace_size(N, T, Hk, Hv, gdn.Options(l2norm_qk=True)), dtype=torch.uint8,
+                        device=dev)
+    l2_stage = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(l2_reps)]
+    l2_call = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(l2_reps)]
+    for e_ in [e for pr in l2_stage for e in pr]:
+        e_.record(stream)
+    for _ in range(3):
+        gdn.chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"], options=gdn.Options(l2norm_qk=True),
+                      out=out, final_state=fin, workspace=l2_ws)
+    torch.cuda.synchronize()
+    for (a_, b_), (sa, sb) in zip(l2_call, l2_stage):
+        sev = [None] * (2 * gdn.NUM_STAGES)
+        sev[2 * gdn.STAGE_L2NORM], sev[2 * gdn.STAGE_L2NORM + 1] = sa, sb
+        flush.zero_()
+        a_.record(stream)
+        gdn.chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"],
+                      options=gdn.Options(l2norm_qk=True, stage_events=sev), out=out, final_state=fin, workspace=l2_ws)
+        b_.record(stream)
+    torch.cuda.synchronize()
+    l2_fwd_ms = float(np.median([a_.elapsed_time(b_) for a_, b_ in l2_call]))
+    l2_pass_ms = float(np.median([a_.elapsed_time(b_) for a_, b_ in l2_stage]))
+    l2_bytes = 2 * (2 * T * Hk * D * 2)  # q and k read once, their normalised copies written once
+    del l2_ws
+
     # Decode: one token for each of DEC_B sequences at the same heads, in place on a pool of states
     # (one entry per sequence); bound by reading and writing every state once.
     DEC_B = 256
@@ -601,6 +628,16 @@ def run_ours(args, rank, world, local_rank):
                                 "log-decay is below the threshold), timed like `fwd`; deviation_from_exact compares "
                                 "its o and final state with the exact forward's on the same inputs (the tests bound "
                                 "both modes against the fp64 oracle)")
+    l2_ach = l2_bytes / (l2_pass_ms * 1e-3) / 1e9
+    res["l2norm"] = {"fwd_ms": l2_fwd_ms, "fwd_value": T / (l2_fwd_ms * 1e-3) / 1e6, "unit": UNIT,
+                     "pass_ms": l2_pass_ms,
+                     "roofline": {"bound": "hbm", "achieved": l2_ach, "peak": peaks["hbm"], "unit": "GB/s",
+                                  "frac": l2_ach / peaks["hbm"], "algorithmic_bytes": l2_bytes,
+                                  "peak_source": peaks["src"] + " hbm_gbs"},
+                     "note": "inference forward with GDN_FLAG_L2NORM_QK (q, k unnormalised): the whole call, and "
+                             "the normalisation pass alone between its stage events (a recorded event costs about "
+                             "two microseconds, so pass_ms is an upper bound); roofline of the pass: q and k read, "
+                             "their normalised copies written"}
     dec_ach = dec_bytes / (dec_ms * 1e-3) / 1e9
     res["decode"] = {"ms": dec_ms, "value": DEC_B / (dec_ms * 1e-3) / 1e6, "unit": "Msequence-steps/s",
                      "batch": DEC_B, "H_v": Hv, "H_k": Hk,

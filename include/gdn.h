@@ -18,8 +18,9 @@
  *
  * Conventions for every entry point below:
  *  - All tensor pointers are DEVICE pointers, token-major and contiguous:
- *      q, k      : bf16 [T, H_k, 128]
- *      v, out    : bf16 [T, H_v, 128]
+ *      q, k      : bf16 [T, H_k, 128]   (fp16 with GDN_FLAG_FP16_INPUTS)
+ *      v         : bf16 [T, H_v, 128]   (fp16 with GDN_FLAG_FP16_INPUTS)
+ *      out       : bf16 [T, H_v, 128]
  *      g, beta   : fp32 [T, H_v]        (g = log-decay, expected <= 0; beta in [0, 1])
  *      cu_seqlens: int32 [N + 1]        (0 = cu[0] <= cu[1] <= ... <= cu[N] = T)
  *      init_idx  : int32 [N] or NULL    (NULL = every document starts from zero)
@@ -89,6 +90,11 @@ enum gdn_flags {
                                 The backward's dq and dk are the gradients with respect to the unnormalised
                                 inputs. The workspace also holds the normalised copies (the size queries
                                 count them); forward and backward of a training step must both set it. */
+  GDN_FLAG_FP16_INPUTS = 16, /* q, k, v (and dout) are IEEE fp16 instead of bf16 ("Using it, and the fine
+                                print": bf16 or fp16 inputs). The kernels' matrix operands are bf16: each
+                                input is rounded once to bf16 (relative error at most 2^-9, as for any other
+                                operand) into workspace copies that the size queries count; accumulation
+                                stays fp32. Gradients stay fp32. Combines with GDN_FLAG_L2NORM_QK. */
   GDN_FLAG_REUSE_FWD = 2     /* backward: the workspace holds the records of a forward run with
                                 GDN_FLAG_SAVE_FOR_BWD on the same inputs, options and stream order, and
                                 nothing has written it since; the backward then skips its recompute
@@ -166,7 +172,7 @@ int gdn_chunk_fwd(const void* q, const void* k, const void* v, const float* g, c
 
 /*
  * Backward of gdn_chunk_fwd for the loss sum(dout * out) + sum(dfinal_state * final_state).
- * dout: bf16 [T, H_v, 128]; dfinal_state: fp32 [N, H_v, 128, 128] or NULL (zero).
+ * dout: bf16 [T, H_v, 128] (fp16 with GDN_FLAG_FP16_INPUTS); dfinal_state: fp32 [N, H_v, 128, 128] or NULL (zero).
  * Outputs, all fp32: dq, dk [T, H_k, 128] (summed over the value heads of each key head);
  * dv [T, H_v, 128]; dg, dbeta [T, H_v]; dinitial_state [n_init, H_v, 128, 128]
  * (summed over every document that starts from the same pool entry; NULL allowed when n_init == 0).
@@ -223,8 +229,8 @@ int gdn_noalloc_status(int device, gdn_stream_t stream);
  *   status     : device int32 or NULL; a sequence whose index is out of range is skipped (its out row
  *                is zero, its pool entry untouched) and GDN_ERR_INVALID_ARG is written here (never
  *                cleared: the caller zeroes it)
- * opt may be NULL; opt->scale and the GDN_FLAG_L2NORM_QK bit of opt->flags are used (q and k then
- * come unnormalised and are scaled to unit norm in fp32 first). Same device rules as gdn_chunk_fwd (the pool's GPU);
+ * opt may be NULL; opt->scale and the GDN_FLAG_L2NORM_QK and GDN_FLAG_FP16_INPUTS bits of opt->flags
+ * are used (q and k unnormalised, scaled to unit norm in fp32 first; q, k, v in fp16; out stays bf16). Same device rules as gdn_chunk_fwd (the pool's GPU);
  * nothing is allocated, everything runs on `stream`. B = 0 is a no-op.
  */
 int gdn_decode_step(const void* q, const void* k, const void* v, const float* g, const float* beta, int B, int H_k,

@@ -51,6 +51,7 @@ FLAG_SAVE_FOR_BWD = 1  # forward of a training step: keep the records for the ba
 FLAG_REUSE_FWD = 2     # backward: use the records of a FLAG_SAVE_FOR_BWD forward instead of recomputing
 FLAG_TEST_WITHHOLD_FORK = 4  # forward, tests of the bounded waits only: forked documents never get their start
 FLAG_L2NORM_QK = 8     # q and k come unnormalised: the library scales each row to unit L2 norm (both directions)
+FLAG_FP16_INPUTS = 16  # q, k, v (and dout) are fp16; set by the calls below when the tensors are float16
 
 
 @dataclass
@@ -65,6 +66,7 @@ class Options:
     save_for_backward: bool = False
     reuse_forward: bool = False
     l2norm_qk: bool = False          # q and k unnormalised: normalise each row first (forward and backward)
+    fp16_inputs: bool = False        # q, k, v (and dout) in fp16 (the tensor calls below set it from the dtype)
     flag_wait_us: int = 0            # limit of a wait for another item's published state (0 = about 2 s)
     test_withhold_fork: bool = False  # tests only: make the waits of forked documents run out
 
@@ -81,7 +83,8 @@ class Options:
             ev = ctypes.cast(self._ev_array, ctypes.c_void_p)
         flags = ((FLAG_SAVE_FOR_BWD if self.save_for_backward else 0) | (FLAG_REUSE_FWD if self.reuse_forward else 0)
                  | (FLAG_TEST_WITHHOLD_FORK if self.test_withhold_fork else 0)
-                 | (FLAG_L2NORM_QK if self.l2norm_qk else 0))
+                 | (FLAG_L2NORM_QK if self.l2norm_qk else 0)
+                 | (FLAG_FP16_INPUTS if self.fp16_inputs else 0))
         return COptions(m, float(self.trunc_log_threshold), int(self.segment_chunks), float(self.scale), flags, ev,
                         int(self.flag_wait_us))
 
@@ -149,6 +152,21 @@ def status_string(status: int) -> str:
 
 def _opts(options: Optional[Options]) -> COptions:
     return (options or Options()).c()
+
+
+def _half_dtype(q):
+    """bf16 or fp16 inputs: the dtype of q decides, k and v (and dout) must match it."""
+    torch = _torch()
+    if q.dtype not in (torch.bfloat16, torch.float16):
+        raise ValueError("q: expected a bfloat16 or float16 tensor")
+    return q.dtype
+
+
+def _with_dtype(options: Optional[Options], half) -> Options:
+    import dataclasses
+    torch = _torch()
+    base = options or Options()
+    return dataclasses.replace(base, fp16_inputs=(half == torch.float16))
 
 
 def fwd_workspace_size(N: int, T: int, H_k: int, H_v: int, options: Optional[Options] = None) -> int:
@@ -225,9 +243,11 @@ def chunk_fwd(q, k, v, g, beta, cu_seqlens, init_idx=None, initial_state=None, o
     T, Hk, D = q.shape
     Hv = v.shape[1]
     N = cu_seqlens.shape[0] - 1
-    _check(q, "q", torch.bfloat16, (T, Hk, D))
-    _check(k, "k", torch.bfloat16, (T, Hk, D))
-    _check(v, "v", torch.bfloat16, (T, Hv, D))
+    half = _half_dtype(q)
+    options = _with_dtype(options, half)
+    _check(q, "q", half, (T, Hk, D))
+    _check(k, "k", half, (T, Hk, D))
+    _check(v, "v", half, (T, Hv, D))
     _check(g, "g", torch.float32, (T, Hv))
     _check(beta, "beta", torch.float32, (T, Hv))
     _check(cu_seqlens, "cu_seqlens", torch.int32, (N + 1,))
@@ -265,7 +285,12 @@ def chunk_bwd(q, k, v, g, beta, cu_seqlens, dout, dfinal_state=None, init_idx=No
     T, Hk, D = q.shape
     Hv = v.shape[1]
     N = cu_seqlens.shape[0] - 1
-    _check(dout, "dout", torch.bfloat16, (T, Hv, D))
+    half = _half_dtype(q)
+    options = _with_dtype(options, half)
+    _check(q, "q", half, (T, Hk, D))
+    _check(k, "k", half, (T, Hk, D))
+    _check(v, "v", half, (T, Hv, D))
+    _check(dout, "dout", half, (T, Hv, D))
     if dfinal_state is not None:
         _check(dfinal_state, "dfinal_state", torch.float32, (N, Hv, D, D))
     n_init = 0 if initial_state is None else initial_state.shape[0]
@@ -307,9 +332,11 @@ def decode_step(q, k, v, g, beta, state_pool, state_idx, options: Optional[Optio
     torch = _torch()
     B, Hk, D = q.shape
     Hv = v.shape[1]
-    _check(q, "q", torch.bfloat16, (B, Hk, D))
-    _check(k, "k", torch.bfloat16, (B, Hk, D))
-    _check(v, "v", torch.bfloat16, (B, Hv, D))
+    half = _half_dtype(q)
+    options = _with_dtype(options, half)
+    _check(q, "q", half, (B, Hk, D))
+    _check(k, "k", half, (B, Hk, D))
+    _check(v, "v", half, (B, Hv, D))
     _check(g, "g", torch.float32, (B, Hv))
     _check(beta, "beta", torch.float32, (B, Hv))
     _check(state_idx, "state_idx", torch.int32, (B,))

@@ -90,8 +90,8 @@ gdn_options resolve(const gdn_options* opt) {
 
 bool valid_options(const gdn_options& o) {
   return (o.mode == GDN_MODE_EXACT || o.mode == GDN_MODE_TRUNCATE) &&
-         (o.flags & ~(GDN_FLAG_SAVE_FOR_BWD | GDN_FLAG_REUSE_FWD | GDN_FLAG_TEST_WITHHOLD_FORK | GDN_FLAG_L2NORM_QK)) ==
-             0 &&
+         (o.flags & ~(GDN_FLAG_SAVE_FOR_BWD | GDN_FLAG_REUSE_FWD | GDN_FLAG_TEST_WITHHOLD_FORK | GDN_FLAG_L2NORM_QK |
+                      GDN_FLAG_FP16_INPUTS)) == 0 &&
          o.scale == o.scale && o.flag_wait_us >= 0;
 }
 
@@ -160,7 +160,7 @@ size_t gdn_fwd_workspace_size(int N, int T, int H_k, int H_v, const gdn_options*
   if (!valid_options(o)) return 0;
   if (o.flags & GDN_FLAG_SAVE_FOR_BWD) return gdn_bwd_workspace_size(N, T, H_k, H_v, opt);
   return fwd_layout(make_dims(N, T, H_k, H_v, 0, o, current_sm_count())).total +
-         ((o.flags & GDN_FLAG_L2NORM_QK) ? l2norm_bytes(T, H_k) : 0);
+         input_copies(T, H_k, H_v, o.flags, false).total;
 }
 
 size_t gdn_bwd_workspace_size(int N, int T, int H_k, int H_v, const gdn_options* opt) {
@@ -169,7 +169,7 @@ size_t gdn_bwd_workspace_size(int N, int T, int H_k, int H_v, const gdn_options*
   if (!valid_options(o)) return 0;
   o.mode = GDN_MODE_EXACT;  // the backward is always exact
   return bwd_layout(make_dims(N, T, H_k, H_v, 0, o, current_sm_count())).total +
-         ((o.flags & GDN_FLAG_L2NORM_QK) ? l2norm_bytes(T, H_k) : 0);
+         input_copies(T, H_k, H_v, o.flags, true).total;
 }
 
 int gdn_workspace_status(const void* workspace, gdn_stream_t stream) {
@@ -216,8 +216,8 @@ int prepare_fwd(const void* q, const void* k, const void* v, const float* g, con
   const int arch = check_arch();
   if (arch != kOk) return arch;
   const PlanDims d = make_dims(N, T, H_k, H_v, n_init, *o, current_sm_count());
-  const size_t need = ((o->flags & GDN_FLAG_SAVE_FOR_BWD) ? bwd_layout(d).total : fwd_layout(d).total) +
-                      ((o->flags & GDN_FLAG_L2NORM_QK) ? l2norm_bytes(T, H_k) : 0);
+  const bool save = (o->flags & GDN_FLAG_SAVE_FOR_BWD) != 0;
+  const size_t need = (save ? bwd_layout(d).total : fwd_layout(d).total) + input_copies(T, H_k, H_v, o->flags, save).total;
   if (ws_bytes < need) return GDN_ERR_WORKSPACE;
   return GDN_OK;
 }
@@ -251,8 +251,34 @@ int prepare_bwd(const void* q, const void* k, const void* v, const float* g, con
   gdn_options oe = *o;
   oe.mode = GDN_MODE_EXACT;
   if (ws_bytes < bwd_layout(make_dims(N, T, H_k, H_v, n_init, oe, current_sm_count())).total +
-                     ((o->flags & GDN_FLAG_L2NORM_QK) ? l2norm_bytes(T, H_k) : 0))
+                     input_copies(T, H_k, H_v, o->flags, true).total)
     return GDN_ERR_WORKSPACE;
+  return GDN_OK;
+}
+
+// The input copies of GDN_FLAG_L2NORM_QK / GDN_FLAG_FP16_INPUTS at `base`: q and k normalised (from
+// bf16 or fp16) or converted, v and dout converted; the pointers are redirected to the copies.
+int stage_inputs(const void*& q, const void*& k, const void*& v, const void** dout, uint8_t* base,
+                 const InputCopies& c, int flags, int T, int H_k, int H_v, cudaStream_t stream) {
+  const bool f16 = (flags & GDN_FLAG_FP16_INPUTS) != 0;
+  uint8_t* qn = base + c.q;
+  uint8_t* kn = base + c.k;
+  const int64_t nqk = (int64_t)T * H_k * kDim, nv = (int64_t)T * H_v * kDim;
+  if (flags & GDN_FLAG_L2NORM_QK) {
+    if (launch_l2norm_fwd(q, k, qn, kn, (int64_t)T * H_k, f16, stream) != kOk) return GDN_ERR_CUDA;
+  } else if (launch_f16_to_bf16(q, qn, nqk, stream) != kOk || launch_f16_to_bf16(k, kn, nqk, stream) != kOk) {
+    return GDN_ERR_CUDA;
+  }
+  q = qn;
+  k = kn;
+  if (f16) {
+    if (launch_f16_to_bf16(v, base + c.v, nv, stream) != kOk) return GDN_ERR_CUDA;
+    v = base + c.v;
+    if (dout) {
+      if (launch_f16_to_bf16(*dout, base + c.dout, nv, stream) != kOk) return GDN_ERR_CUDA;
+      *dout = base + c.dout;
+    }
+  }
   return GDN_OK;
 }
 
@@ -292,17 +318,16 @@ int gdn_chunk_fwd(const void* q, const void* k, const void* v, const float* g, c
   if (rc != GDN_OK) return rc;
   const int sms = current_sm_count();
   cudaEvent_t* ev = reinterpret_cast<cudaEvent_t*>(o.stage_events);
-  if (o.flags & GDN_FLAG_L2NORM_QK) {
-    // normalised copies of q and k after the layout; every later kernel reads them instead
+  if (o.flags & (GDN_FLAG_L2NORM_QK | GDN_FLAG_FP16_INPUTS)) {
+    // normalised / converted copies of the inputs after the layout; every later kernel reads them
     const PlanDims d0 = make_dims(N, T, H_k, H_v, n_init, o, sms);
-    uint8_t* qn = reinterpret_cast<uint8_t*>(workspace) +
-                  ((o.flags & GDN_FLAG_SAVE_FOR_BWD) ? bwd_layout(d0).total : fwd_layout(d0).total);
-    uint8_t* kn = qn + (size_t)T * H_k * kDim * 2;
+    const bool save = (o.flags & GDN_FLAG_SAVE_FOR_BWD) != 0;
+    uint8_t* base = reinterpret_cast<uint8_t*>(workspace) + (save ? bwd_layout(d0).total : fwd_layout(d0).total);
     if (ev && ev[18]) cudaEventRecord(ev[18], (cudaStream_t)stream);
-    if (launch_l2norm_fwd(q, k, qn, kn, (int64_t)T * H_k, (cudaStream_t)stream) != kOk) return GDN_ERR_CUDA;
+    const int rs = stage_inputs(q, k, v, nullptr, base, input_copies(T, H_k, H_v, o.flags, save), o.flags, T, H_k,
+                                H_v, (cudaStream_t)stream);
+    if (rs != GDN_OK) return rs;
     if (ev && ev[19]) cudaEventRecord(ev[19], (cudaStream_t)stream);
-    q = qn;
-    k = kn;
   } else if (ev) {
     for (int i = 18; i < 20; ++i)
       if (ev[i]) cudaEventRecord(ev[i], (cudaStream_t)stream);
@@ -375,14 +400,13 @@ int gdn_chunk_bwd(const void* q, const void* k, const void* v, const float* g, c
   const PlanDims dims = make_dims(N, T, H_k, H_v, n_init, oe, current_sm_count());
   const void* q_raw = q;
   const void* k_raw = k;
-  if (o.flags & GDN_FLAG_L2NORM_QK) {
-    uint8_t* qn = reinterpret_cast<uint8_t*>(workspace) + bwd_layout(dims).total;
-    uint8_t* kn = qn + (size_t)T * H_k * kDim * 2;
+  if (o.flags & (GDN_FLAG_L2NORM_QK | GDN_FLAG_FP16_INPUTS)) {
+    uint8_t* base = reinterpret_cast<uint8_t*>(workspace) + bwd_layout(dims).total;
     if (ev && ev[18]) cudaEventRecord(ev[18], (cudaStream_t)stream);
-    if (launch_l2norm_fwd(q, k, qn, kn, (int64_t)T * H_k, (cudaStream_t)stream) != kOk) return GDN_ERR_CUDA;
+    const int rs = stage_inputs(q, k, v, &dout, base, input_copies(T, H_k, H_v, o.flags, true), o.flags, T, H_k,
+                                H_v, (cudaStream_t)stream);
+    if (rs != GDN_OK) return rs;
     if (ev && ev[19]) cudaEventRecord(ev[19], (cudaStream_t)stream);
-    q = qn;
-    k = kn;
   } else if (ev) {
     for (int i = 18; i < 20; ++i)
       if (ev[i]) cudaEventRecord(ev[i], (cudaStream_t)stream);
@@ -421,7 +445,9 @@ int gdn_chunk_bwd(const void* q, const void* k, const void* v, const float* g, c
   }
   // gradients with respect to the unnormalised q and k
   if (ev && ev[20]) cudaEventRecord(ev[20], (cudaStream_t)stream);
-  if (launch_l2norm_bwd(q_raw, k_raw, dq, dk, (int64_t)T * H_k, (cudaStream_t)stream) != kOk) return GDN_ERR_CUDA;
+  if (launch_l2norm_bwd(q_raw, k_raw, dq, dk, (int64_t)T * H_k, (o.flags & GDN_FLAG_FP16_INPUTS) != 0,
+                        (cudaStream_t)stream) != kOk)
+    return GDN_ERR_CUDA;
   if (ev && ev[21]) cudaEventRecord(ev[21], (cudaStream_t)stream);
   return GDN_OK;
 }

@@ -32,9 +32,26 @@ constexpr int kMinSegChunks = 4;  // shortest automatic segment (chunks)
 
 // q and k normalisation (GDN_FLAG_L2NORM_QK): y = x (x . x + kL2NormEps)^{-1/2} per row of 128.
 constexpr float kL2NormEps = 1e-6f;
-// Workspace bytes of the normalised copies of q and k (bf16, [T][Hk][128] each), placed after the
-// forward's or the backward's layout.
-inline size_t l2norm_bytes(int T, int Hk) { return ((size_t)2 * T * Hk * kDim * 2 + 255) / 256 * 256; }
+// Option flags that change the inputs (mirror include/gdn.h).
+constexpr int kFlagL2Norm = 8, kFlagFp16 = 16;
+
+// Workspace copies of the inputs, placed after the forward's or the backward's layout: with
+// GDN_FLAG_L2NORM_QK and/or GDN_FLAG_FP16_INPUTS, q' and k' (bf16 [T][Hk][128], normalised and/or
+// converted); with fp16 inputs also v' and, in a backward workspace, dout' (bf16 [T][Hv][128]).
+struct InputCopies {
+  size_t q, k, v, dout, total;  // byte offsets from the start of the region, and its size
+};
+inline InputCopies input_copies(int T, int Hk, int Hv, int flags, bool bwd) {
+  InputCopies c{0, 0, 0, 0, 0};
+  if (!(flags & (kFlagL2Norm | kFlagFp16))) return c;
+  const size_t qk = (size_t)T * Hk * kDim * 2, vv = (size_t)T * Hv * kDim * 2;
+  c.k = qk;
+  c.v = 2 * qk;
+  c.dout = 2 * qk + ((flags & kFlagFp16) ? vv : 0);
+  c.total = c.dout + ((flags & kFlagFp16) && bwd ? vv : 0);
+  c.total = (c.total + 255) / 256 * 256;
+  return c;
+}
 
 // Status codes (mirror include/gdn.h).
 constexpr int kOk = 0, kErrInvalid = -1, kErrUnsupported = -2, kErrCuda = -3, kErrTimeout = -4,

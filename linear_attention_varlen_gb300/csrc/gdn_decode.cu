@@ -17,6 +17,7 @@
 // memory. The state is read and written once: the step is bound by HBM traffic (128 KB per
 // sequence and value head).
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -30,9 +31,20 @@ namespace {
 
 constexpr int kDecThreads = 256;
 
-__global__ void __launch_bounds__(kDecThreads) decode_kernel(const __nv_bfloat16* __restrict__ q,
-                                                             const __nv_bfloat16* __restrict__ k,
-                                                             const __nv_bfloat16* __restrict__ v,
+// one 16-bit input element (bf16, or fp16 with GDN_FLAG_FP16_INPUTS) as fp32
+template <bool kF16>
+__device__ __forceinline__ float ld16(const uint16_t* p) {
+  const uint16_t b = *p;
+  if constexpr (kF16)
+    return __half2float(__ushort_as_half(b));
+  else
+    return __bfloat162float(__ushort_as_bfloat16(b));
+}
+
+template <bool kF16>
+__global__ void __launch_bounds__(kDecThreads) decode_kernel(const uint16_t* __restrict__ q,
+                                                             const uint16_t* __restrict__ k,
+                                                             const uint16_t* __restrict__ v,
                                                              const float* __restrict__ g,
                                                              const float* __restrict__ beta,
                                                              const int32_t* __restrict__ state_idx, float* pool,
@@ -49,8 +61,8 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const __nv_bfloat16
     return;
   }
   if (t < kDim) {
-    s_k[t] = __bfloat162float(k[((size_t)b * Hk + hk) * kDim + t]);
-    s_q[t] = __bfloat162float(q[((size_t)b * Hk + hk) * kDim + t]);
+    s_k[t] = ld16<kF16>(k + ((size_t)b * Hk + hk) * kDim + t);
+    s_q[t] = ld16<kF16>(q + ((size_t)b * Hk + hk) * kDim + t);
   }
   __syncthreads();
   if (t < 64) {
@@ -95,7 +107,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const __nv_bfloat16
     float p = 0.f;
 #pragma unroll
     for (int r = 0; r < 8; ++r) p += s_red[r][t];
-    s_d[t] = bt * (__bfloat162float(v[((size_t)b * Hv + h) * kDim + t]) - p);
+    s_d[t] = bt * (ld16<kF16>(v + ((size_t)b * Hv + h) * kDim + t) - p);
   }
   __syncthreads();
   // S = S' + k d^T, written back; this thread's part of o = S^T (scale q)
@@ -154,9 +166,18 @@ extern "C" int gdn_decode_step(const void* q, const void* k, const void* v, cons
       cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
     return GDN_ERR_CUDA;
   if (major != 10 || minor != 3) return GDN_ERR_UNSUPPORTED;
-  gdn::decode_kernel<<<(unsigned)(B * H_v), gdn::kDecThreads, 0, (cudaStream_t)stream>>>(
-      reinterpret_cast<const __nv_bfloat16*>(q), reinterpret_cast<const __nv_bfloat16*>(k),
-      reinterpret_cast<const __nv_bfloat16*>(v), g, beta, state_idx, state_pool, n_pool, H_k, H_v, o.scale,
-      (o.flags & GDN_FLAG_L2NORM_QK) ? 1 : 0, reinterpret_cast<__nv_bfloat16*>(out), status);
+  auto q16 = reinterpret_cast<const uint16_t*>(q);
+  auto k16 = reinterpret_cast<const uint16_t*>(k);
+  auto v16 = reinterpret_cast<const uint16_t*>(v);
+  const int l2 = (o.flags & GDN_FLAG_L2NORM_QK) ? 1 : 0;
+  const unsigned grid = (unsigned)(B * H_v);
+  if (o.flags & GDN_FLAG_FP16_INPUTS)
+    gdn::decode_kernel<true><<<grid, gdn::kDecThreads, 0, (cudaStream_t)stream>>>(
+        q16, k16, v16, g, beta, state_idx, state_pool, n_pool, H_k, H_v, o.scale, l2,
+        reinterpret_cast<__nv_bfloat16*>(out), status);
+  else
+    gdn::decode_kernel<false><<<grid, gdn::kDecThreads, 0, (cudaStream_t)stream>>>(
+        q16, k16, v16, g, beta, state_idx, state_pool, n_pool, H_k, H_v, o.scale, l2,
+        reinterpret_cast<__nv_bfloat16*>(out), status);
   return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }

@@ -88,6 +88,20 @@ def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
     return (np.ascontiguousarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
 
 
+def to_f16_bits(x: np.ndarray) -> np.ndarray:
+    """Round to IEEE fp16 (numpy's round-to-nearest-even) and return the uint16 bit patterns."""
+    return np.ascontiguousarray(x, dtype=np.float64).astype(np.float16).view(np.uint16)
+
+
+def f16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
+    """Exact fp32 values of fp16 bit patterns."""
+    return np.ascontiguousarray(bits, dtype=np.uint16).view(np.float16).astype(np.float32)
+
+
+_ROUND = {"bf16": to_bf16_bits, "f16": to_f16_bits}
+_DECODE = {"bf16": bf16_bits_to_f32, "f16": f16_bits_to_f32}
+
+
 # ----------------------------------------------------------------------------- problems
 
 
@@ -96,13 +110,14 @@ class Problem:
     """One packed varlen problem: token-major tensors plus the document layout.
 
     Layouts (T tokens, N documents):
-      q, k  : bf16 bits uint16 [T, Hk, Dk]
-      v     : bf16 bits uint16 [T, Hv, Dv]
+      q, k  : bf16 (or fp16, see dtype) bits uint16 [T, Hk, Dk]
+      v     : bf16 (or fp16) bits uint16 [T, Hv, Dv]
       g, beta : float32 [T, Hv]
       cu_seqlens : int32 [N + 1]
       init_idx : int32 [N] (-1 zero, 0..n_init-1 pool, n_init + j fork from document j < i) or None
       initial_state : float32 [n_init, Hv, Dk, Dv] or None
-      dout : bf16 bits [T, Hv, Dv] or None ; dfinal : float32 [N, Hv, Dk, Dv] or None
+      dout : bf16 (or fp16) bits [T, Hv, Dv] or None ; dfinal : float32 [N, Hv, Dk, Dv] or None
+      dtype : "bf16" or "f16", the format of q, k, v and dout
     """
     name: str
     q: np.ndarray
@@ -120,6 +135,7 @@ class Problem:
     dout: Optional[np.ndarray] = None
     dfinal: Optional[np.ndarray] = None
     meta: dict = field(default_factory=dict)
+    dtype: str = "bf16"
 
     @property
     def T(self) -> int:
@@ -135,17 +151,18 @@ class Problem:
 
     def as_f64(self):
         """Exact fp64 upcasts of every input (what the oracle consumes)."""
+        dec = _DECODE[self.dtype]
         d = dict(
-            q=bf16_bits_to_f32(self.q).astype(np.float64),
-            k=bf16_bits_to_f32(self.k).astype(np.float64),
-            v=bf16_bits_to_f32(self.v).astype(np.float64),
+            q=dec(self.q).astype(np.float64),
+            k=dec(self.k).astype(np.float64),
+            v=dec(self.v).astype(np.float64),
             g=self.g.astype(np.float64),
             beta=self.beta.astype(np.float64),
         )
         if self.initial_state is not None:
             d["initial_state"] = self.initial_state.astype(np.float64)
         if self.dout is not None:
-            d["dout"] = bf16_bits_to_f32(self.dout).astype(np.float64)
+            d["dout"] = dec(self.dout).astype(np.float64)
         if self.dfinal is not None:
             d["dfinal"] = self.dfinal.astype(np.float64)
         return d
@@ -163,10 +180,11 @@ def _unit_rows(x: np.ndarray) -> np.ndarray:
 def make_problem(name: str, seed: int, lengths: List[int], Hk: int, Hv: int, Dk: int = 128, Dv: int = 128,
                  init_idx: Optional[List[int]] = None, n_init: int = 0, with_dout: bool = False,
                  with_dfinal: bool = False, q_scale: Optional[float] = None,
-                 g_mean: float = 2.0) -> Problem:
+                 g_mean: float = 2.0, dtype: str = "bf16") -> Problem:
     """Draw one problem with the recipe in the module docstring.
 
-    `g_mean` is the mean of u in g = log sigmoid(u); 2.0 is the workload value.
+    `g_mean` is the mean of u in g = log sigmoid(u); 2.0 is the workload value. `dtype` "f16" rounds
+    q, k, v and dO to IEEE fp16 instead of bf16 (the same draws).
     Pool initial states (n_init > 0) are N(0, 1) scaled by 0.1 in fp32.
     """
     if Hv % Hk != 0:
@@ -183,16 +201,17 @@ def make_problem(name: str, seed: int, lengths: List[int], Hk: int, Hv: int, Dk:
     g = -np.logaddexp(0.0, -u)  # log(sigmoid(u))
     w = normal(seed, _STREAM_B, T * Hv).reshape(T, Hv)
     beta = 1.0 / (1.0 + np.exp(-w))
-    p = Problem(name=name, q=to_bf16_bits(q), k=to_bf16_bits(k), v=to_bf16_bits(v),
+    rnd = _ROUND[dtype]
+    p = Problem(name=name, q=rnd(q), k=rnd(k), v=rnd(v),
                 g=g.astype(np.float32), beta=beta.astype(np.float32), cu_seqlens=cu,
-                Hk=Hk, Hv=Hv, Dk=Dk, Dv=Dv)
+                Hk=Hk, Hv=Hv, Dk=Dk, Dv=Dv, dtype=dtype)
     if init_idx is not None:
         p.init_idx = np.asarray(init_idx, dtype=np.int32)
     if n_init > 0:
         p.initial_state = (0.1 * normal(seed, _STREAM_H0, n_init * Hv * Dk * Dv)).astype(
             np.float32).reshape(n_init, Hv, Dk, Dv)
     if with_dout:
-        p.dout = to_bf16_bits(normal(seed, _STREAM_DO, T * Hv * Dv).reshape(T, Hv, Dv))
+        p.dout = rnd(normal(seed, _STREAM_DO, T * Hv * Dv).reshape(T, Hv, Dv))
     if with_dfinal:
         p.dfinal = normal(seed, _STREAM_DHT, len(lengths) * Hv * Dk * Dv).astype(
             np.float32).reshape(len(lengths), Hv, Dk, Dv)
@@ -283,10 +302,11 @@ def workload_train(n_docs: int = 4, doc_len: int = 16384, Hk: int = 2, Hv: int =
 
 
 def to_device(p: Problem, device="cuda"):
-    """The problem's arrays as torch tensors on `device` (bf16 bit patterns viewed as bfloat16,
-    fp32 and int32 as they are): plain copies, no arithmetic."""
+    """The problem's arrays as torch tensors on `device` (bf16 or fp16 bit patterns viewed as
+    bfloat16 or float16, fp32 and int32 as they are): plain copies, no arithmetic."""
     import torch
-    bf = lambda a: torch.from_numpy(np.ascontiguousarray(a)).view(torch.bfloat16).to(device)
+    half = torch.bfloat16 if p.dtype == "bf16" else torch.float16
+    bf = lambda a: torch.from_numpy(np.ascontiguousarray(a)).view(half).to(device)
     f32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(device)
     d = dict(q=bf(p.q), k=bf(p.k), v=bf(p.v), g=f32(p.g), beta=f32(p.beta),
              cu_seqlens=torch.from_numpy(p.cu_seqlens.astype(np.int32)).to(device))

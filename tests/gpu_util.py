@@ -19,9 +19,18 @@ def bf16_to_f64(t):
     return t.detach().to(torch.float32).cpu().numpy().astype(np.float64)
 
 
+def with_dtype(p: synth.Problem, options):
+    """The options with the input format of the problem (fp16 inputs need their workspace copies)."""
+    import dataclasses
+
+    import linear_attention_varlen_gb300 as gdn
+    return dataclasses.replace(options or gdn.Options(), fp16_inputs=(p.dtype == "f16"))
+
+
 def run_fwd(p: synth.Problem, options=None):
     import linear_attention_varlen_gb300 as gdn
     import torch
+    options = with_dtype(p, options)
     d = to_device(p)
     ws = torch.empty(gdn.fwd_workspace_size(p.N, p.T, p.Hk, p.Hv, options), dtype=torch.uint8, device="cuda")
     out, fin = gdn.chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"], d["init_idx"],
@@ -71,6 +80,7 @@ def run_bwd(p: synth.Problem, options=None):
     """Backward through the library; returns fp64 numpy dq, dk, dv, dg, dbeta, dinit."""
     import linear_attention_varlen_gb300 as gdn
     import torch
+    options = with_dtype(p, options)
     d = to_device(p)
     ws = torch.empty(gdn.bwd_workspace_size(p.N, p.T, p.Hk, p.Hv, options), dtype=torch.uint8, device="cuda")
     gr = gdn.chunk_bwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"], d["dout"], d.get("dfinal_state"),
@@ -90,7 +100,7 @@ def run_train(p: synth.Problem, options=None):
 
     import linear_attention_varlen_gb300 as gdn
     import torch
-    base = options or gdn.Options()
+    base = with_dtype(p, options)
     fo = dataclasses.replace(base, save_for_backward=True, reuse_forward=False)
     bo = dataclasses.replace(base, save_for_backward=False, reuse_forward=True)
     d = to_device(p)

@@ -143,3 +143,14 @@ def test_workload_layouts_at_small_sizes():
     assert list(fk.init_idx) == [-1, 0, 0, 0] and fk.n_init == 0  # every branch forks document 0
     tr = synth.workload_train(n_docs=2, doc_len=100, Hk=1, Hv=2)
     assert list(tr.cu_seqlens) == [0, 100, 200] and tr.dout is not None and tr.dout.shape == (200, 2, 128)
+
+
+def test_f16_rounding_matches_torch():
+    torch = __import__("pytest").importorskip("torch")
+    import numpy as np
+    x = np.random.default_rng(5).standard_normal(4096) * np.exp(np.random.default_rng(6).uniform(-12, 10, 4096))
+    ours = synth.to_f16_bits(x)
+    ref = torch.from_numpy(x).to(torch.float16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(ours, ref)
+    back = synth.f16_bits_to_f32(ours)
+    assert np.array_equal(back, torch.from_numpy(x).to(torch.float16).float().numpy())
