@@ -1,7 +1,8 @@
 """fp64 oracle for the gated delta rule over packed varlen batches.
 
 TEST INFRASTRUCTURE ONLY: imported by tests/, by the smoke check and by the
-benchmark's CPU-baseline leg. The product path never imports it.
+benchmark's CPU-baseline leg. The product path never imports it. The width-4
+causal convolution's oracle is oracle/conv.py (numpy, fp64).
 
 `gdn_oracle.cpp` holds the token-by-token recurrence and its hand-written
 reverse mode (fp64, std::thread); this module compiles it with the host C++
