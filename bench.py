@@ -527,6 +527,35 @@ def run_ours(args, rank, world, local_rank):
     l2_bytes = 2 * (2 * T * Hk * D * 2)  # q and k read once, their normalised copies written once
     del l2_ws
 
+    # The width-4 causal convolution in front of the recurrence, over the packed training layout (four
+    # 16384-token documents) with the channels of q, k and v at these heads
+    CONV_T, CONV_C = 65536, 2 * Hk * D + Hv * D
+    cvx = torch.randn((CONV_T, CONV_C), device=dev).to(torch.bfloat16)
+    cvdy = torch.randn((CONV_T, CONV_C), device=dev).to(torch.bfloat16)
+    cvw = 0.5 * torch.randn((CONV_C, 4), device=dev)
+    cvb = 0.1 * torch.randn((CONV_C,), device=dev)
+    cvcu = torch.arange(0, CONV_T + 1, 16384, dtype=torch.int32, device=dev)
+    cvws = torch.empty(gdn.conv_workspace_size(4, CONV_T, CONV_C, True), dtype=torch.uint8, device=dev)
+    conv_reps = max(10, min(args.steps, 50))
+
+    def time_conv(fn):
+        for _ in range(3):
+            fn()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(conv_reps)]
+        torch.cuda.synchronize()
+        for a_, b_ in evs:
+            flush.zero_()
+            a_.record(stream)
+            fn()
+            b_.record(stream)
+        torch.cuda.synchronize()
+        return float(np.median([a_.elapsed_time(b_) for a_, b_ in evs]))
+    conv_f_ms = time_conv(lambda: gdn.conv_fwd(cvx, cvw, cvcu, cvb, workspace=cvws))
+    conv_b_ms = time_conv(lambda: gdn.conv_bwd(cvx, cvw, cvcu, cvdy, cvb, workspace=cvws))
+    conv_f_bytes = CONV_T * CONV_C * (2 + 2)          # x read, y written (bf16)
+    conv_b_bytes = CONV_T * CONV_C * (2 + 2 + 4)      # x, dy read, dx written (fp32)
+    del cvx, cvdy, cvws
+
     # Decode: one token for each of DEC_B sequences at the same heads, in place on a pool of states
     # (one entry per sequence); bound by reading and writing every state once.
     DEC_B = 256
@@ -638,6 +667,17 @@ def run_ours(args, rank, world, local_rank):
                              "the normalisation pass alone between its stage events (a recorded event costs about "
                              "two microseconds, so pass_ms is an upper bound); roofline of the pass: q and k read, "
                              "their normalised copies written"}
+    def hbm_obj(bytes_, ms_):
+        ach = bytes_ / (ms_ * 1e-3) / 1e9
+        return {"bound": "hbm", "achieved": ach, "peak": peaks["hbm"], "unit": "GB/s", "frac": ach / peaks["hbm"],
+                "algorithmic_bytes": bytes_, "peak_source": peaks["src"] + " hbm_gbs"}
+    res["conv"] = {"fwd_ms": conv_f_ms, "bwd_ms": conv_b_ms, "T": CONV_T, "C": CONV_C,
+                   "fwd_value": CONV_T / (conv_f_ms * 1e-3) / 1e6, "bwd_value": CONV_T / (conv_b_ms * 1e-3) / 1e6,
+                   "unit": UNIT, "fwd_roofline": hbm_obj(conv_f_bytes, conv_f_ms),
+                   "bwd_roofline": hbm_obj(conv_b_bytes, conv_b_ms),
+                   "note": "width-4 causal convolution (gdn_conv_fwd / gdn_conv_bwd) over four 16384-token "
+                           "documents, channels of q, k and v; one event pair around each call, L2 flushed "
+                           "before it"}
     dec_ach = dec_bytes / (dec_ms * 1e-3) / 1e9
     res["decode"] = {"ms": dec_ms, "value": DEC_B / (dec_ms * 1e-3) / 1e6, "unit": "Msequence-steps/s",
                      "batch": DEC_B, "H_v": Hv, "H_k": Hk,

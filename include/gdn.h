@@ -237,6 +237,35 @@ int gdn_decode_step(const void* q, const void* k, const void* v, const float* g,
                     int H_v, int head_dim, const int32_t* state_idx, float* state_pool, int n_pool, void* out,
                     int32_t* status, const gdn_options* opt, gdn_stream_t stream);
 
+/*
+ * Width-4 causal depthwise convolution over packed documents, the short convolution in front of the
+ * recurrence ("Musings on long-context fine-tuning", section "Isolating the recurrent layers": it
+ * reads the current input and the three before it; documents do not read each other; a continuation
+ * forked from a prefix reads the prefix's last three inputs first; section "Backward through P": the
+ * gradients through those inputs sum into the prefix). Per channel c, document i with inputs x[0..n-1]:
+ *     E = (init[0], init[1], init[2], x[0], ..., x[n-1]),  y[p] = bias[c] + sum_m w[c][m] E[p + m],
+ *     final_tail[i] = (E[n], E[n+1], E[n+2]).
+ * init_idx has the encoding of gdn_chunk_fwd: -1 zeros, 0..n_init-1 conv_init[x], n_init + j the
+ * final tail of document j < i of the same call (a fork). Layouts (device, contiguous):
+ *   x, y, dy : bf16 [T, C] (C a multiple of 8);  w : fp32 [C, 4];  bias : fp32 [C] or NULL (zero)
+ *   conv_init : bf16 [n_init, 3, C] or NULL;  final_tail : bf16 [N, 3, C] (copies of inputs)
+ *   dfinal_tail : fp32 [N, 3, C] or NULL;  dx : fp32 [T, C];  dw : fp32 [C, 4];  dbias : fp32 [C] or NULL
+ *   dconv_init : fp32 [n_init, 3, C] (summed over the documents that start from each entry)
+ * The backward is that of the loss sum(dy * y) + sum(dfinal_tail * final_tail); forks send their
+ * gradient into the forked document's last inputs. Every sum is formed in a fixed order
+ * (deterministic). workspace: gdn_conv_workspace_size(N, T, C, backward) bytes, 256-byte aligned;
+ * bad cu_seqlens / init_idx are reported in its status word (gdn_workspace_status). Same device and
+ * ownership rules as gdn_chunk_fwd; nothing is allocated.
+ */
+size_t gdn_conv_workspace_size(int N, int T, int C, int backward);
+int gdn_conv_fwd(const void* x, const float* w, const float* bias, const int32_t* cu_seqlens, int N, int T, int C,
+                 const int32_t* init_idx, const void* conv_init, int n_init, void* y, void* final_tail,
+                 void* workspace, size_t ws_bytes, gdn_stream_t stream);
+int gdn_conv_bwd(const void* x, const float* w, const float* bias, const int32_t* cu_seqlens, int N, int T, int C,
+                 const int32_t* init_idx, const void* conv_init, int n_init, const void* dy,
+                 const float* dfinal_tail, float* dx, float* dw, float* dbias, float* dconv_init, void* workspace,
+                 size_t ws_bytes, gdn_stream_t stream);
+
 /* Copy the workspace's device status word to the host (synchronises `stream`) and return it:
  * GDN_OK or the first device-side error of the last call that used this workspace. */
 int gdn_workspace_status(const void* workspace, gdn_stream_t stream);

@@ -29,7 +29,7 @@ CHUNK = 64
 EXPORTS = ("gdn_default_options", "gdn_fwd_workspace_size", "gdn_bwd_workspace_size", "gdn_chunk_fwd",
            "gdn_chunk_bwd", "gdn_workspace_status", "gdn_status_string", "gdn_plan_host", "gdn_chunk_fwd_noalloc",
            "gdn_noalloc_scratch_bytes", "gdn_noalloc_status", "gdn_fwd_check_args", "gdn_bwd_check_args",
-           "gdn_decode_step")
+           "gdn_decode_step", "gdn_conv_workspace_size", "gdn_conv_fwd", "gdn_conv_bwd")
 
 
 class GdnError(RuntimeError):
@@ -137,6 +137,12 @@ def load(path: Optional[str] = None):
         lib.gdn_bwd_check_args.restype = I
         lib.gdn_decode_step.argtypes = [P, P, P, P, P, I, I, I, I, P, P, I, P, P, OP, P]
         lib.gdn_decode_step.restype = I
+        lib.gdn_conv_workspace_size.argtypes = [I, I, I, I]
+        lib.gdn_conv_workspace_size.restype = Z
+        lib.gdn_conv_fwd.argtypes = [P, P, P, P, I, I, I, P, P, I, P, P, P, Z, P]
+        lib.gdn_conv_fwd.restype = I
+        lib.gdn_conv_bwd.argtypes = [P, P, P, P, I, I, I, P, P, I, P, P, P, P, P, P, P, Z, P]
+        lib.gdn_conv_bwd.restype = I
         if path is None:
             _lib = lib
         return lib
@@ -354,6 +360,69 @@ def decode_step(q, k, v, g, beta, state_pool, state_idx, options: Optional[Optio
     if rc != GDN_OK:
         raise GdnError(rc, "gdn_decode_step")
     return out
+
+
+def conv_workspace_size(N: int, T: int, C: int, backward: bool = False) -> int:
+    return int(load().gdn_conv_workspace_size(N, T, C, 1 if backward else 0))
+
+
+def conv_fwd(x, w, cu_seqlens, bias=None, init_idx=None, conv_init=None, y=None, final_tail=None, workspace=None,
+             stream=None):
+    """Width-4 causal convolution over packed documents. x [T, C] bf16; w [C, 4] fp32; bias [C] fp32 or
+    None; cu_seqlens [N+1] int32; init_idx [N] int32 or None; conv_init [n_init, 3, C] bf16 or None.
+    Returns (y [T, C] bf16, final_tail [N, 3, C] bf16)."""
+    torch = _torch()
+    T, C = x.shape
+    N = cu_seqlens.shape[0] - 1
+    _check(x, "x", torch.bfloat16, (T, C))
+    _check(w, "w", torch.float32, (C, 4))
+    _check(cu_seqlens, "cu_seqlens", torch.int32, (N + 1,))
+    if bias is not None:
+        _check(bias, "bias", torch.float32, (C,))
+    if init_idx is not None:
+        _check(init_idx, "init_idx", torch.int32, (N,))
+    n_init = 0
+    if conv_init is not None:
+        _check(conv_init, "conv_init", torch.bfloat16)
+        n_init = conv_init.shape[0]
+    if y is None:
+        y = torch.empty((T, C), dtype=torch.bfloat16, device=x.device)
+    if final_tail is None:
+        final_tail = torch.empty((N, 3, C), dtype=torch.bfloat16, device=x.device)
+    if workspace is None:
+        workspace = torch.empty(conv_workspace_size(N, T, C), dtype=torch.uint8, device=x.device)
+    rc = load().gdn_conv_fwd(_ptr(x), _ptr(w), _ptr(bias), _ptr(cu_seqlens), N, T, C, _ptr(init_idx), _ptr(conv_init),
+                             n_init, _ptr(y), _ptr(final_tail), _ptr(workspace), workspace.numel(),
+                             _stream_handle(stream))
+    if rc != GDN_OK:
+        raise GdnError(rc, "gdn_conv_fwd")
+    return y, final_tail
+
+
+def conv_bwd(x, w, cu_seqlens, dy, bias=None, init_idx=None, conv_init=None, dfinal_tail=None, workspace=None,
+             stream=None):
+    """Backward of conv_fwd. Returns dict dx [T, C], dw [C, 4], dbias [C] (None without bias),
+    dconv_init [n_init, 3, C] (None without a pool), all fp32."""
+    torch = _torch()
+    T, C = x.shape
+    N = cu_seqlens.shape[0] - 1
+    _check(dy, "dy", torch.bfloat16, (T, C))
+    if dfinal_tail is not None:
+        _check(dfinal_tail, "dfinal_tail", torch.float32, (N, 3, C))
+    n_init = 0 if conv_init is None else conv_init.shape[0]
+    f32 = dict(dtype=torch.float32, device=x.device)
+    dx = torch.empty((T, C), **f32)
+    dw = torch.empty((C, 4), **f32)
+    dbias = torch.empty((C,), **f32) if bias is not None else None
+    dci = torch.empty((n_init, 3, C), **f32) if n_init > 0 else None
+    if workspace is None:
+        workspace = torch.empty(conv_workspace_size(N, T, C, True), dtype=torch.uint8, device=x.device)
+    rc = load().gdn_conv_bwd(_ptr(x), _ptr(w), _ptr(bias), _ptr(cu_seqlens), N, T, C, _ptr(init_idx), _ptr(conv_init),
+                             n_init, _ptr(dy), _ptr(dfinal_tail), _ptr(dx), _ptr(dw), _ptr(dbias), _ptr(dci),
+                             _ptr(workspace), workspace.numel(), _stream_handle(stream))
+    if rc != GDN_OK:
+        raise GdnError(rc, "gdn_conv_bwd")
+    return dict(dx=dx, dw=dw, dbias=dbias, dconv_init=dci)
 
 
 def workspace_status(workspace, stream=None) -> int:

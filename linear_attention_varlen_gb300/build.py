@@ -15,7 +15,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libgdn_gb300.so")
-SOURCES = ["gdn_api.cu", "gdn_fwd.cu", "gdn_bwd.cu", "gdn_noalloc.cu", "gdn_decode.cu", "gdn_l2norm.cu"]
+SOURCES = ["gdn_api.cu", "gdn_fwd.cu", "gdn_bwd.cu", "gdn_noalloc.cu", "gdn_decode.cu", "gdn_l2norm.cu", "gdn_conv.cu"]
 HEADERS = ["bw_prims.cuh", "gdn_common.cuh", "gdn_dev.cuh", "gdn_fwd.h", "gdn_bwd.h", "gdn_host.h", "gdn_l2norm.h", "tmap.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall"]
