@@ -13,7 +13,7 @@
 // Kernels (all bound by memory traffic; two channels per thread, bf16 pairs):
 //   conv_check_kernel      cu_seqlens / init_idx validation into the status word
 //   conv_tails_kernel      every document's tail, documents in order (forks read earlier tails)
-//   conv_fwd_kernel        y over blocks of 128 tokens x 256 channels, a 3-input window in registers
+//   conv_fwd_kernel        y over blocks of 32 tokens x 256 channels, a 3-input window in registers
 //   conv_bwd_kernel        dx, per-block partial sums of dw and dbias, and each document's gradient at
 //                          its three initial inputs (by the block that holds the document's start)
 //   conv_reduce_kernel     dw, dbias from the partial sums in block order (deterministic)
@@ -32,7 +32,7 @@
 namespace gdn {
 namespace {
 
-constexpr int kConvTB = 128;      // tokens per block
+constexpr int kConvTB = 32;       // tokens per block
 constexpr int kConvThreads = 128;  // two channels each: 256 channels per block
 
 struct ConvArgs {
@@ -243,17 +243,25 @@ __global__ void __launch_bounds__(kConvThreads) conv_bwd_kernel(ConvArgs a, cons
   pp[9] = dbb;
 }
 
+// One warp per channel: lane l sums the partials l, l + 32, ... in order, then a fixed shuffle tree
+// (the same order every call: deterministic).
 __global__ void __launch_bounds__(256) conv_reduce_kernel(ConvArgs a, const float* part, int n_tb, float* dw,
                                                           float* dbias) {
   if (conv_failed(a.status)) return;
-  const int c = blockIdx.x * 256 + threadIdx.x;
+  const int c = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   if (c >= a.C) return;
   float s[5] = {0.f, 0.f, 0.f, 0.f, 0.f};
-  for (int b = 0; b < n_tb; ++b)
+  for (int b = lane; b < n_tb; b += 32)
 #pragma unroll
     for (int m = 0; m < 5; ++m) s[m] += part[((size_t)b * a.C + c) * 5 + m];
-  *reinterpret_cast<float4*>(dw + (size_t)c * 4) = make_float4(s[0], s[1], s[2], s[3]);
-  if (dbias) dbias[c] = s[4];
+#pragma unroll
+  for (int m = 0; m < 5; ++m)
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s[m] += __shfl_xor_sync(0xffffffffu, s[m], o);
+  if (lane == 0) {
+    *reinterpret_cast<float4*>(dw + (size_t)c * 4) = make_float4(s[0], s[1], s[2], s[3]);
+    if (dbias) dbias[c] = s[4];
+  }
 }
 
 // One thread per channel, documents in reverse order.
@@ -385,7 +393,7 @@ extern "C" int gdn_conv_bwd(const void* x, const float* w, const float* bias, co
     conv_bwd_kernel<<<dim3(L.n_tb, cb), kConvThreads, 0, s>>>(a, tails, reinterpret_cast<const __nv_bfloat162*>(dy),
                                                                dx, dinit, part);
   }
-  conv_reduce_kernel<<<(C + 255) / 256, 256, 0, s>>>(a, part, L.n_tb, dw, dbias);
+  conv_reduce_kernel<<<(C + 7) / 8, 256, 0, s>>>(a, part, L.n_tb, dw, dbias);
   conv_tails_bwd_kernel<<<(C + 255) / 256, 256, 0, s>>>(a, dfinal_tail, dinit, dtail, dx, dconv_init);
   return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
