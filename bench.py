@@ -410,7 +410,9 @@ def run_ours(args, rank, world, local_rank):
         ctx_b = np.zeros((ctx_n, gdn.NUM_STAGES))
         for i in range(ctx_n):
             flush.zero_()
+            torch.cuda.nvtx.range_push("fwd_inference")  # a marker for profiler filters (no-op otherwise)
             fwd(dataclasses.replace(opts, stage_events=ev_f))
+            torch.cuda.nvtx.range_pop()
             gdn.chunk_bwd(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"], dout,
                           options=dataclasses.replace(opts, stage_events=ev_b), workspace=ws)
             torch.cuda.synchronize()
@@ -646,7 +648,11 @@ def run_ours(args, rank, world, local_rank):
                 "roofline": {"bound": bound_, "achieved": ach, "peak": pk, "unit": "GB/s" if bound_ == "hbm" else
                              "TFLOP/s", "frac": ach / pk, "algorithmic_bytes": fb_inf, "algorithmic_flops": ff_inf,
                              "peak_source": peaks["src"] + (" hbm_gbs" if bound_ == "hbm" else " bf16_tflops")}}
-    res["fwd"] = dict(fwd_object(fwd_exact_ms), mode="exact",
+    fwd_tr = [traffic_record(k_) for k_ in ("kkt_solve_kernel", "chain_kernel<out>")]
+    fwd_traffic = sum(r_["bytes_per_launch"] for r_ in fwd_tr) if all(fwd_tr) else None
+    res["fwd"] = dict(fwd_object(fwd_exact_ms), mode="exact", traffic=fwd_traffic,
+                      traffic_note="DRAM bytes of kkt_solve + the chain output pass (profiles/traffic.json, ncu, "
+                                   "scaled from 16384 tokens), null once either kernel's source has changed",
                       note=f"inference forward alone (o and final state), {T} tokens x {Hv} value heads, median of "
                            f"{fwd_reps} calls with one event pair around each and L2 flushed before it; roofline "
                            f"over the whole call (q, k, v, g, beta read once, o and the final state written once)")
