@@ -29,6 +29,9 @@ namespace gdn {
 constexpr int kChunk = 64;        // tokens per chunk
 constexpr int kDim = 128;         // d_k = d_v
 constexpr int kMinSegChunks = 4;  // shortest automatic segment (chunks)
+// Per-token factors of the inference chain per (chunk, value head): e^{gamma_C - gamma_t} (t < 64),
+// the output factor of token t (64 + t), e^{gamma_C} (128); 144 floats keep records 16-byte aligned.
+constexpr int kFacFloats = 144;
 
 // q and k normalisation (GDN_FLAG_L2NORM_QK): y = x (x . x + kL2NormEps)^{-1/2} per row of 128.
 constexpr float kL2NormEps = 1e-6f;
@@ -99,7 +102,7 @@ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // Forward workspace layout (byte offsets from the workspace base).
 struct FwdLayout {
   size_t header, seq_chunk0, seq_seg0, chunk_seq, chunk_tok0, chunk_len, seg_info, seg_slot, p1_list;
-  size_t flags_seg, flags_fin, mzero, gam, contr, tw, tu, pimg, pub, mmat, bmat, total;
+  size_t flags_seg, flags_fin, mzero, gam, fac, contr, tw, tu, pimg, pub, mmat, bmat, total;
   int64_t cmax, smax, slots;
 };
 
@@ -128,6 +131,7 @@ inline FwdLayout fwd_layout(const PlanDims& d) {
   L.flags_fin = take(sizeof(int32_t) * (size_t)(d.N + 1) * d.Hv);
   L.mzero = take(sizeof(int32_t) * ((size_t)L.slots * d.Hv + 1));
   L.gam = take(sizeof(float) * (size_t)L.cmax * d.Hv * kChunk);
+  L.fac = take(sizeof(float) * (size_t)L.cmax * d.Hv * kFacFloats);
   L.contr = take(sizeof(int32_t) * (size_t)L.cmax * d.Hv);
   L.tw = take((size_t)L.cmax * d.Hv * kChunk * kChunk * 2);
   L.tu = take((size_t)L.cmax * d.Hv * kChunk * kChunk * 2);

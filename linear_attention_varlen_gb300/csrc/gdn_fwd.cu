@@ -10,11 +10,13 @@
 //                     64x64 system per chunk per head) and "Lever 2" (gate cumsum once per chunk;
 //                     one inverse per chunk serves both o and the state recurrence)).
 //   chain_kernel<OUT> persistent over (segment, value head) items in dependency order: the state S
-//                     (fp32, 128x128) lives in registers across 8 warps; per chunk, tcgen05 MMAs compute
-//                     W = T_w K, then [Q~; -W] S + [0; U] (U = T_u V), V' = U - W S,
-//                     S += K^T diag(e^{gamma_C - gamma}) V', O = Q~ S + P V'. A segment starts from the
-//                     state published by the previous one, or from a warm-up from zero when the decay
-//                     in between provably leaves the earlier state below fp32 resolution.
+//                     (fp32, 128x128) lives transposed in registers across 8 warps; per chunk, tcgen05
+//                     MMAs with the value index on the accumulator lanes compute U^T = V^T T_u^T,
+//                     V'^T = U^T - S^T W^T (W^T = K^T T_w^T), S^T += V'_s^T K with V'_s = diag(
+//                     e^{gamma_C - gamma}) V', and O^T = S^T Q^T + V'^T P''^T, the bf16 operands S^T and
+//                     V'^T kept in tensor memory. A segment starts from the state published by the
+//                     previous one, or from a warm-up from zero when the decay in between provably
+//                     leaves the earlier state below fp32 resolution.
 //   chain_kernel<P1>  pass 1 of the exact segment split: per segment, the end state from zero (B) and
 //                     the segment transition (M, started from I) -- or, for a first segment with a known
 //                     start, its end state directly -- so that segment end states can be published as
@@ -376,6 +378,15 @@ __global__ void __launch_bounds__(256, 2) kkt_solve_kernel(const __grid_constant
         if (t >= 32) gam[t] = sc;
         group_sync(grp);
       }
+      if (p.p_factored) {
+        // the inference chain's per-token factors: e^{gamma_C - gamma_t} (V'_s), the output row
+        // factor scale e^{gamma_t} (1 for a row past the cut, whose P'' row is the plain P), e^{gamma_C}
+        float* f = ws_ptr<float>(p, p.L.fac) + rec * kFacFloats;
+        const float gt = gam[t], gC = gam[63];
+        f[t] = __expf(gC - gt);
+        f[64 + t] = gt >= kExactCut ? p.scale * __expf(gt) : 1.f;
+        if (t == 0) f[128] = __expf(gC);
+      }
       const bool factored = gam[63] > kFactorMin;  // gamma is nonincreasing: gam[63] is the minimum
       if (factored) {
         // T = (I + A)^{-1}, column t, with A_rm = (beta_r e^{gamma_r}) (K K^T)_rm e^{-gamma_m} for
@@ -583,10 +594,6 @@ __global__ void __launch_bounds__(256, 2) kkt_solve_kernel(const __grid_constant
 
 enum ChainMode { kModeOut = 0, kModeP1 = 1 };
 
-// TMEM columns of the forward chain.
-constexpr uint32_t kTmD1 = 0;    // [Q~ S + P V' ; U - W S]   (M = 128, 128 cols)
-constexpr uint32_t kTmD2 = 128;  // K^T V's                   (M = 128, 128 cols)
-constexpr uint32_t kTmW = 256;   // W                         (M = 64, 128 cols)
 
 struct ChainCtx {
   uint8_t* base;   // 1024-aligned dynamic shared memory (every layout starts here)
@@ -596,19 +603,6 @@ struct ChainCtx {
   uint32_t ph_ld, ph_mma;
   int tid, warp, lane, q4, half;
 };
-
-// Write this thread's 64 state values (row dk = 32*q4 + lane, columns 64*half ..) as bf16 into sm.s.
-template <class SM>
-__device__ __forceinline__ void store_state_bf16_to(SM& sm, const ChainCtx& cx, const float* S) {
-  const int r = 32 * cx.q4 + cx.lane;
-  uint8_t* blk = sm.s[cx.half];
-#pragma unroll
-  for (int cj = 0; cj < 8; ++cj) {
-    uint4 w = make_uint4(pack_bf16x2(S[8 * cj + 0], S[8 * cj + 1]), pack_bf16x2(S[8 * cj + 2], S[8 * cj + 3]),
-                         pack_bf16x2(S[8 * cj + 4], S[8 * cj + 5]), pack_bf16x2(S[8 * cj + 6], S[8 * cj + 7]));
-    *reinterpret_cast<uint4*>(blk + r * 128 + ((cj ^ (r & 7)) << 4)) = w;
-  }
-}
 
 // Compensated bf16 pair: hi = bf16(a, b), lo = bf16 of what the rounding left out.
 __device__ __forceinline__ float bf16_round(float x) { return __bfloat162float(__float2bfloat16_rn(x)); }
@@ -632,6 +626,19 @@ __device__ __forceinline__ void save_state(const ChainCtx& cx, float* dst, const
   float* row = dst + (size_t)(32 * cx.q4 + cx.lane) * kDim + 64 * cx.half;
   for (int c = 0; c < 64; c += 4) *reinterpret_cast<float4*>(row + c) = make_float4(S[c], S[c + 1], S[c + 2], S[c + 3]);
 }
+// The inference chain keeps S transposed over its epilogue threads: thread (q4, half, lane) holds
+// S(a, b) for b = 32 q4 + lane (its tensor-memory lane) and a = 64 half + c, c < 64. A warp reads
+// and writes 128-byte rows of the row-major state.
+__device__ __forceinline__ void load_state_t(const ChainCtx& cx, const float* src, float* S, bool cg) {
+  const float* col = src + (size_t)(64 * cx.half) * kDim + 32 * cx.q4 + cx.lane;
+#pragma unroll
+  for (int c = 0; c < 64; ++c) S[c] = cg ? __ldcg(col + (size_t)c * kDim) : col[(size_t)c * kDim];
+}
+__device__ __forceinline__ void save_state_t(const ChainCtx& cx, float* dst, const float* S) {
+  float* col = dst + (size_t)(64 * cx.half) * kDim + 32 * cx.q4 + cx.lane;
+#pragma unroll
+  for (int c = 0; c < 64; ++c) col[(size_t)c * kDim] = S[c];
+}
 
 // Shared-memory buffers that affine_apply borrows; at the start of an item every staging buffer
 // of the chain except S hi is idle.
@@ -641,14 +648,18 @@ struct AffineBufs {
   uint32_t mlo_stride;
   uint8_t* slo;         // S_start lo, dv block 0 (block 1 at slo + slo_stride) (B MN-major)
   uint32_t slo_stride;
-  uint8_t* shi;         // S_start hi as staged by the chain: two dv blocks, 16 KB apart
+  uint8_t* shi;         // S_start hi: two blocks, 16 KB apart (staged by the record chain)
   float* stage;         // 32 KB of fp32 staging for the product
 };
 
 // out = M S_start + B (B may be null) on the tensor cores with compensated bf16 operands (x = hi + lo):
-// M hi S hi + M hi S lo + M lo S hi.
+// M hi S hi + M hi S lo + M lo S hi, accumulated in the TMEM columns d_col .. d_col + 127. kT: S is
+// held transposed (the inference chain) and both of its images are written here, K-major (row b,
+// 64 values of a per dk block); otherwise S hi is the chain's staged image and S lo is written
+// MN-major (row a).
+template <bool kT>
 __device__ bool affine_apply(const FwdParams& p, ChainCtx& cx, const AffineBufs& sm, const float* Mm,
-                             const float* Bm, const float* S, float* out) {
+                             const float* Bm, const float* S, float* out, uint32_t d_col) {
   if (cx.tid < 256) {
     // M hi / lo from coalesced loads (16 threads per 512-byte row), four 32-byte pieces in flight
 #pragma unroll
@@ -676,28 +687,35 @@ __device__ bool affine_apply(const FwdParams& p, ChainCtx& cx, const AffineBufs&
             pack_bf16x2(lo[0], lo[1]), pack_bf16x2(lo[2], lo[3]), pack_bf16x2(lo[4], lo[5]), pack_bf16x2(lo[6], lo[7]));
       }
     }
-    // S lo (this thread's row of S_start, 64 columns of dv block `half`)
+    // S lo (and for kT S hi): this thread's 64 values, row rr of the image's block `half`
     const int rr = 32 * cx.q4 + cx.lane;  // (threads below 256 only)
     uint8_t* slo = sm.slo + cx.half * sm.slo_stride;
+    uint8_t* shi = sm.shi + cx.half * 16384;
     for (int cj = 0; cj < 8; ++cj) {
       float lo[8];
       for (int u = 0; u < 8; ++u) lo[u] = S[8 * cj + u] - __bfloat162float(__float2bfloat16_rn(S[8 * cj + u]));
-      *reinterpret_cast<uint4*>(slo + rr * 128 + ((cj ^ (rr & 7)) << 4)) =
-          make_uint4(pack_bf16x2(lo[0], lo[1]), pack_bf16x2(lo[2], lo[3]), pack_bf16x2(lo[4], lo[5]),
-                     pack_bf16x2(lo[6], lo[7]));
+      const uint32_t off = rr * 128 + ((cj ^ (rr & 7)) << 4);
+      *reinterpret_cast<uint4*>(slo + off) = make_uint4(pack_bf16x2(lo[0], lo[1]), pack_bf16x2(lo[2], lo[3]),
+                                                        pack_bf16x2(lo[4], lo[5]), pack_bf16x2(lo[6], lo[7]));
+      if constexpr (kT)
+        *reinterpret_cast<uint4*>(shi + off) =
+            make_uint4(pack_bf16x2(S[8 * cj], S[8 * cj + 1]), pack_bf16x2(S[8 * cj + 2], S[8 * cj + 3]),
+                       pack_bf16x2(S[8 * cj + 4], S[8 * cj + 5]), pack_bf16x2(S[8 * cj + 6], S[8 * cj + 7]));
     }
   }
   sync_generic_to_async();
   if (cx.tid == 0) {
+    // S as the B operand: K-major (kT) or MN-major rows of a
+    auto sdesc = [&](const uint8_t* base, uint32_t stride, int ks) {
+      return kT ? kmajor_desc(smem_u32(base), stride, ks) : mnmajor_desc(smem_u32(base), stride, ks);
+    };
+    const uint32_t id = idesc_bf16(128, 128, 0, kT ? 0 : 1);
     for (int ks = 0; ks < 8; ++ks)
-      umma_bf16(cx.tmem + kTmD2, kmajor_desc(smem_u32(sm.mhi), 16384, ks), mnmajor_desc(smem_u32(sm.shi), 16384, ks),
-                idesc_bf16(128, 128, 0, 1), ks > 0);
+      umma_bf16(cx.tmem + d_col, kmajor_desc(smem_u32(sm.mhi), 16384, ks), sdesc(sm.shi, 16384, ks), id, ks > 0);
     for (int ks = 0; ks < 8; ++ks)
-      umma_bf16(cx.tmem + kTmD2, kmajor_desc(smem_u32(sm.mhi), 16384, ks),
-                mnmajor_desc(smem_u32(sm.slo), sm.slo_stride, ks), idesc_bf16(128, 128, 0, 1), 1);
+      umma_bf16(cx.tmem + d_col, kmajor_desc(smem_u32(sm.mhi), 16384, ks), sdesc(sm.slo, sm.slo_stride, ks), id, 1);
     for (int ks = 0; ks < 8; ++ks)
-      umma_bf16(cx.tmem + kTmD2, kmajor_desc(smem_u32(sm.mlo), sm.mlo_stride, ks),
-                mnmajor_desc(smem_u32(sm.shi), 16384, ks), idesc_bf16(128, 128, 0, 1), 1);
+      umma_bf16(cx.tmem + d_col, kmajor_desc(smem_u32(sm.mlo), sm.mlo_stride, ks), sdesc(sm.shi, 16384, ks), id, 1);
     umma_commit(cx.bar_mma);
   }
   if (!wait_all(cx.bar_mma, cx.ph_mma)) return false;
@@ -714,7 +732,7 @@ __device__ bool affine_apply(const FwdParams& p, ChainCtx& cx, const AffineBufs&
 #pragma unroll
       for (int cc = 0; cc < 64; cc += 16) {
         float v[16];
-        tmem_ld16(cx.tmem + kTmD2 + lane_base + 64 * cx.half + cc, v);
+        tmem_ld16(cx.tmem + d_col + lane_base + 64 * cx.half + cc, v);
         tmem_ld_wait();
 #pragma unroll
         for (int x = 0; x < 4; ++x) {
@@ -755,65 +773,103 @@ __device__ __forceinline__ void prefetch_state_l2(const float* m, int tid, int n
 
 // =========================================================================== warp-specialized chain
 //
-// The forward chain with three roles in one CTA of 10 warps:
-//   warp 8      TMA producer: K, V, P'' (from kkt_solve) and gamma of chunk j into stage j & 1; T_u and
-//               T_w (one buffer each, refilled once their product has read them); Q straight into
-//               rows 64-127 of the stacked operand once the previous chunk's product has read it.
-//   warp 9      MMA issuer (one lane), per chunk j:
-//                 D1 = [T_u; 0] V (issued early: the tensor pipe is idle while the state is
-//                 staged), then D1 += [-W; Q] S (the state product, alone on the critical path), so
-//                 that D1 = [V'; Q S]; chunk j+1's W = T_w K as soon as its operands are in (tested
-//                 without blocking); D2 = K^T V'_s (the state update, committed on its own); then
-//                 D1 += [*; P''] V' for the output.
-//   warps 0-7   epilogue: V' (rows 0-63 of D1), staging of chunk j+1 (-W), S += K^T V'_s, O.
-// The query enters the product unscaled: D1 rows 64-127 = Q S + P'' V' with P''_ij = (Q K^T)_ij
-// e^{-gamma_j}, so O_i = scale e^{gamma_i} (Q S + P'' V')_i. A row whose decay since the chunk
+// The forward chain (inference output pass and pass 1) in transposed form. Every per-chunk product
+// has the value index b (for W^T: the key index a) on the 128 accumulator lanes, so that each
+// epilogue spreads over the four lane quarters of all eight epilogue warps, and the chunk-to-chunk
+// operands S^T, V'^T and V'_s^T stay in tensor memory as bf16 A operands (written by tcgen05.st).
+// Per chunk j of one value head:
+//   W^T  = K^T T_w^T               formed one chunk ahead (A: K; B: T_w)
+//   D_V  = V^T T_u^T               = U^T, issued while the previous state is staged
+//   D_V += S^T (-W^T)              the state product, alone on the critical path: D_V = V'^T
+//   O^T  = S^T Q^T                 then O^T += V'^T P''^T
+//   D_2  = V'_s^T K                V'_s = diag(e^{gamma_C - gamma}) V'
+//   S^T <- e^{gamma_C} S^T + D_2   in fp32 registers, staged as bf16 for the next chunk
+// The query enters unscaled: P''_ij = (Q K^T)_ij e^{-gamma_j}, and O_i = scale e^{gamma_i} (Q S +
+// P'' V')_i with the per-token factors written by kkt_solve. A row whose decay since the chunk
 // start is below kExactCut keeps the plain P and has its query row zeroed instead: its Q S term is
 // below e^{kExactCut} of the chunk-start state (the cut of the exact split's warm-ups).
-// Hand-offs are mbarriers only: tcgen05.commit from the issuer, one elected arrival from the
-// epilogue after a named barrier, TMA transaction counts from the producer. The P'' product adds
-// to rows 0-63 of D1 (V', already read) whatever precedes P'' in shared memory.
+// Roles in one CTA of 10 warps:
+//   warp 8    TMA producer, three lanes with one ring each: A = K, T_w, gamma and the factors
+//             (three slots, since W^T runs a chunk ahead), B = V, T_u (two slots, released by the
+//             U product), C = Q, P'' of the output chunks (two slots).
+//   warp 9    MMA issuer (one lane).
+//   warps 0-7 epilogue: V'^T and V'_s^T into tensor memory, -W^T of the next chunk into shared
+//             memory, the state update, O.
+// Hand-offs are mbarriers only: tcgen05.commit from the issuer, one arrival per epilogue warp,
+// TMA transaction counts from the producer.
 
-struct WsSmem {
-  uint8_t k[2][16384];   // [stage] K rows t, two dk blocks     (B K-major, B MN-major, A MN-major)
-  uint8_t v[2][16384];   // [stage] V rows t, two dv blocks     (B MN-major)
-  uint8_t ostage[2][8192];  // O rows t, two dv blocks (bf16), the source of the TMA store
-  uint8_t pt[4][8192];   // T_u (one buffer), a zero block, P'' stage 0, P'' stage 1: [T_u; 0] and
-                         // [*; P''] are M = 128 operands (contiguous, 1024-aligned)
-  uint8_t tw[8192];      // T diag(beta e^gamma) (one buffer)  (A, M = 64)
-  uint8_t qw[2][16384];  // dk block b: rows 0-63 -W, rows 64-127 Q (TMA)   (A, M = 128)
-  uint8_t vo[2][8192];   // V'                                  (B MN-major)
-  uint8_t vs[2][8192];   // diag(e^{gamma_C - gamma}) V'        (B MN-major)
-  uint8_t s[2][16384];   // S bf16 rows dk                      (B MN-major)
-  float gam[2][64];      // [stage] chunk-local cumulative gate
+// TMEM columns of the chain (512 allocated).
+constexpr uint32_t kTtS = 0;     // S^T bf16 (A operand: lane b, column c holds a = 2c, 2c + 1)    64 cols
+constexpr uint32_t kTtDV = 64;   // D_V = (U - W S)^T fp32 (lane b, column t)                      64 cols
+constexpr uint32_t kTtVp = 128;  // V'^T bf16 (A operand: lane b, column c holds t = 2c, 2c + 1)   32 cols
+constexpr uint32_t kTtVs = 160;  // V'_s^T bf16 (A operand)                                        32 cols
+constexpr uint32_t kTtW = 192;   // W^T fp32 (lane a, column t)                                    64 cols
+constexpr uint32_t kTtD2 = 256;  // D_2 = (K^T V'_s)^T fp32 (lane b, column a)                     128 cols
+constexpr uint32_t kTtO = 384;   // O^T fp32 (lane b, column t), two buffers of 64 columns         128 cols
+
+// bf16 S^T into this thread's lane of the A operand: column 32 half + i holds a = 64 half + 2i, 2i + 1.
+__device__ __forceinline__ void stage_state_t(const ChainCtx& cx, const float* S) {
+  const uint32_t base = cx.tmem + ((uint32_t)(32 * cx.q4) << 16) + kTtS + 32 * cx.half;
+  uint32_t r[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) r[i] = pack_bf16x2(S[2 * i], S[2 * i + 1]);
+  tmem_st16(base, r);
+#pragma unroll
+  for (int i = 0; i < 16; ++i) r[i] = pack_bf16x2(S[32 + 2 * i], S[33 + 2 * i]);
+  tmem_st16(base + 16, r);
+}
+
+constexpr int kRingA = 3;
+struct WtSmem {
+  uint8_t k[kRingA][16384];  // K rows t, two dk blocks      (A MN-major for W^T, B MN-major for D_2)
+  uint8_t tw[kRingA][8192];  // T diag(beta e^gamma) rows t   (B K-major)
+  uint8_t v[2][16384];       // V rows t, two dv blocks      (A MN-major)
+  uint8_t tu[2][8192];       // T diag(beta) rows t           (B K-major)
+  uint8_t q[2][16384];       // Q rows t, two dk blocks      (B K-major)
+  uint8_t pp[2][8192];       // P'' rows t                    (B K-major)
+  uint8_t wn[16384];         // -W^T rows dk, 64 t per row   (B MN-major)
+  uint8_t ostage[2][16384];  // O rows t, two dv blocks (bf16, 128B-swizzled), the source of its TMA store
+  float gam[kRingA][64];     // chunk-local cumulative gate
+  float fac[kRingA][kFacFloats];
 };
 constexpr int kWsThreads = 320;
-// Buffers affine_apply borrows (idle at the start of an item): M hi in the stacked operand, M lo in
-// the two V stages, S_start lo in V' and V'_s (contiguous), the fp32 stage in K. The zero block is
-// not touched.
-__device__ __forceinline__ AffineBufs affine_bufs(WsSmem& sm) {
-  return {sm.qw[0], sm.v[0], 16384u, sm.vo[0], (uint32_t)(sm.vs[0] - sm.vo[0]), sm.s[0],
-          reinterpret_cast<float*>(sm.k[0])};
+// Buffers affine_apply borrows (all idle between chain runs): M hi in K slots 0-1, S_start lo in K
+// slot 2 and the T_w slots, M lo in the V slots, S_start hi in the Q slots, the fp32 stage in the
+// P'' slots and -W^T.
+__device__ __forceinline__ AffineBufs affine_bufs(WtSmem& sm) {
+  return {sm.k[0], sm.v[0], 16384u, sm.k[2], 16384u, sm.q[0], reinterpret_cast<float*>(sm.pp[0])};
 }
-// Zero the zero block once per CTA (nothing writes it afterwards).
-__device__ __forceinline__ void ws_zero_block(WsSmem& sm, int tid, int nthreads) {
-  for (int e = tid; e < 8192 / 16; e += nthreads) reinterpret_cast<uint4*>(sm.pt[1])[e] = make_uint4(0, 0, 0, 0);
+static_assert(offsetof(WtSmem, tw) == offsetof(WtSmem, k) + 3 * 16384, "S lo block 1 follows K slot 2");
+static_assert(offsetof(WtSmem, wn) == offsetof(WtSmem, pp) + 16384, "the fp32 stage spans P'' and -W^T");
+
+struct WtBars {
+  uint64_t full_a[kRingA], empty_a[kRingA], full_b[2], empty_b[2], full_c[2], empty_c[2];
+  uint64_t a_done, pre_done, b_done, o_done, staged, epi1, epi2, o_read[2];
+};
+struct WtPhase {
+  uint32_t full_a[kRingA], empty_a[kRingA], full_b[2], empty_b[2], full_c[2], empty_c[2];
+  uint32_t a_done, pre_done, b_done, o_done, staged, epi1, epi2, o_read[2];
+};
+__device__ __forceinline__ void wt_bars_init(WtBars& bb) {
+  for (int i = 0; i < kRingA; ++i) {
+    mbar_init(&bb.full_a[i], 1);
+    mbar_init(&bb.empty_a[i], 1 + 8);  // the issuer's commit and one arrival per epilogue warp
+  }
+  for (int i = 0; i < 2; ++i) {
+    mbar_init(&bb.full_b[i], 1);
+    mbar_init(&bb.empty_b[i], 1);
+    mbar_init(&bb.full_c[i], 1);
+    mbar_init(&bb.empty_c[i], 1);
+    mbar_init(&bb.o_read[i], 8);
+  }
+  mbar_init(&bb.a_done, 1);
+  mbar_init(&bb.pre_done, 1);
+  mbar_init(&bb.b_done, 1);
+  mbar_init(&bb.o_done, 1);
+  mbar_init(&bb.staged, 8);
+  mbar_init(&bb.epi1, 8);
+  mbar_init(&bb.epi2, 8);
 }
-
-struct WsBars {
-  uint64_t full[3], fullq, fullu, fullo, empty[3], emptyq, qfree, tufree, o_read[2], a_done, pre_done, b_done, o_done,
-      epi1, staged, epi2, vfree;
-};
-struct WsPhase {
-  uint32_t full[3], fullq, fullu, fullo, empty[3], emptyq, qfree, tufree, o_read[2], a_done, pre_done, b_done, o_done,
-      epi1, staged, epi2, vfree;
-};
-// TMEM columns of D1 for chunk j: two accumulators in turn, so that the output of chunk j is
-// read while chunk j + 1 already runs (columns 384-511 hold Q K^T only in the record path).
-__device__ __forceinline__ uint32_t d1_col(int j) { return (j & 1) ? 384u : kTmD1; }
-__device__ __forceinline__ void o_sync() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
-
-__device__ __forceinline__ void e_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
 // Bounded wait that never diverges: after the first failure (recorded in *abort) every later
 // wait returns at once, so all threads keep executing the same barriers.
@@ -822,6 +878,315 @@ __device__ __forceinline__ void role_wait(uint64_t* bar, uint32_t& ph, volatile 
   ph ^= 1;
   tc_fence_after();
 }
+
+// Named barrier of the 256 epilogue threads.
+__device__ __forceinline__ void e_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+
+// One arrival per epilogue warp once the warp's tensor-memory accesses (and, with smem, its
+// shared-memory writes) are ordered before the products that follow.
+__device__ __forceinline__ void warp_handoff(const ChainCtx& cx, bool smem, uint64_t* bar) {
+  if (smem) fence_proxy_async_smem();
+  tc_fence_before();
+  __syncwarp();
+  if (cx.lane == 0) mbar_arrive(bar);
+}
+
+// Run chunks [gc0, gc1) of one document for value head h from S (epilogue registers, transposed
+// layout). Chunks gc >= gc_out write O. kWithU = false runs the transition chain (no U term, no
+// output). All 320 threads call this; returns false after a failed wait.
+template <bool kWithU>
+__device__ bool run_wt(const FwdParams& p, ChainCtx& cx, WtBars& bb, WtPhase& ph, volatile int* abort, float* S,
+                       int gc0, int gc1, int gc_out, int h, int hk) {
+  WtSmem& sm = *reinterpret_cast<WtSmem*>(cx.base);
+  const int n = gc1 - gc0;
+  if (n <= 0) return true;
+  const int Hv = p.d.Hv;
+  const int32_t* ctok = ws_ptr<int32_t>(p, p.L.chunk_tok0);
+  const int32_t* clen = ws_ptr<int32_t>(p, p.L.chunk_len);
+  // the output chunks are the last n - j_out of the run
+  const int j_out = !kWithU ? n : (gc_out <= gc0 ? 0 : (gc_out - gc0 < n ? gc_out - gc0 : n));
+  const int n_out = n - j_out;
+
+  if (cx.warp == 8) {
+    // ------------------------------------------------------------------ TMA producer
+    if (cx.lane == 0) {
+      // ring A: K, T_w, gamma, factors of every chunk
+      for (int j = 0; j < n; ++j) {
+        const int gc = gc0 + j, s = j % kRingA;
+        const size_t r = (size_t)gc * Hv + h;
+        if (j + kRingA < n) {  // chunk j + 3 into L2 while the ring is full
+          const int g3 = gc + kRingA, t3 = ctok[g3];
+          tma_prefetch_3d(&p.tm_k, 0, hk, t3);
+          tma_prefetch_3d(&p.tm_k, 64, hk, t3);
+          bulk_prefetch_l2(p.ws + p.L.tw + ((size_t)g3 * Hv + h) * 8192, 8192);
+        }
+        if (j >= kRingA) role_wait(&bb.empty_a[s], ph.empty_a[s], abort);
+        if (*abort) break;
+        mbar_arrive_expect_tx(&bb.full_a[s], 16384 + 8192 + 256 + kFacFloats * 4);
+        tma_load_3d(sm.k[s], &p.tm_k, 0, hk, ctok[gc], &bb.full_a[s]);
+        tma_load_3d(sm.k[s] + 8192, &p.tm_k, 64, hk, ctok[gc], &bb.full_a[s]);
+        bulk_load(sm.tw[s], p.ws + p.L.tw + r * 8192, 8192, &bb.full_a[s]);
+        bulk_load(sm.gam[s], p.ws + p.L.gam + r * 256, 256, &bb.full_a[s]);
+        bulk_load(sm.fac[s], p.ws + p.L.fac + r * (kFacFloats * 4), kFacFloats * 4, &bb.full_a[s]);
+      }
+      for (int j = (n > kRingA ? n - kRingA : 0); j < n; ++j)
+        role_wait(&bb.empty_a[j % kRingA], ph.empty_a[j % kRingA], abort);
+    } else if (cx.lane == 1 && kWithU) {
+      // ring B: V, T_u of every chunk
+      for (int j = 0; j < n; ++j) {
+        const int gc = gc0 + j, s = j & 1;
+        const size_t r = (size_t)gc * Hv + h;
+        if (j + 2 < n) {
+          const int g2 = gc + 2, t2 = ctok[g2];
+          tma_prefetch_3d(&p.tm_v, 0, h, t2);
+          tma_prefetch_3d(&p.tm_v, 64, h, t2);
+          bulk_prefetch_l2(p.ws + p.L.tu + ((size_t)g2 * Hv + h) * 8192, 8192);
+        }
+        if (j >= 2) role_wait(&bb.empty_b[s], ph.empty_b[s], abort);
+        if (*abort) break;
+        mbar_arrive_expect_tx(&bb.full_b[s], 16384 + 8192);
+        tma_load_3d(sm.v[s], &p.tm_v, 0, h, ctok[gc], &bb.full_b[s]);
+        tma_load_3d(sm.v[s] + 8192, &p.tm_v, 64, h, ctok[gc], &bb.full_b[s]);
+        bulk_load(sm.tu[s], p.ws + p.L.tu + r * 8192, 8192, &bb.full_b[s]);
+      }
+      for (int j = (n > 2 ? n - 2 : 0); j < n; ++j) role_wait(&bb.empty_b[j & 1], ph.empty_b[j & 1], abort);
+    } else if (cx.lane == 2) {
+      // ring C: Q, P'' of the output chunks
+      for (int jc = 0; jc < n_out; ++jc) {
+        const int gc = gc0 + j_out + jc, s = jc & 1;
+        const size_t r = (size_t)gc * Hv + h;
+        if (jc + 2 < n_out) {
+          const int g2 = gc + 2, t2 = ctok[g2];
+          tma_prefetch_3d(&p.tm_q, 0, hk, t2);
+          tma_prefetch_3d(&p.tm_q, 64, hk, t2);
+          bulk_prefetch_l2(p.p_img + ((size_t)g2 * Hv + h) * 8192, 8192);
+        }
+        if (jc >= 2) role_wait(&bb.empty_c[s], ph.empty_c[s], abort);
+        if (*abort) break;
+        mbar_arrive_expect_tx(&bb.full_c[s], 16384 + 8192);
+        tma_load_3d(sm.q[s], &p.tm_q, 0, hk, ctok[gc], &bb.full_c[s]);
+        tma_load_3d(sm.q[s] + 8192, &p.tm_q, 64, hk, ctok[gc], &bb.full_c[s]);
+        bulk_load(sm.pp[s], p.p_img + r * 8192, 8192, &bb.full_c[s]);
+      }
+      for (int jc = (n_out > 2 ? n_out - 2 : 0); jc < n_out; ++jc)
+        role_wait(&bb.empty_c[jc & 1], ph.empty_c[jc & 1], abort);
+    }
+    return !*abort;
+  }
+  if (cx.warp == 9) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (cx.lane == 0) {
+      const uint32_t tm = cx.tmem;
+      const uint32_t id_kt = idesc_bf16(128, 64, 1, 0);   // MN-major A x K-major B: W^T, U^T
+      const uint32_t id_sw = idesc_bf16(128, 64, 0, 1);   // tensor-memory A x MN-major B: S^T (-W^T)
+      const uint32_t id_tk = idesc_bf16(128, 64, 0, 0);   // tensor-memory A x K-major B: S^T Q^T, V'^T P''^T
+      const uint32_t id_d2 = idesc_bf16(128, 128, 0, 1);  // tensor-memory A x MN-major B: V'_s^T K
+      auto prep = [&](int j) {  // W^T of chunk j
+        const int s = j % kRingA;
+        role_wait(&bb.full_a[s], ph.full_a[s], abort);
+        if (*abort) return;
+        const uint32_t ka = smem_u32(sm.k[s]), ta = smem_u32(sm.tw[s]);
+        for (int ks = 0; ks < 4; ++ks)
+          umma_bf16(tm + kTtW, mnmajor_desc(ka, 8192, ks), kmajor_desc(ta, 8192, ks), id_kt, ks > 0);
+        umma_commit(&bb.pre_done);
+      };
+      auto issue_u = [&](int j) {  // U^T of chunk j into D_V (the V' epilogue of chunk j - 1 has read it)
+        const int s = j & 1;
+        role_wait(&bb.full_b[s], ph.full_b[s], abort);
+        if (*abort) return;
+        const uint32_t va = smem_u32(sm.v[s]), ua = smem_u32(sm.tu[s]);
+        for (int ks = 0; ks < 4; ++ks)
+          umma_bf16(tm + kTtDV, mnmajor_desc(va, 8192, ks), kmajor_desc(ua, 8192, ks), id_kt, ks > 0);
+        umma_commit(&bb.empty_b[s]);
+      };
+      prep(0);
+      if (kWithU) issue_u(0);
+      const uint32_t wa = smem_u32(sm.wn);
+      for (int j = 0; j < n && !*abort; ++j) {
+        const int s = j % kRingA;
+        const bool out = j >= j_out;
+        const int so = (j - j_out) & 1;
+        role_wait(&bb.staged, ph.staged, abort);  // -W^T(j) and Q(j) are staged
+        role_wait(&bb.epi2, ph.epi2, abort);      // S^T(j) is staged
+        if (*abort) break;
+        for (int ks = 0; ks < 8; ++ks)
+          umma_bf16_ts(tm + kTtDV, tm + kTtS + 8 * ks, mnmajor_desc(wa, 8192, ks), id_sw, (kWithU || ks > 0) ? 1 : 0);
+        umma_commit(&bb.a_done);
+        if (out) {
+          // Q S while the V' epilogue runs (the output of chunk j - 2 has left this buffer)
+          if (j - j_out >= 2) role_wait(&bb.o_read[so], ph.o_read[so], abort);
+          role_wait(&bb.full_c[so], ph.full_c[so], abort);
+          if (*abort) break;
+          const uint32_t qa = smem_u32(sm.q[so]);
+          for (int ks = 0; ks < 8; ++ks)
+            umma_bf16_ts(tm + kTtO + 64 * so, tm + kTtS + 8 * ks, kmajor_desc(qa, 8192, ks), id_tk, ks > 0);
+        }
+        if (j + 1 < n) {
+          prep(j + 1);  // the epilogue stages -W^T(j + 1) while D_2 runs
+          if (*abort) break;
+        }
+        role_wait(&bb.epi1, ph.epi1, abort);
+        if (*abort) break;
+        const uint32_t ka = smem_u32(sm.k[s]);
+        for (int ks = 0; ks < 4; ++ks)
+          umma_bf16_ts(tm + kTtD2, tm + kTtVs + 8 * ks, mnmajor_desc(ka, 8192, ks), id_d2, ks > 0);
+        umma_commit(&bb.b_done);
+        umma_commit(&bb.empty_a[s]);
+        if (out) {
+          const uint32_t pa = smem_u32(sm.pp[so]);
+          for (int ks = 0; ks < 4; ++ks)
+            umma_bf16_ts(tm + kTtO + 64 * so, tm + kTtVp + 8 * ks, kmajor_desc(pa, 8192, ks), id_tk, 1);
+          umma_commit(&bb.o_done);
+          umma_commit(&bb.empty_c[so]);
+        }
+        if (kWithU && j + 1 < n) issue_u(j + 1);
+      }
+      role_wait(&bb.epi2, ph.epi2, abort);  // the epilogue's last state hand-off
+      // the outputs of the last two chunks have been read (every phase consumed)
+      for (int jc = (n_out > 2 ? n_out - 2 : 0); jc < n_out; ++jc)
+        role_wait(&bb.o_read[jc & 1], ph.o_read[jc & 1], abort);
+    }
+    return !*abort;
+  }
+  // -------------------------------------------------------------------- epilogue warps 0-7
+  const uint32_t lq = (uint32_t)(32 * cx.q4) << 16;
+  const int b = 32 * cx.q4 + cx.lane;  // this thread's lane: the value index (the key index of W^T)
+  stage_state_t(cx, S);
+  tmem_st_wait();
+  warp_handoff(cx, false, &bb.epi2);
+  // -W^T of chunk j into shared memory (row a = this lane, tokens 32 half ..); for an output chunk,
+  // its query rows past the cut zeroed
+  auto staging = [&](int j) {
+    const int s = j % kRingA;
+    role_wait(&bb.pre_done, ph.pre_done, abort);
+    role_wait(&bb.full_a[s], ph.full_a[s], abort);
+    {
+      float w[32];
+      tmem_ld32(cx.tmem + lq + kTtW + 32 * cx.half, w);
+      tmem_ld_wait();
+#pragma unroll
+      for (int c4 = 0; c4 < 4; ++c4) {
+        const int cj = 4 * cx.half + c4;
+        const float* x = w + 8 * c4;
+        *reinterpret_cast<uint4*>(sm.wn + b * 128 + ((cj ^ (b & 7)) << 4)) =
+            make_uint4(pack_bf16x2(-x[0], -x[1]), pack_bf16x2(-x[2], -x[3]), pack_bf16x2(-x[4], -x[5]),
+                       pack_bf16x2(-x[6], -x[7]));
+      }
+    }
+    if (j >= j_out) {
+      const int so = (j - j_out) & 1;
+      role_wait(&bb.full_c[so], ph.full_c[so], abort);
+      const float* gm = sm.gam[s];
+      if (gm[63] < kExactCut) {  // gamma is nonincreasing: zero the query rows past the cut
+        for (int e = cx.tid; e < 2 * 64 * 8; e += 256) {
+          const int blk = e >> 9, r = (e >> 3) & 63, cj = e & 7;
+          if (gm[r] < kExactCut)
+            *reinterpret_cast<uint4*>(sm.q[so] + blk * 8192 + r * 128 + (cj << 4)) = make_uint4(0, 0, 0, 0);
+        }
+      }
+    }
+    warp_handoff(cx, true, &bb.staged);
+  };
+  staging(0);
+  for (int j = 0; j < n; ++j) {
+    const int gc = gc0 + j, s = j % kRingA;
+    const bool out = j >= j_out;
+    const int so = (j - j_out) & 1;
+    const float* fc = sm.fac[s];  // e^{gamma_C - gamma_t} [0, 64), output factors [64, 128), e^{gamma_C}
+    role_wait(&bb.a_done, ph.a_done, abort);
+    {
+      // V' of this lane's value index, tokens 32 half ..: V'^T and V'_s^T as bf16 A operands
+      float v[32];
+      tmem_ld32(cx.tmem + lq + kTtDV + 32 * cx.half, v);
+      tmem_ld_wait();
+      uint32_t rp[16], rs[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const float2 sc = *reinterpret_cast<const float2*>(fc + 32 * cx.half + 2 * i);
+        rp[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+        rs[i] = pack_bf16x2(v[2 * i] * sc.x, v[2 * i + 1] * sc.y);
+      }
+      tmem_st16(cx.tmem + lq + kTtVp + 16 * cx.half, rp);
+      tmem_st16(cx.tmem + lq + kTtVs + 16 * cx.half, rs);
+      tmem_st_wait();
+    }
+    warp_handoff(cx, false, &bb.epi1);
+    if (j + 1 < n) staging(j + 1);
+    role_wait(&bb.b_done, ph.b_done, abort);
+    {
+      const float GC = fc[128];
+#pragma unroll
+      for (int hc = 0; hc < 2; ++hc) {
+        float d[32];
+        tmem_ld32(cx.tmem + lq + kTtD2 + 64 * cx.half + 32 * hc, d);
+        tmem_ld_wait();
+#pragma unroll
+        for (int x = 0; x < 32; ++x) S[32 * hc + x] = GC * S[32 * hc + x] + d[x];
+      }
+      stage_state_t(cx, S);
+      tmem_st_wait();
+    }
+    warp_handoff(cx, false, &bb.epi2);
+    if (out) {
+      // O of chunk j while chunk j + 1 runs: O^T (lane b, tokens 32 half ..) is turned into rows of
+      // O in a 128B-swizzled shared tile (lane pairs swap one value per token pair, so that each
+      // 4-byte store holds two neighbouring values of b) and leaves by one TMA store; a partial
+      // chunk (the end of a document) is copied row by row so that the next document's rows are not
+      // touched
+      role_wait(&bb.o_done, ph.o_done, abort);
+      float o[32];
+      tmem_ld32(cx.tmem + lq + kTtO + 64 * so + 32 * cx.half, o);
+      tmem_ld_wait();
+      warp_handoff(cx, false, &bb.o_read[so]);
+      uint8_t* stg = sm.ostage[so];
+      if (cx.tid == 0) bulk_wait_read_all();  // earlier stores have read their tiles
+      e_sync();
+      const bool odd = cx.lane & 1;
+      const int be = b & ~1;  // the even value index of the pair
+      const uint32_t blk = (uint32_t)(be >> 6) * 8192, c = (uint32_t)(be & 63) >> 3, e2 = (uint32_t)(be & 7) * 2;
+#pragma unroll
+      for (int m = 0; m < 16; ++m) {
+        // tokens t0 and t0 + 4 (rows four apart keep the two halves of a warp's store on
+        // different banks); the even lane stores row t0, the odd lane row t0 + 4
+        const int i0 = 8 * (m >> 2) + (m & 3), t0 = 32 * cx.half + i0;
+        const float x0 = o[i0] * fc[64 + t0], x1 = o[i0 + 4] * fc[68 + t0];
+        const float got = __shfl_xor_sync(0xffffffffu, odd ? x0 : x1, 1);
+        const int t = odd ? t0 + 4 : t0;
+        const uint32_t v = odd ? pack_bf16x2(got, x1) : pack_bf16x2(x0, got);
+        *reinterpret_cast<uint32_t*>(stg + blk + t * 128 + ((c ^ (t & 7)) << 4) + e2) = v;
+      }
+      fence_proxy_async_smem();
+      e_sync();
+      const int nn = clen[gc];
+      if (nn == kChunk) {
+        if (cx.tid == 0) {
+          tma_store_3d(&p.tm_o, stg, 0, h, ctok[gc]);
+          tma_store_3d(&p.tm_o, stg + 8192, 64, h, ctok[gc]);
+          bulk_commit_group();
+        }
+      } else {
+        for (int e = cx.tid; e < nn * 16; e += 256) {
+          const int t = e >> 4, u = e & 15, cj = u & 7;
+          reinterpret_cast<uint4*>(p.out + ((size_t)(ctok[gc] + t) * Hv + h) * kDim)[u] =
+              *reinterpret_cast<const uint4*>(stg + (u >> 3) * 8192 + t * 128 + ((cj ^ (t & 7)) << 4));
+        }
+      }
+    }
+    __syncwarp();
+    if (cx.lane == 0) mbar_arrive(&bb.empty_a[s]);  // gamma and the factors of chunk j are read
+  }
+  if (cx.tid == 0) bulk_wait_all();  // every output store has landed before the tiles are reused
+  return !*abort;
+}
+
+// ----------------------------------------------------------------- barriers of the record chain
+struct WsBars {
+  uint64_t full[3], fullq, fullu, empty[3], emptyq, a_done, pre_done, b_done, epi1, staged, epi2, vfree;
+};
+struct WsPhase {
+  uint32_t full[3], fullq, fullu, empty[3], emptyq, a_done, pre_done, b_done, epi1, staged, epi2, vfree;
+};
+
 
 // Epilogue hand-off: make this thread's shared-memory writes visible to the async proxy and its
 // TMEM reads ordered, meet the other epilogue threads, then one thread arrives on each barrier.
@@ -833,311 +1198,6 @@ __device__ __forceinline__ void e_handoff(int tid, uint64_t* b1, uint64_t* b2 = 
     mbar_arrive(b1);
     if (b2) mbar_arrive(b2);
   }
-}
-
-// Run chunks [gc0, gc1) of one document for value head h from S (epilogue registers; its bf16
-// copy is already in sm.s). Chunks gc >= gc_out write O. kWithU = false runs the transition
-// chain (no U term, no output). All 320 threads call this; returns false after a failed wait.
-template <bool kWithU>
-__device__ bool run_ws(const FwdParams& p, ChainCtx& cx, WsBars& bb, WsPhase& ph, volatile int* abort, float* S,
-                       int gc0, int gc1, int gc_out, int h, int hk) {
-  WsSmem& sm = *reinterpret_cast<WsSmem*>(cx.base);
-  const int n = gc1 - gc0;
-  if (n <= 0) return true;
-  const int Hv = p.d.Hv;
-  const int32_t* ctok = ws_ptr<int32_t>(p, p.L.chunk_tok0);
-  const int32_t* clen = ws_ptr<int32_t>(p, p.L.chunk_len);
-  auto is_out = [&](int j) { return gc0 + j >= gc_out; };
-
-  if (cx.warp == 8) {
-    // ------------------------------------------------------------------ TMA producer
-    if (cx.lane == 0) {
-      for (int j = 0; j < n; ++j) {
-        const int gc = gc0 + j, st = j & 1, tok0 = ctok[gc];
-        const bool out = is_out(j);
-        const size_t r = (size_t)gc * Hv + h;
-        if (j + 2 < n) {  // chunk j + 2 into L2 while its stage is still in use
-          const int g2 = gc + 2, t2 = ctok[g2];
-          const size_t r2 = (size_t)g2 * Hv + h;
-          tma_prefetch_3d(&p.tm_k, 0, hk, t2);
-          tma_prefetch_3d(&p.tm_k, 64, hk, t2);
-          bulk_prefetch_l2(p.ws + p.L.gam + r2 * 256, 256);
-          bulk_prefetch_l2(p.ws + p.L.tw + r2 * 8192, 8192);
-          if (kWithU) {
-            tma_prefetch_3d(&p.tm_v, 0, h, t2);
-            tma_prefetch_3d(&p.tm_v, 64, h, t2);
-            bulk_prefetch_l2(p.ws + p.L.tu + r2 * 8192, 8192);
-          }
-          if (g2 >= gc_out) {
-            tma_prefetch_3d(&p.tm_q, 0, hk, t2);
-            tma_prefetch_3d(&p.tm_q, 64, hk, t2);
-            bulk_prefetch_l2(p.p_img + r2 * 8192, 8192);
-          }
-        }
-        if (j >= 2) role_wait(&bb.empty[st], ph.empty[st], abort);
-        if (*abort) break;
-        mbar_arrive_expect_tx(&bb.full[st], 16384 + 256 + (kWithU ? 16384 : 0) + (out ? 8192 : 0));
-        if (out) bulk_load(sm.pt[2 + st], p.p_img + r * 8192, 8192, &bb.full[st]);
-        tma_load_3d(sm.k[st], &p.tm_k, 0, hk, tok0, &bb.full[st]);
-        tma_load_3d(sm.k[st] + 8192, &p.tm_k, 64, hk, tok0, &bb.full[st]);
-        bulk_load(sm.gam[st], p.ws + p.L.gam + r * 256, 256, &bb.full[st]);
-        if (kWithU) {
-          tma_load_3d(sm.v[st], &p.tm_v, 0, h, tok0, &bb.full[st]);
-          tma_load_3d(sm.v[st] + 8192, &p.tm_v, 64, h, tok0, &bb.full[st]);
-          if (j >= 1) role_wait(&bb.tufree, ph.tufree, abort);  // the previous U product has read T_u
-          if (*abort) break;
-          mbar_arrive_expect_tx(&bb.fullu, 8192);
-          bulk_load(sm.pt[0], p.ws + p.L.tu + r * 8192, 8192, &bb.fullu);
-        }
-        if (j >= 1) role_wait(&bb.emptyq, ph.emptyq, abort);  // the previous W product has read T_w
-        if (*abort) break;
-        mbar_arrive_expect_tx(&bb.fullq, 8192);
-        bulk_load(sm.tw, p.ws + p.L.tw + r * 8192, 8192, &bb.fullq);
-        if (out) {
-          // Q into rows 64-127 of the stacked operand once the product of chunk j - 1 has read it
-          if (j >= 1) role_wait(&bb.qfree, ph.qfree, abort);
-          if (*abort) break;
-          mbar_arrive_expect_tx(&bb.fullo, 16384);
-          tma_load_3d(sm.qw[0] + 8192, &p.tm_q, 0, hk, tok0, &bb.fullo);
-          tma_load_3d(sm.qw[1] + 8192, &p.tm_q, 64, hk, tok0, &bb.fullo);
-        }
-      }
-      // drain: wait for the release of the last uses so that every phase is consumed
-      for (int j = (n >= 2 ? n - 2 : 0); j < n; ++j) role_wait(&bb.empty[j & 1], ph.empty[j & 1], abort);
-      role_wait(&bb.emptyq, ph.emptyq, abort);
-      if (kWithU) role_wait(&bb.tufree, ph.tufree, abort);
-    }
-    return !*abort;
-  }
-  if (cx.warp == 9) {
-    // ------------------------------------------------------------------ MMA issuer
-    if (cx.lane == 0) {
-      const uint32_t tm = cx.tmem;
-      auto prep = [&](int j) {
-        const int st = j & 1;
-        const uint32_t k0 = smem_u32(sm.k[st]);
-        for (int ks = 0; ks < 4; ++ks)
-          umma_bf16(tm + kTmW, kmajor_desc(smem_u32(sm.tw), 8192, ks), mnmajor_desc(k0, 8192, ks),
-                    idesc_bf16(64, 128, 0, 1), ks > 0);
-        umma_commit(&bb.pre_done);
-        umma_commit(&bb.emptyq);
-      };
-      role_wait(&bb.full[0], ph.full[0], abort);
-      role_wait(&bb.fullq, ph.fullq, abort);
-      if (!*abort) prep(0);
-      for (int j = 0; j < n && !*abort; ++j) {
-        const int st = j & 1;
-        const bool out = is_out(j);
-        const uint32_t d1 = tm + d1_col(j);
-        if (kWithU) {
-          // U = T_u V into rows 0-63 of D1 (rows 64-127 get zero) once the output of chunk j - 2 has
-          // left these columns; V(j) came with the stage prep(j) waited for. One o_read barrier per
-          // D1 buffer: the read of chunk j - 1 goes to the other one, so this wait is never two
-          // phases behind.
-          role_wait(&bb.fullu, ph.fullu, abort);
-          if (j >= 2 && is_out(j - 2)) role_wait(&bb.o_read[st], ph.o_read[st], abort);
-          if (*abort) break;
-          for (int ks = 0; ks < 4; ++ks)
-            umma_bf16(d1, kmajor_desc(smem_u32(sm.pt[0]), 16384, ks), mnmajor_desc(smem_u32(sm.v[st]), 8192, ks),
-                      idesc_bf16(128, 128, 0, 1), ks > 0);
-          umma_commit(&bb.tufree);
-        }
-        role_wait(&bb.staged, ph.staged, abort);
-        role_wait(&bb.epi2, ph.epi2, abort);
-        if (*abort) break;
-        for (int ks = 0; ks < 8; ++ks)
-          umma_bf16(d1, kmajor_desc(smem_u32(sm.qw[0]), 16384, ks), mnmajor_desc(smem_u32(sm.s[0]), 16384, ks),
-                    idesc_bf16(128, 128, 0, 1), (kWithU || ks > 0) ? 1 : 0);
-        umma_commit(&bb.a_done);
-        if (j + 1 < n && is_out(j + 1)) umma_commit(&bb.qfree);  // the producer may load Q(j + 1)
-        // chunk j + 1's W now if its operands are in (the tensor pipe is idle during the V' epilogue),
-        // else after the state update
-        bool next_prepped = false;
-        if (j + 1 < n && mbar_test(&bb.full[st ^ 1], ph.full[st ^ 1]) && mbar_test(&bb.fullq, ph.fullq)) {
-          role_wait(&bb.full[st ^ 1], ph.full[st ^ 1], abort);
-          role_wait(&bb.fullq, ph.fullq, abort);
-          prep(j + 1);
-          next_prepped = true;
-        }
-        role_wait(&bb.epi1, ph.epi1, abort);
-        if (*abort) break;
-        for (int ks = 0; ks < 4; ++ks)
-          umma_bf16(tm + kTmD2, mnmajor_desc(smem_u32(sm.k[st]), 8192, ks), mnmajor_desc(smem_u32(sm.vs[0]), 8192, ks),
-                    idesc_bf16(128, 128, 1, 1), ks > 0);
-        umma_commit(&bb.b_done);
-        if (out) {
-          for (int ks = 0; ks < 4; ++ks)
-            umma_bf16(d1, kmajor_desc(smem_u32(sm.pt[1 + st]), 16384, ks), mnmajor_desc(smem_u32(sm.vo[0]), 8192, ks),
-                      idesc_bf16(128, 128, 0, 1), 1);
-          umma_commit(&bb.o_done);
-        }
-        umma_commit(&bb.empty[st]);
-        if (j + 1 < n && !next_prepped) {
-          role_wait(&bb.full[st ^ 1], ph.full[st ^ 1], abort);
-          role_wait(&bb.fullq, ph.fullq, abort);
-          if (*abort) break;
-          prep(j + 1);
-        }
-      }
-      role_wait(&bb.epi2, ph.epi2, abort);  // the epilogue's last state hand-off
-      // the outputs of the last two chunks have been read (every phase consumed)
-      if (kWithU)
-        for (int j = (n >= 2 ? n - 2 : 0); j < n; ++j)
-          if (is_out(j)) role_wait(&bb.o_read[j & 1], ph.o_read[j & 1], abort);
-    }
-    return !*abort;
-  }
-  // -------------------------------------------------------------------- epilogue warps 0-7
-  const uint32_t lane_base = (uint32_t)(32 * cx.q4) << 16;
-  e_handoff(cx.tid, &bb.epi2);  // S(gc0) is staged
-  auto staging = [&](int j) {
-    const int st = j & 1;
-    role_wait(&bb.full[st], ph.full[st], abort);
-    role_wait(&bb.pre_done, ph.pre_done, abort);
-    {
-      // all 32 lanes: rows r0 = 16 q4 + lane / 4 and r0 + 8 of W (M = 64) go to rows r of the
-      // stacked operand, column pairs
-      const int c2 = 2 * (cx.lane & 3), r0 = 16 * cx.q4 + (cx.lane >> 2);
-#pragma unroll
-      for (int hc = 0; hc < 2; ++hc) {
-        float v[16];
-        tmem_ld16x256_x4(cx.tmem + kTmW + lane_base + 64 * cx.half + 32 * hc, v);
-        tmem_ld_wait();
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int c = 32 * hc + 8 * k + c2;
-          *reinterpret_cast<uint32_t*>(sm.qw[cx.half] + sw128_pair(r0, c)) = pack_bf16x2(-v[4 * k], -v[4 * k + 1]);
-          *reinterpret_cast<uint32_t*>(sm.qw[cx.half] + sw128_pair(r0 + 8, c)) =
-              pack_bf16x2(-v[4 * k + 2], -v[4 * k + 3]);
-        }
-      }
-    }
-    if (is_out(j)) {
-      role_wait(&bb.fullo, ph.fullo, abort);  // Q(j) is in rows 64-127
-      const float* gm = sm.gam[st];
-      if (gm[63] < kExactCut) {  // gamma is nonincreasing: zero the query rows past the cut
-        for (int e = cx.tid; e < 2 * 64 * 8; e += 256) {
-          const int b = e >> 9, r = (e >> 3) & 63, cj = e & 7;
-          if (gm[r] < kExactCut)
-            *reinterpret_cast<uint4*>(sm.qw[b] + 8192 + r * 128 + (cj << 4)) = make_uint4(0, 0, 0, 0);
-        }
-      }
-    }
-    e_handoff(cx.tid, &bb.staged);
-  };
-  staging(0);
-  for (int j = 0; j < n; ++j) {
-    const int gc = gc0 + j, st = j & 1;
-    const bool out = is_out(j);
-    role_wait(&bb.a_done, ph.a_done, abort);
-    const float* gm = sm.gam[st];
-    const float gC = gm[63];
-    // this thread's output row factor (read before the stage is released)
-    float of = 0.f;
-    if (out && cx.q4 >= 2) {
-      const float gt = gm[32 * (cx.q4 - 2) + cx.lane];
-      of = gt >= kExactCut ? p.scale * __expf(gt) : 1.f;
-    }
-    if (cx.q4 < 2) {
-      // V' = U - W S, rows t = lanes 0-63
-      const int t = 32 * cx.q4 + cx.lane;
-      const float sc = __expf(gC - gm[t]);
-#pragma unroll
-      for (int hc = 0; hc < 2; ++hc) {
-        float v[32];
-        tmem_ld16(cx.tmem + d1_col(j) + lane_base + 64 * cx.half + 32 * hc, v);
-        tmem_ld16(cx.tmem + d1_col(j) + lane_base + 64 * cx.half + 32 * hc + 16, v + 16);
-        tmem_ld_wait();
-#pragma unroll
-        for (int cj4 = 0; cj4 < 4; ++cj4) {
-          const int cj = 4 * hc + cj4;
-          const uint32_t off = t * 128 + ((cj ^ (t & 7)) << 4);
-          const float* x = v + 8 * cj4;
-          *reinterpret_cast<uint4*>(sm.vo[cx.half] + off) =
-              make_uint4(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]), pack_bf16x2(x[4], x[5]), pack_bf16x2(x[6], x[7]));
-          *reinterpret_cast<uint4*>(sm.vs[cx.half] + off) =
-              make_uint4(pack_bf16x2(x[0] * sc, x[1] * sc), pack_bf16x2(x[2] * sc, x[3] * sc),
-                         pack_bf16x2(x[4] * sc, x[5] * sc), pack_bf16x2(x[6] * sc, x[7] * sc));
-        }
-      }
-    }
-    // the epilogue reads nothing of stage st after this point (gamma is in registers): release it
-    // here, so that chunk j + 2's loads go out as soon as the issuer's last product has read it
-    e_handoff(cx.tid, &bb.epi1, &bb.empty[st]);
-    if (j + 1 < n) staging(j + 1);
-    role_wait(&bb.b_done, ph.b_done, abort);
-    {
-      const float GC = __expf(gC);
-#pragma unroll
-      for (int hc = 0; hc < 2; ++hc) {
-        float v[32];
-        tmem_ld16(cx.tmem + kTmD2 + lane_base + 64 * cx.half + 32 * hc, v);
-        tmem_ld16(cx.tmem + kTmD2 + lane_base + 64 * cx.half + 32 * hc + 16, v + 16);
-        tmem_ld_wait();
-#pragma unroll
-        for (int x = 0; x < 32; ++x) S[32 * hc + x] = GC * S[32 * hc + x] + v[x];
-      }
-      store_state_bf16_to(sm, cx, S);
-    }
-    e_handoff(cx.tid, &bb.epi2);
-    // O of chunk j (rows 64-127 of D1[j], warps of lane quadrants 2-3), while chunk j + 1 runs:
-    // a whole chunk goes out by TMA store from a shared-memory stage, a partial one (the end of a
-    // document) row by row so that the next document's rows are not touched
-    if (out && cx.q4 >= 2) {
-      role_wait(&bb.o_done, ph.o_done, abort);
-      const int t = 32 * (cx.q4 - 2) + cx.lane;
-      const int nn = clen[gc];
-      if (nn == kChunk) {
-        if (cx.tid == 64) bulk_wait_read_all();  // the previous store has read the stage
-        o_sync();
-      }
-      float v[64];
-#pragma unroll
-      for (int hc = 0; hc < 2; ++hc) {
-        tmem_ld16(cx.tmem + d1_col(j) + lane_base + 64 * cx.half + 32 * hc, v + 32 * hc);
-        tmem_ld16(cx.tmem + d1_col(j) + lane_base + 64 * cx.half + 32 * hc + 16, v + 32 * hc + 16);
-      }
-      tmem_ld_wait();
-      // these TMEM columns may take the U product of chunk j + 2 from here on
-      tc_fence_before();
-      o_sync();
-      if (kWithU && cx.tid == 64) mbar_arrive(&bb.o_read[st]);
-#pragma unroll
-      for (int x = 0; x < 64; ++x) v[x] *= of;
-#pragma unroll
-      for (int hc = 0; hc < 2; ++hc) {
-        if (nn == kChunk) {
-#pragma unroll
-          for (int cj4 = 0; cj4 < 4; ++cj4) {
-            const int cj = 4 * hc + cj4;
-            const float* x = v + 32 * hc + 8 * cj4;
-            *reinterpret_cast<uint4*>(sm.ostage[cx.half] + t * 128 + ((cj ^ (t & 7)) << 4)) =
-                make_uint4(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]), pack_bf16x2(x[4], x[5]),
-                           pack_bf16x2(x[6], x[7]));
-          }
-        } else if (t < nn) {
-          uint4* dst = reinterpret_cast<uint4*>(p.out + ((size_t)(ctok[gc] + t) * Hv + h) * kDim + 64 * cx.half);
-#pragma unroll
-          for (int cj4 = 0; cj4 < 4; ++cj4) {
-            const float* x = v + 32 * hc + 8 * cj4;
-            dst[4 * hc + cj4] = make_uint4(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]), pack_bf16x2(x[4], x[5]),
-                                           pack_bf16x2(x[6], x[7]));
-          }
-        }
-      }
-      if (nn == kChunk) {
-        fence_proxy_async_smem();
-        o_sync();
-        if (cx.tid == 64) {
-          tma_store_3d(&p.tm_o, sm.ostage[0], 0, h, ctok[gc]);
-          tma_store_3d(&p.tm_o, sm.ostage[1], 64, h, ctok[gc]);
-          bulk_commit_group();
-        }
-      }
-    }
-  }
-  if (cx.tid == 64) bulk_wait_all();  // every output store has landed before the buffers are reused
-  return !*abort;
 }
 
 // ============================================================== warp-specialized record chain
@@ -1168,7 +1228,7 @@ struct RecSmem {
   uint8_t vslo[2][8192];  // V'_s lo
   float gam[kRecStages][64];  // [stage] chunk-local cumulative gate
 };
-constexpr size_t kSmemBytes = (sizeof(WsSmem) > sizeof(RecSmem) ? sizeof(WsSmem) : sizeof(RecSmem)) + 1024;
+constexpr size_t kSmemBytes = (sizeof(WtSmem) > sizeof(RecSmem) ? sizeof(WtSmem) : sizeof(RecSmem)) + 1024;
 static_assert(kSmemBytes <= 232448, "chain shared memory");
 __device__ __forceinline__ AffineBufs affine_bufs(RecSmem& sm) {
   return {sm.wn[0], sm.k[0], 16384u, sm.slo[0], 16384u, sm.s[0], reinterpret_cast<float*>(sm.tu[0])};
@@ -1433,10 +1493,11 @@ template <int kMode, bool kRec>
 __global__ void __launch_bounds__(kWsThreads, 1) chain_kernel(const __grid_constant__ FwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = smem_align1024(smem_raw);
-  WsSmem* wss = reinterpret_cast<WsSmem*>(base);
+  WtSmem* wts = reinterpret_cast<WtSmem*>(base);
   RecSmem* rss = reinterpret_cast<RecSmem*>(base);
   __shared__ uint64_t bar_ld, bar_mma;
-  __shared__ WsBars wbars;
+  __shared__ WsBars wbars;  // record chain
+  __shared__ WtBars tbars;  // inference chain
   __shared__ uint32_t tmem_holder;
   __shared__ int s_item, s_ok, s_abort;
   Header* hd = ws_ptr<Header>(p, p.L.header);
@@ -1455,6 +1516,8 @@ __global__ void __launch_bounds__(kWsThreads, 1) chain_kernel(const __grid_const
   const bool epi = cx.warp < 8;  // threads that hold state rows
   WsPhase ph;
   memset(&ph, 0, sizeof(ph));
+  WtPhase tph;
+  memset(&tph, 0, sizeof(tph));
   const int Hv = p.d.Hv, G = p.d.Hv / p.d.Hk;
   const int n_items = (kMode == kModeOut ? hd->n_segs : hd->n_p1) * Hv;
   if (blockIdx.x >= n_items || get_status(hd) != 0) return;
@@ -1502,33 +1565,30 @@ __global__ void __launch_bounds__(kWsThreads, 1) chain_kernel(const __grid_const
   if (cx.tid == 0) {
     mbar_init(&bar_ld, 1);
     mbar_init(&bar_mma, 1);
-    mbar_init(&wbars.full[0], 1);
-    mbar_init(&wbars.full[1], 1);
-    mbar_init(&wbars.full[2], 1);
-    mbar_init(&wbars.fullq, 1);
-    mbar_init(&wbars.fullu, 1);
-    mbar_init(&wbars.fullo, 1);
-    mbar_init(&wbars.qfree, 1);
-    mbar_init(&wbars.tufree, 1);
-    mbar_init(&wbars.o_read[0], 1);
-    mbar_init(&wbars.o_read[1], 1);
-    mbar_init(&wbars.o_done, 1);
-    mbar_init(&wbars.empty[0], 2);
-    mbar_init(&wbars.empty[1], 2);
-    mbar_init(&wbars.empty[2], 2);
-    mbar_init(&wbars.emptyq, 1);
-    mbar_init(&wbars.a_done, 1);
-    mbar_init(&wbars.pre_done, 1);
-    mbar_init(&wbars.b_done, 1);
-    mbar_init(&wbars.epi1, 1);
-    mbar_init(&wbars.staged, 1);
-    mbar_init(&wbars.epi2, 1);
-    mbar_init(&wbars.vfree, 1);
+    if constexpr (kRec) {
+      mbar_init(&wbars.full[0], 1);
+      mbar_init(&wbars.full[1], 1);
+      mbar_init(&wbars.full[2], 1);
+      mbar_init(&wbars.fullq, 1);
+      mbar_init(&wbars.fullu, 1);
+      mbar_init(&wbars.empty[0], 2);
+      mbar_init(&wbars.empty[1], 2);
+      mbar_init(&wbars.empty[2], 2);
+      mbar_init(&wbars.emptyq, 1);
+      mbar_init(&wbars.a_done, 1);
+      mbar_init(&wbars.pre_done, 1);
+      mbar_init(&wbars.b_done, 1);
+      mbar_init(&wbars.epi1, 1);
+      mbar_init(&wbars.staged, 1);
+      mbar_init(&wbars.epi2, 1);
+      mbar_init(&wbars.vfree, 1);
+    } else {
+      wt_bars_init(tbars);
+    }
     s_abort = 0;
     fence_mbar_init();
   }
   if (cx.warp == 0) tmem_alloc(&tmem_holder, 512);
-  if constexpr (!kRec) ws_zero_block(*wss, cx.tid, kWsThreads);
   sync_generic_to_async();
   cx.tmem = tmem_holder;
 
@@ -1537,18 +1597,29 @@ __global__ void __launch_bounds__(kWsThreads, 1) chain_kernel(const __grid_const
   int* mzero = ws_ptr<int>(p, p.L.mzero);
   const size_t st_elems = (size_t)kDim * kDim;
   float S[64];
+  // the record chain reads S from shared-memory images staged here; the inference chain stages
+  // its tensor-memory operand itself at the start of every run
   auto store_s = [&]() {
-    if (epi) {
-      if constexpr (rec)
-        store_state_comp(*rss, cx, S);
-      else
-        store_state_bf16_to(*wss, cx, S);
-    }
+    if constexpr (rec)
+      if (epi) store_state_comp(*rss, cx, S);
+  };
+  auto ld_state = [&](const float* src, bool cg) {
+    if constexpr (rec)
+      load_state(cx, src, S, cg);
+    else
+      load_state_t(cx, src, S, cg);
+  };
+  auto sv_state = [&](float* dst) {
+    if constexpr (rec)
+      save_state(cx, dst, S);
+    else
+      save_state_t(cx, dst, S);
   };
   auto set_zero = [&]() {
     for (int c = 0; c < 64; ++c) S[c] = 0.f;
   };
   auto set_identity = [&]() {
+    // row-block layout (record chain): thread row a = 32 q4 + lane; transposed: column b = 32 q4 + lane
     const int r = 32 * cx.q4 + cx.lane;
     for (int c = 0; c < 64; ++c) S[c] = (r == 64 * cx.half + c) ? 1.f : 0.f;
   };
@@ -1572,18 +1643,18 @@ __global__ void __launch_bounds__(kWsThreads, 1) chain_kernel(const __grid_const
       }
     } else {
       if (with_u)
-        run_ws<true>(p, cx, wbars, ph, &s_abort, S, g0, g1, g_out, h, hk);
+        run_wt<true>(p, cx, tbars, tph, &s_abort, S, g0, g1, g_out, h, hk);
       else
-        run_ws<false>(p, cx, wbars, ph, &s_abort, S, g0, g1, g_out, h, hk);
+        run_wt<false>(p, cx, tbars, tph, &s_abort, S, g0, g1, g_out, h, hk);
     }
     __syncthreads();
     return s_abort == 0;
   };
   auto affine = [&](const float* Mm, const float* Bm, float* out) -> bool {
     if constexpr (rec)
-      return affine_apply(p, cx, affine_bufs(*rss), Mm, Bm, S, out);
+      return affine_apply<false>(p, cx, affine_bufs(*rss), Mm, Bm, S, out, kRtV);
     else
-      return affine_apply(p, cx, affine_bufs(*wss), Mm, Bm, S, out);
+      return affine_apply<true>(p, cx, affine_bufs(*wts), Mm, Bm, S, out, kTtD2);
   };
 
   for (;;) {
@@ -1620,7 +1691,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) chain_kernel(const __grid_const
         sync_generic_to_async();
         if (!run_fast(c0 + nch - w, c0 + nch, c0 + nch, h, hk, false)) break;
         m_zero = all_zero();
-        if (epi) save_state(cx, mdst, S);
+        if (epi) sv_state(mdst);
         if (!m_zero && w < nch) {
           set_identity();
           store_s();
@@ -1640,7 +1711,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) chain_kernel(const __grid_const
         } else {
           const int x = p.init_idx ? p.init_idx[seq] : -1;
           if (epi && x >= 0 && x < p.d.n_init)
-            load_state(cx, p.initial_state + ((size_t)x * Hv + h) * st_elems, S, false);
+            ld_state(p.initial_state + ((size_t)x * Hv + h) * st_elems, false);
           else
             set_zero();
         }
@@ -1648,7 +1719,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) chain_kernel(const __grid_const
         sync_generic_to_async();
         if (!run_fast(c0, c0 + nch, c0 + nch, h, hk, true)) break;
         float* dst = (part == 1) ? ws_ptr<float>(p, p.L.bmat) : ws_ptr<float>(p, p.L.pub);
-        if (epi) save_state(cx, dst + ((size_t)sl * Hv + h) * st_elems, S);
+        if (epi) sv_state(dst + ((size_t)sl * Hv + h) * st_elems);
       }
       // A transition that is exactly zero makes the segment's end state its local end state B:
       // the next segment can start without waiting for this segment's start state.
@@ -1678,7 +1749,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) chain_kernel(const __grid_const
     if (dep == -1) {
       const int x = p.init_idx ? p.init_idx[seq] : -1;
       if (epi && x >= 0 && x < p.d.n_init)
-        load_state(cx, p.initial_state + ((size_t)x * Hv + h) * st_elems, S, false);
+        ld_state(p.initial_state + ((size_t)x * Hv + h) * st_elems, false);
       else
         set_zero();
     } else if (dep <= -2) {
@@ -1689,7 +1760,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) chain_kernel(const __grid_const
       }
       __syncthreads();
       have_start = s_ok != 0;
-      if (have_start && epi) load_state(cx, p.final_state + ((size_t)j * Hv + h) * st_elems, S, true);
+      if (have_start && epi) ld_state(p.final_state + ((size_t)j * Hv + h) * st_elems, true);
     } else if (p.d.mode == 0) {
       const int dsl = slot[dep];
       if (wb >= 0) {
@@ -1698,7 +1769,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) chain_kernel(const __grid_const
         set_zero();
       } else if (__ldcg(&mzero[dsl * Hv + h])) {
         // the previous segment's transition is exactly zero: its end state is its local B
-        if (epi) load_state(cx, ws_ptr<float>(p, p.L.bmat) + ((size_t)dsl * Hv + h) * st_elems, S, true);
+        if (epi) ld_state(ws_ptr<float>(p, p.L.bmat) + ((size_t)dsl * Hv + h) * st_elems, true);
       } else {
         if (cx.tid == 0) {
           s_ok = wait_flag(&flags_seg[dep * Hv + h], hd, p.flag_budget) ? 1 : 0;
@@ -1707,7 +1778,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) chain_kernel(const __grid_const
         __syncthreads();
         have_start = s_ok != 0;
         if (have_start && epi)
-          load_state(cx, ws_ptr<float>(p, p.L.pub) + ((size_t)dsl * Hv + h) * st_elems, S, true);
+          ld_state(ws_ptr<float>(p, p.L.pub) + ((size_t)dsl * Hv + h) * st_elems, true);
       }
     } else {
       // truncation: fewest preceding whole chunks of this document whose summed log-decay is
@@ -1728,7 +1799,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) chain_kernel(const __grid_const
         if (d0 == -1) {
           const int x = p.init_idx ? p.init_idx[seq] : -1;
           if (epi && x >= 0 && x < p.d.n_init)
-            load_state(cx, p.initial_state + ((size_t)x * Hv + h) * st_elems, S, false);
+            ld_state(p.initial_state + ((size_t)x * Hv + h) * st_elems, false);
         } else {
           const int j = dep_fork_seq(d0);
           if (cx.tid == 0) {
@@ -1737,7 +1808,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) chain_kernel(const __grid_const
           }
           __syncthreads();
           have_start = s_ok != 0;
-          if (have_start && epi) load_state(cx, p.final_state + ((size_t)j * Hv + h) * st_elems, S, true);
+          if (have_start && epi) ld_state(p.final_state + ((size_t)j * Hv + h) * st_elems, true);
         }
       }
     }
@@ -1770,7 +1841,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) chain_kernel(const __grid_const
       break;
     }
     if (last) {
-      if (epi) save_state(cx, p.final_state + ((size_t)seq * Hv + h) * st_elems, S);
+      if (epi) sv_state(p.final_state + ((size_t)seq * Hv + h) * st_elems);
       if (!p.withhold_fin)
         publish(&flags_fin[seq * Hv + h]);
       else
