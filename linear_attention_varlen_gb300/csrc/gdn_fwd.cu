@@ -871,10 +871,20 @@ __device__ __forceinline__ void wt_bars_init(WtBars& bb) {
   mbar_init(&bb.epi2, 8);
 }
 
-// Bounded wait that never diverges: after the first failure (recorded in *abort) every later
-// wait returns at once, so all threads keep executing the same barriers.
+// Bounded wait that never diverges: a phase that is already complete costs one try_wait; otherwise
+// the thread polls until the phase completes, the budget runs out or another role has given up
+// (recorded in *abort), so all threads keep executing the same barriers and none waits for a
+// phase that an aborted role will not complete.
 __device__ __forceinline__ void role_wait(uint64_t* bar, uint32_t& ph, volatile int* abort) {
-  if (!*abort && !mbar_wait(bar, ph, kWaitBudget)) *abort = 1;
+  if (!mbar_try_wait(bar, ph)) {
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, ph)) {
+      if (*abort || clock64() - t0 > kWaitBudget) {
+        *abort = 1;
+        break;
+      }
+    }
+  }
   ph ^= 1;
   tc_fence_after();
 }
@@ -977,65 +987,72 @@ __device__ bool run_wt(const FwdParams& p, ChainCtx& cx, WtBars& bb, WtPhase& ph
     // ------------------------------------------------------------------ MMA issuer
     if (cx.lane == 0) {
       const uint32_t tm = cx.tmem;
-      const uint32_t id_kt = idesc_bf16(128, 64, 1, 0);   // MN-major A x K-major B: W^T, U^T
-      const uint32_t id_sw = idesc_bf16(128, 64, 0, 1);   // tensor-memory A x MN-major B: S^T (-W^T)
-      const uint32_t id_tk = idesc_bf16(128, 64, 0, 0);   // tensor-memory A x K-major B: S^T Q^T, V'^T P''^T
-      const uint32_t id_d2 = idesc_bf16(128, 128, 0, 1);  // tensor-memory A x MN-major B: V'_s^T K
+      constexpr uint32_t id_kt = idesc_bf16(128, 64, 1, 0);   // MN-major A x K-major B: W^T, U^T
+      constexpr uint32_t id_sw = idesc_bf16(128, 64, 0, 1);   // tensor-memory A x MN-major B: S^T (-W^T)
+      constexpr uint32_t id_tk = idesc_bf16(128, 64, 0, 0);   // tensor-memory A x K-major B: S^T Q^T, V'^T P''^T
+      constexpr uint32_t id_d2 = idesc_bf16(128, 128, 0, 1);  // tensor-memory A x MN-major B: V'_s^T K
+      // k-step-0 descriptors of slot 0 of every operand (the buffers do not move; a slot s of a ring
+      // adds s times its size to the start-address field, which never carries out of it): the issue
+      // loop only adds constants
+      const uint64_t d_k = mnmajor_desc(smem_u32(sm.k[0]), 8192, 0);    // slots 16 KB apart
+      const uint64_t d_tw = kmajor_desc(smem_u32(sm.tw[0]), 8192, 0);   // 8 KB
+      const uint64_t d_v = mnmajor_desc(smem_u32(sm.v[0]), 8192, 0);    // 16 KB
+      const uint64_t d_tu = kmajor_desc(smem_u32(sm.tu[0]), 8192, 0);   // 8 KB
+      const uint64_t d_q = kmajor_desc(smem_u32(sm.q[0]), 8192, 0);     // 16 KB
+      const uint64_t d_pp = kmajor_desc(smem_u32(sm.pp[0]), 8192, 0);   // 8 KB
+      const uint64_t d_wn = mnmajor_desc(smem_u32(sm.wn), 8192, 0);
       auto prep = [&](int j) {  // W^T of chunk j
         const int s = j % kRingA;
         role_wait(&bb.full_a[s], ph.full_a[s], abort);
-        if (*abort) return;
-        const uint32_t ka = smem_u32(sm.k[s]), ta = smem_u32(sm.tw[s]);
+        const uint64_t ka = d_k + (uint64_t)(s * (16384 >> 4)), ta = d_tw + (uint64_t)(s * (8192 >> 4));
+#pragma unroll
         for (int ks = 0; ks < 4; ++ks)
-          umma_bf16(tm + kTtW, mnmajor_desc(ka, 8192, ks), kmajor_desc(ta, 8192, ks), id_kt, ks > 0);
+          umma_bf16(tm + kTtW, mnmajor_step(ka, ks), kmajor_step(ta, 8192, ks), id_kt, ks > 0);
         umma_commit(&bb.pre_done);
       };
       auto issue_u = [&](int j) {  // U^T of chunk j into D_V (the V' epilogue of chunk j - 1 has read it)
         const int s = j & 1;
         role_wait(&bb.full_b[s], ph.full_b[s], abort);
-        if (*abort) return;
-        const uint32_t va = smem_u32(sm.v[s]), ua = smem_u32(sm.tu[s]);
+        const uint64_t va = d_v + (uint64_t)(s * (16384 >> 4)), ua = d_tu + (uint64_t)(s * (8192 >> 4));
+#pragma unroll
         for (int ks = 0; ks < 4; ++ks)
-          umma_bf16(tm + kTtDV, mnmajor_desc(va, 8192, ks), kmajor_desc(ua, 8192, ks), id_kt, ks > 0);
+          umma_bf16(tm + kTtDV, mnmajor_step(va, ks), kmajor_step(ua, 8192, ks), id_kt, ks > 0);
         umma_commit(&bb.empty_b[s]);
       };
       prep(0);
       if (kWithU) issue_u(0);
-      const uint32_t wa = smem_u32(sm.wn);
       for (int j = 0; j < n && !*abort; ++j) {
         const int s = j % kRingA;
         const bool out = j >= j_out;
         const int so = (j - j_out) & 1;
         role_wait(&bb.staged, ph.staged, abort);  // -W^T(j) and Q(j) are staged
         role_wait(&bb.epi2, ph.epi2, abort);      // S^T(j) is staged
-        if (*abort) break;
+#pragma unroll
         for (int ks = 0; ks < 8; ++ks)
-          umma_bf16_ts(tm + kTtDV, tm + kTtS + 8 * ks, mnmajor_desc(wa, 8192, ks), id_sw, (kWithU || ks > 0) ? 1 : 0);
+          umma_bf16_ts(tm + kTtDV, tm + kTtS + 8 * ks, mnmajor_step(d_wn, ks), id_sw, (kWithU || ks > 0) ? 1 : 0);
         umma_commit(&bb.a_done);
         if (out) {
           // Q S while the V' epilogue runs (the output of chunk j - 2 has left this buffer)
           if (j - j_out >= 2) role_wait(&bb.o_read[so], ph.o_read[so], abort);
           role_wait(&bb.full_c[so], ph.full_c[so], abort);
-          if (*abort) break;
-          const uint32_t qa = smem_u32(sm.q[so]);
+          const uint64_t qa = d_q + (uint64_t)(so * (16384 >> 4));
+#pragma unroll
           for (int ks = 0; ks < 8; ++ks)
-            umma_bf16_ts(tm + kTtO + 64 * so, tm + kTtS + 8 * ks, kmajor_desc(qa, 8192, ks), id_tk, ks > 0);
+            umma_bf16_ts(tm + kTtO + 64 * so, tm + kTtS + 8 * ks, kmajor_step(qa, 8192, ks), id_tk, ks > 0);
         }
-        if (j + 1 < n) {
-          prep(j + 1);  // the epilogue stages -W^T(j + 1) while D_2 runs
-          if (*abort) break;
-        }
+        if (j + 1 < n) prep(j + 1);  // the epilogue stages -W^T(j + 1) while D_2 runs
         role_wait(&bb.epi1, ph.epi1, abort);
-        if (*abort) break;
-        const uint32_t ka = smem_u32(sm.k[s]);
+        const uint64_t ka = d_k + (uint64_t)(s * (16384 >> 4));
+#pragma unroll
         for (int ks = 0; ks < 4; ++ks)
-          umma_bf16_ts(tm + kTtD2, tm + kTtVs + 8 * ks, mnmajor_desc(ka, 8192, ks), id_d2, ks > 0);
+          umma_bf16_ts(tm + kTtD2, tm + kTtVs + 8 * ks, mnmajor_step(ka, ks), id_d2, ks > 0);
         umma_commit(&bb.b_done);
         umma_commit(&bb.empty_a[s]);
         if (out) {
-          const uint32_t pa = smem_u32(sm.pp[so]);
+          const uint64_t pa = d_pp + (uint64_t)(so * (8192 >> 4));
+#pragma unroll
           for (int ks = 0; ks < 4; ++ks)
-            umma_bf16_ts(tm + kTtO + 64 * so, tm + kTtVp + 8 * ks, kmajor_desc(pa, 8192, ks), id_tk, 1);
+            umma_bf16_ts(tm + kTtO + 64 * so, tm + kTtVp + 8 * ks, kmajor_step(pa, 8192, ks), id_tk, 1);
           umma_commit(&bb.o_done);
           umma_commit(&bb.empty_c[so]);
         }
@@ -1141,6 +1158,17 @@ __device__ bool run_wt(const FwdParams& p, ChainCtx& cx, WtBars& bb, WtPhase& ph
       uint8_t* stg = sm.ostage[so];
       if (cx.tid == 0) bulk_wait_read_all();  // earlier stores have read their tiles
       e_sync();
+      // the output factors of this thread's 32 tokens, in registers before any store to the tile
+      // (the stores could otherwise alias them and serialize the loop)
+      float of[32];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const float4 f4 = *reinterpret_cast<const float4*>(fc + 64 + 32 * cx.half + 4 * q);
+        of[4 * q] = f4.x;
+        of[4 * q + 1] = f4.y;
+        of[4 * q + 2] = f4.z;
+        of[4 * q + 3] = f4.w;
+      }
       const bool odd = cx.lane & 1;
       const int be = b & ~1;  // the even value index of the pair
       const uint32_t blk = (uint32_t)(be >> 6) * 8192, c = (uint32_t)(be & 63) >> 3, e2 = (uint32_t)(be & 7) * 2;
@@ -1149,7 +1177,7 @@ __device__ bool run_wt(const FwdParams& p, ChainCtx& cx, WtBars& bb, WtPhase& ph
         // tokens t0 and t0 + 4 (rows four apart keep the two halves of a warp's store on
         // different banks); the even lane stores row t0, the odd lane row t0 + 4
         const int i0 = 8 * (m >> 2) + (m & 3), t0 = 32 * cx.half + i0;
-        const float x0 = o[i0] * fc[64 + t0], x1 = o[i0 + 4] * fc[68 + t0];
+        const float x0 = o[i0] * of[i0], x1 = o[i0 + 4] * of[i0 + 4];
         const float got = __shfl_xor_sync(0xffffffffu, odd ? x0 : x1, 1);
         const int t = odd ? t0 + 4 : t0;
         const uint32_t v = odd ? pack_bf16x2(got, x1) : pack_bf16x2(x0, got);
