@@ -846,9 +846,11 @@ struct WtBars {
   uint64_t full_a[kRingA], empty_a[kRingA], full_b[2], empty_b[2], full_c[2], empty_c[2];
   uint64_t a_done, pre_done, b_done, o_done, staged, epi1, epi2, o_read[2];
 };
-struct WtPhase {
-  uint32_t full_a[kRingA], empty_a[kRingA], full_b[2], empty_b[2], full_c[2], empty_c[2];
-  uint32_t a_done, pre_done, b_done, o_done, staged, epi1, epi2, o_read[2];
+// Phase parities of these barriers as the bits of one register (slots indexed at run time would
+// otherwise put them in local memory).
+enum WtBit : int {
+  kBitFullA = 0, kBitEmptyA = 3, kBitFullB = 6, kBitEmptyB = 8, kBitFullC = 10, kBitEmptyC = 12, kBitADone = 14,
+  kBitPreDone = 15, kBitBDone = 16, kBitODone = 17, kBitStaged = 18, kBitEpi1 = 19, kBitEpi2 = 20, kBitORead = 21
 };
 __device__ __forceinline__ void wt_bars_init(WtBars& bb) {
   for (int i = 0; i < kRingA; ++i) {
@@ -892,6 +894,22 @@ __device__ __forceinline__ void role_wait(uint64_t* bar, uint32_t& ph, volatile 
 // Named barrier of the 256 epilogue threads.
 __device__ __forceinline__ void e_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
+// role_wait on the parity bit `bit` of ph.
+__device__ __forceinline__ void bit_wait(uint64_t* bar, uint32_t& ph, int bit, volatile int* abort) {
+  const uint32_t par = (ph >> bit) & 1u;
+  if (!mbar_try_wait(bar, par)) {
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, par)) {
+      if (*abort || clock64() - t0 > kWaitBudget) {
+        *abort = 1;
+        break;
+      }
+    }
+  }
+  ph ^= 1u << bit;
+  tc_fence_after();
+}
+
 // One arrival per epilogue warp once the warp's tensor-memory accesses (and, with smem, its
 // shared-memory writes) are ordered before the products that follow.
 __device__ __forceinline__ void warp_handoff(const ChainCtx& cx, bool smem, uint64_t* bar) {
@@ -905,7 +923,7 @@ __device__ __forceinline__ void warp_handoff(const ChainCtx& cx, bool smem, uint
 // layout). Chunks gc >= gc_out write O. kWithU = false runs the transition chain (no U term, no
 // output). All 320 threads call this; returns false after a failed wait.
 template <bool kWithU>
-__device__ bool run_wt(const FwdParams& p, ChainCtx& cx, WtBars& bb, WtPhase& ph, volatile int* abort, float* S,
+__device__ bool run_wt(const FwdParams& p, ChainCtx& cx, WtBars& bb, uint32_t& ph, volatile int* abort, float* S,
                        int gc0, int gc1, int gc_out, int h, int hk) {
   WtSmem& sm = *reinterpret_cast<WtSmem*>(cx.base);
   const int n = gc1 - gc0;
@@ -930,7 +948,7 @@ __device__ bool run_wt(const FwdParams& p, ChainCtx& cx, WtBars& bb, WtPhase& ph
           tma_prefetch_3d(&p.tm_k, 64, hk, t3);
           bulk_prefetch_l2(p.ws + p.L.tw + ((size_t)g3 * Hv + h) * 8192, 8192);
         }
-        if (j >= kRingA) role_wait(&bb.empty_a[s], ph.empty_a[s], abort);
+        if (j >= kRingA) bit_wait(&bb.empty_a[s], ph, kBitEmptyA + (s), abort);
         if (*abort) break;
         mbar_arrive_expect_tx(&bb.full_a[s], 16384 + 8192 + 256 + kFacFloats * 4);
         tma_load_3d(sm.k[s], &p.tm_k, 0, hk, ctok[gc], &bb.full_a[s]);
@@ -940,7 +958,7 @@ __device__ bool run_wt(const FwdParams& p, ChainCtx& cx, WtBars& bb, WtPhase& ph
         bulk_load(sm.fac[s], p.ws + p.L.fac + r * (kFacFloats * 4), kFacFloats * 4, &bb.full_a[s]);
       }
       for (int j = (n > kRingA ? n - kRingA : 0); j < n; ++j)
-        role_wait(&bb.empty_a[j % kRingA], ph.empty_a[j % kRingA], abort);
+        bit_wait(&bb.empty_a[j % kRingA], ph, kBitEmptyA + (j % kRingA), abort);
     } else if (cx.lane == 1 && kWithU) {
       // ring B: V, T_u of every chunk
       for (int j = 0; j < n; ++j) {
@@ -952,14 +970,14 @@ __device__ bool run_wt(const FwdParams& p, ChainCtx& cx, WtBars& bb, WtPhase& ph
           tma_prefetch_3d(&p.tm_v, 64, h, t2);
           bulk_prefetch_l2(p.ws + p.L.tu + ((size_t)g2 * Hv + h) * 8192, 8192);
         }
-        if (j >= 2) role_wait(&bb.empty_b[s], ph.empty_b[s], abort);
+        if (j >= 2) bit_wait(&bb.empty_b[s], ph, kBitEmptyB + (s), abort);
         if (*abort) break;
         mbar_arrive_expect_tx(&bb.full_b[s], 16384 + 8192);
         tma_load_3d(sm.v[s], &p.tm_v, 0, h, ctok[gc], &bb.full_b[s]);
         tma_load_3d(sm.v[s] + 8192, &p.tm_v, 64, h, ctok[gc], &bb.full_b[s]);
         bulk_load(sm.tu[s], p.ws + p.L.tu + r * 8192, 8192, &bb.full_b[s]);
       }
-      for (int j = (n > 2 ? n - 2 : 0); j < n; ++j) role_wait(&bb.empty_b[j & 1], ph.empty_b[j & 1], abort);
+      for (int j = (n > 2 ? n - 2 : 0); j < n; ++j) bit_wait(&bb.empty_b[j & 1], ph, kBitEmptyB + (j & 1), abort);
     } else if (cx.lane == 2) {
       // ring C: Q, P'' of the output chunks
       for (int jc = 0; jc < n_out; ++jc) {
@@ -971,7 +989,7 @@ __device__ bool run_wt(const FwdParams& p, ChainCtx& cx, WtBars& bb, WtPhase& ph
           tma_prefetch_3d(&p.tm_q, 64, hk, t2);
           bulk_prefetch_l2(p.p_img + ((size_t)g2 * Hv + h) * 8192, 8192);
         }
-        if (jc >= 2) role_wait(&bb.empty_c[s], ph.empty_c[s], abort);
+        if (jc >= 2) bit_wait(&bb.empty_c[s], ph, kBitEmptyC + (s), abort);
         if (*abort) break;
         mbar_arrive_expect_tx(&bb.full_c[s], 16384 + 8192);
         tma_load_3d(sm.q[s], &p.tm_q, 0, hk, ctok[gc], &bb.full_c[s]);
@@ -979,7 +997,7 @@ __device__ bool run_wt(const FwdParams& p, ChainCtx& cx, WtBars& bb, WtPhase& ph
         bulk_load(sm.pp[s], p.p_img + r * 8192, 8192, &bb.full_c[s]);
       }
       for (int jc = (n_out > 2 ? n_out - 2 : 0); jc < n_out; ++jc)
-        role_wait(&bb.empty_c[jc & 1], ph.empty_c[jc & 1], abort);
+        bit_wait(&bb.empty_c[jc & 1], ph, kBitEmptyC + (jc & 1), abort);
     }
     return !*abort;
   }
@@ -1003,7 +1021,7 @@ __device__ bool run_wt(const FwdParams& p, ChainCtx& cx, WtBars& bb, WtPhase& ph
       const uint64_t d_wn = mnmajor_desc(smem_u32(sm.wn), 8192, 0);
       auto prep = [&](int j) {  // W^T of chunk j
         const int s = j % kRingA;
-        role_wait(&bb.full_a[s], ph.full_a[s], abort);
+        bit_wait(&bb.full_a[s], ph, kBitFullA + (s), abort);
         const uint64_t ka = d_k + (uint64_t)(s * (16384 >> 4)), ta = d_tw + (uint64_t)(s * (8192 >> 4));
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
@@ -1012,7 +1030,7 @@ __device__ bool run_wt(const FwdParams& p, ChainCtx& cx, WtBars& bb, WtPhase& ph
       };
       auto issue_u = [&](int j) {  // U^T of chunk j into D_V (the V' epilogue of chunk j - 1 has read it)
         const int s = j & 1;
-        role_wait(&bb.full_b[s], ph.full_b[s], abort);
+        bit_wait(&bb.full_b[s], ph, kBitFullB + (s), abort);
         const uint64_t va = d_v + (uint64_t)(s * (16384 >> 4)), ua = d_tu + (uint64_t)(s * (8192 >> 4));
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
@@ -1025,23 +1043,23 @@ __device__ bool run_wt(const FwdParams& p, ChainCtx& cx, WtBars& bb, WtPhase& ph
         const int s = j % kRingA;
         const bool out = j >= j_out;
         const int so = (j - j_out) & 1;
-        role_wait(&bb.staged, ph.staged, abort);  // -W^T(j) and Q(j) are staged
-        role_wait(&bb.epi2, ph.epi2, abort);      // S^T(j) is staged
+        bit_wait(&bb.staged, ph, kBitStaged, abort);  // -W^T(j) and Q(j) are staged
+        bit_wait(&bb.epi2, ph, kBitEpi2, abort);      // S^T(j) is staged
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks)
           umma_bf16_ts(tm + kTtDV, tm + kTtS + 8 * ks, mnmajor_step(d_wn, ks), id_sw, (kWithU || ks > 0) ? 1 : 0);
         umma_commit(&bb.a_done);
         if (out) {
           // Q S while the V' epilogue runs (the output of chunk j - 2 has left this buffer)
-          if (j - j_out >= 2) role_wait(&bb.o_read[so], ph.o_read[so], abort);
-          role_wait(&bb.full_c[so], ph.full_c[so], abort);
+          if (j - j_out >= 2) bit_wait(&bb.o_read[so], ph, kBitORead + (so), abort);
+          bit_wait(&bb.full_c[so], ph, kBitFullC + (so), abort);
           const uint64_t qa = d_q + (uint64_t)(so * (16384 >> 4));
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks)
             umma_bf16_ts(tm + kTtO + 64 * so, tm + kTtS + 8 * ks, kmajor_step(qa, 8192, ks), id_tk, ks > 0);
         }
         if (j + 1 < n) prep(j + 1);  // the epilogue stages -W^T(j + 1) while D_2 runs
-        role_wait(&bb.epi1, ph.epi1, abort);
+        bit_wait(&bb.epi1, ph, kBitEpi1, abort);
         const uint64_t ka = d_k + (uint64_t)(s * (16384 >> 4));
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
@@ -1058,10 +1076,10 @@ __device__ bool run_wt(const FwdParams& p, ChainCtx& cx, WtBars& bb, WtPhase& ph
         }
         if (kWithU && j + 1 < n) issue_u(j + 1);
       }
-      role_wait(&bb.epi2, ph.epi2, abort);  // the epilogue's last state hand-off
+      bit_wait(&bb.epi2, ph, kBitEpi2, abort);  // the epilogue's last state hand-off
       // the outputs of the last two chunks have been read (every phase consumed)
       for (int jc = (n_out > 2 ? n_out - 2 : 0); jc < n_out; ++jc)
-        role_wait(&bb.o_read[jc & 1], ph.o_read[jc & 1], abort);
+        bit_wait(&bb.o_read[jc & 1], ph, kBitORead + (jc & 1), abort);
     }
     return !*abort;
   }
@@ -1075,8 +1093,8 @@ __device__ bool run_wt(const FwdParams& p, ChainCtx& cx, WtBars& bb, WtPhase& ph
   // its query rows past the cut zeroed
   auto staging = [&](int j) {
     const int s = j % kRingA;
-    role_wait(&bb.pre_done, ph.pre_done, abort);
-    role_wait(&bb.full_a[s], ph.full_a[s], abort);
+    bit_wait(&bb.pre_done, ph, kBitPreDone, abort);
+    bit_wait(&bb.full_a[s], ph, kBitFullA + (s), abort);
     {
       float w[32];
       tmem_ld32(cx.tmem + lq + kTtW + 32 * cx.half, w);
@@ -1092,7 +1110,7 @@ __device__ bool run_wt(const FwdParams& p, ChainCtx& cx, WtBars& bb, WtPhase& ph
     }
     if (j >= j_out) {
       const int so = (j - j_out) & 1;
-      role_wait(&bb.full_c[so], ph.full_c[so], abort);
+      bit_wait(&bb.full_c[so], ph, kBitFullC + (so), abort);
       const float* gm = sm.gam[s];
       if (gm[63] < kExactCut) {  // gamma is nonincreasing: zero the query rows past the cut
         for (int e = cx.tid; e < 2 * 64 * 8; e += 256) {
@@ -1110,7 +1128,7 @@ __device__ bool run_wt(const FwdParams& p, ChainCtx& cx, WtBars& bb, WtPhase& ph
     const bool out = j >= j_out;
     const int so = (j - j_out) & 1;
     const float* fc = sm.fac[s];  // e^{gamma_C - gamma_t} [0, 64), output factors [64, 128), e^{gamma_C}
-    role_wait(&bb.a_done, ph.a_done, abort);
+    bit_wait(&bb.a_done, ph, kBitADone, abort);
     {
       // V' of this lane's value index, tokens 32 half ..: V'^T and V'_s^T as bf16 A operands
       float v[32];
@@ -1129,7 +1147,7 @@ __device__ bool run_wt(const FwdParams& p, ChainCtx& cx, WtBars& bb, WtPhase& ph
     }
     warp_handoff(cx, false, &bb.epi1);
     if (j + 1 < n) staging(j + 1);
-    role_wait(&bb.b_done, ph.b_done, abort);
+    bit_wait(&bb.b_done, ph, kBitBDone, abort);
     {
       const float GC = fc[128];
 #pragma unroll
@@ -1150,7 +1168,7 @@ __device__ bool run_wt(const FwdParams& p, ChainCtx& cx, WtBars& bb, WtPhase& ph
       // 4-byte store holds two neighbouring values of b) and leaves by one TMA store; a partial
       // chunk (the end of a document) is copied row by row so that the next document's rows are not
       // touched
-      role_wait(&bb.o_done, ph.o_done, abort);
+      bit_wait(&bb.o_done, ph, kBitODone, abort);
       float o[32];
       tmem_ld32(cx.tmem + lq + kTtO + 64 * so + 32 * cx.half, o);
       tmem_ld_wait();
@@ -1544,8 +1562,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) chain_kernel(const __grid_const
   const bool epi = cx.warp < 8;  // threads that hold state rows
   WsPhase ph;
   memset(&ph, 0, sizeof(ph));
-  WtPhase tph;
-  memset(&tph, 0, sizeof(tph));
+  uint32_t tph = 0;  // phase bits of the inference chain's barriers
   const int Hv = p.d.Hv, G = p.d.Hv / p.d.Hk;
   const int n_items = (kMode == kModeOut ? hd->n_segs : hd->n_p1) * Hv;
   if (blockIdx.x >= n_items || get_status(hd) != 0) return;
