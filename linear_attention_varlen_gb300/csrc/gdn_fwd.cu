@@ -788,11 +788,12 @@ __device__ __forceinline__ void prefetch_state_l2(const float* m, int tid, int n
 // P'' V')_i with the per-token factors written by kkt_solve. A row whose decay since the chunk
 // start is below kExactCut keeps the plain P and has its query row zeroed instead: its Q S term is
 // below e^{kExactCut} of the chunk-start state (the cut of the exact split's warm-ups).
-// Roles in one CTA of 10 warps:
+// Roles in one CTA of 11 warps:
 //   warp 8    TMA producer, three lanes with one ring each: A = K, T_w, gamma and the factors
 //             (three slots, since W^T runs a chunk ahead), B = V, T_u (two slots, released by the
 //             U product), C = Q, P'' of the output chunks (two slots).
-//   warp 9    MMA issuer (one lane).
+//   warp 9    MMA issuer of the two state products (one lane).
+//   warp 10   MMA issuer of W^T, U^T, Q S and P'' V' (one lane).
 //   warps 0-7 epilogue: V'^T and V'_s^T into tensor memory, -W^T of the next chunk into shared
 //             memory, the state update, O.
 // Hand-offs are mbarriers only: tcgen05.commit from the issuer, one arrival per epilogue warp,
@@ -832,7 +833,7 @@ struct WtSmem {
   float gam[kRingA][64];     // chunk-local cumulative gate
   float fac[kRingA][kFacFloats];
 };
-constexpr int kWsThreads = 320;
+constexpr int kWsThreads = 352;
 // Buffers affine_apply borrows (all idle between chain runs): M hi in K slots 0-1, S_start lo in K
 // slot 2 and the T_w slots, M lo in the V slots, S_start hi in the Q slots, the fp32 stage in the
 // P'' slots and -W^T.
@@ -844,18 +845,19 @@ static_assert(offsetof(WtSmem, wn) == offsetof(WtSmem, pp) + 16384, "the fp32 st
 
 struct WtBars {
   uint64_t full_a[kRingA], empty_a[kRingA], full_b[2], empty_b[2], full_c[2], empty_c[2];
-  uint64_t a_done, pre_done, b_done, o_done, staged, epi1, epi2, o_read[2];
+  uint64_t a_done, pre_done, b_done, o_done, qs_done, u_done, staged, epi1, epi2, o_read[2];
 };
 // Phase parities of these barriers as the bits of one register (slots indexed at run time would
 // otherwise put them in local memory).
 enum WtBit : int {
   kBitFullA = 0, kBitEmptyA = 3, kBitFullB = 6, kBitEmptyB = 8, kBitFullC = 10, kBitEmptyC = 12, kBitADone = 14,
-  kBitPreDone = 15, kBitBDone = 16, kBitODone = 17, kBitStaged = 18, kBitEpi1 = 19, kBitEpi2 = 20, kBitORead = 21
+  kBitPreDone = 15, kBitBDone = 16, kBitODone = 17, kBitStaged = 18, kBitEpi1 = 19, kBitEpi2 = 20, kBitORead = 21,
+  kBitQsDone = 23, kBitUDone = 24
 };
 __device__ __forceinline__ void wt_bars_init(WtBars& bb) {
   for (int i = 0; i < kRingA; ++i) {
     mbar_init(&bb.full_a[i], 1);
-    mbar_init(&bb.empty_a[i], 1 + 8);  // the issuer's commit and one arrival per epilogue warp
+    mbar_init(&bb.empty_a[i], 2 + 8);  // both issuers' commits and one arrival per epilogue warp
   }
   for (int i = 0; i < 2; ++i) {
     mbar_init(&bb.full_b[i], 1);
@@ -868,6 +870,8 @@ __device__ __forceinline__ void wt_bars_init(WtBars& bb) {
   mbar_init(&bb.pre_done, 1);
   mbar_init(&bb.b_done, 1);
   mbar_init(&bb.o_done, 1);
+  mbar_init(&bb.qs_done, 1);
+  mbar_init(&bb.u_done, 1);
   mbar_init(&bb.staged, 8);
   mbar_init(&bb.epi1, 8);
   mbar_init(&bb.epi2, 8);
@@ -921,7 +925,7 @@ __device__ __forceinline__ void warp_handoff(const ChainCtx& cx, bool smem, uint
 
 // Run chunks [gc0, gc1) of one document for value head h from S (epilogue registers, transposed
 // layout). Chunks gc >= gc_out write O. kWithU = false runs the transition chain (no U term, no
-// output). All 320 threads call this; returns false after a failed wait.
+// output). All threads of the CTA call this; returns false after a failed wait.
 template <bool kWithU>
 __device__ bool run_wt(const FwdParams& p, ChainCtx& cx, WtBars& bb, uint32_t& ph, volatile int* abort, float* S,
                        int gc0, int gc1, int gc_out, int h, int hk) {
@@ -1001,25 +1005,52 @@ __device__ bool run_wt(const FwdParams& p, ChainCtx& cx, WtBars& bb, uint32_t& p
     }
     return !*abort;
   }
+  // MMA issue: an issuing thread waits for the tensor pipe at every product, and shares its
+  // sub-partition's issue slots with two epilogue warps, so the products are split over two
+  // threads in different sub-partitions: warp 9 issues the two state products, warp 10 the rest.
+  const uint32_t tm = cx.tmem;
+  constexpr uint32_t id_kt = idesc_bf16(128, 64, 1, 0);   // MN-major A x K-major B: W^T, U^T
+  constexpr uint32_t id_sw = idesc_bf16(128, 64, 0, 1);   // tensor-memory A x MN-major B: S^T (-W^T)
+  constexpr uint32_t id_tk = idesc_bf16(128, 64, 0, 0);   // tensor-memory A x K-major B: S^T Q^T, V'^T P''^T
+  constexpr uint32_t id_d2 = idesc_bf16(128, 128, 0, 1);  // tensor-memory A x MN-major B: V'_s^T K
+  // k-step-0 descriptors of slot 0 of every operand (the buffers do not move; slot s of a ring adds
+  // s times its size to the start-address field, which never carries out of it)
+  const uint64_t d_k = mnmajor_desc(smem_u32(sm.k[0]), 8192, 0);  // slots 16 KB apart
   if (cx.warp == 9) {
-    // ------------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------ issuer of the state products (one lane)
     if (cx.lane == 0) {
-      const uint32_t tm = cx.tmem;
-      constexpr uint32_t id_kt = idesc_bf16(128, 64, 1, 0);   // MN-major A x K-major B: W^T, U^T
-      constexpr uint32_t id_sw = idesc_bf16(128, 64, 0, 1);   // tensor-memory A x MN-major B: S^T (-W^T)
-      constexpr uint32_t id_tk = idesc_bf16(128, 64, 0, 0);   // tensor-memory A x K-major B: S^T Q^T, V'^T P''^T
-      constexpr uint32_t id_d2 = idesc_bf16(128, 128, 0, 1);  // tensor-memory A x MN-major B: V'_s^T K
-      // k-step-0 descriptors of slot 0 of every operand (the buffers do not move; a slot s of a ring
-      // adds s times its size to the start-address field, which never carries out of it): the issue
-      // loop only adds constants
-      const uint64_t d_k = mnmajor_desc(smem_u32(sm.k[0]), 8192, 0);    // slots 16 KB apart
+      const uint64_t d_wn = mnmajor_desc(smem_u32(sm.wn), 8192, 0);
+      for (int j = 0; j < n && !*abort; ++j) {
+        const int s = j % kRingA;
+        bit_wait(&bb.staged, ph, kBitStaged, abort);  // -W^T(j) and Q(j) are staged
+        bit_wait(&bb.epi2, ph, kBitEpi2, abort);      // S^T(j) is staged
+        if (kWithU) bit_wait(&bb.u_done, ph, kBitUDone, abort);  // U^T(j) is in D_V
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)
+          umma_bf16_ts(tm + kTtDV, tm + kTtS + 8 * ks, mnmajor_step(d_wn, ks), id_sw, (kWithU || ks > 0) ? 1 : 0);
+        umma_commit(&bb.a_done);
+        bit_wait(&bb.epi1, ph, kBitEpi1, abort);
+        const uint64_t ka = d_k + (uint64_t)(s * (16384 >> 4));
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+          umma_bf16_ts(tm + kTtD2, tm + kTtVs + 8 * ks, mnmajor_step(ka, ks), id_d2, ks > 0);
+        umma_commit(&bb.b_done);
+        umma_commit(&bb.empty_a[s]);
+      }
+      bit_wait(&bb.epi2, ph, kBitEpi2, abort);  // the epilogue's last state hand-off
+    }
+    return !*abort;
+  }
+  if (cx.warp == 10) {
+    // ------------------------------------------------ issuer of the other products (one lane):
+    // Q S and chunk j + 1's W^T behind the state product D_V, P'' V' and chunk j + 1's U^T behind D_2
+    if (cx.lane == 0) {
       const uint64_t d_tw = kmajor_desc(smem_u32(sm.tw[0]), 8192, 0);   // 8 KB
       const uint64_t d_v = mnmajor_desc(smem_u32(sm.v[0]), 8192, 0);    // 16 KB
       const uint64_t d_tu = kmajor_desc(smem_u32(sm.tu[0]), 8192, 0);   // 8 KB
       const uint64_t d_q = kmajor_desc(smem_u32(sm.q[0]), 8192, 0);     // 16 KB
       const uint64_t d_pp = kmajor_desc(smem_u32(sm.pp[0]), 8192, 0);   // 8 KB
-      const uint64_t d_wn = mnmajor_desc(smem_u32(sm.wn), 8192, 0);
-      auto prep = [&](int j) {  // W^T of chunk j
+      auto prep = [&](int j) {  // W^T of chunk j (the staging of chunk j - 1 has read W^T)
         const int s = j % kRingA;
         bit_wait(&bb.full_a[s], ph, kBitFullA + (s), abort);
         const uint64_t ka = d_k + (uint64_t)(s * (16384 >> 4)), ta = d_tw + (uint64_t)(s * (8192 >> 4));
@@ -1027,6 +1058,7 @@ __device__ bool run_wt(const FwdParams& p, ChainCtx& cx, WtBars& bb, uint32_t& p
         for (int ks = 0; ks < 4; ++ks)
           umma_bf16(tm + kTtW, mnmajor_step(ka, ks), kmajor_step(ta, 8192, ks), id_kt, ks > 0);
         umma_commit(&bb.pre_done);
+        umma_commit(&bb.empty_a[s]);
       };
       auto issue_u = [&](int j) {  // U^T of chunk j into D_V (the V' epilogue of chunk j - 1 has read it)
         const int s = j & 1;
@@ -1035,37 +1067,27 @@ __device__ bool run_wt(const FwdParams& p, ChainCtx& cx, WtBars& bb, uint32_t& p
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
           umma_bf16(tm + kTtDV, mnmajor_step(va, ks), kmajor_step(ua, 8192, ks), id_kt, ks > 0);
+        umma_commit(&bb.u_done);
         umma_commit(&bb.empty_b[s]);
       };
       prep(0);
       if (kWithU) issue_u(0);
       for (int j = 0; j < n && !*abort; ++j) {
-        const int s = j % kRingA;
         const bool out = j >= j_out;
         const int so = (j - j_out) & 1;
-        bit_wait(&bb.staged, ph, kBitStaged, abort);  // -W^T(j) and Q(j) are staged
-        bit_wait(&bb.epi2, ph, kBitEpi2, abort);      // S^T(j) is staged
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks)
-          umma_bf16_ts(tm + kTtDV, tm + kTtS + 8 * ks, mnmajor_step(d_wn, ks), id_sw, (kWithU || ks > 0) ? 1 : 0);
-        umma_commit(&bb.a_done);
+        bit_wait(&bb.a_done, ph, kBitADone, abort);  // the state product of chunk j has run
         if (out) {
-          // Q S while the V' epilogue runs (the output of chunk j - 2 has left this buffer)
+          // Q S (the output of chunk j - 2 has left this buffer)
           if (j - j_out >= 2) bit_wait(&bb.o_read[so], ph, kBitORead + (so), abort);
           bit_wait(&bb.full_c[so], ph, kBitFullC + (so), abort);
           const uint64_t qa = d_q + (uint64_t)(so * (16384 >> 4));
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks)
             umma_bf16_ts(tm + kTtO + 64 * so, tm + kTtS + 8 * ks, kmajor_step(qa, 8192, ks), id_tk, ks > 0);
+          umma_commit(&bb.qs_done);
         }
         if (j + 1 < n) prep(j + 1);  // the epilogue stages -W^T(j + 1) while D_2 runs
-        bit_wait(&bb.epi1, ph, kBitEpi1, abort);
-        const uint64_t ka = d_k + (uint64_t)(s * (16384 >> 4));
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks)
-          umma_bf16_ts(tm + kTtD2, tm + kTtVs + 8 * ks, mnmajor_step(ka, ks), id_d2, ks > 0);
-        umma_commit(&bb.b_done);
-        umma_commit(&bb.empty_a[s]);
+        bit_wait(&bb.b_done, ph, kBitBDone, abort);  // D_2 has run (V'^T is in place)
         if (out) {
           const uint64_t pa = d_pp + (uint64_t)(so * (8192 >> 4));
 #pragma unroll
@@ -1076,7 +1098,6 @@ __device__ bool run_wt(const FwdParams& p, ChainCtx& cx, WtBars& bb, uint32_t& p
         }
         if (kWithU && j + 1 < n) issue_u(j + 1);
       }
-      bit_wait(&bb.epi2, ph, kBitEpi2, abort);  // the epilogue's last state hand-off
       // the outputs of the last two chunks have been read (every phase consumed)
       for (int jc = (n_out > 2 ? n_out - 2 : 0); jc < n_out; ++jc)
         bit_wait(&bb.o_read[jc & 1], ph, kBitORead + (jc & 1), abort);
@@ -1128,6 +1149,7 @@ __device__ bool run_wt(const FwdParams& p, ChainCtx& cx, WtBars& bb, uint32_t& p
     const bool out = j >= j_out;
     const int so = (j - j_out) & 1;
     const float* fc = sm.fac[s];  // e^{gamma_C - gamma_t} [0, 64), output factors [64, 128), e^{gamma_C}
+    const int nn = out ? clen[gc] : 0, tok0 = out ? ctok[gc] : 0;  // (global loads, used by the O stores)
     bit_wait(&bb.a_done, ph, kBitADone, abort);
     {
       // V' of this lane's value index, tokens 32 half ..: V'^T and V'_s^T as bf16 A operands
@@ -1158,6 +1180,7 @@ __device__ bool run_wt(const FwdParams& p, ChainCtx& cx, WtBars& bb, uint32_t& p
 #pragma unroll
         for (int x = 0; x < 32; ++x) S[32 * hc + x] = GC * S[32 * hc + x] + d[x];
       }
+      if (out) bit_wait(&bb.qs_done, ph, kBitQsDone, abort);  // Q S(j) has read S^T(j)
       stage_state_t(cx, S);
       tmem_st_wait();
     }
@@ -1174,7 +1197,8 @@ __device__ bool run_wt(const FwdParams& p, ChainCtx& cx, WtBars& bb, uint32_t& p
       tmem_ld_wait();
       warp_handoff(cx, false, &bb.o_read[so]);
       uint8_t* stg = sm.ostage[so];
-      if (cx.tid == 0) bulk_wait_read_all();  // earlier stores have read their tiles
+      if (cx.tid == 0) bulk_wait_read<1>();  // the store from this tile two chunks ago has read it (only a
+                                             // run's last chunk can be partial and skip its store)
       e_sync();
       // the output factors of this thread's 32 tokens, in registers before any store to the tile
       // (the stores could otherwise alias them and serialize the loop)
@@ -1203,17 +1227,16 @@ __device__ bool run_wt(const FwdParams& p, ChainCtx& cx, WtBars& bb, uint32_t& p
       }
       fence_proxy_async_smem();
       e_sync();
-      const int nn = clen[gc];
       if (nn == kChunk) {
         if (cx.tid == 0) {
-          tma_store_3d(&p.tm_o, stg, 0, h, ctok[gc]);
-          tma_store_3d(&p.tm_o, stg + 8192, 64, h, ctok[gc]);
+          tma_store_3d(&p.tm_o, stg, 0, h, tok0);
+          tma_store_3d(&p.tm_o, stg + 8192, 64, h, tok0);
           bulk_commit_group();
         }
       } else {
         for (int e = cx.tid; e < nn * 16; e += 256) {
           const int t = e >> 4, u = e & 15, cj = u & 7;
-          reinterpret_cast<uint4*>(p.out + ((size_t)(ctok[gc] + t) * Hv + h) * kDim)[u] =
+          reinterpret_cast<uint4*>(p.out + ((size_t)(tok0 + t) * Hv + h) * kDim)[u] =
               *reinterpret_cast<const uint4*>(stg + (u >> 3) * 8192 + t * 128 + ((cj ^ (t & 7)) << 4));
         }
       }
@@ -1251,7 +1274,7 @@ __device__ __forceinline__ void e_handoff(int tid, uint64_t* b1, uint64_t* b2 = 
 // The backward's recompute of the forward chain: the same recurrence with compensated bf16
 // operands (x = hi + lo for T_w, T_u, W, S and V'_s; K and V are exact in bf16), optionally
 // writing the per-chunk records that the gradient kernels read (chunk-start S hi / lo and V'
-// hi / lo as 128B-swizzled images). No output. Roles in one CTA of 10 warps:
+// hi / lo as 128B-swizzled images). No output. Roles in the chain's CTA (warp 10 idles):
 //   warp 8      TMA producer: K and gamma of chunk j into stage j % 3; T_w hi / lo (one buffer,
 //               released by the W product); V and T_u hi / lo (one buffer, released by the U
 //               product).
@@ -1301,8 +1324,8 @@ __device__ __forceinline__ void store_state_comp(RecSmem& sm, const ChainCtx& cx
 
 // Run chunks [gc0, gc1) of one document for value head h from S (epilogue registers; its hi / lo
 // images are already in sm.s / sm.slo). kWithU = false runs the transition chain (no U term).
-// kStore writes the records of the chunks from gc_rec on (the ones before are a warm-up). All 320
-// threads call this; returns false after a failed wait.
+// kStore writes the records of the chunks from gc_rec on (the ones before are a warm-up). All
+// threads of the CTA call this; returns false after a failed wait.
 template <bool kWithU, bool kStore>
 __device__ bool run_ws_rec(const FwdParams& p, ChainCtx& cx, WsBars& bb, WsPhase& ph, volatile int* abort,
                            float* S, int gc0, int gc1, int h, int hk, int gc_rec) {
@@ -1312,6 +1335,7 @@ __device__ bool run_ws_rec(const FwdParams& p, ChainCtx& cx, WsBars& bb, WsPhase
   const int Hv = p.d.Hv;
   const int32_t* ctok = ws_ptr<int32_t>(p, p.L.chunk_tok0);
   auto rec = [&](int gc) { return (size_t)gc * Hv + h; };
+  if (cx.warp == 10) return true;  // the record chain has one issuer
 
   if (cx.warp == 8) {
     // ------------------------------------------------------------------ TMA producer
@@ -1532,7 +1556,7 @@ __device__ __forceinline__ void publish(int* flag) {
 }
 
 // kRec: the backward's recompute (compensated arithmetic, records in the output pass); otherwise
-// the forward. Both warp-specialized, 320 threads.
+// the forward. Both warp-specialized, 352 threads.
 constexpr int kTransWindow = 12;  // chunks of the transition evaluated first (see pass 1, part 0)
 
 template <int kMode, bool kRec>
