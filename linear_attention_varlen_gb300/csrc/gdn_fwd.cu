@@ -269,7 +269,17 @@ __global__ void __launch_bounds__(256, 2) kkt_solve_kernel(const __grid_constant
   const int tok0 = ws_ptr<int32_t>(p, p.L.chunk_tok0)[chunk];
   const int n = ws_ptr<int32_t>(p, p.L.chunk_len)[chunk];
   const int Hv = p.d.Hv, G = p.d.Hv / p.d.Hk;
-  const int grp = tid >> 6, t = tid & 63;  // value-head group and its thread (token / column)
+  // value-head group (warps g and g + 4) and its thread (token / column): the warp of columns 0-31
+  // carries about four times the substitution work of the other, and warps g and g + 4 share a
+  // sub-partition, so every sub-partition gets one of each per group
+  const int grp = warp & 3, t = 32 * (warp >> 2) + lane;
+  // the first round's gate and beta, loaded while the K and Q tiles and their products are in flight
+  float g_first = 0.f, b_first = 0.f;
+  if (grp < G && t < n) {
+    const size_t at = (size_t)(tok0 + t) * Hv + hk * G + grp;
+    g_first = p.g[at];
+    b_first = p.beta[at];
+  }
 
   if (tid == 0) {
     mbar_init(&bar_ld, 1);
@@ -354,8 +364,8 @@ __global__ void __launch_bounds__(256, 2) kkt_solve_kernel(const __grid_constant
       const size_t rec = (size_t)chunk * Hv + h;
       // chunk-local cumulative gate: inclusive scan over the 64 tokens in the group's two warps
       {
-        const float gi = (t < n) ? p.g[(size_t)(tok0 + t) * Hv + h] : 0.f;
-        const float bi = (t < n) ? p.beta[(size_t)(tok0 + t) * Hv + h] : 0.f;
+        const float gi = hb == 0 ? g_first : ((t < n) ? p.g[(size_t)(tok0 + t) * Hv + h] : 0.f);
+        const float bi = hb == 0 ? b_first : ((t < n) ? p.beta[(size_t)(tok0 + t) * Hv + h] : 0.f);
         float sc = gi;
         for (int off = 1; off < 32; off <<= 1) {
           const float o = __shfl_up_sync(0xffffffffu, sc, off);
@@ -489,12 +499,34 @@ __global__ void __launch_bounds__(256, 2) kkt_solve_kernel(const __grid_constant
         for (int r = 0; r < 64; ++r) A[r][t] = x[r];
         group_sync(grp);
       }
-      // outputs, row by row (8 threads per 128-byte row of the bf16 images)
+      // outputs, row by row (8 threads per 128-byte row of the bf16 images): a thread keeps its
+      // 16-byte column group cj = t mod 8 in every row, so its beta and e^{gamma} (and e^{-gamma}
+      // for P'') are loaded once
+      const int cjt = t & 7;
+      float bcol[8], ecol[8], eicol[8];
+      {
+        const float4 b0 = *reinterpret_cast<const float4*>(&bet[8 * cjt]);
+        const float4 b1 = *reinterpret_cast<const float4*>(&bet[8 * cjt + 4]);
+        const float4 e0 = *reinterpret_cast<const float4*>(&eg[8 * cjt]);
+        const float4 e1 = *reinterpret_cast<const float4*>(&eg[8 * cjt + 4]);
+        const float4 i0 = *reinterpret_cast<const float4*>(&egi[8 * cjt]);
+        const float4 i1 = *reinterpret_cast<const float4*>(&egi[8 * cjt + 4]);
+        const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+        const float ev[8] = {e0.x, e0.y, e0.z, e0.w, e1.x, e1.y, e1.z, e1.w};
+        const float iv[8] = {i0.x, i0.y, i0.z, i0.w, i1.x, i1.y, i1.z, i1.w};
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          bcol[u] = bv[u];
+          ecol[u] = ev[u];
+          eicol[u] = iv[u];
+        }
+      }
       uint8_t* dw = tw_ws + rec * 8192;
       uint8_t* du = tu_ws + rec * 8192;
       float* tdst = p.t_f32 ? p.t_f32 + rec * 4096 : nullptr;
+#pragma unroll 2
       for (int e = t; e < 64 * 8; e += 64) {
-        const int r = e >> 3, cj = e & 7;
+        const int r = e >> 3, cj = cjt;
         const float4 t0 = *reinterpret_cast<const float4*>(&A[r][8 * cj]);
         const float4 t1 = *reinterpret_cast<const float4*>(&A[r][8 * cj + 4]);
         const float tv[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
@@ -505,9 +537,8 @@ __global__ void __launch_bounds__(256, 2) kkt_solve_kernel(const __grid_constant
         float xw[8], xu[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
-          const int j = 8 * cj + u;
-          xu[u] = tv[u] * bet[j];
-          xw[u] = xu[u] * eg[j];
+          xu[u] = tv[u] * bcol[u];
+          xw[u] = xu[u] * ecol[u];
         }
         const uint32_t off = r * 128 + ((cj ^ (r & 7)) << 4);
         uint32_t w[4], wl[4], uu[4], ul[4];
@@ -534,19 +565,17 @@ __global__ void __launch_bounds__(256, 2) kkt_solve_kernel(const __grid_constant
       // drops its Q S term in the chain (that term is below e^{kExactCut} of the chunk-start state).
       if (want_p && p.p_factored) {
         uint8_t* dp = p.p_img + rec * 8192;
+#pragma unroll 2
         for (int e = t; e < 64 * 8; e += 64) {
-          const int i = e >> 3, cj = e & 7;
+          const int i = e >> 3, cj = cjt;
           const float4 q0 = *reinterpret_cast<const float4*>(qk + fz(i, 8 * cj));
           const float4 q1 = *reinterpret_cast<const float4*>(qk + fz(i, 8 * cj + 4));
           const float qv[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
           const float gi = gam[i];
           float pv[8];
           if (gi >= kExactCut) {
-            const float4 e0 = *reinterpret_cast<const float4*>(egi + 8 * cj);
-            const float4 e1 = *reinterpret_cast<const float4*>(egi + 8 * cj + 4);
-            const float ev[8] = {e0.x, e0.y, e0.z, e0.w, e1.x, e1.y, e1.z, e1.w};
 #pragma unroll
-            for (int u = 0; u < 8; ++u) pv[u] = (8 * cj + u <= i && i < n) ? ev[u] * qv[u] : 0.f;
+            for (int u = 0; u < 8; ++u) pv[u] = (8 * cj + u <= i && i < n) ? eicol[u] * qv[u] : 0.f;
           } else {
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
