@@ -249,8 +249,10 @@ __device__ bool run_rev_ws(const BwdParams& p, Ctx& cx, RevSmem& sm, RevBars& bb
     if (cx.lane == 0) {
       auto prep = [&](int j) {  // W = T_w K of chunk j
         const int st = j & 1;
+        #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
-          umma_bf16(tm + kRtW, kmajor_desc(smem_u32(sm.tw[st]), 8192, ks), mnmajor_desc(smem_u32(sm.k[st]), 8192, ks),
+          umma_bf16(tm + kRtW, kmajor_step(kmajor_desc(smem_u32(sm.tw[st]), 8192, 0), 8192, ks),
+                    mnmajor_step(mnmajor_desc(smem_u32(sm.k[st]), 8192, 0), ks),
                     idesc_bf16(64, 128, 0, 1), ks > 0);
         umma_commit(&bb.pre_done);
       };
@@ -264,14 +266,20 @@ __device__ bool run_rev_ws(const BwdParams& p, Ctx& cx, RevSmem& sm, RevBars& bb
         rrole_wait(&bb.epi2, ph.epi2, abort);
         if (*abort) break;
         // Q~^T dO first: a_done then also covers it, so that the epilogue may restage Q~ right after
+        #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
-          umma_bf16(tm + kRtC, mnmajor_desc(smem_u32(sm.qt), 8192, ks), mnmajor_desc(smem_u32(sm.dout[st]), 8192, ks),
+          umma_bf16(tm + kRtC, mnmajor_step(mnmajor_desc(smem_u32(sm.qt), 8192, 0), ks),
+                    mnmajor_step(mnmajor_desc(smem_u32(sm.dout[st]), 8192, 0), ks),
                     idesc_bf16(128, 128, 1, 1), ks > 0);
+        #pragma unroll
         for (int ks = 0; ks < 8; ++ks)
-          umma_bf16(tm + kRtA, kmajor_desc(smem_u32(sm.kt), 8192, ks), mnmajor_desc(smem_u32(sm.ds), 16384, ks),
+          umma_bf16(tm + kRtA, kmajor_step(kmajor_desc(smem_u32(sm.kt), 8192, 0), 8192, ks),
+                    mnmajor_step(mnmajor_desc(smem_u32(sm.ds), 16384, 0), ks),
                     idesc_bf16(64, 128, 0, 1), ks > 0);
+        #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
-          umma_bf16(tm + kRtA, mnmajor_desc(smem_u32(sm.p[st]), 8192, ks), mnmajor_desc(smem_u32(sm.dout[st]), 8192, ks),
+          umma_bf16(tm + kRtA, mnmajor_step(mnmajor_desc(smem_u32(sm.p[st]), 8192, 0), ks),
+                    mnmajor_step(mnmajor_desc(smem_u32(sm.dout[st]), 8192, 0), ks),
                     idesc_bf16(64, 128, 1, 1), 1);
         umma_commit(&bb.a_done);
         // B as soon as dV' and -W are staged; chunk j + 1's W as soon as its operands have landed
@@ -293,8 +301,10 @@ __device__ bool run_rev_ws(const BwdParams& p, Ctx& cx, RevSmem& sm, RevBars& bb
           if (w_read && mbar_test(&bb.epi1, ph.epi1)) {
             ph.epi1 ^= 1;
             tc_fence_after();
+            #pragma unroll
             for (int ks = 0; ks < 4; ++ks)
-              umma_bf16(tm + kRtC, mnmajor_desc(smem_u32(sm.wn), 8192, ks), mnmajor_desc(smem_u32(sm.dvp), 8192, ks),
+              umma_bf16(tm + kRtC, mnmajor_step(mnmajor_desc(smem_u32(sm.wn), 8192, 0), ks),
+                        mnmajor_step(mnmajor_desc(smem_u32(sm.dvp), 8192, 0), ks),
                         idesc_bf16(128, 128, 1, 1), 1);
             umma_commit(&bb.b_done);
             umma_commit(&bb.empty[st]);
@@ -511,14 +521,20 @@ __device__ bool rev_affine(Ctx& cx, RevSmem& sm, const float* Mm, const float* B
   }
   sync_generic_to_async();
   if (cx.tid == 0) {
+    #pragma unroll
     for (int ks = 0; ks < 8; ++ks)
-      umma_bf16(cx.tmem + kRtC, mnmajor_desc(smem_u32(mhi), 16384, ks), mnmajor_desc(smem_u32(sm.ds), 16384, ks),
+      umma_bf16(cx.tmem + kRtC, mnmajor_step(mnmajor_desc(smem_u32(mhi), 16384, 0), ks),
+                mnmajor_step(mnmajor_desc(smem_u32(sm.ds), 16384, 0), ks),
                 idesc_bf16(128, 128, 1, 1), ks > 0);
+    #pragma unroll
     for (int ks = 0; ks < 8; ++ks)
-      umma_bf16(cx.tmem + kRtC, mnmajor_desc(smem_u32(mhi), 16384, ks), mnmajor_desc(smem_u32(dlo), 16384, ks),
+      umma_bf16(cx.tmem + kRtC, mnmajor_step(mnmajor_desc(smem_u32(mhi), 16384, 0), ks),
+                mnmajor_step(mnmajor_desc(smem_u32(dlo), 16384, 0), ks),
                 idesc_bf16(128, 128, 1, 1), 1);
+    #pragma unroll
     for (int ks = 0; ks < 8; ++ks)
-      umma_bf16(cx.tmem + kRtC, mnmajor_desc(smem_u32(mlo), 16384, ks), mnmajor_desc(smem_u32(sm.ds), 16384, ks),
+      umma_bf16(cx.tmem + kRtC, mnmajor_step(mnmajor_desc(smem_u32(mlo), 16384, 0), ks),
+                mnmajor_step(mnmajor_desc(smem_u32(sm.ds), 16384, 0), ks),
                 idesc_bf16(128, 128, 1, 1), 1);
   }
   if (!cx.commit_wait()) return false;
@@ -912,10 +928,13 @@ __global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ Bw
   ok = cx.wait_ld();
   if (ok) {
     if (tid == 0) {
+      #pragma unroll
       for (int ks = 0; ks < 8; ++ks) {
-        umma_bf16(tm + kGtC, kmajor_desc(smem_u32(sm.k[0]), 8192, ks), kmajor_desc(smem_u32(sm.k[0]), 8192, ks),
+        umma_bf16(tm + kGtC, kmajor_step(kmajor_desc(smem_u32(sm.k[0]), 8192, 0), 8192, ks),
+                  kmajor_step(kmajor_desc(smem_u32(sm.k[0]), 8192, 0), 8192, ks),
                   idesc_bf16(64, 64, 0, 0), ks > 0);
-        umma_bf16(tm + kGtC + 64, kmajor_desc(smem_u32(sm.q[0]), 8192, ks), kmajor_desc(smem_u32(sm.k[0]), 8192, ks),
+        umma_bf16(tm + kGtC + 64, kmajor_step(kmajor_desc(smem_u32(sm.q[0]), 8192, 0), 8192, ks),
+                  kmajor_step(kmajor_desc(smem_u32(sm.k[0]), 8192, 0), 8192, ks),
                   idesc_bf16(64, 64, 0, 0), ks > 0);
       }
     }
@@ -970,11 +989,15 @@ __global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ Bw
     float* dEg = reinterpret_cast<float*>(sm.bW[0]);
     // ---------------- (a) dP = dO V'^T ; K dS
     if (tid == 0) {
+      #pragma unroll
       for (int ks = 0; ks < 8; ++ks)
-        umma_bf16(tm + kGt1, kmajor_desc(smem_u32(sm.bdO[0]), 8192, ks), kmajor_desc(smem_u32(sm.bVp[0]), 8192, ks),
+        umma_bf16(tm + kGt1, kmajor_step(kmajor_desc(smem_u32(sm.bdO[0]), 8192, 0), 8192, ks),
+                  kmajor_step(kmajor_desc(smem_u32(sm.bVp[0]), 8192, 0), 8192, ks),
                   idesc_bf16(64, 64, 0, 0), ks > 0);
+      #pragma unroll
       for (int ks = 0; ks < 8; ++ks)
-        umma_bf16(tm + kGt2, kmajor_desc(smem_u32(sm.k[0]), 8192, ks), mnmajor_desc(smem_u32(sm.bdS[0]), 16384, ks),
+        umma_bf16(tm + kGt2, kmajor_step(kmajor_desc(smem_u32(sm.k[0]), 8192, 0), 8192, ks),
+                  mnmajor_step(mnmajor_desc(smem_u32(sm.bdS[0]), 16384, 0), ks),
                   idesc_bf16(64, 128, 0, 1), ks > 0);
     }
     if (!(ok = cx.commit_wait())) break;
@@ -1048,8 +1071,10 @@ __global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ Bw
     col_sums(sm, dEg, nullptr, sm.part[4], nullptr, tid);
     // ---------------- (b) dV' S^T (-> dW) ; <dS, S>  (the term of dgamma in q S dO is dq_kernel's)
     if (tid == 0) {
+      #pragma unroll
       for (int ks = 0; ks < 8; ++ks)
-        umma_bf16(tm + kGt2, kmajor_desc(smem_u32(sm.bdVp[0]), 8192, ks), kmajor_desc(smem_u32(sm.bS[0]), 16384, ks),
+        umma_bf16(tm + kGt2, kmajor_step(kmajor_desc(smem_u32(sm.bdVp[0]), 8192, 0), 8192, ks),
+                  kmajor_step(kmajor_desc(smem_u32(sm.bS[0]), 16384, 0), 16384, ks),
                   idesc_bf16(64, 128, 0, 0), ks > 0);
     }
     {
@@ -1103,11 +1128,15 @@ __global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ Bw
     scale_rows(sm.bVp[1], sm.cA, tid);
     sync_generic_to_async();
     if (tid == 0) {
+      #pragma unroll
       for (int ks = 0; ks < 8; ++ks)
-        umma_bf16(tm + kGtK, kmajor_desc(smem_u32(sm.bVp[0]), 8192, ks), kmajor_desc(smem_u32(sm.bdS[0]), 16384, ks),
+        umma_bf16(tm + kGtK, kmajor_step(kmajor_desc(smem_u32(sm.bVp[0]), 8192, 0), 8192, ks),
+                  kmajor_step(kmajor_desc(smem_u32(sm.bdS[0]), 16384, 0), 16384, ks),
                   idesc_bf16(64, 128, 0, 0), (!first_k || ks > 0) ? 1 : 0);
+      #pragma unroll
       for (int ks = 0; ks < 4; ++ks)
-        umma_bf16(tm + kGtK, mnmajor_desc(smem_u32(sm.bP), 8192, ks), mnmajor_desc(smem_u32(sm.q[0]), 8192, ks),
+        umma_bf16(tm + kGtK, mnmajor_step(mnmajor_desc(smem_u32(sm.bP), 8192, 0), ks),
+                  mnmajor_step(mnmajor_desc(smem_u32(sm.q[0]), 8192, 0), ks),
                   idesc_bf16(64, 128, 1, 1), 1);
     }
     first_k = false;
@@ -1138,17 +1167,25 @@ __global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ Bw
     sync_generic_to_async();
     // ---------------- (d) dv = T_u^T dV' ; D1 = dV' V^T ; D2 = dW K^T ; dk += T_w^T dW
     if (tid == 0) {
+      #pragma unroll
       for (int ks = 0; ks < 4; ++ks)
-        umma_bf16(tm + kGt1, mnmajor_desc(smem_u32(Tu), 8192, ks), mnmajor_desc(smem_u32(sm.bdVp[0]), 8192, ks),
+        umma_bf16(tm + kGt1, mnmajor_step(mnmajor_desc(smem_u32(Tu), 8192, 0), ks),
+                  mnmajor_step(mnmajor_desc(smem_u32(sm.bdVp[0]), 8192, 0), ks),
                   idesc_bf16(64, 128, 1, 1), ks > 0);
+      #pragma unroll
       for (int ks = 0; ks < 8; ++ks)
-        umma_bf16(tm + kGt2, kmajor_desc(smem_u32(sm.bdVp[0]), 8192, ks), kmajor_desc(smem_u32(sm.bdO[0]), 8192, ks),
+        umma_bf16(tm + kGt2, kmajor_step(kmajor_desc(smem_u32(sm.bdVp[0]), 8192, 0), 8192, ks),
+                  kmajor_step(kmajor_desc(smem_u32(sm.bdO[0]), 8192, 0), 8192, ks),
                   idesc_bf16(64, 64, 0, 0), ks > 0);
+      #pragma unroll
       for (int ks = 0; ks < 8; ++ks)
-        umma_bf16(tm + kGt2 + 64, kmajor_desc(smem_u32(sm.bW[0]), 8192, ks), kmajor_desc(smem_u32(sm.k[0]), 8192, ks),
+        umma_bf16(tm + kGt2 + 64, kmajor_step(kmajor_desc(smem_u32(sm.bW[0]), 8192, 0), 8192, ks),
+                  kmajor_step(kmajor_desc(smem_u32(sm.k[0]), 8192, 0), 8192, ks),
                   idesc_bf16(64, 64, 0, 0), ks > 0);
+      #pragma unroll
       for (int ks = 0; ks < 4; ++ks)
-        umma_bf16(tm + kGtK, mnmajor_desc(smem_u32(Tw), 8192, ks), mnmajor_desc(smem_u32(sm.bW[0]), 8192, ks),
+        umma_bf16(tm + kGtK, mnmajor_step(mnmajor_desc(smem_u32(Tw), 8192, 0), ks),
+                  mnmajor_step(mnmajor_desc(smem_u32(sm.bW[0]), 8192, 0), ks),
                   idesc_bf16(64, 128, 1, 1), 1);
     }
     if (!(ok = cx.commit_wait())) break;
@@ -1202,8 +1239,10 @@ __global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ Bw
     sync_generic_to_async();
     // ---------------- (e) R = dT T^T (the column sums of vy / kx run meanwhile)
     if (tid == 0)
+      #pragma unroll
       for (int ks = 0; ks < 4; ++ks)
-        umma_bf16(tm + kGt1, kmajor_desc(smem_u32(dTt), 8192, ks), kmajor_desc(smem_u32(Tb), 8192, ks),
+        umma_bf16(tm + kGt1, kmajor_step(kmajor_desc(smem_u32(dTt), 8192, 0), 8192, ks),
+                  kmajor_step(kmajor_desc(smem_u32(Tb), 8192, 0), 8192, ks),
                   idesc_bf16(64, 64, 0, 0), ks > 0);
     col_sums(sm, vyM, kxM, sm.vy, sm.kx, tid);
     if (tid == 0 && next) load_dvp(hh + 1);  // the kx scratch is summed: the next head's dV'
@@ -1225,8 +1264,10 @@ __global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ Bw
     // gamma_j}: L = dA o diag(beta) E (bf16, for dk += (L + L^T) K), the row sums of dA o E o KK
     // (dbeta) and the matrix L o KK for its column sums (dgamma).
     if (tid == 0)
+      #pragma unroll
       for (int ks = 0; ks < 4; ++ks)
-        umma_bf16(tm + kGt1, mnmajor_desc(smem_u32(Tb), 8192, ks), mnmajor_desc(smem_u32(Rt), 8192, ks),
+        umma_bf16(tm + kGt1, mnmajor_step(mnmajor_desc(smem_u32(Tb), 8192, 0), ks),
+                  mnmajor_step(mnmajor_desc(smem_u32(Rt), 8192, 0), ks),
                   idesc_bf16(64, 64, 1, 1), ks > 0);
     if (!(ok = cx.commit_wait())) break;
     if (tid == 0 && next) load_ds(hh + 1);  // R, T_w, T_u, dT are read: the next head's dS
@@ -1278,11 +1319,15 @@ __global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ Bw
     sync_generic_to_async();
     // ---------------- (g) dk += (L + L^T) K: the image of L read K-major (L) and MN-major (L^T)
     if (tid == 0) {
+      #pragma unroll
       for (int ks = 0; ks < 4; ++ks)
-        umma_bf16(tm + kGtK, kmajor_desc(smem_u32(sm.bP), 8192, ks), mnmajor_desc(smem_u32(sm.k[0]), 8192, ks),
+        umma_bf16(tm + kGtK, kmajor_step(kmajor_desc(smem_u32(sm.bP), 8192, 0), 8192, ks),
+                  mnmajor_step(mnmajor_desc(smem_u32(sm.k[0]), 8192, 0), ks),
                   idesc_bf16(64, 128, 0, 1), 1);
+      #pragma unroll
       for (int ks = 0; ks < 4; ++ks)
-        umma_bf16(tm + kGtK, mnmajor_desc(smem_u32(sm.bP), 8192, ks), mnmajor_desc(smem_u32(sm.k[0]), 8192, ks),
+        umma_bf16(tm + kGtK, mnmajor_step(mnmajor_desc(smem_u32(sm.bP), 8192, 0), ks),
+                  mnmajor_step(mnmajor_desc(smem_u32(sm.k[0]), 8192, 0), ks),
                   idesc_bf16(64, 128, 1, 1), 1);
     }
     col_sums(sm, LK, nullptr, sm.cA, nullptr, tid);
@@ -1460,11 +1505,15 @@ __global__ void __launch_bounds__(256, 1) dq_kernel(const __grid_constant__ BwdP
     }
     // dP = dO V'^T (hi + lo)
     if (tid == 0) {
+      #pragma unroll
       for (int ks = 0; ks < 8; ++ks)
-        umma_bf16(tm + kDtP, kmajor_desc(smem_u32(sm.dout[bp][0]), 8192, ks), kmajor_desc(smem_u32(sm.vh[0]), 8192, ks),
+        umma_bf16(tm + kDtP, kmajor_step(kmajor_desc(smem_u32(sm.dout[bp][0]), 8192, 0), 8192, ks),
+                  kmajor_step(kmajor_desc(smem_u32(sm.vh[0]), 8192, 0), 8192, ks),
                   idesc_bf16(64, 64, 0, 0), ks > 0);
+      #pragma unroll
       for (int ks = 0; ks < 8; ++ks)
-        umma_bf16(tm + kDtP, kmajor_desc(smem_u32(sm.dout[bp][0]), 8192, ks), kmajor_desc(smem_u32(sm.vl[0]), 8192, ks),
+        umma_bf16(tm + kDtP, kmajor_step(kmajor_desc(smem_u32(sm.dout[bp][0]), 8192, 0), 8192, ks),
+                  kmajor_step(kmajor_desc(smem_u32(sm.vl[0]), 8192, 0), 8192, ks),
                   idesc_bf16(64, 64, 0, 0), 1);
     }
     if (!(ok = cx.commit_wait())) break;  // (its barrier also publishes eg / egi)
@@ -1508,17 +1557,25 @@ __global__ void __launch_bounds__(256, 1) dq_kernel(const __grid_constant__ BwdP
     tc_fence_after();
     // dO S^T (hi + lo) and dQK K (hi + lo)
     if (tid == 0) {
+      #pragma unroll
       for (int ks = 0; ks < 8; ++ks)
-        umma_bf16(tm + kDt1, kmajor_desc(smem_u32(sm.dout[bp][0]), 8192, ks), kmajor_desc(smem_u32(sm.sh[0]), 16384, ks),
+        umma_bf16(tm + kDt1, kmajor_step(kmajor_desc(smem_u32(sm.dout[bp][0]), 8192, 0), 8192, ks),
+                  kmajor_step(kmajor_desc(smem_u32(sm.sh[0]), 16384, 0), 16384, ks),
                   idesc_bf16(64, 128, 0, 0), ks > 0);
+      #pragma unroll
       for (int ks = 0; ks < 8; ++ks)
-        umma_bf16(tm + kDt1, kmajor_desc(smem_u32(sm.dout[bp][0]), 8192, ks), kmajor_desc(smem_u32(sm.sl[0]), 16384, ks),
+        umma_bf16(tm + kDt1, kmajor_step(kmajor_desc(smem_u32(sm.dout[bp][0]), 8192, 0), 8192, ks),
+                  kmajor_step(kmajor_desc(smem_u32(sm.sl[0]), 16384, 0), 16384, ks),
                   idesc_bf16(64, 128, 0, 0), 1);
+      #pragma unroll
       for (int ks = 0; ks < 4; ++ks)
-        umma_bf16(tm + kDt2, kmajor_desc(smem_u32(sm.qh), 8192, ks), mnmajor_desc(smem_u32(sm.k[0]), 8192, ks),
+        umma_bf16(tm + kDt2, kmajor_step(kmajor_desc(smem_u32(sm.qh), 8192, 0), 8192, ks),
+                  mnmajor_step(mnmajor_desc(smem_u32(sm.k[0]), 8192, 0), ks),
                   idesc_bf16(64, 128, 0, 1), ks > 0);
+      #pragma unroll
       for (int ks = 0; ks < 4; ++ks)
-        umma_bf16(tm + kDt2, kmajor_desc(smem_u32(sm.ql), 8192, ks), mnmajor_desc(smem_u32(sm.k[0]), 8192, ks),
+        umma_bf16(tm + kDt2, kmajor_step(kmajor_desc(smem_u32(sm.ql), 8192, 0), 8192, ks),
+                  mnmajor_step(mnmajor_desc(smem_u32(sm.k[0]), 8192, 0), ks),
                   idesc_bf16(64, 128, 0, 1), 1);
     }
     if (!(ok = cx.commit_wait())) break;

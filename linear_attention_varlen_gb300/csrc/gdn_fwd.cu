@@ -307,11 +307,15 @@ __global__ void __launch_bounds__(256, 2) kkt_solve_kernel(const __grid_constant
     if (ok) {
       tc_fence_after();
       const uint32_t kt = smem_u32(sm.k_tile[0]);
+      #pragma unroll
       for (int ks = 0; ks < 8; ++ks)
-        umma_bf16(tmem, kmajor_desc(kt, 8192, ks), kmajor_desc(kt, 8192, ks), idesc_bf16(64, 64, 0, 0), ks > 0);
+        umma_bf16(tmem, kmajor_step(kmajor_desc(kt, 8192, 0), 8192, ks),
+                  kmajor_step(kmajor_desc(kt, 8192, 0), 8192, ks), idesc_bf16(64, 64, 0, 0), ks > 0);
       if (want_p)
+        #pragma unroll
         for (int ks = 0; ks < 8; ++ks)
-          umma_bf16(tmem + 64, kmajor_desc(smem_u32(q_tile), 8192, ks), kmajor_desc(kt, 8192, ks),
+          umma_bf16(tmem + 64, kmajor_step(kmajor_desc(smem_u32(q_tile), 8192, 0), 8192, ks),
+                    kmajor_step(kmajor_desc(kt, 8192, 0), 8192, ks),
                     idesc_bf16(64, 64, 0, 0), ks > 0);
       umma_commit(&bar_mma);
     }
@@ -736,15 +740,22 @@ __device__ bool affine_apply(const FwdParams& p, ChainCtx& cx, const AffineBufs&
   if (cx.tid == 0) {
     // S as the B operand: K-major (kT) or MN-major rows of a
     auto sdesc = [&](const uint8_t* base, uint32_t stride, int ks) {
-      return kT ? kmajor_desc(smem_u32(base), stride, ks) : mnmajor_desc(smem_u32(base), stride, ks);
+      return kT ? kmajor_step(kmajor_desc(smem_u32(base), stride, 0), stride, ks)
+                : mnmajor_step(mnmajor_desc(smem_u32(base), stride, 0), ks);
     };
     const uint32_t id = idesc_bf16(128, 128, 0, kT ? 0 : 1);
+    #pragma unroll
     for (int ks = 0; ks < 8; ++ks)
-      umma_bf16(cx.tmem + d_col, kmajor_desc(smem_u32(sm.mhi), 16384, ks), sdesc(sm.shi, 16384, ks), id, ks > 0);
+      umma_bf16(cx.tmem + d_col, kmajor_step(kmajor_desc(smem_u32(sm.mhi), 16384, 0), 16384, ks),
+                sdesc(sm.shi, 16384, ks), id, ks > 0);
+    #pragma unroll
     for (int ks = 0; ks < 8; ++ks)
-      umma_bf16(cx.tmem + d_col, kmajor_desc(smem_u32(sm.mhi), 16384, ks), sdesc(sm.slo, sm.slo_stride, ks), id, 1);
+      umma_bf16(cx.tmem + d_col, kmajor_step(kmajor_desc(smem_u32(sm.mhi), 16384, 0), 16384, ks),
+                sdesc(sm.slo, sm.slo_stride, ks), id, 1);
+    #pragma unroll
     for (int ks = 0; ks < 8; ++ks)
-      umma_bf16(cx.tmem + d_col, kmajor_desc(smem_u32(sm.mlo), sm.mlo_stride, ks), sdesc(sm.shi, 16384, ks), id, 1);
+      umma_bf16(cx.tmem + d_col, kmajor_step(kmajor_desc(smem_u32(sm.mlo), sm.mlo_stride, 0), sm.mlo_stride, ks),
+                sdesc(sm.shi, 16384, ks), id, 1);
     umma_commit(cx.bar_mma);
   }
   if (!wait_all(cx.bar_mma, cx.ph_mma)) return false;
@@ -1419,9 +1430,11 @@ __device__ bool run_ws_rec(const FwdParams& p, ChainCtx& cx, WsBars& bb, WsPhase
       auto prep = [&](int j) {
         const uint64_t kb = d_kb[j % kRecStages];
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks) umma_bf16(tm + kRtW, kmajor_step(d_tw[0], 8192, ks), mnmajor_step(kb, ks), i64, ks > 0);
+        for (int ks = 0; ks < 4; ++ks) umma_bf16(tm + kRtW, kmajor_step(d_tw[0], 8192, ks),
+                  mnmajor_step(kb, ks), i64, ks > 0);
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks) umma_bf16(tm + kRtW, kmajor_step(d_tw[1], 8192, ks), mnmajor_step(kb, ks), i64, 1);
+        for (int ks = 0; ks < 4; ++ks) umma_bf16(tm + kRtW, kmajor_step(d_tw[1], 8192, ks),
+                  mnmajor_step(kb, ks), i64, 1);
         umma_commit(&bb.pre_done);
         umma_commit(&bb.emptyq);
       };
@@ -1437,7 +1450,8 @@ __device__ bool run_ws_rec(const FwdParams& p, ChainCtx& cx, WsBars& bb, WsPhase
         const uint32_t dv = tm + kRtV;
         if (kWithU) {
 #pragma unroll
-          for (int ks = 0; ks < 4; ++ks) umma_bf16(dv, kmajor_step(d_tu[0], 8192, ks), mnmajor_step(d_v, ks), i64, ks > 0);
+          for (int ks = 0; ks < 4; ++ks) umma_bf16(dv, kmajor_step(d_tu[0], 8192, ks),
+                    mnmajor_step(d_v, ks), i64, ks > 0);
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks) umma_bf16(dv, kmajor_step(d_tu[1], 8192, ks), mnmajor_step(d_v, ks), i64, 1);
         }
@@ -1460,7 +1474,8 @@ __device__ bool run_ws_rec(const FwdParams& p, ChainCtx& cx, WsBars& bb, WsPhase
         if (*abort) break;
         const uint64_t ka = d_kb[st];
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks) umma_bf16(tm + kRtD2, mnmajor_step(ka, ks), mnmajor_step(d_vs[0], ks), i128, ks > 0);
+        for (int ks = 0; ks < 4; ++ks) umma_bf16(tm + kRtD2, mnmajor_step(ka, ks),
+                  mnmajor_step(d_vs[0], ks), i128, ks > 0);
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks) umma_bf16(tm + kRtD2, mnmajor_step(ka, ks), mnmajor_step(d_vs[1], ks), i128, 1);
         umma_commit(&bb.b_done);
@@ -2027,11 +2042,15 @@ __global__ void __launch_bounds__(kOutThreads) out_kernel(const __grid_constant_
     sync_generic_to_async();
     if (tid == 0) {
       constexpr uint32_t i64 = idesc_bf16(64, 128, 0, 1);
+      #pragma unroll
       for (int ks = 0; ks < 8; ++ks)
-        umma_bf16(tm, kmajor_desc(smem_u32(sm.q[0]), 8192, ks), mnmajor_desc(smem_u32(sm.s[0]), 16384, ks), i64,
+        umma_bf16(tm, kmajor_step(kmajor_desc(smem_u32(sm.q[0]), 8192, 0), 8192, ks),
+                  mnmajor_step(mnmajor_desc(smem_u32(sm.s[0]), 16384, 0), ks), i64,
                   ks > 0);
+      #pragma unroll
       for (int ks = 0; ks < 4; ++ks)
-        umma_bf16(tm, kmajor_desc(smem_u32(sm.p), 8192, ks), mnmajor_desc(smem_u32(sm.vp[0]), 8192, ks), i64, 1);
+        umma_bf16(tm, kmajor_step(kmajor_desc(smem_u32(sm.p), 8192, 0), 8192, ks),
+                  mnmajor_step(mnmajor_desc(smem_u32(sm.vp[0]), 8192, 0), ks), i64, 1);
       umma_commit(&bar_mma);
     }
     ok = wait_all(&bar_mma, 0);
