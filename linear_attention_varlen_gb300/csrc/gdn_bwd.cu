@@ -880,6 +880,7 @@ __global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ Bw
     fence_mbar_init();
   }
   uint32_t ph_p1 = 0, ph_v = 0, ph_tw = 0;
+  bool p1_seen = false;  // the first head's record phase has been waited for
   // bounded wait of every thread on one of the load barriers (uniform outcome)
   auto wait_bar = [&](uint64_t* bar, uint32_t& ph) -> bool {
     if (!wait_all(bar, ph)) return false;
@@ -917,8 +918,15 @@ __global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ Bw
   const int i_row = 16 * cx.q4 + cx.lane;  // row held by this thread in M = 64 accumulators (lane < 16)
   const bool has_row = cx.lane < 16;
 
-  // ---- per key head: Q, K, K K^T, Q K^T
+  // ---- per key head: Q, K, K K^T, Q K^T (the first head's records are already on their way: their
+  // buffers are free at the start)
   if (tid == 0) {
+    // the pieces with their own expect_tx first: the arrival in load_do_gam must come last
+    load_s(0);
+    load_vp(0);
+    load_do_gam(0);
+    load_dvp(0);
+    load_ds(0);
     mbar_arrive_expect_tx(&bar_ld, 4 * 8192);
     tma_load_3d(sm.q[0], &p.tm_q, 0, hk, tok0, &bar_ld);
     tma_load_3d(sm.q[1], &p.tm_q, 64, hk, tok0, &bar_ld);
@@ -942,14 +950,6 @@ __global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ Bw
   }
   __syncthreads();
 
-  if (tid == 0 && ok) {
-    // the pieces with their own expect_tx first: the arrival in load_do_gam must come last
-    load_s(0);
-    load_vp(0);
-    load_do_gam(0);
-    load_dvp(0);
-    load_ds(0);
-  }
   bool first_k = true;
   for (int hh = 0; hh < G && ok; ++hh) {
     const int h = hk * G + hh;
@@ -974,6 +974,7 @@ __global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ Bw
       }
     }
     if (tid < 64) sm.beta[tid] = (tid < n) ? p.beta[(size_t)(tok0 + tid) * Hv + h] : 0.f;
+    p1_seen = true;
     if (!(ok = wait_bar(&bar_p1, ph_p1))) break;
     const float* gam = sm.gam[hh & 1];
     if (tid == 0 && next) {  // the next head's gamma, into the other buffer, on the next phase
@@ -1381,6 +1382,8 @@ __global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ Bw
   } else if (tid == 0) {
     set_status(hd, kErrTimeout);
   }
+  // a CTA that gave up before its first head lets that head's record copies land before it leaves
+  if (tid == 0 && !p1_seen) mbar_wait(&bar_p1, 0, kWaitBudget);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();

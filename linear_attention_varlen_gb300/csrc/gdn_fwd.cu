@@ -1290,10 +1290,10 @@ __device__ bool run_wt(const FwdParams& p, ChainCtx& cx, WtBars& bb, uint32_t& p
 
 // ----------------------------------------------------------------- barriers of the record chain
 struct WsBars {
-  uint64_t full[3], fullq, fullu, empty[3], emptyq, a_done, pre_done, b_done, epi1, staged, epi2, vfree;
+  uint64_t full[3], fullq, fullu, empty[3], emptyq, a_done, pre_done, b_done, u_done, epi1, staged, epi2, vfree;
 };
 struct WsPhase {
-  uint32_t full[3], fullq, fullu, empty[3], emptyq, a_done, pre_done, b_done, epi1, staged, epi2, vfree;
+  uint32_t full[3], fullq, fullu, empty[3], emptyq, a_done, pre_done, b_done, u_done, epi1, staged, epi2, vfree;
 };
 
 
@@ -1314,13 +1314,13 @@ __device__ __forceinline__ void e_handoff(int tid, uint64_t* b1, uint64_t* b2 = 
 // The backward's recompute of the forward chain: the same recurrence with compensated bf16
 // operands (x = hi + lo for T_w, T_u, W, S and V'_s; K and V are exact in bf16), optionally
 // writing the per-chunk records that the gradient kernels read (chunk-start S hi / lo and V'
-// hi / lo as 128B-swizzled images). No output. Roles in the chain's CTA (warp 10 idles):
+// hi / lo as 128B-swizzled images). No output. Roles in the chain's CTA:
 //   warp 8      TMA producer: K and gamma of chunk j into stage j % 3; T_w hi / lo (one buffer,
 //               released by the W product); V and T_u hi / lo (one buffer, released by the U
 //               product).
-//   warp 9      MMA issuer, per chunk j: D_V = T_u V - W S (M = 64; W S as W hi S hi + W hi S lo +
-//               W lo S hi), then chunk j+1's W = T_w K (M = 64), then D2 = K^T (V'_s hi + V'_s lo)
-//               (M = 128).
+//   warp 9      MMA issuer of the state products, per chunk j: D_V -= W S (M = 64; W S as W hi S hi +
+//               W hi S lo + W lo S hi), then D2 = K^T (V'_s hi + V'_s lo) (M = 128).
+//   warp 10     MMA issuer of D_V = T_u V (behind chunk j - 1's D2) and chunk j+1's W = T_w K (M = 64).
 //   warps 0-7   epilogue: -W hi / lo staging, V' (records, V'_s hi / lo), S = e^{gamma_C} S + D2
 //               with its hi / lo staging. A chunk-start state reaches its record by bulk store
 //               straight from the staged images.
@@ -1375,7 +1375,6 @@ __device__ bool run_ws_rec(const FwdParams& p, ChainCtx& cx, WsBars& bb, WsPhase
   const int Hv = p.d.Hv;
   const int32_t* ctok = ws_ptr<int32_t>(p, p.L.chunk_tok0);
   auto rec = [&](int gc) { return (size_t)gc * Hv + h; };
-  if (cx.warp == 10) return true;  // the record chain has one issuer
 
   if (cx.warp == 8) {
     // ------------------------------------------------------------------ TMA producer
@@ -1411,50 +1410,27 @@ __device__ bool run_ws_rec(const FwdParams& p, ChainCtx& cx, WsBars& bb, WsPhase
     }
     return !*abort;
   }
+  // MMA issue in two threads of different sub-partitions (an issuing thread waits for the tensor
+  // pipe at every product and shares its sub-partition's issue slots with two epilogue warps):
+  // warp 9 issues the state products D_V -= W S and D_2, warp 10 U and chunk j + 1's W.
+  const uint32_t tm = cx.tmem;
+  constexpr uint32_t i64 = idesc_bf16(64, 128, 0, 1);
+  constexpr uint32_t i128 = idesc_bf16(128, 128, 1, 1);
+  // k-step-0 descriptors of every operand (the buffers do not move)
+  const uint64_t d_kb0 = mnmajor_desc(smem_u32(sm.k[0]), 8192, 0);  // K stages 16 KB apart
   if (cx.warp == 9) {
-    // ------------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------ issuer of the state products (one lane)
     if (cx.lane == 0) {
-      const uint32_t tm = cx.tmem;
-      constexpr uint32_t i64 = idesc_bf16(64, 128, 0, 1);
-      // k-step-0 descriptors of every operand (the buffers do not move)
-      const uint64_t d_tw[2] = {kmajor_desc(smem_u32(sm.tw[0]), 8192, 0), kmajor_desc(smem_u32(sm.tw[1]), 8192, 0)};
-      const uint64_t d_tu[2] = {kmajor_desc(smem_u32(sm.tu[0]), 8192, 0), kmajor_desc(smem_u32(sm.tu[1]), 8192, 0)};
       const uint64_t d_wn[2] = {kmajor_desc(smem_u32(sm.wn[0]), 8192, 0), kmajor_desc(smem_u32(sm.wn[1]), 8192, 0)};
-      const uint64_t d_kb[kRecStages] = {mnmajor_desc(smem_u32(sm.k[0]), 8192, 0), mnmajor_desc(smem_u32(sm.k[1]), 8192, 0),
-                                         mnmajor_desc(smem_u32(sm.k[2]), 8192, 0)};
-      const uint64_t d_v = mnmajor_desc(smem_u32(sm.v), 8192, 0);
       const uint64_t d_s = mnmajor_desc(smem_u32(sm.s[0]), 16384, 0);
       const uint64_t d_slo = mnmajor_desc(smem_u32(sm.slo[0]), 16384, 0);
       const uint64_t d_vs[2] = {mnmajor_desc(smem_u32(sm.vs[0]), 8192, 0), mnmajor_desc(smem_u32(sm.vslo[0]), 8192, 0)};
-      constexpr uint32_t i128 = idesc_bf16(128, 128, 1, 1);
-      auto prep = [&](int j) {
-        const uint64_t kb = d_kb[j % kRecStages];
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks) umma_bf16(tm + kRtW, kmajor_step(d_tw[0], 8192, ks),
-                  mnmajor_step(kb, ks), i64, ks > 0);
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks) umma_bf16(tm + kRtW, kmajor_step(d_tw[1], 8192, ks),
-                  mnmajor_step(kb, ks), i64, 1);
-        umma_commit(&bb.pre_done);
-        umma_commit(&bb.emptyq);
-      };
-      role_wait(&bb.full[0], ph.full[0], abort);
-      role_wait(&bb.fullq, ph.fullq, abort);
-      if (!*abort) prep(0);
+      const uint32_t dv = tm + kRtV;
       for (int j = 0; j < n && !*abort; ++j) {
-        const int st = j % kRecStages, st1 = (j + 1) % kRecStages;
+        const int st = j % kRecStages;
         role_wait(&bb.staged, ph.staged, abort);
         role_wait(&bb.epi2, ph.epi2, abort);
-        if (kWithU) role_wait(&bb.fullu, ph.fullu, abort);
-        if (*abort) break;
-        const uint32_t dv = tm + kRtV;
-        if (kWithU) {
-#pragma unroll
-          for (int ks = 0; ks < 4; ++ks) umma_bf16(dv, kmajor_step(d_tu[0], 8192, ks),
-                    mnmajor_step(d_v, ks), i64, ks > 0);
-#pragma unroll
-          for (int ks = 0; ks < 4; ++ks) umma_bf16(dv, kmajor_step(d_tu[1], 8192, ks), mnmajor_step(d_v, ks), i64, 1);
-        }
+        if (kWithU) role_wait(&bb.u_done, ph.u_done, abort);  // U(j) is in D_V
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks)
           umma_bf16(dv, kmajor_step(d_wn[0], 8192, ks), mnmajor_step(d_s, ks), i64, (kWithU || ks > 0) ? 1 : 0);
@@ -1463,25 +1439,59 @@ __device__ bool run_ws_rec(const FwdParams& p, ChainCtx& cx, WsBars& bb, WsPhase
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) umma_bf16(dv, kmajor_step(d_wn[1], 8192, ks), mnmajor_step(d_s, ks), i64, 1);
         umma_commit(&bb.a_done);
-        if (kWithU) umma_commit(&bb.vfree);
-        if (j + 1 < n) {
-          role_wait(&bb.full[st1], ph.full[st1], abort);
-          role_wait(&bb.fullq, ph.fullq, abort);
-          if (*abort) break;
-          prep(j + 1);
-        }
         role_wait(&bb.epi1, ph.epi1, abort);
-        if (*abort) break;
-        const uint64_t ka = d_kb[st];
+        const uint64_t ka = d_kb0 + (uint64_t)(st * (16384 >> 4));
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks) umma_bf16(tm + kRtD2, mnmajor_step(ka, ks),
-                  mnmajor_step(d_vs[0], ks), i128, ks > 0);
+        for (int ks = 0; ks < 4; ++ks) umma_bf16(tm + kRtD2, mnmajor_step(ka, ks), mnmajor_step(d_vs[0], ks), i128, ks > 0);
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks) umma_bf16(tm + kRtD2, mnmajor_step(ka, ks), mnmajor_step(d_vs[1], ks), i128, 1);
         umma_commit(&bb.b_done);
         umma_commit(&bb.empty[st]);
       }
       role_wait(&bb.epi2, ph.epi2, abort);  // the epilogue's last state hand-off
+    }
+    return !*abort;
+  }
+  if (cx.warp == 10) {
+    // ------------------------------------------------ issuer of U and W (one lane)
+    if (cx.lane == 0) {
+      const uint64_t d_tw[2] = {kmajor_desc(smem_u32(sm.tw[0]), 8192, 0), kmajor_desc(smem_u32(sm.tw[1]), 8192, 0)};
+      const uint64_t d_tu[2] = {kmajor_desc(smem_u32(sm.tu[0]), 8192, 0), kmajor_desc(smem_u32(sm.tu[1]), 8192, 0)};
+      const uint64_t d_v = mnmajor_desc(smem_u32(sm.v), 8192, 0);
+      const uint32_t dv = tm + kRtV;
+      auto prep = [&](int j) {  // W(j): the staging of chunk j - 1 has read W (its state product has run)
+        role_wait(&bb.full[j % kRecStages], ph.full[j % kRecStages], abort);
+        role_wait(&bb.fullq, ph.fullq, abort);
+        const uint64_t kb = d_kb0 + (uint64_t)((j % kRecStages) * (16384 >> 4));
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) umma_bf16(tm + kRtW, kmajor_step(d_tw[0], 8192, ks), mnmajor_step(kb, ks), i64, ks > 0);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) umma_bf16(tm + kRtW, kmajor_step(d_tw[1], 8192, ks), mnmajor_step(kb, ks), i64, 1);
+        umma_commit(&bb.pre_done);
+        umma_commit(&bb.emptyq);
+      };
+      auto issue_u = [&]() {  // U(j) into D_V: the V' epilogue of chunk j - 1 has read it
+        role_wait(&bb.fullu, ph.fullu, abort);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) umma_bf16(dv, kmajor_step(d_tu[0], 8192, ks), mnmajor_step(d_v, ks), i64, ks > 0);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) umma_bf16(dv, kmajor_step(d_tu[1], 8192, ks), mnmajor_step(d_v, ks), i64, 1);
+        umma_commit(&bb.u_done);
+        umma_commit(&bb.vfree);
+      };
+      prep(0);
+      if (kWithU) issue_u();
+      for (int j = 0; j < n && !*abort; ++j) {
+        role_wait(&bb.a_done, ph.a_done, abort);  // the state product of chunk j has run
+        if (j + 1 < n) prep(j + 1);
+        role_wait(&bb.epi1, ph.epi1, abort);  // V'(j) is read: D_V is free
+        if (kWithU && j + 1 < n) {
+          role_wait(&bb.b_done, ph.b_done, abort);  // behind D_2 in the tensor pipe
+          issue_u();
+        } else {
+          role_wait(&bb.b_done, ph.b_done, abort);
+        }
+      }
     }
     return !*abort;
   }
@@ -1691,6 +1701,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) chain_kernel(const __grid_const
       mbar_init(&wbars.a_done, 1);
       mbar_init(&wbars.pre_done, 1);
       mbar_init(&wbars.b_done, 1);
+      mbar_init(&wbars.u_done, 1);
       mbar_init(&wbars.epi1, 1);
       mbar_init(&wbars.staged, 1);
       mbar_init(&wbars.epi2, 1);
