@@ -102,7 +102,7 @@ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // Forward workspace layout (byte offsets from the workspace base).
 struct FwdLayout {
   size_t header, seq_chunk0, seq_seg0, chunk_seq, chunk_tok0, chunk_len, seg_info, seg_slot, p1_list;
-  size_t flags_seg, flags_fin, mzero, gam, fac, contr, tw, tu, pimg, pub, mmat, bmat, total;
+  size_t flags_seg, flags_fin, flags_p1, walk_ctr, mzero, gam, fac, contr, tw, tu, pimg, pub, mmat, bmat, mimg, total;
   int64_t cmax, smax, slots;
 };
 
@@ -129,6 +129,10 @@ inline FwdLayout fwd_layout(const PlanDims& d) {
   L.p1_list = take(sizeof(int32_t) * 2 * (2 * L.slots + 1));
   L.flags_seg = take(sizeof(int32_t) * (size_t)L.smax * d.Hv);
   L.flags_fin = take(sizeof(int32_t) * (size_t)(d.N + 1) * d.Hv);
+  L.flags_p1 = take(sizeof(int32_t) * ((size_t)L.slots * d.Hv + 1));  // a segment's M and B are written
+  // per (document, value head): pass-1 units that compute a transition M and a local end state B,
+  // and units that have decided (the first count is final once the second is complete)
+  L.walk_ctr = take(sizeof(int32_t) * 2 * (size_t)(d.N + 1) * d.Hv);
   L.mzero = take(sizeof(int32_t) * ((size_t)L.slots * d.Hv + 1));
   L.gam = take(sizeof(float) * (size_t)L.cmax * d.Hv * kChunk);
   L.fac = take(sizeof(float) * (size_t)L.cmax * d.Hv * kFacFloats);
@@ -140,6 +144,7 @@ inline FwdLayout fwd_layout(const PlanDims& d) {
   const bool exact = d.mode == 0;
   L.mmat = take(exact ? state * (size_t)L.slots * d.Hv : 0);
   L.bmat = take(exact ? state * (size_t)L.slots * d.Hv : 0);
+  L.mimg = take(exact ? state * (size_t)L.slots * d.Hv : 0);  // M as compensated bf16 operand images
   L.total = o;
   return L;
 }

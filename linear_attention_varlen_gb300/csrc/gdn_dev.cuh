@@ -38,6 +38,20 @@ __device__ __forceinline__ bool wait_flag(const int* flag, Header* hd, long long
   return true;
 }
 
+// Waits (bounded as wait_flag) until the counter *ctr reaches `target`.
+__device__ __forceinline__ bool wait_count(const int* ctr, int target, Header* hd, long long budget) {
+  const long long t0 = clock64();
+  while (ld_acquire(ctr) < target) {
+    if (get_status(hd) != 0) return false;
+    if (clock64() - t0 > budget) {
+      set_status(hd, kErrTimeout);
+      return false;
+    }
+    __nanosleep(64);
+  }
+  return true;
+}
+
 // All threads of the CTA wait on `bar`; the outcome is made uniform with a vote so that no
 // thread leaves while others still expect a barrier. On failure each thread waits once more
 // (bounded) so that copies or MMAs still in flight can land before the caller gives up.

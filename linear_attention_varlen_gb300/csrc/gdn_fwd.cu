@@ -148,6 +148,10 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
   int32_t* ff = ws_ptr<int32_t>(p, p.L.flags_fin);
   for (int e = tid; e < total_segs * p.d.Hv; e += nt) fs[e] = 0;
   for (int e = tid; e < N * p.d.Hv; e += nt) ff[e] = 0;
+  int32_t* wc = ws_ptr<int32_t>(p, p.L.walk_ctr);
+  for (int e = tid; e < 2 * N * p.d.Hv; e += nt) wc[e] = 0;
+  int32_t* fp1 = ws_ptr<int32_t>(p, p.L.flags_p1);
+  for (int e = tid; e < (int)p.L.slots * p.d.Hv; e += nt) fp1[e] = 0;
   int32_t* mz = ws_ptr<int32_t>(p, p.L.mzero);
   if (!keep_mzero)
     for (int e = tid; e < (int)p.L.slots * p.d.Hv; e += nt) mz[e] = 0;
@@ -162,7 +166,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
   __syncthreads();
   for (int base = 0; base < total_segs; base += nt) {
     const int s = base + tid;
-    int need = 0, units = 0;
+    int need = 0, units = 0, known_start = 0;
     if (s < total_segs) {
       // the segment's document and dependency, recomputed (the table above is in global memory)
       int32_t info[4];
@@ -171,7 +175,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
       const bool last = (s + 1 == seq_seg0[i + 1]);
       const bool split = (seq_seg0[i + 1] - seq_seg0[i]) > 1;
       need = (split && !last && p.d.mode == 0) ? 1 : 0;
-      units = need ? (info[3] == -1 ? 1 : 2) : 0;
+      units = need;
+      known_start = info[3] == -1 ? 1 : 0;
     }
     const int mine = (need << 16) | units;  // a tile holds at most nt segments: no carry between the halves
     s_scan[tid] = mine;
@@ -187,15 +192,10 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
       const int sl = s_carry[0] + (excl >> 16), u = s_carry[1] + (excl & 0xFFFF);
       slot[s] = (need && sl < p.L.slots) ? sl : -1;
       if (need && sl < p.L.slots) {
-        if (units == 1) {
-          p1[2 * u] = s;
-          p1[2 * u + 1] = 2;  // end state from the known start, published directly
-        } else {
-          p1[2 * u] = s;
-          p1[2 * u + 1] = 0;  // transition M
-          p1[2 * u + 2] = s;
-          p1[2 * u + 3] = 1;  // end state from zero B
-        }
+        p1[2 * u] = s;
+        // 2: the end state from the document's known start; 0: the transition M and the end state
+        // B from zero, or, when the segment's own start warms up, its end state directly
+        p1[2 * u + 1] = known_start ? 2 : 0;
       }
     }
     __syncthreads();
@@ -667,6 +667,26 @@ __device__ __forceinline__ void load_state_t(const ChainCtx& cx, const float* sr
 #pragma unroll
   for (int c = 0; c < 64; ++c) S[c] = cg ? __ldcg(col + (size_t)c * kDim) : col[(size_t)c * kDim];
 }
+// The 64 values a thread holds (its row r = 32 q4 + lane of block `half`) as compensated bf16
+// operand images hi (dst) and lo (dst + 32 KB): 128-byte rows, two blocks of 128 rows 16 KB apart,
+// 16-byte granules swizzled by the row (the SW128 pattern). From the transposed layout (column b of
+// S) this is S^T-as-operand MN-major (row b); from the record chain's row layout, K-major (row a).
+__device__ __forceinline__ void store_images(const ChainCtx& cx, uint8_t* dst, const float* S) {
+  const int r = 32 * cx.q4 + cx.lane;
+  uint8_t* hi = dst + cx.half * 16384 + r * 128;
+#pragma unroll
+  for (int cj = 0; cj < 8; ++cj) {
+    float lo[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) lo[u] = S[8 * cj + u] - __bfloat162float(__float2bfloat16_rn(S[8 * cj + u]));
+    const uint32_t g = (cj ^ (r & 7)) << 4;
+    *reinterpret_cast<uint4*>(hi + g) =
+        make_uint4(pack_bf16x2(S[8 * cj], S[8 * cj + 1]), pack_bf16x2(S[8 * cj + 2], S[8 * cj + 3]),
+                   pack_bf16x2(S[8 * cj + 4], S[8 * cj + 5]), pack_bf16x2(S[8 * cj + 6], S[8 * cj + 7]));
+    *reinterpret_cast<uint4*>(hi + 32768 + g) = make_uint4(pack_bf16x2(lo[0], lo[1]), pack_bf16x2(lo[2], lo[3]),
+                                                           pack_bf16x2(lo[4], lo[5]), pack_bf16x2(lo[6], lo[7]));
+  }
+}
 __device__ __forceinline__ void save_state_t(const ChainCtx& cx, float* dst, const float* S) {
   float* col = dst + (size_t)(64 * cx.half) * kDim + 32 * cx.q4 + cx.lane;
 #pragma unroll
@@ -685,6 +705,38 @@ struct AffineBufs {
   float* stage;         // 32 KB of fp32 staging for the product
 };
 
+// M (row-major fp32, 128 x 128) as compensated bf16 images hi / lo, K-major with rows a and two
+// 64-column blocks 16 KB apart (hi) or mlo_stride apart (lo): 256 threads, 16 per 512-byte row,
+// four 32-byte pieces in flight.
+__device__ __forceinline__ void stage_m_hilo(const float* Mm, uint8_t* mhi, uint8_t* mlo, uint32_t mlo_stride,
+                                           int tid) {
+#pragma unroll
+  for (int k0 = 0; k0 < 8; k0 += 4) {
+    float4 mv[8];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int e = tid + 256 * (k0 + k);
+      const float* src = Mm + (size_t)(e >> 4) * kDim + 8 * (e & 15);
+      mv[2 * k] = __ldcg(reinterpret_cast<const float4*>(src));
+      mv[2 * k + 1] = __ldcg(reinterpret_cast<const float4*>(src + 4));
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int e = tid + 256 * (k0 + k), r = e >> 4, c8 = e & 15, cj = c8 & 7;
+      const float x[8] = {mv[2 * k].x, mv[2 * k].y, mv[2 * k].z, mv[2 * k].w,
+                          mv[2 * k + 1].x, mv[2 * k + 1].y, mv[2 * k + 1].z, mv[2 * k + 1].w};
+      float lo[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) lo[u] = x[u] - __bfloat162float(__float2bfloat16_rn(x[u]));
+      const uint32_t off = r * 128 + ((cj ^ (r & 7)) << 4);
+      *reinterpret_cast<uint4*>(mhi + (c8 >> 3) * 16384 + off) = make_uint4(
+          pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]), pack_bf16x2(x[4], x[5]), pack_bf16x2(x[6], x[7]));
+      *reinterpret_cast<uint4*>(mlo + (c8 >> 3) * mlo_stride + off) = make_uint4(
+          pack_bf16x2(lo[0], lo[1]), pack_bf16x2(lo[2], lo[3]), pack_bf16x2(lo[4], lo[5]), pack_bf16x2(lo[6], lo[7]));
+    }
+  }
+}
+
 // out = M S_start + B (B may be null) on the tensor cores with compensated bf16 operands (x = hi + lo):
 // M hi S hi + M hi S lo + M lo S hi, accumulated in the TMEM columns d_col .. d_col + 127. kT: S is
 // held transposed (the inference chain) and both of its images are written here, K-major (row b,
@@ -694,32 +746,7 @@ template <bool kT>
 __device__ bool affine_apply(const FwdParams& p, ChainCtx& cx, const AffineBufs& sm, const float* Mm,
                              const float* Bm, const float* S, float* out, uint32_t d_col) {
   if (cx.tid < 256) {
-    // M hi / lo from coalesced loads (16 threads per 512-byte row), four 32-byte pieces in flight
-#pragma unroll
-    for (int k0 = 0; k0 < 8; k0 += 4) {
-      float4 mv[8];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int e = cx.tid + 256 * (k0 + k);
-        const float* src = Mm + (size_t)(e >> 4) * kDim + 8 * (e & 15);
-        mv[2 * k] = __ldcg(reinterpret_cast<const float4*>(src));
-        mv[2 * k + 1] = __ldcg(reinterpret_cast<const float4*>(src + 4));
-      }
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int e = cx.tid + 256 * (k0 + k), r = e >> 4, c8 = e & 15, cj = c8 & 7;
-        const float x[8] = {mv[2 * k].x, mv[2 * k].y, mv[2 * k].z, mv[2 * k].w,
-                            mv[2 * k + 1].x, mv[2 * k + 1].y, mv[2 * k + 1].z, mv[2 * k + 1].w};
-        float lo[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) lo[u] = x[u] - __bfloat162float(__float2bfloat16_rn(x[u]));
-        const uint32_t off = r * 128 + ((cj ^ (r & 7)) << 4);
-        *reinterpret_cast<uint4*>(sm.mhi + (c8 >> 3) * 16384 + off) = make_uint4(
-            pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]), pack_bf16x2(x[4], x[5]), pack_bf16x2(x[6], x[7]));
-        *reinterpret_cast<uint4*>(sm.mlo + (c8 >> 3) * sm.mlo_stride + off) = make_uint4(
-            pack_bf16x2(lo[0], lo[1]), pack_bf16x2(lo[2], lo[3]), pack_bf16x2(lo[4], lo[5]), pack_bf16x2(lo[6], lo[7]));
-      }
-    }
+    stage_m_hilo(Mm, sm.mhi, sm.mlo, sm.mlo_stride, cx.tid);
     // S lo (and for kT S hi): this thread's 64 values, row rr of the image's block `half`
     const int rr = 32 * cx.q4 + cx.lane;  // (threads below 256 only)
     uint8_t* slo = sm.slo + cx.half * sm.slo_stride;
@@ -1611,7 +1638,11 @@ __device__ __forceinline__ void publish(int* flag) {
 
 // kRec: the backward's recompute (compensated arithmetic, records in the output pass); otherwise
 // the forward. Both warp-specialized, 352 threads.
-constexpr int kTransWindow = 12;  // chunks of the transition evaluated first (see pass 1, part 0)
+// The cross-segment walk borrows 192 KB of the chain's shared memory for M and the operand images
+// and keeps two bytes per segment after them.
+constexpr int kWalkWindow = 4096;
+constexpr size_t kWalkFlagsAt = 196608;
+static_assert(kWalkFlagsAt + 2 * (kWalkWindow + 64) + 1024 <= kSmemBytes, "walk buffers fit the chain's shared memory");
 
 template <int kMode, bool kRec>
 __global__ void __launch_bounds__(kWsThreads, 1) chain_kernel(const __grid_constant__ FwdParams p) {
@@ -1642,7 +1673,10 @@ __global__ void __launch_bounds__(kWsThreads, 1) chain_kernel(const __grid_const
   memset(&ph, 0, sizeof(ph));
   uint32_t tph = 0;  // phase bits of the inference chain's barriers
   const int Hv = p.d.Hv, G = p.d.Hv / p.d.Hk;
-  const int n_items = (kMode == kModeOut ? hd->n_segs : hd->n_p1) * Hv;
+  // pass 1: one ticket per (unit, value head), then one per (unit, value head) for the walk that
+  // composes a document's segment maps (only units of a document's first segment walk)
+  const int n_unit_items = (kMode == kModeOut ? 0 : hd->n_p1) * Hv;
+  const int n_items = kMode == kModeOut ? hd->n_segs * Hv : 2 * n_unit_items;
   if (blockIdx.x >= n_items || get_status(hd) != 0) return;
   const int32_t* si = ws_ptr<int32_t>(p, p.L.seg_info);
   const int32_t* slot = ws_ptr<int32_t>(p, p.L.seg_slot);
@@ -1651,18 +1685,44 @@ __global__ void __launch_bounds__(kWsThreads, 1) chain_kernel(const __grid_const
   const int32_t* contr = ws_ptr<int32_t>(p, p.L.contr);
 
   // Pass 1: a unit serves the next segment's start, unless that segment warms up; the transition
-  // also serves the reverse chain's publication of this segment's start gradient (record mode).
-  // All threads call this (the window evaluation is warp-wide).
+  // also serves the reverse chain's publication of this segment's start gradient (record mode). A
+  // walk runs for a document whose first segment starts from a known state and that has middle
+  // segments. All threads call this (the window evaluation is warp-wide).
+  const int32_t* p1 = ws_ptr<int32_t>(p, p.L.p1_list);
+  const int32_t* dch = ws_ptr<int32_t>(p, p.L.seq_chunk0);
+  auto rev_needs_m = [&](int s, int part, int seq, int c0, int h) -> bool {
+    return kRec && part == 0 && s != seq_seg0[seq] && warm_fwd(gam_ws, contr, Hv, h, c0, dch[seq + 1]) < 0;
+  };
+  // A unit records its decision per (document, value head) when it draws its ticket: a walk
+  // waits for every unit of its document and has nothing to do when none computes M and B.
+  int* walk_ctr = ws_ptr<int>(p, p.L.walk_ctr);
   auto p1_skips = [&](int item) -> bool {
-    const int32_t* p1 = ws_ptr<int32_t>(p, p.L.p1_list);
-    const int unit = item / Hv, h = item % Hv;
+    const bool walk = item >= n_unit_items;
+    const int idx = walk ? item - n_unit_items : item;
+    const int unit = idx / Hv, h = idx % Hv;
     const int s = p1[2 * unit], part = p1[2 * unit + 1];
     const int seq = si[4 * s], c0 = si[4 * s + 1], nch = si[4 * s + 2];
-    const int32_t* dch = ws_ptr<int32_t>(p, p.L.seq_chunk0);
+    int* ctr = walk_ctr + 2 * ((size_t)seq * Hv + h);
+    if (walk) {
+      const int n_units = seq_seg0[seq + 1] - seq_seg0[seq] - 1;  // every split segment but the last
+      if (part != 2 || n_units < 2) return true;
+      if (cx.tid == 0) {
+        const bool ok = wait_count(ctr + 1, n_units, hd, p.flag_budget);
+        s_ok = (ok && __ldcg(ctr) > 0) ? 1 : 0;
+      }
+      __syncthreads();
+      const bool skip = s_ok == 0;
+      __syncthreads();
+      return skip;
+    }
     const bool next_warms = warm_back(gam_ws, contr, Hv, h, c0 + nch, dch[seq]) >= 0;
-    const bool rev_needs_m =
-        kRec && part == 0 && s != seq_seg0[seq] && warm_fwd(gam_ws, contr, Hv, h, c0, dch[seq + 1]) < 0;
-    return next_warms && !rev_needs_m;
+    const bool own_warms = part == 0 && si[4 * s + 3] >= 0 && warm_back(gam_ws, contr, Hv, h, c0, dch[seq]) >= 0;
+    if (cx.tid == 0) {
+      if (part == 0 && !next_warms && !own_warms) atomicAdd(ctr, 1);  // computes M and B
+      __threadfence();
+      atomicAdd(ctr + 1, 1);
+    }
+    return next_warms && !rev_needs_m(s, part, seq, c0, h);
   };
   // Pass 1 claims its tickets before it sets anything up: when every unit it draws is skipped
   // (each boundary warms up), the CTA leaves without touching tensor memory or barriers.
@@ -1718,6 +1778,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) chain_kernel(const __grid_const
 
   int* flags_seg = ws_ptr<int>(p, p.L.flags_seg);
   int* flags_fin = ws_ptr<int>(p, p.L.flags_fin);
+  int* flags_p1 = ws_ptr<int>(p, p.L.flags_p1);
   int* mzero = ws_ptr<int>(p, p.L.mzero);
   const size_t st_elems = (size_t)kDim * kDim;
   float S[64];
@@ -1781,6 +1842,170 @@ __global__ void __launch_bounds__(kWsThreads, 1) chain_kernel(const __grid_const
       return affine_apply<true>(p, cx, affine_bufs(*wts), Mm, Bm, S, out, kTtD2);
   };
 
+  // wait (uniform outcome) for a publication flag
+  auto wait_uniform = [&](const int* flag) -> bool {
+    if (cx.tid == 0) {
+      s_ok = wait_flag(flag, hd, p.flag_budget) ? 1 : 0;
+      __threadfence();
+    }
+    __syncthreads();
+    const bool r = s_ok != 0;
+    __syncthreads();
+    return r;
+  };
+  // Cross-segment fix-up of one document and value head (pass 1, after the units it reads): the
+  // end state of every middle segment whose successor does not warm up and whose own start does
+  // not warm up (those publish their own), in segment order: E_s = M_s E_{s-1} + B_s, or E_s = B_s
+  // for an exactly zero transition. Each is published as soon as it is written (its flag after
+  // the next product is issued), so no output item waits on another output item.
+  // E is held transposed (thread: column b = 32 q4 + lane, rows a = 64 half + c) and the product
+  // runs as E^T M^T on the tensor cores with compensated bf16 operands; the units stored M's
+  // operand images, and they and B arrive by bulk copies while the previous step finishes.
+  // Which segment starts warm up, the units' flags and their zero findings are read up front,
+  // kWalkWindow segments at a time.
+  auto walk_document = [&](int s0, int seq, int h) -> bool {
+    float* pub = ws_ptr<float>(p, p.L.pub);
+    float* bmat = ws_ptr<float>(p, p.L.bmat);
+    const uint8_t* mimg = ws_ptr<uint8_t>(p, p.L.mimg);
+    auto at = [&](float* b, int s) { return b + ((size_t)slot[s] * Hv + h) * st_elems; };
+    float* bf = reinterpret_cast<float*>(base);  // B fp32 (bulk copy)
+    uint8_t* mhi = base + 65536;                 // M hi / lo images (bulk copy, 64 KB)
+    uint8_t* mlo = base + 98304;
+    uint8_t* ehi = base + 131072;                // E^T hi / lo images, K-major rows b
+    uint8_t* warms = base + kWalkFlagsAt;        // warms[s - w0]: segment s starts with a warm-up
+    uint8_t* mz = warms + kWalkWindow + 64;      // mz[s - w0]: M_s is exactly zero
+    const uint32_t dcol = kRec ? kRtV : kTtD2;
+    // B = M^T: MN-major images from the transposed chain's layout, K-major from the record chain's
+    const uint32_t id = idesc_bf16(128, 128, 0, kRec ? 0 : 1);
+    auto mdesc = [&](const uint8_t* img, int ks) {
+      return kRec ? kmajor_step(kmajor_desc(smem_u32(img), 16384, 0), 16384, ks)
+                  : mnmajor_step(mnmajor_desc(smem_u32(img), 16384, 0), ks);
+    };
+    const int s_last = seq_seg0[seq + 1] - 1;  // its end state is the final state
+    const int b = 32 * cx.q4 + cx.lane;
+    bool have = false;     // E_{s-1} is in S
+    bool inflight = false; // bulk copies into bf / mhi are in flight
+    int pend = -1;         // segment whose end state is written but not yet flagged
+    auto bail = [&]() -> bool {
+      if (inflight) wait_all(cx.bar_ld, cx.ph_ld);  // (the copies land before the walk gives up)
+      return false;
+    };
+    auto fetch = [&](int s) {  // M_s images and B_s into shared memory
+      if (cx.tid == 0) {
+        fence_proxy_async_global();  // (written through the generic proxy by the units)
+        mbar_arrive_expect_tx(cx.bar_ld, 131072);
+        bulk_load(mhi, mimg + ((size_t)slot[s] * Hv + h) * 65536, 65536, cx.bar_ld);
+        bulk_load(bf, at(bmat, s), 65536, cx.bar_ld);
+      }
+      inflight = true;
+    };
+    for (int w0 = s0 + 1; w0 < s_last; w0 += kWalkWindow) {
+      const int w1 = min(w0 + kWalkWindow, s_last);
+      for (int s = w0 + cx.warp; s <= w1; s += kWsThreads / 32) {  // (warp-uniform)
+        const bool wv = warm_back(gam_ws, contr, Hv, h, si[4 * s + 1], dch[seq]) >= 0;
+        if (cx.lane == 0) warms[s - w0] = wv ? 1 : 0;
+      }
+      __syncthreads();
+      auto computed = [&](int s) { return !warms[s - w0] && !warms[s - w0 + 1]; };
+      bool fail = false;
+      for (int s = w0 + cx.tid; s < w1; s += kWsThreads) {
+        if (!computed(s)) continue;
+        if (!wait_flag(&flags_p1[slot[s] * Hv + h], hd, p.flag_budget)) {
+          fail = true;
+          break;
+        }
+        mz[s - w0] = __ldcg(&mzero[slot[s] * Hv + h]) ? 1 : 0;
+      }
+      if (__syncthreads_or(fail)) return bail();
+      auto next_m = [&](int from) {  // the next segment whose step runs the product
+        while (from < w1 && !(computed(from) && !mz[from - w0])) ++from;
+        return from;
+      };
+      if (next_m(w0) < w1) fetch(next_m(w0));
+      for (int s = w0; s < w1; ++s) {
+        if (!computed(s)) {
+          if (pend >= 0) publish(&flags_seg[pend * Hv + h]);
+          pend = -1;
+          have = false;
+          continue;
+        }
+        if (mz[s - w0]) {
+          if (epi) load_state_t(cx, at(bmat, s), S, true);
+        } else {
+          if (!have) {  // published by its own unit (a known start or a warm-up)
+            if (!wait_uniform(&flags_seg[(s - 1) * Hv + h])) return bail();
+            if (epi) load_state_t(cx, at(pub, s - 1), S, true);
+          }
+          if (epi) {  // E^T hi / lo, K-major (row b, 64 values of a per block)
+            uint8_t* eh = ehi + cx.half * 16384;
+#pragma unroll
+            for (int cj = 0; cj < 8; ++cj) {
+              float lo[8];
+#pragma unroll
+              for (int u = 0; u < 8; ++u)
+                lo[u] = S[8 * cj + u] - __bfloat162float(__float2bfloat16_rn(S[8 * cj + u]));
+              const uint32_t off = b * 128 + ((cj ^ (b & 7)) << 4);
+              *reinterpret_cast<uint4*>(eh + off) =
+                  make_uint4(pack_bf16x2(S[8 * cj], S[8 * cj + 1]), pack_bf16x2(S[8 * cj + 2], S[8 * cj + 3]),
+                             pack_bf16x2(S[8 * cj + 4], S[8 * cj + 5]), pack_bf16x2(S[8 * cj + 6], S[8 * cj + 7]));
+              *reinterpret_cast<uint4*>(eh + 32768 + off) = make_uint4(pack_bf16x2(lo[0], lo[1]), pack_bf16x2(lo[2], lo[3]),
+                                                                       pack_bf16x2(lo[4], lo[5]), pack_bf16x2(lo[6], lo[7]));
+            }
+          }
+          if (!wait_all(cx.bar_ld, cx.ph_ld)) return false;  // M_s and B_s have landed
+          cx.ph_ld ^= 1;
+          inflight = false;
+          sync_generic_to_async();
+          if (cx.tid == 0) {
+            const uint64_t ah0 = kmajor_desc(smem_u32(ehi), 16384, 0);
+            const uint64_t al0 = kmajor_desc(smem_u32(ehi + 32768), 16384, 0);
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks)
+              umma_bf16(cx.tmem + dcol, kmajor_step(ah0, 16384, ks), mdesc(mhi, ks), id, ks > 0);
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks)
+              umma_bf16(cx.tmem + dcol, kmajor_step(al0, 16384, ks), mdesc(mhi, ks), id, 1);
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks)
+              umma_bf16(cx.tmem + dcol, kmajor_step(ah0, 16384, ks), mdesc(mlo, ks), id, 1);
+            umma_commit(cx.bar_mma);
+          }
+          if (pend >= 0 && cx.tid == kWsThreads - 32) {  // (a thread outside the epilogue)
+            // the previous end state was stored before the barrier above
+            __threadfence();
+            st_release(&flags_seg[pend * Hv + h], 1);
+          }
+          pend = -1;
+          if (!wait_all(cx.bar_mma, cx.ph_mma)) return bail();
+          cx.ph_mma ^= 1;
+          tc_fence_after();
+          if (epi) {
+            const uint32_t lane_base = (uint32_t)(32 * cx.q4) << 16;
+#pragma unroll
+            for (int hc = 0; hc < 4; ++hc) {
+              float d[16];
+              tmem_ld16(cx.tmem + dcol + lane_base + 64 * cx.half + 16 * hc, d);
+              tmem_ld_wait();
+#pragma unroll
+              for (int j = 0; j < 16; ++j) S[16 * hc + j] = d[j] + bf[(64 * cx.half + 16 * hc + j) * kDim + b];
+            }
+          }
+          tc_fence_before();
+          __syncthreads();  // bf and the images are consumed
+          const int sf = next_m(s + 1);
+          if (sf < w1) fetch(sf);
+        }
+        if (pend >= 0) publish(&flags_seg[pend * Hv + h]);
+        if (epi) save_state_t(cx, at(pub, s), S);
+        pend = s;
+        have = true;
+      }
+      __syncthreads();  // (the next window's flags overwrite these)
+    }
+    if (pend >= 0) publish(&flags_seg[pend * Hv + h]);
+    return true;
+  };
+
   for (;;) {
     if (first_item < 0 && cx.tid == 0) {
       const int it = (int)atomicAdd(kMode == kModeOut ? &hd->q_chain : &hd->q_p1, 1u);
@@ -1793,8 +2018,8 @@ __global__ void __launch_bounds__(kWsThreads, 1) chain_kernel(const __grid_const
     const int h = item % Hv, hk = h / G;
     bool ok = true;
     if (kMode == kModeP1) {
-      const int32_t* p1 = ws_ptr<int32_t>(p, p.L.p1_list);
-      const int unit = item / Hv;
+      const bool walk = item >= n_unit_items;
+      const int unit = (walk ? item - n_unit_items : item) / Hv;
       const int s = p1[2 * unit], part = p1[2 * unit + 1];
       const int seq = si[4 * s], c0 = si[4 * s + 1], nch = si[4 * s + 2];
       const int sl = slot[s];
@@ -1802,53 +2027,70 @@ __global__ void __launch_bounds__(kWsThreads, 1) chain_kernel(const __grid_const
         __syncthreads();  // every thread has read s_item before the next ticket
         continue;
       }
-      float* mdst = ws_ptr<float>(p, p.L.mmat) + ((size_t)sl * Hv + h) * st_elems;
-      bool m_zero = false;
-      if (part == 0) {
-        // Transition M = Phi_last ... Phi_first, evaluated as Y X with Y the product over the
-        // last kTransWindow chunks (a chain from I). When Y is exactly zero so is M, and the
-        // segment boundary needs no start state; otherwise X (chain from I over the first
-        // chunks) and M = Y X.
-        const int w = nch < kTransWindow ? nch : kTransWindow;
-        set_identity();
-        store_s();
-        sync_generic_to_async();
-        if (!run_fast(c0 + nch - w, c0 + nch, c0 + nch, h, hk, false)) break;
-        m_zero = all_zero();
-        if (epi) sv_state(mdst);
-        if (!m_zero && w < nch) {
-          set_identity();
-          store_s();
-          sync_generic_to_async();
-          if (!run_fast(c0, c0 + nch - w, c0 + nch, h, hk, false)) break;
-          __syncthreads();  // Y is in global memory
-          store_s();        // X for the product
-          sync_generic_to_async();
-          if (!affine(mdst, nullptr, mdst)) {
-            set_status(hd, kErrTimeout);
-            break;
-          }
+      if (walk) {
+        if (!walk_document(s, seq, h)) {
+          set_status(hd, kErrTimeout);
+          break;
         }
-      } else {
-        if (part == 1) {
+        __syncthreads();
+        continue;
+      }
+      // the next segment needs this segment's end state (it does not warm up)
+      const bool need_e = warm_back(gam_ws, contr, Hv, h, c0 + nch, dch[seq]) < 0;
+      if (part == 2) {
+        // the end state from the document's known start, published directly
+        const int x = p.init_idx ? p.init_idx[seq] : -1;
+        if (epi && x >= 0 && x < p.d.n_init)
+          ld_state(p.initial_state + ((size_t)x * Hv + h) * st_elems, false);
+        else
           set_zero();
-        } else {
-          const int x = p.init_idx ? p.init_idx[seq] : -1;
-          if (epi && x >= 0 && x < p.d.n_init)
-            ld_state(p.initial_state + ((size_t)x * Hv + h) * st_elems, false);
-          else
-            set_zero();
-        }
         store_s();
         sync_generic_to_async();
         if (!run_fast(c0, c0 + nch, c0 + nch, h, hk, true)) break;
-        float* dst = (part == 1) ? ws_ptr<float>(p, p.L.bmat) : ws_ptr<float>(p, p.L.pub);
-        if (epi) sv_state(dst + ((size_t)sl * Hv + h) * st_elems);
+        if (epi) sv_state(ws_ptr<float>(p, p.L.pub) + ((size_t)sl * Hv + h) * st_elems);
+        publish(&flags_seg[s * Hv + h]);
+        __syncthreads();
+        continue;
       }
-      // A transition that is exactly zero makes the segment's end state its local end state B:
-      // the next segment can start without waiting for this segment's start state.
-      if (part == 0 && m_zero && cx.tid == 0) mzero[sl * Hv + h] = 1;
-      if (part == 2) publish(&flags_seg[s * Hv + h]);
+      // a segment whose own start warms up has its end state directly (from zero at the warm-up
+      // chunk); otherwise its transition M and its end state B from zero, for the walk
+      const int wb = si[4 * s + 3] >= 0 ? warm_back(gam_ws, contr, Hv, h, c0, dch[seq]) : -1;
+      const bool direct = need_e && wb >= 0;
+      const bool want_b = need_e && !direct;
+      const bool want_m = want_b || rev_needs_m(s, part, seq, c0, h);
+      if (direct) {
+        set_zero();
+        store_s();
+        sync_generic_to_async();
+        if (!run_fast(wb, c0 + nch, c0 + nch, h, hk, true)) break;
+        if (epi) sv_state(ws_ptr<float>(p, p.L.pub) + ((size_t)sl * Hv + h) * st_elems);
+        publish(&flags_seg[s * Hv + h]);
+      }
+      float* mdst = ws_ptr<float>(p, p.L.mmat) + ((size_t)sl * Hv + h) * st_elems;
+      bool m_zero = false;
+      if (want_m) {
+        // Transition M = Phi_last ... Phi_first: the chain from I over the segment. An exactly
+        // zero M makes the segment's end state its local end state B, and the next segment can
+        // start without waiting for this segment's start state.
+        set_identity();
+        store_s();
+        sync_generic_to_async();
+        if (!run_fast(c0, c0 + nch, c0 + nch, h, hk, false)) break;
+        m_zero = all_zero();
+        if (epi) {
+          sv_state(mdst);
+          store_images(cx, ws_ptr<uint8_t>(p, p.L.mimg) + ((size_t)sl * Hv + h) * 65536, S);
+        }
+        if (m_zero && cx.tid == 0) mzero[sl * Hv + h] = 1;
+      }
+      if (want_b) {
+        set_zero();
+        store_s();
+        sync_generic_to_async();
+        if (!run_fast(c0, c0 + nch, c0 + nch, h, hk, true)) break;
+        if (epi) sv_state(ws_ptr<float>(p, p.L.bmat) + ((size_t)sl * Hv + h) * st_elems);
+        publish(&flags_p1[sl * Hv + h]);  // M and B of this segment are written
+      }
       __syncthreads();
       continue;
     }
@@ -1861,9 +2103,10 @@ __global__ void __launch_bounds__(kWsThreads, 1) chain_kernel(const __grid_const
     bool have_start = true;
     // exact split: this segment warms up instead of waiting, and the next one needs this item's
     // published end state only when it cannot warm up itself
-    const int32_t* dch = ws_ptr<int32_t>(p, p.L.seq_chunk0);
     const int wb = (p.d.mode == 0 && dep >= 0) ? warm_back(gam_ws, contr, Hv, h, c0, dch[seq]) : -1;
-    const bool pub_next = p.d.mode == 0 && slot[s] >= 0 && dep != -1 &&
+    // (pass 1 has published it already when the document starts from a known state or when this
+    // segment warms up)
+    const bool pub_next = p.d.mode == 0 && slot[s] >= 0 && wb < 0 && si[4 * seq_seg0[seq] + 3] <= -2 &&
                           warm_back(gam_ws, contr, Hv, h, c0 + nch, dch[seq]) < 0;
     if (pub_next) {  // this item publishes its end state early
       const size_t off = ((size_t)slot[s] * Hv + h) * st_elems;
@@ -2155,7 +2398,7 @@ int launch_fwd(const FwdParams& p, cudaStream_t stream, cudaEvent_t* ev, bool pl
   const int64_t items_cap = (int64_t)p.d.num_sms;
   mark(4);
   if (p.d.mode == 0 && p.L.slots > 0 && p.d.T > 0) {
-    const int64_t units = (2 * p.L.slots + 1) * p.d.Hv;
+    const int64_t units = 2 * p.L.slots * p.d.Hv;  // units and walks
     const int grid = (int)(units < items_cap ? units : items_cap);
     if (p.st_img)
       chain_kernel<kModeP1, true><<<grid, kWsThreads, kSmemBytes, stream>>>(p);
