@@ -69,10 +69,11 @@ __device__ __forceinline__ bool wait_all(uint64_t* bar, uint32_t parity) {
 // e^{g_t} (I - beta_t k_t k_t^T), whose spectral norm is at most e^{g_t} while
 // 0 <= beta_t |k_t|^2 <= 2 (the chunk's flag in `contr`, written by kkt_solve). Over a window
 // whose summed log-decay is below kExactCut the neglected term is therefore below
-// e^{-60} (about 2^-86, 62 bits under fp32's resolution) times the norm of the state it neglects:
-// the chain can start from zero at the window's far end (a warm-up) instead of waiting for the
-// neighbouring segment.
-constexpr float kExactCut = -60.f;
+// e^{-30} (about 2^-43, 19 bits under fp32's unit roundoff of 2^-24) times the norm of the state it
+// neglects, while every chunk step of the chain itself rounds that state at 2^-24: the chain can
+// start from zero at the window's far end (a warm-up) instead of waiting for the neighbouring
+// segment, and the result is the exact recurrence to fp32 resolution.
+constexpr float kExactCut = -30.f;
 constexpr int kWarmCap = 32;  // longest warm-up window, chunks: one per lane of the warp that evaluates it
 
 // One warp evaluates a window in one round trip: lane i takes chunk `first + step * i`, an

@@ -256,6 +256,28 @@ __device__ __forceinline__ void group_sync(int group) {
   }
 }
 
+// T21 = -T22 X for one column c of the lower-left 32 x 32 block (rows 32 + j, j = 2 i + kOdd):
+// T22 is unit lower triangular (rows and columns 32-63 of A's buffer), x holds X's column.
+template <int kOdd>
+__device__ __forceinline__ void kkt_t21_rows(float (*A)[kAStride], const float* x, int c) {
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const int j = 2 * i + kOdd;
+    float a0 = x[j], a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+    for (int m = 0; m + 4 <= j; m += 4) {
+      const float4 tv = *reinterpret_cast<const float4*>(&A[32 + j][32 + m]);
+      a0 += tv.x * x[m];
+      a1 += tv.y * x[m + 1];
+      a2 += tv.z * x[m + 2];
+      a3 += tv.w * x[m + 3];
+    }
+#pragma unroll
+    for (int m = j & ~3; m < j; ++m) a1 += A[32 + j][32 + m] * x[m];
+    A[32 + j][c] = -((a0 + a1) + (a2 + a3));
+  }
+}
+
 __global__ void __launch_bounds__(256, 2) kkt_solve_kernel(const __grid_constant__ FwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   KktSmem& sm = *reinterpret_cast<KktSmem*>(smem_align1024(smem_raw));
@@ -403,30 +425,32 @@ __global__ void __launch_bounds__(256, 2) kkt_solve_kernel(const __grid_constant
       }
       const bool factored = gam[63] > kFactorMin;  // gamma is nonincreasing: gam[63] is the minimum
       if (factored) {
-        // T = (I + A)^{-1}, column t, with A_rm = (beta_r e^{gamma_r}) (K K^T)_rm e^{-gamma_m} for
-        // m < r: forward substitution on y_m = e^{-gamma_m} x_m reads K K^T itself (no A matrix).
-        // T goes to A's buffer row by row; the second warp of the group (columns 32-63) starts
-        // at row 32 (rows and terms below are zero).
-        float y[64];
+        // T = (I + A)^{-1} with A_rm = (beta_r e^{gamma_r}) (K K^T)_rm e^{-gamma_m} for m < r, in 32 x 32
+        // blocks: T11 = (I + A11)^{-1} (columns 0-31, first warp of the group) and T22 (columns
+        // 32-63, second warp) by forward substitution on y_m = e^{-gamma_m} x_m, one thread per
+        // column, reading K K^T itself (no A matrix); then X = A21 T11 and T21 = -T22 X with both
+        // warps on columns 0-31 (halves of the rows each), so that neither warp carries the whole
+        // column-0 substitution. T goes to A's buffer.
+        float y[32];
         // rows in groups of four: their beta e^{gamma} and e^{-gamma} come in two vector loads
 #define GDN_KKT_ROW(R, M0)                                                                 \
   {                                                                                        \
     float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;                                          \
     _Pragma("unroll") for (int m = (M0); m + 4 <= (R); m += 4) {                           \
       const float4 kv = *reinterpret_cast<const float4*>(&sm.kk[(R)][m]);                  \
-      a0 += kv.x * y[m];                                                                   \
-      a1 += kv.y * y[m + 1];                                                               \
-      a2 += kv.z * y[m + 2];                                                               \
-      a3 += kv.w * y[m + 3];                                                               \
+      a0 += kv.x * y[m - (M0)];                                                            \
+      a1 += kv.y * y[m - (M0) + 1];                                                        \
+      a2 += kv.z * y[m - (M0) + 2];                                                        \
+      a3 += kv.w * y[m - (M0) + 3];                                                        \
     }                                                                                      \
-    _Pragma("unroll") for (int m = (R) & ~3; m < (R); ++m) a0 += sm.kk[(R)][m] * y[m];    \
+    _Pragma("unroll") for (int m = (R) & ~3; m < (R); ++m) a0 += sm.kk[(R)][m] * y[m - (M0)]; \
     const float xr = (((R) == t) ? 1.f : 0.f) - cq[(R) & 3] * ((a0 + a1) + (a2 + a3));     \
     A[(R)][t] = xr;                                                                        \
-    y[(R)] = eq[(R) & 3] * xr;                                                             \
+    y[(R) - (M0)] = eq[(R) & 3] * xr;                                                      \
   }
         if (sub == 0) {
 #pragma unroll
-          for (int rb = 0; rb < 64; rb += 4) {
+          for (int rb = 0; rb < 32; rb += 4) {
             const float4 c4 = *reinterpret_cast<const float4*>(&be[rb]);
             const float4 e4 = *reinterpret_cast<const float4*>(&egi[rb]);
             const float cq[4] = {c4.x, c4.y, c4.z, c4.w}, eq[4] = {e4.x, e4.y, e4.z, e4.w};
@@ -450,6 +474,41 @@ __global__ void __launch_bounds__(256, 2) kkt_solve_kernel(const __grid_constant
           }
         }
 #undef GDN_KKT_ROW
+        group_sync(grp);
+        {
+          // X = A21 T11 = diag(beta e^gamma) (K K^T)_21 (diag(e^{-gamma}) T11): column c = lane, rows
+          // 32 + 16 sub .. + 15, into the T21 block
+          const int c = lane;
+#pragma unroll
+          for (int m = 0; m < 32; ++m) y[m] = egi[m] * A[m][c];
+          const int r0 = 32 + 16 * sub;
+#pragma unroll 2
+          for (int i = 0; i < 16; ++i) {
+            const int r = r0 + i;
+            float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+            for (int m = 0; m < 32; m += 4) {
+              const float4 kv = *reinterpret_cast<const float4*>(&sm.kk[r][m]);
+              a0 += kv.x * y[m];
+              a1 += kv.y * y[m + 1];
+              a2 += kv.z * y[m + 2];
+              a3 += kv.w * y[m + 3];
+            }
+            A[r][c] = be[r] * ((a0 + a1) + (a2 + a3));
+          }
+        }
+        group_sync(grp);
+        {
+          // T21 = -T22 X: column c = lane, the even rows (first warp) or the odd rows (second)
+          const int c = lane;
+#pragma unroll
+          for (int m = 0; m < 32; ++m) y[m] = A[32 + m][c];
+          group_sync(grp);  // X is read: T21 replaces it
+          if (sub == 0)
+            kkt_t21_rows<0>(A, y, c);
+          else
+            kkt_t21_rows<1>(A, y, c);
+        }
         group_sync(grp);
       } else {
         // A, column t (rows below the diagonal), one exponential per entry
