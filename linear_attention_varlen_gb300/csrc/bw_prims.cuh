@@ -87,6 +87,17 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
+// ------------------------------------------------------------------------------ dependent launch
+
+// A kernel launched with programmatic stream serialization may start while the kernel before it
+// in the stream still runs: it waits here (before touching anything that kernel writes) until
+// that kernel has completed and its memory is visible. A no-op for a plain launch.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Allow the next kernel of the stream (if it was launched that way) to start early.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------------------------------------ TMA
 
 // 3-D tiled load of one box into shared memory; completion counted on `bar` (bytes).

@@ -46,6 +46,7 @@ using namespace bw;
 constexpr int kPlanThreads = 256;  // one block; the scans run in tiles of this many documents / segments
 constexpr int kPlanSmemDocs = 2048;  // per-document offsets kept in shared memory up to this many documents
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constant__ FwdParams p, int keep_mzero) {
+  griddep_launch_dependents();  // kkt_solve may start; it waits for the maps below
   Header* hd = ws_ptr<Header>(p, p.L.header);
   const int N = p.d.N;
   const int tid = threadIdx.x, nt = blockDim.x;
@@ -284,6 +285,8 @@ __global__ void __launch_bounds__(256, 2) kkt_solve_kernel(const __grid_constant
   __shared__ uint64_t bar_ld, bar_mma;
   __shared__ uint32_t tmem_holder;
   __shared__ int s_ld_ok;
+  griddep_launch_dependents();
+  griddep_wait();  // the maps of plan_kernel
   Header* hd = ws_ptr<Header>(p, p.L.header);
   const int chunk = blockIdx.x, hk = blockIdx.y;
   if (chunk >= hd->n_chunks || get_status(hd) != 0) return;
@@ -432,45 +435,40 @@ __global__ void __launch_bounds__(256, 2) kkt_solve_kernel(const __grid_constant
         // warps on columns 0-31 (halves of the rows each), so that neither warp carries the whole
         // column-0 substitution. T goes to A's buffer.
         float y[32];
-        // rows in groups of four: their beta e^{gamma} and e^{-gamma} come in two vector loads
-#define GDN_KKT_ROW(R, M0)                                                                 \
+        {
+          // both warps run the same code on their diagonal block (offset o): the instruction stream
+          // is shared, and the rows come in groups of four whose beta e^{gamma} and e^{-gamma} take
+          // two vector loads
+          const int o = 32 * sub;
+          const float(*kkb)[kAStride] = reinterpret_cast<const float(*)[kAStride]>(&sm.kk[o][o]);
+          float(*Ab)[kAStride] = reinterpret_cast<float(*)[kAStride]>(&A[o][o]);
+          if (sub)
+#pragma unroll
+            for (int r = 0; r < 32; ++r) A[r][t] = 0.f;
+#define GDN_KKT_ROW(R)                                                                     \
   {                                                                                        \
     float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;                                          \
-    _Pragma("unroll") for (int m = (M0); m + 4 <= (R); m += 4) {                           \
-      const float4 kv = *reinterpret_cast<const float4*>(&sm.kk[(R)][m]);                  \
-      a0 += kv.x * y[m - (M0)];                                                            \
-      a1 += kv.y * y[m - (M0) + 1];                                                        \
-      a2 += kv.z * y[m - (M0) + 2];                                                        \
-      a3 += kv.w * y[m - (M0) + 3];                                                        \
+    _Pragma("unroll") for (int m = 0; m + 4 <= (R); m += 4) {                              \
+      const float4 kv = *reinterpret_cast<const float4*>(&kkb[(R)][m]);                    \
+      a0 += kv.x * y[m];                                                                   \
+      a1 += kv.y * y[m + 1];                                                               \
+      a2 += kv.z * y[m + 2];                                                               \
+      a3 += kv.w * y[m + 3];                                                               \
     }                                                                                      \
-    _Pragma("unroll") for (int m = (R) & ~3; m < (R); ++m) a0 += sm.kk[(R)][m] * y[m - (M0)]; \
-    const float xr = (((R) == t) ? 1.f : 0.f) - cq[(R) & 3] * ((a0 + a1) + (a2 + a3));     \
-    A[(R)][t] = xr;                                                                        \
-    y[(R) - (M0)] = eq[(R) & 3] * xr;                                                      \
+    _Pragma("unroll") for (int m = (R) & ~3; m < (R); ++m) a0 += kkb[(R)][m] * y[m];      \
+    const float xr = (((R) == lane) ? 1.f : 0.f) - cq[(R) & 3] * ((a0 + a1) + (a2 + a3));  \
+    Ab[(R)][lane] = xr;                                                                    \
+    y[(R)] = eq[(R) & 3] * xr;                                                             \
   }
-        if (sub == 0) {
 #pragma unroll
           for (int rb = 0; rb < 32; rb += 4) {
-            const float4 c4 = *reinterpret_cast<const float4*>(&be[rb]);
-            const float4 e4 = *reinterpret_cast<const float4*>(&egi[rb]);
+            const float4 c4 = *reinterpret_cast<const float4*>(&be[o + rb]);
+            const float4 e4 = *reinterpret_cast<const float4*>(&egi[o + rb]);
             const float cq[4] = {c4.x, c4.y, c4.z, c4.w}, eq[4] = {e4.x, e4.y, e4.z, e4.w};
-            GDN_KKT_ROW(rb, 0)
-            GDN_KKT_ROW(rb + 1, 0)
-            GDN_KKT_ROW(rb + 2, 0)
-            GDN_KKT_ROW(rb + 3, 0)
-          }
-        } else {
-#pragma unroll
-          for (int r = 0; r < 32; ++r) A[r][t] = 0.f;
-#pragma unroll
-          for (int rb = 32; rb < 64; rb += 4) {
-            const float4 c4 = *reinterpret_cast<const float4*>(&be[rb]);
-            const float4 e4 = *reinterpret_cast<const float4*>(&egi[rb]);
-            const float cq[4] = {c4.x, c4.y, c4.z, c4.w}, eq[4] = {e4.x, e4.y, e4.z, e4.w};
-            GDN_KKT_ROW(rb, 32)
-            GDN_KKT_ROW(rb + 1, 32)
-            GDN_KKT_ROW(rb + 2, 32)
-            GDN_KKT_ROW(rb + 3, 32)
+            GDN_KKT_ROW(rb)
+            GDN_KKT_ROW(rb + 1)
+            GDN_KKT_ROW(rb + 2)
+            GDN_KKT_ROW(rb + 3)
           }
         }
 #undef GDN_KKT_ROW
@@ -1714,6 +1712,8 @@ __global__ void __launch_bounds__(kWsThreads, 1) chain_kernel(const __grid_const
   __shared__ WtBars tbars;  // inference chain
   __shared__ uint32_t tmem_holder;
   __shared__ int s_item, s_ok, s_abort;
+  griddep_launch_dependents();
+  griddep_wait();  // everything the kernels before this one write
   Header* hd = ws_ptr<Header>(p, p.L.header);
   constexpr bool rec = kRec;
   ChainCtx cx;
@@ -2415,6 +2415,24 @@ __global__ void __launch_bounds__(kOutThreads) out_kernel(const __grid_constant_
 
 // ========================================================================================= launch
 
+// A launch that may start while the previous kernel of the stream finishes (programmatic stream
+// serialization): the kernel waits for it with griddep_wait before reading what it writes, so
+// only the launch and the CTAs' placement overlap its tail.
+template <typename K>
+static void launch_early(K kernel, dim3 grid, unsigned threads, size_t smem, cudaStream_t stream, const FwdParams& p) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaLaunchKernelEx(&cfg, kernel, p);
+}
+
 int launch_fwd(const FwdParams& p, cudaStream_t stream, cudaEvent_t* ev, bool plan_only) {
   static PerDevice attr_done;
   int dev = 0;
@@ -2451,7 +2469,7 @@ int launch_fwd(const FwdParams& p, cudaStream_t stream, cudaEvent_t* ev, bool pl
   mark(2);
   if (p.d.T > 0) {
     dim3 grid((unsigned)p.L.cmax, (unsigned)p.d.Hk);
-    kkt_solve_kernel<<<grid, 256, sizeof(KktSmem) + 1024, stream>>>(p);
+    launch_early(kkt_solve_kernel, grid, 256, sizeof(KktSmem) + 1024, stream, p);
   }
   mark(3);
   const int64_t items_cap = (int64_t)p.d.num_sms;
@@ -2460,9 +2478,9 @@ int launch_fwd(const FwdParams& p, cudaStream_t stream, cudaEvent_t* ev, bool pl
     const int64_t units = 2 * p.L.slots * p.d.Hv;  // units and walks
     const int grid = (int)(units < items_cap ? units : items_cap);
     if (p.st_img)
-      chain_kernel<kModeP1, true><<<grid, kWsThreads, kSmemBytes, stream>>>(p);
+      launch_early(chain_kernel<kModeP1, true>, grid, kWsThreads, kSmemBytes, stream, p);
     else
-      chain_kernel<kModeP1, false><<<grid, kWsThreads, kSmemBytes, stream>>>(p);
+      launch_early(chain_kernel<kModeP1, false>, grid, kWsThreads, kSmemBytes, stream, p);
   }
   mark(5);
   mark(6);
@@ -2470,9 +2488,9 @@ int launch_fwd(const FwdParams& p, cudaStream_t stream, cudaEvent_t* ev, bool pl
     const int64_t items = p.L.smax * p.d.Hv;
     const int grid = (int)(items < items_cap ? items : items_cap);
     if (p.st_img)
-      chain_kernel<kModeOut, true><<<grid, kWsThreads, kSmemBytes, stream>>>(p);
+      launch_early(chain_kernel<kModeOut, true>, grid, kWsThreads, kSmemBytes, stream, p);
     else
-      chain_kernel<kModeOut, false><<<grid, kWsThreads, kSmemBytes, stream>>>(p);
+      launch_early(chain_kernel<kModeOut, false>, grid, kWsThreads, kSmemBytes, stream, p);
   }
   mark(7);
   // a forward that keeps its records for the backward forms o from them

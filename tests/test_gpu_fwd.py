@@ -111,6 +111,45 @@ def test_split_matches_unsplit_closely():
 # ----------------------------------------------------------------------------- truncation mode
 
 
+def _median_fwd_us(p, reps=15):
+    d = to_device(p)
+    args = (d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"])
+    for _ in range(3):
+        gdn.chunk_fwd(*args)
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(reps):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        gdn.chunk_fwd(*args)
+        b.record()
+        torch.cuda.synchronize()
+        times.append(a.elapsed_time(b) * 1e3)
+    return float(np.median(times))
+
+
+def test_long_slow_decay_exact_sampled_heads_and_time(record_property):
+    """One 32768-token sequence at u ~ N(6, 1) (about -0.0025 per token): no segment boundary of the
+    exact split can warm up, so every middle segment starts from the state the cross-segment walk
+    composes. All 8 heads run on the GPU; the oracle checks one head of each key head. The forward
+    stays within 2x of the same shape at the workload's gates (u ~ N(2, 1)), where every boundary
+    warms up."""
+    slow = synth.make_problem("long_T32768_slow", synth.SEEDS[2], [32768], 2, 8, g_mean=6.0)
+    out, fin = run_fwd(slow)
+    for heads in ([1], [6]):
+        sub = head_slice(slow, heads)
+        ro, rf = oracle.fwd_problem(sub)
+        assert_close(f"slow-decay out heads {heads}", out[:, heads], ro)
+        assert_close(f"slow-decay final heads {heads}", fin[:, heads], rf)
+    t_slow = _median_fwd_us(slow)
+    t_fast = _median_fwd_us(synth.workload_long())
+    record_property("fwd_us_slow_decay", round(t_slow, 1))
+    record_property("fwd_us_workload_gates", round(t_fast, 1))
+    record_property("ratio", round(t_slow / t_fast, 3))
+    assert t_slow <= 2.0 * t_fast, (t_slow, t_fast)
+
+
 def test_truncation_mode_against_chunked_truncation():
     """Truncation mode matches the fp64 chunked truncation algebra (same windows), and its
     distance from the exact result stays within the e^-10 bound plus bf16 rounding."""
