@@ -258,24 +258,21 @@ __device__ __forceinline__ void group_sync(int group) {
 }
 
 // T21 = -T22 X for one column c of the lower-left 32 x 32 block (rows 32 + j, j = 2 i + kOdd):
-// T22 is unit lower triangular (rows and columns 32-63 of A's buffer), x holds X's column.
+// T22 is unit lower triangular (rows and columns 32-63 of A's buffer, zeros above the diagonal),
+// x2 holds X's column in packed pairs; a row's sum runs to the next multiple of four.
 template <int kOdd>
-__device__ __forceinline__ void kkt_t21_rows(float (*A)[kAStride], const float* x, int c) {
+__device__ __forceinline__ void kkt_t21_rows(float (*A)[kAStride], const uint64_t* x2, int c) {
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
     const int j = 2 * i + kOdd;
-    float a0 = x[j], a1 = 0.f, a2 = 0.f, a3 = 0.f;
+    uint64_t s01 = 0ull, s23 = 0ull;
 #pragma unroll
-    for (int m = 0; m + 4 <= j; m += 4) {
-      const float4 tv = *reinterpret_cast<const float4*>(&A[32 + j][32 + m]);
-      a0 += tv.x * x[m];
-      a1 += tv.y * x[m + 1];
-      a2 += tv.z * x[m + 2];
-      a3 += tv.w * x[m + 3];
+    for (int m = 0; m <= j; m += 4) {
+      const ulonglong2 tv = *reinterpret_cast<const ulonglong2*>(&A[32 + j][32 + m]);
+      s01 = f2_fma(tv.x, x2[m / 2], s01);
+      s23 = f2_fma(tv.y, x2[m / 2 + 1], s23);
     }
-#pragma unroll
-    for (int m = j & ~3; m < j; ++m) a1 += A[32 + j][32 + m] * x[m];
-    A[32 + j][c] = -((a0 + a1) + (a2 + a3));
+    A[32 + j][c] = -(f2_sum(s01) + f2_sum(s23));
   }
 }
 
@@ -434,7 +431,9 @@ __global__ void __launch_bounds__(256, 2) kkt_solve_kernel(const __grid_constant
         // column, reading K K^T itself (no A matrix); then X = A21 T11 and T21 = -T22 X with both
         // warps on columns 0-31 (halves of the rows each), so that neither warp carries the whole
         // column-0 substitution. T goes to A's buffer.
-        float y[32];
+        // y_m = e^{-gamma_m} x_m in packed pairs (lane pairs of the fp32x2 products): entries not yet
+        // solved are zero, so a row's sum may run to the next multiple of four
+        uint64_t y2[16];
         {
           // both warps run the same code on their diagonal block (offset o): the instruction stream
           // is shared, and the rows come in groups of four whose beta e^{gamma} and e^{-gamma} take
@@ -445,20 +444,20 @@ __global__ void __launch_bounds__(256, 2) kkt_solve_kernel(const __grid_constant
           if (sub)
 #pragma unroll
             for (int r = 0; r < 32; ++r) A[r][t] = 0.f;
+#pragma unroll
+          for (int m = 0; m < 16; ++m) y2[m] = 0ull;
 #define GDN_KKT_ROW(R)                                                                     \
   {                                                                                        \
-    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;                                          \
-    _Pragma("unroll") for (int m = 0; m + 4 <= (R); m += 4) {                              \
-      const float4 kv = *reinterpret_cast<const float4*>(&kkb[(R)][m]);                    \
-      a0 += kv.x * y[m];                                                                   \
-      a1 += kv.y * y[m + 1];                                                               \
-      a2 += kv.z * y[m + 2];                                                               \
-      a3 += kv.w * y[m + 3];                                                               \
+    uint64_t s01 = 0ull, s23 = 0ull;                                                       \
+    _Pragma("unroll") for (int m = 0; m < (R); m += 4) {                                   \
+      const ulonglong2 kv = *reinterpret_cast<const ulonglong2*>(&kkb[(R)][m]);            \
+      s01 = f2_fma(kv.x, y2[m / 2], s01);                                                  \
+      s23 = f2_fma(kv.y, y2[m / 2 + 1], s23);                                              \
     }                                                                                      \
-    _Pragma("unroll") for (int m = (R) & ~3; m < (R); ++m) a0 += kkb[(R)][m] * y[m];      \
-    const float xr = (((R) == lane) ? 1.f : 0.f) - cq[(R) & 3] * ((a0 + a1) + (a2 + a3));  \
+    const float xr = (((R) == lane) ? 1.f : 0.f) - cq[(R) & 3] * (f2_sum(s01) + f2_sum(s23)); \
     Ab[(R)][lane] = xr;                                                                    \
-    y[(R)] = eq[(R) & 3] * xr;                                                             \
+    const float yr = eq[(R) & 3] * xr;                                                     \
+    y2[(R) / 2] = ((R) & 1) ? f2_pack(f2_lo(y2[(R) / 2]), yr) : f2_pack(yr, 0.f);          \
   }
 #pragma unroll
           for (int rb = 0; rb < 32; rb += 4) {
@@ -478,21 +477,19 @@ __global__ void __launch_bounds__(256, 2) kkt_solve_kernel(const __grid_constant
           // 32 + 16 sub .. + 15, into the T21 block
           const int c = lane;
 #pragma unroll
-          for (int m = 0; m < 32; ++m) y[m] = egi[m] * A[m][c];
+          for (int m = 0; m < 32; m += 2) y2[m / 2] = f2_pack(egi[m] * A[m][c], egi[m + 1] * A[m + 1][c]);
           const int r0 = 32 + 16 * sub;
 #pragma unroll 2
           for (int i = 0; i < 16; ++i) {
             const int r = r0 + i;
-            float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+            uint64_t s01 = 0ull, s23 = 0ull;
 #pragma unroll
             for (int m = 0; m < 32; m += 4) {
-              const float4 kv = *reinterpret_cast<const float4*>(&sm.kk[r][m]);
-              a0 += kv.x * y[m];
-              a1 += kv.y * y[m + 1];
-              a2 += kv.z * y[m + 2];
-              a3 += kv.w * y[m + 3];
+              const ulonglong2 kv = *reinterpret_cast<const ulonglong2*>(&sm.kk[r][m]);
+              s01 = f2_fma(kv.x, y2[m / 2], s01);
+              s23 = f2_fma(kv.y, y2[m / 2 + 1], s23);
             }
-            A[r][c] = be[r] * ((a0 + a1) + (a2 + a3));
+            A[r][c] = be[r] * (f2_sum(s01) + f2_sum(s23));
           }
         }
         group_sync(grp);
@@ -500,12 +497,12 @@ __global__ void __launch_bounds__(256, 2) kkt_solve_kernel(const __grid_constant
           // T21 = -T22 X: column c = lane, the even rows (first warp) or the odd rows (second)
           const int c = lane;
 #pragma unroll
-          for (int m = 0; m < 32; ++m) y[m] = A[32 + m][c];
+          for (int m = 0; m < 32; m += 2) y2[m / 2] = f2_pack(A[32 + m][c], A[33 + m][c]);
           group_sync(grp);  // X is read: T21 replaces it
           if (sub == 0)
-            kkt_t21_rows<0>(A, y, c);
+            kkt_t21_rows<0>(A, y2, c);
           else
-            kkt_t21_rows<1>(A, y, c);
+            kkt_t21_rows<1>(A, y2, c);
         }
         group_sync(grp);
       } else {
