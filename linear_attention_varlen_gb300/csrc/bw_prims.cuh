@@ -353,13 +353,13 @@ __device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
   return r;
 }
 __device__ __forceinline__ float f2_lo(uint64_t v) {
-  float lo, hi;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+  float lo;
+  asm("{\n .reg .f32 t;\n mov.b64 {%0, t}, %1;\n}" : "=f"(lo) : "l"(v));
   return lo;
 }
 __device__ __forceinline__ float f2_hi(uint64_t v) {
-  float lo, hi;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+  float hi;
+  asm("{\n .reg .f32 t;\n mov.b64 {t, %0}, %1;\n}" : "=f"(hi) : "l"(v));
   return hi;
 }
 __device__ __forceinline__ float f2_sum(uint64_t v) { return f2_lo(v) + f2_hi(v); }

@@ -623,6 +623,8 @@ __global__ void __launch_bounds__(kRevThreads, 1) rev_chain_kernel(const __grid_
   __shared__ RevBars rbars;
   __shared__ uint32_t tmem_holder;
   __shared__ int s_item, s_ok, s_abort;
+  griddep_launch_dependents();
+  griddep_wait();  // everything the kernels before this one write
   Header* hd = reinterpret_cast<Header*>(p.ws + p.L.f.header);
   Header* h2 = reinterpret_cast<Header*>(p.ws + p.L.hdr2);
   const int N = p.d.N, Hv = p.d.Hv, G = p.d.Hv / p.d.Hk;
@@ -862,6 +864,8 @@ __global__ void __launch_bounds__(256, 1) grad_kernel(const __grid_constant__ Bw
   GradSmem& sm = *reinterpret_cast<GradSmem*>(smem_align1024(smem_raw));
   __shared__ uint64_t bar_ld, bar_mma, bar_p1, bar_v, bar_tw;
   __shared__ uint32_t tmem_holder;
+  griddep_launch_dependents();
+  griddep_wait();  // the records and the reverse chain's state gradients
   Header* hd = reinterpret_cast<Header*>(p.ws + p.L.f.header);
   const int chunk = blockIdx.x, hk = blockIdx.y;
   if (chunk >= hd->n_chunks || get_status(hd) != 0) return;
@@ -1425,6 +1429,8 @@ __global__ void __launch_bounds__(256, 1) dq_kernel(const __grid_constant__ BwdP
   DqSmem& sm = *reinterpret_cast<DqSmem*>(smem_align1024(smem_raw));
   __shared__ uint64_t bar_ld, bar_mma, bar_a, bar_b;
   __shared__ uint32_t tmem_holder;
+  griddep_launch_dependents();
+  griddep_wait();  // grad_kernel's dg (and the records)
   Header* hd = reinterpret_cast<Header*>(p.ws + p.L.f.header);
   const int chunk = blockIdx.x, hk = blockIdx.y;
   if (chunk >= hd->n_chunks || get_status(hd) != 0) return;
@@ -1652,6 +1658,7 @@ __global__ void __launch_bounds__(256, 1) dq_kernel(const __grid_constant__ BwdP
 
 // d(initial_state)[x][h] = sum over documents i (in order) with init_idx[i] == x of dL/dS_start(i, h).
 __global__ void __launch_bounds__(256) dinit_reduce_kernel(const __grid_constant__ BwdParams p) {
+  griddep_wait();  // the start-state gradients
   const int x = blockIdx.x / p.d.Hv, h = blockIdx.x % p.d.Hv;
   const float* ds0 = reinterpret_cast<const float*>(p.ws + p.L.ds0);
   const size_t st = (size_t)kDim * kDim;
@@ -1758,6 +1765,11 @@ int launch_bwd(const BwdArgs& a, bool reuse, cudaStream_t stream, cudaEvent_t* e
   p.tm_q = f.tm_q;
   p.tm_k = f.tm_k;
   p.tm_v = f.tm_v;
+  // the backward's own flags, reset before the forward so that its kernels and the reverse chain
+  // follow one another as kernels (dependent launches)
+  if (cudaMemsetAsync(ws + p.L.flags_ds0, 0, (size_t)d.N * d.Hv * 4, stream) != cudaSuccess) return kErrCuda;
+  if (cudaMemsetAsync(ws + p.L.hdr2, 0, sizeof(Header), stream) != cudaSuccess) return kErrCuda;
+  if (cudaMemsetAsync(ws + p.L.flags_rseg, 0, (size_t)p.L.f.smax * d.Hv * 4, stream) != cudaSuccess) return kErrCuda;
   rc = launch_fwd(f, stream, ev, reuse);
   if (rc != kOk) return rc;
   p.g = a.g;
@@ -1777,25 +1789,22 @@ int launch_bwd(const BwdArgs& a, bool reuse, cudaStream_t stream, cudaEvent_t* e
   auto mark = [&](int i) {
     if (ev && ev[i]) cudaEventRecord(ev[i], stream);
   };
-  if (cudaMemsetAsync(ws + p.L.flags_ds0, 0, (size_t)d.N * d.Hv * 4, stream) != cudaSuccess) return kErrCuda;
-  if (cudaMemsetAsync(ws + p.L.hdr2, 0, sizeof(Header), stream) != cudaSuccess) return kErrCuda;
-  if (cudaMemsetAsync(ws + p.L.flags_rseg, 0, (size_t)p.L.f.smax * d.Hv * 4, stream) != cudaSuccess) return kErrCuda;
   mark(8);
   {
     const int64_t items = p.L.f.smax * d.Hv;
     const int grid = (int)(items < d.num_sms ? items : d.num_sms);
-    if (p.L.f.slots > 0 && d.T > 0) rev_chain_kernel<1><<<grid, kRevThreads, kRevSmemBytes, stream>>>(p);
-    rev_chain_kernel<2><<<grid, kRevThreads, kRevSmemBytes, stream>>>(p);
+    if (p.L.f.slots > 0 && d.T > 0) launch_early(rev_chain_kernel<1>, grid, kRevThreads, kRevSmemBytes, stream, p);
+    launch_early(rev_chain_kernel<2>, grid, kRevThreads, kRevSmemBytes, stream, p);
   }
   mark(9);
   mark(10);
-  if (d.T > 0) grad_kernel<<<dim3((unsigned)p.L.f.cmax, (unsigned)d.Hk), 256, kGradSmemBytes, stream>>>(p);
+  if (d.T > 0) launch_early(grad_kernel, dim3((unsigned)p.L.f.cmax, (unsigned)d.Hk), 256, kGradSmemBytes, stream, p);
   mark(11);
   mark(14);
-  if (d.T > 0) dq_kernel<<<dim3((unsigned)p.L.f.cmax, (unsigned)d.Hk), 256, kDqSmemBytes, stream>>>(p);
+  if (d.T > 0) launch_early(dq_kernel, dim3((unsigned)p.L.f.cmax, (unsigned)d.Hk), 256, kDqSmemBytes, stream, p);
   mark(15);
   mark(12);
-  if (d.n_init > 0) dinit_reduce_kernel<<<d.n_init * d.Hv, 256, 0, stream>>>(p);
+  if (d.n_init > 0) launch_early(dinit_reduce_kernel, dim3(d.n_init * d.Hv), 256, 0, stream, p);
   mark(13);
   return cudaGetLastError() == cudaSuccess ? kOk : kErrCuda;
 }

@@ -2306,6 +2306,8 @@ __global__ void __launch_bounds__(kOutThreads) out_kernel(const __grid_constant_
   OutSmem& sm = *reinterpret_cast<OutSmem*>(smem_align1024(smem_raw));
   __shared__ uint64_t bar_ld, bar_mma;
   __shared__ uint32_t tmem_holder;
+  griddep_launch_dependents();
+  griddep_wait();  // the records of the chain before it
   Header* hd = ws_ptr<Header>(p, p.L.header);
   const int gc = blockIdx.x, h = blockIdx.y, Hv = p.d.Hv, hk = h / (Hv / p.d.Hk);
   if (gc >= hd->n_chunks || get_status(hd) != 0) return;
@@ -2412,24 +2414,6 @@ __global__ void __launch_bounds__(kOutThreads) out_kernel(const __grid_constant_
 
 // ========================================================================================= launch
 
-// A launch that may start while the previous kernel of the stream finishes (programmatic stream
-// serialization): the kernel waits for it with griddep_wait before reading what it writes, so
-// only the launch and the CTAs' placement overlap its tail.
-template <typename K>
-static void launch_early(K kernel, dim3 grid, unsigned threads, size_t smem, cudaStream_t stream, const FwdParams& p) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
-  cfg.blockDim = dim3(threads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  cudaLaunchKernelEx(&cfg, kernel, p);
-}
-
 int launch_fwd(const FwdParams& p, cudaStream_t stream, cudaEvent_t* ev, bool plan_only) {
   static PerDevice attr_done;
   int dev = 0;
@@ -2493,7 +2477,7 @@ int launch_fwd(const FwdParams& p, cudaStream_t stream, cudaEvent_t* ev, bool pl
   // a forward that keeps its records for the backward forms o from them
   mark(16);
   if (p.st_img && p.out && p.d.T > 0)
-    out_kernel<<<dim3((unsigned)p.L.cmax, (unsigned)p.d.Hv), kOutThreads, kOutSmemBytes, stream>>>(p);
+    launch_early(out_kernel, dim3((unsigned)p.L.cmax, (unsigned)p.d.Hv), kOutThreads, kOutSmemBytes, stream, p);
   mark(17);
   return cudaGetLastError() == cudaSuccess ? kOk : kErrCuda;
 }

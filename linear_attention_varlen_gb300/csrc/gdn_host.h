@@ -59,4 +59,24 @@ class PerDevice {
   std::atomic<unsigned long long> mask_{0};
 };
 
+// A launch that may start while the previous kernel of the stream finishes (programmatic stream
+// serialization): the kernel waits for it on the device (griddepcontrol.wait) before it reads or
+// writes anything that kernel touches, so only the launch and the CTAs' placement overlap its
+// tail. The launch error, if any, is left for cudaGetLastError.
+template <typename Params>
+inline void launch_early(void (*kernel)(Params), dim3 grid, unsigned threads, size_t smem, cudaStream_t stream,
+                         const Params& p) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaLaunchKernelEx(&cfg, kernel, p);
+}
+
 }  // namespace gdn
