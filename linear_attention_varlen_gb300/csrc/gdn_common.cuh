@@ -74,7 +74,8 @@ struct Header {
   int32_t n_p1;        // pass-1 units (segment, part)
   uint32_t q_p1;       // work-queue tickets
   uint32_t q_chain;
-  int32_t pad[57];
+  int32_t n_walk;      // pass-1 walks (documents whose known-start first segment has middle segments)
+  int32_t pad[56];
 };
 static_assert(sizeof(Header) == 256, "header is 256 bytes");
 
@@ -101,7 +102,7 @@ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Forward workspace layout (byte offsets from the workspace base).
 struct FwdLayout {
-  size_t header, seq_chunk0, seq_seg0, chunk_seq, chunk_tok0, chunk_len, seg_info, seg_slot, p1_list;
+  size_t header, seq_chunk0, seq_seg0, chunk_seq, chunk_tok0, chunk_len, seg_info, seg_slot, p1_list, walk_list;
   size_t flags_seg, flags_fin, flags_p1, walk_ctr, mzero, gam, fac, contr, tw, tu, pimg, pub, mmat, bmat, mimg, total;
   int64_t cmax, smax, slots;
 };
@@ -127,6 +128,7 @@ inline FwdLayout fwd_layout(const PlanDims& d) {
   L.seg_info = take(sizeof(int32_t) * 4 * L.smax);
   L.seg_slot = take(sizeof(int32_t) * L.smax);
   L.p1_list = take(sizeof(int32_t) * 2 * (2 * L.slots + 1));
+  L.walk_list = take(sizeof(int32_t) * (L.slots + 1));
   L.flags_seg = take(sizeof(int32_t) * (size_t)L.smax * d.Hv);
   L.flags_fin = take(sizeof(int32_t) * (size_t)(d.N + 1) * d.Hv);
   L.flags_p1 = take(sizeof(int32_t) * ((size_t)L.slots * d.Hv + 1));  // a segment's M and B are written

@@ -44,6 +44,30 @@ using namespace bw;
 // keep_mzero: a backward that reuses a forward's records keeps that forward's pass-1 findings
 // (which segment transitions are exactly zero); the maps it rebuilds are the same.
 constexpr int kPlanThreads = 256;  // one block; the scans run in tiles of this many documents / segments
+
+// Inclusive prefix sum over the 256 threads of the block: a shuffle scan per warp, then one over the
+// eight warp totals (two barriers). The caller synchronises before the next call reuses s_tot.
+__device__ __forceinline__ int block_inclusive_scan(int v, int* s_tot) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += t;
+  }
+  if (lane == 31) s_tot[w] = v;
+  __syncthreads();
+  if (w == 0) {
+    int t = lane < kPlanThreads / 32 ? s_tot[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < kPlanThreads / 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, t, o);
+      if (lane >= o) t += u;
+    }
+    if (lane < kPlanThreads / 32) s_tot[lane] = t;
+  }
+  __syncthreads();
+  return w > 0 ? v + s_tot[w - 1] : v;
+}
 constexpr int kPlanSmemDocs = 2048;  // per-document offsets kept in shared memory up to this many documents
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constant__ FwdParams p, int keep_mzero) {
   griddep_launch_dependents();  // kkt_solve may start; it waits for the maps below
@@ -74,6 +98,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
       hd->n_chunks = 0;
       hd->n_segs = 0;
       hd->n_p1 = 0;
+      hd->n_walk = 0;
       hd->q_p1 = 0;
       hd->q_chain = 0;
     }
@@ -86,17 +111,10 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
     const int i = base + tid;
     const int c = (i < N) ? doc_chunks(i, p.cu) : 0;
     if (i < N) atomicMax(&s_longest, c);
-    s_scan[tid] = c;
+    const int incl = block_inclusive_scan(c, s_scan);
+    if (i < N) seq_chunk0[i] = s_carry[0] + incl - c;
     __syncthreads();
-    for (int off = 1; off < nt; off <<= 1) {
-      const int v = (tid >= off) ? s_scan[tid - off] : 0;
-      __syncthreads();
-      s_scan[tid] += v;
-      __syncthreads();
-    }
-    if (i < N) seq_chunk0[i] = s_carry[0] + s_scan[tid] - c;
-    __syncthreads();
-    if (tid == nt - 1) s_carry[0] += s_scan[tid];
+    if (tid == nt - 1) s_carry[0] += incl;
     __syncthreads();
   }
   const int total_chunks = s_carry[0];
@@ -112,17 +130,10 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
   for (int base = 0; base < N; base += nt) {
     const int i = base + tid;
     const int c = (i < N) ? doc_segs(doc_chunks(i, p.cu), L) : 0;
-    s_scan[tid] = c;
+    const int incl = block_inclusive_scan(c, s_scan);
+    if (i < N) seq_seg0[i] = s_carry[1] + incl - c;
     __syncthreads();
-    for (int off = 1; off < nt; off <<= 1) {
-      const int v = (tid >= off) ? s_scan[tid - off] : 0;
-      __syncthreads();
-      s_scan[tid] += v;
-      __syncthreads();
-    }
-    if (i < N) seq_seg0[i] = s_carry[1] + s_scan[tid] - c;
-    __syncthreads();
-    if (tid == nt - 1) s_carry[1] += s_scan[tid];
+    if (tid == nt - 1) s_carry[1] += incl;
     __syncthreads();
   }
   const int total_segs = s_carry[1];
@@ -157,9 +168,11 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
   if (!keep_mzero)
     for (int e = tid; e < (int)p.L.slots * p.d.Hv; e += nt) mz[e] = 0;
   // slots and pass-1 units: only split segments other than the last of their document get them
-  // (exact mode); a block scan over the segments numbers them in segment order
+  // (exact mode), numbered in segment order; a document whose first segment starts from a known
+  // state and that has middle segments also gets a walk (its first segment's unit)
   int32_t* slot = ws_ptr<int32_t>(p, p.L.seg_slot);
   int32_t* p1 = ws_ptr<int32_t>(p, p.L.p1_list);
+  int32_t* walks = ws_ptr<int32_t>(p, p.L.walk_list);
   if (tid == 0) {
     s_carry[0] = 0;
     s_carry[1] = 0;
@@ -167,7 +180,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
   __syncthreads();
   for (int base = 0; base < total_segs; base += nt) {
     const int s = base + tid;
-    int need = 0, units = 0, known_start = 0;
+    int need = 0, walk = 0, known_start = 0;
     if (s < total_segs) {
       // the segment's document and dependency, recomputed (the table above is in global memory)
       int32_t info[4];
@@ -176,33 +189,27 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
       const bool last = (s + 1 == seq_seg0[i + 1]);
       const bool split = (seq_seg0[i + 1] - seq_seg0[i]) > 1;
       need = (split && !last && p.d.mode == 0) ? 1 : 0;
-      units = need;
       known_start = info[3] == -1 ? 1 : 0;
+      walk = (need && known_start && s == seq_seg0[i] && seq_seg0[i + 1] - seq_seg0[i] >= 3) ? 1 : 0;
     }
-    const int mine = (need << 16) | units;  // a tile holds at most nt segments: no carry between the halves
-    s_scan[tid] = mine;
-    __syncthreads();
-    for (int off = 1; off < nt; off <<= 1) {
-      const int v = (tid >= off) ? s_scan[tid - off] : 0;
-      __syncthreads();
-      s_scan[tid] += v;
-      __syncthreads();
-    }
-    const int excl = s_scan[tid] - mine;
+    const int mine = (need << 16) | walk;  // a tile holds at most nt segments: no carry between the halves
+    const int incl = block_inclusive_scan(mine, s_scan);
+    const int excl = incl - mine;
     if (s < total_segs) {
-      const int sl = s_carry[0] + (excl >> 16), u = s_carry[1] + (excl & 0xFFFF);
-      slot[s] = (need && sl < p.L.slots) ? sl : -1;
-      if (need && sl < p.L.slots) {
+      const int u = s_carry[0] + (excl >> 16);  // the unit and the slot of the segment
+      slot[s] = (need && u < p.L.slots) ? u : -1;
+      if (need && u < p.L.slots) {
         p1[2 * u] = s;
         // 2: the end state from the document's known start; 0: the transition M and the end state
         // B from zero, or, when the segment's own start warms up, its end state directly
         p1[2 * u + 1] = known_start ? 2 : 0;
+        if (walk) walks[s_carry[1] + (excl & 0xFFFF)] = u;
       }
     }
     __syncthreads();
     if (tid == nt - 1) {
-      s_carry[0] += s_scan[tid] >> 16;
-      s_carry[1] += s_scan[tid] & 0xFFFF;
+      s_carry[0] += incl >> 16;
+      s_carry[1] += incl & 0xFFFF;
     }
     __syncthreads();
   }
@@ -212,7 +219,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
     hd->n_chunks = out_of_slots ? 0 : total_chunks;
     hd->n_segs = out_of_slots ? 0 : total_segs;
     hd->seg_chunks = L;
-    hd->n_p1 = out_of_slots ? 0 : s_carry[1];
+    hd->n_p1 = out_of_slots ? 0 : s_carry[0];
+    hd->n_walk = out_of_slots ? 0 : s_carry[1];
     hd->q_p1 = 0;
     hd->q_chain = 0;
   }
@@ -1729,10 +1737,10 @@ __global__ void __launch_bounds__(kWsThreads, 1) chain_kernel(const __grid_const
   memset(&ph, 0, sizeof(ph));
   uint32_t tph = 0;  // phase bits of the inference chain's barriers
   const int Hv = p.d.Hv, G = p.d.Hv / p.d.Hk;
-  // pass 1: one ticket per (unit, value head), then one per (unit, value head) for the walk that
-  // composes a document's segment maps (only units of a document's first segment walk)
+  // pass 1: one ticket per (unit, value head), then one per (walk, value head) for the walks that
+  // compose a document's segment maps
   const int n_unit_items = (kMode == kModeOut ? 0 : hd->n_p1) * Hv;
-  const int n_items = kMode == kModeOut ? hd->n_segs * Hv : 2 * n_unit_items;
+  const int n_items = kMode == kModeOut ? hd->n_segs * Hv : n_unit_items + hd->n_walk * Hv;
   if (blockIdx.x >= n_items || get_status(hd) != 0) return;
   const int32_t* si = ws_ptr<int32_t>(p, p.L.seg_info);
   const int32_t* slot = ws_ptr<int32_t>(p, p.L.seg_slot);
@@ -1745,7 +1753,12 @@ __global__ void __launch_bounds__(kWsThreads, 1) chain_kernel(const __grid_const
   // walk runs for a document whose first segment starts from a known state and that has middle
   // segments. All threads call this (the window evaluation is warp-wide).
   const int32_t* p1 = ws_ptr<int32_t>(p, p.L.p1_list);
+  const int32_t* walk_list = ws_ptr<int32_t>(p, p.L.walk_list);
   const int32_t* dch = ws_ptr<int32_t>(p, p.L.seq_chunk0);
+  // a ticket's unit (the document's first-segment unit for a walk ticket)
+  auto ticket_unit = [&](int item) {
+    return item >= n_unit_items ? walk_list[(item - n_unit_items) / Hv] : item / Hv;
+  };
   auto rev_needs_m = [&](int s, int part, int seq, int c0, int h) -> bool {
     return kRec && part == 0 && s != seq_seg0[seq] && warm_fwd(gam_ws, contr, Hv, h, c0, dch[seq + 1]) < 0;
   };
@@ -1754,8 +1767,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) chain_kernel(const __grid_const
   int* walk_ctr = ws_ptr<int>(p, p.L.walk_ctr);
   auto p1_skips = [&](int item) -> bool {
     const bool walk = item >= n_unit_items;
-    const int idx = walk ? item - n_unit_items : item;
-    const int unit = idx / Hv, h = idx % Hv;
+    const int unit = ticket_unit(item), h = item % Hv;
     const int s = p1[2 * unit], part = p1[2 * unit + 1];
     const int seq = si[4 * s], c0 = si[4 * s + 1], nch = si[4 * s + 2];
     int* ctr = walk_ctr + 2 * ((size_t)seq * Hv + h);
@@ -2075,7 +2087,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) chain_kernel(const __grid_const
     bool ok = true;
     if (kMode == kModeP1) {
       const bool walk = item >= n_unit_items;
-      const int unit = (walk ? item - n_unit_items : item) / Hv;
+      const int unit = ticket_unit(item);
       const int s = p1[2 * unit], part = p1[2 * unit + 1];
       const int seq = si[4 * s], c0 = si[4 * s + 1], nch = si[4 * s + 2];
       const int sl = slot[s];
@@ -2456,7 +2468,7 @@ int launch_fwd(const FwdParams& p, cudaStream_t stream, cudaEvent_t* ev, bool pl
   const int64_t items_cap = (int64_t)p.d.num_sms;
   mark(4);
   if (p.d.mode == 0 && p.L.slots > 0 && p.d.T > 0) {
-    const int64_t units = 2 * p.L.slots * p.d.Hv;  // units and walks
+    const int64_t units = 2 * p.L.slots * p.d.Hv;  // units and walks (at most one per unit)
     const int grid = (int)(units < items_cap ? units : items_cap);
     if (p.st_img)
       launch_early(chain_kernel<kModeP1, true>, grid, kWsThreads, kSmemBytes, stream, p);
