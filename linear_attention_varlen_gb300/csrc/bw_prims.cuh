@@ -363,6 +363,12 @@ __device__ __forceinline__ float f2_hi(uint64_t v) {
   return hi;
 }
 __device__ __forceinline__ float f2_sum(uint64_t v) { return f2_lo(v) + f2_hi(v); }
+// a * b, lane by lane
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
 // a * b + c, lane by lane
 __device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
   uint64_t d;

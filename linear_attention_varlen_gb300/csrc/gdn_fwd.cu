@@ -1288,9 +1288,10 @@ __device__ bool run_wt(const FwdParams& p, ChainCtx& cx, WtBars& bb, uint32_t& p
       uint32_t rp[16], rs[16];
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
-        const float2 sc = *reinterpret_cast<const float2*>(fc + 32 * cx.half + 2 * i);
+        const uint64_t sc = *reinterpret_cast<const uint64_t*>(fc + 32 * cx.half + 2 * i);
+        const uint64_t vs = f2_mul(f2_pack(v[2 * i], v[2 * i + 1]), sc);
         rp[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
-        rs[i] = pack_bf16x2(v[2 * i] * sc.x, v[2 * i + 1] * sc.y);
+        rs[i] = pack_bf16x2(f2_lo(vs), f2_hi(vs));
       }
       tmem_st16(cx.tmem + lq + kTtVp + 16 * cx.half, rp);
       tmem_st16(cx.tmem + lq + kTtVs + 16 * cx.half, rs);
@@ -1301,13 +1302,18 @@ __device__ bool run_wt(const FwdParams& p, ChainCtx& cx, WtBars& bb, uint32_t& p
     bit_wait(&bb.b_done, ph, kBitBDone, abort);
     {
       const float GC = fc[128];
+      const uint64_t gc2 = f2_pack(GC, GC);
 #pragma unroll
       for (int hc = 0; hc < 2; ++hc) {
         float d[32];
         tmem_ld32(cx.tmem + lq + kTtD2 + 64 * cx.half + 32 * hc, d);
         tmem_ld_wait();
 #pragma unroll
-        for (int x = 0; x < 32; ++x) S[32 * hc + x] = GC * S[32 * hc + x] + d[x];
+        for (int x = 0; x < 32; x += 2) {  // e^{gamma_C} S + D_2, two values per instruction
+          const uint64_t r = f2_fma(gc2, f2_pack(S[32 * hc + x], S[32 * hc + x + 1]), f2_pack(d[x], d[x + 1]));
+          S[32 * hc + x] = f2_lo(r);
+          S[32 * hc + x + 1] = f2_hi(r);
+        }
       }
       if (out) bit_wait(&bb.qs_done, ph, kBitQsDone, abort);  // Q S(j) has read S^T(j)
       stage_state_t(cx, S);
