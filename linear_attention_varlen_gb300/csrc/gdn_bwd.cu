@@ -431,7 +431,11 @@ __device__ bool run_rev_ws(const BwdParams& p, Ctx& cx, RevSmem& sm, RevBars& bb
         tmem_ld16(tm + kRtC + lane_base + 64 * cx.half + 32 * hc + 16, v + 16);
         tmem_ld_wait();
 #pragma unroll
-        for (int x = 0; x < 32; ++x) dS[32 * hc + x] = GC * dS[32 * hc + x] + v[x];
+        for (int x = 0; x < 32; x += 2) {  // two values per instruction
+          const uint64_t r = f2_fma(f2_pack(GC, GC), f2_pack(dS[32 * hc + x], dS[32 * hc + x + 1]), f2_pack(v[x], v[x + 1]));
+          dS[32 * hc + x] = f2_lo(r);
+          dS[32 * hc + x + 1] = f2_hi(r);
+        }
       }
       if (kRecord && cx.tid == 0) bulk_wait_read_all();  // the dS record of chunk j has read sm.ds
       __syncwarp();

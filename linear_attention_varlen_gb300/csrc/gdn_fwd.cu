@@ -1337,14 +1337,19 @@ __device__ bool run_wt(const FwdParams& p, ChainCtx& cx, WtBars& bb, uint32_t& p
       e_sync();
       // the output factors of this thread's 32 tokens, in registers before any store to the tile
       // (the stores could otherwise alias them and serialize the loop)
-      float of[32];
+      uint64_t of[16];
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
-        const float4 f4 = *reinterpret_cast<const float4*>(fc + 64 + 32 * cx.half + 4 * q);
-        of[4 * q] = f4.x;
-        of[4 * q + 1] = f4.y;
-        of[4 * q + 2] = f4.z;
-        of[4 * q + 3] = f4.w;
+        const ulonglong2 f4 = *reinterpret_cast<const ulonglong2*>(fc + 64 + 32 * cx.half + 4 * q);
+        of[2 * q] = f4.x;
+        of[2 * q + 1] = f4.y;
+      }
+      // O times its output factors, two tokens per instruction
+#pragma unroll
+      for (int q = 0; q < 16; ++q) {
+        const uint64_t x = f2_mul(f2_pack(o[2 * q], o[2 * q + 1]), of[q]);
+        o[2 * q] = f2_lo(x);
+        o[2 * q + 1] = f2_hi(x);
       }
       const bool odd = cx.lane & 1;
       const int be = b & ~1;  // the even value index of the pair
@@ -1354,7 +1359,7 @@ __device__ bool run_wt(const FwdParams& p, ChainCtx& cx, WtBars& bb, uint32_t& p
         // tokens t0 and t0 + 4 (rows four apart keep the two halves of a warp's store on
         // different banks); the even lane stores row t0, the odd lane row t0 + 4
         const int i0 = 8 * (m >> 2) + (m & 3), t0 = 32 * cx.half + i0;
-        const float x0 = o[i0] * of[i0], x1 = o[i0 + 4] * of[i0 + 4];
+        const float x0 = o[i0], x1 = o[i0 + 4];
         const float got = __shfl_xor_sync(0xffffffffu, odd ? x0 : x1, 1);
         const int t = odd ? t0 + 4 : t0;
         const uint32_t v = odd ? pack_bf16x2(got, x1) : pack_bf16x2(x0, got);
@@ -1685,7 +1690,11 @@ __device__ bool run_ws_rec(const FwdParams& p, ChainCtx& cx, WsBars& bb, WsPhase
         tmem_ld16(cx.tmem + kRtD2 + lane_base + 64 * cx.half + 32 * hc + 16, v + 16);
         tmem_ld_wait();
 #pragma unroll
-        for (int x = 0; x < 32; ++x) S[32 * hc + x] = GC * S[32 * hc + x] + v[x];
+        for (int x = 0; x < 32; x += 2) {  // two values per instruction
+          const uint64_t r = f2_fma(f2_pack(GC, GC), f2_pack(S[32 * hc + x], S[32 * hc + x + 1]), f2_pack(v[x], v[x + 1]));
+          S[32 * hc + x] = f2_lo(r);
+          S[32 * hc + x + 1] = f2_hi(r);
+        }
       }
       store_state_comp(sm, cx, S);
     }
