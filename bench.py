@@ -473,7 +473,7 @@ def run_ours(args, rank, world, local_rank):
     e2e_ms = ea.elapsed_time(ev_out[-1]) / e2e_steps
     e2e_value = T * world / (e2e_ms * 1e-3) / 1e6
 
-    # The inference forward alone (exact mode, the spec prefill) and the truncation mode, each
+    # The inference forward alone (exact mode, the 32K x 8-head prefill) and the truncation mode, each
     # timed with one event pair around the whole call (L2 flushed before each), outside the step
     # loop; truncation's deviation from the exact forward on the same inputs.
     def time_forward(mode, reps):
