@@ -70,6 +70,26 @@ def test_truncation_error_within_printed_bound():
     assert err_S > 0  # it is an approximation
 
 
+def test_exact_warmup_cut_is_below_fp32_resolution():
+    """The exact split starts a segment from zero over a window of whole chunks whose summed
+    log-decay is below -30: the neglected term is at most e^-30 (about 2^-43) of the norm of the
+    state at the window's start, 19 bits under fp32's unit roundoff. Checked in fp64 with the same
+    window rule at that cut, on gates where windows span several chunks."""
+    cut = -30.0
+    assert np.exp(cut) < 2.0 ** -43 * 1.1 and np.exp(cut) < 2.0 ** -24 / 2.0 ** 19 * 1.1
+    L = 64 * 24
+    q, k, v, g, beta, S0 = one_doc(11, L, g_mean=2.0)  # about -8 per chunk: windows of about 4 chunks
+    Ow, Sw, nw = cr.doc_fwd_truncated(q, k, v, g, beta, S0, seg_chunks=4, log_threshold=cut)
+    Oe, Se, starts = cr.doc_fwd(q, k, v, g, beta, S0)
+    assert min(nw[1:]) >= 3
+    smax = max(np.linalg.norm(s, 2) for s in starts)
+    bound = np.exp(cut) * smax
+    assert np.linalg.norm(Sw - Se, 2) <= bound * 1.0001 + 1e-14 * smax
+    assert np.max(np.linalg.norm(Ow - Oe, axis=1)) <= bound * np.max(np.linalg.norm(q, axis=1)) * 1.0001 + 1e-14 * smax
+    # what it neglects is far below what fp32 resolves of the state itself
+    assert bound < 2.0 ** -24 * smax / 1000
+
+
 @pytest.mark.parametrize("L", [1, 50, 64, 130])
 def test_chunked_backward_matches_oracle(L):
     q, k, v, g, beta, S0 = one_doc(200 + L, L, Dk=8, Dv=6)
