@@ -231,9 +231,10 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
 // kkt_solve: one CTA of 256 threads per (chunk, key head). K K^T runs once on the tensor cores;
 // the value heads of the group are then processed four at a time, one group of 64 threads per
 // value head: the chunk-local cumulative gate gamma, A = diag(beta) (e^{gamma_i - gamma_j} o K K^T)
-// (strictly lower), T = (I + A)^{-1} by forward substitution with one thread per column of T
-// (x_r = [r == c] - sum_{m<r} A_rm x_m, unrolled, x in registers), and the outputs T diag(beta
-// e^gamma), T diag(beta) as bf16 images (plus T in fp32 and the low bf16 parts in record mode).
+// (strictly lower), T = (I + A)^{-1} (32 x 32 diagonal blocks by forward substitution with one
+// thread per column, x_r = [r == c] - sum_{m<r} A_rm x_m in registers, then the off-diagonal block
+// from two block products), and the outputs T diag(beta e^gamma), T diag(beta) as bf16 images
+// (plus T in fp32 and the low bf16 parts in record mode).
 // A plain forward also computes Q K^T once per key head (tensor cores) and writes P = scale
 // (Q K^T o E) per value head as a bf16 image, so that the state chain never forms it.
 // The decay factors e^{gamma_i - gamma_j} (j <= i) are taken as e^{gamma_i} e^{-gamma_j} when the
