@@ -700,6 +700,28 @@ def run_ours(args, rank, world, local_rank):
     return res
 
 
+def profile_fwd(T, g_mean):
+    """The inference forward alone on one T-token sequence (H_v=8, H_k=2) with gates
+    u ~ N(g_mean, 1), for ncu captures of its kernels (g_mean 6: no exact-split boundary can warm
+    up, so pass 1 computes every transition and walks them)."""
+    import torch
+
+    import linear_attention_varlen_gb300 as gdn
+    import synth
+    from synth import to_device
+    p = synth.make_problem(f"profile_T{T}_g{g_mean}", synth.SEEDS[2], [T], 2, 8, g_mean=g_mean)
+    d = to_device(p)
+    args = (d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"])
+    for _ in range(3):
+        gdn.chunk_fwd(*args)
+    torch.cuda.synchronize()
+    torch.cuda.nvtx.range_push("profile_fwd")
+    for _ in range(2):
+        gdn.chunk_fwd(*args)
+    torch.cuda.synchronize()
+    torch.cuda.nvtx.range_pop()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -710,7 +732,13 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--tokens", type=int, default=32768,
                     help="sequence length (32768 = the benchmark; smaller only for profiler captures)")
+    ap.add_argument("--profile-fwd", type=float, default=None, metavar="G_MEAN",
+                    help="for profiler captures only: run the inference forward alone (3 calls, then 2 in the "
+                         "NVTX range 'profile_fwd') with gates u ~ N(G_MEAN, 1), print nothing else, exit")
     args = ap.parse_args()
+    if args.profile_fwd is not None:
+        profile_fwd(args.tokens, args.profile_fwd)
+        return
     args.warmup = max(args.warmup, 3)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
